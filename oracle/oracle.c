@@ -1,0 +1,707 @@
+/*
+ * CPU oracle for the tensor quantizers: plain, slow, obviously correct.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline / reference leg use it.  It shares no code, header, table or
+ * constant generator with the CUDA path.
+ *
+ * Build: gcc -O2 -std=c11 -fno-fast-math -ffp-contract=off -shared -fPIC
+ * (-ffp-contract=off matters: every FP32 product and quotient below must be
+ * one IEEE round-to-nearest-even operation, never fused into an FMA).
+ *
+ * Pages this follows (cited by tag below):
+ *   [MP]  "Mixed-precision training: fp16 to fp8"
+ *         (garden.houmin.site/infra/mixed-precision-fp8)
+ *   [CS]  "FP8 Current Scaling: quantization, scaling and precision bounds"
+ *         (notes.kuangjux.top/Foundations/08_Quantization/fp8-current-scaling)
+ *   [LP]  "From BF16 to FP8/FP4: low-precision and mixed-precision LLM
+ *         pretraining" (r00kie-liu.github.io/2026/07/23/
+ *         low-precision-mixed-precision-pretraining)
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   R-SAT    casts saturate: finite or infinite magnitudes above Fmax give
+ *            +-Fmax; NaN gives 0x7F (FP8) or +6 (E2M1).
+ *   R-ZERO   a zero tensor / block gets scale 1 (alpha = s = 1; NVFP4 block
+ *            scale code 0x38 = 1.0).
+ *   R-INF    alpha = Fmax / amax that overflows to +inf is replaced by
+ *            FLT_MAX (so that 0 * inf never appears).
+ *   R-MX     MXFP8 scale exponent = floor(log2 b) - emax(element format),
+ *            biased code clamped to [0, 254].
+ *   R-BW     blockwise FP32 tile scale is formed exactly like the per-tensor
+ *            scale, per tile.
+ *   R-NV     NVFP4: alpha_g = (6*448)/A, block scale sb = e4m3((b*alpha_g)/6),
+ *            enc = alpha_g / sb, q = e2m1(x*enc); decode q * (sb * s_g).
+ *   R-PACK   E2M1 packing: element 2j in bits 3-0, element 2j+1 in bits 7-4.
+ *   R-SR     stochastic rounding on the E2M1 grid with 16 random bits per
+ *            element drawn from Philox4x32-10 (see or_sr_e2m1 and
+ *            or_philox_bits16).
+ *   R-LAYOUT columnwise outputs of current scaling, blockwise and NVFP4 are
+ *            stored transposed [K, M]; MXFP8 columnwise stays [M, K].
+ *   R-AMAX   amax is the largest |x| bit pattern, which is the largest |x|
+ *            for finite inputs (non-finite inputs are outside the contract).
+ *
+ * Parity status: every function below is pinned by the tests in tests/
+ * (worked examples, brute-force nearest-value search, library casts,
+ * invariants, transposition identities).  The NVFP4 scale formula (R-NV) is
+ * a reading of the pages, pinned only by invariants and the decode identity.
+ */
+#include <math.h>
+#include <float.h>
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Input widening                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Input dtype codes (same numbering as the library's, restated here). */
+enum { OR_BF16 = 0, OR_F32 = 1 };
+/* FP8 element formats. */
+enum { OR_E4M3 = 0, OR_E5M2 = 1 };
+
+static float f32_from_bits(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t bits_from_f32(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+/* BF16 is the top half of an FP32 word, so widening is exact. */
+static float load_x(const void *x, int dtype, int64_t i)
+{
+    if (dtype == OR_BF16) {
+        uint16_t h = ((const uint16_t *)x)[i];
+        return f32_from_bits((uint32_t)h << 16);
+    }
+    return ((const float *)x)[i];
+}
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------ */
+/*
+ * A format with mbits stored mantissa bits, smallest normal exponent emin
+ * and largest finite value fmax.  E4M3: 1/4/3 bits, bias 7, max 448, no inf
+ * ([MP] "FP8 data formats"; [CS] "The two FP8 formats" table).  E5M2: 1/5/2
+ * bits, bias 15, max 57344, IEEE-like inf/NaN (same passages).  E2M1: values
+ * {0,0.5,1,1.5,2,3,4,6} and negatives ([MP] "NVFP4", value list of
+ * float4_e2m1fn_x2).  BF16: 8 exponent bits, 7 mantissa bits.
+ */
+typedef struct { int mbits; int emin; double fmax; } fmt_t;
+
+static const fmt_t FMT_E4M3 = { 3, -6, 448.0 };
+static const fmt_t FMT_E5M2 = { 2, -14, 57344.0 };
+static const fmt_t FMT_E2M1 = { 1, 0, 6.0 };
+
+/* floor(log2 a) for finite a > 0, exactly: frexp gives a = m * 2^e with
+ * m in [0.5, 1), so floor(log2 a) = e - 1.  Works for FP32 subnormals too,
+ * since they are normal doubles. */
+static int floor_log2(double a)
+{
+    int e;
+    (void)frexp(a, &e);
+    return e - 1;
+}
+
+/*
+ * Round a >= 0 (finite) to the nearest value of a format with mbits mantissa
+ * bits and smallest normal exponent emin, unbounded above, ties to the value
+ * whose last mantissa bit is even (RTNE: [MP] "NVFP4" rounding note; [CS]
+ * "Current Scaling", the cast is round-to-nearest, ties to even).
+ *
+ * In the binade [2^e, 2^(e+1)) (e clamped to emin for subnormals) the
+ * representable values are n * 2^(e - mbits) for integers n; a / 2^(e-mbits)
+ * is exact in double, nearbyint() rounds it to the nearest integer with ties
+ * to even (default rounding mode), and the parity of n is the parity of the
+ * stored mantissa's last bit.
+ */
+static double round_rtne(double a, int mbits, int emin)
+{
+    if (a == 0.0) return 0.0;
+    int e = floor_log2(a);
+    if (e < emin) e = emin;
+    double quantum = ldexp(1.0, e - mbits);
+    double n = nearbyint(a / quantum);
+    return n * quantum;
+}
+
+/* Bits of a representable magnitude v of format (ebits, mbits, bias). */
+static uint32_t mag_bits(double v, int mbits, int emin)
+{
+    if (v == 0.0) return 0;
+    int bias = 1 - emin;
+    if (v < ldexp(1.0, emin)) {                 /* subnormal: E = 0 */
+        double m = v / ldexp(1.0, emin - mbits);
+        return (uint32_t)m;
+    }
+    int e = floor_log2(v);
+    double m = (v / ldexp(1.0, e) - 1.0) * ldexp(1.0, mbits);
+    return ((uint32_t)(e + bias) << mbits) | (uint32_t)m;
+}
+
+/* Saturating RTNE cast of an FP32 value to an FP8 code (R-SAT). */
+static uint8_t enc_fp8(float f, const fmt_t *F)
+{
+    if (isnan(f)) return 0x7F;
+    uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    double v;
+    if (a >= F->fmax) v = F->fmax;              /* includes +-inf */
+    else {
+        v = round_rtne(a, F->mbits, F->emin);
+        if (v > F->fmax) v = F->fmax;
+    }
+    return (uint8_t)(sign | mag_bits(v, F->mbits, F->emin));
+}
+
+uint8_t or_enc_e4m3(float f) { return enc_fp8(f, &FMT_E4M3); }
+uint8_t or_enc_e5m2(float f) { return enc_fp8(f, &FMT_E5M2); }
+static uint8_t enc_fmt8(float f, int fmt) { return fmt == OR_E5M2 ? or_enc_e5m2(f) : or_enc_e4m3(f); }
+
+/* Saturating RTNE cast to a 4-bit E2M1 code (sign in bit 3). */
+uint8_t or_enc_e2m1(float f)
+{
+    if (isnan(f)) return 0x7;                   /* R-SAT: NaN -> +6 */
+    uint8_t sign = signbit(f) ? 0x8 : 0x0;
+    double a = fabs((double)f);
+    double v;
+    if (a >= 6.0) v = 6.0;
+    else {
+        v = round_rtne(a, FMT_E2M1.mbits, FMT_E2M1.emin);
+        if (v > 6.0) v = 6.0;
+    }
+    return (uint8_t)(sign | mag_bits(v, FMT_E2M1.mbits, FMT_E2M1.emin));
+}
+
+/* Decoders: sign, exponent field E, mantissa field m.  E = 0 is subnormal. */
+float or_dec_e4m3(uint8_t c)
+{
+    int s = c >> 7, E = (c >> 3) & 0xF, m = c & 7;
+    if (E == 15 && m == 7) return NAN;          /* the only NaN pattern */
+    double v = (E == 0) ? ldexp((double)m, -6 - 3) : ldexp(1.0 + m / 8.0, E - 7);
+    return (float)(s ? -v : v);
+}
+
+float or_dec_e5m2(uint8_t c)
+{
+    int s = c >> 7, E = (c >> 2) & 0x1F, m = c & 3;
+    double v;
+    if (E == 31) v = (m == 0) ? INFINITY : NAN;
+    else if (E == 0) v = ldexp((double)m, -14 - 2);
+    else v = ldexp(1.0 + m / 4.0, E - 15);
+    return (float)(s ? -v : v);
+}
+
+static float dec_fmt8(uint8_t c, int fmt) { return fmt == OR_E5M2 ? or_dec_e5m2(c) : or_dec_e4m3(c); }
+
+float or_dec_e2m1(uint8_t c)
+{
+    int s = (c >> 3) & 1, E = (c >> 1) & 3, m = c & 1;
+    double v = (E == 0) ? 0.5 * m : ldexp(1.0 + m / 2.0, E - 1);
+    return (float)(s ? -v : v);
+}
+
+/* E8M0: 8 exponent bits, bias 127, no sign, no mantissa; 0xFF is NaN
+ * ([MP] "MXFP8", float8_e8m0fnu stores the FP32 exponent field). */
+float or_dec_e8m0(uint8_t c)
+{
+    if (c == 0xFF) return NAN;
+    return (float)ldexp(1.0, (int)c - 127);
+}
+
+/* FP32 -> BF16 round to nearest even with IEEE overflow to inf. */
+uint16_t or_f32_to_bf16(float f)
+{
+    uint32_t u = bits_from_f32(f);
+    if (isnan(f)) return (uint16_t)((u >> 16) | 0x0040);     /* quiet NaN, keep sign/payload top */
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000);
+    double a = fabs((double)f);
+    if (isinf(f)) return (uint16_t)(sign | 0x7F80);
+    double v = round_rtne(a, 7, -126);
+    if (v >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+    float vf = (float)v;                         /* exact: BF16 values are FP32 values */
+    return (uint16_t)(sign | (bits_from_f32(vf) >> 16));
+}
+
+/* Batch helpers for the tests. */
+void or_cast_fp8(const float *in, int64_t n, int fmt, uint8_t *out)
+{ for (int64_t i = 0; i < n; i++) out[i] = enc_fmt8(in[i], fmt); }
+void or_cast_e2m1(const float *in, int64_t n, uint8_t *out)
+{ for (int64_t i = 0; i < n; i++) out[i] = or_enc_e2m1(in[i]); }
+void or_decode_fp8(const uint8_t *in, int64_t n, int fmt, float *out)
+{ for (int64_t i = 0; i < n; i++) out[i] = dec_fmt8(in[i], fmt); }
+void or_decode_e2m1(const uint8_t *in, int64_t n, float *out)
+{ for (int64_t i = 0; i < n; i++) out[i] = or_dec_e2m1(in[i]); }
+void or_bf16_round(const float *in, int64_t n, uint16_t *out)
+{ for (int64_t i = 0; i < n; i++) out[i] = or_f32_to_bf16(in[i]); }
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as   */
+/* easy as 1, 2, 3", SC'11).                                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * Written once for a general word width w (32 or 64) so that the 64-bit
+ * instance can be checked against numpy.random.Philox (Philox4x64-10) and the
+ * 32-bit instance, which stochastic rounding uses, runs the same code.
+ *
+ * One round on counter (c0,c1,c2,c3) with key (k0,k1):
+ *   (hi0,lo0) = M0 * c0, (hi1,lo1) = M1 * c2   (double-width products)
+ *   c' = (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0)
+ * and between rounds the key is bumped by the Weyl constants (W0, W1).
+ */
+static void mulhilo(uint64_t a, uint64_t b, int w, uint64_t *hi, uint64_t *lo)
+{
+    unsigned __int128 p = (unsigned __int128)a * (unsigned __int128)b;
+    if (w == 32) {
+        *lo = (uint64_t)(p & 0xFFFFFFFFu);
+        *hi = (uint64_t)((p >> 32) & 0xFFFFFFFFu);
+    } else {
+        *lo = (uint64_t)p;
+        *hi = (uint64_t)(p >> 64);
+    }
+}
+
+void or_philox4_generic(int w, int rounds, const uint64_t ctr_in[4], const uint64_t key_in[2],
+                        const uint64_t mult[2], const uint64_t weyl[2], uint64_t out[4])
+{
+    uint64_t mask = (w == 32) ? 0xFFFFFFFFull : ~0ull;
+    uint64_t c[4] = { ctr_in[0] & mask, ctr_in[1] & mask, ctr_in[2] & mask, ctr_in[3] & mask };
+    uint64_t k[2] = { key_in[0] & mask, key_in[1] & mask };
+    for (int r = 0; r < rounds; r++) {
+        if (r > 0) {
+            k[0] = (k[0] + weyl[0]) & mask;
+            k[1] = (k[1] + weyl[1]) & mask;
+        }
+        uint64_t hi0, lo0, hi1, lo1;
+        mulhilo(mult[0], c[0], w, &hi0, &lo0);
+        mulhilo(mult[1], c[2], w, &hi1, &lo1);
+        uint64_t n0 = (hi1 ^ c[1] ^ k[0]) & mask;
+        uint64_t n2 = (hi0 ^ c[3] ^ k[1]) & mask;
+        c[0] = n0; c[1] = lo1; c[2] = n2; c[3] = lo0;
+    }
+    for (int i = 0; i < 4; i++) out[i] = c[i];
+}
+
+/* The 32-bit constants of the paper: multipliers 0xD2511F53, 0xCD9E8D57 and
+ * key increments 0x9E3779B9 (golden ratio), 0xBB67AE85 (sqrt(3) - 1). */
+void or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    static const uint64_t M[2] = { 0xD2511F53u, 0xCD9E8D57u };
+    static const uint64_t W[2] = { 0x9E3779B9u, 0xBB67AE85u };
+    uint64_t c[4] = { ctr[0], ctr[1], ctr[2], ctr[3] }, k[2] = { key[0], key[1] }, o[4];
+    or_philox4_generic(32, 10, c, k, M, W, o);
+    for (int i = 0; i < 4; i++) out[i] = (uint32_t)o[i];
+}
+
+/*
+ * The 16 random bits stochastic rounding gives element i of an output whose
+ * draws come from stream `stream` (R-SR): Philox4x32-10 with key
+ * (seed lo32, seed hi32) and counter (g lo32, g hi32, stream, 0), where
+ * g = offset + floor(i / 8); the four 32-bit output words give elements
+ * 8g'..8g'+7 as word (i % 8) / 2, low half for even i, high half for odd i.
+ */
+uint32_t or_philox_bits16(uint64_t seed, uint64_t offset, uint32_t stream, uint64_t i)
+{
+    uint64_t g = offset + i / 8;
+    uint32_t ctr[4] = { (uint32_t)g, (uint32_t)(g >> 32), stream, 0 };
+    uint32_t key[2] = { (uint32_t)seed, (uint32_t)(seed >> 32) };
+    uint32_t w[4];
+    or_philox4x32_10(ctr, key, w);
+    uint32_t word = w[(i % 8) / 2];
+    return (i % 2 == 0) ? (word & 0xFFFFu) : (word >> 16);
+}
+
+/*
+ * Stochastic rounding of y onto the E2M1 grid ([MP] "NVFP4": stochastic
+ * rounding is an option; [LP] 2.4 item 5: SR on gradients).  With a = |y|:
+ * a >= 6 gives 6; otherwise lo is the largest grid value <= a, ulp the grid
+ * spacing there (0.5 below 2, 1 below 4, 2 below 6), frac = (a - lo) / ulp,
+ * and the result rounds up to lo + ulp iff R < frac * 2^16 for the
+ * element's 16 random bits R, so P(up) = ceil(frac * 2^16) / 2^16.
+ * NaN takes the RTNE rule.  The sign is y's.
+ */
+uint8_t or_sr_e2m1(float y, uint32_t r16)
+{
+    if (isnan(y)) return or_enc_e2m1(y);
+    uint8_t sign = signbit(y) ? 0x8 : 0x0;
+    double a = fabs((double)y);
+    double v;
+    if (a >= 6.0) v = 6.0;
+    else {
+        double ulp = (a < 2.0) ? 0.5 : (a < 4.0) ? 1.0 : 2.0;
+        double lo = floor(a / ulp) * ulp;
+        double frac = (a - lo) / ulp;
+        v = ((double)r16 < frac * 65536.0) ? lo + ulp : lo;
+    }
+    return (uint8_t)(sign | mag_bits(v, FMT_E2M1.mbits, FMT_E2M1.emin));
+}
+
+/* Batch stochastic rounding for the tests: element i of y takes the 16 bits
+ * or_philox_bits16(seed, offset, stream, i). */
+void or_sr_e2m1_batch(const float *y, int64_t n, uint64_t seed, uint64_t offset, uint32_t stream,
+                      uint8_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = or_sr_e2m1(y[i], or_philox_bits16(seed, offset, stream, (uint64_t)i));
+}
+
+/* ------------------------------------------------------------------------ */
+/* a1: tensor amax                                                           */
+/* ------------------------------------------------------------------------ */
+/* [CS] "Current Scaling": a = max_i |x_i|; [MP] recipe 3 step 1. (R-AMAX) */
+float or_amax(const void *x, int dtype, int64_t n)
+{
+    uint32_t best = 0;
+    for (int64_t i = 0; i < n; i++) {
+        uint32_t u = bits_from_f32(load_x(x, dtype, i)) & 0x7FFFFFFFu;
+        if (u > best) best = u;
+    }
+    return f32_from_bits(best);
+}
+
+/* ------------------------------------------------------------------------ */
+/* a2: per-tensor scale                                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * [CS] "Current Scaling": alpha = Fmax / a, s = 1 / alpha (FP32 scale factor
+ * per tensor).  R-ZERO for a = 0; R-INF for an overflowing alpha.
+ */
+static float fmax_of(int fmt) { return fmt == OR_E5M2 ? 57344.0f : 448.0f; }
+
+static void scale_from_amax(float fmax, float a, float *alpha, float *s)
+{
+    float al;
+    if (a == 0.0f) al = 1.0f;
+    else {
+        al = fmax / a;
+        if (isinf(al) && al > 0) al = FLT_MAX;
+    }
+    *alpha = al;
+    *s = 1.0f / al;
+}
+
+void or_cs_scale(float amax, int fmt, float *alpha, float *s)
+{
+    scale_from_amax(fmax_of(fmt), amax, alpha, s);
+}
+
+/* ------------------------------------------------------------------------ */
+/* a3: per-tensor current scaling cast                                       */
+/* ------------------------------------------------------------------------ */
+/*
+ * q_i = Q(alpha * x_i) with the product rounded to FP32 first ([CS]
+ * "Current Scaling"; [MP] recipe 3).  Rowwise codes q_row[m*K + k]; the
+ * columnwise copy is the same codes transposed, q_colT[k*M + m] (cast +
+ * cast_transpose, [MP] "Per-tensor Current Scaling", Hopper flow).
+ * Either output may be NULL.  amax_in: if non-NULL, *amax_in is used instead
+ * of computing the amax (the sharded case, [CS] "Cost and multi-GPU use").
+ */
+void or_current_scaling(const void *x, int dtype, int64_t M, int64_t K, int fmt,
+                        const float *amax_in, uint8_t *q_row, uint8_t *q_colT,
+                        float *amax_out, float *s_out)
+{
+    float a = amax_in ? *amax_in : or_amax(x, dtype, M * K);
+    float alpha, s;
+    or_cs_scale(a, fmt, &alpha, &s);
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t k = 0; k < K; k++) {
+            float y = alpha * load_x(x, dtype, m * K + k);
+            uint8_t c = enc_fmt8(y, fmt);
+            if (q_row) q_row[m * K + k] = c;
+            if (q_colT) q_colT[k * M + m] = c;
+        }
+    if (amax_out) *amax_out = a;
+    if (s_out) *s_out = s;
+}
+
+/* x_hat = q * s ([CS] "Current Scaling": x_hat_i = q_i * s). out_dtype BF16
+ * rounds the FP32 product to nearest even. */
+static void store_y(void *y, int out_dtype, int64_t i, float v)
+{
+    if (out_dtype == OR_BF16) ((uint16_t *)y)[i] = or_f32_to_bf16(v);
+    else ((float *)y)[i] = v;
+}
+
+void or_dq_current_scaling(const uint8_t *q, float s, int64_t R, int64_t C, int fmt,
+                           int out_dtype, void *y)
+{
+    for (int64_t i = 0; i < R * C; i++) store_y(y, out_dtype, i, dec_fmt8(q[i], fmt) * s);
+}
+
+/* Largest |x| bit pattern over the h x w tile at (m0, k0) (R-AMAX). */
+static float tile_amax(const void *x, int dtype, int64_t K, int64_t m0, int64_t k0, int64_t h, int64_t w)
+{
+    uint32_t best = 0;
+    for (int64_t m = m0; m < m0 + h; m++)
+        for (int64_t k = k0; k < k0 + w; k++) {
+            uint32_t u = bits_from_f32(load_x(x, dtype, m * K + k)) & 0x7FFFFFFFu;
+            if (u > best) best = u;
+        }
+    return f32_from_bits(best);
+}
+
+/* ------------------------------------------------------------------------ */
+/* a4/a5: MXFP8                                                              */
+/* ------------------------------------------------------------------------ */
+/*
+ * 32 consecutive elements share one E8M0 scale; value = element * scale
+ * ([MP] "MXFP8").  Rowwise blocks are 1x32 along K, columnwise blocks 32x1
+ * along M, both stored in the [M, K] layout of x ([MP] "MXFP8 recipe": the
+ * two directions differ only in the quantization direction).
+ * Scale code (R-MX): e = floor(log2 b) - emax, emax = 8 for E4M3
+ * (448 = 1.75 * 2^8) and 15 for E5M2 (57344 = 1.75 * 2^15); code =
+ * clamp(e + 127, 0, 254); b = 0 gives code 127.  Elements: q = Q(x * 2^(127 -
+ * code)), one exact FP32 multiply by a power of two.
+ */
+static uint8_t mx_scale_code(float b, int fmt)
+{
+    int emax = (fmt == OR_E5M2) ? 15 : 8;
+    if (b == 0.0f) return 127;
+    int e = isfinite(b) ? floor_log2((double)b) : 128;   /* non-finite: exponent field 255 */
+    int code = e - emax + 127;
+    if (code < 0) code = 0;
+    if (code > 254) code = 254;
+    return (uint8_t)code;
+}
+
+static float mx_inv_scale(uint8_t code) { return (float)ldexp(1.0, 127 - (int)code); }
+
+void or_mxfp8(const void *x, int dtype, int64_t M, int64_t K, int fmt,
+              uint8_t *q_row, uint8_t *e8m0_row, uint8_t *q_col, uint8_t *e8m0_col)
+{
+    if (q_row) {
+        for (int64_t m = 0; m < M; m++)
+            for (int64_t kb = 0; kb < K / 32; kb++) {
+                float b = tile_amax(x, dtype, K, m, kb * 32, 1, 32);
+                uint8_t code = mx_scale_code(b, fmt);
+                float inv = mx_inv_scale(code);
+                e8m0_row[m * (K / 32) + kb] = code;
+                for (int j = 0; j < 32; j++) {
+                    int64_t i = m * K + kb * 32 + j;
+                    q_row[i] = enc_fmt8(load_x(x, dtype, i) * inv, fmt);
+                }
+            }
+    }
+    if (q_col) {
+        for (int64_t mb = 0; mb < M / 32; mb++)
+            for (int64_t k = 0; k < K; k++) {
+                float b = tile_amax(x, dtype, K, mb * 32, k, 32, 1);
+                uint8_t code = mx_scale_code(b, fmt);
+                float inv = mx_inv_scale(code);
+                e8m0_col[mb * K + k] = code;
+                for (int j = 0; j < 32; j++) {
+                    int64_t i = (mb * 32 + j) * K + k;
+                    q_col[i] = enc_fmt8(load_x(x, dtype, i) * inv, fmt);
+                }
+            }
+    }
+}
+
+/* value = element * 2^(code - 127) ([MP] "MXFP8").  dir 0: scales along
+ * rows, e8m0[r*(C/32) + c/32]; dir 1: scales along columns,
+ * e8m0[(r/32)*C + c]. */
+void or_dq_mxfp8(const uint8_t *q, const uint8_t *e8m0, int64_t R, int64_t C, int fmt,
+                 int dir, int out_dtype, void *y)
+{
+    for (int64_t r = 0; r < R; r++)
+        for (int64_t c = 0; c < C; c++) {
+            uint8_t code = dir == 0 ? e8m0[r * (C / 32) + c / 32] : e8m0[(r / 32) * C + c];
+            float v = dec_fmt8(q[r * C + c], fmt) * or_dec_e8m0(code);
+            store_y(y, out_dtype, r * C + c, v);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* a6/a7: blockwise (DeepSeek-V3-like)                                       */
+/* ------------------------------------------------------------------------ */
+/*
+ * E4M3 only; activations and gradients on 1x128 tiles, weights on 128x128
+ * tiles; FP32 scale per tile ([MP] recipe 4 "Blockwise scaling", and the
+ * "Blockwise scaling" flow: X^T[k, m][1x128] is the columnwise operand).
+ * Per tile (R-BW): b = max|x|, alpha_b = 448 / b (b = 0 -> 1, overflow ->
+ * FLT_MAX), s_b = 1 / alpha_b, q = Q(alpha_b * x).
+ *
+ * tile 0 (1x128): q_row [M, K] with s_row [M, K/128]; q_colT [K, M] with
+ *   s_colT [K, M/128], blocks of 128 along M for each column k.
+ * tile 1 (128x128): q_row [M, K] with s_row [M/128, K/128]; q_colT [K, M] is
+ *   the same codes transposed with s_colT [K/128, M/128] (the 2D cast and
+ *   cast_transpose hold the same values, [MP] "Blockwise scaling").
+ */
+
+void or_blockwise(const void *x, int dtype, int64_t M, int64_t K, int tile,
+                  uint8_t *q_row, float *s_row, uint8_t *q_colT, float *s_colT)
+{
+    if (tile == 0) {
+        if (q_row)
+            for (int64_t m = 0; m < M; m++)
+                for (int64_t kb = 0; kb < K / 128; kb++) {
+                    float alpha, s;
+                    scale_from_amax(448.0f, tile_amax(x, dtype, K, m, kb * 128, 1, 128), &alpha, &s);
+                    s_row[m * (K / 128) + kb] = s;
+                    for (int j = 0; j < 128; j++) {
+                        int64_t i = m * K + kb * 128 + j;
+                        q_row[i] = or_enc_e4m3(alpha * load_x(x, dtype, i));
+                    }
+                }
+        if (q_colT)
+            for (int64_t k = 0; k < K; k++)
+                for (int64_t mb = 0; mb < M / 128; mb++) {
+                    float alpha, s;
+                    scale_from_amax(448.0f, tile_amax(x, dtype, K, mb * 128, k, 128, 1), &alpha, &s);
+                    s_colT[k * (M / 128) + mb] = s;
+                    for (int j = 0; j < 128; j++) {
+                        int64_t m = mb * 128 + j;
+                        q_colT[k * M + m] = or_enc_e4m3(alpha * load_x(x, dtype, m * K + k));
+                    }
+                }
+    } else {
+        for (int64_t mb = 0; mb < M / 128; mb++)
+            for (int64_t kb = 0; kb < K / 128; kb++) {
+                float alpha, s;
+                scale_from_amax(448.0f, tile_amax(x, dtype, K, mb * 128, kb * 128, 128, 128), &alpha, &s);
+                if (s_row) s_row[mb * (K / 128) + kb] = s;
+                if (s_colT) s_colT[kb * (M / 128) + mb] = s;
+                for (int64_t m = mb * 128; m < mb * 128 + 128; m++)
+                    for (int64_t k = kb * 128; k < kb * 128 + 128; k++) {
+                        uint8_t c = or_enc_e4m3(alpha * load_x(x, dtype, m * K + k));
+                        if (q_row) q_row[m * K + k] = c;
+                        if (q_colT) q_colT[k * M + m] = c;
+                    }
+            }
+    }
+}
+
+/* dq: x_hat = q * s_tile.  tile 0: s[r*(C/128) + c/128] (rowwise data, or
+ * the columnwise copy viewed as [K, M]); tile 1: s[(r/128)*(C/128) + c/128]. */
+void or_dq_blockwise(const uint8_t *q, const float *s, int64_t R, int64_t C, int tile,
+                     int out_dtype, void *y)
+{
+    for (int64_t r = 0; r < R; r++)
+        for (int64_t c = 0; c < C; c++) {
+            float sc = tile == 0 ? s[r * (C / 128) + c / 128] : s[(r / 128) * (C / 128) + c / 128];
+            store_y(y, out_dtype, r * C + c, or_dec_e4m3(q[r * C + c]) * sc);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* a8-a11: NVFP4                                                             */
+/* ------------------------------------------------------------------------ */
+/*
+ * E2M1 elements, 16 elements share one E4M3 block scale, plus one FP32
+ * tensor scale ([MP] "NVFP4" and recipe 6; [LP] 2.4 item 1).  1x16 blocks for
+ * activations and gradients, 16x16 blocks for weights ([LP] 2.4 item 4);
+ * stochastic rounding for gradients, RTNE otherwise ([LP] 2.4 item 5).
+ * Two-level scale (R-NV):
+ *   alpha_g = (6 * 448) / A   (A = 0 -> 1, overflow -> FLT_MAX), s_g = 1/alpha_g
+ *   per block: sb = e4m3((b * alpha_g) / 6)  (b = 0 -> sb = 1.0, code 0x38)
+ *              enc = alpha_g / sb           (sb == 0 with b > 0 -> enc = 0)
+ *              q = e2m1(x * enc)
+ * Packing (R-PACK): element 2j -> bits 3-0, element 2j+1 -> bits 7-4.
+ *
+ * blk 0 (1x16): q_row [M, K/2], sb_row [M, K/16]; q_colT [K, M/2] with
+ *   sb_colT [K, M/16] quantizes 16x1 blocks along M of each column.
+ * blk 1 (16x16): q_row [M, K/2], sb_row [M/16, K/16]; q_colT [K, M/2] is the
+ *   same codes transposed, sb_colT [K/16, M/16].
+ * rnd 0: RTNE; rnd 1: stochastic rounding (R-SR) with stream 0 for the
+ *   rowwise output (index m*K + k) and stream 1 for the 1x16 columnwise
+ *   output (index k*M + m); a 16x16 transposed copy reuses the row codes.
+ */
+typedef struct { float alpha_g; int rnd; uint64_t seed, offset; } nv_ctx;
+
+static void nv_block_scale(float b, float alpha_g, uint8_t *sb, float *enc)
+{
+    if (b == 0.0f) { *sb = 0x38; *enc = alpha_g / 1.0f; return; }
+    float sbf = (b * alpha_g) / 6.0f;
+    uint8_t code = or_enc_e4m3(sbf);
+    float sbv = or_dec_e4m3(code);
+    *sb = code;
+    *enc = (sbv == 0.0f) ? 0.0f : alpha_g / sbv;
+}
+
+static uint8_t nv_code(const nv_ctx *c, float xv, float enc, uint32_t stream, uint64_t idx)
+{
+    float y = xv * enc;
+    if (c->rnd == 0) return or_enc_e2m1(y);
+    return or_sr_e2m1(y, or_philox_bits16(c->seed, c->offset, stream, idx));
+}
+
+static void put_nibble(uint8_t *buf, int64_t i, uint8_t code)
+{
+    if (i % 2 == 0) buf[i / 2] = (uint8_t)((buf[i / 2] & 0xF0) | code);
+    else buf[i / 2] = (uint8_t)((buf[i / 2] & 0x0F) | (code << 4));
+}
+
+void or_nvfp4_global(float amax, float *alpha_g, float *s_g)
+{
+    scale_from_amax(6.0f * 448.0f, amax, alpha_g, s_g);
+}
+
+void or_nvfp4(const void *x, int dtype, int64_t M, int64_t K, int blk, int rnd,
+              uint64_t seed, uint64_t offset, const float *amax_in,
+              uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT,
+              float *amax_out, float *s_g_out)
+{
+    float A = amax_in ? *amax_in : or_amax(x, dtype, M * K);
+    nv_ctx c;
+    float s_g;
+    or_nvfp4_global(A, &c.alpha_g, &s_g);
+    c.rnd = rnd; c.seed = seed; c.offset = offset;
+
+    if (blk == 0) {
+        if (q_row)
+            for (int64_t m = 0; m < M; m++)
+                for (int64_t kb = 0; kb < K / 16; kb++) {
+                    uint8_t sb; float enc;
+                    nv_block_scale(tile_amax(x, dtype, K, m, kb * 16, 1, 16), c.alpha_g, &sb, &enc);
+                    sb_row[m * (K / 16) + kb] = sb;
+                    for (int j = 0; j < 16; j++) {
+                        int64_t i = m * K + kb * 16 + j;
+                        put_nibble(q_row, i, nv_code(&c, load_x(x, dtype, i), enc, 0, (uint64_t)i));
+                    }
+                }
+        if (q_colT)
+            for (int64_t k = 0; k < K; k++)
+                for (int64_t mb = 0; mb < M / 16; mb++) {
+                    uint8_t sb; float enc;
+                    nv_block_scale(tile_amax(x, dtype, K, mb * 16, k, 16, 1), c.alpha_g, &sb, &enc);
+                    sb_colT[k * (M / 16) + mb] = sb;
+                    for (int j = 0; j < 16; j++) {
+                        int64_t m = mb * 16 + j;
+                        int64_t it = k * M + m;
+                        put_nibble(q_colT, it, nv_code(&c, load_x(x, dtype, m * K + k), enc, 1, (uint64_t)it));
+                    }
+                }
+    } else {
+        for (int64_t mb = 0; mb < M / 16; mb++)
+            for (int64_t kb = 0; kb < K / 16; kb++) {
+                uint8_t sb; float enc;
+                nv_block_scale(tile_amax(x, dtype, K, mb * 16, kb * 16, 16, 16), c.alpha_g, &sb, &enc);
+                if (sb_row) sb_row[mb * (K / 16) + kb] = sb;
+                if (sb_colT) sb_colT[kb * (M / 16) + mb] = sb;
+                for (int64_t m = mb * 16; m < mb * 16 + 16; m++)
+                    for (int64_t k = kb * 16; k < kb * 16 + 16; k++) {
+                        int64_t i = m * K + k;
+                        uint8_t code = nv_code(&c, load_x(x, dtype, i), enc, 0, (uint64_t)i);
+                        if (q_row) put_nibble(q_row, i, code);
+                        if (q_colT) put_nibble(q_colT, k * M + m, code);
+                    }
+            }
+    }
+    if (amax_out) *amax_out = A;
+    if (s_g_out) *s_g_out = s_g;
+}
+
+/* x_hat = q * (sb * s_g), the block factor formed once per block.
+ * blk 0: sb[r*(C/16) + c/16]; blk 1: sb[(r/16)*(C/16) + c/16].
+ * q is [R, C/2] packed (R-PACK). */
+void or_dq_nvfp4(const uint8_t *q, const uint8_t *sb, float s_g, int64_t R, int64_t C, int blk,
+                 int out_dtype, void *y)
+{
+    for (int64_t r = 0; r < R; r++)
+        for (int64_t c = 0; c < C; c++) {
+            uint8_t code = blk == 0 ? sb[r * (C / 16) + c / 16] : sb[(r / 16) * (C / 16) + c / 16];
+            float f = or_dec_e4m3(code) * s_g;
+            int64_t i = r * C + c;
+            uint8_t byte = q[i / 2];
+            uint8_t nib = (i % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+            store_y(y, out_dtype, i, or_dec_e2m1(nib) * f);
+        }
+}

@@ -1,0 +1,412 @@
+"""Pins of the oracle's recipes against the pages' worked examples, closed
+forms, invariants and reductions to already-pinned pieces.
+
+Each test is chosen so that a plausible slip (a swapped Fmax, s = alpha
+instead of 1/alpha, a wrong emax, a transposed index, a wrong block
+boundary, a nibble order flip) fails it.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def f32(v):
+    return np.asarray(v, np.float32)
+
+
+def dec8(c, fmt=O.E4M3):
+    """Decode via torch (library), not via the oracle."""
+    dt = torch.float8_e4m3fn if fmt == O.E4M3 else torch.float8_e5m2
+    return torch.from_numpy(np.ascontiguousarray(c, np.uint8)).view(dt).float().numpy()
+
+
+E2M1_VALUES = np.array(gold("e2m1_values.json")["values"], np.float32)
+
+
+def dec4(nibbles):
+    return E2M1_VALUES[np.asarray(nibbles, np.int64)]
+
+
+# ---------------------------------------------------------------------------
+# per-tensor current scaling
+# ---------------------------------------------------------------------------
+
+def test_cs_worked_example():
+    g = gold("cs_worked_example.json")
+    x = f32([g["x"]])
+    r = O.current_scaling(x, O.E4M3, rowwise=True, colwise=True)
+    assert r.amax == g["amax"]
+    alpha, s = O.cs_scale(r.amax, O.E4M3)
+    assert alpha == np.float32(g["alpha"])                # 448 / 1000 in FP32
+    assert np.array_equal(dec8(r.q_row)[0], f32(g["q"]))
+    assert np.array_equal(r.q_colT[:, 0], r.q_row[0])
+    assert abs(float(r.scale) - g["s_approx"]) < g["s_tol"]
+    assert r.scale == np.float32(1) / np.float32(g["alpha"])
+    xhat = O.dq_current_scaling(r.q_row, r.scale)[0]
+    assert np.allclose(xhat, g["xhat_approx"], rtol=g["xhat_tol"], atol=0)
+    # scaled values before the cast
+    assert np.allclose(alpha * x[0], g["scaled"], rtol=1e-6)
+
+
+def test_cs_error_example():
+    g = gold("cs_error_example.json")
+    w = gold("cs_worked_example.json")
+    x = f32([w["x"]])
+    r = O.current_scaling(x)
+    alpha, _ = O.cs_scale(r.amax)
+    q = dec8(r.q_row)[0, 1]
+    assert abs((q - alpha * np.float32(g["x"])) - g["scaled_error"]) < g["tol"]
+    xhat = O.dq_current_scaling(r.q_row, r.scale)[0, 1]
+    assert abs((xhat - g["x"]) - g["restored_error_approx"]) < g["tol"]
+    rel_scaled = abs(q - alpha * g["x"]) / abs(alpha * g["x"])
+    rel_restored = abs(xhat - g["x"]) / g["x"]
+    assert abs(rel_scaled - g["relative_error_approx"]) < g["tol"]
+    assert abs(rel_restored - g["relative_error_approx"]) < g["tol"]
+
+
+def test_cs_underflow_and_cancellation_examples():
+    g = gold("cs_underflow_example.json")
+    r = O.current_scaling(f32([g["x"]]))
+    assert np.array_equal(dec8(r.q_row)[0], f32(g["q_expected"]))
+    c = gold("cs_cancellation_example.json")
+    # the two inputs sit in a tensor whose amax is 1000 (alpha = 0.448)
+    r = O.current_scaling(f32([c["x"]]))
+    xhat = O.dq_current_scaling(r.q_row, r.scale)[0]
+    assert c["x"][1] - c["x"][0] == c["true_difference"]
+    assert xhat[1] - xhat[0] == c["quantized_difference"]
+
+
+def test_cs_multi_rank_amax_example():
+    g = gold("multi_rank_amax.json")
+    shards = [f32([s]) for s in g["shards"]]
+    local = [O.amax(s) for s in shards]
+    assert local == g["local_amax"]
+    glob = max(local)
+    assert glob == g["global_amax"]
+    alpha, _ = O.cs_scale(glob)
+    assert alpha == np.float32(448) / np.float32(100) and abs(alpha - g["alpha"]) < 1e-6
+    # quantizing each shard with the global amax equals quantizing the whole tensor
+    whole = O.current_scaling(np.concatenate(shards, axis=1))
+    parts = [O.current_scaling(s, amax_in=glob) for s in shards]
+    assert np.array_equal(np.concatenate([p.q_row for p in parts], axis=1), whole.q_row)
+    assert all(p.scale == whole.scale for p in parts)
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+def test_cs_row_sharding_invariance(fmt):
+    """The quantized tensor must not depend on how rows are split across ranks
+    once the amax is MAX-reduced ("Mixed-precision training: fp16 to fp8",
+    section "FP8 communication", TP all-gather)."""
+    x = W.gen("grad" if fmt == O.E5M2 else "normal", (96, 64), 5, bf16=True)
+    whole = O.current_scaling(x, fmt, rowwise=True, colwise=True)
+    cuts = [0, 16, 48, 96]
+    shards = [x[a:b] for a, b in zip(cuts[:-1], cuts[1:])]
+    glob = max(O.amax(s) for s in shards)
+    parts = [O.current_scaling(s, fmt, rowwise=True, colwise=True, amax_in=glob) for s in shards]
+    assert np.array_equal(np.concatenate([p.q_row for p in parts], 0), whole.q_row)
+    assert np.array_equal(np.concatenate([p.q_colT for p in parts], 1), whole.q_colT)
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+def test_cs_power_of_two_invariance(fmt):
+    """Relative error is scale-invariant ("FP8 Current Scaling ...", section
+    "Does scaling amplify the error"): x * 2^k gives the same codes and
+    s * 2^k exactly."""
+    x = W.gen("outliers", (64, 48), 9, bf16=False)
+    base = O.current_scaling(x, fmt)
+    for k in (-20, -3, 1, 7, 30):
+        r = O.current_scaling((x * np.float32(2.0 ** k)).astype(np.float32), fmt)
+        assert np.array_equal(r.q_row, base.q_row)
+        assert r.scale == base.scale * np.float32(2.0 ** k)
+        assert r.amax == base.amax * np.float32(2.0 ** k)
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+def test_cs_codes_are_nearest_of_scaled_values(fmt):
+    """q_i is the saturated nearest code of the FP32 product alpha * x_i,
+    alpha = Fmax / amax; the nearest code is found by search over
+    torch-decoded codes."""
+    x = W.gen("outliers", (32, 40), 3, bf16=True)
+    r = O.current_scaling(x, fmt, colwise=True)
+    xf = W.bf16_bits_to_f32(x)
+    fmax = np.float32(448.0 if fmt == O.E4M3 else 57344.0)
+    alpha = fmax / np.float32(np.abs(xf).max())
+    y = (alpha * xf).astype(np.float32).ravel()
+    table = dec8(np.arange(256, dtype=np.uint8), fmt).astype(np.float64)
+    fin = np.isfinite(table)
+    got = dec8(r.q_row, fmt).astype(np.float64).ravel()
+    best = np.abs(table[fin][None, :] - y[:, None]).min(axis=1)
+    assert np.all(np.abs(got - y) == best)
+    assert np.array_equal(r.q_colT, r.q_row.T)
+    assert r.scale == np.float32(1) / alpha
+    assert np.abs(got).max() == fmax
+
+
+def test_cs_zero_tensor_scale_one():
+    r = O.current_scaling(np.zeros((4, 8), np.float32))
+    assert r.amax == 0 and r.scale == 1
+    assert not r.q_row.any()
+
+
+@pytest.mark.parametrize("out", [O.F32, O.BF16])
+def test_cs_dequant_closed_form(out):
+    x = W.gen("normal", (16, 32), 1, bf16=True)
+    r = O.current_scaling(x, O.E5M2)
+    y = O.dq_current_scaling(r.q_row, r.scale, O.E5M2, out)
+    want = (dec8(r.q_row, O.E5M2) * r.scale).astype(np.float32)
+    if out == O.BF16:
+        want = W.to_bf16_bits(want)
+    assert np.array_equal(y, want)
+
+
+# ---------------------------------------------------------------------------
+# MXFP8
+# ---------------------------------------------------------------------------
+
+def _mx_closed_form_codes(blocks, emax):
+    """Scale code per block from numpy's frexp: floor(log2 b) = exponent - 1."""
+    b = np.abs(blocks.astype(np.float64)).max(axis=-1)
+    _, e = np.frexp(b)
+    code = np.clip(e - 1 - emax + 127, 0, 254)
+    return np.where(b == 0, 127, code).astype(np.uint8)
+
+
+@pytest.mark.parametrize("fmt,emax", [(O.E4M3, 8), (O.E5M2, 15)])
+def test_mx_scale_closed_form_and_block_range(fmt, emax):
+    x = W.gen("lognormal_rows", (64, 128), 1, bf16=True)
+    xf = W.bf16_bits_to_f32(x)
+    r = O.mxfp8(x, fmt)
+    assert np.array_equal(r.e8m0_row, _mx_closed_form_codes(xf.reshape(64, 4, 32), emax))
+    assert np.array_equal(r.e8m0_col, _mx_closed_form_codes(xf.reshape(2, 32, 128).transpose(0, 2, 1), emax))
+    # the block maximum lands in [2^emax, 2^(emax+1)) before saturation, so its code
+    # magnitude lies in [256, 448] for E4M3 and [32768, 57344] for E5M2
+    q = np.abs(dec8(r.q_row, fmt).reshape(64, 4, 32)).max(axis=-1)
+    assert np.all(q >= 2.0 ** emax) and np.all(q <= (448.0 if fmt == O.E4M3 else 57344.0))
+
+
+def test_mx_power_of_two_invariance_and_symmetry():
+    x = W.gen("normal", (64, 96), 2, bf16=False)
+    r = O.mxfp8(x)
+    for k in (-9, 5):
+        r2 = O.mxfp8((x * np.float32(2.0 ** k)).astype(np.float32))
+        assert np.array_equal(r2.q_row, r.q_row) and np.array_equal(r2.q_col, r.q_col)
+        assert np.array_equal(r2.e8m0_row.astype(int), r.e8m0_row.astype(int) + k)
+        assert np.array_equal(r2.e8m0_col.astype(int), r.e8m0_col.astype(int) + k)
+    # columnwise 32x1 of x equals rowwise 1x32 of x^T, transposed back
+    rt = O.mxfp8(np.ascontiguousarray(x.T))
+    assert np.array_equal(r.q_col, rt.q_row.T) and np.array_equal(r.e8m0_col, rt.e8m0_row.T)
+
+
+@pytest.mark.parametrize("direction", [O.ROW, O.COL])
+def test_mx_dequant_value_is_element_times_scale(direction):
+    """value = element * block scale ("Mixed-precision training: fp16 to
+    fp8", section "MXFP8"); relative error of a normal-range element <= 2^-4,
+    or < 1/8 where the scaled value in [448, 512) saturated to 448."""
+    x = W.gen("lognormal_rows", (64, 64), 4, bf16=True)
+    r = O.mxfp8(x)
+    q, e = (r.q_row, r.e8m0_row) if direction == O.ROW else (r.q_col, r.e8m0_col)
+    y = O.dq_mxfp8(q, e, O.E4M3, direction)
+    sc = torch.from_numpy(e).view(torch.float8_e8m0fnu).float().numpy()
+    sc = np.repeat(sc, 32, axis=1) if direction == O.ROW else np.repeat(sc, 32, axis=0)
+    assert np.array_equal(y, (dec8(q) * sc).astype(np.float32))
+    xf = W.bf16_bits_to_f32(x)
+    normal = np.abs(dec8(q)) >= 2.0 ** -6
+    rel = np.where(np.abs(dec8(q)) == 448, 0.125, 2.0 ** -4)
+    assert np.all((np.abs(y - xf) <= np.abs(xf) * rel)[normal])
+    assert np.any(np.abs(dec8(q)) == 448)
+
+
+def test_mx_zero_block():
+    x = W.gen("normal", (32, 64), 7, bf16=False)
+    x[:, :32] = 0
+    r = O.mxfp8(x)
+    assert np.all(r.e8m0_row[:, 0] == 127) and not r.q_row[:, :32].any()
+    assert np.all(r.e8m0_col[0, :32] == 127)
+
+
+def test_mx_row_to_col_requant_near_identity():
+    """Power-of-two scales make dequantize -> requantize in the other direction
+    nearly lossless ("Mixed-precision training: fp16 to fp8", section "FP8
+    communication", EP): requantizing the rowwise dequantized tensor
+    columnwise matches direct columnwise quantization almost everywhere."""
+    x = W.gen("lognormal_rows", (128, 128), 8, bf16=True)
+    r = O.mxfp8(x)
+    y = O.dq_mxfp8(r.q_row, r.e8m0_row, O.E4M3, O.ROW)
+    r2 = O.mxfp8(y)
+    assert np.mean(r2.q_col == r.q_col) > 0.95
+    assert np.mean(r2.e8m0_col == r.e8m0_col) > 0.95
+
+
+# ---------------------------------------------------------------------------
+# blockwise
+# ---------------------------------------------------------------------------
+
+def test_bw_1x128_reduces_to_current_scaling_per_tile():
+    x = W.gen("normal", (8, 384), 2, bf16=True)
+    r = O.blockwise(x, O.T1x128, rowwise=True, colwise=False)
+    for m in range(8):
+        for kb in range(3):
+            t = O.current_scaling(np.ascontiguousarray(x[m:m + 1, kb * 128:(kb + 1) * 128]))
+            assert np.array_equal(r.q_row[m, kb * 128:(kb + 1) * 128], t.q_row[0])
+            assert r.s_row[m, kb] == t.scale
+
+
+def test_bw_1x128_colwise_is_rowwise_of_transpose():
+    x = W.gen("normal", (256, 256), 3, bf16=True)
+    r = O.blockwise(x, O.T1x128, rowwise=True, colwise=True)
+    rt = O.blockwise(np.ascontiguousarray(x.T), O.T1x128, rowwise=True)
+    assert np.array_equal(r.q_colT, rt.q_row) and np.array_equal(r.s_colT, rt.s_row)
+    assert r.s_colT.shape == (256, 2)
+
+
+def test_bw_128x128_tile_and_transpose():
+    x = W.gen("weight", (256, 384), 4, bf16=True)
+    r = O.blockwise(x, O.T128x128, rowwise=True, colwise=True)
+    assert np.array_equal(r.q_colT, r.q_row.T) and np.array_equal(r.s_colT, r.s_row.T)
+    for mb in range(2):
+        for kb in range(3):
+            t = O.current_scaling(np.ascontiguousarray(x[mb * 128:(mb + 1) * 128, kb * 128:(kb + 1) * 128]))
+            assert np.array_equal(r.q_row[mb * 128:(mb + 1) * 128, kb * 128:(kb + 1) * 128], t.q_row)
+            assert r.s_row[mb, kb] == t.scale
+
+
+@pytest.mark.parametrize("tile", [O.T1x128, O.T128x128])
+def test_bw_dequant(tile):
+    x = W.gen("normal", (128, 256), 5, bf16=True)
+    r = O.blockwise(x, tile, rowwise=True, colwise=True)
+    y = O.dq_blockwise(r.q_row, r.s_row, tile)
+    s = np.repeat(r.s_row, 128, axis=1) if tile == O.T1x128 else np.repeat(np.repeat(r.s_row, 128, 0), 128, 1)
+    assert np.array_equal(y, (dec8(r.q_row) * s).astype(np.float32))
+    yt = O.dq_blockwise(r.q_colT, r.s_colT, tile)
+    if tile == O.T128x128:
+        assert np.array_equal(yt, y.T)
+
+
+# ---------------------------------------------------------------------------
+# NVFP4
+# ---------------------------------------------------------------------------
+
+def test_nv_global_scale_and_max_block():
+    x = W.gen("normal", (32, 64), 6, bf16=False)
+    r = O.nvfp4(x, O.B1x16, rowwise=True, colwise=True)
+    A = np.float32(np.abs(x).max())
+    assert r.amax == A
+    assert r.s_global == np.float32(1) / (np.float32(2688) / A)
+    # the block holding the tensor's amax gets the largest E4M3 scale and a +-6 code
+    m, k = np.unravel_index(np.abs(x).argmax(), x.shape)
+    assert r.sb_row[m, k // 16] == 0x7E and r.sb_colT[k, m // 16] == 0x7E
+    assert O.unpack_e2m1(r.q_row, 64)[m, k] & 7 == 7
+    assert O.unpack_e2m1(r.q_colT, 32)[k, m] & 7 == 7
+
+
+def test_nv_power_of_two_invariance():
+    x = W.gen("t3", (32, 64), 6, bf16=False)
+    base = O.nvfp4(x, O.B1x16, rowwise=True, colwise=True)
+    for k in (-10, 4):
+        r = O.nvfp4((x * np.float32(2.0 ** k)).astype(np.float32), O.B1x16, rowwise=True, colwise=True)
+        assert np.array_equal(r.q_row, base.q_row) and np.array_equal(r.q_colT, base.q_colT)
+        assert np.array_equal(r.sb_row, base.sb_row) and np.array_equal(r.sb_colT, base.sb_colT)
+        assert r.s_global == base.s_global * np.float32(2.0 ** k)
+
+
+def test_nv_1x16_colwise_is_rowwise_of_transpose_and_nibble_order():
+    x = W.gen("normal", (48, 32), 2, bf16=True)
+    r = O.nvfp4(x, O.B1x16, rowwise=True, colwise=True)
+    rt = O.nvfp4(np.ascontiguousarray(x.T), O.B1x16, rowwise=True)
+    assert np.array_equal(r.q_colT, rt.q_row) and np.array_equal(r.sb_colT, rt.sb_row)
+    # even element in the low nibble: a tensor whose even columns are +max and odd columns 0
+    z = np.zeros((1, 16), np.float32)
+    z[0, 0::2] = 1.0
+    q = O.nvfp4(z, O.B1x16).q_row
+    assert np.all(q == 0x07)
+
+
+def test_nv_16x16_transpose_identity():
+    x = W.gen("weight", (64, 96), 3, bf16=True)
+    r = O.nvfp4(x, O.B16x16, rowwise=True, colwise=True)
+    codes = O.unpack_e2m1(r.q_row, 96)
+    codes_t = O.unpack_e2m1(r.q_colT, 64)
+    assert np.array_equal(codes_t, codes.T)
+    assert np.array_equal(r.sb_colT, r.sb_row.T)
+    # one scale per 16x16 tile: its value is the E4M3 cast of (tile max * alpha_g) / 6
+    xf = W.bf16_bits_to_f32(x)
+    alpha_g = np.float32(2688) / np.float32(np.abs(xf).max())
+    tb = np.abs(xf).reshape(4, 16, 6, 16).max(axis=(1, 3)).astype(np.float32)
+    sbf = ((tb * alpha_g).astype(np.float32) / np.float32(6)).astype(np.float32)
+    want = torch.from_numpy(sbf).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(r.sb_row, want)
+
+
+@pytest.mark.parametrize("blk", [O.B1x16, O.B16x16])
+def test_nv_dequant_identity_and_error_bound(blk):
+    x = W.gen("normal", (64, 64), 11, bf16=True)
+    r = O.nvfp4(x, blk, rowwise=True)
+    y = O.dq_nvfp4(r.q_row, r.sb_row, r.s_global, blk)
+    sb = dec8(r.sb_row)
+    f = (sb * r.s_global).astype(np.float32)
+    f = np.repeat(f, 16, axis=1) if blk == O.B1x16 else np.repeat(np.repeat(f, 16, 0), 16, 1)
+    codes = O.unpack_e2m1(r.q_row, 64)
+    assert np.array_equal(y, (dec4(codes) * f).astype(np.float32))
+    # error bound: half an E2M1 spacing at the scaled value, plus any saturation overshoot
+    xf = W.bf16_bits_to_f32(x)
+    yscaled = np.abs(xf) / f
+    spacing = np.where(yscaled < 2, 0.5, np.where(yscaled < 4, 1.0, 2.0))
+    bound = (spacing / 2 + np.maximum(yscaled - 6, 0)) * f * (1 + 1e-5)
+    assert np.all(np.abs(y - xf) <= bound)
+
+
+def test_nv_zero_block_scale_one():
+    x = W.gen("normal", (16, 32), 1, bf16=False)
+    x[:, 16:] = 0
+    r = O.nvfp4(x, O.B1x16, rowwise=True)
+    assert np.all(r.sb_row[:, 1] == 0x38)
+    assert not O.unpack_e2m1(r.q_row, 32)[:, 16:].any()
+    r = O.nvfp4(np.zeros((16, 16), np.float32), O.B16x16, rowwise=True)
+    assert r.s_global == 1 and np.all(r.sb_row == 0x38)
+
+
+def test_nv_sr_rounds_to_neighbours_and_matches_rn_on_grid():
+    x = W.gen("t3", (32, 64), 12, bf16=True)
+    rn = O.nvfp4(x, O.B1x16, O.RN, rowwise=True, colwise=True)
+    sr = O.nvfp4(x, O.B1x16, O.SR, seed=4, offset=0, rowwise=True, colwise=True)
+    assert np.array_equal(sr.sb_row, rn.sb_row) and np.array_equal(sr.sb_colT, rn.sb_colT)
+    d_rn = dec4(O.unpack_e2m1(rn.q_row, 64))
+    d_sr = dec4(O.unpack_e2m1(sr.q_row, 64))
+    # SR lands on the other neighbour only; the RN code is always one of the two
+    assert np.all(np.abs(d_sr - d_rn) <= 2)
+    assert 0 < np.mean(d_sr != d_rn) < 0.6
+    sr2 = O.nvfp4(x, O.B1x16, O.SR, seed=4, offset=0, rowwise=True, colwise=True)
+    assert np.array_equal(sr.q_row, sr2.q_row) and np.array_equal(sr.q_colT, sr2.q_colT)
+    sr3 = O.nvfp4(x, O.B1x16, O.SR, seed=5, offset=0, rowwise=True)
+    assert not np.array_equal(sr.q_row, sr3.q_row)
+
+
+def test_nv_sr_uses_row_and_column_indices():
+    """Rowwise element (m, k) draws index m*K + k on stream 0, columnwise
+    (k, m) draws k*M + m on stream 1."""
+    x = W.gen("t3", (16, 32), 13, bf16=False)
+    r = O.nvfp4(x, O.B1x16, O.SR, seed=99, offset=5, rowwise=True, colwise=True)
+    alpha_g, _ = O.nvfp4_global(r.amax)
+    sbv = dec8(r.sb_row)
+    enc = (alpha_g / sbv).astype(np.float32)
+    y = (x * np.repeat(enc, 16, axis=1)).astype(np.float32)
+    want = O.sr_e2m1_batch(y.ravel(), seed=99, offset=5, stream=0).reshape(16, 32)
+    assert np.array_equal(O.unpack_e2m1(r.q_row, 32), want)
+    sbc = dec8(r.sb_colT)
+    encc = (alpha_g / sbc).astype(np.float32)
+    yt = (np.ascontiguousarray(x.T) * np.repeat(encc, 16, axis=1)).astype(np.float32)
+    wantc = O.sr_e2m1_batch(yt.ravel(), seed=99, offset=5, stream=1).reshape(32, 16)
+    assert np.array_equal(O.unpack_e2m1(r.q_colT, 16), wantc)
