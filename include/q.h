@@ -1,0 +1,208 @@
+/*
+ * q.h -- C ABI of the GB300 (sm_103a) tensor quantizers.
+ *
+ * The operations turn a BF16 or FP32 tensor into low-precision codes plus
+ * scales, and back, for FP8 / FP4 mixed-precision training.  Sources (cited
+ * by tag in each entry):
+ *   [MP] "Mixed-precision training: fp16 to fp8"
+ *        (garden.houmin.site/infra/mixed-precision-fp8)
+ *   [CS] "FP8 Current Scaling: quantization, scaling and precision bounds"
+ *        (notes.kuangjux.top/Foundations/08_Quantization/fp8-current-scaling)
+ *   [LP] "From BF16 to FP8/FP4: low-precision and mixed-precision LLM
+ *        pretraining" (r00kie-liu.github.io/2026/07/23/
+ *        low-precision-mixed-precision-pretraining)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Tensors are row-major and contiguous.  x is [M, K]: M rows (tokens or
+ * output features), K contiguous columns.  "Rowwise" quantizes blocks that
+ * run along K; "columnwise" quantizes blocks that run along M.  Columnwise
+ * outputs of current scaling, blockwise and NVFP4 are stored transposed,
+ * [K, M] (the operand of the wgrad GEMM X^T, [MP] "Per-tensor Current
+ * Scaling" and "Blockwise scaling" flows); the MXFP8 columnwise output stays
+ * in the [M, K] layout ([MP] "MXFP8 recipe").
+ *
+ * Ownership: every pointer is caller-owned DEVICE memory (except where a
+ * parameter says otherwise); the library never allocates, never frees and
+ * keeps no per-call state.  Each call enqueues its kernels on `stream`
+ * (NULL = the legacy default stream) and returns without synchronizing.
+ *
+ * Alignment: x, y and every code buffer must be 16-byte aligned; FP32 scale
+ * buffers 4-byte aligned.
+ *
+ * Errors: argument problems are detected on the host, before any launch,
+ * and returned as a q_status (nothing is enqueued).  A failed launch returns
+ * Q_ERR_CUDA.  q_last_error() gives a message for the calling thread's last
+ * failure.  Conditions found on the device (non-finite input) are ORed into
+ * the optional device word *status (may be NULL); the caller zeroes it.
+ *
+ * Empty tensors (M == 0 or K == 0) are valid: amax is 0, scales are 1 and no
+ * code is written.
+ */
+#ifndef Q_H_
+#define Q_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same object as cudaStream_t). */
+typedef struct CUstream_st *q_stream_t;
+
+typedef enum {
+    Q_OK = 0,
+    Q_ERR_ARG = 1,     /* NULL where a buffer is required, bad enum, nothing requested */
+    Q_ERR_SHAPE = 2,   /* negative size, M*K >= 2^62, or a dimension not a multiple of the block */
+    Q_ERR_ALIGN = 3,   /* a pointer violates the alignment rule above */
+    Q_ERR_DTYPE = 4,   /* unsupported input / output dtype */
+    Q_ERR_CUDA = 5     /* a CUDA launch failed; see q_last_error() */
+} q_status;
+
+typedef enum { Q_BF16 = 0, Q_F32 = 1 } q_dtype;
+typedef enum { Q_E4M3 = 0, Q_E5M2 = 1 } q_fp8;
+typedef enum { Q_T1x128 = 0, Q_T128x128 = 1 } q_tile;
+typedef enum { Q_B1x16 = 0, Q_B16x16 = 1 } q_nvblk;
+typedef enum { Q_RN = 0, Q_SR = 1 } q_round;
+typedef enum { Q_ROW = 0, Q_COL = 1 } q_dir;
+/* Whether the per-tensor amax is computed by the call (Q_AMAX_COMPUTE, the
+ * value is written to *amax) or given by the caller in *amax on the device
+ * (Q_AMAX_GIVEN), e.g. after a MAX all-reduce over the shards of a tensor
+ * ([CS] "Cost and multi-GPU use": compute amax, synchronize amax, then
+ * scale + cast). */
+typedef enum { Q_AMAX_COMPUTE = 0, Q_AMAX_GIVEN = 1 } q_amax_mode;
+
+/* Bits ORed into *status by the kernels. */
+#define Q_ST_NONFINITE 1   /* an amax (tensor or block) was inf or NaN */
+
+/* Thread-local message describing this thread's last failed call ("" if none). */
+const char *q_last_error(void);
+
+/* Version of this ABI (incremented on incompatible change). */
+int q_abi_version(void);
+
+/*
+ * a1: tensor amax.  *amax = max_i |x_i| over the n elements of x
+ * ([CS] "Current Scaling": a = max_i |x_i|; [MP] recipe 3 step 1).
+ * x: n elements of dtype `in`.  amax: one float.  Any n >= 0.
+ */
+q_status q_amax(const void *x, q_dtype in, int64_t n, float *amax, int32_t *status,
+                q_stream_t stream);
+
+/*
+ * a1-a3: per-tensor current scaling ([CS] "Current Scaling"; [MP] recipe 3,
+ * "Per-tensor Current Scaling" flow).
+ *   amax  = max|x| (or given), alpha = Fmax / amax (Fmax 448 for E4M3,
+ *   57344 for E5M2), s = 1 / alpha, q = saturate(RTNE(alpha * x)).
+ *   amax = 0 gives alpha = s = 1; an alpha that overflows is FLT_MAX.
+ * Reads x twice when the amax is computed (once for the amax, once for the
+ * cast); the cast pass walks the tensor backwards so that the part still in
+ * L2 from the first pass is read first.
+ *   q_row  [M, K] codes or NULL;  q_colT [K, M] codes (the same codes,
+ *   transposed) or NULL; at least one is required.
+ *   amax   one float: written (Q_AMAX_COMPUTE) or read (Q_AMAX_GIVEN).
+ *   scale  one float: s.
+ * Shapes: any M, K >= 0 for q_row alone; q_colT needs M % 16 == 0 and
+ * K % 16 == 0.
+ */
+q_status q_current_scaling(const void *x, q_dtype in, int64_t M, int64_t K, q_fp8 fmt,
+                           uint8_t *q_row, uint8_t *q_colT,
+                           float *amax, q_amax_mode amax_mode, float *scale,
+                           int32_t *status, q_stream_t stream);
+
+/*
+ * a4/a5: MXFP8 ([MP] "MXFP8" and recipe 5): 32 elements share one E8M0
+ * scale (an FP32 exponent field, 2^(code-127)).  Per block with
+ * b = max|x|: code = clamp(floor(log2 b) - emax + 127, 0, 254), emax = 8 for
+ * E4M3 and 15 for E5M2 (b = 0 gives 127); q = saturate(RTNE(x * 2^(127-code))).
+ *   q_row    [M, K] codes, 1x32 blocks along K;  e8m0_row [M, K/32]
+ *   q_col    [M, K] codes, 32x1 blocks along M;  e8m0_col [M/32, K]
+ * Either direction may be NULL (both buffers of it), not both.
+ * Shapes: K % 32 == 0; with q_col also M % 32 == 0.
+ */
+q_status q_mxfp8(const void *x, q_dtype in, int64_t M, int64_t K, q_fp8 fmt,
+                 uint8_t *q_row, uint8_t *e8m0_row, uint8_t *q_col, uint8_t *e8m0_col,
+                 int32_t *status, q_stream_t stream);
+
+/*
+ * a6/a7: DeepSeek-V3-like blockwise FP8 ([MP] recipe 4 and "Blockwise
+ * scaling"): E4M3 only, FP32 scale per tile, formed like the per-tensor
+ * scale on the tile: alpha_b = 448 / b, s_b = 1 / alpha_b.
+ *   tile Q_T1x128 (activations, gradients):
+ *     q_row [M, K], s_row [M, K/128];  q_colT [K, M], s_colT [K, M/128]
+ *     (128x1 blocks along M of each column).  K % 128 == 0; with q_colT
+ *     also M % 128 == 0.
+ *   tile Q_T128x128 (weights):
+ *     q_row [M, K], s_row [M/128, K/128]; q_colT [K, M] = the same codes
+ *     transposed, s_colT [K/128, M/128].  M % 128 == 0 and K % 128 == 0.
+ * Either direction may be NULL, not both.
+ */
+q_status q_blockwise(const void *x, q_dtype in, int64_t M, int64_t K, q_tile tile,
+                     uint8_t *q_row, float *s_row, uint8_t *q_colT, float *s_colT,
+                     int32_t *status, q_stream_t stream);
+
+/*
+ * a8-a11: NVFP4 ([MP] "NVFP4" and recipe 6; [LP] 2.4 items 1, 4, 5):
+ * E2M1 codes packed two per byte (element 2j in bits 3-0, 2j+1 in bits 7-4),
+ * one E4M3 scale per block, one FP32 tensor scale.
+ *   alpha_g = 2688 / amax (= 6 * 448 / amax; amax = 0 -> 1), s_global = 1/alpha_g
+ *   per block: sb = E4M3(RTNE((b * alpha_g) / 6)), b = 0 -> sb = 1.0;
+ *              enc = alpha_g / sb (0 if sb == 0); q = E2M1(x * enc)
+ *   rnd Q_RN: round to nearest even.  rnd Q_SR: stochastic rounding; the
+ *   16 random bits of element i of an output come from Philox4x32-10 with
+ *   key (seed lo, seed hi) and counter (g lo, g hi, stream, 0),
+ *   g = offset + i / 8, word (i % 8) / 2, low half for even i; stream 0 for
+ *   q_row (i = m*K + k), 1 for a 1x16 q_colT (i = k*M + m); it rounds up iff
+ *   the 16 bits, as an integer, are below frac * 65536 where frac is the
+ *   position of |x * enc| between its two neighbouring E2M1 values.
+ *   blk Q_B1x16 (activations, gradients):
+ *     q_row [M, K/2], sb_row [M, K/16];  q_colT [K, M/2], sb_colT [K, M/16]
+ *     (16x1 blocks along M of each column).
+ *   blk Q_B16x16 (weights): one scale per 16x16 tile,
+ *     q_row [M, K/2], sb_row [M/16, K/16]; q_colT [K, M/2] = the same codes
+ *     transposed, sb_colT [K/16, M/16].
+ *   amax      one float, written (Q_AMAX_COMPUTE) or read (Q_AMAX_GIVEN)
+ *   s_global  one float, written.
+ * Shapes: K % 16 == 0 and M % 16 == 0.  Either direction may be NULL, not
+ * both.
+ */
+q_status q_nvfp4(const void *x, q_dtype in, int64_t M, int64_t K, q_nvblk blk, q_round rnd,
+                 uint64_t seed, uint64_t offset,
+                 uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT,
+                 float *amax, q_amax_mode amax_mode, float *s_global,
+                 int32_t *status, q_stream_t stream);
+
+/*
+ * a12: dequantizers.  Output y [R, C] in `out` (Q_F32, or Q_BF16 rounded to
+ * nearest even from the FP32 value).  A transposed columnwise output is
+ * passed as the [K, M] matrix it is (R = K, C = M).
+ */
+
+/* x_hat = q * s ([CS] "Current Scaling": x_hat_i = q_i * s).  q [R, C]
+ * FP8 codes; scale: one device float.  Any R, C >= 0. */
+q_status dq_current_scaling(const uint8_t *q, const float *scale, int64_t R, int64_t C,
+                            q_fp8 fmt, q_dtype out, void *y, q_stream_t stream);
+
+/* x_hat = q * 2^(code-127) ([MP] "MXFP8": value = element x block scale).
+ * dir Q_ROW: e8m0 [R, C/32]; dir Q_COL: e8m0 [R/32, C].  C % 32 == 0
+ * (Q_ROW) or R % 32 == 0 and C % 16 == 0 (Q_COL). */
+q_status dq_mxfp8(const uint8_t *q, const uint8_t *e8m0, int64_t R, int64_t C, q_fp8 fmt,
+                  q_dir dir, q_dtype out, void *y, q_stream_t stream);
+
+/* x_hat = q * s_tile.  Q_T1x128: s [R, C/128]; Q_T128x128: s [R/128, C/128].
+ * C % 128 == 0 (and R % 128 == 0 for Q_T128x128). */
+q_status dq_blockwise(const uint8_t *q, const float *s, int64_t R, int64_t C, q_tile tile,
+                      q_dtype out, void *y, q_stream_t stream);
+
+/* x_hat = q * (sb * s_global), the block factor formed once per block.
+ * q [R, C/2] packed; Q_B1x16: sb [R, C/16]; Q_B16x16: sb [R/16, C/16].
+ * s_global: one device float.  C % 16 == 0 (and R % 16 == 0 for 16x16). */
+q_status dq_nvfp4(const uint8_t *q, const uint8_t *sb, const float *s_global, int64_t R,
+                  int64_t C, q_nvblk blk, q_dtype out, void *y, q_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q_H_ */

@@ -1,0 +1,319 @@
+// Device helpers shared by the quantizer kernels (sm_103a).
+//
+// Every kernel that tiles the input uses the same geometry: a CTA of 8 warps
+// owns a tile of 128 rows x (32 * VEC) columns, each warp 16 rows, each lane
+// a 16-row x VEC-column micro-tile held in registers as 16 x 16-byte vectors
+// (VEC = 8 BF16 or 4 FP32 elements).  A warp's load of one row is 512
+// contiguous bytes; a thread keeps 16 independent 16-byte loads in flight.
+//
+// FP32 arithmetic that decides a code is written with explicit round-to-
+// nearest intrinsics (__fmul_rn, __fdiv_rn) so that no product is fused into
+// an FMA and no division is approximated; the library is also compiled with
+// -fmad=false.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <float.h>
+
+#define QD __device__ __forceinline__
+
+namespace qk {
+
+enum { BF16 = 0, F32 = 1 };
+enum { E4M3 = 0, E5M2 = 1 };
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRowsPerWarp = 16;
+constexpr int kTileRows = kWarps * kRowsPerWarp;   // 128
+constexpr int32_t kStNonFinite = 1;
+
+template <int DT> struct In;
+template <> struct In<BF16> { static constexpr int VEC = 8; static constexpr int BYTES = 2; };
+template <> struct In<F32> { static constexpr int VEC = 4; static constexpr int BYTES = 4; };
+
+template <int FMT> struct Fp8;
+template <> struct Fp8<E4M3> { static constexpr float FMAX = 448.0f; static constexpr int EMAX = 8; };
+template <> struct Fp8<E5M2> { static constexpr float FMAX = 57344.0f; static constexpr int EMAX = 15; };
+
+// ---------------------------------------------------------------------------
+// memory
+// ---------------------------------------------------------------------------
+
+// Streaming 16-byte load: read-only path, no L1 allocation.
+QD uint4 ldg_stream(const void *p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+QD void stg16(void *p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+QD void stg8(void *p, uint32_t a, uint32_t b)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" :: "l"(p), "r"(a), "r"(b) : "memory");
+}
+QD void stg4(void *p, uint32_t a)
+{
+    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(a) : "memory");
+}
+
+QD uint32_t word(const uint4 &v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+
+// ---------------------------------------------------------------------------
+// element access
+// ---------------------------------------------------------------------------
+
+// Element j (0..VEC-1) of a 16-byte vector as an exact FP32 value.
+template <int DT> QD float elem(const uint4 &v, int j);
+template <> QD float elem<BF16>(const uint4 &v, int j)
+{
+    uint32_t w = word(v, j >> 1);
+    return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+template <> QD float elem<F32>(const uint4 &v, int j) { return __uint_as_float(word(v, j)); }
+
+// |x| bit patterns compare like the magnitudes they encode (finite values,
+// then inf, then NaN), so maxima are taken on integers.
+// absmax_bits: FP32 bit pattern of the largest |element| of the vector.
+template <int DT> QD uint32_t absmax_bits(const uint4 &v);
+template <> QD uint32_t absmax_bits<BF16>(const uint4 &v)
+{
+    const uint32_t M = 0x7FFF7FFFu;
+    uint32_t m = __vmaxu2(__vmaxu2(v.x & M, v.y & M), __vmaxu2(v.z & M, v.w & M));
+    return max(m << 16, m & 0xFFFF0000u);
+}
+template <> QD uint32_t absmax_bits<F32>(const uint4 &v)
+{
+    const uint32_t M = 0x7FFFFFFFu;
+    return max(max(v.x & M, v.y & M), max(v.z & M, v.w & M));
+}
+
+// Per-column running maximum of |x| over rows, kept in the input's packing:
+// BF16 packs two columns per word (max with __vmaxu2), FP32 one per word.
+template <int DT> QD uint32_t colmax_word(uint32_t acc, uint32_t w);
+template <> QD uint32_t colmax_word<BF16>(uint32_t acc, uint32_t w) { return __vmaxu2(acc, w & 0x7FFF7FFFu); }
+template <> QD uint32_t colmax_word<F32>(uint32_t acc, uint32_t w) { return max(acc, w & 0x7FFFFFFFu); }
+// FP32 bits of column j's maximum from the packed accumulators.
+template <int DT> QD uint32_t colmax_bits(const uint4 &acc, int j);
+template <> QD uint32_t colmax_bits<BF16>(const uint4 &acc, int j)
+{
+    uint32_t w = word(acc, j >> 1);
+    return (j & 1) ? (w & 0xFFFF0000u) : (w << 16);
+}
+template <> QD uint32_t colmax_bits<F32>(const uint4 &acc, int j) { return word(acc, j); }
+
+// ---------------------------------------------------------------------------
+// conversions (PTX cvt; RTNE, saturating to the largest finite value)
+// ---------------------------------------------------------------------------
+
+// Four FP32 values -> four FP8 codes in one word, a in the lowest byte.
+template <int FMT> QD uint32_t cvt_fp8x4(float a, float b, float c, float d);
+template <> QD uint32_t cvt_fp8x4<E4M3>(float a, float b, float c, float d)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+template <> QD uint32_t cvt_fp8x4<E5M2>(float a, float b, float c, float d)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+
+// Eight FP32 values -> eight E2M1 codes in one word, v0 in bits 3-0.
+QD uint32_t cvt_fp4x8(float v0, float v1, float v2, float v3, float v4, float v5, float v6, float v7)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r) : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+    return r;
+}
+
+// One E4M3 code (saturating RTNE) of an FP32 value, and its exact value.
+QD uint32_t e4m3_code(float f) { return cvt_fp8x4<E4M3>(f, 0.f, 0.f, 0.f) & 0xFFu; }
+QD float e4m3_value(uint32_t code)
+{
+    uint32_t h2;
+    uint16_t c = (uint16_t)code;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    float f;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+// Two FP8 codes (low, high byte of a 16-bit value) -> two exact FP32 values.
+template <int FMT> QD float2 fp8x2_to_f32(uint32_t two);
+template <> QD float2 fp8x2_to_f32<E4M3>(uint32_t two)
+{
+    uint32_t h2;
+    uint16_t c = (uint16_t)two;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return make_float2(lo, hi);
+}
+template <> QD float2 fp8x2_to_f32<E5M2>(uint32_t two)
+{
+    uint32_t h2;
+    uint16_t c = (uint16_t)two;
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(c));
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+// Two E2M1 codes (one byte: low nibble first) -> two exact FP32 values.
+QD float2 fp4x2_to_f32(uint32_t byte)
+{
+    uint32_t h2;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h2) : "r"(byte));
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+// FP32 -> BF16 bits, round to nearest even.
+QD uint32_t bf16_bits(float f)
+{
+    uint16_t h;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+    return h;
+}
+
+// ---------------------------------------------------------------------------
+// scales
+// ---------------------------------------------------------------------------
+
+// alpha = fmax / a; a = 0 -> 1; an alpha that overflows -> FLT_MAX.
+QD float alpha_from_amax(float fmax, float a)
+{
+    if (a == 0.0f) return 1.0f;
+    float al = __fdiv_rn(fmax, a);
+    if (al == __int_as_float(0x7F800000)) al = FLT_MAX;
+    return al;
+}
+
+// floor(log2 b) for the FP32 bit pattern b of a positive value, exact:
+// normals from the exponent field, subnormals from the leading one of the
+// mantissa; inf / NaN give 128 (exponent field 255).
+QD int floor_log2_bits(uint32_t b)
+{
+    uint32_t E = b >> 23;
+    if (E == 0) return (31 - __clz(b & 0x7FFFFFu)) - 149;
+    return (int)E - 127;
+}
+
+// E8M0 code for a block whose largest magnitude has FP32 bits b.
+template <int FMT> QD uint32_t mx_code(uint32_t b)
+{
+    if (b == 0) return 127u;
+    int c = floor_log2_bits(b) - Fp8<FMT>::EMAX + 127;
+    c = c < 0 ? 0 : (c > 254 ? 254 : c);
+    return (uint32_t)c;
+}
+
+// 2^(127 - code) as an FP32 value (code in [0, 254]; 2^-127 is subnormal).
+QD float mx_inv_scale(uint32_t code)
+{
+    int e = 127 - (int)code;
+    return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11)
+// ---------------------------------------------------------------------------
+
+QD uint4 philox4x32_10(uint4 c, uint2 k)
+{
+#pragma unroll
+    for (int r = 0; r < 10; r++) {
+        uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+        k.x += 0x9E3779B9u;
+        k.y += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// The 128 random bits of block g (= offset + element index / 8) of a stream.
+QD uint4 sr_bits(uint64_t seed, uint64_t g, uint32_t stream)
+{
+    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, 0u),
+                         make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+}
+
+// Stochastic rounding of y onto the E2M1 grid with 16 random bits r16:
+// with a = |y| < 6, lo the grid value below a, ulp the spacing there and
+// frac = (a - lo) / ulp, round up iff r16 < frac * 2^16.  Every step is
+// exact in FP32 (the spacing is a power of two).  Returns a value on the
+// grid with y's sign (NaN passes through to the RTNE conversion).
+QD float sr_e2m1_value(float y, uint32_t r16)
+{
+    float a = fabsf(y);
+    if (!(a < 6.0f)) return y;                      // >= 6 saturates in cvt; NaN stays NaN
+    float ulp = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
+    float t = __fmul_rn(a, a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f));   // a / ulp, exact
+    float fl = floorf(t);
+    float frac = t - fl;                            // exact
+    float v = __fmul_rn(fl, ulp);
+    if ((float)r16 < __fmul_rn(frac, 65536.0f)) v = v + ulp;   // exact sum on the grid
+    return copysignf(v, y);
+}
+
+// ---------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------
+
+QD uint32_t warp_max(uint32_t v) { return __reduce_max_sync(0xFFFFFFFFu, v); }
+
+// Max over groups of G consecutive lanes (G a power of two <= 32).
+template <int G> QD uint32_t group_max(uint32_t v)
+{
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+QD void flag_nonfinite(int32_t *status, uint32_t amax_bits)
+{
+    if (status != nullptr && amax_bits >= 0x7F800000u) atomicOr(status, kStNonFinite);
+}
+
+// 4x4 byte transpose: in r[i] byte j = element (row i, col j);
+// out c[j] byte i = the same element.
+QD void transpose4x4(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
+                     uint32_t &c0, uint32_t &c1, uint32_t &c2, uint32_t &c3)
+{
+    uint32_t t0 = __byte_perm(r0, r1, 0x5140), t1 = __byte_perm(r2, r3, 0x5140);
+    uint32_t t2 = __byte_perm(r0, r1, 0x7362), t3 = __byte_perm(r2, r3, 0x7362);
+    c0 = __byte_perm(t0, t1, 0x5410);
+    c1 = __byte_perm(t0, t1, 0x7632);
+    c2 = __byte_perm(t2, t3, 0x5410);
+    c3 = __byte_perm(t2, t3, 0x7632);
+}
+
+}  // namespace qk

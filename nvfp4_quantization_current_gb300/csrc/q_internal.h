@@ -1,0 +1,44 @@
+// Launchers shared between the C-ABI layer (q_api.cu) and the kernel files.
+// Every launcher enqueues on `st` and returns cudaGetLastError().
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qk {
+
+int sm_count();
+
+// current scaling
+cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *status, cudaStream_t st);
+cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *amax,
+                           uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st);
+
+// MXFP8
+cudaError_t launch_mxfp8(const void *x, int dt, int64_t M, int64_t K, int fmt, uint8_t *q_row,
+                         uint8_t *e_row, uint8_t *q_col, uint8_t *e_col, int32_t *status, cudaStream_t st);
+
+// blockwise
+cudaError_t launch_blockwise(const void *x, int dt, int64_t M, int64_t K, int tile, uint8_t *q_row,
+                             float *s_row, uint8_t *q_colT, float *s_colT, int32_t *status, cudaStream_t st);
+
+// NVFP4 (the amax is already in *amax)
+cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, int rnd, uint64_t seed,
+                         uint64_t offset, const float *amax, uint8_t *q_row, uint8_t *sb_row,
+                         uint8_t *q_colT, uint8_t *sb_colT, float *s_global, int32_t *status,
+                         cudaStream_t st);
+
+// dequantizers
+cudaError_t launch_dq_cs(const uint8_t *q, const float *s, int64_t R, int64_t C, int fmt, int out,
+                         void *y, cudaStream_t st);
+cudaError_t launch_dq_mxfp8(const uint8_t *q, const uint8_t *e, int64_t R, int64_t C, int fmt, int dir,
+                            int out, void *y, cudaStream_t st);
+cudaError_t launch_dq_blockwise(const uint8_t *q, const float *s, int64_t R, int64_t C, int tile, int out,
+                                void *y, cudaStream_t st);
+cudaError_t launch_dq_nvfp4(const uint8_t *q, const uint8_t *sb, const float *s_g, int64_t R, int64_t C,
+                            int blk, int out, void *y, cudaStream_t st);
+
+// Scales of an empty tensor (amax 0): writes *amax = 0 (if amax_out), *scale = 1.
+cudaError_t launch_empty_scales(float *amax_out, float *scale, cudaStream_t st);
+
+}  // namespace qk

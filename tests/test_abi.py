@@ -1,0 +1,116 @@
+"""The C-ABI library loads, exports every entry point include/q.h declares,
+and rejects bad arguments on the host before any CUDA call (no GPU needed:
+every call below fails validation, so nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_quantization_current_gb300 as Q
+from nvfp4_quantization_current_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return Q.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:q|dq)_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["q_amax", "q_current_scaling", "q_mxfp8", "q_blockwise", "q_nvfp4", "dq_current_scaling",
+              "dq_mxfp8", "dq_blockwise", "dq_nvfp4", "q_last_error", "q_abi_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+        assert n in Q.SIGNATURES, n
+    assert L.q_abi_version() == 1
+
+
+A = ctypes.c_void_p(0x10000)        # an aligned non-NULL address that is never dereferenced
+MIS = ctypes.c_void_p(0x10008)      # 8-byte aligned only
+
+
+def status_of(L, fn, *args):
+    st = getattr(L, fn)(*args)
+    return st, L.q_last_error().decode()
+
+
+def test_current_scaling_validation(L):
+    st, msg = status_of(L, "q_current_scaling", None, Q.Q_BF16, 4, 16, Q.Q_E4M3, A, None, A, 0, A, None, None)
+    assert st == Q.Q_ERR_ARG and "x is NULL" in msg
+    st, _ = status_of(L, "q_current_scaling", A, 7, 4, 16, Q.Q_E4M3, A, None, A, 0, A, None, None)
+    assert st == Q.Q_ERR_DTYPE
+    st, _ = status_of(L, "q_current_scaling", A, Q.Q_BF16, 4, 16, 9, A, None, A, 0, A, None, None)
+    assert st == Q.Q_ERR_ARG
+    st, _ = status_of(L, "q_current_scaling", A, Q.Q_BF16, 4, 16, Q.Q_E4M3, None, None, A, 0, A, None, None)
+    assert st == Q.Q_ERR_ARG                       # nothing requested
+    st, _ = status_of(L, "q_current_scaling", MIS, Q.Q_BF16, 4, 16, Q.Q_E4M3, A, None, A, 0, A, None, None)
+    assert st == Q.Q_ERR_ALIGN
+    st, _ = status_of(L, "q_current_scaling", A, Q.Q_BF16, 24, 16, Q.Q_E4M3, None, A, A, 0, A, None, None)
+    assert st == Q.Q_ERR_SHAPE                     # colT needs M % 16
+    st, _ = status_of(L, "q_current_scaling", A, Q.Q_BF16, -1, 16, Q.Q_E4M3, A, None, A, 0, A, None, None)
+    assert st == Q.Q_ERR_SHAPE
+    st, msg = status_of(L, "q_current_scaling", A, Q.Q_BF16, 1 << 40, 1 << 30, Q.Q_E4M3, A, None, A, 0, A, None, None)
+    assert st == Q.Q_ERR_SHAPE and "too large" in msg
+    st, _ = status_of(L, "q_current_scaling", A, Q.Q_BF16, 4, 16, Q.Q_E4M3, A, None, None, 0, A, None, None)
+    assert st == Q.Q_ERR_ARG                       # amax required
+    st, _ = status_of(L, "q_current_scaling", A, Q.Q_BF16, 4, 16, Q.Q_E4M3, A, None, A, 5, A, None, None)
+    assert st == Q.Q_ERR_ARG                       # bad amax mode
+
+
+def test_block_recipes_validation(L):
+    st, _ = status_of(L, "q_mxfp8", A, Q.Q_BF16, 64, 48, Q.Q_E4M3, A, A, None, None, None, None)
+    assert st == Q.Q_ERR_SHAPE                     # K % 32
+    st, _ = status_of(L, "q_mxfp8", A, Q.Q_BF16, 48, 64, Q.Q_E4M3, None, None, A, A, None, None)
+    assert st == Q.Q_ERR_SHAPE                     # M % 32 with the columnwise output
+    st, _ = status_of(L, "q_mxfp8", A, Q.Q_BF16, 64, 64, Q.Q_E4M3, A, None, None, None, None, None)
+    assert st == Q.Q_ERR_ARG                       # missing scale buffer
+    st, _ = status_of(L, "q_blockwise", A, Q.Q_BF16, 128, 192, Q.Q_T1x128, A, A, None, None, None, None)
+    assert st == Q.Q_ERR_SHAPE
+    st, _ = status_of(L, "q_blockwise", A, Q.Q_BF16, 192, 128, Q.Q_T128x128, A, A, None, None, None, None)
+    assert st == Q.Q_ERR_SHAPE
+    st, _ = status_of(L, "q_blockwise", A, Q.Q_BF16, 128, 128, 3, A, A, None, None, None, None)
+    assert st == Q.Q_ERR_ARG
+    st, _ = status_of(L, "q_nvfp4", A, Q.Q_BF16, 16, 24, Q.Q_B1x16, Q.Q_RN, 0, 0, A, A, None, None, A, 0, A, None, None)
+    assert st == Q.Q_ERR_SHAPE
+    st, _ = status_of(L, "q_nvfp4", A, Q.Q_BF16, 16, 32, Q.Q_B1x16, 2, 0, 0, A, A, None, None, A, 0, A, None, None)
+    assert st == Q.Q_ERR_ARG
+    st, _ = status_of(L, "q_nvfp4", A, Q.Q_BF16, 16, 32, Q.Q_B1x16, Q.Q_RN, 0, 0, A, A, None, None, A, 0, None, None, None)
+    assert st == Q.Q_ERR_ARG                       # s_global required
+
+
+def test_dequant_validation(L):
+    st, _ = status_of(L, "dq_current_scaling", A, A, 4, 4, Q.Q_E4M3, 5, A, None)
+    assert st == Q.Q_ERR_DTYPE
+    st, _ = status_of(L, "dq_mxfp8", A, A, 4, 48, Q.Q_E4M3, Q.Q_ROW, Q.Q_F32, A, None)
+    assert st == Q.Q_ERR_SHAPE
+    st, _ = status_of(L, "dq_mxfp8", A, MIS, 32, 48, Q.Q_E4M3, Q.Q_COL, Q.Q_F32, A, None)
+    assert st == Q.Q_ERR_ALIGN
+    st, _ = status_of(L, "dq_blockwise", A, A, 4, 100, Q.Q_T1x128, Q.Q_F32, A, None)
+    assert st == Q.Q_ERR_SHAPE
+    st, _ = status_of(L, "dq_nvfp4", A, A, A, 4, 24, Q.Q_B1x16, Q.Q_F32, A, None)
+    assert st == Q.Q_ERR_SHAPE
+    st, _ = status_of(L, "dq_nvfp4", A, A, A, 8, 32, Q.Q_B16x16, Q.Q_F32, A, None)
+    assert st == Q.Q_ERR_SHAPE
+    st, _ = status_of(L, "dq_nvfp4", A, A, None, 16, 32, Q.Q_B1x16, Q.Q_F32, A, None)
+    assert st == Q.Q_ERR_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    with pytest.raises(ValueError, match="CUDA"):
+        Q.q_current_scaling(torch.zeros(4, 16))

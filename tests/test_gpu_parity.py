@@ -1,0 +1,327 @@
+"""GPU parity: every recipe through the C ABI against the CPU oracle on the
+same seeded inputs, element by element, 0 ULP (codes and scale bytes
+bit-identical; FP32 / BF16 values bit-identical).
+
+Sizes span several 128 x 256 CTA tiles with ragged tails in both
+dimensions; edge cases: the pages' worked example, empty tensors, zero
+tensors and zero blocks, FP32 inputs, tiny values (subnormal scaled
+values), non-zero SR offsets.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+Q = pytest.importorskip("nvfp4_quantization_current_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    Q.lib()
+
+
+def dev(x):
+    """numpy BF16 bits (uint16) or FP32 -> CUDA tensor of the same values."""
+    if x.dtype == np.uint16:
+        return torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    return torch.from_numpy(x.copy()).cuda()
+
+
+def host(t):
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def same(a, b, what=""):
+    a, b = np.asarray(a), np.asarray(b)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    if a.dtype == np.float32:
+        a, b = a.view(np.uint32), b.view(np.uint32)
+    bad = np.argwhere(a != b)
+    assert bad.size == 0, f"{what}: {len(bad)} mismatches, first at {bad[:5].tolist()}: gpu {a[tuple(bad[0])]} oracle {b[tuple(bad[0])]}"
+
+
+def f32eq(a, b, what=""):
+    assert np.float32(a).view(np.uint32) == np.float32(b).view(np.uint32), (what, a, b)
+
+
+OUTS = [torch.float32, torch.bfloat16]
+
+
+def o_out(dtype):
+    return O.F32 if dtype == torch.float32 else O.BF16
+
+
+# ---------------------------------------------------------------------------
+# amax + current scaling
+# ---------------------------------------------------------------------------
+
+CS_CASES = [
+    # (kind, shape, bf16, fmt, colwise)
+    ("outliers", (1024, 1024), False, O.E4M3, True),      # the small FP32 workload
+    ("outliers", (272, 528), True, O.E4M3, True),         # ragged in both tile dimensions
+    ("grad", (384, 640), True, O.E5M2, True),
+    ("weight", (256, 256), True, O.E4M3, False),
+    ("normal", (1000, 784), True, O.E4M3, False),         # rowwise only: any shape
+    ("t3", (37, 61), False, O.E5M2, False),               # odd sizes: vector tail + scalar tail
+    ("normal", (16, 16), False, O.E4M3, True),
+]
+
+
+@pytest.mark.parametrize("kind,shape,bf16,fmt,colwise", CS_CASES)
+def test_current_scaling_parity(kind, shape, bf16, fmt, colwise):
+    x = W.gen(kind, shape, 101, bf16=bf16)
+    want = O.current_scaling(x, fmt, rowwise=True, colwise=colwise)
+    got = Q.q_current_scaling(dev(x), "e4m3" if fmt == O.E4M3 else "e5m2", rowwise=True, colwise=colwise)
+    torch.cuda.synchronize()
+    f32eq(got.amax.item(), want.amax, "amax")
+    f32eq(got.scale.item(), want.scale, "scale")
+    same(host(got.q_row), want.q_row, "q_row")
+    if colwise:
+        same(host(got.q_colT), want.q_colT, "q_colT")
+    for dt in OUTS:
+        y = got.dequantize(Q.Q_ROW, dt)
+        same(host(y), O.dq_current_scaling(want.q_row, want.scale, fmt, o_out(dt)), f"dq {dt}")
+
+
+def test_current_scaling_worked_example():
+    x = W.EXAMPLE_X
+    want = O.current_scaling(x)
+    got = Q.q_current_scaling(dev(x))
+    same(host(got.q_row), want.q_row)
+    f32eq(got.scale.item(), want.scale)
+    y = host(got.dequantize())
+    same(y, O.dq_current_scaling(want.q_row, want.scale))
+    assert host(got.q_row).tolist() == [[0xFE, 0x63, 0x7E]]     # -448, 44, 448
+
+
+def test_amax_alone_and_given_amax_sharding():
+    x = W.gen("outliers", (512, 384), 7, bf16=True)
+    a = Q.q_amax(dev(x))
+    f32eq(a.item(), O.amax(x))
+    # two row shards quantized with the MAX of their local amaxes equal the whole tensor
+    xs = [x[:128], x[128:]]
+    loc = [Q.q_amax(dev(s)) for s in xs]
+    g = torch.maximum(loc[0], loc[1])
+    parts = [Q.q_current_scaling(dev(s), colwise=True, amax=g.clone()) for s in xs]
+    whole = Q.q_current_scaling(dev(x), colwise=True)
+    same(np.concatenate([host(p.q_row) for p in parts]), host(whole.q_row))
+    same(np.concatenate([host(p.q_colT) for p in parts], axis=1), host(whole.q_colT))
+
+
+def test_current_scaling_zero_and_empty():
+    z = np.zeros((64, 64), np.uint16)
+    got = Q.q_current_scaling(dev(z), colwise=True)
+    assert got.amax.item() == 0 and got.scale.item() == 1
+    assert not host(got.q_row).any() and not host(got.q_colT).any()
+    e = torch.empty((0, 16), dtype=torch.bfloat16, device="cuda")
+    got = Q.q_current_scaling(e)
+    assert got.amax.item() == 0 and got.scale.item() == 1
+    assert Q.q_amax(torch.empty((0,), dtype=torch.float32, device="cuda").view(0, 1)).item() == 0
+
+
+def test_tiny_values_scale_to_fp32_subnormals():
+    x = (W.gen("normal", (64, 64), 3, bf16=False) * np.float32(1e-38)).astype(np.float32)
+    x[0, 0] = np.float32(1e-30)
+    want = O.current_scaling(x, O.E4M3, colwise=True)
+    got = Q.q_current_scaling(dev(x), colwise=True)
+    same(host(got.q_row), want.q_row)
+    same(host(got.q_colT), want.q_colT)
+    f32eq(got.scale.item(), want.scale)
+
+
+def test_nonfinite_sets_status():
+    x = W.gen("normal", (32, 32), 3, bf16=False)
+    x[3, 4] = np.inf
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.q_current_scaling(dev(x), status=st)
+    assert st.item() & Q.Q_ST_NONFINITE
+    st.zero_()
+    Q.q_mxfp8(dev(x), status=st)
+    assert st.item() & Q.Q_ST_NONFINITE
+    st.zero_()
+    Q.q_nvfp4(dev(x), status=st)
+    assert st.item() & Q.Q_ST_NONFINITE
+    st.zero_()
+    Q.q_current_scaling(dev(W.gen("normal", (32, 32), 3, bf16=False)), status=st)
+    assert st.item() == 0
+
+
+# ---------------------------------------------------------------------------
+# MXFP8
+# ---------------------------------------------------------------------------
+
+MX_CASES = [
+    ("lognormal_rows", (256, 512), True, O.E4M3),
+    ("lognormal_rows", (96, 800), True, O.E4M3),     # ragged: 800 = 3 * 256 + 32
+    ("t3", (160, 288), True, O.E5M2),
+    ("normal", (64, 416), False, O.E4M3),             # FP32 input, 128-column CTA tiles
+    ("grad", (32, 32), True, O.E5M2),
+]
+
+
+@pytest.mark.parametrize("kind,shape,bf16,fmt", MX_CASES)
+def test_mxfp8_parity(kind, shape, bf16, fmt):
+    x = W.gen(kind, shape, 202, bf16=bf16)
+    x_t = x.copy()
+    if bf16:
+        x_t[:, :32] = 0          # an all-zero row block in every row and a zero column block
+    want = O.mxfp8(x_t, fmt)
+    got = Q.q_mxfp8(dev(x_t), "e4m3" if fmt == O.E4M3 else "e5m2")
+    torch.cuda.synchronize()
+    same(host(got.q_row), want.q_row, "q_row")
+    same(host(got.e8m0_row), want.e8m0_row, "e8m0_row")
+    same(host(got.q_col), want.q_col, "q_col")
+    same(host(got.e8m0_col), want.e8m0_col, "e8m0_col")
+    for dt in OUTS:
+        same(host(got.dequantize(Q.Q_ROW, dt)), O.dq_mxfp8(want.q_row, want.e8m0_row, fmt, O.ROW, o_out(dt)), "dq row")
+        same(host(got.dequantize(Q.Q_COL, dt)), O.dq_mxfp8(want.q_col, want.e8m0_col, fmt, O.COL, o_out(dt)), "dq col")
+
+
+def test_mxfp8_rowwise_only_ragged_rows():
+    x = W.gen("lognormal_rows", (100, 288), 5, bf16=True)
+    want = O.mxfp8(x, O.E4M3, rowwise=True, colwise=False)
+    got = Q.q_mxfp8(dev(x), colwise=False)
+    same(host(got.q_row), want.q_row)
+    same(host(got.e8m0_row), want.e8m0_row)
+
+
+def test_mxfp8_extreme_exponents():
+    """Block maxima at FP32 subnormal / huge magnitudes exercise the clamps
+    of the E8M0 code and the 2^-127 factor."""
+    x = W.gen("normal", (64, 64), 6, bf16=False)
+    x[:32, :32] *= np.float32(1e-42)          # subnormal inputs
+    x[32:, 32:] *= np.float32(1e36)
+    x = x.astype(np.float32)
+    want = O.mxfp8(x, O.E4M3)
+    got = Q.q_mxfp8(dev(x))
+    same(host(got.q_row), want.q_row)
+    same(host(got.e8m0_row), want.e8m0_row)
+    same(host(got.q_col), want.q_col)
+    same(host(got.e8m0_col), want.e8m0_col)
+    same(host(got.dequantize(Q.Q_ROW)), O.dq_mxfp8(want.q_row, want.e8m0_row, O.E4M3, O.ROW, O.F32))
+
+
+# ---------------------------------------------------------------------------
+# blockwise
+# ---------------------------------------------------------------------------
+
+BW_CASES = [
+    ("normal", (256, 640), True, O.T1x128, True),
+    ("normal", (384, 384), False, O.T1x128, True),
+    ("t3", (300, 384), True, O.T1x128, False),          # ragged rows, rowwise only
+    ("weight", (384, 640), True, O.T128x128, True),
+    ("weight", (128, 128), False, O.T128x128, True),
+]
+
+
+@pytest.mark.parametrize("kind,shape,bf16,tile,colwise", BW_CASES)
+def test_blockwise_parity(kind, shape, bf16, tile, colwise):
+    x = W.gen(kind, shape, 303, bf16=bf16)
+    if shape[0] >= 256:
+        x[128:256, 128:256] = 0      # an all-zero tile
+    want = O.blockwise(x, tile, rowwise=True, colwise=colwise)
+    got = Q.q_blockwise(dev(x), "1x128" if tile == O.T1x128 else "128x128", rowwise=True, colwise=colwise)
+    torch.cuda.synchronize()
+    same(host(got.q_row), want.q_row, "q_row")
+    same(host(got.s_row), want.s_row, "s_row")
+    if colwise:
+        same(host(got.q_colT), want.q_colT, "q_colT")
+        same(host(got.s_colT), want.s_colT, "s_colT")
+    for dt in OUTS:
+        same(host(got.dequantize(Q.Q_ROW, dt)), O.dq_blockwise(want.q_row, want.s_row, tile, o_out(dt)), "dq row")
+        if colwise:
+            same(host(got.dequantize(Q.Q_COL, dt)), O.dq_blockwise(want.q_colT, want.s_colT, tile, o_out(dt)), "dq colT")
+
+
+# ---------------------------------------------------------------------------
+# NVFP4
+# ---------------------------------------------------------------------------
+
+NV_CASES = [
+    # kind, shape, bf16, blk, rnd, seed, offset
+    ("normal", (256, 512), True, O.B1x16, O.RN, 0, 0),
+    ("normal", (272, 528), True, O.B1x16, O.RN, 0, 0),      # ragged both ways
+    ("t3", (272, 528), True, O.B1x16, O.SR, 4, 0),
+    ("t3", (128, 256), True, O.B1x16, O.SR, 0xDEADBEEFCAFE, 12345),
+    ("normal", (48, 160), False, O.B1x16, O.RN, 0, 0),      # FP32 input
+    ("t3", (48, 160), False, O.B1x16, O.SR, 9, 3),
+    ("weight", (256, 512), True, O.B16x16, O.RN, 0, 0),
+    ("weight", (144, 272), True, O.B16x16, O.RN, 0, 0),
+    ("weight", (144, 272), True, O.B16x16, O.SR, 77, 5),
+    ("weight", (64, 96), False, O.B16x16, O.RN, 0, 0),
+]
+
+
+@pytest.mark.parametrize("kind,shape,bf16,blk,rnd,seed,offset", NV_CASES)
+def test_nvfp4_parity(kind, shape, bf16, blk, rnd, seed, offset):
+    x = W.gen(kind, shape, 404, bf16=bf16)
+    x[:16, :16] = 0                                   # an all-zero block
+    want = O.nvfp4(x, blk, rnd, seed=seed, offset=offset, rowwise=True, colwise=True)
+    got = Q.q_nvfp4(dev(x), "1x16" if blk == O.B1x16 else "16x16", "rn" if rnd == O.RN else "sr",
+                    seed=seed, offset=offset, rowwise=True, colwise=True)
+    torch.cuda.synchronize()
+    f32eq(got.amax.item(), want.amax, "amax")
+    f32eq(got.s_global.item(), want.s_global, "s_global")
+    same(host(got.sb_row), want.sb_row, "sb_row")
+    same(host(got.q_row), want.q_row, "q_row")
+    same(host(got.sb_colT), want.sb_colT, "sb_colT")
+    same(host(got.q_colT), want.q_colT, "q_colT")
+    for dt in OUTS:
+        same(host(got.dequantize(Q.Q_ROW, dt)), O.dq_nvfp4(want.q_row, want.sb_row, want.s_global, blk, o_out(dt)), "dq row")
+        same(host(got.dequantize(Q.Q_COL, dt)), O.dq_nvfp4(want.q_colT, want.sb_colT, want.s_global, blk, o_out(dt)), "dq colT")
+
+
+def test_nvfp4_single_direction_and_given_amax():
+    x = W.gen("t3", (128, 256), 5, bf16=True)
+    a = Q.q_amax(dev(x)) * 2          # a larger (e.g. all-reduced) amax
+    want = O.nvfp4(x, O.B1x16, O.SR, seed=1, offset=0, rowwise=False, colwise=True, amax_in=float(a.item()))
+    got = Q.q_nvfp4(dev(x), rounding="sr", seed=1, rowwise=False, colwise=True, amax=a)
+    same(host(got.q_colT), want.q_colT)
+    same(host(got.sb_colT), want.sb_colT)
+    f32eq(got.s_global.item(), want.s_global)
+
+
+def test_nvfp4_empty():
+    got = Q.q_nvfp4(torch.empty((0, 32), dtype=torch.bfloat16, device="cuda"))
+    assert got.amax.item() == 0 and got.s_global.item() == 1
+
+
+def test_e2m1_cast_exhaustive_through_nvfp4():
+    """Every BF16 magnitude below 6 reaches the E2M1 conversion unscaled:
+    with a given amax of 2688 (alpha_g = 1), a 16-element block whose
+    largest entry is 6 has block scale 1 and enc = 1."""
+    vals = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    vals = vals[np.isfinite(vals) & (np.abs(vals) <= 6)]
+    n = (len(vals) + 14) // 15 * 15
+    vals = np.concatenate([vals, np.zeros(n - len(vals), np.float32)]).reshape(-1, 15)
+    blocks = np.concatenate([np.full((vals.shape[0], 1), 6.0, np.float32), vals], axis=1)
+    rows = (blocks.shape[0] + 15) // 16 * 16
+    x = np.zeros((rows, 16), np.float32)
+    x[: blocks.shape[0]] = blocks
+    amax = torch.tensor([2688.0], device="cuda")
+    want = O.nvfp4(x, O.B1x16, O.RN, rowwise=True, amax_in=2688.0)
+    got = Q.q_nvfp4(dev(x), rowwise=True, amax=amax)
+    same(host(got.sb_row), want.sb_row)
+    same(host(got.q_row), want.q_row)
+    assert np.all(want.sb_row[: blocks.shape[0]] == 0x38)
+
+
+@pytest.mark.parametrize("fmt,fmax", [(O.E4M3, 448.0), (O.E5M2, 57344.0)])
+def test_fp8_cast_exhaustive_bf16(fmt, fmax):
+    """Every BF16 bit pattern (NaN and inf included) through the cast with
+    alpha = Fmax / Fmax = 1: the codes are the plain saturating RTNE cast."""
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(4096, 16)
+    amax = torch.tensor([fmax], device="cuda")
+    want = O.current_scaling(x, fmt, rowwise=True, colwise=True, amax_in=fmax)
+    got = Q.q_current_scaling(dev(x), "e4m3" if fmt == O.E4M3 else "e5m2", colwise=True, amax=amax)
+    f32eq(got.scale.item(), 1.0)
+    same(host(got.q_row), want.q_row, "q_row")
+    same(host(got.q_colT), want.q_colT, "q_colT")
