@@ -1,0 +1,687 @@
+#!/usr/bin/env python
+"""Benchmark of the quantizer hot path on synthetic tensors shaped like the
+pages' workloads.
+
+One step = one pass of every recipe over its full-size tensors (all five
+workloads of ``workloads.WORKLOADS``): current-scaling amax + cast (+ the
+transposed copy), MXFP8 row + col, blockwise 1x128 (+ transposed) and
+128x128 (+ transposed), NVFP4 1x16 RTNE, 1x16 stochastic rounding and 16x16,
+and the dequantizer of each.  Every call goes through the C ABI with
+preallocated outputs.
+
+Metric: quantize GB/s = algorithmic bytes (input bytes x reads + all output
+bytes; reads = 2 for current scaling and NVFP4, whose amax pass reads the
+tensor once more, 1 otherwise) / device time, summed over the step.  L2 is
+flushed (a 256 MiB write) before every timed call; the time of a call is
+taken with CUDA events on the launching stream around that call only.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (the plain C reference
+implementation) on a bounded row sample of the same workload instead.
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as WL  # noqa: E402
+
+METRIC = "quantize GB/s (bytes read+written) and % of GB300 HBM peak per recipe"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+CPU_SAMPLE_FRAC = 1.0 / 8.0
+REF_BUDGET_S = 120.0
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
+# ncu capture, keyed by kernel, with the hash of the kernel's source file at
+# capture time; reported as null when the source has changed since.
+TRAFFIC = {}
+
+
+def src_hash(fname):
+    p = os.path.join(ROOT, "nvfp4_quantization_current_gb300", "csrc", fname)
+    with open(p, "rb") as f:
+        h = hashlib.sha256(f.read())
+    with open(os.path.join(ROOT, "nvfp4_quantization_current_gb300", "csrc", "q_common.cuh"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------------
+# the step: a list of calls, each a list of (kernel name, source file,
+# algorithmic bytes, thunk issuing one C-ABI call)
+# --------------------------------------------------------------------------
+
+class Call:
+    def __init__(self, name, recipe, pieces, h2d, d2h, e2e_thunk):
+        self.name = name            # e.g. "hy4.grad cs_e5m2 row+colT"
+        self.recipe = recipe        # current_scaling | mxfp8 | blockwise | nvfp4 | dequant
+        self.pieces = pieces        # [(kernel, srcfile, alg_bytes, thunk)]
+        self.h2d = h2d              # input tensors (device) whose bytes an end-to-end call copies in
+        self.d2h = d2h              # output tensors copied back end to end
+        self.e2e_thunk = e2e_thunk  # the single public-API call (amax computed inside)
+
+    @property
+    def alg_bytes(self):
+        return sum(p[2] for p in self.pieces)
+
+
+def nbytes(*ts):
+    return sum(int(t.numel() * t.element_size()) for t in ts if t is not None)
+
+
+def build_step(dev_tensors, torch, Q):
+    """Preallocate every output and return the list of calls of one step."""
+    calls = []
+    d = dev_tensors
+
+    def cs(tag, x, fmt, colwise):
+        out = Q.alloc_current_scaling(x.shape[0], x.shape[1], x.device, fmt, True, colwise)
+        amax = out.amax
+        ins = nbytes(x)
+        outs = nbytes(out.q_row, out.q_colT, out.scale)
+        pieces = [
+            ("amax", "k_current_scaling.cu", ins, lambda: Q.q_amax(x, out=amax)),
+            ("cs_cast" + ("_T" if colwise else ""), "k_current_scaling.cu", ins + outs + 4,
+             lambda: Q.q_current_scaling(x, fmt, True, colwise, amax=amax, out=out)),
+        ]
+
+        def e2e():
+            o = Q.q_current_scaling(x, fmt, True, colwise, out=out)
+            o.amax = amax
+            return o
+        calls.append(Call(f"{tag} cs_{fmt} row{'+colT' if colwise else ''}", "current_scaling", pieces, [x],
+                          [out.q_row, out.q_colT, out.scale], e2e))
+        y = torch.empty(x.shape, dtype=torch.bfloat16 if x.dtype == torch.bfloat16 else torch.float32, device=x.device)
+        calls.append(Call(f"{tag} dq_cs row->{str(y.dtype)[6:]}", "dequant",
+                          [("dq_cs", "k_dequant.cu", nbytes(out.q_row, out.scale, y),
+                            lambda: Q.dq_current_scaling(out.q_row, out.scale, fmt, y.dtype, out=y))],
+                          [out.q_row], [y], lambda: Q.dq_current_scaling(out.q_row, out.scale, fmt, y.dtype, out=y)))
+
+    def mx(tag, x):
+        out = Q.alloc_mxfp8(x.shape[0], x.shape[1], x.device, "e4m3", True, True)
+        b = nbytes(x, out.q_row, out.e8m0_row, out.q_col, out.e8m0_col)
+        run = lambda: Q.q_mxfp8(x, "e4m3", True, True, out=out)
+        calls.append(Call(f"{tag} mxfp8_e4m3 row+col", "mxfp8", [("mxfp8", "k_mxfp8.cu", b, run)], [x],
+                          [out.q_row, out.e8m0_row, out.q_col, out.e8m0_col], run))
+        for direction, q, e in ((Q.Q_ROW, out.q_row, out.e8m0_row), (Q.Q_COL, out.q_col, out.e8m0_col)):
+            y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+            r = (lambda q=q, e=e, direction=direction, y=y: Q.dq_mxfp8(q, e, "e4m3", direction, torch.bfloat16, out=y))
+            calls.append(Call(f"{tag} dq_mxfp8 {'row' if direction == Q.Q_ROW else 'col'}->bf16", "dequant",
+                              [("dq_mxfp8", "k_dequant.cu", nbytes(q, e, y), r)], [q, e], [y], r))
+
+    def bw(tag, x, tile, colwise):
+        out = Q.alloc_blockwise(x.shape[0], x.shape[1], x.device, tile, True, colwise)
+        b = nbytes(x, out.q_row, out.s_row, out.q_colT, out.s_colT)
+        run = lambda: Q.q_blockwise(x, tile, True, colwise, out=out)
+        calls.append(Call(f"{tag} blockwise_{tile} row{'+colT' if colwise else ''}", "blockwise",
+                          [("bw_" + tile + ("_T" if colwise else ""), "k_blockwise.cu", b, run)], [x],
+                          [out.q_row, out.s_row, out.q_colT, out.s_colT], run))
+        y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+        r = lambda: Q.dq_blockwise(out.q_row, out.s_row, tile, torch.bfloat16, out=y)
+        calls.append(Call(f"{tag} dq_blockwise_{tile} row->bf16", "dequant",
+                          [("dq_blockwise", "k_dequant.cu", nbytes(out.q_row, out.s_row, y), r)],
+                          [out.q_row, out.s_row], [y], r))
+
+    def nv(tag, x, blk, rnd, seed):
+        out = Q.alloc_nvfp4(x.shape[0], x.shape[1], x.device, blk, True, True)
+        amax = out.amax
+        ins = nbytes(x)
+        outs = nbytes(out.q_row, out.sb_row, out.q_colT, out.sb_colT, out.s_global)
+        pieces = [
+            ("amax", "k_current_scaling.cu", ins, lambda: Q.q_amax(x, out=amax)),
+            (f"nvfp4_{blk}_{rnd}", "k_nvfp4.cu", ins + outs + 4,
+             lambda: Q.q_nvfp4(x, blk, rnd, seed, 0, True, True, amax=amax, out=out)),
+        ]
+
+        def e2e():
+            o = Q.q_nvfp4(x, blk, rnd, seed, 0, True, True, out=out)
+            o.amax = amax
+            return o
+        calls.append(Call(f"{tag} nvfp4_{blk}_{rnd} row+colT", "nvfp4", pieces, [x],
+                          [out.q_row, out.sb_row, out.q_colT, out.sb_colT, out.s_global], e2e))
+        y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+        r = lambda: Q.dq_nvfp4(out.q_row, out.sb_row, out.s_global, blk, torch.bfloat16, out=y)
+        calls.append(Call(f"{tag} dq_nvfp4_{blk} row->bf16", "dequant",
+                          [("dq_nvfp4", "k_dequant.cu", nbytes(out.q_row, out.sb_row, y), r)],
+                          [out.q_row, out.sb_row, out.s_global], [y], r))
+
+    if "cs1" in d:
+        cs("cs1.x", d["cs1"]["x"], "e4m3", True)
+    if "mx2" in d:
+        mx("mx2.act", d["mx2"]["act"])
+    if "bw3" in d:
+        bw("bw3.act", d["bw3"]["act"], "1x128", True)
+        bw("bw3.w", d["bw3"]["w"], "128x128", True)
+    if "hy4" in d:
+        cs("hy4.grad", d["hy4"]["grad"], "e5m2", True)
+        cs("hy4.w", d["hy4"]["w"], "e4m3", True)
+    if "nv5" in d:
+        nv("nv5.act", d["nv5"]["act"], "1x16", "rn", 0)
+        nv("nv5.grad", d["nv5"]["grad"], "1x16", "sr", 4)
+        nv("nv5.w", d["nv5"]["w"], "16x16", "rn", 0)
+    return calls
+
+
+# --------------------------------------------------------------------------
+# sampled 0-ULP parity of the full-size outputs against the oracle
+# --------------------------------------------------------------------------
+
+def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
+    """For one aligned band of `rows` rows per tensor, recompute every
+    rowwise output and every columnwise output that the band determines with
+    the oracle (per-tensor amax taken from the oracle over the whole tensor)
+    and compare bit for bit with the library's full-size outputs."""
+    def host(t):
+        return t.view(torch.int16).cpu().numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.cpu().numpy()
+
+    checked = []
+
+    def band(M):
+        rng = np.random.default_rng(seed + M)
+        return int(rng.integers(0, M // rows)) * rows
+
+    def eq(a, b, what):
+        a, b = np.ascontiguousarray(a), np.ascontiguousarray(b)
+        if a.dtype == np.float32:
+            a, b = a.view(np.uint32), b.view(np.uint32)
+        if a.shape != b.shape or not np.array_equal(a, b):
+            raise AssertionError(f"sampled parity failed: {what}")
+        checked.append(what)
+
+    for wl, tn, kind in [("cs1", "x", "cs_e4m3"), ("hy4", "grad", "cs_e5m2"), ("hy4", "w", "cs_e4m3"),
+                         ("mx2", "act", "mx"), ("bw3", "act", "bw1"), ("bw3", "w", "bw128"),
+                         ("nv5", "act", "nv_rn"), ("nv5", "grad", "nv_sr"), ("nv5", "w", "nv16")]:
+        xh, xd = host_tensors[wl][tn], dev_tensors[wl][tn]
+        M, K = xh.shape
+        r0 = band(M)
+        xs = np.ascontiguousarray(xh[r0:r0 + rows])
+        if kind.startswith("cs"):
+            fmt = O.E5M2 if kind == "cs_e5m2" else O.E4M3
+            A = O.amax(xh)
+            g = Q.q_current_scaling(xd, "e5m2" if fmt == O.E5M2 else "e4m3", True, True)
+            w = O.current_scaling(xs, fmt, True, True, amax_in=A)
+            eq(np.float32(g.amax.item()), np.float32(A), f"{wl}.{tn} amax")
+            eq(np.float32(g.scale.item()), w.scale, f"{wl}.{tn} scale")
+            eq(host(g.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} q_row band")
+            eq(host(g.q_colT[:, r0:r0 + rows]), w.q_colT, f"{wl}.{tn} q_colT band")
+            y = Q.dq_current_scaling(g.q_row[r0:r0 + rows].contiguous(), g.scale, "e4m3" if fmt == O.E4M3 else "e5m2",
+                                     torch.bfloat16)
+            eq(host(y), O.dq_current_scaling(w.q_row, w.scale, fmt, O.BF16), f"{wl}.{tn} dq band")
+        elif kind == "mx":
+            g = Q.q_mxfp8(xd)
+            w = O.mxfp8(xs)
+            eq(host(g.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} q_row band")
+            eq(host(g.e8m0_row[r0:r0 + rows]), w.e8m0_row, f"{wl}.{tn} e8m0_row band")
+            eq(host(g.q_col[r0:r0 + rows]), w.q_col, f"{wl}.{tn} q_col band")
+            eq(host(g.e8m0_col[r0 // 32:(r0 + rows) // 32]), w.e8m0_col, f"{wl}.{tn} e8m0_col band")
+        elif kind == "bw1":
+            g = Q.q_blockwise(xd, "1x128", True, True)
+            w = O.blockwise(xs, O.T1x128, True, True)
+            eq(host(g.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} q_row band")
+            eq(host(g.s_row[r0:r0 + rows]), w.s_row, f"{wl}.{tn} s_row band")
+            eq(host(g.q_colT[:, r0:r0 + rows]), w.q_colT, f"{wl}.{tn} q_colT band")
+            eq(host(g.s_colT[:, r0 // 128:(r0 + rows) // 128]), w.s_colT, f"{wl}.{tn} s_colT band")
+        elif kind == "bw128":
+            g = Q.q_blockwise(xd, "128x128", True, True)
+            w = O.blockwise(xs, O.T128x128, True, True)
+            eq(host(g.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} q_row band")
+            eq(host(g.s_row[r0 // 128:(r0 + rows) // 128]), w.s_row, f"{wl}.{tn} s band")
+            eq(host(g.q_colT[:, r0:r0 + rows]), w.q_colT, f"{wl}.{tn} q_colT band")
+        else:
+            blk = O.B16x16 if kind == "nv16" else O.B1x16
+            rnd = O.SR if kind == "nv_sr" else O.RN
+            seed = 4 if rnd == O.SR else 0
+            A = O.amax(xh)
+            g = Q.q_nvfp4(xd, "16x16" if blk == O.B16x16 else "1x16", "sr" if rnd == O.SR else "rn", seed, 0, True, True)
+            # the rowwise stream of the band starts at element r0*K: a counter offset of r0*K/8
+            w = O.nvfp4(xs, blk, rnd, seed=seed, offset=r0 * K // 8, rowwise=True, colwise=(rnd == O.RN), amax_in=A)
+            eq(np.float32(g.s_global.item()), w.s_global, f"{wl}.{tn} s_global")
+            eq(host(g.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} q_row band")
+            if blk == O.B1x16:
+                eq(host(g.sb_row[r0:r0 + rows]), w.sb_row, f"{wl}.{tn} sb_row band")
+            else:
+                eq(host(g.sb_row[r0 // 16:(r0 + rows) // 16]), w.sb_row, f"{wl}.{tn} sb band")
+            if rnd == O.RN:
+                eq(host(g.q_colT[:, r0 // 2:(r0 + rows) // 2]), w.q_colT, f"{wl}.{tn} q_colT band")
+            else:
+                # SR columnwise draws depend on the full-height index k*M + m: check the
+                # deterministic block scales of the band instead
+                w2 = O.nvfp4(xs, blk, O.RN, colwise=True, rowwise=False, amax_in=A)
+                eq(host(g.sb_colT[:, r0 // 16:(r0 + rows) // 16]), w2.sb_colT, f"{wl}.{tn} sb_colT band")
+    torch.cuda.synchronize()
+    return checked
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# ours
+# --------------------------------------------------------------------------
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_quantization_current_gb300 as Q
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    Q.lib()
+
+    # ---- inputs: host (numpy, for the oracle checks and the end-to-end copies) and device
+    host_t, dev_t, pinned = {}, {}, {}
+    wanted = [wl for wl in WL.WORKLOADS if not args.only or args.only.split(".")[0] in wl]
+    for wl in wanted:
+        host_t[wl] = WL.workload(wl, args.scale_rows)
+        dev_t[wl], pinned[wl] = {}, {}
+        for tn, a in host_t[wl].items():
+            t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)
+            pinned[wl][tn] = t.pin_memory()
+            dev_t[wl][tn] = t.to(dev)
+    torch.cuda.synchronize()
+
+    parity = "not run"
+    if not args.skip_parity and not args.only:
+        import oracle as O
+        checked = sampled_parity(host_t, dev_t, torch, Q, O)
+        parity = f"0-ULP on {len(checked)} sampled output bands"
+
+    calls = [c for c in build_step(dev_t, torch, Q) if args.only in c.name]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_step(evs):
+        for ci, c in enumerate(calls):
+            flush.fill_(float(ci))
+            evs[ci][0].record(stream)
+            for pi, p in enumerate(c.pieces):
+                p[3]()
+                evs[ci][pi + 1].record(stream)
+
+    def new_events():
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(len(c.pieces) + 1)] for c in calls]
+
+    for _ in range(args.warmup):
+        one_step(new_events())
+    torch.cuda.synchronize()
+
+    all_evs = [new_events() for _ in range(args.steps)]
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        one_step(all_evs[s])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    # per-kernel and per-call device times
+    kern_ms = {}      # (call index, piece index) -> list of ms
+    for s in range(args.steps):
+        for ci, c in enumerate(calls):
+            ev = all_evs[s][ci]
+            for pi in range(len(c.pieces)):
+                kern_ms.setdefault((ci, pi), []).append(ev[pi].elapsed_time(ev[pi + 1]))
+    step_ms = sum(statistics.mean(v) for v in kern_ms.values())
+    step_bytes = sum(c.alg_bytes for c in calls)
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = step_bytes * world / (step_ms * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    per_call = []
+    per_recipe = {}
+    per_kernel = {}
+    for ci, c in enumerate(calls):
+        ms = sum(statistics.mean(kern_ms[(ci, pi)]) for pi in range(len(c.pieces)))
+        gbs = c.alg_bytes / (ms * 1e-3) / 1e9
+        per_call.append({"call": c.name, "us": round(ms * 1e3, 2), "bytes": c.alg_bytes, "GB/s": round(gbs, 1),
+                         "frac": round(gbs / peak, 3)})
+        r = per_recipe.setdefault(c.recipe, {"bytes": 0, "us": 0.0})
+        r["bytes"] += c.alg_bytes
+        r["us"] += ms * 1e3
+        for pi, p in enumerate(c.pieces):
+            k = per_kernel.setdefault(p[0], {"src": p[1], "bytes": 0, "us": 0.0, "launches": 0})
+            k["bytes"] += p[2]
+            k["us"] += statistics.mean(kern_ms[(ci, pi)]) * 1e3
+            k["launches"] += 1
+    for r in per_recipe.values():
+        r["GB/s"] = round(r["bytes"] / (r["us"] * 1e-6) / 1e9, 1)
+        r["frac"] = round(r["GB/s"] / peak, 3)
+        r["us"] = round(r["us"], 2)
+    # dominant kernel: the largest share of step time
+    dom_name, dom = max(per_kernel.items(), key=lambda kv: kv[1]["us"])
+    dom_bytes = dom["bytes"] / dom["launches"]
+    dom_us = dom["us"] / dom["launches"]
+    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+    tr = TRAFFIC.get(dom_name)
+    traffic = None
+    if tr is not None and tr.get("src_hash") == src_hash(dom["src"]):
+        traffic = tr["bytes_per_launch"]
+    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 3), "traffic": traffic,
+                "alg_bytes_per_launch": int(dom_bytes), "us_per_launch": round(dom_us, 2),
+                "share_of_step": round(dom["us"] / (step_ms * 1e3), 3), "peak_kind": peak_kind + " hbm_gbs"}
+    n_launches = args.steps * sum(len(c.pieces) for c in calls)
+
+    # ---- end to end: pinned host input -> device, the public call, outputs -> pinned host
+    e2e = None
+    if not args.skip_e2e:
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        dev_to_pin = {}
+        for wl in host_t:
+            for tn in host_t[wl]:
+                dev_to_pin[id(dev_t[wl][tn])] = pinned[wl][tn]
+        out_host = {}
+        for c in calls:
+            for t in c.d2h:
+                if t is not None and id(t) not in out_host:
+                    out_host[id(t)] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        in_host = {}
+        for c in calls:
+            for t in c.h2d:
+                if t is not None and id(t) not in in_host:
+                    in_host[id(t)] = dev_to_pin.get(id(t))
+                    if in_host[id(t)] is None:
+                        in_host[id(t)] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        h2d_b = sum(nbytes(t) for c in calls for t in c.h2d if t is not None)
+        d2h_b = sum(nbytes(t) for c in calls for t in c.d2h if t is not None)
+        e_ms = []
+        for s in range(e2e_steps + 1):
+            tot = 0.0
+            for c in calls:
+                flush.fill_(1.0)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for t in c.h2d:
+                    t.copy_(in_host[id(t)], non_blocking=True)
+                c.e2e_thunk()
+                for t in c.d2h:
+                    if t is not None:
+                        out_host[id(t)].copy_(t, non_blocking=True)
+                b.record(stream)
+                b.synchronize()
+                tot += a.elapsed_time(b)
+            if s > 0:          # the first pass warms the copy engines
+                e_ms.append(tot)
+        ems = statistics.mean(e_ms)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": round(step_bytes * world / (ems * 1e-3) / 1e9, 1), "unit": UNIT,
+               "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b, "ms_per_step": round(ems, 3),
+               "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu and not args.only:
+        cpu = cpu_baseline(host_t)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy; see workloads.WORKLOADS)",
+            "config": {"workload": "all five workloads at full size per step: cs1 FP32 1024x1024 CS-E4M3+T; "
+                                   "mx2 BF16 8192x4096 MXFP8 row+col; bw3 BF16 16384x7168 1x128+T and 7168x18432 "
+                                   "128x128+T; hy4 BF16 8192x14336 CS-E5M2+T and 14336x4096 CS-E4M3+T; nv5 BF16 "
+                                   "8192x4096 NVFP4 1x16 RN+T, 1x16 SR+T, 4096x4096 16x16 RN+T; each with a dequant",
+                       "l2": "flushed (256 MiB write) before every timed call",
+                       "scale_rows": args.scale_rows, "parallelism": f"replicas x{world} (independent tensors)"},
+            "parity": parity,
+            "roofline": roofline,
+            "per_recipe": per_recipe,
+            "per_kernel": {k: {"launches_per_step": v["launches"], "us_per_launch": round(v["us"] / v["launches"], 2),
+                               "GB/s": round(v["bytes"] / (v["us"] * 1e-6) / 1e9, 1),
+                               "frac": round(v["bytes"] / (v["us"] * 1e-6) / 1e9 / peak, 3),
+                               "share_of_step": round(v["us"] / (step_ms * 1e3), 3)}
+                           for k, v in sorted(per_kernel.items(), key=lambda kv: -kv[1]["us"])},
+            "per_call": per_call,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": n_launches,
+            "clocks": clocks,
+            "wall_s_timed": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle on a bounded row sample
+# --------------------------------------------------------------------------
+
+def oracle_sample_work(host_t, frac):
+    """(thunk, algorithmic bytes) pairs over the first `frac` of the rows of
+    every tensor (rows rounded to a multiple of 128), same recipes as a step."""
+    import oracle as O
+    work = []
+
+    def rows(a):
+        return max(128, int(a.shape[0] * frac) // 128 * 128)
+
+    def isz(a):
+        return a.dtype.itemsize
+
+    def cs(a, fmt):
+        s = np.ascontiguousarray(a[:rows(a)])
+        M, K = s.shape
+        work.append((lambda: O.current_scaling(s, fmt, True, True), 2 * s.nbytes + 2 * M * K + 4))
+        r = O.current_scaling(s, fmt, True, False)
+        work.append((lambda: O.dq_current_scaling(r.q_row, r.scale, fmt, O.BF16 if a.dtype == np.uint16 else O.F32),
+                     M * K + M * K * isz(a) + 4))
+
+    def mx(a):
+        s = np.ascontiguousarray(a[:rows(a)])
+        M, K = s.shape
+        work.append((lambda: O.mxfp8(s), s.nbytes + 2 * M * K + M * K // 16))
+        r = O.mxfp8(s)
+        work.append((lambda: O.dq_mxfp8(r.q_row, r.e8m0_row, O.E4M3, O.ROW, O.BF16), M * K * 3 + M * K // 32))
+        work.append((lambda: O.dq_mxfp8(r.q_col, r.e8m0_col, O.E4M3, O.COL, O.BF16), M * K * 3 + M * K // 32))
+
+    def bw(a, tile):
+        s = np.ascontiguousarray(a[:rows(a)])
+        M, K = s.shape
+        sc = (M * K // 128) * 4 if tile == O.T1x128 else (M * K // 16384) * 4
+        work.append((lambda: O.blockwise(s, tile, True, True), s.nbytes + 2 * M * K + 2 * sc))
+        r = O.blockwise(s, tile, True, False)
+        work.append((lambda: O.dq_blockwise(r.q_row, r.s_row, tile, O.BF16), M * K * 3 + sc))
+
+    def nv(a, blk, rnd, seed):
+        s = np.ascontiguousarray(a[:rows(a)])
+        M, K = s.shape
+        sb = M * K // 16 if blk == O.B1x16 else M * K // 256
+        work.append((lambda: O.nvfp4(s, blk, rnd, seed=seed, rowwise=True, colwise=True), 2 * s.nbytes + M * K + 2 * sb + 4))
+        r = O.nvfp4(s, blk, rnd, seed=seed)
+        work.append((lambda: O.dq_nvfp4(r.q_row, r.sb_row, r.s_global, blk, O.BF16), M * K // 2 + sb + 2 * M * K + 4))
+
+    cs(host_t["cs1"]["x"], O.E4M3)
+    mx(host_t["mx2"]["act"])
+    bw(host_t["bw3"]["act"], O.T1x128)
+    bw(host_t["bw3"]["w"], O.T128x128)
+    cs(host_t["hy4"]["grad"], O.E5M2)
+    cs(host_t["hy4"]["w"], O.E4M3)
+    nv(host_t["nv5"]["act"], O.B1x16, O.RN, 0)
+    nv(host_t["nv5"]["grad"], O.B1x16, O.SR, 4)
+    nv(host_t["nv5"]["w"], O.B16x16, O.RN, 0)
+    return work
+
+
+def cpu_baseline(host_t, frac=CPU_SAMPLE_FRAC):
+    work = oracle_sample_work(host_t, frac)
+    t0 = time.perf_counter()
+    total = 0
+    for fn, b in work:
+        fn()
+        total += b
+    dt = time.perf_counter() - t0
+    return {"value": round(total / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {frac:.3f} of the rows (multiple of 128) of every tensor of the step, all recipes "
+                      f"and dequants, single-threaded C oracle; {total / 1e9:.3f} GB in {dt:.1f} s",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    host_t = {wl: WL.workload(wl, args.scale_rows) for wl in WL.WORKLOADS}
+    import oracle as O
+    O.build()
+    # each step is a bounded row sample, sized so that warm-up + steps take
+    # about REF_BUDGET_S seconds (never less than 128 rows of every tensor)
+    small = oracle_sample_work(host_t, 0.0)
+    t0 = time.perf_counter()
+    for fn, _b in small:
+        fn()
+    t_small = time.perf_counter() - t0
+    budget = REF_BUDGET_S / max(1, args.steps + args.warmup)
+    frac = min(CPU_SAMPLE_FRAC, max(0.0, budget / max(t_small, 1e-6)) * min(
+        128 / a.shape[0] for d in host_t.values() for a in d.values()))
+    work = oracle_sample_work(host_t, frac)
+    for _ in range(args.warmup):
+        for fn, _b in work:
+            fn()
+    times, total = [], sum(b for _, b in work)
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for fn, _b in work:
+            fn()
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = total / (ms * 1e-3) / 1e9
+    sample = (f"first {frac:.4f} of the rows (multiple of 128) of every tensor of the step, all recipes and "
+              f"dequants, single-threaded C oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy)",
+        "config": {"workload": "same five workloads as the library arm, bounded row sample per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--skip-parity", action="store_true", help="skip the sampled oracle check before timing")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--scale-rows", type=float, default=1.0, help="shrink every tensor's rows (debug only)")
+    ap.add_argument("--only", default="", help="time only the calls whose name contains this text (profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -104,16 +104,17 @@ q_status q_current_scaling(const void *x, q_dtype in, int64_t M, int64_t K, q_fp
     TRY(check_in(fn, x, in, M * K));
     if (fmt != Q_E4M3 && fmt != Q_E5M2) return fail(Q_ERR_ARG, "%s: fmt %d is not Q_E4M3 or Q_E5M2", fn, (int)fmt);
     if (amax_mode != Q_AMAX_COMPUTE && amax_mode != Q_AMAX_GIVEN) return fail(Q_ERR_ARG, "%s: bad amax_mode %d", fn, (int)amax_mode);
-    if (q_row == nullptr && q_colT == nullptr) return fail(Q_ERR_ARG, "%s: neither q_row nor q_colT requested", fn);
-    if (q_row != nullptr) TRY(need(fn, "q_row", q_row, 16));
-    if (q_colT != nullptr) {
+    const int64_t n = M * K;
+    // an empty tensor has no codes to write (its buffers may be NULL)
+    if (n > 0 && q_row == nullptr && q_colT == nullptr) return fail(Q_ERR_ARG, "%s: neither q_row nor q_colT requested", fn);
+    if (n > 0 && q_row != nullptr) TRY(need(fn, "q_row", q_row, 16));
+    if (n > 0 && q_colT != nullptr) {
         TRY(need(fn, "q_colT", q_colT, 16));
         TRY(multiple(fn, "M (with q_colT)", M, 16));
         TRY(multiple(fn, "K (with q_colT)", K, 16));
     }
     TRY(need(fn, "amax", amax, 4));
     TRY(need(fn, "scale", scale, 4));
-    const int64_t n = M * K;
     if (amax_mode == Q_AMAX_COMPUTE) LAUNCH("q_current_scaling/amax", qk::launch_amax(x, (int)in, n, amax, status, S(stream)));
     // an empty tensor takes the flat path, which only writes the scale
     LAUNCH("q_current_scaling/cast",
@@ -129,8 +130,9 @@ q_status q_mxfp8(const void *x, q_dtype in, int64_t M, int64_t K, q_fp8 fmt, uin
     TRY(check_dims(fn, M, K));
     TRY(check_in(fn, x, in, M * K));
     if (fmt != Q_E4M3 && fmt != Q_E5M2) return fail(Q_ERR_ARG, "%s: fmt %d is not Q_E4M3 or Q_E5M2", fn, (int)fmt);
-    if (q_row == nullptr && q_col == nullptr) return fail(Q_ERR_ARG, "%s: neither direction requested", fn);
     TRY(multiple(fn, "K", K, 32));
+    if (M * K == 0) return Q_OK;
+    if (q_row == nullptr && q_col == nullptr) return fail(Q_ERR_ARG, "%s: neither direction requested", fn);
     if (q_row != nullptr) {
         TRY(need(fn, "q_row", q_row, 16));
         TRY(need(fn, "e8m0_row", e8m0_row, 1));
@@ -140,7 +142,6 @@ q_status q_mxfp8(const void *x, q_dtype in, int64_t M, int64_t K, q_fp8 fmt, uin
         TRY(need(fn, "e8m0_col", e8m0_col, 16));
         TRY(multiple(fn, "M (with q_col)", M, 32));
     }
-    if (M * K == 0) return Q_OK;
     LAUNCH(fn, qk::launch_mxfp8(x, (int)in, M, K, (int)fmt, q_row, e8m0_row, q_col, e8m0_col, status, S(stream)));
     return Q_OK;
 }
@@ -152,9 +153,10 @@ q_status q_blockwise(const void *x, q_dtype in, int64_t M, int64_t K, q_tile til
     TRY(check_dims(fn, M, K));
     TRY(check_in(fn, x, in, M * K));
     if (tile != Q_T1x128 && tile != Q_T128x128) return fail(Q_ERR_ARG, "%s: tile %d is not Q_T1x128 or Q_T128x128", fn, (int)tile);
-    if (q_row == nullptr && q_colT == nullptr) return fail(Q_ERR_ARG, "%s: neither direction requested", fn);
     TRY(multiple(fn, "K", K, 128));
     if (tile == Q_T128x128) TRY(multiple(fn, "M (128x128 tiles)", M, 128));
+    if (M * K == 0) return Q_OK;
+    if (q_row == nullptr && q_colT == nullptr) return fail(Q_ERR_ARG, "%s: neither direction requested", fn);
     if (q_row != nullptr) {
         TRY(need(fn, "q_row", q_row, 16));
         TRY(need(fn, "s_row", s_row, 4));
@@ -164,7 +166,6 @@ q_status q_blockwise(const void *x, q_dtype in, int64_t M, int64_t K, q_tile til
         TRY(need(fn, "s_colT", s_colT, 4));
         TRY(multiple(fn, "M (with q_colT)", M, 128));
     }
-    if (M * K == 0) return Q_OK;
     LAUNCH(fn, qk::launch_blockwise(x, (int)in, M, K, (int)tile, q_row, s_row, q_colT, s_colT, status, S(stream)));
     return Q_OK;
 }
@@ -179,14 +180,15 @@ q_status q_nvfp4(const void *x, q_dtype in, int64_t M, int64_t K, q_nvblk blk, q
     if (blk != Q_B1x16 && blk != Q_B16x16) return fail(Q_ERR_ARG, "%s: blk %d is not Q_B1x16 or Q_B16x16", fn, (int)blk);
     if (rnd != Q_RN && rnd != Q_SR) return fail(Q_ERR_ARG, "%s: rnd %d is not Q_RN or Q_SR", fn, (int)rnd);
     if (amax_mode != Q_AMAX_COMPUTE && amax_mode != Q_AMAX_GIVEN) return fail(Q_ERR_ARG, "%s: bad amax_mode %d", fn, (int)amax_mode);
-    if (q_row == nullptr && q_colT == nullptr) return fail(Q_ERR_ARG, "%s: neither direction requested", fn);
     TRY(multiple(fn, "K", K, 16));
     TRY(multiple(fn, "M", M, 16));
-    if (q_row != nullptr) {
+    const bool empty = M * K == 0;   // no codes to write; buffers may be NULL
+    if (!empty && q_row == nullptr && q_colT == nullptr) return fail(Q_ERR_ARG, "%s: neither direction requested", fn);
+    if (!empty && q_row != nullptr) {
         TRY(need(fn, "q_row", q_row, 16));
         TRY(need(fn, "sb_row", sb_row, 1));
     }
-    if (q_colT != nullptr) {
+    if (!empty && q_colT != nullptr) {
         TRY(need(fn, "q_colT", q_colT, 16));
         TRY(need(fn, "sb_colT", sb_colT, 16));
     }
