@@ -36,8 +36,8 @@
  * failure.  Conditions found on the device (non-finite input) are ORed into
  * the optional device word *status (may be NULL); the caller zeroes it.
  *
- * Empty tensors (M == 0 or K == 0) are valid: amax is 0, scales are 1 and no
- * code is written.
+ * Empty tensors (M == 0 or K == 0) are valid: amax is 0, scales are 1, no
+ * code is written and the code / block-scale buffers may be NULL.
  */
 #ifndef Q_H_
 #define Q_H_
@@ -75,6 +75,7 @@ typedef enum { Q_AMAX_COMPUTE = 0, Q_AMAX_GIVEN = 1 } q_amax_mode;
 
 /* Bits ORed into *status by the kernels. */
 #define Q_ST_NONFINITE 1   /* an amax (tensor or block) was inf or NaN */
+#define Q_ST_TIMEOUT 2     /* a kernel gave up waiting for its input tiles (outputs incomplete) */
 
 /* Thread-local message describing this thread's last failed call ("" if none). */
 const char *q_last_error(void);

@@ -8,171 +8,190 @@
 // Per tile: b = max|x|, alpha = 448 / b (b = 0 -> 1, overflow -> FLT_MAX),
 // s = 1 / alpha, q = RTNE-saturate(alpha * x).
 //
-// A CTA owns 128 rows x (32*VEC) columns, i.e. exactly one 128-row block in
-// M and 2 (BF16) or 1 (FP32) 128-column blocks in K.  Column maxima over the
-// 128 rows are combined across the 8 warps in shared memory; the columnwise
-// codes (own per-column scales) are produced directly in column order and
-// staged in shared memory for full 128-byte transposed row writes.
-#include "q_common.cuh"
+// On the tile engine: a 128 x TC tile holds exactly one 128-row block in M
+// and TC/128 blocks in K.
+//  row pass - thread (warp w, lane l): rows 8w..8w+7, 16 bytes each; a
+//             1x128 block spans 128/VEC lanes (xor-shuffle max);
+//  col pass - thread (word column t % 128, 32-row quarter t / 128) reads 32
+//             words; 1x128 (128x1 blocks along M): quarter maxima meet in
+//             shared memory; the codes of each column are produced in
+//             column order and parked in the stage (now free) as
+//             [column][128 rows] with swizzled 16-byte chunks;
+//  copy-out - 8 threads per q_colT row write its 128 bytes.
+// For 128x128 the tile maxima come from the row-pass registers (warp
+// shuffles, then shared memory across the 16 warps).
+#include "q_engine.cuh"
 #include "q_internal.h"
 
 namespace qk {
 
-template <int DT, int TILE>
-__global__ void __launch_bounds__(kThreads) k_blockwise(const void *__restrict__ x, int64_t M, int64_t K,
-                                                        uint8_t *__restrict__ q_row, float *__restrict__ s_row,
-                                                        uint8_t *__restrict__ q_colT, float *__restrict__ s_colT,
-                                                        int32_t *status)
+// alpha = 448 / b and s = 1 / alpha for a tile maximum b.  For BF16 inputs b
+// has a 7-bit mantissa m, b = (1 + m/128) 2^e; while alpha and s stay normal,
+// RN(448 / b) = RN(448 / (1 + m/128)) 2^-e and RN(1 / alpha) =
+// RN(1 / RN(448 / (1 + m/128))) 2^e exactly (rounding commutes with scaling
+// by a power of two), so both come from two 128-entry tables per CTA and an
+// exponent shift.  Exponent fields below 10 (b < 2^-117, where s would be
+// subnormal), inf / NaN and FP32 inputs take the divisions.
+struct BwScaleTab {
+    float a[128], s[128];
+};
+
+template <int DT> QD void bw_scales(uint32_t b, const BwScaleTab &tab, float &alpha, float &s)
 {
-    constexpr int VEC = In<DT>::VEC, BYTES = In<DT>::BYTES, TC = 32 * VEC, CW = VEC / 4, LPB = 128 / VEC;
-    constexpr int NT = TC / 128;   // 128-column blocks per CTA
-    __shared__ __align__(16) uint8_t sT[TC * kTileRows];
-    __shared__ uint32_t red[kWarps][TC];
-    __shared__ float calpha[TC];
+    const uint32_t E = b >> 23;
+    if (DT == BF16 && E >= 10u && E < 255u) {
+        const uint32_t m = (b >> 16) & 0x7Fu;
+        const int sh = ((int)E - 127) << 23;
+        alpha = __uint_as_float((uint32_t)((int)__float_as_uint(tab.a[m]) - sh));
+        s = __uint_as_float((uint32_t)((int)__float_as_uint(tab.s[m]) + sh));
+    } else {
+        alpha = alpha_from_amax(448.0f, __uint_as_float(b));
+        s = __fdiv_rn(1.0f, alpha);
+    }
+}
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tiles_k = (K + TC - 1) / TC;
-    const int64_t tm = blockIdx.x / tiles_k, tk = blockIdx.x - tm * tiles_k;
-    const int64_t m0 = tm * kTileRows + warp * kRowsPerWarp;
-    const int64_t k0 = tk * TC + lane * VEC;
-    const bool colok = k0 < K;
+template <int DT, int TILE>
+__global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
+                                                              uint8_t *__restrict__ q_row, float *__restrict__ s_row,
+                                                              uint8_t *__restrict__ q_colT, float *__restrict__ s_colT,
+                                                              int32_t *status)
+{
+    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, LPB = 128 / VEC, CPW = 4 / In<DT>::BYTES;
+    constexpr int NT = TC / 128;   // 128-column blocks per tile
+    __shared__ uint32_t red[4][TC];
+    __shared__ uint32_t tred[kEngWarps][NT];
+    __shared__ BwScaleTab tab;
+    if (DT == BF16 && threadIdx.x < 128) {
+        const float a = __fdiv_rn(448.0f, 1.0f + (float)threadIdx.x * (1.0f / 128.0f));
+        tab.a[threadIdx.x] = a;
+        tab.s[threadIdx.x] = __fdiv_rn(1.0f, a);
+    }   // visible after the engine's first barrier
 
-    uint4 v[kRowsPerWarp];
-    const char *base = static_cast<const char *>(x) + (m0 * K + k0) * BYTES;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31, wc = t & 127, quarter = t >> 7;
+    const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
+
+    run_tiles(&tmap, tiles_m, tiles_k, TC, false, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
+        const int64_t mb = tm * kTileRowsE, kb = tk * TC;
+        const int64_t k = kb + lane * VEC;
+        float colalpha[CPW];
+        uint32_t w[32];
+
+        if constexpr (TILE == 0) {
+            // ---------------- 1x128 rowwise ----------------
+            if (q_row != nullptr) {
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; r++)
-        v[r] = (colok && m0 + r < M) ? ldg_stream(base + (int64_t)r * K * BYTES) : make_uint4(0, 0, 0, 0);
-
-    if (TILE == 0) {
-        // ---------------- 1x128 rowwise ----------------
-        if (q_row != nullptr) {
-#pragma unroll
-            for (int r = 0; r < kRowsPerWarp; r++) {
-                const uint32_t b = group_max<LPB>(absmax_bits<DT>(v[r]));
-                const float alpha = alpha_from_amax(448.0f, __uint_as_float(b));
-                if (colok && m0 + r < M) {
+                for (int j = 0; j < 8; j++) {
+                    const int r = 8 * warp + j;
+                    const uint4 v = lds16(st + r * kRowBytes + lane * 16);
+                    const uint32_t b = group_max<LPB>(absmax_bits<DT>(v));
+                    float alpha, sc;
+                    bw_scales<DT>(b, tab, alpha, sc);
                     uint32_t o[CW];
-#pragma unroll
-                    for (int w = 0; w < CW; w++)
-                        o[w] = cvt_fp8x4<E4M3>(__fmul_rn(alpha, elem<DT>(v[r], 4 * w)), __fmul_rn(alpha, elem<DT>(v[r], 4 * w + 1)),
-                                               __fmul_rn(alpha, elem<DT>(v[r], 4 * w + 2)), __fmul_rn(alpha, elem<DT>(v[r], 4 * w + 3)));
-                    uint8_t *dst = q_row + (m0 + r) * K + k0;
-                    if (CW == 2) stg8(dst, o[0], o[CW - 1]);
-                    else stg4(dst, o[0]);
-                    if (lane % LPB == 0) {
-                        s_row[(m0 + r) * (K / 128) + k0 / 128] = __fdiv_rn(1.0f, alpha);
-                        flag_nonfinite(status, b);
+                    chunk_fp8<DT, E4M3>(v, alpha, o);
+                    if (mb + r < M && k < K) {
+                        uint8_t *dst = q_row + (mb + r) * K + k;
+                        if (CW == 2) stg8(dst, o[0], o[CW - 1]);
+                        else stg4(dst, o[0]);
+                        if (lane % LPB == 0) {
+                            s_row[(mb + r) * (K / 128) + k / 128] = sc;
+                            flag_nonfinite(status, b);
+                        }
                     }
                 }
             }
-        }
-        if (q_colT == nullptr) return;
-        // ---------------- 128x1 columnwise, transposed ----------------
-        {
-            uint4 acc = make_uint4(0, 0, 0, 0);
+            if (q_colT == nullptr) return;
+            // ---------------- 128x1 columnwise ----------------
 #pragma unroll
-            for (int r = 0; r < kRowsPerWarp; r++) {
-                acc.x = colmax_word<DT>(acc.x, v[r].x);
-                acc.y = colmax_word<DT>(acc.y, v[r].y);
-                acc.z = colmax_word<DT>(acc.z, v[r].z);
-                acc.w = colmax_word<DT>(acc.w, v[r].w);
+            for (int r = 0; r < 32; r++) w[r] = lds4(st + (32 * quarter + r) * kRowBytes + wc * 4);
+            {
+                uint32_t bm[CPW];
+                column_absmax<DT, 32>(w, bm);
+#pragma unroll
+                for (int c = 0; c < CPW; c++) red[quarter][wc * CPW + c] = bm[c];
             }
+            __syncthreads();   // partial maxima visible; every read of the stage is done
 #pragma unroll
-            for (int j = 0; j < VEC; j++) red[warp][lane * VEC + j] = colmax_bits<DT>(acc, j);
-        }
-        __syncthreads();
-        for (int col = threadIdx.x; col < TC; col += kThreads) {
+            for (int c = 0; c < CPW; c++) {
+                const int col = wc * CPW + c;
+                const uint32_t b = max(max(red[0][col], red[1][col]), max(red[2][col], red[3][col]));
+                float sc;
+                bw_scales<DT>(b, tab, colalpha[c], sc);
+                if (quarter == 0 && kb + col < K) {
+                    s_colT[(kb + col) * (M / 128) + tm] = sc;
+                    flag_nonfinite(status, b);
+                }
+            }
+        } else {
+            // ---------------- 128x128: one scale per tile ----------------
+            uint4 v[8];
             uint32_t b = 0;
 #pragma unroll
-            for (int w = 0; w < kWarps; w++) b = max(b, red[w][col]);
-            const float alpha = alpha_from_amax(448.0f, __uint_as_float(b));
-            calpha[col] = alpha;
-            const int64_t kg = tk * TC + col;
-            if (kg < K) {
-                s_colT[kg * (M / 128) + tm] = __fdiv_rn(1.0f, alpha);
-                flag_nonfinite(status, b);
+            for (int j = 0; j < 8; j++) {
+                v[j] = lds16(st + (8 * warp + j) * kRowBytes + lane * 16);
+                b = max(b, absmax_bits<DT>(v[j]));
             }
-        }
-        __syncthreads();
-        if (colok) {
-#pragma unroll
-            for (int j = 0; j < VEC; j++) {
-                const int col = lane * VEC + j;
-                const float alpha = calpha[col];
-                uint32_t c[4];
-#pragma unroll
-                for (int g = 0; g < 4; g++)
-                    c[g] = cvt_fp8x4<E4M3>(__fmul_rn(alpha, elem<DT>(v[4 * g], j)), __fmul_rn(alpha, elem<DT>(v[4 * g + 1], j)),
-                                           __fmul_rn(alpha, elem<DT>(v[4 * g + 2], j)), __fmul_rn(alpha, elem<DT>(v[4 * g + 3], j)));
-                *reinterpret_cast<uint4 *>(sT + col * kTileRows + (warp ^ (lane & 7)) * 16) = make_uint4(c[0], c[1], c[2], c[3]);
-            }
-        }
-    } else {
-        // ---------------- 128x128: one scale per tile ----------------
-        uint32_t b = 0;
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; r++) b = max(b, absmax_bits<DT>(v[r]));
-        b = group_max<LPB>(b);
-        __shared__ uint32_t tred[kWarps][NT];
-        if (lane % LPB == 0) tred[warp][lane / LPB] = b;
-        __syncthreads();
-        b = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; w++) b = max(b, tred[w][lane / LPB]);
-        const float alpha = alpha_from_amax(448.0f, __uint_as_float(b));
-        if (colok && warp == 0 && lane % LPB == 0) {
-            const float s = __fdiv_rn(1.0f, alpha);
-            const int64_t kb = k0 / 128;
-            if (s_row != nullptr) s_row[tm * (K / 128) + kb] = s;
-            if (s_colT != nullptr) s_colT[kb * (M / 128) + tm] = s;
-            flag_nonfinite(status, b);
-        }
-        if (colok) {
-            uint32_t code[kRowsPerWarp][CW];
-#pragma unroll
-            for (int r = 0; r < kRowsPerWarp; r++)
-#pragma unroll
-                for (int w = 0; w < CW; w++)
-                    code[r][w] = cvt_fp8x4<E4M3>(__fmul_rn(alpha, elem<DT>(v[r], 4 * w)), __fmul_rn(alpha, elem<DT>(v[r], 4 * w + 1)),
-                                                 __fmul_rn(alpha, elem<DT>(v[r], 4 * w + 2)), __fmul_rn(alpha, elem<DT>(v[r], 4 * w + 3)));
-            if (q_row != nullptr) {
-                uint8_t *dst = q_row + m0 * K + k0;
-#pragma unroll
-                for (int r = 0; r < kRowsPerWarp; r++) {
-                    if (CW == 2) stg8(dst + (int64_t)r * K, code[r][0], code[r][CW - 1]);
-                    else stg4(dst + (int64_t)r * K, code[r][0]);
-                }
-            }
+            b = group_max<LPB>(b);
+            if (lane % LPB == 0) tred[warp][lane / LPB] = b;
             if (q_colT != nullptr) {
 #pragma unroll
-                for (int w = 0; w < CW; w++) {
-                    uint32_t c[4][4];
+                for (int r = 0; r < 16; r++) w[r] = lds4(st + (16 * quarter + r) * kRowBytes + wc * 4);
 #pragma unroll
-                    for (int g = 0; g < 4; g++)
-                        transpose4x4(code[4 * g][w], code[4 * g + 1][w], code[4 * g + 2][w], code[4 * g + 3][w],
-                                     c[0][g], c[1][g], c[2][g], c[3][g]);
+                for (int r = 0; r < 16; r++) w[16 + r] = lds4(st + (16 * (quarter + 4) + r) * kRowBytes + wc * 4);
+            }
+            __syncthreads();   // tile maxima visible; every read of the stage is done
+            uint32_t bt = 0;
 #pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const int col = lane * VEC + 4 * w + i;
-                        *reinterpret_cast<uint4 *>(sT + col * kTileRows + (warp ^ (lane & 7)) * 16) =
-                            make_uint4(c[i][0], c[i][1], c[i][2], c[i][3]);
-                    }
+            for (int q = 0; q < kEngWarps; q++) bt = max(bt, tred[q][lane / LPB]);
+            float alpha, sc;
+            bw_scales<DT>(bt, tab, alpha, sc);
+            if (warp == 0 && lane % LPB == 0 && k < K) {
+                if (s_row != nullptr) s_row[tm * (K / 128) + k / 128] = sc;
+                if (s_colT != nullptr) s_colT[(k / 128) * (M / 128) + tm] = sc;
+                flag_nonfinite(status, bt);
+            }
+            if (q_row != nullptr && k < K) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    uint32_t o[CW];
+                    chunk_fp8<DT, E4M3>(v[j], alpha, o);
+                    uint8_t *dst = q_row + (mb + 8 * warp + j) * K + k;
+                    if (CW == 2) stg8(dst, o[0], o[CW - 1]);
+                    else stg4(dst, o[0]);
                 }
             }
-        }
-        if (q_colT == nullptr) return;
-    }
-    __syncthreads();
+            if (q_colT == nullptr) return;
 #pragma unroll
-    for (int it = 0; it < TC * 8 / kThreads; it++) {
-        const int idx = it * kThreads + threadIdx.x;
-        const int col = idx >> 3, ch = idx & 7;
-        const int64_t kg = tk * TC + col, mg = tm * kTileRows + ch * 16;
-        if (kg < K && mg < M) {
-            const int phys = ch ^ ((col / VEC) & 7);
-            stg16(q_colT + kg * M + mg, *reinterpret_cast<const uint4 *>(sT + col * kTileRows + phys * 16));
+            for (int c = 0; c < CPW; c++) {
+                const int blk = (wc * CPW + c) / 128;
+                uint32_t bb = 0;
+#pragma unroll
+                for (int q = 0; q < kEngWarps; q++) bb = max(bb, tred[q][blk]);
+                float sc;
+                bw_scales<DT>(bb, tab, colalpha[c], sc);
+            }
         }
-    }
+        // ---- columnwise codes, column order, into the stage as [column][128 rows]
+        // (1x128: rows 32*quarter..+31 in w; 128x128: rows 16*quarter..+15 and 16*(quarter+4)..+15)
+#pragma unroll
+        for (int c = 0; c < CPW; c++) {
+            const int col = wc * CPW + c;
+            uint32_t o[8];
+            column_fp8<DT, E4M3, 32>(w, c, colalpha[c], o);
+            const int ch0 = TILE == 0 ? 2 * quarter : quarter, ch1 = TILE == 0 ? 2 * quarter + 1 : quarter + 4;
+            uint8_t *base = st + col * 128;
+            *reinterpret_cast<uint4 *>(base + ((ch0 ^ (wc & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(base + ((ch1 ^ (wc & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < TC * 8 / kEngThreads; it++) {
+            const int idx = it * kEngThreads + t;
+            const int col = idx >> 3, ch = idx & 7;
+            const int64_t kg = kb + col, mg = mb + ch * 16;
+            if (kg < K && mg < M)
+                stg16(q_colT + kg * M + mg, lds16(st + col * 128 + ((ch ^ ((col / CPW) & 7)) * 16)));
+        }
+    });
 }
 
 template <int DT, int TILE>
@@ -180,8 +199,18 @@ static cudaError_t bw_t(const void *x, int64_t M, int64_t K, uint8_t *q_row, flo
                         float *s_colT, int32_t *status, cudaStream_t st)
 {
     constexpr int TC = 32 * In<DT>::VEC;
-    const int64_t tiles = ((M + kTileRows - 1) / kTileRows) * ((K + TC - 1) / TC);
-    k_blockwise<DT, TILE><<<(unsigned)tiles, kThreads, 0, st>>>(x, M, K, q_row, s_row, q_colT, s_colT, status);
+    alignas(64) CUtensorMap map;
+    cudaError_t e = make_tile_map(&map, x, DT, M, K);
+    if (e != cudaSuccess) return e;
+    static bool attr = false;
+    if (!attr) {
+        e = cudaFuncSetAttribute(k_blockwise<DT, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
+    const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+    k_blockwise<DT, TILE><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, q_row, s_row, q_colT, s_colT, status);
     return cudaGetLastError();
 }
 

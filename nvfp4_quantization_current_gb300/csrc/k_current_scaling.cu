@@ -12,7 +12,7 @@
 // word (identical in every CTA); CTA 0 writes s.  The cast pass walks the
 // tensor from its end, so the last part the amax pass streamed (still in L2)
 // is consumed first.
-#include "q_common.cuh"
+#include "q_engine.cuh"
 #include "q_internal.h"
 
 namespace qk {
@@ -29,11 +29,13 @@ int sm_count()
 }
 
 // ---------------------------------------------------------------------------
-// a1: amax.  Grid-stride 16-byte loads (four in flight per thread), |x| max
-// on bit patterns, warp reduce, CTA reduce, one atomicMax per CTA.
+// a1: amax.  Grid-stride 16-byte loads, sixteen in flight per thread, |x|
+// max on bit patterns, warp reduce, CTA reduce, one atomicMax per CTA.
 // ---------------------------------------------------------------------------
+constexpr int kAmaxThreads = 256, kAmaxUnroll = 8;
+
 template <int DT>
-__global__ void __launch_bounds__(512) k_amax(const void *__restrict__ x, int64_t n, uint32_t *__restrict__ amax)
+__global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict__ x, int64_t n, uint32_t *__restrict__ amax)
 {
     constexpr int VEC = In<DT>::VEC;
     const uint4 *xv = static_cast<const uint4 *>(x);
@@ -41,28 +43,45 @@ __global__ void __launch_bounds__(512) k_amax(const void *__restrict__ x, int64_
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     uint32_t m = 0;
-    for (; i + 3 * stride < nv; i += 4 * stride) {
-        uint4 a = ldg_stream(xv + i), b = ldg_stream(xv + i + stride);
-        uint4 c = ldg_stream(xv + i + 2 * stride), d = ldg_stream(xv + i + 3 * stride);
-        m = max(m, max(max(absmax_bits<DT>(a), absmax_bits<DT>(b)), max(absmax_bits<DT>(c), absmax_bits<DT>(d))));
+    // double-buffered: the next group's eight loads are in flight while this
+    // group is reduced
+    const int64_t span = kAmaxUnroll * stride;
+    if (i + (kAmaxUnroll - 1) * stride < nv) {
+        uint4 a[kAmaxUnroll], b[kAmaxUnroll];
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; u++) a[u] = ldg_stream(xv + i + u * stride);
+        i += span;
+        while (i + (kAmaxUnroll - 1) * stride < nv) {
+#pragma unroll
+            for (int u = 0; u < kAmaxUnroll; u++) b[u] = ldg_stream(xv + i + u * stride);
+#pragma unroll
+            for (int u = 0; u < kAmaxUnroll; u++) m = max(m, absmax_bits<DT>(a[u]));
+#pragma unroll
+            for (int u = 0; u < kAmaxUnroll; u++) a[u] = b[u];
+            i += span;
+        }
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; u++) m = max(m, absmax_bits<DT>(a[u]));
     }
     for (; i < nv; i += stride) m = max(m, absmax_bits<DT>(ldg_stream(xv + i)));
     // the last n % VEC elements, one per thread of CTA 0
     if (blockIdx.x == 0 && threadIdx.x < n - nv * VEC) {
-        int64_t t = nv * VEC + threadIdx.x;
-        uint32_t u = DT == BF16 ? (uint32_t)static_cast<const uint16_t *>(x)[t] << 16
-                                : __float_as_uint(static_cast<const float *>(x)[t]);
+        const int64_t t = nv * VEC + threadIdx.x;
+        const uint32_t u = DT == BF16 ? (uint32_t)static_cast<const uint16_t *>(x)[t] << 16
+                                      : __float_as_uint(static_cast<const float *>(x)[t]);
         m = max(m, u & 0x7FFFFFFFu);
     }
     m = warp_max(m);
-    __shared__ uint32_t red[16];
+    __shared__ uint32_t red[kAmaxThreads / 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) red[warp] = m;
     __syncthreads();
     if (warp == 0) {
-        m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
+        m = lane < kAmaxThreads / 32 ? red[lane] : 0u;
         m = warp_max(m);
-        if (lane == 0 && m != 0) atomicMax(amax, m);
+        // same-address atomics serialize in L2: only a CTA that raises the
+        // running maximum pays for one
+        if (lane == 0 && m > *reinterpret_cast<volatile uint32_t *>(amax)) atomicMax(amax, m);
     }
 }
 
@@ -76,6 +95,7 @@ __global__ void __launch_bounds__(256) k_cs_cast_flat(const void *__restrict__ x
 {
     constexpr int VEC = In<DT>::VEC;
     constexpr int VPC = 16 / VEC;   // 16-byte input vectors per 16-element chunk
+    constexpr int U = 4;            // chunks in flight per thread
     const float a = *amax;
     const float alpha = alpha_from_amax(Fp8<FMT>::FMAX, a);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -85,134 +105,110 @@ __global__ void __launch_bounds__(256) k_cs_cast_flat(const void *__restrict__ x
     const uint4 *xv = static_cast<const uint4 *>(x);
     const int64_t nc = n / 16;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nc; i += 2 * stride) {
-        const int64_t c0 = nc - 1 - i, c1 = c0 - stride;   // backwards: L2-resident data first
-        uint4 v0[VPC], v1[VPC];
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nc; i += U * stride) {
+        uint4 v[U][VPC];
 #pragma unroll
-        for (int j = 0; j < VPC; j++) v0[j] = ldg_stream(xv + c0 * VPC + j);
-        if (c1 >= 0) {
+        for (int u = 0; u < U; u++) {
+            const int64_t c = nc - 1 - (i + u * stride);   // backwards: L2-resident data first
+            if (c >= 0)
 #pragma unroll
-            for (int j = 0; j < VPC; j++) v1[j] = ldg_stream(xv + c1 * VPC + j);
+                for (int j = 0; j < VPC; j++) v[u][j] = ldg_stream(xv + c * VPC + j);
         }
-        uint32_t o[4];
 #pragma unroll
-        for (int w = 0; w < 4; w++) {
-            const int e = 4 * w;   // element index within the chunk
-            o[w] = cvt_fp8x4<FMT>(__fmul_rn(alpha, elem<DT>(v0[e / VEC], e % VEC)),
-                                  __fmul_rn(alpha, elem<DT>(v0[(e + 1) / VEC], (e + 1) % VEC)),
-                                  __fmul_rn(alpha, elem<DT>(v0[(e + 2) / VEC], (e + 2) % VEC)),
-                                  __fmul_rn(alpha, elem<DT>(v0[(e + 3) / VEC], (e + 3) % VEC)));
-        }
-        stg16(q + c0 * 16, make_uint4(o[0], o[1], o[2], o[3]));
-        if (c1 >= 0) {
+        for (int u = 0; u < U; u++) {
+            const int64_t c = nc - 1 - (i + u * stride);
+            if (c < 0) break;
+            uint32_t o[4];
 #pragma unroll
-            for (int w = 0; w < 4; w++) {
-                const int e = 4 * w;
-                o[w] = cvt_fp8x4<FMT>(__fmul_rn(alpha, elem<DT>(v1[e / VEC], e % VEC)),
-                                      __fmul_rn(alpha, elem<DT>(v1[(e + 1) / VEC], (e + 1) % VEC)),
-                                      __fmul_rn(alpha, elem<DT>(v1[(e + 2) / VEC], (e + 2) % VEC)),
-                                      __fmul_rn(alpha, elem<DT>(v1[(e + 3) / VEC], (e + 3) % VEC)));
-            }
-            stg16(q + c1 * 16, make_uint4(o[0], o[1], o[2], o[3]));
+            for (int j = 0; j < VPC; j++) chunk_fp8<DT, FMT>(v[u][j], alpha, o + j * (VEC / 4));
+            stg16(q + c * 16, make_uint4(o[0], o[1], o[2], o[3]));
         }
     }
     // the last n % 16 elements, one per thread of CTA 0
     if (blockIdx.x == 0 && threadIdx.x < n - nc * 16) {
         const int64_t t = nc * 16 + threadIdx.x;
-        float v = DT == BF16 ? __uint_as_float((uint32_t)static_cast<const uint16_t *>(x)[t] << 16)
-                             : static_cast<const float *>(x)[t];
+        const float v = DT == BF16 ? __uint_as_float((uint32_t)static_cast<const uint16_t *>(x)[t] << 16)
+                                   : static_cast<const float *>(x)[t];
         q[t] = (uint8_t)(cvt_fp8x4<FMT>(__fmul_rn(alpha, v), 0.f, 0.f, 0.f) & 0xFFu);
     }
 }
 
 // ---------------------------------------------------------------------------
-// a3 with the transposed copy: a CTA owns a 128 x (32*VEC) tile.  The codes
-// are computed once; rowwise they are stored straight from registers, and
-// for the transpose each thread turns its 16 x VEC byte block around with
-// byte permutes, parks it in shared memory ([column][128 rows], 16-byte
-// chunks XOR-swizzled by column group so that neither side conflicts), and
-// the CTA then writes full 128-byte rows of q_colT.
-// Requires M % 16 == 0 and K % 16 == 0 (checked by the host).
+// a3 with the transposed copy, on the tile engine.  Per 128 x TC tile:
+//  row pass  - thread (warp w, lane l) casts rows 8w..8w+7, 16 bytes each,
+//              and stores the codes of q_row straight from registers;
+//  col pass  - thread (word column wc = t % 128, 16-row bands t/128 and
+//              t/128 + 4) reads one 4-byte word per row (CPW columns), casts
+//              the 16 values of each column and parks 16 code bytes per
+//              column in the stage, now free, laid out [column][128 rows] with
+//              16-byte chunks XOR-swizzled by word column;
+//  copy-out  - 8 threads per q_colT row write its 128 bytes.
+// The same codes come out of both passes (one deterministic cast of the same
+// FP32 product).  Requires M % 16 == 0 and K % 16 == 0.
 // ---------------------------------------------------------------------------
 template <int DT, int FMT>
-__global__ void __launch_bounds__(kThreads) k_cs_cast_tiled(const void *__restrict__ x, int64_t M, int64_t K,
-                                                            const float *__restrict__ amax,
-                                                            uint8_t *__restrict__ q_row,
-                                                            uint8_t *__restrict__ q_colT,
-                                                            float *__restrict__ scale, int32_t *status)
+__global__ void __launch_bounds__(kEngThreads, 1) k_cs_tiles(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
+                                                             const float *__restrict__ amax, uint8_t *__restrict__ q_row,
+                                                             uint8_t *__restrict__ q_colT, float *__restrict__ scale,
+                                                             int32_t *status)
 {
-    constexpr int VEC = In<DT>::VEC, BYTES = In<DT>::BYTES, TC = 32 * VEC, CW = VEC / 4;
-    __shared__ __align__(16) uint8_t sT[TC * kTileRows];
-
+    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, CPW = 4 / In<DT>::BYTES;
     const float a = *amax;
     const float alpha = alpha_from_amax(Fp8<FMT>::FMAX, a);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         *scale = __fdiv_rn(1.0f, alpha);
         flag_nonfinite(status, __float_as_uint(a) & 0x7FFFFFFFu);
     }
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31, wc = t & 127;
+    const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tiles_k = (K + TC - 1) / TC;
-    const int64_t t = (int64_t)gridDim.x - 1 - blockIdx.x;    // backwards
-    const int64_t tm = t / tiles_k, tk = t - tm * tiles_k;
-    const int64_t m0 = tm * kTileRows + warp * kRowsPerWarp;
-    const int64_t k0 = tk * TC + lane * VEC;
-    const bool ok = (m0 < M) && (k0 < K);
-
-    uint32_t code[kRowsPerWarp][CW];
-    if (ok) {
-        uint4 v[kRowsPerWarp];
-        const char *base = static_cast<const char *>(x) + (m0 * K + k0) * BYTES;
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; r++) v[r] = ldg_stream(base + (int64_t)r * K * BYTES);
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; r++)
-#pragma unroll
-            for (int w = 0; w < CW; w++)
-                code[r][w] = cvt_fp8x4<FMT>(__fmul_rn(alpha, elem<DT>(v[r], 4 * w)),
-                                            __fmul_rn(alpha, elem<DT>(v[r], 4 * w + 1)),
-                                            __fmul_rn(alpha, elem<DT>(v[r], 4 * w + 2)),
-                                            __fmul_rn(alpha, elem<DT>(v[r], 4 * w + 3)));
+    run_tiles(&tmap, tiles_m, tiles_k, TC, true, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
+        const int64_t mb = tm * kTileRowsE, kb = tk * TC;
         if (q_row != nullptr) {
-            uint8_t *dst = q_row + m0 * K + k0;
+            const int64_t k = kb + lane * VEC;
 #pragma unroll
-            for (int r = 0; r < kRowsPerWarp; r++) {
-                if (CW == 2) stg8(dst + (int64_t)r * K, code[r][0], code[r][CW - 1]);
-                else stg4(dst + (int64_t)r * K, code[r][0]);
-            }
-        }
-        if (q_colT != nullptr) {
-#pragma unroll
-            for (int w = 0; w < CW; w++) {
-                uint32_t c[4][4];   // c[i][g]: column 4w+i, rows 4g..4g+3
-#pragma unroll
-                for (int g = 0; g < 4; g++)
-                    transpose4x4(code[4 * g][w], code[4 * g + 1][w], code[4 * g + 2][w], code[4 * g + 3][w],
-                                 c[0][g], c[1][g], c[2][g], c[3][g]);
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const int col = lane * VEC + 4 * w + i;
-                    const int chunk = warp ^ (lane & 7);
-                    *reinterpret_cast<uint4 *>(sT + col * kTileRows + chunk * 16) =
-                        make_uint4(c[i][0], c[i][1], c[i][2], c[i][3]);
+            for (int j = 0; j < 8; j++) {
+                const int r = 8 * warp + j;
+                const uint4 v = lds16(st + r * kRowBytes + lane * 16);
+                uint32_t o[CW];
+                chunk_fp8<DT, FMT>(v, alpha, o);
+                if (mb + r < M && k < K) {
+                    uint8_t *dst = q_row + (mb + r) * K + k;
+                    if (CW == 2) stg8(dst, o[0], o[CW - 1]);
+                    else stg4(dst, o[0]);
                 }
             }
         }
-    }
-    if (q_colT == nullptr) return;
-    __syncthreads();
-    // 8 lanes per column row: each writes one 16-byte chunk (16 rows of m)
+        if (q_colT == nullptr) return;
+        uint32_t w[2][16];
 #pragma unroll
-    for (int it = 0; it < TC * 8 / kThreads; it++) {
-        const int idx = it * kThreads + threadIdx.x;
-        const int col = idx >> 3, ch = idx & 7;
-        const int64_t kg = tk * TC + col, mg = tm * kTileRows + ch * 16;
-        if (kg < K && mg < M) {
-            const int phys = ch ^ ((col / VEC) & 7);
-            uint4 val = *reinterpret_cast<const uint4 *>(sT + col * kTileRows + phys * 16);
-            stg16(q_colT + kg * M + mg, val);
+        for (int i = 0; i < 2; i++) {
+            const int band = (t >> 7) + 4 * i;
+#pragma unroll
+            for (int r = 0; r < 16; r++) w[i][r] = lds4(st + (16 * band + r) * kRowBytes + wc * 4);
         }
-    }
+        __syncthreads();   // every read of the stage is done: reuse it for the transposed codes
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int band = (t >> 7) + 4 * i;
+#pragma unroll
+            for (int c = 0; c < CPW; c++) {
+                uint32_t o[4];
+                column_fp8<DT, FMT, 16>(w[i], c, alpha, o);
+                const int col = wc * CPW + c;
+                *reinterpret_cast<uint4 *>(st + col * 128 + ((band ^ (wc & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < TC * 8 / kEngThreads; it++) {
+            const int idx = it * kEngThreads + t;
+            const int col = idx >> 3, ch = idx & 7;
+            const int64_t kg = kb + col, mg = mb + ch * 16;
+            if (kg < K && mg < M)
+                stg16(q_colT + kg * M + mg, lds16(st + col * 128 + ((ch ^ ((col / CPW) & 7)) * 16)));
+        }
+    });
 }
 
 // Scales of an empty tensor.
@@ -226,19 +222,24 @@ __global__ void k_empty_scales(float *amax_out, float *scale)
 // launchers
 // ---------------------------------------------------------------------------
 
+// Zeroes the amax word before the reduction (a kernel on the same stream: the
+// next kernel starts right behind it, which a driver memset does not).
+__global__ void k_zero_word(uint32_t *w) { *w = 0u; }
+
 cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *status, cudaStream_t st)
 {
     (void)status;
-    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
+    k_zero_word<<<1, 1, 0, st>>>(reinterpret_cast<uint32_t *>(amax));
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || n == 0) return e;
     const int vec = dt == BF16 ? 8 : 4;
     const int64_t nv = n / vec;
-    int64_t blocks = (nv + 511) / 512;
+    int64_t blocks = (nv + (int64_t)kAmaxThreads * kAmaxUnroll - 1) / ((int64_t)kAmaxThreads * kAmaxUnroll);
     const int64_t cap = (int64_t)sm_count() * 4;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (dt == BF16) k_amax<BF16><<<(unsigned)blocks, 512, 0, st>>>(x, n, reinterpret_cast<uint32_t *>(amax));
-    else k_amax<F32><<<(unsigned)blocks, 512, 0, st>>>(x, n, reinterpret_cast<uint32_t *>(amax));
+    if (dt == BF16) k_amax<BF16><<<(unsigned)blocks, kAmaxThreads, 0, st>>>(x, n, reinterpret_cast<uint32_t *>(amax));
+    else k_amax<F32><<<(unsigned)blocks, kAmaxThreads, 0, st>>>(x, n, reinterpret_cast<uint32_t *>(amax));
     return cudaGetLastError();
 }
 
@@ -248,16 +249,26 @@ static cudaError_t cs_cast_t(const void *x, int64_t M, int64_t K, const float *a
 {
     if (q_colT == nullptr) {
         const int64_t n = M * K, nc = n / 16;
-        int64_t blocks = (nc + 2 * 256 - 1) / (2 * 256);
+        int64_t blocks = (nc + 4 * 256 - 1) / (4 * 256);
         const int64_t cap = (int64_t)sm_count() * 8;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
         k_cs_cast_flat<DT, FMT><<<(unsigned)blocks, 256, 0, st>>>(x, n, amax, q_row, scale, status);
-    } else {
-        constexpr int TC = 32 * In<DT>::VEC;
-        const int64_t tiles = ((M + kTileRows - 1) / kTileRows) * ((K + TC - 1) / TC);
-        k_cs_cast_tiled<DT, FMT><<<(unsigned)tiles, kThreads, 0, st>>>(x, M, K, amax, q_row, q_colT, scale, status);
+        return cudaGetLastError();
     }
+    constexpr int TC = 32 * In<DT>::VEC;
+    alignas(64) CUtensorMap map;
+    cudaError_t e = make_tile_map(&map, x, DT, M, K);
+    if (e != cudaSuccess) return e;
+    static bool attr = false;
+    if (!attr) {
+        e = cudaFuncSetAttribute(k_cs_tiles<DT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
+    const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+    k_cs_tiles<DT, FMT><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, amax, q_row, q_colT, scale, status);
     return cudaGetLastError();
 }
 

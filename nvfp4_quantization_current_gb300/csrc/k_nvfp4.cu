@@ -12,29 +12,34 @@
 // sb = E4M3((b * alpha_g) / 6) (b = 0 -> 1.0), enc = alpha_g / sb,
 // q = E2M1(x * enc).
 //
-// The amax comes from the preceding amax pass (or the caller); this pass
-// walks the tensor backwards for L2 reuse, like the current-scaling cast.
-// CTA tile 128 x (32*VEC).  Rowwise 1x16 blocks span 16/VEC lanes; a
-// columnwise 16x1 block is the 16 rows one thread holds, so its scale needs
-// no communication; its codes are produced in column order and staged in
-// shared memory for transposed writes.  For 16x16 tiles the transposed copy
-// is the row codes turned around by an in-register nibble transpose.
-#include "q_common.cuh"
+// On the tile engine (the amax comes from the preceding amax pass or the
+// caller; tiles are walked backwards for L2 reuse):
+//  row pass - thread (warp w, lane l): rows 8w..8w+7, 16 bytes each; a 1x16
+//             block spans 16/VEC lanes; stochastic rounding draws one
+//             Philox block (8 elements) per thread and row;
+//  col pass - 1x16: thread (word column t % 128, 16-row bands t/128 and
+//             t/128 + 4) reads 16 words and quantizes the CPW column blocks
+//             it holds entirely (two Philox blocks per column for SR);
+//             16x16: the row codes, kept in shared memory, are turned around
+//             with 8x8 nibble transposes;
+//             either way 8 code bytes per column block are parked in the
+//             stage (now free) as [column][64 bytes], 8-byte chunks swizzled;
+//  copy-out - 8 threads per q_colT row.
+#include <cstring>
+
+#include "q_engine.cuh"
 #include "q_internal.h"
 
 namespace qk {
 
-QD void nv_block_scale(uint32_t b, float alpha_g, uint32_t &sb, float &enc)
+// Block scale code sb = E4M3(RN(RN(b * alpha_g) / 6)) (b = 0 -> 1.0) and the
+// encode factor enc = alpha_g / f(sb) (0 when f(sb) = 0).  enc depends only
+// on the code, so each CTA tabulates alpha_g / f(c) for the 128 positive
+// codes once (enc_tab[0x38] = alpha_g covers b = 0).
+QD void nv_block_scale(uint32_t b, float alpha_g, const float *enc_tab, uint32_t &sb, float &enc)
 {
-    if (b == 0) {
-        sb = 0x38u;   // 1.0
-        enc = alpha_g;
-        return;
-    }
-    const float sbf = __fdiv_rn(__fmul_rn(__uint_as_float(b), alpha_g), 6.0f);
-    sb = e4m3_code(sbf);
-    const float sv = e4m3_value(sb);
-    enc = (sv == 0.0f) ? 0.0f : __fdiv_rn(alpha_g, sv);
+    sb = b == 0 ? 0x38u : e4m3_code(__fdiv_rn(__fmul_rn(__uint_as_float(b), alpha_g), 6.0f));
+    enc = enc_tab[sb];
 }
 
 // 16 random bits for element e (0..7) of a Philox block.
@@ -65,213 +70,219 @@ QD void transpose8x8_nibbles(uint32_t *a)
     }
 }
 
-template <int DT, int BLK, int RND>
-__global__ void __launch_bounds__(kThreads) k_nvfp4(const void *__restrict__ x, int64_t M, int64_t K,
-                                                    const float *__restrict__ amax, uint64_t seed, uint64_t offset,
-                                                    uint8_t *__restrict__ q_row, uint8_t *__restrict__ sb_row,
-                                                    uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
-                                                    float *__restrict__ s_global, int32_t *status)
+// Codes of one row chunk (VEC elements, VEC/2 bytes) with scale factor enc;
+// SR draws the Philox block of element index i0 (row-major, stream 0).
+template <int DT, int RND>
+QD uint32_t nv_row_codes(const uint4 &v, float enc, uint64_t seed, uint64_t offset, int64_t i0)
 {
-    constexpr int VEC = In<DT>::VEC, BYTES = In<DT>::BYTES, TC = 32 * VEC, LPB = 16 / VEC;
-    __shared__ __align__(16) uint8_t sT[TC * (kTileRows / 2)];
-    __shared__ uint8_t sSB[kWarps * TC];
+    constexpr int VEC = In<DT>::VEC;
+    float y[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) y[j] = j < VEC ? elem<DT>(v, j < VEC ? j : 0) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < VEC; j += 2) mul2(y[j], y[j + 1], enc, enc);
+    if (RND == 1) {
+        const uint4 R = sr_bits(seed, offset + (uint64_t)(i0 >> 3), 0u);
+        const int e0 = (int)(i0 & 7);
+#pragma unroll
+        for (int j = 0; j < VEC; j++) y[j] = sr_e2m1_value(y[j], r16_of(R, e0 + j));
+    }
+    return cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+}
 
+template <int DT, int BLK, int RND>
+__global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
+                                                          const float *__restrict__ amax, uint64_t seed, uint64_t offset,
+                                                          uint8_t *__restrict__ q_row, uint8_t *__restrict__ sb_row,
+                                                          uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
+                                                          float *__restrict__ s_global, int32_t *status)
+{
+    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, LPB = 16 / VEC, CPW = 4 / In<DT>::BYTES;
+    constexpr int RB = TC / 2;   // packed code bytes per tile row
+    __shared__ uint8_t sSB[8][TC];                       // 1x16 columnwise block scales of a tile
+    __shared__ uint32_t bred[kEngWarps][TC / 16];        // 16x16: half-block maxima
+    __shared__ __align__(16) uint8_t sC[BLK == 1 ? kTileRowsE * RB : 16];   // 16x16: row codes of a tile
+
+    __shared__ float enc_tab[128];
     const float A = *amax;
     const float alpha_g = alpha_from_amax(2688.0f, A);
+    if (threadIdx.x < 128) {
+        const float sv = e4m3_value(threadIdx.x);
+        enc_tab[threadIdx.x] = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_g, sv);
+    }   // visible after the engine's first barrier
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         *s_global = __fdiv_rn(1.0f, alpha_g);
         flag_nonfinite(status, __float_as_uint(A) & 0x7FFFFFFFu);
     }
-    const int64_t tiles_k = (K + TC - 1) / TC;
-    if (M == 0 || tiles_k == 0) return;
+    if (M == 0 || K == 0) return;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31, wc = t & 127;
+    const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
+    // 8-byte chunk swizzle of the parked codes, chosen so that the writers of
+    // each variant (a word column per lane, or 8 columns per lane) and the
+    // copy-out spread over the banks
+    auto swz = [](int col) { return BLK == 0 ? (col / CPW) & 7 : (col >> 3) & 7; };
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)gridDim.x - 1 - blockIdx.x;   // backwards: L2-resident data first
-    const int64_t tm = t / tiles_k, tk = t - tm * tiles_k;
-    const int64_t m0 = tm * kTileRows + warp * kRowsPerWarp;
-    const int64_t k0 = tk * TC + lane * VEC;
-    const bool ok = (k0 < K) && (m0 < M);   // M % 16 == 0: a warp's rows are all valid or none
-
-    uint4 v[kRowsPerWarp];
-    const char *base = static_cast<const char *>(x) + (m0 * K + k0) * BYTES;
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; r++) v[r] = ok ? ldg_stream(base + (int64_t)r * K * BYTES) : make_uint4(0, 0, 0, 0);
-
-    uint32_t rowcode[kRowsPerWarp];   // VEC nibbles per row (BF16: 8 -> a word, FP32: 4 -> low half)
-
-    if (BLK == 0) {
-        // ---------------- 1x16 rowwise ----------------
-        if (q_row != nullptr) {
-#pragma unroll
-            for (int r = 0; r < kRowsPerWarp; r++) {
-                const uint32_t b = group_max<LPB>(absmax_bits<DT>(v[r]));
-                uint32_t sb;
-                float enc;
-                nv_block_scale(b, alpha_g, sb, enc);
-                float y[8];
-#pragma unroll
-                for (int j = 0; j < 8; j++) y[j] = j < VEC ? __fmul_rn(elem<DT>(v[r], j < VEC ? j : 0), enc) : 0.0f;
-                if (RND == 1) {
-                    const int64_t i0 = (m0 + r) * K + k0;
-                    const uint4 R = sr_bits(seed, offset + (uint64_t)(i0 >> 3), 0u);
-                    const int e0 = (int)(i0 & 7);
-#pragma unroll
-                    for (int j = 0; j < VEC; j++) y[j] = sr_e2m1_value(y[j], r16_of(R, e0 + j));
-                }
-                rowcode[r] = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-                if (ok) {
-                    uint8_t *dst = q_row + (m0 + r) * (K / 2) + k0 / 2;
-                    if (VEC == 8) stg4(dst, rowcode[r]);
-                    else *reinterpret_cast<uint16_t *>(dst) = (uint16_t)rowcode[r];
-                    if (lane % LPB == 0) {
-                        sb_row[(m0 + r) * (K / 16) + k0 / 16] = (uint8_t)sb;
-                        flag_nonfinite(status, b);
-                    }
-                }
-            }
-        }
-        if (q_colT == nullptr) return;
-        // ---------------- 16x1 columnwise (in-thread blocks), transposed ----------------
-        uint4 acc = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; r++) {
-            acc.x = colmax_word<DT>(acc.x, v[r].x);
-            acc.y = colmax_word<DT>(acc.y, v[r].y);
-            acc.z = colmax_word<DT>(acc.z, v[r].z);
-            acc.w = colmax_word<DT>(acc.w, v[r].w);
-        }
-        if (ok) {
-#pragma unroll
-            for (int j = 0; j < VEC; j++) {
-                const uint32_t b = colmax_bits<DT>(acc, j);
-                uint32_t sb;
-                float enc;
-                nv_block_scale(b, alpha_g, sb, enc);
-                float y[16];
-#pragma unroll
-                for (int r = 0; r < 16; r++) y[r] = __fmul_rn(elem<DT>(v[r], j), enc);
-                if (RND == 1) {
-                    const int64_t it0 = (k0 + j) * M + m0;   // multiple of 16
-                    const uint4 R0 = sr_bits(seed, offset + (uint64_t)(it0 >> 3), 1u);
-                    const uint4 R1 = sr_bits(seed, offset + (uint64_t)(it0 >> 3) + 1u, 1u);
-#pragma unroll
-                    for (int r = 0; r < 8; r++) {
-                        y[r] = sr_e2m1_value(y[r], r16_of(R0, r));
-                        y[r + 8] = sr_e2m1_value(y[r + 8], r16_of(R1, r));
-                    }
-                }
-                const uint32_t lo = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-                const uint32_t hi = cvt_fp4x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
-                const int col = lane * VEC + j;
-                *reinterpret_cast<uint2 *>(sT + col * (kTileRows / 2) + (warp ^ (lane & 7)) * 8) = make_uint2(lo, hi);
-                sSB[warp * TC + col] = (uint8_t)sb;
-                flag_nonfinite(status, b);
-            }
-        }
-    } else {
-        // ---------------- 16x16: one scale per tile ----------------
-        uint32_t b = 0;
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; r++) b = max(b, absmax_bits<DT>(v[r]));
-        b = group_max<LPB>(b);
-        uint32_t sb;
-        float enc;
-        nv_block_scale(b, alpha_g, sb, enc);
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; r++) {
-            float y[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++) y[j] = j < VEC ? __fmul_rn(elem<DT>(v[r], j < VEC ? j : 0), enc) : 0.0f;
-            if (RND == 1) {
-                const int64_t i0 = (m0 + r) * K + k0;
-                const uint4 R = sr_bits(seed, offset + (uint64_t)(i0 >> 3), 0u);
-                const int e0 = (int)(i0 & 7);
-#pragma unroll
-                for (int j = 0; j < VEC; j++) y[j] = sr_e2m1_value(y[j], r16_of(R, e0 + j));
-            }
-            rowcode[r] = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-        }
-        if (ok) {
+    run_tiles(&tmap, tiles_m, tiles_k, TC, true, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
+        const int64_t mb = tm * kTileRowsE, kb = tk * TC;
+        const int64_t k = kb + lane * VEC;
+        if constexpr (BLK == 0) {
+            // ---------------- 1x16 rowwise ----------------
             if (q_row != nullptr) {
-#pragma unroll
-                for (int r = 0; r < kRowsPerWarp; r++) {
-                    uint8_t *dst = q_row + (m0 + r) * (K / 2) + k0 / 2;
-                    if (VEC == 8) stg4(dst, rowcode[r]);
-                    else *reinterpret_cast<uint16_t *>(dst) = (uint16_t)rowcode[r];
+#pragma unroll 2
+                for (int j = 0; j < 8; j++) {
+                    const int r = 8 * warp + j;
+                    const int64_t m = mb + r;
+                    const uint4 v = lds16(st + r * kRowBytes + lane * 16);
+                    const uint32_t b = group_max<LPB>(absmax_bits<DT>(v));
+                    uint32_t sb;
+                    float enc;
+                    nv_block_scale(b, alpha_g, enc_tab, sb, enc);
+                    const uint32_t code = nv_row_codes<DT, RND>(v, enc, seed, offset, m * K + k);
+                    if (m < M && k < K) {
+                        uint8_t *dst = q_row + m * (K / 2) + k / 2;
+                        if (VEC == 8) stg4(dst, code);
+                        else *reinterpret_cast<uint16_t *>(dst) = (uint16_t)code;
+                        if (lane % LPB == 0) {
+                            sb_row[m * (K / 16) + k / 16] = (uint8_t)sb;
+                            flag_nonfinite(status, b);
+                        }
+                    }
                 }
             }
-            if (lane % LPB == 0) {
-                if (sb_row != nullptr) sb_row[(m0 / 16) * (K / 16) + k0 / 16] = (uint8_t)sb;
-                if (sb_colT != nullptr) sb_colT[(k0 / 16) * (M / 16) + m0 / 16] = (uint8_t)sb;
-                flag_nonfinite(status, b);
+            if (q_colT == nullptr) return;
+            // ---------------- 16x1 columnwise ----------------
+            uint32_t w[2][16];
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+                const int band = (t >> 7) + 4 * i;
+#pragma unroll
+                for (int r = 0; r < 16; r++) w[i][r] = lds4(st + (16 * band + r) * kRowBytes + wc * 4);
             }
-            if (q_colT != nullptr) {
-                uint32_t lo[8], hi[8];
-                if (VEC == 8) {
+            __syncthreads();   // every read of the stage is done: reuse it for the transposed codes
 #pragma unroll
-                    for (int r = 0; r < 8; r++) {
-                        lo[r] = rowcode[r];
-                        hi[r] = rowcode[r + 8];
-                    }
-                    transpose8x8_nibbles(lo);
-                    transpose8x8_nibbles(hi);
-                } else {
+            for (int i = 0; i < 2; i++) {
+                const int band = (t >> 7) + 4 * i;
+                const int64_t m0 = mb + 16 * band;
+                uint32_t bm[CPW];
+                column_absmax<DT, 16>(w[i], bm);
 #pragma unroll
-                    for (int j = 0; j < VEC; j++) {
-                        uint32_t l = 0, h = 0;
+                for (int c = 0; c < CPW; c++) {
+                    const int col = wc * CPW + c;
+                    const int64_t kg = kb + col;
+                    const uint32_t b = bm[c];
+                    uint32_t sb;
+                    float enc;
+                    nv_block_scale(b, alpha_g, enc_tab, sb, enc);
+                    float y[16];
+#pragma unroll
+                    for (int r = 0; r < 16; r++) y[r] = word_elem<DT>(w[i][r], c);
+#pragma unroll
+                    for (int r = 0; r < 16; r += 2) mul2(y[r], y[r + 1], enc, enc);
+                    if (RND == 1) {
+                        const uint64_t g = offset + (uint64_t)((kg * M + m0) >> 3);   // kg*M + m0 is a multiple of 16
+                        const uint4 R0 = sr_bits(seed, g, 1u), R1 = sr_bits(seed, g + 1u, 1u);
 #pragma unroll
                         for (int r = 0; r < 8; r++) {
-                            l |= ((rowcode[r] >> (4 * j)) & 0xFu) << (4 * r);
-                            h |= ((rowcode[r + 8] >> (4 * j)) & 0xFu) << (4 * r);
+                            y[r] = sr_e2m1_value(y[r], r16_of(R0, r));
+                            y[r + 8] = sr_e2m1_value(y[r + 8], r16_of(R1, r));
                         }
-                        lo[j] = l;
-                        hi[j] = h;
                     }
+                    const uint32_t lo = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+                    const uint32_t hi = cvt_fp4x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+                    *reinterpret_cast<uint2 *>(st + col * 64 + ((band ^ swz(col)) * 8)) = make_uint2(lo, hi);
+                    sSB[band][col] = (uint8_t)sb;
+                    if (kg < K && m0 < M) flag_nonfinite(status, b);
                 }
+            }
+        } else {
+            // ---------------- 16x16: one scale per tile ----------------
+            uint4 v[8];
+            uint32_t b = 0;
 #pragma unroll
-                for (int j = 0; j < VEC; j++) {
-                    const int col = lane * VEC + j;
-                    *reinterpret_cast<uint2 *>(sT + col * (kTileRows / 2) + (warp ^ (lane & 7)) * 8) = make_uint2(lo[j], hi[j]);
+            for (int j = 0; j < 8; j++) {
+                v[j] = lds16(st + (8 * warp + j) * kRowBytes + lane * 16);
+                b = max(b, absmax_bits<DT>(v[j]));
+            }
+            b = group_max<LPB>(b);
+            if (lane % LPB == 0) bred[warp][lane / LPB] = b;
+            __syncthreads();   // half-block maxima visible; every read of the stage is done
+            b = max(bred[warp & ~1][lane / LPB], bred[warp | 1][lane / LPB]);
+            uint32_t sb;
+            float enc;
+            nv_block_scale(b, alpha_g, enc_tab, sb, enc);
+            const int64_t m16 = mb + 16 * (warp >> 1);
+            if ((warp & 1) == 0 && lane % LPB == 0 && m16 < M && k < K) {
+                if (sb_row != nullptr) sb_row[(m16 / 16) * (K / 16) + k / 16] = (uint8_t)sb;
+                if (sb_colT != nullptr) sb_colT[(k / 16) * (M / 16) + m16 / 16] = (uint8_t)sb;
+                flag_nonfinite(status, b);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const int r = 8 * warp + j;
+                const int64_t m = mb + r;
+                const uint32_t code = nv_row_codes<DT, RND>(v[j], enc, seed, offset, m * K + k);
+                if (q_row != nullptr && m < M && k < K) {
+                    uint8_t *dst = q_row + m * (K / 2) + k / 2;
+                    if (VEC == 8) stg4(dst, code);
+                    else *reinterpret_cast<uint16_t *>(dst) = (uint16_t)code;
+                }
+                if (VEC == 8) *reinterpret_cast<uint32_t *>(sC + r * RB + lane * 4) = code;
+                else *reinterpret_cast<uint16_t *>(sC + r * RB + lane * 2) = (uint16_t)code;
+            }
+            if (q_colT == nullptr) return;
+            __syncthreads();   // row codes of the tile visible
+            // items: (8-column group g, 16-row band); read 16 words (8 nibbles each), transpose
+            constexpr int NG = TC / 8;
+            if (t < NG * 8) {
+                const int g = t % NG, band = t / NG;
+                uint32_t lo[8], hi[8];
+#pragma unroll
+                for (int r = 0; r < 8; r++) {
+                    lo[r] = *reinterpret_cast<const uint32_t *>(sC + (16 * band + r) * RB + 4 * g);
+                    hi[r] = *reinterpret_cast<const uint32_t *>(sC + (16 * band + 8 + r) * RB + 4 * g);
+                }
+                transpose8x8_nibbles(lo);
+                transpose8x8_nibbles(hi);
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const int col = 8 * g + j;
+                    *reinterpret_cast<uint2 *>(st + col * 64 + ((band ^ swz(col)) * 8)) = make_uint2(lo[j], hi[j]);
                 }
             }
         }
-        if (q_colT == nullptr) return;
-    }
-
-    __syncthreads();
-    // transposed codes: 8 lanes per q_colT row, one 8-byte chunk (16 rows of m) each
+        __syncthreads();
+        // transposed codes: 8 threads per q_colT row, one 8-byte chunk (16 rows of m) each
 #pragma unroll
-    for (int it = 0; it < TC * 8 / kThreads; it++) {
-        const int idx = it * kThreads + threadIdx.x;
-        const int col = idx >> 3, ch = idx & 7;
-        const int64_t kg = tk * TC + col, mg = tm * kTileRows + ch * 16;
-        if (kg < K && mg < M) {
-            const int phys = ch ^ ((col / VEC) & 7);
-            const uint2 val = *reinterpret_cast<const uint2 *>(sT + col * (kTileRows / 2) + phys * 8);
-            stg8(q_colT + kg * (M / 2) + mg / 2, val.x, val.y);
-        }
-    }
-    if (BLK == 0) {
-        // columnwise block scales: 8 per column of the tile (one per warp)
-        const int64_t rows_left = (M - tm * kTileRows) / 16;
-        const int nb = rows_left < kWarps ? (int)rows_left : kWarps;
-        for (int col = threadIdx.x; col < TC; col += kThreads) {
-            const int64_t kg = tk * TC + col;
-            if (kg >= K) continue;
-            uint8_t *dst = sb_colT + kg * (M / 16) + tm * kWarps;
-            if (nb == kWarps && (M % 128) == 0) {
-                uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-                for (int w = 0; w < 4; w++) {
-                    w0 |= (uint32_t)sSB[w * TC + col] << (8 * w);
-                    w1 |= (uint32_t)sSB[(w + 4) * TC + col] << (8 * w);
-                }
-                stg8(dst, w0, w1);
-            } else {
-                for (int w = 0; w < nb; w++) dst[w] = sSB[w * TC + col];
+        for (int it = 0; it < TC * 8 / kEngThreads; it++) {
+            const int idx = it * kEngThreads + t;
+            const int col = idx >> 3, ch = idx & 7;
+            const int64_t kg = kb + col, mg = mb + ch * 16;
+            if (kg < K && mg < M) {
+                const uint2 val = *reinterpret_cast<const uint2 *>(st + col * 64 + ((ch ^ swz(col)) * 8));
+                stg8(q_colT + kg * (M / 2) + mg / 2, val.x, val.y);
             }
         }
-    }
+        if constexpr (BLK == 0) {
+            const int64_t left = (M - mb) / 16;
+            const int nb = left < 8 ? (int)left : 8;
+            for (int col = t; col < TC; col += kEngThreads) {
+                const int64_t kg = kb + col;
+                if (kg >= K) continue;
+                uint8_t *dst = sb_colT + kg * (M / 16) + tm * 8;
+                if (nb == 8 && (M % 128) == 0) {
+                    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        w0 |= (uint32_t)sSB[q][col] << (8 * q);
+                        w1 |= (uint32_t)sSB[q + 4][col] << (8 * q);
+                    }
+                    stg8(dst, w0, w1);
+                } else {
+                    for (int q = 0; q < nb; q++) dst[q] = sSB[q][col];
+                }
+            }
+        }
+    });
 }
 
 template <int DT, int BLK, int RND>
@@ -280,10 +291,25 @@ static cudaError_t nv_t(const void *x, int64_t M, int64_t K, const float *amax, 
                         int32_t *status, cudaStream_t st)
 {
     constexpr int TC = 32 * In<DT>::VEC;
-    int64_t tiles = ((M + kTileRows - 1) / kTileRows) * ((K + TC - 1) / TC);
-    if (tiles < 1) tiles = 1;   // an empty tensor still gets its global scale
-    k_nvfp4<DT, BLK, RND><<<(unsigned)tiles, kThreads, 0, st>>>(x, M, K, amax, seed, offset, q_row, sb_row, q_colT,
-                                                                sb_colT, s_global, status);
+    alignas(64) CUtensorMap map;
+    const bool empty = M == 0 || K == 0;
+    if (!empty) {
+        cudaError_t e = make_tile_map(&map, x, DT, M, K);
+        if (e != cudaSuccess) return e;
+    } else {
+        memset(&map, 0, sizeof map);   // never dereferenced: the kernel returns before touching tiles
+    }
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_nvfp4<DT, BLK, RND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
+    int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+    if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
+    k_nvfp4<DT, BLK, RND><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, amax, seed, offset, q_row, sb_row, q_colT,
+                                                               sb_colT, s_global, status);
     return cudaGetLastError();
 }
 

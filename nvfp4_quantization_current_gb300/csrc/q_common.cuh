@@ -203,6 +203,70 @@ QD uint32_t bf16_bits(float f)
     return h;
 }
 
+// a *= s0 and b *= s1: two IEEE round-to-nearest FP32 products in one
+// packed instruction (the same results as two separate multiplies).
+QD void mul2(float &a, float &b, float s0, float s1)
+{
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %3};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "+f"(a), "+f"(b) : "f"(s0), "f"(s1));
+}
+
+// The VEC elements of a 16-byte row chunk times s, as FP8 codes (VEC/4 words,
+// element 0 in the lowest byte).
+template <int DT, int FMT> QD void chunk_fp8(const uint4 &v, float s, uint32_t *o)
+{
+    constexpr int VEC = In<DT>::VEC;
+    float f[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; j++) f[j] = elem<DT>(v, j);
+#pragma unroll
+    for (int j = 0; j < VEC; j += 2) mul2(f[j], f[j + 1], s, s);
+#pragma unroll
+    for (int w = 0; w < VEC / 4; w++) o[w] = cvt_fp8x4<FMT>(f[4 * w], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
+}
+
+// Element c (0..CPW-1) of a 4-byte word of the input (two BF16 or one FP32).
+template <int DT> QD float word_elem(uint32_t w, int c)
+{
+    return DT == BF16 ? __uint_as_float(c ? (w & 0xFFFF0000u) : (w << 16)) : __uint_as_float(w);
+}
+
+// Column c of N consecutive rows (N words) times s, as FP8 codes (N/4 words,
+// row 0 in the lowest byte).
+template <int DT, int FMT, int N> QD void column_fp8(const uint32_t *w, int c, float s, uint32_t *o)
+{
+    float f[N];
+#pragma unroll
+    for (int r = 0; r < N; r++) f[r] = word_elem<DT>(w[r], c);
+#pragma unroll
+    for (int r = 0; r < N; r += 2) mul2(f[r], f[r + 1], s, s);
+#pragma unroll
+    for (int g = 0; g < N / 4; g++) o[g] = cvt_fp8x4<FMT>(f[4 * g], f[4 * g + 1], f[4 * g + 2], f[4 * g + 3]);
+}
+
+// Per-column |x| maxima over N rows of words, as FP32 bit patterns:
+// m[c] for c < CPW.  BF16 words keep both columns' maxima packed
+// (one 16x2 max per row).
+template <int DT, int N> QD void column_absmax(const uint32_t *w, uint32_t *m)
+{
+    if (DT == BF16) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int r = 0; r < N; r++) acc = __vmaxu2(acc, w[r] & 0x7FFF7FFFu);
+        m[0] = acc << 16;
+        m[DT == BF16 ? 1 : 0] = acc & 0xFFFF0000u;
+    } else {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int r = 0; r < N; r++) acc = max(acc, w[r] & 0x7FFFFFFFu);
+        m[0] = acc;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // scales
 // ---------------------------------------------------------------------------

@@ -1,0 +1,143 @@
+// Tile engine: a persistent, TMA-fed, multi-stage pipeline that streams
+// 128-row x 512-byte tiles of the input through shared memory.
+//
+// One CTA of 512 threads per SM.  Thread 0 keeps kStages tiles in flight:
+// each is one cp.async.bulk.tensor.2d load (the tensor map's box is 128 rows
+// x 512 bytes; rows or columns past the tensor's edge arrive as zeros) that
+// completes on the stage's mbarrier.  All threads then run the recipe's tile
+// body on the stage; when they are done (barrier) thread 0 refills the stage
+// with the tile kS tiles ahead.  Bytes in flight per SM are set by the
+// stages, not by registers or occupancy, so the bodies can spend registers on
+// arithmetic.
+//
+// Every wait is bounded: thread 0 polls the stage barrier with try_wait and
+// gives up after kWaitNs of %globaltimer, ORs Q_ST_TIMEOUT into the status
+// word, waits (bounded again) for the copies it still has in flight, and
+// the CTA returns.
+#pragma once
+
+#include <cuda.h>
+#include "q_common.cuh"
+
+namespace qk {
+
+constexpr int kEngThreads = 512;
+constexpr int kEngWarps = kEngThreads / 32;
+constexpr int kStages = 3;
+constexpr int kTileRowsE = 128;
+constexpr int kRowBytes = 512;                          // one tile row in shared memory
+constexpr int kTileBytes = kTileRowsE * kRowBytes;      // 64 KiB
+constexpr int kEngSmem = kStages * kTileBytes;          // dynamic shared memory of an engine CTA
+constexpr int32_t kStTimeout = 2;
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
+
+QD uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+QD void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+QD void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+QD void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+QD void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+QD bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return done != 0;
+}
+
+QD unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Poll until the barrier's phase with this parity completes; false after kWaitNs.
+QD bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kWaitNs) return false;
+    }
+}
+
+// One 2-D tile (x = first column in elements, y = first row) into shared memory.
+QD void tma_load_tile(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
+}
+
+QD uint4 lds16(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+QD uint32_t lds4(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
+// Tiles of this CTA: t = blockIdx.x + i * gridDim.x (reversed when `reverse`,
+// so that a second pass over a tensor meets the part the first pass left in
+// L2 first).  body(stage, tm, tk) runs with all threads; it may use
+// __syncthreads() and may overwrite its stage.
+template <class Body>
+__device__ __forceinline__ void run_tiles(const CUtensorMap *tmap, int64_t tiles_m, int64_t tiles_k, int tile_cols,
+                                          bool reverse, int32_t *status, Body &&body)
+{
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    __shared__ __align__(8) uint64_t full[kStages];
+    __shared__ int s_ok;
+
+    const int64_t ntiles = tiles_m * tiles_k;
+    const int64_t count = ntiles > (int64_t)blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    auto tile_of = [&](int64_t i) -> int64_t {
+        const int64_t t = (int64_t)blockIdx.x + i * gridDim.x;
+        return reverse ? ntiles - 1 - t : t;
+    };
+    auto issue = [&](int64_t i, int s) {
+        const int64_t t = tile_of(i);
+        const int64_t tm = t / tiles_k, tk = t - tm * tiles_k;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)kTileBytes);
+        tma_load_tile(dsm + s * kTileBytes, tmap, (int)(tk * tile_cols), (int)(tm * kTileRowsE), &full[s]);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; s++) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int64_t i = 0; i < count && i < kStages; i++) issue(i, (int)i);
+
+    for (int64_t i = 0; i < count; i++) {
+        const int s = (int)(i % kStages);
+        if (threadIdx.x == 0) s_ok = mbar_wait_bounded(&full[s], (uint32_t)((i / kStages) & 1)) ? 1 : 0;
+        __syncthreads();
+        if (!s_ok) {
+            if (threadIdx.x == 0) {
+                if (status != nullptr) atomicOr(status, kStTimeout);
+                // let the copies still in flight land before the CTA's shared memory goes away
+                for (int64_t j = i; j < count && j < i + kStages; j++)
+                    (void)mbar_wait_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1));
+            }
+            return;
+        }
+        const int64_t t = tile_of(i);
+        const int64_t tm = t / tiles_k, tk = t - tm * tiles_k;
+        body(dsm + s * kTileBytes, tm, tk);
+        __syncthreads();
+        if (threadIdx.x == 0 && i + kStages < count) {
+            fence_proxy_async();   // generic-proxy accesses of the stage before the async-proxy refill
+            issue(i + kStages, s);
+        }
+    }
+}
+
+}  // namespace qk

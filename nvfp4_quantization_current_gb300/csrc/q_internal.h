@@ -9,6 +9,11 @@ namespace qk {
 
 int sm_count();
 
+// A 2-D TMA tensor map over a row-major [M, K] input (dtype dt) whose box is
+// 128 rows x 512 bytes (the tile engine's stage).  Fails with
+// cudaErrorNotSupported if the driver entry point is unavailable.
+cudaError_t make_tile_map(void *map /* CUtensorMap, 64-byte aligned */, const void *x, int dt, int64_t M, int64_t K);
+
 // current scaling
 cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *status, cudaStream_t st);
 cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *amax,

@@ -1,0 +1,56 @@
+"""Sharded quantization: the one exchange the quantizers need.
+
+Per-tensor current scaling and NVFP4 use one amax for the whole tensor.
+When the tensor is split across ranks (data-parallel master-weight shards,
+tensor-parallel sequence shards), every rank computes the amax of its own
+shard, the ranks agree on the global amax with a MAX all-reduce of one float,
+and each rank then quantizes its shard with that amax, so that the codes do
+not depend on the split ("FP8 Current Scaling ...", section "Cost and
+multi-GPU use": compute amax, synchronize amax, scale + cast, all-gather;
+"Mixed-precision training: fp16 to fp8", section "FP8 communication", TP:
+the FP8 tensor must be identical with or without TP).
+
+The block-scaled recipes (MXFP8, blockwise, NVFP4 block scales) need no
+exchange when shards split rows on block boundaries.
+
+``allreduce_amax_`` works on any torch.distributed backend (NCCL for CUDA
+tensors, gloo for CPU tensors); the ``quantize_shard_*`` helpers run the
+library's CUDA kernels around it.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+import torch.distributed as dist
+
+
+def allreduce_amax_(amax: torch.Tensor, group=None) -> torch.Tensor:
+    """In-place MAX all-reduce of a one-element FP32 amax.  A no-op when
+    torch.distributed is not initialized (a single rank)."""
+    if amax.numel() != 1 or amax.dtype != torch.float32:
+        raise ValueError("amax must be a one-element float32 tensor")
+    if dist.is_available() and dist.is_initialized():
+        dist.all_reduce(amax, op=dist.ReduceOp.MAX, group=group)
+    return amax
+
+
+def quantize_shard_current_scaling(x_local: torch.Tensor, fmt="e4m3", rowwise=True, colwise=False, group=None,
+                                   status: Optional[torch.Tensor] = None):
+    """Current scaling of this rank's row shard with the amax of the whole
+    (distributed) tensor."""
+    from . import q_amax, q_current_scaling
+    a = q_amax(x_local, status=status)
+    allreduce_amax_(a, group)
+    return q_current_scaling(x_local, fmt, rowwise, colwise, amax=a, status=status)
+
+
+def quantize_shard_nvfp4(x_local: torch.Tensor, blk="1x16", rounding="rn", seed=0, offset=0, rowwise=True,
+                         colwise=False, group=None, status: Optional[torch.Tensor] = None):
+    """NVFP4 of this rank's row shard with the global amax (so the FP32 tensor
+    scale, and therefore every block scale, matches the unsharded tensor).
+    For stochastic rounding pass each rank its own counter ``offset``."""
+    from . import q_amax, q_nvfp4
+    a = q_amax(x_local, status=status)
+    allreduce_amax_(a, group)
+    return q_nvfp4(x_local, blk, rounding, seed, offset, rowwise, colwise, amax=a, status=status)
