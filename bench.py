@@ -50,15 +50,24 @@ REF_BUDGET_S = 120.0
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, keyed by kernel, with the hash of the kernel's source file at
 # capture time; reported as null when the source has changed since.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/k_blockwise_1x128T_bw3_act.md
+    "bw3.act:bw_1x128_T": {"bytes_per_launch": 421391616, "src_hash": "fddd6d313857c53e"},
+    # profiles/k_cs_tiles_e5m2T_hy4_grad.md
+    "hy4.grad:cs_cast_T": {"bytes_per_launch": 415883520, "src_hash": "d12e6156f38966b8"},
+    # profiles/k_mxfp8_mx2_act.md
+    "mx2.act:mxfp8": {"bytes_per_launch": 80156160, "src_hash": "0845a8fdfed6070a"},
+    # profiles/k_nvfp4_1x16_rn_T_nv5_act.md
+    "nv5.act:nvfp4_1x16_rn": {"bytes_per_launch": 70753280, "src_hash": "6643a1db22a5044b"},
+}
 
 
 def src_hash(fname):
-    p = os.path.join(ROOT, "nvfp4_quantization_current_gb300", "csrc", fname)
-    with open(p, "rb") as f:
-        h = hashlib.sha256(f.read())
-    with open(os.path.join(ROOT, "nvfp4_quantization_current_gb300", "csrc", "q_common.cuh"), "rb") as f:
-        h.update(f.read())
+    """Hash of a kernel's source file plus the shared device headers."""
+    h = hashlib.sha256()
+    for name in (fname, "q_common.cuh", "q_engine.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_quantization_current_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -456,19 +465,22 @@ def run_ours(args):
         r["GB/s"] = round(r["bytes"] / (r["us"] * 1e-6) / 1e9, 1)
         r["frac"] = round(r["GB/s"] / peak, 3)
         r["us"] = round(r["us"], 2)
-    # dominant kernel: the largest share of step time
-    dom_name, dom = max(per_kernel.items(), key=lambda kv: kv[1]["us"])
-    dom_bytes = dom["bytes"] / dom["launches"]
-    dom_us = dom["us"] / dom["launches"]
+    # dominant kernel: the single launch with the longest mean time in the step
+    (dci, dpi) = max(kern_ms, key=lambda key: statistics.mean(kern_ms[key]))
+    dcall, dpiece = calls[dci], calls[dci].pieces[dpi]
+    dom_us = statistics.mean(kern_ms[(dci, dpi)]) * 1e3
+    dom_bytes = dpiece[2]
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
-    tr = TRAFFIC.get(dom_name)
+    key = f"{dcall.name.split()[0]}:{dpiece[0]}"
+    tr = TRAFFIC.get(key)
     traffic = None
-    if tr is not None and tr.get("src_hash") == src_hash(dom["src"]):
+    if tr is not None and tr.get("src_hash") == src_hash(dpiece[1]):
         traffic = tr["bytes_per_launch"]
-    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+    roofline = {"bound": "alu" if dpiece[0].endswith("_sr") else "hbm", "kernel": dpiece[0], "call": dcall.name,
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 3), "traffic": traffic,
                 "alg_bytes_per_launch": int(dom_bytes), "us_per_launch": round(dom_us, 2),
-                "share_of_step": round(dom["us"] / (step_ms * 1e3), 3), "peak_kind": peak_kind + " hbm_gbs"}
+                "share_of_step": round(dom_us / (step_ms * 1e3), 3), "peak_kind": peak_kind + " hbm_gbs"}
     # q_amax launches two kernels (zero the word, reduce); every other call one
     n_launches = args.steps * sum((2 if p[0] == "amax" else 1) for c in calls for p in c.pieces)
 

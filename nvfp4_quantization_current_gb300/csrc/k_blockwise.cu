@@ -9,17 +9,17 @@
 // s = 1 / alpha, q = RTNE-saturate(alpha * x).
 //
 // On the tile engine: a 128 x TC tile holds exactly one 128-row block in M
-// and TC/128 blocks in K.
-//  row pass - thread (warp w, lane l): rows 8w..8w+7, 16 bytes each; a
-//             1x128 block spans 128/VEC lanes (xor-shuffle max);
-//  col pass - thread (word column t % 128, 32-row quarter t / 128) reads 32
-//             words; 1x128 (128x1 blocks along M): quarter maxima meet in
-//             shared memory; the codes of each column are produced in
-//             column order and parked in the stage (now free) as
-//             [column][128 rows] with swizzled 16-byte chunks;
-//  copy-out - 8 threads per q_colT row write its 128 bytes.
-// For 128x128 the tile maxima come from the row-pass registers (warp
-// shuffles, then shared memory across the 16 warps).
+// and TC/128 blocks in K; thread (warp w, lane l) holds rows 8w..8w+7 x one
+// 16-byte column chunk in registers.
+//  1x128 rowwise  - a block spans 128/VEC lanes (xor-shuffle max);
+//  128x1 colwise  - per-warp column maxima of the registers meet in shared
+//                   memory, one thread per column reduces them to the
+//                   column's alpha and s; the column-scaled codes of the same
+//                   registers are byte-transposed, parked in the consumed
+//                   stage and written as full 128-byte q_colT rows;
+//  128x128        - the tile maximum comes from warp shuffles and one
+//                   shared-memory reduction across the 16 warps; the
+//                   transposed copy is the same codes byte-transposed.
 #include "q_engine.cuh"
 #include "q_internal.h"
 
@@ -56,10 +56,11 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
                                                               uint8_t *__restrict__ q_colT, float *__restrict__ s_colT,
                                                               int32_t *status)
 {
-    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, LPB = 128 / VEC, CPW = 4 / In<DT>::BYTES;
+    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, LPB = 128 / VEC;
     constexpr int NT = TC / 128;   // 128-column blocks per tile
-    __shared__ uint32_t red[4][TC];
-    __shared__ uint32_t tred[kEngWarps][NT];
+    __shared__ uint4 part[kEngWarps][32];      // 1x128: per-warp column maxima (packed like the input)
+    __shared__ float calpha[TC];               // 1x128: column alphas of the tile
+    __shared__ uint32_t tred[kEngWarps][NT];   // 128x128: per-warp tile maxima
     __shared__ BwScaleTab tab;
     if (DT == BF16 && threadIdx.x < 128) {
         const float a = __fdiv_rn(448.0f, 1.0f + (float)threadIdx.x * (1.0f / 128.0f));
@@ -67,130 +68,114 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
         tab.s[threadIdx.x] = __fdiv_rn(1.0f, a);
     }   // visible after the engine's first barrier
 
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31, wc = t & 127, quarter = t >> 7;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
 
     run_tiles(&tmap, tiles_m, tiles_k, TC, false, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
-        const int64_t k = kb + lane * VEC;
-        float colalpha[CPW];
-        uint32_t w[32];
+        const int64_t k = kb + lane * VEC, m0 = mb + 8 * warp;
+        const bool kok = k < K;
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) v[j] = lds16(st + (8 * warp + j) * kRowBytes + lane * 16);
+        uint32_t code[8][CW];
 
         if constexpr (TILE == 0) {
+            if (q_colT != nullptr) {   // column maxima of this warp's 8 rows
+                uint4 acc = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    acc.x = colmax_word<DT>(acc.x, v[j].x);
+                    acc.y = colmax_word<DT>(acc.y, v[j].y);
+                    acc.z = colmax_word<DT>(acc.z, v[j].z);
+                    acc.w = colmax_word<DT>(acc.w, v[j].w);
+                }
+                part[warp][lane] = acc;
+            }
             // ---------------- 1x128 rowwise ----------------
             if (q_row != nullptr) {
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
-                    const int r = 8 * warp + j;
-                    const uint4 v = lds16(st + r * kRowBytes + lane * 16);
-                    const uint32_t b = group_max<LPB>(absmax_bits<DT>(v));
+                    const uint32_t b = group_max<LPB>(absmax_bits<DT>(v[j]));
                     float alpha, sc;
                     bw_scales<DT>(b, tab, alpha, sc);
                     uint32_t o[CW];
-                    chunk_fp8<DT, E4M3>(v, alpha, o);
-                    if (mb + r < M && k < K) {
-                        uint8_t *dst = q_row + (mb + r) * K + k;
+                    chunk_fp8<DT, E4M3>(v[j], alpha, o);
+                    if (m0 + j < M && kok) {
+                        uint8_t *dst = q_row + (m0 + j) * K + k;
                         if (CW == 2) stg8(dst, o[0], o[CW - 1]);
                         else stg4(dst, o[0]);
                         if (lane % LPB == 0) {
-                            s_row[(mb + r) * (K / 128) + k / 128] = sc;
+                            s_row[(m0 + j) * (K / 128) + k / 128] = sc;
                             flag_nonfinite(status, b);
                         }
                     }
                 }
             }
             if (q_colT == nullptr) return;
-            // ---------------- 128x1 columnwise ----------------
+            __syncthreads();   // partial column maxima posted
+            // ---------------- 128x1 columnwise: one thread per column reduces the 16 partials
+            if (t < TC) {
+                const int q = t / VEC, c = t % VEC;   // lane q of the partials holds this column
+                uint32_t b = 0;
 #pragma unroll
-            for (int r = 0; r < 32; r++) w[r] = lds4(st + (32 * quarter + r) * kRowBytes + wc * 4);
-            {
-                uint32_t bm[CPW];
-                column_absmax<DT, 32>(w, bm);
-#pragma unroll
-                for (int c = 0; c < CPW; c++) red[quarter][wc * CPW + c] = bm[c];
-            }
-            __syncthreads();   // partial maxima visible; every read of the stage is done
-#pragma unroll
-            for (int c = 0; c < CPW; c++) {
-                const int col = wc * CPW + c;
-                const uint32_t b = max(max(red[0][col], red[1][col]), max(red[2][col], red[3][col]));
-                float sc;
-                bw_scales<DT>(b, tab, colalpha[c], sc);
-                if (quarter == 0 && kb + col < K) {
-                    s_colT[(kb + col) * (M / 128) + tm] = sc;
+                for (int w = 0; w < kEngWarps; w++) b = max(b, colmax_bits<DT>(part[w][q], c));
+                float alpha, sc;
+                bw_scales<DT>(b, tab, alpha, sc);
+                calpha[t] = alpha;
+                if (kb + t < K) {
+                    s_colT[(kb + t) * (M / 128) + tm] = sc;
                     flag_nonfinite(status, b);
                 }
             }
-        } else {
-            // ---------------- 128x128: one scale per tile ----------------
-            uint4 v[8];
-            uint32_t b = 0;
+            __syncthreads();   // column alphas visible; every read of the stage is done
+            float ca[VEC];
+#pragma unroll
+            for (int c = 0; c < VEC; c++) ca[c] = calpha[lane * VEC + c];
 #pragma unroll
             for (int j = 0; j < 8; j++) {
-                v[j] = lds16(st + (8 * warp + j) * kRowBytes + lane * 16);
-                b = max(b, absmax_bits<DT>(v[j]));
+                float f[VEC];
+#pragma unroll
+                for (int c = 0; c < VEC; c++) f[c] = elem<DT>(v[j], c);
+#pragma unroll
+                for (int c = 0; c < VEC; c += 2) mul2(f[c], f[c + 1], ca[c], ca[c + 1]);
+#pragma unroll
+                for (int q = 0; q < CW; q++) code[j][q] = cvt_fp8x4<E4M3>(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
             }
+        } else {
+            // ---------------- 128x128: one scale per tile ----------------
+            uint32_t b = 0;
+#pragma unroll
+            for (int j = 0; j < 8; j++) b = max(b, absmax_bits<DT>(v[j]));
             b = group_max<LPB>(b);
             if (lane % LPB == 0) tred[warp][lane / LPB] = b;
-            if (q_colT != nullptr) {
-#pragma unroll
-                for (int r = 0; r < 16; r++) w[r] = lds4(st + (16 * quarter + r) * kRowBytes + wc * 4);
-#pragma unroll
-                for (int r = 0; r < 16; r++) w[16 + r] = lds4(st + (16 * (quarter + 4) + r) * kRowBytes + wc * 4);
-            }
-            __syncthreads();   // tile maxima visible; every read of the stage is done
+            __syncthreads();   // tile maxima posted; every read of the stage is done
             uint32_t bt = 0;
 #pragma unroll
             for (int q = 0; q < kEngWarps; q++) bt = max(bt, tred[q][lane / LPB]);
             float alpha, sc;
             bw_scales<DT>(bt, tab, alpha, sc);
-            if (warp == 0 && lane % LPB == 0 && k < K) {
+            if (warp == 0 && lane % LPB == 0 && kok) {
                 if (s_row != nullptr) s_row[tm * (K / 128) + k / 128] = sc;
                 if (s_colT != nullptr) s_colT[(k / 128) * (M / 128) + tm] = sc;
                 flag_nonfinite(status, bt);
             }
-            if (q_row != nullptr && k < K) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) chunk_fp8<DT, E4M3>(v[j], alpha, code[j]);
+            if (q_row != nullptr && kok) {
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
-                    uint32_t o[CW];
-                    chunk_fp8<DT, E4M3>(v[j], alpha, o);
-                    uint8_t *dst = q_row + (mb + 8 * warp + j) * K + k;
-                    if (CW == 2) stg8(dst, o[0], o[CW - 1]);
-                    else stg4(dst, o[0]);
+                    uint8_t *dst = q_row + (m0 + j) * K + k;
+                    if (CW == 2) stg8(dst, code[j][0], code[j][CW - 1]);
+                    else stg4(dst, code[j][0]);
                 }
             }
             if (q_colT == nullptr) return;
-#pragma unroll
-            for (int c = 0; c < CPW; c++) {
-                const int blk = (wc * CPW + c) / 128;
-                uint32_t bb = 0;
-#pragma unroll
-                for (int q = 0; q < kEngWarps; q++) bb = max(bb, tred[q][blk]);
-                float sc;
-                bw_scales<DT>(bb, tab, colalpha[c], sc);
-            }
         }
-        // ---- columnwise codes, column order, into the stage as [column][128 rows]
-        // (1x128: rows 32*quarter..+31 in w; 128x128: rows 16*quarter..+15 and 16*(quarter+4)..+15)
-#pragma unroll
-        for (int c = 0; c < CPW; c++) {
-            const int col = wc * CPW + c;
-            uint32_t o[8];
-            column_fp8<DT, E4M3, 32>(w, c, colalpha[c], o);
-            const int ch0 = TILE == 0 ? 2 * quarter : quarter, ch1 = TILE == 0 ? 2 * quarter + 1 : quarter + 4;
-            uint8_t *base = st + col * 128;
-            *reinterpret_cast<uint4 *>(base + ((ch0 ^ (wc & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4 *>(base + ((ch1 ^ (wc & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
+        // ---- transposed codes: parked in the consumed stage, then full 128-byte rows
+        park_fp8T<VEC>(st, code, warp, lane);
         __syncthreads();
-#pragma unroll
-        for (int it = 0; it < TC * 8 / kEngThreads; it++) {
-            const int idx = it * kEngThreads + t;
-            const int col = idx >> 3, ch = idx & 7;
-            const int64_t kg = kb + col, mg = mb + ch * 16;
-            if (kg < K && mg < M)
-                stg16(q_colT + kg * M + mg, lds16(st + col * 128 + ((ch ^ ((col / CPW) & 7)) * 16)));
-        }
+        copy_out_fp8T<VEC>(st, q_colT, M, K, mb, kb);
     });
 }
 

@@ -29,13 +29,13 @@ int sm_count()
 }
 
 // ---------------------------------------------------------------------------
-// a1: amax.  Grid-stride 16-byte loads, sixteen in flight per thread, |x|
-// max on bit patterns, warp reduce, CTA reduce, one atomicMax per CTA.
+// a1: amax.  Grid-stride 16-byte loads, eight in flight per thread, |x| max
+// on bit patterns, warp reduce, CTA reduce, one atomicMax per CTA.
 // ---------------------------------------------------------------------------
 constexpr int kAmaxThreads = 256, kAmaxUnroll = 8;
 
 template <int DT>
-__global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict__ x, int64_t n, uint32_t *__restrict__ amax)
+__global__ void __launch_bounds__(kAmaxThreads, 8) k_amax(const void *__restrict__ x, int64_t n, uint32_t *__restrict__ amax)
 {
     constexpr int VEC = In<DT>::VEC;
     const uint4 *xv = static_cast<const uint4 *>(x);
@@ -43,23 +43,10 @@ __global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     uint32_t m = 0;
-    // double-buffered: the next group's eight loads are in flight while this
-    // group is reduced
-    const int64_t span = kAmaxUnroll * stride;
-    if (i + (kAmaxUnroll - 1) * stride < nv) {
-        uint4 a[kAmaxUnroll], b[kAmaxUnroll];
+    for (; i + (kAmaxUnroll - 1) * stride < nv; i += kAmaxUnroll * stride) {
+        uint4 a[kAmaxUnroll];
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; u++) a[u] = ldg_stream(xv + i + u * stride);
-        i += span;
-        while (i + (kAmaxUnroll - 1) * stride < nv) {
-#pragma unroll
-            for (int u = 0; u < kAmaxUnroll; u++) b[u] = ldg_stream(xv + i + u * stride);
-#pragma unroll
-            for (int u = 0; u < kAmaxUnroll; u++) m = max(m, absmax_bits<DT>(a[u]));
-#pragma unroll
-            for (int u = 0; u < kAmaxUnroll; u++) a[u] = b[u];
-            i += span;
-        }
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; u++) m = max(m, absmax_bits<DT>(a[u]));
     }
@@ -134,17 +121,11 @@ __global__ void __launch_bounds__(256) k_cs_cast_flat(const void *__restrict__ x
 }
 
 // ---------------------------------------------------------------------------
-// a3 with the transposed copy, on the tile engine.  Per 128 x TC tile:
-//  row pass  - thread (warp w, lane l) casts rows 8w..8w+7, 16 bytes each,
-//              and stores the codes of q_row straight from registers;
-//  col pass  - thread (word column wc = t % 128, 16-row bands t/128 and
-//              t/128 + 4) reads one 4-byte word per row (CPW columns), casts
-//              the 16 values of each column and parks 16 code bytes per
-//              column in the stage, now free, laid out [column][128 rows] with
-//              16-byte chunks XOR-swizzled by word column;
-//  copy-out  - 8 threads per q_colT row write its 128 bytes.
-// The same codes come out of both passes (one deterministic cast of the same
-// FP32 product).  Requires M % 16 == 0 and K % 16 == 0.
+// a3 with the transposed copy, on the tile engine.  Per 128 x TC tile,
+// thread (warp w, lane l) casts rows 8w..8w+7 of its 16-byte column chunk
+// once; q_row leaves straight from registers, and the same codes, turned
+// around by byte transposes, are parked in the consumed stage and written as
+// full 128-byte q_colT rows.  Requires M % 16 == 0 and K % 16 == 0.
 // ---------------------------------------------------------------------------
 template <int DT, int FMT>
 __global__ void __launch_bounds__(kEngThreads, 1) k_cs_tiles(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
@@ -152,62 +133,36 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_cs_tiles(const __grid_consta
                                                              uint8_t *__restrict__ q_colT, float *__restrict__ scale,
                                                              int32_t *status)
 {
-    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, CPW = 4 / In<DT>::BYTES;
+    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4;
     const float a = *amax;
     const float alpha = alpha_from_amax(Fp8<FMT>::FMAX, a);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         *scale = __fdiv_rn(1.0f, alpha);
         flag_nonfinite(status, __float_as_uint(a) & 0x7FFFFFFFu);
     }
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31, wc = t & 127;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
 
     run_tiles(&tmap, tiles_m, tiles_k, TC, true, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
-        if (q_row != nullptr) {
-            const int64_t k = kb + lane * VEC;
+        const int64_t k = kb + lane * VEC, m0 = mb + 8 * warp;
+        uint32_t code[8][CW];
+#pragma unroll
+        for (int j = 0; j < 8; j++) chunk_fp8<DT, FMT>(lds16(st + (8 * warp + j) * kRowBytes + lane * 16), alpha, code[j]);
+        if (q_row != nullptr && k < K) {
 #pragma unroll
             for (int j = 0; j < 8; j++) {
-                const int r = 8 * warp + j;
-                const uint4 v = lds16(st + r * kRowBytes + lane * 16);
-                uint32_t o[CW];
-                chunk_fp8<DT, FMT>(v, alpha, o);
-                if (mb + r < M && k < K) {
-                    uint8_t *dst = q_row + (mb + r) * K + k;
-                    if (CW == 2) stg8(dst, o[0], o[CW - 1]);
-                    else stg4(dst, o[0]);
-                }
+                if (m0 + j >= M) break;
+                uint8_t *dst = q_row + (m0 + j) * K + k;
+                if (CW == 2) stg8(dst, code[j][0], code[j][CW - 1]);
+                else stg4(dst, code[j][0]);
             }
         }
         if (q_colT == nullptr) return;
-        uint32_t w[2][16];
-#pragma unroll
-        for (int i = 0; i < 2; i++) {
-            const int band = (t >> 7) + 4 * i;
-#pragma unroll
-            for (int r = 0; r < 16; r++) w[i][r] = lds4(st + (16 * band + r) * kRowBytes + wc * 4);
-        }
-        __syncthreads();   // every read of the stage is done: reuse it for the transposed codes
-#pragma unroll
-        for (int i = 0; i < 2; i++) {
-            const int band = (t >> 7) + 4 * i;
-#pragma unroll
-            for (int c = 0; c < CPW; c++) {
-                uint32_t o[4];
-                column_fp8<DT, FMT, 16>(w[i], c, alpha, o);
-                const int col = wc * CPW + c;
-                *reinterpret_cast<uint4 *>(st + col * 128 + ((band ^ (wc & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-        }
+        __syncthreads();   // every read of the stage is done: park the transposed codes in it
+        park_fp8T<VEC>(st, code, warp, lane);
         __syncthreads();
-#pragma unroll
-        for (int it = 0; it < TC * 8 / kEngThreads; it++) {
-            const int idx = it * kEngThreads + t;
-            const int col = idx >> 3, ch = idx & 7;
-            const int64_t kg = kb + col, mg = mb + ch * 16;
-            if (kg < K && mg < M)
-                stg16(q_colT + kg * M + mg, lds16(st + col * 128 + ((ch ^ ((col / CPW) & 7)) * 16)));
-        }
+        copy_out_fp8T<VEC>(st, q_colT, M, K, mb, kb);
     });
 }
 

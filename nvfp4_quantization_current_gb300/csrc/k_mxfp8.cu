@@ -7,15 +7,15 @@
 // Scale code = clamp(floor(log2 b) - emax + 127, 0, 254), emax = 8 (E4M3) or
 // 15 (E5M2), b = 0 -> 127; q = RTNE-saturate(x * 2^(127 - code)).
 //
-// On the tile engine (128 x TC tiles in shared memory):
-//  row pass - thread (warp w, lane l) handles rows 8w..8w+7, 16 bytes each;
-//             a 1x32 block spans 32/VEC lanes (xor-shuffle max); codes and
-//             scales go to global memory straight from registers;
-//  col pass - thread (word column t % 128, 32-row block t / 128) reads the
-//             32 words of its block, reduces each of its CPW columns, writes
-//             the E8M0 codes, and parks the element codes in the stage (now
-//             free) as a row-major [128][TC] byte tile;
-//  copy-out - 16-byte row segments of q_col.
+// On the tile engine (128 x TC tiles in shared memory): thread (warp w,
+// lane l) holds rows 8w..8w+7 x one 16-byte column chunk in registers.
+//  row pass - a 1x32 block spans 32/VEC lanes (xor-shuffle max);
+//  col pass - each warp reduces its 8 rows per column in registers; the four
+//             warps of a 32-row block meet in shared memory (one barrier);
+//             the column-scaled codes of the same registers are stored in the
+//             [M, K] layout.
+// Both outputs leave straight from registers, 256 contiguous bytes per warp
+// and row.
 #include "q_engine.cuh"
 #include "q_internal.h"
 
@@ -27,97 +27,94 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8(const __grid_constant_
                                                           uint8_t *__restrict__ q_col, uint8_t *__restrict__ e_col,
                                                           int32_t *status)
 {
-    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, LPB = 32 / VEC, CPW = 4 / In<DT>::BYTES;
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31, wc = t & 127, band = t >> 7;
+    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, LPB = 32 / VEC;
+    __shared__ uint4 part[kEngWarps][32];   // per-warp column maxima over 8 rows (packed like the input)
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
 
     run_tiles(&tmap, tiles_m, tiles_k, TC, false, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
-        if (q_row != nullptr) {
-            const int64_t k = kb + lane * VEC;
+        const int64_t k = kb + lane * VEC, m0 = mb + 8 * warp;
+        const bool kok = k < K;
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) v[j] = lds16(st + (8 * warp + j) * kRowBytes + lane * 16);
+
+        if (q_col != nullptr) {   // column maxima of this warp's 8 rows, before the row pass
+            uint4 acc = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int j = 0; j < 8; j++) {
-                const int r = 8 * warp + j;
-                const uint4 v = lds16(st + r * kRowBytes + lane * 16);
-                const uint32_t b = group_max<LPB>(absmax_bits<DT>(v));
+                acc.x = colmax_word<DT>(acc.x, v[j].x);
+                acc.y = colmax_word<DT>(acc.y, v[j].y);
+                acc.z = colmax_word<DT>(acc.z, v[j].z);
+                acc.w = colmax_word<DT>(acc.w, v[j].w);
+            }
+            part[warp][lane] = acc;
+        }
+        if (q_row != nullptr) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const uint32_t b = group_max<LPB>(absmax_bits<DT>(v[j]));
                 const uint32_t code = mx_code<FMT>(b);
-                const float inv = mx_inv_scale(code);
                 uint32_t o[CW];
-                chunk_fp8<DT, FMT>(v, inv, o);
-                if (mb + r < M && k < K) {
-                    uint8_t *dst = q_row + (mb + r) * K + k;
+                chunk_fp8<DT, FMT>(v[j], mx_inv_scale(code), o);
+                if (m0 + j < M && kok) {
+                    uint8_t *dst = q_row + (m0 + j) * K + k;
                     if (CW == 2) stg8(dst, o[0], o[CW - 1]);
                     else stg4(dst, o[0]);
                     if (lane % LPB == 0) {
-                        e_row[(mb + r) * (K / 32) + k / 32] = (uint8_t)code;
+                        e_row[(m0 + j) * (K / 32) + k / 32] = (uint8_t)code;
                         flag_nonfinite(status, b);
                     }
                 }
             }
         }
         if (q_col == nullptr) return;
-        // ---- 32x1 blocks: one block of CPW columns per thread
-        uint32_t w[32];
+        __syncthreads();   // the four warps of each 32-row block have posted their maxima
+        // ---- 32x1 blocks: the block of this warp is rows 32*(warp/4) .. +31
+        const int w0 = warp & ~3;
+        uint4 cm = part[w0][lane];
 #pragma unroll
-        for (int r = 0; r < 32; r++) w[r] = lds4(st + (32 * band + r) * kRowBytes + wc * 4);
-        float inv[CPW];
-        uint32_t codes = 0, bm[CPW];
-        column_absmax<DT, 32>(w, bm);
-#pragma unroll
-        for (int c = 0; c < CPW; c++) {
-            const uint32_t b = bm[c];
-            const uint32_t code = mx_code<FMT>(b);
-            inv[c] = mx_inv_scale(code);
-            codes |= code << (8 * c);
-            if (kb + wc * CPW < K && mb + 32 * band < M) flag_nonfinite(status, b);
+        for (int q = 1; q < 4; q++) {
+            const uint4 o4 = part[w0 + q][lane];
+            cm.x = colmax_word<DT>(cm.x, o4.x);
+            cm.y = colmax_word<DT>(cm.y, o4.y);
+            cm.z = colmax_word<DT>(cm.z, o4.z);
+            cm.w = colmax_word<DT>(cm.w, o4.w);
         }
-        const int64_t kg = kb + wc * CPW;
-        if (kg < K && mb + 32 * band < M) {
-            uint8_t *dst = e_col + (tm * 4 + band) * K + kg;
-            if (CPW == 2) *reinterpret_cast<uint16_t *>(dst) = (uint16_t)codes;
-            else *dst = (uint8_t)codes;
+        float inv[VEC];
+        uint32_t codes[VEC];
+#pragma unroll
+        for (int c = 0; c < VEC; c++) {
+            const uint32_t b = colmax_bits<DT>(cm, c);
+            codes[c] = mx_code<FMT>(b);
+            inv[c] = mx_inv_scale(codes[c]);
+            if ((warp & 3) == 0 && kok && m0 < M) flag_nonfinite(status, b);
         }
-        __syncthreads();   // every read of the stage is done: reuse it as a [128][TC] code tile
+        if ((warp & 3) == 0 && kok && m0 < M) {
+            uint32_t sw[CW];
 #pragma unroll
-        for (int r = 0; r < 32; r += 4) {
-            if (CPW == 2) {
-                // rows r..r+3 x 2 columns -> two words of (row r c0, row r c1, row r+1 c0, row r+1 c1)
-                float f[8];
+            for (int q = 0; q < CW; q++)
+                sw[q] = codes[4 * q] | (codes[4 * q + 1] << 8) | (codes[4 * q + 2] << 16) | (codes[4 * q + 3] << 24);
+            uint8_t *dst = e_col + (m0 / 32) * K + k;
+            if (CW == 2) stg8(dst, sw[0], sw[CW - 1]);
+            else stg4(dst, sw[0]);
+        }
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    f[2 * q] = word_elem<DT>(w[r + q], 0);
-                    f[2 * q + 1] = word_elem<DT>(w[r + q], 1);
-                    mul2(f[2 * q], f[2 * q + 1], inv[0], inv[CPW - 1]);
-                }
-                const uint32_t p0 = cvt_fp8x4<FMT>(f[0], f[1], f[2], f[3]);
-                const uint32_t p1 = cvt_fp8x4<FMT>(f[4], f[5], f[6], f[7]);
-                uint8_t *base = st + (32 * band + r) * TC + wc * 2;
-                *reinterpret_cast<uint16_t *>(base) = (uint16_t)p0;
-                *reinterpret_cast<uint16_t *>(base + TC) = (uint16_t)(p0 >> 16);
-                *reinterpret_cast<uint16_t *>(base + 2 * TC) = (uint16_t)p1;
-                *reinterpret_cast<uint16_t *>(base + 3 * TC) = (uint16_t)(p1 >> 16);
-            } else {
-                float f[4];
+        for (int j = 0; j < 8; j++) {
+            float f[VEC];
 #pragma unroll
-                for (int q = 0; q < 4; q++) f[q] = word_elem<DT>(w[r + q], 0);
-                mul2(f[0], f[1], inv[0], inv[0]);
-                mul2(f[2], f[3], inv[0], inv[0]);
-                const uint32_t p = cvt_fp8x4<FMT>(f[0], f[1], f[2], f[3]);
-                uint8_t *base = st + (32 * band + r) * TC + wc;
-                base[0] = (uint8_t)p;
-                base[TC] = (uint8_t)(p >> 8);
-                base[2 * TC] = (uint8_t)(p >> 16);
-                base[3 * TC] = (uint8_t)(p >> 24);
+            for (int c = 0; c < VEC; c++) f[c] = elem<DT>(v[j], c);
+#pragma unroll
+            for (int c = 0; c < VEC; c += 2) mul2(f[c], f[c + 1], inv[c], inv[c + 1]);
+            uint32_t o[CW];
+#pragma unroll
+            for (int q = 0; q < CW; q++) o[q] = cvt_fp8x4<FMT>(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+            if (m0 + j < M && kok) {
+                uint8_t *dst = q_col + (m0 + j) * K + k;
+                if (CW == 2) stg8(dst, o[0], o[CW - 1]);
+                else stg4(dst, o[0]);
             }
-        }
-        __syncthreads();
-        constexpr int SEGS = TC / 16;   // 16-byte segments per code row
-#pragma unroll
-        for (int it = 0; it < kTileRowsE * SEGS / kEngThreads; it++) {
-            const int idx = it * kEngThreads + t;
-            const int r = idx / SEGS, sg = idx % SEGS;
-            const int64_t m = mb + r, k = kb + 16 * sg;
-            if (m < M && k < K) stg16(q_col + m * K + k, lds16(st + r * TC + 16 * sg));
         }
     });
 }

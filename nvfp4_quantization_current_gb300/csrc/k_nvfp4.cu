@@ -13,18 +13,17 @@
 // q = E2M1(x * enc).
 //
 // On the tile engine (the amax comes from the preceding amax pass or the
-// caller; tiles are walked backwards for L2 reuse):
-//  row pass - thread (warp w, lane l): rows 8w..8w+7, 16 bytes each; a 1x16
-//             block spans 16/VEC lanes; stochastic rounding draws one
-//             Philox block (8 elements) per thread and row;
-//  col pass - 1x16: thread (word column t % 128, 16-row bands t/128 and
-//             t/128 + 4) reads 16 words and quantizes the CPW column blocks
-//             it holds entirely (two Philox blocks per column for SR);
-//             16x16: the row codes, kept in shared memory, are turned around
-//             with 8x8 nibble transposes;
-//             either way 8 code bytes per column block are parked in the
-//             stage (now free) as [column][64 bytes], 8-byte chunks swizzled;
-//  copy-out - 8 threads per q_colT row.
+// caller; tiles are walked backwards for L2 reuse), thread (warp w, lane l)
+// holds rows 8w..8w+7 x one 16-byte column chunk in registers.
+//  1x16 rowwise - a block spans 16/VEC lanes; stochastic rounding draws one
+//                 Philox block (8 elements) per thread and row;
+//  16x1 colwise - a block is the 8 rows of warps 2p and 2p+1: their column
+//                 maxima meet in shared memory; each column's 8 values are
+//                 encoded into one word of row nibbles (SR: one Philox block
+//                 per column), parked in the consumed stage and written as
+//                 q_colT rows;
+//  16x16        - the block maximum spans 2 warps x 16/VEC lanes; the
+//                 transposed copy is the row codes nibble-transposed.
 #include <cstring>
 
 #include "q_engine.cuh"
@@ -90,6 +89,32 @@ QD uint32_t nv_row_codes(const uint4 &v, float enc, uint64_t seed, uint64_t offs
     return cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
 
+// Transposed FP4 codes of a tile: col[c] holds, for column c of this
+// thread's chunk, the 8 codes of rows 8w..8w+7 (row 8w in bits 3-0).  They
+// are parked at [column][64 bytes] in the consumed stage (4-byte slot w,
+// XOR-swizzled by lane) and written as q_colT rows by copy_out_fp4T.
+template <int VEC> QD void park_fp4T(uint8_t *stage, const uint32_t *col, int warp, int lane)
+{
+#pragma unroll
+    for (int c = 0; c < VEC; c++)
+        *reinterpret_cast<uint32_t *>(stage + (lane * VEC + c) * 64 + ((warp ^ (lane & 15)) * 4)) = col[c];
+}
+
+template <int VEC>
+QD void copy_out_fp4T(const uint8_t *stage, uint8_t *q_colT, int64_t M, int64_t K, int64_t mb, int64_t kb)
+{
+    constexpr int TC = 32 * VEC;
+#pragma unroll
+    for (int it = 0; it < TC * 16 / kEngThreads; it++) {
+        const int idx = it * kEngThreads + threadIdx.x;
+        const int col = idx >> 4, sl = idx & 15;   // slot sl = rows 8sl..8sl+7 of the tile
+        const int64_t kg = kb + col, mg = mb + 8 * sl;
+        if (kg < K && mg < M)
+            stg4(q_colT + kg * (M / 2) + mg / 2,
+                 *reinterpret_cast<const uint32_t *>(stage + col * 64 + ((sl ^ ((col / VEC) & 15)) * 4)));
+    }
+}
+
 template <int DT, int BLK, int RND>
 __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
                                                           const float *__restrict__ amax, uint64_t seed, uint64_t offset,
@@ -97,13 +122,12 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                                                           uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
                                                           float *__restrict__ s_global, int32_t *status)
 {
-    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, LPB = 16 / VEC, CPW = 4 / In<DT>::BYTES;
-    constexpr int RB = TC / 2;   // packed code bytes per tile row
-    __shared__ uint8_t sSB[8][TC];                       // 1x16 columnwise block scales of a tile
-    __shared__ uint32_t bred[kEngWarps][TC / 16];        // 16x16: half-block maxima
-    __shared__ __align__(16) uint8_t sC[BLK == 1 ? kTileRowsE * RB : 16];   // 16x16: row codes of a tile
-
+    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, LPB = 16 / VEC;
     __shared__ float enc_tab[128];
+    __shared__ uint4 part[kEngWarps][32];        // 1x16: per-warp column maxima over 8 rows
+    __shared__ uint8_t sSB[8][TC];               // 1x16: columnwise block scales of a tile
+    __shared__ uint32_t bred[kEngWarps][TC / 16];   // 16x16: half-block maxima
+
     const float A = *amax;
     const float alpha_g = alpha_from_amax(2688.0f, A);
     if (threadIdx.x < 128) {
@@ -115,30 +139,41 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
         flag_nonfinite(status, __float_as_uint(A) & 0x7FFFFFFFu);
     }
     if (M == 0 || K == 0) return;
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31, wc = t & 127;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
-    // 8-byte chunk swizzle of the parked codes, chosen so that the writers of
-    // each variant (a word column per lane, or 8 columns per lane) and the
-    // copy-out spread over the banks
-    auto swz = [](int col) { return BLK == 0 ? (col / CPW) & 7 : (col >> 3) & 7; };
 
     run_tiles(&tmap, tiles_m, tiles_k, TC, true, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
-        const int64_t k = kb + lane * VEC;
+        const int64_t k = kb + lane * VEC, m0 = mb + 8 * warp;
+        const bool kok = k < K;
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) v[j] = lds16(st + (8 * warp + j) * kRowBytes + lane * 16);
+        uint32_t colw[8];   // transposed codes: column c -> 8 row nibbles
+
         if constexpr (BLK == 0) {
+            if (q_colT != nullptr) {   // column maxima of this warp's 8 rows
+                uint4 acc = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    acc.x = colmax_word<DT>(acc.x, v[j].x);
+                    acc.y = colmax_word<DT>(acc.y, v[j].y);
+                    acc.z = colmax_word<DT>(acc.z, v[j].z);
+                    acc.w = colmax_word<DT>(acc.w, v[j].w);
+                }
+                part[warp][lane] = acc;
+            }
             // ---------------- 1x16 rowwise ----------------
             if (q_row != nullptr) {
-#pragma unroll 2
+#pragma unroll
                 for (int j = 0; j < 8; j++) {
-                    const int r = 8 * warp + j;
-                    const int64_t m = mb + r;
-                    const uint4 v = lds16(st + r * kRowBytes + lane * 16);
-                    const uint32_t b = group_max<LPB>(absmax_bits<DT>(v));
+                    const int64_t m = m0 + j;
+                    const uint32_t b = group_max<LPB>(absmax_bits<DT>(v[j]));
                     uint32_t sb;
                     float enc;
                     nv_block_scale(b, alpha_g, enc_tab, sb, enc);
-                    const uint32_t code = nv_row_codes<DT, RND>(v, enc, seed, offset, m * K + k);
-                    if (m < M && k < K) {
+                    const uint32_t code = nv_row_codes<DT, RND>(v[j], enc, seed, offset, m * K + k);
+                    if (m < M && kok) {
                         uint8_t *dst = q_row + m * (K / 2) + k / 2;
                         if (VEC == 8) stg4(dst, code);
                         else *reinterpret_cast<uint16_t *>(dst) = (uint16_t)code;
@@ -150,118 +185,79 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                 }
             }
             if (q_colT == nullptr) return;
-            // ---------------- 16x1 columnwise ----------------
-            uint32_t w[2][16];
-#pragma unroll
-            for (int i = 0; i < 2; i++) {
-                const int band = (t >> 7) + 4 * i;
-#pragma unroll
-                for (int r = 0; r < 16; r++) w[i][r] = lds4(st + (16 * band + r) * kRowBytes + wc * 4);
+            __syncthreads();   // partial maxima posted; every read of the stage is done
+            // ---------------- 16x1 columnwise: warps 2p, 2p+1 share a block ----------------
+            uint4 cm = part[warp][lane];
+            {
+                const uint4 o4 = part[warp ^ 1][lane];
+                cm.x = colmax_word<DT>(cm.x, o4.x);
+                cm.y = colmax_word<DT>(cm.y, o4.y);
+                cm.z = colmax_word<DT>(cm.z, o4.z);
+                cm.w = colmax_word<DT>(cm.w, o4.w);
             }
-            __syncthreads();   // every read of the stage is done: reuse it for the transposed codes
+            float enc[VEC];
 #pragma unroll
-            for (int i = 0; i < 2; i++) {
-                const int band = (t >> 7) + 4 * i;
-                const int64_t m0 = mb + 16 * band;
-                uint32_t bm[CPW];
-                column_absmax<DT, 16>(w[i], bm);
-#pragma unroll
-                for (int c = 0; c < CPW; c++) {
-                    const int col = wc * CPW + c;
-                    const int64_t kg = kb + col;
-                    const uint32_t b = bm[c];
-                    uint32_t sb;
-                    float enc;
-                    nv_block_scale(b, alpha_g, enc_tab, sb, enc);
-                    float y[16];
-#pragma unroll
-                    for (int r = 0; r < 16; r++) y[r] = word_elem<DT>(w[i][r], c);
-#pragma unroll
-                    for (int r = 0; r < 16; r += 2) mul2(y[r], y[r + 1], enc, enc);
-                    if (RND == 1) {
-                        const uint64_t g = offset + (uint64_t)((kg * M + m0) >> 3);   // kg*M + m0 is a multiple of 16
-                        const uint4 R0 = sr_bits(seed, g, 1u), R1 = sr_bits(seed, g + 1u, 1u);
-#pragma unroll
-                        for (int r = 0; r < 8; r++) {
-                            y[r] = sr_e2m1_value(y[r], r16_of(R0, r));
-                            y[r + 8] = sr_e2m1_value(y[r + 8], r16_of(R1, r));
-                        }
-                    }
-                    const uint32_t lo = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-                    const uint32_t hi = cvt_fp4x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
-                    *reinterpret_cast<uint2 *>(st + col * 64 + ((band ^ swz(col)) * 8)) = make_uint2(lo, hi);
-                    sSB[band][col] = (uint8_t)sb;
-                    if (kg < K && m0 < M) flag_nonfinite(status, b);
+            for (int c = 0; c < VEC; c++) {
+                const uint32_t b = colmax_bits<DT>(cm, c);
+                uint32_t sb;
+                nv_block_scale(b, alpha_g, enc_tab, sb, enc[c]);
+                if ((warp & 1) == 0) {
+                    sSB[warp >> 1][lane * VEC + c] = (uint8_t)sb;
+                    if (kok && m0 < M) flag_nonfinite(status, b);
                 }
+            }
+            // each column's 8 rows with its factor: one E2M1 word per column (row 8w in bits 3-0)
+#pragma unroll
+            for (int c = 0; c < VEC; c++) {
+                float y[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) y[j] = elem<DT>(v[j], c);
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) mul2(y[j], y[j + 1], enc[c], enc[c]);
+                if (RND == 1) {
+                    // elements (k + c) * M + m0 .. + 7 of stream 1: one Philox block
+                    const uint4 R = sr_bits(seed, offset + (uint64_t)(((k + c) * M + m0) >> 3), 1u);
+#pragma unroll
+                    for (int j = 0; j < 8; j++) y[j] = sr_e2m1_value(y[j], r16_of(R, j));
+                }
+                colw[c] = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
             }
         } else {
             // ---------------- 16x16: one scale per tile ----------------
-            uint4 v[8];
             uint32_t b = 0;
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                v[j] = lds16(st + (8 * warp + j) * kRowBytes + lane * 16);
-                b = max(b, absmax_bits<DT>(v[j]));
-            }
+            for (int j = 0; j < 8; j++) b = max(b, absmax_bits<DT>(v[j]));
             b = group_max<LPB>(b);
             if (lane % LPB == 0) bred[warp][lane / LPB] = b;
-            __syncthreads();   // half-block maxima visible; every read of the stage is done
+            __syncthreads();   // half-block maxima posted; every read of the stage is done
             b = max(bred[warp & ~1][lane / LPB], bred[warp | 1][lane / LPB]);
             uint32_t sb;
             float enc;
             nv_block_scale(b, alpha_g, enc_tab, sb, enc);
             const int64_t m16 = mb + 16 * (warp >> 1);
-            if ((warp & 1) == 0 && lane % LPB == 0 && m16 < M && k < K) {
+            if ((warp & 1) == 0 && lane % LPB == 0 && m16 < M && kok) {
                 if (sb_row != nullptr) sb_row[(m16 / 16) * (K / 16) + k / 16] = (uint8_t)sb;
                 if (sb_colT != nullptr) sb_colT[(k / 16) * (M / 16) + m16 / 16] = (uint8_t)sb;
                 flag_nonfinite(status, b);
             }
 #pragma unroll
             for (int j = 0; j < 8; j++) {
-                const int r = 8 * warp + j;
-                const int64_t m = mb + r;
+                const int64_t m = m0 + j;
                 const uint32_t code = nv_row_codes<DT, RND>(v[j], enc, seed, offset, m * K + k);
-                if (q_row != nullptr && m < M && k < K) {
+                if (q_row != nullptr && m < M && kok) {
                     uint8_t *dst = q_row + m * (K / 2) + k / 2;
                     if (VEC == 8) stg4(dst, code);
                     else *reinterpret_cast<uint16_t *>(dst) = (uint16_t)code;
                 }
-                if (VEC == 8) *reinterpret_cast<uint32_t *>(sC + r * RB + lane * 4) = code;
-                else *reinterpret_cast<uint16_t *>(sC + r * RB + lane * 2) = (uint16_t)code;
+                colw[j] = code;
             }
             if (q_colT == nullptr) return;
-            __syncthreads();   // row codes of the tile visible
-            // items: (8-column group g, 16-row band); read 16 words (8 nibbles each), transpose
-            constexpr int NG = TC / 8;
-            if (t < NG * 8) {
-                const int g = t % NG, band = t / NG;
-                uint32_t lo[8], hi[8];
-#pragma unroll
-                for (int r = 0; r < 8; r++) {
-                    lo[r] = *reinterpret_cast<const uint32_t *>(sC + (16 * band + r) * RB + 4 * g);
-                    hi[r] = *reinterpret_cast<const uint32_t *>(sC + (16 * band + 8 + r) * RB + 4 * g);
-                }
-                transpose8x8_nibbles(lo);
-                transpose8x8_nibbles(hi);
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const int col = 8 * g + j;
-                    *reinterpret_cast<uint2 *>(st + col * 64 + ((band ^ swz(col)) * 8)) = make_uint2(lo[j], hi[j]);
-                }
-            }
+            transpose8x8_nibbles(colw);
         }
+        // ---- transposed codes: parked in the consumed stage, then q_colT rows
+        park_fp4T<VEC>(st, colw, warp, lane);
         __syncthreads();
-        // transposed codes: 8 threads per q_colT row, one 8-byte chunk (16 rows of m) each
-#pragma unroll
-        for (int it = 0; it < TC * 8 / kEngThreads; it++) {
-            const int idx = it * kEngThreads + t;
-            const int col = idx >> 3, ch = idx & 7;
-            const int64_t kg = kb + col, mg = mb + ch * 16;
-            if (kg < K && mg < M) {
-                const uint2 val = *reinterpret_cast<const uint2 *>(st + col * 64 + ((ch ^ swz(col)) * 8));
-                stg8(q_colT + kg * (M / 2) + mg / 2, val.x, val.y);
-            }
-        }
+        copy_out_fp4T<VEC>(st, q_colT, M, K, mb, kb);
         if constexpr (BLK == 0) {
             const int64_t left = (M - mb) / 16;
             const int nb = left < 8 ? (int)left : 8;

@@ -83,6 +83,44 @@ QD void tma_load_tile(void *dst, const CUtensorMap *map, int x, int y, uint64_t 
 QD uint4 lds16(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 QD uint32_t lds4(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
+// Transposed FP8 codes of a tile, staged for full-line writes: each thread
+// holds 8 rows (8w..8w+7) x VEC columns of codes, as VEC/4 words per row
+// (byte c = column c).  4x4 byte transposes turn them into 8 bytes per column,
+// parked at [column][128 rows] in `stage` with the 8-byte chunks XOR-swizzled
+// by lane; after a barrier, copy_out_fp8T writes 128-byte q_colT rows.
+template <int VEC> QD void park_fp8T(uint8_t *stage, const uint32_t (*code)[VEC / 4], int warp, int lane)
+{
+#pragma unroll
+    for (int q = 0; q < VEC / 4; q++) {
+        uint32_t lo[4], hi[4];
+        transpose4x4(code[0][q], code[1][q], code[2][q], code[3][q], lo[0], lo[1], lo[2], lo[3]);
+        transpose4x4(code[4][q], code[5][q], code[6][q], code[7][q], hi[0], hi[1], hi[2], hi[3]);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int col = lane * VEC + 4 * q + i;
+            *reinterpret_cast<uint2 *>(stage + col * 128 + ((warp ^ (lane & 15)) * 8)) = make_uint2(lo[i], hi[i]);
+        }
+    }
+}
+
+// Writes the parked [TC][128] code tile as q_colT rows (16 threads x 8 bytes
+// per 128-byte row).
+template <int VEC>
+QD void copy_out_fp8T(const uint8_t *stage, uint8_t *q_colT, int64_t M, int64_t K, int64_t mb, int64_t kb)
+{
+    constexpr int TC = 32 * VEC;
+#pragma unroll
+    for (int it = 0; it < TC * 16 / kEngThreads; it++) {
+        const int idx = it * kEngThreads + threadIdx.x;
+        const int col = idx >> 4, ch = idx & 15;
+        const int64_t kg = kb + col, mg = mb + 8 * ch;
+        if (kg < K && mg < M) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(stage + col * 128 + ((ch ^ ((col / VEC) & 15)) * 8));
+            stg8(q_colT + kg * M + mg, v.x, v.y);
+        }
+    }
+}
+
 // Tiles of this CTA: t = blockIdx.x + i * gridDim.x (reversed when `reverse`,
 // so that a second pass over a tensor meets the part the first pass left in
 // L2 first).  body(stage, tm, tk) runs with all threads; it may use
