@@ -93,25 +93,30 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
                 part[warp][lane] = acc;
             }
             // ---------------- 1x128 rowwise ----------------
+            uint32_t nf = 0;
             if (q_row != nullptr) {
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const uint32_t b = group_max<LPB>(absmax_bits<DT>(v[j]));
-                    float alpha, sc;
-                    bw_scales<DT>(b, tab, alpha, sc);
-                    uint32_t o[CW];
-                    chunk_fp8<DT, E4M3>(v[j], alpha, o);
-                    if (m0 + j < M && kok) {
-                        uint8_t *dst = q_row + (m0 + j) * K + k;
-                        if (CW == 2) stg8(dst, o[0], o[CW - 1]);
-                        else stg4(dst, o[0]);
-                        if (lane % LPB == 0) {
-                            s_row[(m0 + j) * (K / 128) + k / 128] = sc;
-                            flag_nonfinite(status, b);
+                for (int j = 0; j < 8; j += 2) {
+                    uint32_t bb[2] = {absmax_bits<DT>(v[j]), absmax_bits<DT>(v[j + 1])};
+                    group_max2<DT, LPB>(bb[0], bb[1]);
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        float alpha, sc;
+                        bw_scales<DT>(bb[h], tab, alpha, sc);
+                        uint32_t o[CW];
+                        chunk_fp8<DT, E4M3>(v[j + h], alpha, o);
+                        const bool ok = m0 + j + h < M && kok;
+                        if (ok) {
+                            uint8_t *dst = q_row + (m0 + j + h) * K + k;
+                            if (CW == 2) stg8(dst, o[0], o[CW - 1]);
+                            else stg4(dst, o[0]);
                         }
+                        if (ok && lane % LPB == 0) s_row[(m0 + j + h) * (K / 128) + k / 128] = sc;
+                        nf |= ok ? nonfinite(bb[h]) : 0u;
                     }
                 }
             }
+            post_nonfinite(status, nf);
             if (q_colT == nullptr) return;
             __syncthreads();   // partial column maxima posted
             // ---------------- 128x1 columnwise: one thread per column reduces the 16 partials

@@ -35,7 +35,7 @@ int sm_count()
 constexpr int kAmaxThreads = 256, kAmaxUnroll = 8;
 
 template <int DT>
-__global__ void __launch_bounds__(kAmaxThreads, 8) k_amax(const void *__restrict__ x, int64_t n, uint32_t *__restrict__ amax)
+__global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict__ x, int64_t n, uint32_t *__restrict__ amax)
 {
     constexpr int VEC = In<DT>::VEC;
     const uint4 *xv = static_cast<const uint4 *>(x);

@@ -51,25 +51,32 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8(const __grid_constant_
             }
             part[warp][lane] = acc;
         }
+        uint32_t nf = 0;   // non-finite block maxima seen by this thread
         if (q_row != nullptr) {
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const uint32_t b = group_max<LPB>(absmax_bits<DT>(v[j]));
-                const uint32_t code = mx_code<FMT>(b);
-                uint32_t o[CW];
-                chunk_fp8<DT, FMT>(v[j], mx_inv_scale(code), o);
-                if (m0 + j < M && kok) {
-                    uint8_t *dst = q_row + (m0 + j) * K + k;
-                    if (CW == 2) stg8(dst, o[0], o[CW - 1]);
-                    else stg4(dst, o[0]);
-                    if (lane % LPB == 0) {
-                        e_row[(m0 + j) * (K / 32) + k / 32] = (uint8_t)code;
-                        flag_nonfinite(status, b);
+            for (int j = 0; j < 8; j += 2) {
+                uint32_t bb[2] = {absmax_bits<DT>(v[j]), absmax_bits<DT>(v[j + 1])};
+                group_max2<DT, LPB>(bb[0], bb[1]);
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const uint32_t code = mx_code<FMT>(bb[h]);
+                    uint32_t o[CW];
+                    chunk_fp8<DT, FMT>(v[j + h], mx_inv_scale(code), o);
+                    const bool ok = m0 + j + h < M && kok;
+                    if (ok) {
+                        uint8_t *dst = q_row + (m0 + j + h) * K + k;
+                        if (CW == 2) stg8(dst, o[0], o[CW - 1]);
+                        else stg4(dst, o[0]);
                     }
+                    if (ok && lane % LPB == 0) e_row[(m0 + j + h) * (K / 32) + k / 32] = (uint8_t)code;
+                    nf |= ok ? nonfinite(bb[h]) : 0u;
                 }
             }
         }
-        if (q_col == nullptr) return;
+        if (q_col == nullptr) {
+            post_nonfinite(status, nf);
+            return;
+        }
         __syncthreads();   // the four warps of each 32-row block have posted their maxima
         // ---- 32x1 blocks: the block of this warp is rows 32*(warp/4) .. +31
         const int w0 = warp & ~3;
@@ -89,8 +96,9 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8(const __grid_constant_
             const uint32_t b = colmax_bits<DT>(cm, c);
             codes[c] = mx_code<FMT>(b);
             inv[c] = mx_inv_scale(codes[c]);
-            if ((warp & 3) == 0 && kok && m0 < M) flag_nonfinite(status, b);
+            nf |= ((warp & 3) == 0 && kok && m0 < M) ? nonfinite(b) : 0u;
         }
+        post_nonfinite(status, nf);
         if ((warp & 3) == 0 && kok && m0 < M) {
             uint32_t sw[CW];
 #pragma unroll

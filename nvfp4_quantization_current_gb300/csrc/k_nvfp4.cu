@@ -31,15 +31,29 @@
 
 namespace qk {
 
-// Block scale code sb = E4M3(RN(RN(b * alpha_g) / 6)) (b = 0 -> 1.0) and the
-// encode factor enc = alpha_g / f(sb) (0 when f(sb) = 0).  enc depends only
-// on the code, so each CTA tabulates alpha_g / f(c) for the 128 positive
-// codes once (enc_tab[0x38] = alpha_g covers b = 0).
-QD void nv_block_scale(uint32_t b, float alpha_g, const float *enc_tab, uint32_t &sb, float &enc)
+// Block scale code sb = E4M3(RN(RN(b * alpha_g) / 6)) (b = 0 -> 0x38, 1.0).
+// For BF16 inputs b = (1 + m/128) 2^(E-127); writing alpha_g = a_m 2^ae with
+// a_m in [1, 2), RN(RN(b alpha_g) / 6) = RN(RN((1 + m/128) a_m) / 6)
+// 2^(E-127+ae) while the values stay normal (rounding commutes with
+// power-of-two scaling), so it is a per-CTA 128-entry table plus an exponent
+// shift; anything that would fall below 2^-126 encodes to E4M3 +0 either way.
+// FP32 inputs and subnormal or non-finite b take the two operations.
+template <int DT> QD uint32_t nv_sb_code(uint32_t b, float alpha_g, const uint32_t *T1, int ae)
 {
-    sb = b == 0 ? 0x38u : e4m3_code(__fdiv_rn(__fmul_rn(__uint_as_float(b), alpha_g), 6.0f));
-    enc = enc_tab[sb];
+    if (b == 0) return 0x38u;
+    const uint32_t E = b >> 23;
+    if (DT == BF16 && E != 0u && E != 255u) {
+        const uint32_t t = T1[(b >> 16) & 0x7Fu];
+        const int ne = (int)(t >> 23) + (int)E - 127 + ae;
+        if (ne <= 0) return 0u;
+        return e4m3_code(__uint_as_float((t & 0x807FFFFFu) | ((uint32_t)ne << 23)));
+    }
+    return e4m3_code(__fdiv_rn(__fmul_rn(__uint_as_float(b), alpha_g), 6.0f));
 }
+
+// The encode factor enc = alpha_g / f(sb) (0 when f(sb) = 0) depends only on
+// the code: each CTA tabulates it for the 128 positive codes (enc_tab[0x38]
+// = alpha_g also serves b = 0).
 
 // 16 random bits for element e (0..7) of a Philox block.
 QD uint32_t r16_of(const uint4 &R, int e) { return (word(R, e >> 1) >> (16 * (e & 1))) & 0xFFFFu; }
@@ -124,15 +138,21 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
 {
     constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, LPB = 16 / VEC;
     __shared__ float enc_tab[128];
+    __shared__ uint32_t sb_tab[128];             // BF16: RN(RN((1 + m/128) a_m) / 6) per mantissa m
     __shared__ uint4 part[kEngWarps][32];        // 1x16: per-warp column maxima over 8 rows
     __shared__ uint8_t sSB[8][TC];               // 1x16: columnwise block scales of a tile
     __shared__ uint32_t bred[kEngWarps][TC / 16];   // 16x16: half-block maxima
 
     const float A = *amax;
     const float alpha_g = alpha_from_amax(2688.0f, A);
+    const uint32_t ag = __float_as_uint(alpha_g);
+    const int ae = (int)(ag >> 23) - 127;   // alpha_g is always a normal float
     if (threadIdx.x < 128) {
         const float sv = e4m3_value(threadIdx.x);
         enc_tab[threadIdx.x] = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_g, sv);
+        const float a_m = __uint_as_float((ag & 0x807FFFFFu) | (127u << 23));
+        sb_tab[threadIdx.x] = __float_as_uint(
+            __fdiv_rn(__fmul_rn(1.0f + (float)threadIdx.x * (1.0f / 128.0f), a_m), 6.0f));
     }   // visible after the engine's first barrier
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         *s_global = __fdiv_rn(1.0f, alpha_g);
@@ -164,26 +184,29 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                 part[warp][lane] = acc;
             }
             // ---------------- 1x16 rowwise ----------------
+            uint32_t nf = 0;
             if (q_row != nullptr) {
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const int64_t m = m0 + j;
-                    const uint32_t b = group_max<LPB>(absmax_bits<DT>(v[j]));
-                    uint32_t sb;
-                    float enc;
-                    nv_block_scale(b, alpha_g, enc_tab, sb, enc);
-                    const uint32_t code = nv_row_codes<DT, RND>(v[j], enc, seed, offset, m * K + k);
-                    if (m < M && kok) {
-                        uint8_t *dst = q_row + m * (K / 2) + k / 2;
-                        if (VEC == 8) stg4(dst, code);
-                        else *reinterpret_cast<uint16_t *>(dst) = (uint16_t)code;
-                        if (lane % LPB == 0) {
-                            sb_row[m * (K / 16) + k / 16] = (uint8_t)sb;
-                            flag_nonfinite(status, b);
+                for (int j = 0; j < 8; j += 2) {
+                    uint32_t bb[2] = {absmax_bits<DT>(v[j]), absmax_bits<DT>(v[j + 1])};
+                    group_max2<DT, LPB>(bb[0], bb[1]);
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const int64_t m = m0 + j + h;
+                        const uint32_t sb = nv_sb_code<DT>(bb[h], alpha_g, sb_tab, ae);
+                        const uint32_t code = nv_row_codes<DT, RND>(v[j + h], enc_tab[sb], seed, offset, m * K + k);
+                        const bool ok = m < M && kok;
+                        if (ok) {
+                            uint8_t *dst = q_row + m * (K / 2) + k / 2;
+                            if (VEC == 8) stg4(dst, code);
+                            else *reinterpret_cast<uint16_t *>(dst) = (uint16_t)code;
                         }
+                        if (ok && lane % LPB == 0) sb_row[m * (K / 16) + k / 16] = (uint8_t)sb;
+                        nf |= ok ? nonfinite(bb[h]) : 0u;
                     }
                 }
             }
+            post_nonfinite(status, nf);
             if (q_colT == nullptr) return;
             __syncthreads();   // partial maxima posted; every read of the stage is done
             // ---------------- 16x1 columnwise: warps 2p, 2p+1 share a block ----------------
@@ -196,16 +219,16 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                 cm.w = colmax_word<DT>(cm.w, o4.w);
             }
             float enc[VEC];
+            uint32_t nfc = 0;
 #pragma unroll
             for (int c = 0; c < VEC; c++) {
                 const uint32_t b = colmax_bits<DT>(cm, c);
-                uint32_t sb;
-                nv_block_scale(b, alpha_g, enc_tab, sb, enc[c]);
-                if ((warp & 1) == 0) {
-                    sSB[warp >> 1][lane * VEC + c] = (uint8_t)sb;
-                    if (kok && m0 < M) flag_nonfinite(status, b);
-                }
+                const uint32_t sb = nv_sb_code<DT>(b, alpha_g, sb_tab, ae);
+                enc[c] = enc_tab[sb];
+                if ((warp & 1) == 0) sSB[warp >> 1][lane * VEC + c] = (uint8_t)sb;
+                nfc |= ((warp & 1) == 0 && kok && m0 < M) ? nonfinite(b) : 0u;
             }
+            post_nonfinite(status, nfc);
             // each column's 8 rows with its factor: one E2M1 word per column (row 8w in bits 3-0)
 #pragma unroll
             for (int c = 0; c < VEC; c++) {
@@ -231,9 +254,8 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
             if (lane % LPB == 0) bred[warp][lane / LPB] = b;
             __syncthreads();   // half-block maxima posted; every read of the stage is done
             b = max(bred[warp & ~1][lane / LPB], bred[warp | 1][lane / LPB]);
-            uint32_t sb;
-            float enc;
-            nv_block_scale(b, alpha_g, enc_tab, sb, enc);
+            const uint32_t sb = nv_sb_code<DT>(b, alpha_g, sb_tab, ae);
+            const float enc = enc_tab[sb];
             const int64_t m16 = mb + 16 * (warp >> 1);
             if ((warp & 1) == 0 && lane % LPB == 0 && m16 < M && kok) {
                 if (sb_row != nullptr) sb_row[(m16 / 16) * (K / 16) + k / 16] = (uint8_t)sb;

@@ -78,35 +78,75 @@ template <> QD float elem<BF16>(const uint4 &v, int j)
 }
 template <> QD float elem<F32>(const uint4 &v, int j) { return __uint_as_float(word(v, j)); }
 
-// |x| bit patterns compare like the magnitudes they encode (finite values,
-// then inf, then NaN), so maxima are taken on integers.
-// absmax_bits: FP32 bit pattern of the largest |element| of the vector.
+// |x| maxima.  Packed BF16 pairs use max.NaN.xorsign.abs.bf16x2 (one FP-pipe
+// instruction for two magnitudes; the result's sign bits are the XOR of the
+// inputs' and are masked off where a value is read).  NaN propagates as the
+// canonical NaN, whose bit pattern exceeds every finite value and inf.
+QD uint32_t hmax_abs2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+QD float fmax_abs(float a, float b)
+{
+    float r;
+    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// absmax_bits: FP32 bit pattern of the largest |element| of the vector
+// (non-negative FP32 bit patterns compare like the magnitudes they encode).
 template <int DT> QD uint32_t absmax_bits(const uint4 &v);
 template <> QD uint32_t absmax_bits<BF16>(const uint4 &v)
 {
-    const uint32_t M = 0x7FFF7FFFu;
-    uint32_t m = __vmaxu2(__vmaxu2(v.x & M, v.y & M), __vmaxu2(v.z & M, v.w & M));
-    return max(m << 16, m & 0xFFFF0000u);
+    uint32_t m = hmax_abs2(hmax_abs2(v.x, v.y), hmax_abs2(v.z, v.w));
+    m = hmax_abs2(m, __byte_perm(m, 0u, 0x1032));   // both halves now hold the maximum
+    return (m << 16) & 0x7FFF0000u;
 }
 template <> QD uint32_t absmax_bits<F32>(const uint4 &v)
 {
-    const uint32_t M = 0x7FFFFFFFu;
-    return max(max(v.x & M, v.y & M), max(v.z & M, v.w & M));
+    const float m = fmax_abs(fmax_abs(__uint_as_float(v.x), __uint_as_float(v.y)),
+                             fmax_abs(__uint_as_float(v.z), __uint_as_float(v.w)));
+    return __float_as_uint(m) & 0x7FFFFFFFu;
 }
 
-// Per-column running maximum of |x| over rows, kept in the input's packing:
-// BF16 packs two columns per word (max with __vmaxu2), FP32 one per word.
+// Per-column running maximum of |x| over rows, kept in the input's packing
+// (BF16: two columns per word; FP32: one), sign bits undefined.
 template <int DT> QD uint32_t colmax_word(uint32_t acc, uint32_t w);
-template <> QD uint32_t colmax_word<BF16>(uint32_t acc, uint32_t w) { return __vmaxu2(acc, w & 0x7FFF7FFFu); }
-template <> QD uint32_t colmax_word<F32>(uint32_t acc, uint32_t w) { return max(acc, w & 0x7FFFFFFFu); }
+template <> QD uint32_t colmax_word<BF16>(uint32_t acc, uint32_t w) { return hmax_abs2(acc, w); }
+template <> QD uint32_t colmax_word<F32>(uint32_t acc, uint32_t w)
+{
+    return __float_as_uint(fmax_abs(__uint_as_float(acc), __uint_as_float(w)));
+}
 // FP32 bits of column j's maximum from the packed accumulators.
 template <int DT> QD uint32_t colmax_bits(const uint4 &acc, int j);
 template <> QD uint32_t colmax_bits<BF16>(const uint4 &acc, int j)
 {
-    uint32_t w = word(acc, j >> 1);
-    return (j & 1) ? (w & 0xFFFF0000u) : (w << 16);
+    const uint32_t w = word(acc, j >> 1);
+    return ((j & 1) ? w : (w << 16)) & 0x7FFF0000u;
 }
-template <> QD uint32_t colmax_bits<F32>(const uint4 &acc, int j) { return word(acc, j); }
+template <> QD uint32_t colmax_bits<F32>(const uint4 &acc, int j) { return word(acc, j) & 0x7FFFFFFFu; }
+
+// Maxima of two rows over groups of G consecutive lanes with one shuffle
+// chain: BF16 magnitudes (the high halves of their FP32 bit patterns) travel
+// packed in one word.  FP32 runs two chains.
+template <int DT, int G> QD void group_max2(uint32_t &a, uint32_t &b)
+{
+    if (DT == BF16) {
+        uint32_t p = __byte_perm(a, b, 0x7632);   // a's magnitude low, b's high
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) p = hmax_abs2(p, __shfl_xor_sync(0xFFFFFFFFu, p, o));
+        a = (p << 16) & 0x7FFF0000u;
+        b = p & 0x7FFF0000u;
+    } else {
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) {
+            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+            b = max(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
+        }
+    }
+}
 
 // ---------------------------------------------------------------------------
 // conversions (PTX cvt; RTNE, saturating to the largest finite value)
@@ -280,21 +320,15 @@ QD float alpha_from_amax(float fmax, float a)
     return al;
 }
 
-// floor(log2 b) for the FP32 bit pattern b of a positive value, exact:
-// normals from the exponent field, subnormals from the leading one of the
-// mantissa; inf / NaN give 128 (exponent field 255).
-QD int floor_log2_bits(uint32_t b)
-{
-    uint32_t E = b >> 23;
-    if (E == 0) return (31 - __clz(b & 0x7FFFFFu)) - 149;
-    return (int)E - 127;
-}
-
-// E8M0 code for a block whose largest magnitude has FP32 bits b.
+// E8M0 code for a block whose largest magnitude has FP32 bits b:
+// clamp(floor(log2 b) - emax + 127, 0, 254), b = 0 -> 127.  For a normal b,
+// floor(log2 b) + 127 is the exponent field E, so the code is E - emax; a
+// subnormal b (E = 0) clamps to 0 either way, and inf / NaN (E = 255) give
+// 255 - emax, the same as floor(log2) = 128.
 template <int FMT> QD uint32_t mx_code(uint32_t b)
 {
     if (b == 0) return 127u;
-    int c = floor_log2_bits(b) - Fp8<FMT>::EMAX + 127;
+    int c = (int)(b >> 23) - Fp8<FMT>::EMAX;
     c = c < 0 ? 0 : (c > 254 ? 254 : c);
     return (uint32_t)c;
 }
@@ -365,6 +399,12 @@ template <int G> QD uint32_t group_max(uint32_t v)
 QD void flag_nonfinite(int32_t *status, uint32_t amax_bits)
 {
     if (status != nullptr && amax_bits >= 0x7F800000u) atomicOr(status, kStNonFinite);
+}
+// Thread-local record of non-finite maxima, posted once (see post_nonfinite).
+QD uint32_t nonfinite(uint32_t amax_bits) { return amax_bits >= 0x7F800000u ? 1u : 0u; }
+QD void post_nonfinite(int32_t *status, uint32_t seen)
+{
+    if (seen && status != nullptr) atomicOr(status, kStNonFinite);
 }
 
 // 4x4 byte transpose: in r[i] byte j = element (row i, col j);
