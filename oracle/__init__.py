@@ -83,6 +83,7 @@ def _L():
             "or_dq_current_scaling": (None, [P, F, I64, I64, I, I, P]),
             "or_mxfp8": (None, [P, I, I64, I64, I, P, P, P, P]),
             "or_dq_mxfp8": (None, [P, P, I64, I64, I, I, I, P]),
+            "or_mxfp8_requant_col": (None, [P, P, I64, I64, I, P, P]),
             "or_blockwise": (None, [P, I, I64, I64, I, P, P, P, P]),
             "or_dq_blockwise": (None, [P, P, I64, I64, I, I, P]),
             "or_nvfp4_global": (None, [F, P, P]),
@@ -270,6 +271,17 @@ def dq_mxfp8(q, e8m0, fmt=E4M3, direction=ROW, out=F32):
     y = np.empty((R, C), np.float32 if out == F32 else np.uint16)
     _L().or_dq_mxfp8(_p(q), _p(e8m0), R, C, fmt, direction, out, _p(y))
     return y
+
+
+def mxfp8_requant_col(q_row, e8m0_row, fmt=E4M3):
+    """Columnwise MXFP8 of the rowwise dequantization (the re-quantize step)."""
+    q_row = np.ascontiguousarray(q_row, np.uint8)
+    e8m0_row = np.ascontiguousarray(e8m0_row, np.uint8)
+    M, K = q_row.shape
+    q_col = np.empty((M, K), np.uint8)
+    e_col = np.empty((M // 32, K), np.uint8)
+    _L().or_mxfp8_requant_col(_p(q_row), _p(e8m0_row), M, K, fmt, _p(q_col), _p(e_col))
+    return q_col, e_col
 
 
 @dataclass

@@ -51,6 +51,7 @@
 #include <stdint.h>
 #include <stddef.h>
 #include <string.h>
+#include <stdlib.h>
 
 /* ------------------------------------------------------------------------ */
 /* Input widening                                                            */
@@ -507,6 +508,23 @@ void or_dq_mxfp8(const uint8_t *q, const uint8_t *e8m0, int64_t R, int64_t C, in
             float v = dec_fmt8(q[r * C + c], fmt) * or_dec_e8m0(code);
             store_y(y, out_dtype, r * C + c, v);
         }
+}
+
+/*
+ * Re-quantize MXFP8 rowwise data in the other direction ([MP] "FP8
+ * communication", EP: only the rowwise FP8 copy travels, a dequantize and
+ * re-quantize (in the other direction) kernel makes the columnwise copy; with
+ * power-of-two scales it matches direct columnwise quantization except for
+ * special values such as subnormals).  Written as its definition: the
+ * rowwise dequantization x_hat (FP32) followed by columnwise MXFP8 of x_hat.
+ */
+void or_mxfp8_requant_col(const uint8_t *q_row, const uint8_t *e8m0_row, int64_t M, int64_t K, int fmt,
+                          uint8_t *q_col, uint8_t *e8m0_col)
+{
+    float *xh = (float *)malloc((size_t)(M * K > 0 ? M * K : 1) * sizeof(float));
+    or_dq_mxfp8(q_row, e8m0_row, M, K, fmt, 0, OR_F32, xh);
+    or_mxfp8(xh, OR_F32, M, K, fmt, NULL, NULL, q_col, e8m0_col);
+    free(xh);
 }
 
 /* ------------------------------------------------------------------------ */

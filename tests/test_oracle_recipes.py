@@ -410,3 +410,38 @@ def test_nv_sr_uses_row_and_column_indices():
     yt = (np.ascontiguousarray(x.T) * np.repeat(encc, 16, axis=1)).astype(np.float32)
     wantc = O.sr_e2m1_batch(yt.ravel(), seed=99, offset=5, stream=1).reshape(32, 16)
     assert np.array_equal(O.unpack_e2m1(r.q_colT, 16), wantc)
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 row -> col re-quantization
+# ---------------------------------------------------------------------------
+
+def test_mx_requant_exact_on_grid_inputs():
+    """Inputs that both directions represent exactly (signed powers of two
+    spanning 8 binades, every 32-element block and 32-row block holding a
+    2^7) dequantize exactly, so re-quantizing the rowwise copy gives the
+    direct columnwise quantization bit for bit."""
+    rng = np.random.default_rng(21)
+    k = rng.integers(0, 8, (64, 96))
+    x = (np.where(rng.random((64, 96)) < 0.5, -1.0, 1.0) * 2.0 ** k).astype(np.float32)
+    x[np.arange(64), (np.arange(64) * 7) % 96] = 128.0          # a 2^7 in every row block ...
+    for mb in range(2):
+        x[mb * 32 + (np.arange(96) % 32), np.arange(96)] = 128.0  # ... and in every column block
+    for fmt in (O.E4M3, O.E5M2):
+        r = O.mxfp8(x, fmt)
+        assert np.array_equal(O.dq_mxfp8(r.q_row, r.e8m0_row, fmt, O.ROW), x)
+        q_col, e_col = O.mxfp8_requant_col(r.q_row, r.e8m0_row, fmt)
+        assert np.array_equal(q_col, r.q_col) and np.array_equal(e_col, r.e8m0_col)
+
+
+def test_mx_requant_close_to_direct_columnwise():
+    x = W.gen("lognormal_rows", (128, 128), 8, bf16=True)
+    r = O.mxfp8(x)
+    q_col, e_col = O.mxfp8_requant_col(r.q_row, r.e8m0_row)
+    assert np.mean(q_col == r.q_col) > 0.95 and np.mean(e_col == r.e8m0_col) > 0.95
+    # both decode to within the two quantizations' error of x: each step is off by at
+    # most 1/16 (1/8 where a value in [448, 512) saturated) relative
+    d1 = O.dq_mxfp8(q_col, e_col, O.E4M3, O.COL)
+    xf = W.bf16_bits_to_f32(x)
+    big = np.abs(dec8(r.q_col)) >= 2.0 ** -6
+    assert np.all((np.abs(d1 - xf) <= np.abs(xf) * (1 / 8 + 1 / 8 * 9 / 8) + 1e-30)[big])
