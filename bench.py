@@ -4,7 +4,7 @@ pages' workloads.
 
 One step = one pass of every recipe over its full-size tensors (all five
 workloads of ``workloads.WORKLOADS``): current-scaling amax + cast (+ the
-transposed copy), MXFP8 row + col, blockwise 1x128 (+ transposed) and
+transposed copy), MXFP8 row + col and the row->col re-quantize, blockwise 1x128 (+ transposed) and
 128x128 (+ transposed), NVFP4 1x16 RTNE, 1x16 stochastic rounding and 16x16,
 and the dequantizer of each.  Every call goes through the C ABI with
 preallocated outputs.
@@ -128,6 +128,11 @@ def build_step(dev_tensors, torch, Q):
         run = lambda: Q.q_mxfp8(x, "e4m3", True, True, out=out)
         calls.append(Call(f"{tag} mxfp8_e4m3 row+col", "mxfp8", [("mxfp8", "k_mxfp8.cu", b, run)], [x],
                           [out.q_row, out.e8m0_row, out.q_col, out.e8m0_col], run))
+        rq = Q.alloc_mxfp8(x.shape[0], x.shape[1], x.device, "e4m3", False, True)
+        rrun = lambda: Q.q_mxfp8_requant_col(out.q_row, out.e8m0_row, "e4m3", out=rq)
+        calls.append(Call(f"{tag} mxfp8_requant row->col", "mxfp8",
+                          [("mxfp8_requant", "k_mxfp8.cu", nbytes(out.q_row, out.e8m0_row, rq.q_col, rq.e8m0_col),
+                            rrun)], [out.q_row, out.e8m0_row], [rq.q_col, rq.e8m0_col], rrun))
         for direction, q, e in ((Q.Q_ROW, out.q_row, out.e8m0_row), (Q.Q_COL, out.q_col, out.e8m0_col)):
             y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
             r = (lambda q=q, e=e, direction=direction, y=y: Q.dq_mxfp8(q, e, "e4m3", direction, torch.bfloat16, out=y))
@@ -239,6 +244,10 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
             eq(host(g.e8m0_row[r0:r0 + rows]), w.e8m0_row, f"{wl}.{tn} e8m0_row band")
             eq(host(g.q_col[r0:r0 + rows]), w.q_col, f"{wl}.{tn} q_col band")
             eq(host(g.e8m0_col[r0 // 32:(r0 + rows) // 32]), w.e8m0_col, f"{wl}.{tn} e8m0_col band")
+            rq = Q.q_mxfp8_requant_col(g.q_row, g.e8m0_row)
+            wq, we = O.mxfp8_requant_col(w.q_row, w.e8m0_row)
+            eq(host(rq.q_col[r0:r0 + rows]), wq, f"{wl}.{tn} requant q_col band")
+            eq(host(rq.e8m0_col[r0 // 32:(r0 + rows) // 32]), we, f"{wl}.{tn} requant e8m0_col band")
         elif kind == "bw1":
             g = Q.q_blockwise(xd, "1x128", True, True)
             w = O.blockwise(xs, O.T1x128, True, True)
@@ -543,7 +552,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy; see workloads.WORKLOADS)",
             "config": {"workload": "all five workloads at full size per step: cs1 FP32 1024x1024 CS-E4M3+T; "
-                                   "mx2 BF16 8192x4096 MXFP8 row+col; bw3 BF16 16384x7168 1x128+T and 7168x18432 "
+                                   "mx2 BF16 8192x4096 MXFP8 row+col, row->col requant; bw3 BF16 16384x7168 1x128+T and 7168x18432 "
                                    "128x128+T; hy4 BF16 8192x14336 CS-E5M2+T and 14336x4096 CS-E4M3+T; nv5 BF16 "
                                    "8192x4096 NVFP4 1x16 RN+T, 1x16 SR+T, 4096x4096 16x16 RN+T; each with a dequant",
                        "l2": "flushed (256 MiB write) before every timed call",
@@ -597,6 +606,7 @@ def oracle_sample_work(host_t, frac):
         M, K = s.shape
         work.append((lambda: O.mxfp8(s), s.nbytes + 2 * M * K + M * K // 16))
         r = O.mxfp8(s)
+        work.append((lambda: O.mxfp8_requant_col(r.q_row, r.e8m0_row), 2 * M * K + M * K // 16))
         work.append((lambda: O.dq_mxfp8(r.q_row, r.e8m0_row, O.E4M3, O.ROW, O.BF16), M * K * 3 + M * K // 32))
         work.append((lambda: O.dq_mxfp8(r.q_col, r.e8m0_col, O.E4M3, O.COL, O.BF16), M * K * 3 + M * K // 32))
 

@@ -127,6 +127,23 @@ q_status q_mxfp8(const void *x, q_dtype in, int64_t M, int64_t K, q_fp8 fmt,
                  int32_t *status, q_stream_t stream);
 
 /*
+ * MXFP8 rowwise codes -> columnwise codes ([MP] "FP8 communication", EP:
+ * only the rowwise FP8 copy crosses the expert-parallel all-to-all, and a
+ * de-quantize + re-quantize kernel in the other direction gives the
+ * columnwise copy for the backward pass).  x_hat = q_row * 2^(e_row - 127)
+ * in FP32, then q_col / e8m0_col of x_hat exactly as q_mxfp8 computes them
+ * (32x1 blocks along M).  Power-of-two block scales make the result close
+ * to direct columnwise quantization of the original tensor (equal wherever
+ * the rowwise codes lost no bits that the columnwise codes keep).
+ *   q_row [M, K] codes, e8m0_row [M, K/32] (as written by q_mxfp8);
+ *   q_col [M, K] codes, e8m0_col [M/32, K] (written).  fmt is the format of
+ *   both.  e8m0 code 255 (NaN) decodes to NaN and is reported in *status.
+ * Shapes: M % 32 == 0, K % 32 == 0.  Reads the codes once (TMA tiles).
+ */
+q_status q_mxfp8_requant_col(const uint8_t *q_row, const uint8_t *e8m0_row, int64_t M, int64_t K, q_fp8 fmt,
+                             uint8_t *q_col, uint8_t *e8m0_col, int32_t *status, q_stream_t stream);
+
+/*
  * a6/a7: DeepSeek-V3-like blockwise FP8 ([MP] recipe 4 and "Blockwise
  * scaling"): E4M3 only, FP32 scale per tile, formed like the per-tensor
  * scale on the tile: alpha_b = 448 / b, s_b = 1 / alpha_b.

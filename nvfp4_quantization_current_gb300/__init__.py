@@ -15,6 +15,8 @@ Recipes (each with its dequantizer, rowwise and columnwise outputs):
   section "Current Scaling");
 * :func:`q_mxfp8` -- 1x32 blocks with E8M0 scales ("Mixed-precision
   training: fp16 to fp8", section "MXFP8");
+* :func:`q_mxfp8_requant_col` -- MXFP8 rowwise codes to columnwise codes
+  (dequantize + re-quantize, same page, "FP8 communication");
 * :func:`q_blockwise` -- DeepSeek-V3-like 1x128 / 128x128 FP32-scaled E4M3
   (same page, recipe 4);
 * :func:`q_nvfp4` -- E2M1 with E4M3 1x16 / 16x16 block scales and an FP32
@@ -55,6 +57,7 @@ SIGNATURES = {
     "q_amax": (_I, [_P, _I, _I64, _P, _P, _P]),
     "q_current_scaling": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P]),
     "q_mxfp8": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
+    "q_mxfp8_requant_col": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
     "q_blockwise": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "q_nvfp4": (_I, [_P, _I, _I64, _I64, _I, _I, _U64, _U64, _P, _P, _P, _P, _P, _I, _P, _P, _P]),
     "dq_current_scaling": (_I, [_P, _P, _I64, _I64, _I, _I, _P, _P]),
@@ -220,6 +223,20 @@ def q_mxfp8(x: torch.Tensor, fmt="e4m3", rowwise=True, colwise=True, out: Option
     out = alloc_mxfp8(M, K, x.device, fmt, rowwise, colwise) if out is None else out
     _call("q_mxfp8", _ptr(x), dt, M, K, out.fmt, _ptr(out.q_row), _ptr(out.e8m0_row), _ptr(out.q_col),
           _ptr(out.e8m0_col), _ptr(status), _stream(x.device))
+    return out
+
+
+def q_mxfp8_requant_col(q_row: torch.Tensor, e8m0_row: torch.Tensor, fmt="e4m3", out: Optional[MXFP8Tensor] = None,
+                        status: Optional[torch.Tensor] = None) -> MXFP8Tensor:
+    """Columnwise MXFP8 codes and scales from the rowwise ones: each element is
+    dequantized with its 1x32 row-block scale and re-quantized in 32x1 column
+    blocks.  Returns an MXFP8Tensor with only the columnwise half set (or
+    fills ``out.q_col`` / ``out.e8m0_col``)."""
+    M, K = q_row.shape
+    if out is None:
+        out = alloc_mxfp8(M, K, q_row.device, fmt, rowwise=False, colwise=True)
+    _call("q_mxfp8_requant_col", _ptr(q_row), _ptr(e8m0_row), M, K, _fmt(fmt), _ptr(out.q_col), _ptr(out.e8m0_col),
+          _ptr(status), _stream(q_row.device))
     return out
 
 

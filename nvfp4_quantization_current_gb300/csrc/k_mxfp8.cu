@@ -127,6 +127,127 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8(const __grid_constant_
     });
 }
 
+// ---------------------------------------------------------------------------
+// Rowwise MXFP8 codes -> columnwise MXFP8 codes ("Mixed-precision training:
+// fp16 to fp8", section "FP8 communication", EP: only the rowwise copy
+// travels; a dequantize and re-quantize in the other direction makes the
+// columnwise copy).  x_hat = code * 2^(e_row - 127) (one exact FP32
+// product), then 32x1 blocks of x_hat as in k_mxfp8.  On the tile engine over
+// the code matrix: a stage is 128 rows x 512 codes, thread (warp w, lane l)
+// covers rows 8w..8w+7 x codes 16l..16l+15; x_hat is formed twice from the
+// stage (once for the column maxima, which meet across the 4 warps of a
+// 32-row block in shared memory, once for the codes) instead of being held
+// in registers.
+// ---------------------------------------------------------------------------
+template <int FMT> QD void dq16(const uint4 &c, float f, float *x)
+{
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const uint32_t wd = word(c, q);
+        const float2 a = fp8x2_to_f32<FMT>(wd & 0xFFFFu), b = fp8x2_to_f32<FMT>(wd >> 16);
+        x[4 * q] = a.x;
+        x[4 * q + 1] = a.y;
+        x[4 * q + 2] = b.x;
+        x[4 * q + 3] = b.y;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) mul2(x[i], x[i + 1], f, f);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8_requant(const __grid_constant__ CUtensorMap tmap, int64_t M,
+                                                                  int64_t K, const uint8_t *__restrict__ e_row,
+                                                                  uint8_t *__restrict__ q_col, uint8_t *__restrict__ e_col,
+                                                                  int32_t *status)
+{
+    constexpr int TC = 512;   // codes per tile row
+    __shared__ uint32_t part[kEngWarps][16][32];   // per warp, column, lane: |x_hat| maxima over 8 rows
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
+
+    // the tensor map counts 2-byte elements: a tile is 256 of them per row
+    run_tiles(&tmap, tiles_m, tiles_k, TC / 2, false, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
+        const int64_t mb = tm * kTileRowsE, kb = tk * TC;
+        const int64_t k = kb + lane * 16, m0 = mb + 8 * warp;
+        const bool kok = k < K;
+        const uint8_t *srow = st + (8 * warp) * kRowBytes + lane * 16;
+        float fr[8];   // 2^(e_row - 127) of each row's 1x32 block (code 255 -> NaN)
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const uint32_t er = (m0 + j < M && kok) ? e_row[(m0 + j) * (K / 32) + k / 32] : 0u;
+            fr[j] = er == 255u ? __uint_as_float(0x7FC00000u) : er == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(er << 23);
+        }
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) acc[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            float x[16];
+            dq16<FMT>(lds16(srow + j * kRowBytes), fr[j], x);
+#pragma unroll
+            for (int i = 0; i < 16; i++) acc[i] = fmax_abs(acc[i], x[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i++) part[warp][i][lane] = __float_as_uint(acc[i]) & 0x7FFFFFFFu;
+        __syncthreads();   // the four warps of each 32-row block have posted their maxima
+        const int w0 = warp & ~3;
+        float inv[16];
+        uint32_t code[16], nf = 0;
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const uint32_t b = max(max(part[w0][i][lane], part[w0 + 1][i][lane]), max(part[w0 + 2][i][lane], part[w0 + 3][i][lane]));
+            code[i] = mx_code<FMT>(b);
+            inv[i] = mx_inv_scale(code[i]);
+            nf |= nonfinite(b);
+        }
+        if ((warp & 3) == 0 && kok && m0 < M) {
+            uint32_t sw[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                sw[q] = code[4 * q] | (code[4 * q + 1] << 8) | (code[4 * q + 2] << 16) | (code[4 * q + 3] << 24);
+            stg16(e_col + (m0 / 32) * K + k, make_uint4(sw[0], sw[1], sw[2], sw[3]));
+            post_nonfinite(status, nf);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            float x[16];
+            dq16<FMT>(lds16(srow + j * kRowBytes), fr[j], x);
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) mul2(x[i], x[i + 1], inv[i], inv[i + 1]);
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) o[q] = cvt_fp8x4<FMT>(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            if (m0 + j < M && kok) stg16(q_col + (m0 + j) * K + k, make_uint4(o[0], o[1], o[2], o[3]));
+        }
+    });
+}
+
+template <int FMT>
+static cudaError_t mx_requant_t(const uint8_t *q_row, const uint8_t *e_row, int64_t M, int64_t K, uint8_t *q_col,
+                                uint8_t *e_col, int32_t *status, cudaStream_t st)
+{
+    alignas(64) CUtensorMap map;
+    cudaError_t e = make_tile_map(&map, q_row, U8, M, K);
+    if (e != cudaSuccess) return e;
+    static bool attr = false;
+    if (!attr) {
+        e = cudaFuncSetAttribute(k_mxfp8_requant<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + 511) / 512);
+    const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+    k_mxfp8_requant<FMT><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, e_row, q_col, e_col, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp8_requant_col(const uint8_t *q_row, const uint8_t *e_row, int64_t M, int64_t K, int fmt,
+                                     uint8_t *q_col, uint8_t *e_col, int32_t *status, cudaStream_t st)
+{
+    return fmt == E4M3 ? mx_requant_t<E4M3>(q_row, e_row, M, K, q_col, e_col, status, st)
+                       : mx_requant_t<E5M2>(q_row, e_row, M, K, q_col, e_col, status, st);
+}
+
 template <int DT, int FMT>
 static cudaError_t mx_t(const void *x, int64_t M, int64_t K, uint8_t *q_row, uint8_t *e_row, uint8_t *q_col,
                         uint8_t *e_col, int32_t *status, cudaStream_t st)

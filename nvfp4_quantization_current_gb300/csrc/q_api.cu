@@ -146,6 +146,23 @@ q_status q_mxfp8(const void *x, q_dtype in, int64_t M, int64_t K, q_fp8 fmt, uin
     return Q_OK;
 }
 
+q_status q_mxfp8_requant_col(const uint8_t *q_row, const uint8_t *e8m0_row, int64_t M, int64_t K, q_fp8 fmt,
+                             uint8_t *q_col, uint8_t *e8m0_col, int32_t *status, q_stream_t stream)
+{
+    const char *fn = "q_mxfp8_requant_col";
+    TRY(check_dims(fn, M, K));
+    if (fmt != Q_E4M3 && fmt != Q_E5M2) return fail(Q_ERR_ARG, "%s: fmt %d is not Q_E4M3 or Q_E5M2", fn, (int)fmt);
+    TRY(multiple(fn, "K", K, 32));
+    TRY(multiple(fn, "M", M, 32));
+    if (M * K == 0) return Q_OK;
+    TRY(need(fn, "q_row", q_row, 16));
+    TRY(need(fn, "e8m0_row", e8m0_row, 1));
+    TRY(need(fn, "q_col", q_col, 16));
+    TRY(need(fn, "e8m0_col", e8m0_col, 16));
+    LAUNCH(fn, qk::launch_mxfp8_requant_col(q_row, e8m0_row, M, K, (int)fmt, q_col, e8m0_col, status, S(stream)));
+    return Q_OK;
+}
+
 q_status q_blockwise(const void *x, q_dtype in, int64_t M, int64_t K, q_tile tile, uint8_t *q_row, float *s_row,
                      uint8_t *q_colT, float *s_colT, int32_t *status, q_stream_t stream)
 {

@@ -20,7 +20,7 @@
 
 namespace qk {
 
-enum { BF16 = 0, F32 = 1 };
+enum { BF16 = 0, F32 = 1, U8 = 2 };
 enum { E4M3 = 0, E5M2 = 1 };
 
 constexpr int kWarps = 8;

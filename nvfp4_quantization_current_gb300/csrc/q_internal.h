@@ -9,8 +9,10 @@ namespace qk {
 
 int sm_count();
 
-// A 2-D TMA tensor map over a row-major [M, K] input (dtype dt) whose box is
-// 128 rows x 512 bytes (the tile engine's stage).  Fails with
+// A 2-D TMA tensor map over a row-major [M, K] input (dt: BF16, F32, or U8
+// for code matrices, K even) whose box is 128 rows x 512 bytes (the tile
+// engine's stage).  The x coordinate counts elements of 2 bytes (BF16, U8)
+// or 4 bytes (F32).  Fails with
 // cudaErrorNotSupported if the driver entry point is unavailable.
 cudaError_t make_tile_map(void *map /* CUtensorMap, 64-byte aligned */, const void *x, int dt, int64_t M, int64_t K);
 
@@ -22,6 +24,10 @@ cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt,
 // MXFP8
 cudaError_t launch_mxfp8(const void *x, int dt, int64_t M, int64_t K, int fmt, uint8_t *q_row,
                          uint8_t *e_row, uint8_t *q_col, uint8_t *e_col, int32_t *status, cudaStream_t st);
+
+// MXFP8 rowwise codes -> columnwise codes (dequantize + re-quantize)
+cudaError_t launch_mxfp8_requant_col(const uint8_t *q_row, const uint8_t *e_row, int64_t M, int64_t K, int fmt,
+                                     uint8_t *q_col, uint8_t *e_col, int32_t *status, cudaStream_t st);
 
 // blockwise
 cudaError_t launch_blockwise(const void *x, int dt, int64_t M, int64_t K, int tile, uint8_t *q_row,

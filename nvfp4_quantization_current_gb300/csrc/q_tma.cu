@@ -26,12 +26,16 @@ cudaError_t make_tile_map(void *map, const void *x, int dt, int64_t M, int64_t K
 {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return cudaErrorNotSupported;
-    const int es = dt == BF16 ? 2 : 4;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    cuuint64_t strides[1] = {(cuuint64_t)K * es};
+    // A byte matrix is described as 16-bit elements (K/2 per row, K even):
+    // a box edge may not exceed 256 elements, and 512 bytes of U8 would.
+    const int es = dt == F32 ? 4 : 2;
+    const CUtensorMapDataType ty = dt == BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : (dt == F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16);
+    cuuint64_t dims[2] = {(cuuint64_t)(dt == U8 ? K / 2 : K), (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(dt == U8 ? K : K * es)};
     cuuint32_t box[2] = {(cuuint32_t)(512 / es), 128u};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(static_cast<CUtensorMap *>(map), dt == BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+    CUresult r = fn(static_cast<CUtensorMap *>(map), ty,
                     2, const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;

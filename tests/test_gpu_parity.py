@@ -209,6 +209,72 @@ def test_mxfp8_extreme_exponents():
     same(host(got.dequantize(Q.Q_ROW)), O.dq_mxfp8(want.q_row, want.e8m0_row, O.E4M3, O.ROW, O.F32))
 
 
+RQ_CASES = [
+    ("lognormal_rows", (256, 512), True, O.E4M3),
+    ("lognormal_rows", (96, 800), True, O.E4M3),      # 96 rows < one 128-row tile; 800 = 512 + 288 columns
+    ("t3", (160, 288), True, O.E5M2),
+    ("outliers", (384, 1056), False, O.E4M3),          # FP32 input, 3 x 3 tiles with ragged tails
+    ("grad", (32, 32), True, O.E5M2),
+]
+
+
+@pytest.mark.parametrize("kind,shape,bf16,fmt", RQ_CASES)
+def test_mxfp8_requant_col_parity(kind, shape, bf16, fmt):
+    """Rowwise MXFP8 output -> columnwise codes: GPU requant vs the oracle's
+    dequantize + re-quantize, bit for bit."""
+    x = W.gen(kind, shape, 303, bf16=bf16)
+    x[:32, :64] = 0                                   # zero blocks in both directions
+    f = "e4m3" if fmt == O.E4M3 else "e5m2"
+    rw = O.mxfp8(x, fmt, rowwise=True, colwise=False)
+    want_q, want_e = O.mxfp8_requant_col(rw.q_row, rw.e8m0_row, fmt)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = Q.q_mxfp8_requant_col(dev(rw.q_row), dev(rw.e8m0_row), f, status=st)
+    torch.cuda.synchronize()
+    same(host(got.q_col), want_q, "q_col")
+    same(host(got.e8m0_col), want_e, "e8m0_col")
+    assert st.item() == 0
+    # the chain through the library's own rowwise quantizer gives the same result
+    gr = Q.q_mxfp8(dev(x), f, colwise=False)
+    got2 = Q.q_mxfp8_requant_col(gr.q_row, gr.e8m0_row, f)
+    same(host(got2.q_col), want_q, "q_col via q_mxfp8")
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+def test_mxfp8_requant_col_random_codes(fmt):
+    """Every finite code with block scales over the whole range that does not
+    overflow FP32 on dequantization (x_hat down to 2^-143, FP32 subnormal)."""
+    rng = np.random.default_rng(7)
+    M, K = 224, 640
+    q = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    if fmt == O.E4M3:
+        q[(q & 0x7F) == 0x7F] ^= 0x01                 # no NaN codes
+        top = 246                                     # 448 * 2^(246-127) < FLT_MAX
+    else:
+        q[(q & 0x7C) == 0x7C] &= 0xFB                 # no inf / NaN codes
+        top = 239
+    e = rng.integers(0, top + 1, (M, K // 32), dtype=np.uint8)
+    e[: M // 2, 0] = 0                                # smallest scale in whole column blocks
+    e[M // 2:, 1] = top
+    want_q, want_e = O.mxfp8_requant_col(q, e, fmt)
+    got = Q.q_mxfp8_requant_col(dev(q), dev(e), "e4m3" if fmt == O.E4M3 else "e5m2")
+    same(host(got.q_col), want_q, "q_col")
+    same(host(got.e8m0_col), want_e, "e8m0_col")
+
+
+def test_mxfp8_requant_col_nan_scale_and_args():
+    q = torch.zeros((64, 64), dtype=torch.uint8, device="cuda")
+    e = torch.full((64, 2), 127, dtype=torch.uint8, device="cuda")
+    e[5, 1] = 255
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.q_mxfp8_requant_col(q, e, status=st)
+    torch.cuda.synchronize()
+    assert st.item() & Q.Q_ST_NONFINITE
+    empty = Q.q_mxfp8_requant_col(q[:0], e[:0])
+    assert empty.q_col.shape == (0, 64)
+    with pytest.raises(Q.QuantError):
+        Q.q_mxfp8_requant_col(q[:48], e[:48])         # M % 32 != 0
+
+
 # ---------------------------------------------------------------------------
 # blockwise
 # ---------------------------------------------------------------------------
