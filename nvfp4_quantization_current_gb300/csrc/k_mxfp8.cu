@@ -165,6 +165,19 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8_requant(const __grid_c
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
 
+    // The row scales of this thread's 8 rows are loaded one tile ahead (the
+    // CTA's next tile is t + gridDim.x), so that their latency hides behind a
+    // whole tile instead of stalling the start of each one.
+    uint32_t epre[8];
+    auto load_e = [&](int64_t t) {
+        const int64_t tm = t / tiles_k, tk = t - tm * tiles_k;
+        const int64_t k = tk * TC + lane * 16, m0 = tm * kTileRowsE + 8 * warp;
+        const bool ok = t < tiles_m * tiles_k && k < K;
+#pragma unroll
+        for (int j = 0; j < 8; j++) epre[j] = (ok && m0 + j < M) ? e_row[(m0 + j) * (K / 32) + k / 32] : 0u;
+    };
+    load_e(blockIdx.x);
+
     // the tensor map counts 2-byte elements: a tile is 256 of them per row
     run_tiles(&tmap, tiles_m, tiles_k, TC / 2, false, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
@@ -174,9 +187,10 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8_requant(const __grid_c
         float fr[8];   // 2^(e_row - 127) of each row's 1x32 block (code 255 -> NaN)
 #pragma unroll
         for (int j = 0; j < 8; j++) {
-            const uint32_t er = (m0 + j < M && kok) ? e_row[(m0 + j) * (K / 32) + k / 32] : 0u;
+            const uint32_t er = epre[j];
             fr[j] = er == 255u ? __uint_as_float(0x7FC00000u) : er == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(er << 23);
         }
+        load_e(tm * tiles_k + tk + gridDim.x);
         float acc[16];
 #pragma unroll
         for (int i = 0; i < 16; i++) acc[i] = 0.0f;
@@ -189,7 +203,10 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8_requant(const __grid_c
         }
 #pragma unroll
         for (int i = 0; i < 16; i++) part[warp][i][lane] = __float_as_uint(acc[i]) & 0x7FFFFFFFu;
-        __syncthreads();   // the four warps of each 32-row block have posted their maxima
+        // the four warps of this 32-row block have posted their maxima (named
+        // barrier 1..4 per block; the engine's CTA barrier after each tile
+        // orders the reads here before the next tile's writes)
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + (warp >> 2)) : "memory");
         const int w0 = warp & ~3;
         float inv[16];
         uint32_t code[16], nf = 0;

@@ -365,21 +365,24 @@ QD uint4 sr_bits(uint64_t seed, uint64_t g, uint32_t stream)
 }
 
 // Stochastic rounding of y onto the E2M1 grid with 16 random bits r16:
-// with a = |y| < 6, lo the grid value below a, ulp the spacing there and
-// frac = (a - lo) / ulp, round up iff r16 < frac * 2^16.  Every step is
-// exact in FP32 (the spacing is a power of two).  Returns a value on the
-// grid with y's sign (NaN passes through to the RTNE conversion).
+// with a = |y| < 6, ulp the grid spacing at a (0.5 below 2, 1 in [2, 4), 2
+// in [4, 6)), t = a / ulp, fl = floor(t) and frac = t - fl, the result is
+// (fl + 1) * ulp iff r16 < frac * 2^16, else fl * ulp.  With u = r16 / 2^16
+// that is ceil(t - u) * ulp: frac > u gives fl + 1, frac <= u gives fl.
+// t - u is formed by one FMA; it is exact for t >= 1 (both terms are
+// multiples of 2^-23 and the difference is below 4), and for t < 1 only its
+// sign decides the ceiling (0 or 1), which round-to-nearest keeps.  |y| >= 6
+// and NaN return y unchanged (the RTNE conversion saturates them).  The
+// result carries y's sign.
 QD float sr_e2m1_value(float y, uint32_t r16)
 {
-    float a = fabsf(y);
-    if (!(a < 6.0f)) return y;                      // >= 6 saturates in cvt; NaN stays NaN
-    float ulp = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-    float t = __fmul_rn(a, a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f));   // a / ulp, exact
-    float fl = floorf(t);
-    float frac = t - fl;                            // exact
-    float v = __fmul_rn(fl, ulp);
-    if ((float)r16 < __fmul_rn(frac, 65536.0f)) v = v + ulp;   // exact sum on the grid
-    return copysignf(v, y);
+    const float a = fabsf(y);
+    const float s = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);   // 1 / ulp
+    const float ulp = __uint_as_float(0x7F000000u - __float_as_uint(s));   // 2^-k from 2^k
+    const float t = __fmul_rn(a, s);                                  // exact
+    const float n = ceilf(__fmaf_rn(-(float)r16, 1.0f / 65536.0f, t));
+    const float v = copysignf(__fmul_rn(n, ulp), y);                  // exact, on the grid
+    return a < 6.0f ? v : y;
 }
 
 // ---------------------------------------------------------------------------
