@@ -84,6 +84,8 @@ def _L():
             "or_mxfp8": (None, [P, I, I64, I64, I, P, P, P, P]),
             "or_dq_mxfp8": (None, [P, P, I64, I64, I, I, I, P]),
             "or_mxfp8_requant_col": (None, [P, P, I64, I64, I, P, P]),
+            "or_ds_cast": (None, [P, I, I64, I64, I, F, P, P, P]),
+            "or_ds_scale_update": (None, [P, I64, I64, I, I, P, P]),
             "or_blockwise": (None, [P, I, I64, I64, I, P, P, P, P]),
             "or_dq_blockwise": (None, [P, P, I64, I64, I, I, P]),
             "or_nvfp4_global": (None, [F, P, P]),
@@ -235,6 +237,30 @@ def current_scaling(x, fmt=E4M3, rowwise=True, colwise=False, amax_in=None):
     a_in = None if amax_in is None else _fbuf(amax_in)
     _L().or_current_scaling(_p(x), dt, M, K, fmt, _p(a_in), _p(q_row), _p(q_colT), _p(a_out), _p(s_out))
     return CS(q_row, q_colT, a_out[0], s_out[0])
+
+
+HIST_MAX, HIST_MOST_RECENT = 0, 1
+
+
+def ds_cast(x, alpha, fmt=E4M3, rowwise=True, colwise=False):
+    """Delayed scaling, one step's cast: codes of Q(alpha x) with the given
+    alpha, and the step's amax (to be recorded in the history)."""
+    x, dt = _x(x)
+    M, K = x.shape
+    q_row = np.empty((M, K), np.uint8) if rowwise else None
+    q_colT = np.empty((K, M), np.uint8) if colwise else None
+    a_out = _fbuf()
+    _L().or_ds_cast(_p(x), dt, M, K, fmt, float(np.float32(alpha)), _p(q_row), _p(q_colT), _p(a_out))
+    return q_row, q_colT, a_out[0]
+
+
+def ds_scale_update(hist, pos, algo=HIST_MAX, fmt=E4M3):
+    """(alpha, s) for the next step from the amax window ``hist`` (float32
+    ring, slot ``pos`` holds the latest amax)."""
+    h = np.ascontiguousarray(hist, np.float32)
+    al, s = _fbuf(), _fbuf()
+    _L().or_ds_scale_update(_p(h), h.size, int(pos), algo, fmt, _p(al), _p(s))
+    return al[0], s[0]
 
 
 def dq_current_scaling(q, s, fmt=E4M3, out=F32):

@@ -40,6 +40,13 @@
  *            stored transposed [K, M]; MXFP8 columnwise stays [M, K].
  *   R-AMAX   amax is the largest |x| bit pattern, which is the largest |x|
  *            for finite inputs (non-finite inputs are outside the contract).
+ *   R-DS     delayed scaling: the amax window is a ring of N FP32 slots
+ *            (unfilled slots hold 0); "max" takes the largest entry, "most
+ *            recent" the latest slot; the next step's alpha and s follow the
+ *            current-scaling rule on that value (so the first step, with an
+ *            empty window, uses alpha = s = 1).
+ *   R-REQ    MXFP8 row-to-column re-quantization dequantizes with the 1x32
+ *            scales to FP32 and re-quantizes that tensor in 32x1 blocks.
  *
  * Parity status: every function below is pinned by the tests in tests/
  * (worked examples, brute-force nearest-value search, library casts,
@@ -411,6 +418,49 @@ void or_current_scaling(const void *x, int dtype, int64_t M, int64_t K, int fmt,
         }
     if (amax_out) *amax_out = a;
     if (s_out) *s_out = s;
+}
+
+/* ------------------------------------------------------------------------ */
+/* per-tensor delayed scaling                                                */
+/* ------------------------------------------------------------------------ */
+/*
+ * [MP] "Per-tensor delayed scaling": at step t the tensor is quantized with
+ * a scale predicted from the amaxes of earlier steps, and its own amax is
+ * recorded (in the same read of x) into a window of the last N steps; the
+ * scale for step t+1 is then derived from the window.  Megatron's settings
+ * quoted on [LP] section 4.3: window length 1024, reduction "max".
+ *
+ * or_ds_cast: q = Q(alpha * x) with the given alpha (same element rule as
+ * or_current_scaling), and amax_out = max|x| (largest bit pattern, as
+ * or_amax: NaN wins).
+ */
+void or_ds_cast(const void *x, int dtype, int64_t M, int64_t K, int fmt, float alpha,
+                uint8_t *q_row, uint8_t *q_colT, float *amax_out)
+{
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t k = 0; k < K; k++) {
+            float y = alpha * load_x(x, dtype, m * K + k);
+            uint8_t c = enc_fmt8(y, fmt);
+            if (q_row) q_row[m * K + k] = c;
+            if (q_colT) q_colT[k * M + m] = c;
+        }
+    if (amax_out) *amax_out = or_amax(x, dtype, M * K);
+}
+
+/*
+ * or_ds_scale_update: the scale for the next step from the window
+ * hist[0..N) of recorded amaxes (a ring: slot pos holds the latest one).
+ * algo 0 (max): A = the entry of largest magnitude (bit pattern of |h|, so a
+ * NaN entry wins); algo 1 (most recent): A = |hist[pos]|.  Then alpha and s
+ * follow the current-scaling rule on A (A = 0 gives 1; an alpha that
+ * overflows is FLT_MAX).  Unused slots hold 0 and do not move a maximum.
+ */
+void or_ds_scale_update(const float *hist, int64_t N, int64_t pos, int algo, int fmt, float *alpha, float *s)
+{
+    float A;
+    if (algo == 1) A = f32_from_bits(bits_from_f32(hist[pos]) & 0x7FFFFFFFu);
+    else A = or_amax(hist, OR_F32, N);
+    scale_from_amax(fmax_of(fmt), A, alpha, s);
 }
 
 /* x_hat = q * s ([CS] "Current Scaling": x_hat_i = q_i * s). out_dtype BF16

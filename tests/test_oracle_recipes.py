@@ -445,3 +445,92 @@ def test_mx_requant_close_to_direct_columnwise():
     xf = W.bf16_bits_to_f32(x)
     big = np.abs(dec8(r.q_col)) >= 2.0 ** -6
     assert np.all((np.abs(d1 - xf) <= np.abs(xf) * (1 / 8 + 1 / 8 * 9 / 8) + 1e-30)[big])
+
+
+# ---------------------------------------------------------------------------
+# per-tensor delayed scaling ("Mixed-precision training: fp16 to fp8",
+# "Per-tensor delayed scaling")
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2])
+def test_ds_cast_equals_current_scaling_at_the_same_alpha(fmt):
+    x = W.gen("outliers", (96, 160), 31, bf16=True)
+    A = O.amax(x)
+    alpha, _ = O.cs_scale(A, fmt)
+    q_row, q_colT, a = O.ds_cast(x, alpha, fmt, rowwise=True, colwise=True)
+    cs = O.current_scaling(x, fmt, rowwise=True, colwise=True)
+    assert np.array_equal(q_row, cs.q_row) and np.array_equal(q_colT, cs.q_colT)
+    assert q_colT.shape == (160, 96) and np.array_equal(q_colT, q_row.T)
+    assert a == A
+
+
+def test_ds_cast_alpha_one_reproduces_grid_values():
+    """Every finite E4M3 value cast with alpha = 1 returns its own code."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8).reshape(1, -1)
+    x = dec8(codes).astype(np.float32)
+    q_row, _, a = O.ds_cast(x, 1.0, O.E4M3)
+    assert np.array_equal(q_row, codes)
+    assert a == np.float32(448.0)
+
+
+def test_ds_scale_update_closed_forms():
+    z = np.zeros(16, np.float32)
+    assert O.ds_scale_update(z, 0) == (1.0, 1.0)                        # empty window: alpha = s = 1
+    h = z.copy()
+    h[5] = 8.0
+    al, s = O.ds_scale_update(h, 9)
+    assert al == np.float32(56.0) and s == np.float32(1.0) / np.float32(56.0)   # 448 / 8
+    al, s = O.ds_scale_update(h, 9, fmt=O.E5M2)
+    assert al == np.float32(7168.0)                                      # 57344 / 8
+    assert O.ds_scale_update(h, 9, O.HIST_MOST_RECENT) == (1.0, 1.0)    # slot 9 is empty
+    assert O.ds_scale_update(h, 5, O.HIST_MOST_RECENT)[0] == np.float32(56.0)
+    h[2] = 1e-45                                                         # 448 / 1e-45 overflows: FLT_MAX
+    assert O.ds_scale_update(h, 2, O.HIST_MOST_RECENT)[0] == np.finfo(np.float32).max
+    h[3] = np.nan
+    assert np.isnan(O.ds_scale_update(h, 9)[0])                          # a NaN entry wins the max
+
+
+@pytest.mark.parametrize("algo,N", [(O.HIST_MAX, 4), (O.HIST_MAX, 1), (O.HIST_MOST_RECENT, 4), (O.HIST_MAX, 1024)])
+def test_ds_window_against_a_plain_list_model(algo, N):
+    """A run of steps through the ring (slot = step % N) against a list of
+    the last N amaxes: each step's alpha is 448 / max (or / latest) of the
+    amaxes recorded before it, and 1 before any."""
+    rng = np.random.default_rng(4)
+    base = W.gen("normal", (16, 32), 9, bf16=False)
+    base /= np.abs(base).max()                                           # amax of base = 1 exactly
+    amaxes = [np.float32(2.0) ** int(e) for e in rng.integers(-6, 7, 3 * N + 5)]
+    amaxes[1] = np.float32(4096.0)                                       # an outlier that must leave after N steps
+    hist = np.zeros(N, np.float32)
+    alpha = np.float32(1.0)
+    window = []
+    for t, a in enumerate(amaxes):
+        if window:
+            ref = max(window) if algo == O.HIST_MAX else window[-1]
+            want = np.float32(448.0) / np.float32(ref)
+        else:
+            want = np.float32(1.0)
+        assert alpha == want, (t, alpha, want)
+        x = (base * a).astype(np.float32)
+        q_row, _, got_a = O.ds_cast(x, alpha, O.E4M3)
+        assert got_a == np.float32(a)
+        assert np.array_equal(q_row, O.cast_fp8((alpha * x).astype(np.float32), O.E4M3))
+        hist[t % N] = got_a
+        alpha, s = O.ds_scale_update(hist, t % N, algo)
+        assert s == np.float32(1.0) / alpha
+        window = (window + [np.float32(a)])[-N:]
+
+
+def test_ds_repeated_tensor_converges_to_current_scaling():
+    """Quantizing the same tensor every step: from the second step on the
+    window holds its amax, so the codes are the current-scaling codes."""
+    x = W.gen("t3", (64, 48), 12, bf16=True)
+    hist = np.zeros(8, np.float32)
+    alpha = np.float32(1.0)
+    cs = O.current_scaling(x, O.E4M3, rowwise=True, colwise=True)
+    for t in range(3):
+        q_row, q_colT, a = O.ds_cast(x, alpha, O.E4M3, rowwise=True, colwise=True)
+        if t > 0:
+            assert np.array_equal(q_row, cs.q_row) and np.array_equal(q_colT, cs.q_colT)
+        hist[t % 8] = a
+        alpha, _ = O.ds_scale_update(hist, t % 8)
+    assert alpha == O.cs_scale(O.amax(x))[0]
