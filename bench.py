@@ -4,7 +4,8 @@ pages' workloads.
 
 One step = one pass of every recipe over its full-size tensors (all five
 workloads of ``workloads.WORKLOADS``): current-scaling amax + cast (+ the
-transposed copy), MXFP8 row + col and the row->col re-quantize, blockwise 1x128 (+ transposed) and
+transposed copy), delayed scaling (one read + the window update), MXFP8
+row + col and the row->col re-quantize, blockwise 1x128 (+ transposed) and
 128x128 (+ transposed), NVFP4 1x16 RTNE, 1x16 stochastic rounding and 16x16,
 and the dequantizer of each.  Every call goes through the C ABI with
 preallocated outputs.
@@ -122,6 +123,19 @@ def build_step(dev_tensors, torch, Q):
                             lambda: Q.dq_current_scaling(out.q_row, out.scale, fmt, y.dtype, out=y))],
                           [out.q_row], [y], lambda: Q.dq_current_scaling(out.q_row, out.scale, fmt, y.dtype, out=y)))
 
+    def ds(tag, x, fmt, N=1024):
+        st = Q.DelayedScaling(fmt, history_len=N, algo="max", device=x.device)
+        out = Q.alloc_current_scaling(x.shape[0], x.shape[1], x.device, fmt, True, True)
+        slot = st.hist[0:1]
+        pieces = [
+            ("ds_cast_T", "k_current_scaling.cu", nbytes(x, out.q_row, out.q_colT, out.scale, slot, st.ds),
+             lambda: Q.q_delayed_scaling(x, st.ds, slot, fmt, True, True, out=out)),
+            ("ds_update", "k_current_scaling.cu", nbytes(st.hist, st.ds),
+             lambda: Q.q_delayed_scale_update(st.hist, 0, st.ds, fmt, "max")),
+        ]
+        calls.append(Call(f"{tag} ds_{fmt} row+colT", "delayed_scaling", pieces, [x],
+                          [out.q_row, out.q_colT, out.scale], lambda: st.quantize(x, True, True, out=out)))
+
     def mx(tag, x):
         out = Q.alloc_mxfp8(x.shape[0], x.shape[1], x.device, "e4m3", True, True)
         b = nbytes(x, out.q_row, out.e8m0_row, out.q_col, out.e8m0_col)
@@ -184,6 +198,7 @@ def build_step(dev_tensors, torch, Q):
         bw("bw3.w", d["bw3"]["w"], "128x128", True)
     if "hy4" in d:
         cs("hy4.grad", d["hy4"]["grad"], "e5m2", True)
+        ds("hy4.grad", d["hy4"]["grad"], "e5m2")
         cs("hy4.w", d["hy4"]["w"], "e4m3", True)
     if "nv5" in d:
         nv("nv5.act", d["nv5"]["act"], "1x16", "rn", 0)
@@ -218,14 +233,31 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
             raise AssertionError(f"sampled parity failed: {what}")
         checked.append(what)
 
-    for wl, tn, kind in [("cs1", "x", "cs_e4m3"), ("hy4", "grad", "cs_e5m2"), ("hy4", "w", "cs_e4m3"),
+    for wl, tn, kind in [("cs1", "x", "cs_e4m3"), ("hy4", "grad", "cs_e5m2"), ("hy4", "grad", "ds_e5m2"),
+                         ("hy4", "w", "cs_e4m3"),
                          ("mx2", "act", "mx"), ("bw3", "act", "bw1"), ("bw3", "w", "bw128"),
                          ("nv5", "act", "nv_rn"), ("nv5", "grad", "nv_sr"), ("nv5", "w", "nv16")]:
         xh, xd = host_tensors[wl][tn], dev_tensors[wl][tn]
         M, K = xh.shape
         r0 = band(M)
         xs = np.ascontiguousarray(xh[r0:r0 + rows])
-        if kind.startswith("cs"):
+        if kind.startswith("ds"):
+            # two steps from an empty window: step 0 casts with alpha = 1, step 1
+            # with the alpha of step 0's recorded amax
+            st = Q.DelayedScaling("e5m2", history_len=1024)
+            hist = np.zeros(1024, np.float32)
+            alpha = np.float32(1.0)
+            for t in range(2):
+                g = st.quantize(xd, True, True)
+                w_row, w_colT, _ = O.ds_cast(xs, alpha, O.E5M2, rowwise=True, colwise=True)
+                eq(host(g.q_row[r0:r0 + rows]), w_row, f"{wl}.{tn} delayed step {t} q_row band")
+                eq(host(g.q_colT[:, r0:r0 + rows]), w_colT, f"{wl}.{tn} delayed step {t} q_colT band")
+                A = O.amax(xh)
+                eq(np.float32(g.amax.item()), np.float32(A), f"{wl}.{tn} delayed step {t} amax")
+                hist[t] = A
+                alpha, s = O.ds_scale_update(hist, t, O.HIST_MAX, O.E5M2)
+                eq(host(st.ds), np.array([alpha, s], np.float32), f"{wl}.{tn} delayed step {t} next scale")
+        elif kind.startswith("cs"):
             fmt = O.E5M2 if kind == "cs_e5m2" else O.E4M3
             A = O.amax(xh)
             g = Q.q_current_scaling(xd, "e5m2" if fmt == O.E5M2 else "e4m3", True, True)
@@ -490,8 +522,9 @@ def run_ours(args):
                 "frac": round(achieved / peak, 3), "traffic": traffic,
                 "alg_bytes_per_launch": int(dom_bytes), "us_per_launch": round(dom_us, 2),
                 "share_of_step": round(dom_us / (step_ms * 1e3), 3), "peak_kind": peak_kind + " hbm_gbs"}
-    # q_amax launches two kernels (zero the word, reduce); every other call one
-    n_launches = args.steps * sum((2 if p[0] == "amax" else 1) for c in calls for p in c.pieces)
+    # q_amax and the delayed-scaling cast launch two kernels (zero the amax
+    # word, then the pass); every other call one
+    n_launches = args.steps * sum((2 if p[0] in ("amax", "ds_cast_T") else 1) for c in calls for p in c.pieces)
 
     # ---- end to end: pinned host input -> device, the public call, outputs -> pinned host
     e2e = None
@@ -553,7 +586,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy; see workloads.WORKLOADS)",
             "config": {"workload": "all five workloads at full size per step: cs1 FP32 1024x1024 CS-E4M3+T; "
                                    "mx2 BF16 8192x4096 MXFP8 row+col, row->col requant; bw3 BF16 16384x7168 1x128+T and 7168x18432 "
-                                   "128x128+T; hy4 BF16 8192x14336 CS-E5M2+T and 14336x4096 CS-E4M3+T; nv5 BF16 "
+                                   "128x128+T; hy4 BF16 8192x14336 CS-E5M2+T, delayed-scaling E5M2+T (window 1024, max) and 14336x4096 CS-E4M3+T; nv5 BF16 "
                                    "8192x4096 NVFP4 1x16 RN+T, 1x16 SR+T, 4096x4096 16x16 RN+T; each with a dequant",
                        "l2": "flushed (256 MiB write) before every timed call",
                        "scale_rows": args.scale_rows, "parallelism": f"replicas x{world} (independent tensors)"},
@@ -601,6 +634,14 @@ def oracle_sample_work(host_t, frac):
         work.append((lambda: O.dq_current_scaling(r.q_row, r.scale, fmt, O.BF16 if a.dtype == np.uint16 else O.F32),
                      M * K + M * K * isz(a) + 4))
 
+    def ds(a, fmt):
+        s = np.ascontiguousarray(a[:rows(a)])
+        M, K = s.shape
+        alpha, _ = O.ds_scale_update(np.array([O.amax(a)], np.float32), 0, O.HIST_MAX, fmt)
+        hist = np.zeros(1024, np.float32)
+        work.append((lambda: O.ds_cast(s, alpha, fmt, True, True), s.nbytes + 2 * M * K + 16))
+        work.append((lambda: O.ds_scale_update(hist, 0, O.HIST_MAX, fmt), hist.nbytes + 8))
+
     def mx(a):
         s = np.ascontiguousarray(a[:rows(a)])
         M, K = s.shape
@@ -631,6 +672,7 @@ def oracle_sample_work(host_t, frac):
     bw(host_t["bw3"]["act"], O.T1x128)
     bw(host_t["bw3"]["w"], O.T128x128)
     cs(host_t["hy4"]["grad"], O.E5M2)
+    ds(host_t["hy4"]["grad"], O.E5M2)
     cs(host_t["hy4"]["w"], O.E4M3)
     nv(host_t["nv5"]["act"], O.B1x16, O.RN, 0)
     nv(host_t["nv5"]["grad"], O.B1x16, O.SR, 4)

@@ -72,6 +72,9 @@ typedef enum { Q_ROW = 0, Q_COL = 1 } q_dir;
  * ([CS] "Cost and multi-GPU use": compute amax, synchronize amax, then
  * scale + cast). */
 typedef enum { Q_AMAX_COMPUTE = 0, Q_AMAX_GIVEN = 1 } q_amax_mode;
+/* How delayed scaling reduces its amax window: the largest entry, or the
+ * latest one. */
+typedef enum { Q_HIST_MAX = 0, Q_HIST_MOST_RECENT = 1 } q_hist_algo;
 
 /* Bits ORed into *status by the kernels. */
 #define Q_ST_NONFINITE 1   /* an amax (tensor or block) was inf or NaN */
@@ -111,6 +114,38 @@ q_status q_current_scaling(const void *x, q_dtype in, int64_t M, int64_t K, q_fp
                            uint8_t *q_row, uint8_t *q_colT,
                            float *amax, q_amax_mode amax_mode, float *scale,
                            int32_t *status, q_stream_t stream);
+
+/*
+ * Per-tensor delayed scaling ([MP] "Per-tensor delayed scaling"; window
+ * settings as quoted on [LP] section 4.3: length 1024, reduction max).  Step
+ * t quantizes x with a scale predicted from the amaxes of earlier steps and
+ * records its own amax in the same read of x; q_delayed_scale_update then
+ * derives the scale of step t+1 from the window.  Per step:
+ *   q_delayed_scaling(x, ..., ds, &hist[t % N], scale_t, ...);
+ *   q_delayed_scale_update(hist, N, t % N, algo, fmt, ds, ...);
+ * ds is the device pair [alpha, s] (initially [1, 1], which is also what an
+ * all-zero window gives).  The caller owns hist[N] (FP32, zero-initialized)
+ * and ds, and keeps t.
+ *
+ * q_delayed_scaling: q = saturate(RTNE(alpha * x)) with alpha = ds[0];
+ *   q_row / q_colT as in q_current_scaling (same shape rules);
+ *   amax_out  one float, written: max|x| (this step's window entry);
+ *   scale     one float, written: ds[1], the s that decodes these codes.
+ * An empty tensor writes amax_out = 0 and scale = ds[1].  A non-finite x or
+ * alpha is reported in *status.
+ */
+q_status q_delayed_scaling(const void *x, q_dtype in, int64_t M, int64_t K, q_fp8 fmt,
+                           uint8_t *q_row, uint8_t *q_colT, const float *ds, float *amax_out, float *scale,
+                           int32_t *status, q_stream_t stream);
+
+/*
+ * q_delayed_scale_update: ds = [alpha, s] from the window hist[0..N) (N >= 1,
+ * slot pos < N holds the latest amax).  Q_HIST_MAX: A = the largest |entry|;
+ * Q_HIST_MOST_RECENT: A = |hist[pos]|.  alpha = Fmax / A (A = 0 gives 1; an
+ * alpha that overflows is FLT_MAX), s = 1 / alpha.  One CTA; reads N floats.
+ */
+q_status q_delayed_scale_update(const float *hist, int64_t N, int64_t pos, q_hist_algo algo, q_fp8 fmt,
+                                float *ds, q_stream_t stream);
 
 /*
  * a4/a5: MXFP8 ([MP] "MXFP8" and recipe 5): 32 elements share one E8M0

@@ -13,6 +13,10 @@ Recipes (each with its dequantizer, rowwise and columnwise outputs):
 * :func:`q_current_scaling` -- per-tensor current scaling to E4M3 / E5M2
   ("FP8 Current Scaling: quantization, scaling and precision bounds",
   section "Current Scaling");
+* :func:`q_delayed_scaling` / :class:`DelayedScaling` -- per-tensor delayed
+  scaling: the scale comes from a window of earlier amaxes and the step's
+  amax is recorded in the same read ("Mixed-precision training: fp16 to
+  fp8", "Per-tensor delayed scaling");
 * :func:`q_mxfp8` -- 1x32 blocks with E8M0 scales ("Mixed-precision
   training: fp16 to fp8", section "MXFP8");
 * :func:`q_mxfp8_requant_col` -- MXFP8 rowwise codes to columnwise codes
@@ -57,6 +61,8 @@ SIGNATURES = {
     "q_amax": (_I, [_P, _I, _I64, _P, _P, _P]),
     "q_current_scaling": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P]),
     "q_mxfp8": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
+    "q_delayed_scaling": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "q_delayed_scale_update": (_I, [_P, _I64, _I64, _I, _I, _P, _P]),
     "q_mxfp8_requant_col": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
     "q_blockwise": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "q_nvfp4": (_I, [_P, _I, _I64, _I64, _I, _I, _U64, _U64, _P, _P, _P, _P, _P, _I, _P, _P, _P]),
@@ -190,6 +196,75 @@ def dq_current_scaling(q: torch.Tensor, scale: torch.Tensor, fmt="e4m3", dtype=t
     y = torch.empty((R, C), dtype=dtype, device=q.device) if out is None else out
     _call("dq_current_scaling", _ptr(q), _ptr(scale), R, C, _fmt(fmt), _out(dtype), _ptr(y), _stream(q.device))
     return y
+
+
+# ---------------------------------------------------------------------------
+# per-tensor delayed scaling
+# ---------------------------------------------------------------------------
+
+Q_HIST_MAX, Q_HIST_MOST_RECENT = 0, 1
+
+
+def _algo(algo):
+    return {"max": Q_HIST_MAX, "most_recent": Q_HIST_MOST_RECENT, Q_HIST_MAX: Q_HIST_MAX,
+            Q_HIST_MOST_RECENT: Q_HIST_MOST_RECENT}[algo]
+
+
+def q_delayed_scaling(x: torch.Tensor, ds: torch.Tensor, amax_out: torch.Tensor, fmt="e4m3", rowwise=True,
+                      colwise=False, out: Optional[CurrentScalingTensor] = None,
+                      status: Optional[torch.Tensor] = None) -> CurrentScalingTensor:
+    """One delayed-scaling cast: codes of x with alpha = ds[0] (the pair
+    [alpha, s] from the previous :func:`q_delayed_scale_update`), max|x|
+    written to ``amax_out`` (this step's window slot) and s = ds[1] to the
+    result's ``scale``.  Reads x once."""
+    dt = _in(x)
+    M, K = x.shape
+    if out is None:
+        out = alloc_current_scaling(M, K, x.device, fmt, rowwise, colwise)
+    out.amax = amax_out
+    _call("q_delayed_scaling", _ptr(x), dt, M, K, out.fmt, _ptr(out.q_row), _ptr(out.q_colT), _ptr(ds),
+          _ptr(amax_out), _ptr(out.scale), _ptr(status), _stream(x.device))
+    return out
+
+
+def q_delayed_scale_update(hist: torch.Tensor, pos: int, ds: torch.Tensor, fmt="e4m3", algo="max") -> torch.Tensor:
+    """ds = [alpha, s] for the next step from the amax window ``hist`` (FP32,
+    slot ``pos`` the latest)."""
+    _call("q_delayed_scale_update", _ptr(hist), hist.numel(), int(pos), _algo(algo), _fmt(fmt), _ptr(ds),
+          _stream(hist.device))
+    return ds
+
+
+class DelayedScaling:
+    """Delayed-scaling state of one tensor: a window of ``history_len`` amaxes
+    (a ring, zero-initialized), the pair [alpha, s] (initially [1, 1]) and
+    the step counter.  ``quantize`` runs one step: the cast with the current
+    pair (recording the step's amax in slot ``step % history_len``), an
+    optional MAX all-reduce of that slot over ``group`` (so that every shard
+    of a distributed tensor keeps the same window), and the update of the
+    pair from the window (``algo`` "max" or "most_recent").  The result's
+    ``amax`` is a view of the window slot, overwritten ``history_len`` steps
+    later."""
+
+    def __init__(self, fmt="e4m3", history_len=1024, algo="max", device="cuda"):
+        if history_len < 1:
+            raise ValueError("history_len must be >= 1")
+        self.fmt, self.algo = _fmt(fmt), _algo(algo)
+        self.hist = torch.zeros(history_len, dtype=torch.float32, device=device)
+        self.ds = torch.ones(2, dtype=torch.float32, device=device)
+        self.step = 0
+
+    def quantize(self, x: torch.Tensor, rowwise=True, colwise=False, out: Optional[CurrentScalingTensor] = None,
+                 status: Optional[torch.Tensor] = None, group=None) -> CurrentScalingTensor:
+        pos = self.step % self.hist.numel()
+        slot = self.hist[pos:pos + 1]
+        res = q_delayed_scaling(x, self.ds, slot, self.fmt, rowwise, colwise, out, status)
+        if group is not None:
+            from .distributed import allreduce_amax_
+            allreduce_amax_(slot, group)
+        q_delayed_scale_update(self.hist, pos, self.ds, self.fmt, self.algo)
+        self.step += 1
+        return res
 
 
 # ---------------------------------------------------------------------------

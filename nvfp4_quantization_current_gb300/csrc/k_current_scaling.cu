@@ -7,6 +7,13 @@
 // "Mixed-precision training: fp16 to fp8", "Per-tensor Current Scaling"
 // (Hopper flow): one kernel writes the cast and the cast_transpose.
 //
+// Per-tensor delayed scaling ("Mixed-precision training: fp16 to fp8",
+// "Per-tensor delayed scaling") runs the same cast kernels with DS = true:
+// alpha and s come from a device pair written by the previous step's scale
+// update, and the pass also reduces max|x| into this step's slot of the amax
+// window, so x is read once.  k_ds_update derives the next pair from the
+// window.
+//
 // The two passes are two launches in stream order (no grid-wide barrier, no
 // spin-wait).  Every CTA of the cast pass recomputes alpha from the amax
 // word (identical in every CTA); CTA 0 writes s.  The cast pass walks the
@@ -72,23 +79,54 @@ __global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict
     }
 }
 
+// CTA-wide max of m (blockDim.x a multiple of 32, at most 1024 threads),
+// then one atomicMax into *dst from a CTA that raises it; a non-finite
+// result is reported in *status.
+QD void cta_max_to(uint32_t m, uint32_t *dst, int32_t *status)
+{
+    __shared__ uint32_t red[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    m = warp_max(m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
+        m = warp_max(m);
+        if (lane == 0) {
+            if (m > *reinterpret_cast<volatile uint32_t *>(dst)) atomicMax(dst, m);
+            flag_nonfinite(status, m);
+        }
+    }
+}
+
+// alpha of the cast: from the amax (current scaling) or the pair [alpha, s]
+// (delayed scaling); CTA 0 writes s and reports a non-finite amax or alpha.
+template <int FMT, bool DS>
+QD float cast_alpha(const float *amax, const float *ds, float *scale, int32_t *status)
+{
+    const float a = DS ? 0.0f : *amax;
+    const float alpha = DS ? ds[0] : alpha_from_amax(Fp8<FMT>::FMAX, a);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *scale = DS ? ds[1] : __fdiv_rn(1.0f, alpha);
+        flag_nonfinite(status, DS ? __float_as_uint(alpha) & 0x7FFFFFFFu : __float_as_uint(a) & 0x7FFFFFFFu);
+    }
+    return alpha;
+}
+
 // ---------------------------------------------------------------------------
 // a3, rowwise only: flat streaming cast, 16 elements -> one 16-byte store.
 // ---------------------------------------------------------------------------
-template <int DT, int FMT>
+template <int DT, int FMT, bool DS>
 __global__ void __launch_bounds__(256) k_cs_cast_flat(const void *__restrict__ x, int64_t n,
-                                                      const float *__restrict__ amax, uint8_t *__restrict__ q,
+                                                      const float *__restrict__ amax, const float *__restrict__ ds,
+                                                      uint32_t *amax_rec, uint8_t *__restrict__ q,
                                                       float *__restrict__ scale, int32_t *status)
 {
     constexpr int VEC = In<DT>::VEC;
     constexpr int VPC = 16 / VEC;   // 16-byte input vectors per 16-element chunk
     constexpr int U = 4;            // chunks in flight per thread
-    const float a = *amax;
-    const float alpha = alpha_from_amax(Fp8<FMT>::FMAX, a);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        *scale = __fdiv_rn(1.0f, alpha);
-        flag_nonfinite(status, __float_as_uint(a) & 0x7FFFFFFFu);
-    }
+    const float alpha = cast_alpha<FMT, DS>(amax, ds, scale, status);
+    uint32_t mx = 0;                // DS: max |x| bits seen by this thread
     const uint4 *xv = static_cast<const uint4 *>(x);
     const int64_t nc = n / 16;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -107,7 +145,10 @@ __global__ void __launch_bounds__(256) k_cs_cast_flat(const void *__restrict__ x
             if (c < 0) break;
             uint32_t o[4];
 #pragma unroll
-            for (int j = 0; j < VPC; j++) chunk_fp8<DT, FMT>(v[u][j], alpha, o + j * (VEC / 4));
+            for (int j = 0; j < VPC; j++) {
+                if (DS) mx = max(mx, absmax_bits<DT>(v[u][j]));
+                chunk_fp8<DT, FMT>(v[u][j], alpha, o + j * (VEC / 4));
+            }
             stg16(q + c * 16, make_uint4(o[0], o[1], o[2], o[3]));
         }
     }
@@ -117,7 +158,9 @@ __global__ void __launch_bounds__(256) k_cs_cast_flat(const void *__restrict__ x
         const float v = DT == BF16 ? __uint_as_float((uint32_t)static_cast<const uint16_t *>(x)[t] << 16)
                                    : static_cast<const float *>(x)[t];
         q[t] = (uint8_t)(cvt_fp8x4<FMT>(__fmul_rn(alpha, v), 0.f, 0.f, 0.f) & 0xFFu);
+        mx = max(mx, __float_as_uint(v) & 0x7FFFFFFFu);
     }
+    if (DS) cta_max_to(mx, amax_rec, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -127,19 +170,16 @@ __global__ void __launch_bounds__(256) k_cs_cast_flat(const void *__restrict__ x
 // around by byte transposes, are parked in the consumed stage and written as
 // full 128-byte q_colT rows.  Requires M % 16 == 0 and K % 16 == 0.
 // ---------------------------------------------------------------------------
-template <int DT, int FMT>
+template <int DT, int FMT, bool DS>
 __global__ void __launch_bounds__(kEngThreads, 1) k_cs_tiles(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
-                                                             const float *__restrict__ amax, uint8_t *__restrict__ q_row,
+                                                             const float *__restrict__ amax, const float *__restrict__ ds,
+                                                             uint32_t *amax_rec, uint8_t *__restrict__ q_row,
                                                              uint8_t *__restrict__ q_colT, float *__restrict__ scale,
                                                              int32_t *status)
 {
     constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4;
-    const float a = *amax;
-    const float alpha = alpha_from_amax(Fp8<FMT>::FMAX, a);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        *scale = __fdiv_rn(1.0f, alpha);
-        flag_nonfinite(status, __float_as_uint(a) & 0x7FFFFFFFu);
-    }
+    const float alpha = cast_alpha<FMT, DS>(amax, ds, scale, status);
+    uint32_t mx = 0;   // DS: max |x| bits of this thread's tile chunks (OOB fill is 0)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
 
@@ -148,7 +188,11 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_cs_tiles(const __grid_consta
         const int64_t k = kb + lane * VEC, m0 = mb + 8 * warp;
         uint32_t code[8][CW];
 #pragma unroll
-        for (int j = 0; j < 8; j++) chunk_fp8<DT, FMT>(lds16(st + (8 * warp + j) * kRowBytes + lane * 16), alpha, code[j]);
+        for (int j = 0; j < 8; j++) {
+            const uint4 v = lds16(st + (8 * warp + j) * kRowBytes + lane * 16);
+            if (DS) mx = max(mx, absmax_bits<DT>(v));
+            chunk_fp8<DT, FMT>(v, alpha, code[j]);
+        }
         if (q_row != nullptr && k < K) {
 #pragma unroll
             for (int j = 0; j < 8; j++) {
@@ -164,6 +208,40 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_cs_tiles(const __grid_consta
         __syncthreads();
         copy_out_fp8T<VEC>(st, q_colT, M, K, mb, kb);
     });
+    if (DS) cta_max_to(mx, amax_rec, status);
+}
+
+// ---------------------------------------------------------------------------
+// Delayed scaling: the pair [alpha, s] for the next step from the window of
+// N recorded amaxes (a ring; slot pos is the latest).  algo 0: the largest
+// |entry| (bit patterns, a NaN entry wins); algo 1: |hist[pos]|.  Then the
+// current-scaling rule (amax 0 -> 1, overflowing alpha -> FLT_MAX).
+// ---------------------------------------------------------------------------
+constexpr int kDsThreads = 256;
+
+__global__ void __launch_bounds__(kDsThreads) k_ds_update(const float *__restrict__ hist, int64_t N, int64_t pos, int algo,
+                                                          float fmax, float *__restrict__ ds)
+{
+    uint32_t m = 0;
+    if (algo == 1) {
+        if (threadIdx.x == 0) m = __float_as_uint(hist[pos]) & 0x7FFFFFFFu;
+    } else {
+        for (int64_t i = threadIdx.x; i < N; i += kDsThreads) m = max(m, __float_as_uint(hist[i]) & 0x7FFFFFFFu);
+    }
+    m = warp_max(m);
+    __shared__ uint32_t red[kDsThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < kDsThreads / 32 ? red[lane] : 0u;
+        m = warp_max(m);
+        if (lane == 0) {
+            const float alpha = alpha_from_amax(fmax, __uint_as_float(m));
+            ds[0] = alpha;
+            ds[1] = __fdiv_rn(1.0f, alpha);
+        }
+    }
 }
 
 // Scales of an empty tensor.
@@ -198,17 +276,23 @@ cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *
     return cudaGetLastError();
 }
 
-template <int DT, int FMT>
-static cudaError_t cs_cast_t(const void *x, int64_t M, int64_t K, const float *amax, uint8_t *q_row,
-                             uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st)
+template <int DT, int FMT, bool DS>
+static cudaError_t cs_cast_t(const void *x, int64_t M, int64_t K, const float *amax, const float *ds, float *amax_rec,
+                             uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st)
 {
+    uint32_t *rec = reinterpret_cast<uint32_t *>(amax_rec);
+    if (DS) {
+        k_zero_word<<<1, 1, 0, st>>>(rec);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     if (q_colT == nullptr) {
         const int64_t n = M * K, nc = n / 16;
         int64_t blocks = (nc + 4 * 256 - 1) / (4 * 256);
         const int64_t cap = (int64_t)sm_count() * 8;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        k_cs_cast_flat<DT, FMT><<<(unsigned)blocks, 256, 0, st>>>(x, n, amax, q_row, scale, status);
+        k_cs_cast_flat<DT, FMT, DS><<<(unsigned)blocks, 256, 0, st>>>(x, n, amax, ds, rec, q_row, scale, status);
         return cudaGetLastError();
     }
     constexpr int TC = 32 * In<DT>::VEC;
@@ -217,25 +301,45 @@ static cudaError_t cs_cast_t(const void *x, int64_t M, int64_t K, const float *a
     if (e != cudaSuccess) return e;
     static bool attr = false;
     if (!attr) {
-        e = cudaFuncSetAttribute(k_cs_tiles<DT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
+        e = cudaFuncSetAttribute(k_cs_tiles<DT, FMT, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-    k_cs_tiles<DT, FMT><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, amax, q_row, q_colT, scale, status);
+    k_cs_tiles<DT, FMT, DS><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, amax, ds, rec, q_row, q_colT, scale, status);
     return cudaGetLastError();
+}
+
+template <bool DS>
+static cudaError_t cast_dispatch(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *amax, const float *ds,
+                                 float *amax_rec, uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status,
+                                 cudaStream_t st)
+{
+    if (dt == BF16) {
+        return fmt == E4M3 ? cs_cast_t<BF16, E4M3, DS>(x, M, K, amax, ds, amax_rec, q_row, q_colT, scale, status, st)
+                           : cs_cast_t<BF16, E5M2, DS>(x, M, K, amax, ds, amax_rec, q_row, q_colT, scale, status, st);
+    }
+    return fmt == E4M3 ? cs_cast_t<F32, E4M3, DS>(x, M, K, amax, ds, amax_rec, q_row, q_colT, scale, status, st)
+                       : cs_cast_t<F32, E5M2, DS>(x, M, K, amax, ds, amax_rec, q_row, q_colT, scale, status, st);
 }
 
 cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *amax,
                            uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st)
 {
-    if (dt == BF16) {
-        return fmt == E4M3 ? cs_cast_t<BF16, E4M3>(x, M, K, amax, q_row, q_colT, scale, status, st)
-                           : cs_cast_t<BF16, E5M2>(x, M, K, amax, q_row, q_colT, scale, status, st);
-    }
-    return fmt == E4M3 ? cs_cast_t<F32, E4M3>(x, M, K, amax, q_row, q_colT, scale, status, st)
-                       : cs_cast_t<F32, E5M2>(x, M, K, amax, q_row, q_colT, scale, status, st);
+    return cast_dispatch<false>(x, dt, M, K, fmt, amax, nullptr, nullptr, q_row, q_colT, scale, status, st);
+}
+
+cudaError_t launch_ds_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *ds, float *amax_rec,
+                           uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st)
+{
+    return cast_dispatch<true>(x, dt, M, K, fmt, nullptr, ds, amax_rec, q_row, q_colT, scale, status, st);
+}
+
+cudaError_t launch_ds_update(const float *hist, int64_t N, int64_t pos, int algo, int fmt, float *ds, cudaStream_t st)
+{
+    k_ds_update<<<1, kDsThreads, 0, st>>>(hist, N, pos, algo, fmt == E4M3 ? Fp8<E4M3>::FMAX : Fp8<E5M2>::FMAX, ds);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_empty_scales(float *amax_out, float *scale, cudaStream_t st)

@@ -123,6 +123,45 @@ q_status q_current_scaling(const void *x, q_dtype in, int64_t M, int64_t K, q_fp
     return Q_OK;
 }
 
+q_status q_delayed_scaling(const void *x, q_dtype in, int64_t M, int64_t K, q_fp8 fmt, uint8_t *q_row,
+                           uint8_t *q_colT, const float *ds, float *amax_out, float *scale, int32_t *status,
+                           q_stream_t stream)
+{
+    const char *fn = "q_delayed_scaling";
+    TRY(check_dims(fn, M, K));
+    TRY(check_in(fn, x, in, M * K));
+    if (fmt != Q_E4M3 && fmt != Q_E5M2) return fail(Q_ERR_ARG, "%s: fmt %d is not Q_E4M3 or Q_E5M2", fn, (int)fmt);
+    const int64_t n = M * K;
+    if (n > 0 && q_row == nullptr && q_colT == nullptr) return fail(Q_ERR_ARG, "%s: neither q_row nor q_colT requested", fn);
+    if (n > 0 && q_row != nullptr) TRY(need(fn, "q_row", q_row, 16));
+    if (n > 0 && q_colT != nullptr) {
+        TRY(need(fn, "q_colT", q_colT, 16));
+        TRY(multiple(fn, "M (with q_colT)", M, 16));
+        TRY(multiple(fn, "K (with q_colT)", K, 16));
+    }
+    TRY(need(fn, "ds", ds, 4));
+    TRY(need(fn, "amax_out", amax_out, 4));
+    TRY(need(fn, "scale", scale, 4));
+    // an empty tensor takes the flat path: it writes the scale and a zero amax
+    LAUNCH(fn, qk::launch_ds_cast(x, (int)in, n == 0 ? 0 : M, n == 0 ? 0 : K, (int)fmt, ds, amax_out, q_row,
+                                  n == 0 ? nullptr : q_colT, scale, status, S(stream)));
+    return Q_OK;
+}
+
+q_status q_delayed_scale_update(const float *hist, int64_t N, int64_t pos, q_hist_algo algo, q_fp8 fmt, float *ds,
+                                q_stream_t stream)
+{
+    const char *fn = "q_delayed_scale_update";
+    if (N < 1) return fail(Q_ERR_SHAPE, "%s: window length N = %lld must be >= 1", fn, (long long)N);
+    if (pos < 0 || pos >= N) return fail(Q_ERR_ARG, "%s: pos %lld is outside [0, %lld)", fn, (long long)pos, (long long)N);
+    if (algo != Q_HIST_MAX && algo != Q_HIST_MOST_RECENT) return fail(Q_ERR_ARG, "%s: bad algo %d", fn, (int)algo);
+    if (fmt != Q_E4M3 && fmt != Q_E5M2) return fail(Q_ERR_ARG, "%s: fmt %d is not Q_E4M3 or Q_E5M2", fn, (int)fmt);
+    TRY(need(fn, "hist", hist, 4));
+    TRY(need(fn, "ds", ds, 4));
+    LAUNCH(fn, qk::launch_ds_update(hist, N, pos, (int)algo, (int)fmt, ds, S(stream)));
+    return Q_OK;
+}
+
 q_status q_mxfp8(const void *x, q_dtype in, int64_t M, int64_t K, q_fp8 fmt, uint8_t *q_row, uint8_t *e8m0_row,
                  uint8_t *q_col, uint8_t *e8m0_col, int32_t *status, q_stream_t stream)
 {

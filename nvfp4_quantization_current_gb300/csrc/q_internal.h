@@ -25,6 +25,12 @@ cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt,
 cudaError_t launch_mxfp8(const void *x, int dt, int64_t M, int64_t K, int fmt, uint8_t *q_row,
                          uint8_t *e_row, uint8_t *q_col, uint8_t *e_col, int32_t *status, cudaStream_t st);
 
+// delayed scaling: cast with the pair ds = [alpha, s], recording max|x| into
+// *amax_rec (zeroed first); next pair from the window of N amaxes
+cudaError_t launch_ds_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *ds, float *amax_rec,
+                           uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st);
+cudaError_t launch_ds_update(const float *hist, int64_t N, int64_t pos, int algo, int fmt, float *ds, cudaStream_t st);
+
 // MXFP8 rowwise codes -> columnwise codes (dequantize + re-quantize)
 cudaError_t launch_mxfp8_requant_col(const uint8_t *q_row, const uint8_t *e_row, int64_t M, int64_t K, int fmt,
                                      uint8_t *q_col, uint8_t *e_col, int32_t *status, cudaStream_t st);

@@ -28,8 +28,9 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["q_amax", "q_current_scaling", "q_mxfp8", "q_blockwise", "q_nvfp4", "dq_current_scaling",
-              "dq_mxfp8", "dq_blockwise", "dq_nvfp4", "q_last_error", "q_abi_version"]:
+    for n in ["q_amax", "q_current_scaling", "q_delayed_scaling", "q_delayed_scale_update", "q_mxfp8",
+              "q_mxfp8_requant_col", "q_blockwise", "q_nvfp4", "dq_current_scaling", "dq_mxfp8", "dq_blockwise",
+              "dq_nvfp4", "q_last_error", "q_abi_version"]:
         assert n in names
 
 
@@ -70,6 +71,36 @@ def test_current_scaling_validation(L):
     assert st == Q.Q_ERR_ARG                       # amax required
     st, _ = status_of(L, "q_current_scaling", A, Q.Q_BF16, 4, 16, Q.Q_E4M3, A, None, A, 5, A, None, None)
     assert st == Q.Q_ERR_ARG                       # bad amax mode
+
+
+def test_delayed_scaling_validation(L):
+    st, _ = status_of(L, "q_delayed_scaling", A, Q.Q_BF16, 4, 16, Q.Q_E4M3, A, None, None, A, A, None, None)
+    assert st == Q.Q_ERR_ARG                       # ds required
+    st, _ = status_of(L, "q_delayed_scaling", A, Q.Q_BF16, 4, 16, Q.Q_E4M3, A, None, A, None, A, None, None)
+    assert st == Q.Q_ERR_ARG                       # amax_out required
+    st, _ = status_of(L, "q_delayed_scaling", A, Q.Q_BF16, 24, 16, Q.Q_E4M3, None, A, A, A, A, None, None)
+    assert st == Q.Q_ERR_SHAPE                     # colT needs M % 16
+    st, _ = status_of(L, "q_delayed_scaling", A, Q.Q_BF16, 4, 16, Q.Q_E4M3, None, None, A, A, A, None, None)
+    assert st == Q.Q_ERR_ARG                       # nothing requested
+    st, msg = status_of(L, "q_delayed_scale_update", A, 0, 0, Q.Q_HIST_MAX, Q.Q_E4M3, A, None)
+    assert st == Q.Q_ERR_SHAPE and ">= 1" in msg
+    st, _ = status_of(L, "q_delayed_scale_update", A, 16, 16, Q.Q_HIST_MAX, Q.Q_E4M3, A, None)
+    assert st == Q.Q_ERR_ARG                       # pos outside the window
+    st, _ = status_of(L, "q_delayed_scale_update", A, 16, 3, 7, Q.Q_E4M3, A, None)
+    assert st == Q.Q_ERR_ARG                       # bad algo
+    st, _ = status_of(L, "q_delayed_scale_update", A, 16, 3, Q.Q_HIST_MAX, Q.Q_E4M3, None, None)
+    assert st == Q.Q_ERR_ARG                       # ds required
+
+
+def test_requant_validation(L):
+    st, _ = status_of(L, "q_mxfp8_requant_col", A, A, 48, 64, Q.Q_E4M3, A, A, None, None)
+    assert st == Q.Q_ERR_SHAPE                     # M % 32
+    st, _ = status_of(L, "q_mxfp8_requant_col", A, A, 64, 48, Q.Q_E4M3, A, A, None, None)
+    assert st == Q.Q_ERR_SHAPE                     # K % 32
+    st, _ = status_of(L, "q_mxfp8_requant_col", MIS, A, 64, 64, Q.Q_E4M3, A, A, None, None)
+    assert st == Q.Q_ERR_ALIGN
+    st, _ = status_of(L, "q_mxfp8_requant_col", A, A, 64, 64, 4, A, A, None, None)
+    assert st == Q.Q_ERR_ARG
 
 
 def test_block_recipes_validation(L):

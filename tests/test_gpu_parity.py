@@ -155,6 +155,85 @@ def test_nonfinite_sets_status():
 
 
 # ---------------------------------------------------------------------------
+# per-tensor delayed scaling
+# ---------------------------------------------------------------------------
+
+DS_CASES = [
+    ((256, 512), True, O.E4M3, True, "max", 4),        # tiled row + colT, 2 x 2 tiles
+    ((96, 800), True, O.E5M2, True, "max", 3),         # ragged tiles
+    ((64, 416), False, O.E4M3, True, "most_recent", 2),  # FP32 input
+    ((100, 300), True, O.E4M3, False, "max", 4),       # rowwise only: flat path with a ragged tail (30000 % 16 = 0)
+    ((37, 53), False, O.E5M2, False, "max", 5),        # flat path, 1961 elements (tail of 9)
+]
+
+
+@pytest.mark.parametrize("shape,bf16,fmt,colwise,algo,N", DS_CASES)
+def test_delayed_scaling_steps_parity(shape, bf16, fmt, colwise, algo, N):
+    """Seven steps with tensors of changing range (an outlier step that must
+    leave the window after N steps): codes, s, the recorded amax and the
+    next [alpha, s] all bit-identical to the oracle's run."""
+    f = "e4m3" if fmt == O.E4M3 else "e5m2"
+    oalgo = O.HIST_MAX if algo == "max" else O.HIST_MOST_RECENT
+    state = Q.DelayedScaling(f, history_len=N, algo=algo)
+    hist = np.zeros(N, np.float32)
+    alpha, s = np.float32(1.0), np.float32(1.0)
+    for t, scale in enumerate([1.0, 300.0, 0.5, 2.0, 1e-3, 7.0, 1.0]):
+        x = W.gen("outliers", shape, 400 + t, bf16=False) * np.float32(scale)
+        x = O.bf16_round(x.astype(np.float32)) if bf16 else x.astype(np.float32)
+        q_row, q_colT, a = O.ds_cast(x, alpha, fmt, rowwise=True, colwise=colwise)
+        got = state.quantize(dev(x), rowwise=True, colwise=colwise)
+        torch.cuda.synchronize()
+        same(host(got.q_row), q_row, f"step {t} q_row")
+        if colwise:
+            same(host(got.q_colT), q_colT, f"step {t} q_colT")
+        f32eq(got.scale.item(), s, f"step {t} scale")
+        f32eq(got.amax.item(), a, f"step {t} amax")
+        hist[t % N] = a
+        alpha, s = O.ds_scale_update(hist, t % N, oalgo, fmt)
+        d = host(state.ds)
+        f32eq(d[0], alpha, f"step {t} next alpha")
+        f32eq(d[1], s, f"step {t} next s")
+    same(host(state.hist), hist, "window")
+
+
+@pytest.mark.parametrize("N", [1, 255, 1024, 1500])
+def test_delayed_scale_update_parity(N):
+    rng = np.random.default_rng(N)
+    h = (rng.lognormal(0, 6, N) * (rng.random(N) < 0.9)).astype(np.float32)   # zeros among them
+    hd = dev(h)
+    ds = torch.empty(2, dtype=torch.float32, device="cuda")
+    for fmt in (O.E4M3, O.E5M2):
+        for algo in (O.HIST_MAX, O.HIST_MOST_RECENT):
+            pos = int(rng.integers(0, N))
+            Q.q_delayed_scale_update(hd, pos, ds, "e4m3" if fmt == O.E4M3 else "e5m2", algo)
+            al, s = O.ds_scale_update(h, pos, algo, fmt)
+            d = host(ds)
+            f32eq(d[0], al, (N, fmt, algo))
+            f32eq(d[1], s, (N, fmt, algo))
+    h[N // 2] = 1e-45                                      # most recent: alpha overflows -> FLT_MAX
+    Q.q_delayed_scale_update(dev(h), N // 2, ds, "e4m3", "most_recent")
+    assert host(ds)[0] == np.finfo(np.float32).max
+    h[N // 3] = np.nan                                     # a NaN entry wins the max
+    Q.q_delayed_scale_update(dev(h), 0, ds, "e4m3", "max")
+    assert np.isnan(host(ds)[0])
+
+
+def test_delayed_scaling_empty_and_nonfinite():
+    ds = torch.tensor([2.0, 0.5], device="cuda")
+    a = torch.full((1,), 7.0, device="cuda")
+    got = Q.q_delayed_scaling(torch.empty((0, 16), dtype=torch.bfloat16, device="cuda"), ds, a)
+    assert got.amax.item() == 0.0 and got.scale.item() == 0.5
+    x = W.gen("normal", (32, 48), 3, bf16=False)
+    x[7, 9] = np.inf
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.q_delayed_scaling(dev(x), ds, a, colwise=True, status=st)
+    assert st.item() & Q.Q_ST_NONFINITE and a.item() == np.inf
+    st.zero_()
+    Q.q_delayed_scaling(dev(W.gen("normal", (32, 48), 3, bf16=False)), ds, a, status=st)
+    assert st.item() == 0
+
+
+# ---------------------------------------------------------------------------
 # MXFP8
 # ---------------------------------------------------------------------------
 
