@@ -84,6 +84,9 @@ def _L():
             "or_mxfp8": (None, [P, I, I64, I64, I, P, P, P, P]),
             "or_dq_mxfp8": (None, [P, P, I64, I64, I, I, I, P]),
             "or_mxfp8_requant_col": (None, [P, P, I64, I64, I, P, P]),
+            "or_rht16": (None, [P, U32]),
+            "or_rht_cols": (None, [P, I, I64, I64, U32, P]),
+            "or_nvfp4_rht_colT": (None, [P, I, I64, I64, U32, I, U64, U64, P, P, P, P, P]),
             "or_ds_cast": (None, [P, I, I64, I64, I, F, P, P, P]),
             "or_ds_scale_update": (None, [P, I64, I64, I, I, P, P]),
             "or_blockwise": (None, [P, I, I64, I64, I, P, P, P, P]),
@@ -374,6 +377,37 @@ def nvfp4(x, blk=B1x16, rnd=RN, seed=0, offset=0, rowwise=True, colwise=False, a
     _L().or_nvfp4(_p(x), dt, M, K, blk, rnd, seed, offset, _p(a_in),
                   _p(q_row), _p(sb_row), _p(q_colT), _p(sb_colT), _p(a_out), _p(s_out))
     return NV(q_row, sb_row, q_colT, sb_colT, a_out[0], s_out[0])
+
+
+def rht16(v, sign_mask):
+    """The 16-point random Hadamard transform of one group (float32[16])."""
+    v = np.array(v, np.float32).copy()
+    assert v.size == 16
+    _L().or_rht16(_p(v), int(sign_mask) & 0xFFFF)
+    return v
+
+
+def rht_cols(x, sign_mask):
+    """FP32 [M, K]: the transform along M of every column's 16-row groups."""
+    x, dt = _x(x)
+    M, K = x.shape
+    xr = np.empty((M, K), np.float32)
+    _L().or_rht_cols(_p(x), dt, M, K, int(sign_mask) & 0xFFFF, _p(xr))
+    return xr
+
+
+def nvfp4_rht_colT(x, sign_mask, rnd=RN, seed=0, offset=0, amax_in=None):
+    """Columnwise NVFP4 copy of the transformed tensor: (q_colT [K, M/2],
+    sb_colT [K, M/16], amax of the transformed tensor, s_global)."""
+    x, dt = _x(x)
+    M, K = x.shape
+    q_colT = np.zeros((K, M // 2), np.uint8)
+    sb_colT = np.empty((K, M // 16), np.uint8)
+    a_out, s_out = _fbuf(), _fbuf()
+    a_in = None if amax_in is None else _fbuf(amax_in)
+    _L().or_nvfp4_rht_colT(_p(x), dt, M, K, int(sign_mask) & 0xFFFF, rnd, seed, offset, _p(a_in), _p(q_colT),
+                           _p(sb_colT), _p(a_out), _p(s_out))
+    return q_colT, sb_colT, a_out[0], s_out[0]
 
 
 def dq_nvfp4(q, sb, s_global, blk=B1x16, out=F32):

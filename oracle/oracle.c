@@ -47,6 +47,9 @@
  *            empty window, uses alpha = s = 1).
  *   R-REQ    MXFP8 row-to-column re-quantization dequantizes with the 1x32
  *            scales to FP32 and re-quantizes that tensor in 32x1 blocks.
+ *   R-RHT    the random Hadamard transform of the wgrad inputs: 16-point,
+ *            along M on the 16x1 blocks, signs from a 16-bit mask, FP32
+ *            butterfly with strides 1, 2, 4, 8, then 1/4 (see or_rht16).
  *
  * Parity status: every function below is pinned by the tests in tests/
  * (worked examples, brute-force nearest-value search, library casts,
@@ -755,6 +758,70 @@ void or_nvfp4(const void *x, int dtype, int64_t M, int64_t K, int blk, int rnd,
     }
     if (amax_out) *amax_out = A;
     if (s_g_out) *s_g_out = s_g;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Random Hadamard transform before the NVFP4 columnwise (wgrad) copy        */
+/* ------------------------------------------------------------------------ */
+/*
+ * [LP] section 2.4 (NVFP4 recipe, item 3) and section 5.6: the inputs of
+ * the weight-gradient GEMM go through a Random Hadamard Transform before
+ * FP4 quantization, so that a block-level outlier is spread out and no
+ * longer sets the amax of its whole block.  The pages fix nothing else; the
+ * readings taken (R-RHT):
+ *   - the transform is 16-point (the NVFP4 block length): x' = (1/4) H D x
+ *     with H the 16 x 16 Sylvester Hadamard matrix (H[i][j] = (-1)^popcount(i
+ *     & j)) and D = diag(s), s_j = -1 where bit j of a 16-bit sign mask is
+ *     set (the random signs are an input);
+ *   - it runs along M, the contraction dimension of the wgrad GEMM, on each
+ *     group of 16 consecutive rows of every column, i.e. on exactly the 16x1
+ *     blocks of the columnwise copy (H is orthogonal, so the GEMM product is
+ *     unchanged);
+ *   - arithmetic: the signs, then the fast Walsh-Hadamard butterfly in FP32
+ *     with strides 1, 2, 4, 8 ((a, b) -> (a + b, a - b), one rounding per
+ *     operation), then the exact factor 1/4;
+ *   - the transformed copy is quantized like any columnwise NVFP4 copy, with
+ *     its own tensor amax.
+ */
+void or_rht16(float *v, uint32_t sign_mask)
+{
+    for (int j = 0; j < 16; j++)
+        if ((sign_mask >> j) & 1u) v[j] = -v[j];
+    for (int h = 1; h < 16; h *= 2)
+        for (int i = 0; i < 16; i++)
+            if ((i & h) == 0) {
+                float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+    for (int j = 0; j < 16; j++) v[j] = v[j] * 0.25f;
+}
+
+/* xr[m][k] (FP32, [M, K], M % 16 == 0): the transform of every column's
+ * 16-row groups. */
+void or_rht_cols(const void *x, int dtype, int64_t M, int64_t K, uint32_t sign_mask, float *xr)
+{
+    float v[16];
+    for (int64_t g = 0; g < M / 16; g++)
+        for (int64_t k = 0; k < K; k++) {
+            for (int i = 0; i < 16; i++) v[i] = load_x(x, dtype, (16 * g + i) * K + k);
+            or_rht16(v, sign_mask);
+            for (int i = 0; i < 16; i++) xr[(16 * g + i) * K + k] = v[i];
+        }
+}
+
+/* The columnwise NVFP4 copy (1x16 blocks along M, stored [K, M/2] with
+ * sb_colT [K, M/16]) of the transformed tensor, rounding rnd (stochastic
+ * draws indexed as for or_nvfp4's columnwise copy).  amax_in: the amax of
+ * the transformed tensor if given (sharded case), else computed. */
+void or_nvfp4_rht_colT(const void *x, int dtype, int64_t M, int64_t K, uint32_t sign_mask, int rnd, uint64_t seed,
+                       uint64_t offset, const float *amax_in, uint8_t *q_colT, uint8_t *sb_colT, float *amax_out,
+                       float *s_g_out)
+{
+    float *xr = (float *)malloc((size_t)(M * K > 0 ? M * K : 1) * sizeof(float));
+    or_rht_cols(x, dtype, M, K, sign_mask, xr);
+    or_nvfp4(xr, OR_F32, M, K, 0, rnd, seed, offset, amax_in, NULL, NULL, q_colT, sb_colT, amax_out, s_g_out);
+    free(xr);
 }
 
 /* x_hat = q * (sb * s_g), the block factor formed once per block.
