@@ -7,7 +7,8 @@ workloads of ``workloads.WORKLOADS``): current-scaling amax + cast (+ the
 transposed copy), delayed scaling (one read + the window update), MXFP8
 row + col and the row->col re-quantize, blockwise 1x128 (+ transposed) and
 128x128 (+ transposed), NVFP4 1x16 RTNE, 1x16 stochastic rounding and 16x16,
-and the dequantizer of each.  Every call goes through the C ABI with
+the dequantizer of each, and the random-Hadamard NVFP4 columnwise copies of
+the NVFP4 activation and gradient (weight-gradient GEMM inputs).  Every call goes through the C ABI with
 preallocated outputs.
 
 Metric: quantize GB/s = algorithmic bytes (input bytes x reads + all output
@@ -47,6 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 CPU_SAMPLE_FRAC = 1.0 / 8.0
 REF_BUDGET_S = 120.0
+RHT_MASK = 0xB4E1   # the 16 random signs of the Hadamard transform (any fixed draw)
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, keyed by kernel, with the hash of the kernel's source file at
@@ -189,6 +191,23 @@ def build_step(dev_tensors, torch, Q):
                           [("dq_nvfp4", "k_dequant.cu", nbytes(out.q_row, out.sb_row, y), r)],
                           [out.q_row, out.sb_row, out.s_global], [y], r))
 
+    def rht(tag, x, rnd, seed, mask=RHT_MASK):
+        out = Q.alloc_nvfp4(x.shape[0], x.shape[1], x.device, "1x16", rowwise=False, colwise=True)
+        amax = out.amax
+        ins = nbytes(x)
+        pieces = [
+            ("rht_amax", "k_nvfp4.cu", ins, lambda: Q.q_nvfp4_rht_amax(x, mask, out=amax)),
+            (f"nvfp4_rht_colT_{rnd}", "k_nvfp4.cu", ins + nbytes(out.q_colT, out.sb_colT, out.s_global) + 4,
+             lambda: Q.q_nvfp4_rht_colT(x, mask, rnd, seed, 0, amax=amax, out=out)),
+        ]
+
+        def e2e():
+            o = Q.q_nvfp4_rht_colT(x, mask, rnd, seed, 0, out=out)
+            o.amax = amax
+            return o
+        calls.append(Call(f"{tag} nvfp4_rht_{rnd} colT", "nvfp4_rht", pieces, [x],
+                          [out.q_colT, out.sb_colT, out.s_global], e2e))
+
     if "cs1" in d:
         cs("cs1.x", d["cs1"]["x"], "e4m3", True)
     if "mx2" in d:
@@ -204,6 +223,8 @@ def build_step(dev_tensors, torch, Q):
         nv("nv5.act", d["nv5"]["act"], "1x16", "rn", 0)
         nv("nv5.grad", d["nv5"]["grad"], "1x16", "sr", 4)
         nv("nv5.w", d["nv5"]["w"], "16x16", "rn", 0)
+        rht("nv5.act", d["nv5"]["act"], "rn", 0)
+        rht("nv5.grad", d["nv5"]["grad"], "sr", 4)
     return calls
 
 
@@ -236,7 +257,8 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
     for wl, tn, kind in [("cs1", "x", "cs_e4m3"), ("hy4", "grad", "cs_e5m2"), ("hy4", "grad", "ds_e5m2"),
                          ("hy4", "w", "cs_e4m3"),
                          ("mx2", "act", "mx"), ("bw3", "act", "bw1"), ("bw3", "w", "bw128"),
-                         ("nv5", "act", "nv_rn"), ("nv5", "grad", "nv_sr"), ("nv5", "w", "nv16")]:
+                         ("nv5", "act", "nv_rn"), ("nv5", "grad", "nv_sr"), ("nv5", "w", "nv16"),
+                         ("nv5", "act", "rht_rn"), ("nv5", "grad", "rht_sr")]:
         xh, xd = host_tensors[wl][tn], dev_tensors[wl][tn]
         M, K = xh.shape
         r0 = band(M)
@@ -257,6 +279,16 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
                 hist[t] = A
                 alpha, s = O.ds_scale_update(hist, t, O.HIST_MAX, O.E5M2)
                 eq(host(st.ds), np.array([alpha, s], np.float32), f"{wl}.{tn} delayed step {t} next scale")
+        elif kind.startswith("rht"):
+            rnd = O.SR if kind == "rht_sr" else O.RN
+            A = O.amax(O.rht_cols(xh, RHT_MASK))
+            g = Q.q_nvfp4_rht_colT(xd, RHT_MASK, "sr" if rnd == O.SR else "rn", 4 if rnd == O.SR else 0, 0)
+            eq(np.float32(g.amax.item()), np.float32(A), f"{wl}.{tn} rht amax")
+            q, sb, _, sg = O.nvfp4_rht_colT(xs, RHT_MASK, O.RN, amax_in=A)
+            eq(np.float32(g.s_global.item()), sg, f"{wl}.{tn} rht s_global")
+            eq(host(g.sb_colT[:, r0 // 16:(r0 + rows) // 16]), sb, f"{wl}.{tn} rht sb_colT band")
+            if rnd == O.RN:   # SR draws depend on the full-height index k*M + m: scales only
+                eq(host(g.q_colT[:, r0 // 2:(r0 + rows) // 2]), q, f"{wl}.{tn} rht q_colT band")
         elif kind.startswith("cs"):
             fmt = O.E5M2 if kind == "cs_e5m2" else O.E4M3
             A = O.amax(xh)
@@ -522,9 +554,9 @@ def run_ours(args):
                 "frac": round(achieved / peak, 3), "traffic": traffic,
                 "alg_bytes_per_launch": int(dom_bytes), "us_per_launch": round(dom_us, 2),
                 "share_of_step": round(dom_us / (step_ms * 1e3), 3), "peak_kind": peak_kind + " hbm_gbs"}
-    # q_amax and the delayed-scaling cast launch two kernels (zero the amax
-    # word, then the pass); every other call one
-    n_launches = args.steps * sum((2 if p[0] in ("amax", "ds_cast_T") else 1) for c in calls for p in c.pieces)
+    # q_amax, the delayed-scaling cast and the transform's amax launch two
+    # kernels (zero the amax word, then the pass); every other call one
+    n_launches = args.steps * sum((2 if p[0] in ("amax", "ds_cast_T", "rht_amax") else 1) for c in calls for p in c.pieces)
 
     # ---- end to end: pinned host input -> device, the public call, outputs -> pinned host
     e2e = None
@@ -587,7 +619,7 @@ def run_ours(args):
             "config": {"workload": "all five workloads at full size per step: cs1 FP32 1024x1024 CS-E4M3+T; "
                                    "mx2 BF16 8192x4096 MXFP8 row+col, row->col requant; bw3 BF16 16384x7168 1x128+T and 7168x18432 "
                                    "128x128+T; hy4 BF16 8192x14336 CS-E5M2+T, delayed-scaling E5M2+T (window 1024, max) and 14336x4096 CS-E4M3+T; nv5 BF16 "
-                                   "8192x4096 NVFP4 1x16 RN+T, 1x16 SR+T, 4096x4096 16x16 RN+T; each with a dequant",
+                                   "8192x4096 NVFP4 1x16 RN+T, 1x16 SR+T, 4096x4096 16x16 RN+T; each with a dequant; nv5 act/grad random-Hadamard NVFP4 colT (RN / SR)",
                        "l2": "flushed (256 MiB write) before every timed call",
                        "scale_rows": args.scale_rows, "parallelism": f"replicas x{world} (independent tensors)"},
             "parity": parity,
@@ -642,6 +674,11 @@ def oracle_sample_work(host_t, frac):
         work.append((lambda: O.ds_cast(s, alpha, fmt, True, True), s.nbytes + 2 * M * K + 16))
         work.append((lambda: O.ds_scale_update(hist, 0, O.HIST_MAX, fmt), hist.nbytes + 8))
 
+    def rht(a, rnd, seed):
+        s = np.ascontiguousarray(a[:rows(a)])
+        M, K = s.shape
+        work.append((lambda: O.nvfp4_rht_colT(s, RHT_MASK, rnd, seed=seed), 2 * s.nbytes + M * K // 2 + M * K // 16 + 4))
+
     def mx(a):
         s = np.ascontiguousarray(a[:rows(a)])
         M, K = s.shape
@@ -677,6 +714,8 @@ def oracle_sample_work(host_t, frac):
     nv(host_t["nv5"]["act"], O.B1x16, O.RN, 0)
     nv(host_t["nv5"]["grad"], O.B1x16, O.SR, 4)
     nv(host_t["nv5"]["w"], O.B16x16, O.RN, 0)
+    rht(host_t["nv5"]["act"], O.RN, 0)
+    rht(host_t["nv5"]["grad"], O.SR, 4)
     return work
 
 

@@ -227,6 +227,35 @@ q_status q_nvfp4(const void *x, q_dtype in, int64_t M, int64_t K, q_nvblk blk, q
                  int32_t *status, q_stream_t stream);
 
 /*
+ * NVFP4 columnwise copy of the random-Hadamard-transformed tensor, for the
+ * inputs of the weight-gradient GEMM ([LP] section 2.4, recipe item 3, and
+ * section 5.6: the transform spreads block-level outliers before FP4
+ * quantization).  x' = (1/4) H D x on every group of 16 consecutive rows of
+ * each column (H the 16 x 16 Sylvester Hadamard matrix, D = diag(s) with
+ * s_j = -1 where bit j of sign_mask is set), computed as the signs, the
+ * FP32 butterfly with strides 1, 2, 4, 8, and the factor 1/4.  The groups
+ * are the 16x1 blocks of the columnwise copy; H is orthogonal, so applying
+ * the same transform to both wgrad operands leaves their product unchanged.
+ * Then exactly the columnwise part of q_nvfp4 (Q_B1x16, rounding rnd,
+ * stochastic draws of stream 1 indexed k * M + m) on x':
+ *   q_colT [K, M/2], sb_colT [K, M/16] (written);
+ *   amax   one float: max|x'| written (Q_AMAX_COMPUTE, an extra read of x)
+ *          or read (Q_AMAX_GIVEN, e.g. all-reduced over shards);
+ *   s_global one float, written.
+ * The rowwise (fprop) copy is quantized without the transform (q_nvfp4).
+ * Shapes: M % 16 == 0, K % 16 == 0.
+ */
+/* max|x'| of the same transform (the amax q_nvfp4_rht_colT computes in
+ * Q_AMAX_COMPUTE mode), for a caller that all-reduces it over shards first.
+ * amax: one float, written.  Shapes as q_nvfp4_rht_colT. */
+q_status q_nvfp4_rht_amax(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, float *amax,
+                          int32_t *status, q_stream_t stream);
+
+q_status q_nvfp4_rht_colT(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, q_round rnd,
+                          uint64_t seed, uint64_t offset, uint8_t *q_colT, uint8_t *sb_colT,
+                          float *amax, q_amax_mode amax_mode, float *s_global, int32_t *status, q_stream_t stream);
+
+/*
  * a12: dequantizers.  Output y [R, C] in `out` (Q_F32, or Q_BF16 rounded to
  * nearest even from the FP32 value).  A transposed columnwise output is
  * passed as the [K, M] matrix it is (R = K, C = M).

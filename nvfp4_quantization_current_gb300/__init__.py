@@ -25,7 +25,10 @@ Recipes (each with its dequantizer, rowwise and columnwise outputs):
   (same page, recipe 4);
 * :func:`q_nvfp4` -- E2M1 with E4M3 1x16 / 16x16 block scales and an FP32
   tensor scale, RTNE or stochastic rounding (same page, "NVFP4"; "From BF16
-  to FP8/FP4 ...", section 2.4).
+  to FP8/FP4 ...", section 2.4);
+* :func:`q_nvfp4_rht_colT` -- the columnwise NVFP4 copy of the random
+  Hadamard transform of x, for the weight-gradient GEMM inputs ("From BF16
+  to FP8/FP4 ...", sections 2.4 and 5.6).
 """
 from __future__ import annotations
 
@@ -54,7 +57,7 @@ STATUS_NAMES = {Q_OK: "Q_OK", Q_ERR_ARG: "Q_ERR_ARG", Q_ERR_SHAPE: "Q_ERR_SHAPE"
                 Q_ERR_DTYPE: "Q_ERR_DTYPE", Q_ERR_CUDA: "Q_ERR_CUDA"}
 
 # every exported entry point: name -> (restype, argtypes)
-_P, _I64, _I, _U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+_P, _I64, _I, _U64, _U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32
 SIGNATURES = {
     "q_last_error": (ctypes.c_char_p, []),
     "q_abi_version": (_I, []),
@@ -66,6 +69,8 @@ SIGNATURES = {
     "q_mxfp8_requant_col": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
     "q_blockwise": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "q_nvfp4": (_I, [_P, _I, _I64, _I64, _I, _I, _U64, _U64, _P, _P, _P, _P, _P, _I, _P, _P, _P]),
+    "q_nvfp4_rht_amax": (_I, [_P, _I, _I64, _I64, _U32, _P, _P, _P]),
+    "q_nvfp4_rht_colT": (_I, [_P, _I, _I64, _I64, _U32, _I, _U64, _U64, _P, _P, _P, _I, _P, _P, _P]),
     "dq_current_scaling": (_I, [_P, _P, _I64, _I64, _I, _I, _P, _P]),
     "dq_mxfp8": (_I, [_P, _P, _I64, _I64, _I, _I, _I, _P, _P]),
     "dq_blockwise": (_I, [_P, _P, _I64, _I64, _I, _I, _P, _P]),
@@ -425,6 +430,41 @@ def q_nvfp4(x: torch.Tensor, blk="1x16", rounding="rn", seed=0, offset=0, rowwis
     return out
 
 
+def q_nvfp4_rht_amax(x: torch.Tensor, sign_mask: int, out: Optional[torch.Tensor] = None,
+                     status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """max|x'| of the random Hadamard transform that :func:`q_nvfp4_rht_colT`
+    applies (one-element FP32 device tensor), e.g. to all-reduce over shards
+    and pass back as its ``amax``."""
+    dt = _in(x)
+    M, K = x.shape
+    out = _f32((1,), x.device) if out is None else out
+    _call("q_nvfp4_rht_amax", _ptr(x), dt, M, K, int(sign_mask), _ptr(out), _ptr(status), _stream(x.device))
+    return out
+
+
+def q_nvfp4_rht_colT(x: torch.Tensor, sign_mask: int, rounding="rn", seed=0, offset=0,
+                     amax: Optional[torch.Tensor] = None, out: Optional[NVFP4Tensor] = None,
+                     status: Optional[torch.Tensor] = None) -> NVFP4Tensor:
+    """Columnwise NVFP4 copy (1x16 blocks along M, stored [K, M/2]) of the
+    random Hadamard transform of x: (1/4) H D on each 16-row group of every
+    column, D the signs of the 16-bit ``sign_mask``.  For the inputs of the
+    weight-gradient GEMM; use the same mask for both of its operands.
+    ``amax`` (one-element device tensor) gives the transformed tensor's
+    amax instead of computing it.  Returns an NVFP4Tensor with only the
+    columnwise half set."""
+    dt = _in(x)
+    M, K = x.shape
+    out = alloc_nvfp4(M, K, x.device, "1x16", rowwise=False, colwise=True) if out is None else out
+    rnd = {"rn": Q_RN, "sr": Q_SR, Q_RN: Q_RN, Q_SR: Q_SR}[rounding]
+    mode = Q_AMAX_COMPUTE
+    if amax is not None:
+        out.amax = amax
+        mode = Q_AMAX_GIVEN
+    _call("q_nvfp4_rht_colT", _ptr(x), dt, M, K, int(sign_mask), rnd, int(seed), int(offset), _ptr(out.q_colT),
+          _ptr(out.sb_colT), _ptr(out.amax), mode, _ptr(out.s_global), _ptr(status), _stream(x.device))
+    return out
+
+
 def dq_nvfp4(q, sb, s_global, blk="1x16", dtype=torch.float32, out=None):
     R, C = q.shape[0], q.shape[1] * 2
     y = torch.empty((R, C), dtype=dtype, device=q.device) if out is None else out
@@ -433,4 +473,5 @@ def dq_nvfp4(q, sb, s_global, blk="1x16", dtype=torch.float32, out=None):
 
 
 __all__ = [n for n in dir() if n.startswith(("q_", "dq_", "alloc_", "Q_"))] + [
-    "CurrentScalingTensor", "MXFP8Tensor", "BlockwiseTensor", "NVFP4Tensor", "QuantError", "lib", "SIGNATURES"]
+    "CurrentScalingTensor", "DelayedScaling", "MXFP8Tensor", "BlockwiseTensor", "NVFP4Tensor", "QuantError", "lib",
+    "SIGNATURES"]

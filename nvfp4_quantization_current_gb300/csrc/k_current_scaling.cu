@@ -79,26 +79,6 @@ __global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict
     }
 }
 
-// CTA-wide max of m (blockDim.x a multiple of 32, at most 1024 threads),
-// then one atomicMax into *dst from a CTA that raises it; a non-finite
-// result is reported in *status.
-QD void cta_max_to(uint32_t m, uint32_t *dst, int32_t *status)
-{
-    __shared__ uint32_t red[32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    m = warp_max(m);
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    if (warp == 0) {
-        m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
-        m = warp_max(m);
-        if (lane == 0) {
-            if (m > *reinterpret_cast<volatile uint32_t *>(dst)) atomicMax(dst, m);
-            flag_nonfinite(status, m);
-        }
-    }
-}
-
 // alpha of the cast: from the amax (current scaling) or the pair [alpha, s]
 // (delayed scaling); CTA 0 writes s and reports a non-finite amax or alpha.
 template <int FMT, bool DS>
@@ -258,6 +238,12 @@ __global__ void k_empty_scales(float *amax_out, float *scale)
 // Zeroes the amax word before the reduction (a kernel on the same stream: the
 // next kernel starts right behind it, which a driver memset does not).
 __global__ void k_zero_word(uint32_t *w) { *w = 0u; }
+
+cudaError_t launch_zero_word(float *w, cudaStream_t st)
+{
+    k_zero_word<<<1, 1, 0, st>>>(reinterpret_cast<uint32_t *>(w));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *status, cudaStream_t st)
 {

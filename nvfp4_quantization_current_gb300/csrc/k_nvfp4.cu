@@ -129,6 +129,31 @@ QD void copy_out_fp4T(const uint8_t *stage, uint8_t *q_colT, int64_t M, int64_t 
     }
 }
 
+// Columnwise block scales of a tile, sSB[g][col] for the 16-row group g of
+// tile column col, written as sb_colT[kb + col][mb/16 + g].
+template <int TC>
+QD void copy_out_sbT(const uint8_t (*sSB)[TC], uint8_t *sb_colT, int64_t M, int64_t K, int64_t mb, int64_t kb)
+{
+    const int64_t left = (M - mb) / 16;
+    const int nb = left < 8 ? (int)left : 8;
+    for (int col = threadIdx.x; col < TC; col += kEngThreads) {
+        const int64_t kg = kb + col;
+        if (kg >= K) continue;
+        uint8_t *dst = sb_colT + kg * (M / 16) + mb / 16;
+        if (nb == 8 && (M % 128) == 0) {
+            uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                w0 |= (uint32_t)sSB[q][col] << (8 * q);
+                w1 |= (uint32_t)sSB[q + 4][col] << (8 * q);
+            }
+            stg8(dst, w0, w1);
+        } else {
+            for (int q = 0; q < nb; q++) dst[q] = sSB[q][col];
+        }
+    }
+}
+
 template <int DT, int BLK, int RND>
 __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
                                                           const float *__restrict__ amax, uint64_t seed, uint64_t offset,
@@ -280,26 +305,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
         park_fp4T<VEC>(st, colw, warp, lane);
         __syncthreads();
         copy_out_fp4T<VEC>(st, q_colT, M, K, mb, kb);
-        if constexpr (BLK == 0) {
-            const int64_t left = (M - mb) / 16;
-            const int nb = left < 8 ? (int)left : 8;
-            for (int col = t; col < TC; col += kEngThreads) {
-                const int64_t kg = kb + col;
-                if (kg >= K) continue;
-                uint8_t *dst = sb_colT + kg * (M / 16) + tm * 8;
-                if (nb == 8 && (M % 128) == 0) {
-                    uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        w0 |= (uint32_t)sSB[q][col] << (8 * q);
-                        w1 |= (uint32_t)sSB[q + 4][col] << (8 * q);
-                    }
-                    stg8(dst, w0, w1);
-                } else {
-                    for (int q = 0; q < nb; q++) dst[q] = sSB[q][col];
-                }
-            }
-        }
+        if constexpr (BLK == 0) copy_out_sbT<TC>(sSB, sb_colT, M, K, mb, kb);
     });
 }
 
@@ -343,6 +349,203 @@ cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, i
     if (blk == 0) return rnd == 0 ? nv_t<F32, 0, 0>(NV_ARGS) : nv_t<F32, 0, 1>(NV_ARGS);
     return rnd == 0 ? nv_t<F32, 1, 0>(NV_ARGS) : nv_t<F32, 1, 1>(NV_ARGS);
 #undef NV_ARGS
+}
+
+// ---------------------------------------------------------------------------
+// Random Hadamard transform + columnwise NVFP4 of the result ("From BF16 to
+// FP8/FP4 ...", sections 2.4 and 5.6: RHT on the weight-gradient GEMM
+// inputs, to spread block-level outliers before FP4 quantization).
+// x' = (1/4) H D x on every 16-row group of every column (H the 16-point
+// Sylvester Hadamard matrix, D the signs of a 16-bit mask): signs, then the
+// butterfly with strides 1, 2, 4, 8 in FP32, then the exact factor 1/4.
+// The 16x1 blocks of the columnwise copy are exactly these groups.
+// Thread t of a tile owns group g = t / 64 and 8 bytes of each of its 16
+// rows (CPT = 4 BF16 or 2 FP32 columns), so a block never leaves its thread;
+// column pairs go through the butterfly as packed FP32x2 operations.
+// PASS 0 reduces max|x'| (the tensor amax of the transformed copy) into
+// *amax; PASS 1 encodes with the tensor scale from *amax, parks the codes in
+// the consumed stage and writes q_colT rows (as k_nvfp4 does).
+// ---------------------------------------------------------------------------
+template <int DT, int RND, int PASS>
+__global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_constant__ CUtensorMap tmap, int64_t M,
+                                                              int64_t K, uint32_t sign_mask, float *amax, uint64_t seed,
+                                                              uint64_t offset, uint8_t *__restrict__ q_colT,
+                                                              uint8_t *__restrict__ sb_colT, float *__restrict__ s_global,
+                                                              int32_t *status)
+{
+    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CPT = VEC / 2;
+    __shared__ float enc_tab[128];
+    __shared__ uint8_t sSB[8][TC];
+    float alpha_g = 1.0f;
+    if (PASS == 1) {
+        const float A = *amax;
+        alpha_g = alpha_from_amax(2688.0f, A);
+        if (threadIdx.x < 128) {
+            const float sv = e4m3_value(threadIdx.x);
+            enc_tab[threadIdx.x] = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_g, sv);
+        }   // visible after the engine's first barrier
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            *s_global = __fdiv_rn(1.0f, alpha_g);
+            flag_nonfinite(status, __float_as_uint(A) & 0x7FFFFFFFu);
+        }
+    }
+    if (M == 0 || K == 0) return;
+    const int g = threadIdx.x >> 6, q = threadIdx.x & 63;
+    const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
+    uint32_t mx = 0;   // PASS 0: max |x'| bits of this thread (zero-filled rows and columns give 0)
+
+    run_tiles(&tmap, tiles_m, tiles_k, TC, PASS == 1, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
+        const int64_t mb = tm * kTileRowsE, kb = tk * TC;
+        uint2 raw[16];
+#pragma unroll
+        for (int r = 0; r < 16; r++) raw[r] = *reinterpret_cast<const uint2 *>(st + (16 * g + r) * kRowBytes + q * 8);
+        uint32_t code[CPT][2];   // per column: rows 16g..16g+7 and 16g+8..16g+15, first row in bits 3-0
+#pragma unroll
+        for (int p = 0; p < CPT / 2; p++) {   // column pair (2p, 2p+1) of the thread's CPT columns
+            float a[16], b[16];
+#pragma unroll
+            for (int r = 0; r < 16; r++) {
+                const uint32_t neg = ((sign_mask >> r) & 1u) << 31;
+                if (DT == BF16) {
+                    const uint32_t w = p == 0 ? raw[r].x : raw[r].y;
+                    a[r] = __uint_as_float((w << 16) ^ neg);
+                    b[r] = __uint_as_float((w & 0xFFFF0000u) ^ neg);
+                } else {
+                    a[r] = __uint_as_float(raw[r].x ^ neg);
+                    b[r] = __uint_as_float(raw[r].y ^ neg);
+                }
+            }
+#pragma unroll
+            for (int h = 1; h < 16; h *= 2)
+#pragma unroll
+                for (int i = 0; i < 16; i++)
+                    if ((i & h) == 0) bfly2(a[i], b[i], a[i + h], b[i + h]);
+#pragma unroll
+            for (int i = 0; i < 16; i++) mul2(a[i], b[i], 0.25f, 0.25f);
+            if (PASS == 0) {
+#pragma unroll
+                for (int i = 0; i < 16; i++) mx = max(mx, __float_as_uint(fmax_abs(a[i], b[i])) & 0x7FFFFFFFu);
+                continue;
+            }
+            // block scales and encode factors of the two columns
+            float ma = 0.0f, mbx = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                ma = fmax_abs(ma, a[i]);
+                mbx = fmax_abs(mbx, b[i]);
+            }
+            const uint32_t ba = __float_as_uint(ma) & 0x7FFFFFFFu, bb = __float_as_uint(mbx) & 0x7FFFFFFFu;
+            const uint32_t sa = nv_sb_code<F32>(ba, alpha_g, nullptr, 0), sbb = nv_sb_code<F32>(bb, alpha_g, nullptr, 0);
+            const float ea = enc_tab[sa], eb = enc_tab[sbb];
+            const int c0 = q * CPT + 2 * p;   // tile column of a
+            sSB[g][c0] = (uint8_t)sa;
+            sSB[g][c0 + 1] = (uint8_t)sbb;
+            const bool live = mb + 16 * g < M;
+            post_nonfinite(status, live && (kb + c0 < K) ? nonfinite(ba) | nonfinite(bb) : 0u);
+#pragma unroll
+            for (int i = 0; i < 16; i++) mul2(a[i], b[i], ea, eb);
+            if constexpr (RND == 1) {
+                // elements k * M + m of the transposed layout, stream 1: two Philox blocks per column
+                const int64_t m = mb + 16 * g;
+#pragma unroll
+                for (int hh = 0; hh < 2; hh++) {
+                    const uint4 Ra = sr_bits(seed, offset + (uint64_t)(((kb + c0) * M + m + 8 * hh) >> 3), 1u);
+                    const uint4 Rb = sr_bits(seed, offset + (uint64_t)(((kb + c0 + 1) * M + m + 8 * hh) >> 3), 1u);
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        a[8 * hh + j] = sr_e2m1_value(a[8 * hh + j], r16_of(Ra, j));
+                        b[8 * hh + j] = sr_e2m1_value(b[8 * hh + j], r16_of(Rb, j));
+                    }
+                }
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                code[2 * p][hh] = cvt_fp4x8(a[8 * hh], a[8 * hh + 1], a[8 * hh + 2], a[8 * hh + 3], a[8 * hh + 4],
+                                            a[8 * hh + 5], a[8 * hh + 6], a[8 * hh + 7]);
+                code[2 * p + 1][hh] = cvt_fp4x8(b[8 * hh], b[8 * hh + 1], b[8 * hh + 2], b[8 * hh + 3], b[8 * hh + 4],
+                                                b[8 * hh + 5], b[8 * hh + 6], b[8 * hh + 7]);
+            }
+        }
+        if (PASS == 0) return;
+        __syncthreads();   // every read of the stage is done: park the codes in it
+#pragma unroll
+        for (int c = 0; c < CPT; c++) {
+            const int col = q * CPT + c;
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                const int sl = 2 * g + hh;   // 8-row slot, as copy_out_fp4T reads it
+                *reinterpret_cast<uint32_t *>(st + col * 64 + ((sl ^ ((col / VEC) & 15)) * 4)) = code[c][hh];
+            }
+        }
+        __syncthreads();
+        copy_out_fp4T<VEC>(st, q_colT, M, K, mb, kb);
+        copy_out_sbT<TC>(sSB, sb_colT, M, K, mb, kb);
+    });
+    if (PASS == 0) cta_max_to(mx, reinterpret_cast<uint32_t *>(amax), status);
+}
+
+template <int DT, int RND, int PASS>
+static cudaError_t rht_pass(const CUtensorMap &map, int64_t M, int64_t K, uint32_t mask, float *amax, uint64_t seed,
+                            uint64_t offset, uint8_t *q_colT, uint8_t *sb_colT, float *s_global, int32_t *status,
+                            cudaStream_t st)
+{
+    constexpr int TC = 32 * In<DT>::VEC;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_nvfp4_rht<DT, RND, PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
+    int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+    if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
+    k_nvfp4_rht<DT, RND, PASS><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, mask, amax, seed, offset, q_colT, sb_colT,
+                                                                    s_global, status);
+    return cudaGetLastError();
+}
+
+template <int DT, int RND>
+static cudaError_t rht_t(const void *x, int64_t M, int64_t K, uint32_t mask, bool compute_amax, float *amax,
+                         uint64_t seed, uint64_t offset, uint8_t *q_colT, uint8_t *sb_colT, float *s_global,
+                         int32_t *status, cudaStream_t st)
+{
+    alignas(64) CUtensorMap map;
+    const bool empty = M == 0 || K == 0;
+    if (!empty) {
+        cudaError_t e = make_tile_map(&map, x, DT, M, K);
+        if (e != cudaSuccess) return e;
+    } else {
+        memset(&map, 0, sizeof map);   // never dereferenced: the kernels return before touching tiles
+    }
+    if (compute_amax) {
+        cudaError_t e = launch_zero_word(amax, st);
+        if (e != cudaSuccess) return e;
+        e = rht_pass<DT, 0, 0>(map, M, K, mask, amax, seed, offset, q_colT, sb_colT, s_global, status, st);   // no rounding in the amax pass
+        if (e != cudaSuccess) return e;
+    }
+    return rht_pass<DT, RND, 1>(map, M, K, mask, amax, seed, offset, q_colT, sb_colT, s_global, status, st);
+}
+
+cudaError_t launch_rht_amax(const void *x, int dt, int64_t M, int64_t K, uint32_t sign_mask, float *amax,
+                           int32_t *status, cudaStream_t st)
+{
+    alignas(64) CUtensorMap map;
+    if (M == 0 || K == 0) return launch_zero_word(amax, st);
+    cudaError_t e = make_tile_map(&map, x, dt, M, K);
+    if (e == cudaSuccess) e = launch_zero_word(amax, st);
+    if (e != cudaSuccess) return e;
+    return dt == BF16 ? rht_pass<BF16, 0, 0>(map, M, K, sign_mask, amax, 0, 0, nullptr, nullptr, nullptr, status, st)
+                      : rht_pass<F32, 0, 0>(map, M, K, sign_mask, amax, 0, 0, nullptr, nullptr, nullptr, status, st);
+}
+
+cudaError_t launch_nvfp4_rht_colT(const void *x, int dt, int64_t M, int64_t K, uint32_t sign_mask, int rnd,
+                                  uint64_t seed, uint64_t offset, bool compute_amax, float *amax, uint8_t *q_colT,
+                                  uint8_t *sb_colT, float *s_global, int32_t *status, cudaStream_t st)
+{
+#define RHT_ARGS x, M, K, sign_mask, compute_amax, amax, seed, offset, q_colT, sb_colT, s_global, status, st
+    if (dt == BF16) return rnd == 0 ? rht_t<BF16, 0>(RHT_ARGS) : rht_t<BF16, 1>(RHT_ARGS);
+    return rnd == 0 ? rht_t<F32, 0>(RHT_ARGS) : rht_t<F32, 1>(RHT_ARGS);
+#undef RHT_ARGS
 }
 
 }  // namespace qk

@@ -256,6 +256,43 @@ q_status q_nvfp4(const void *x, q_dtype in, int64_t M, int64_t K, q_nvblk blk, q
     return Q_OK;
 }
 
+q_status q_nvfp4_rht_amax(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, float *amax,
+                          int32_t *status, q_stream_t stream)
+{
+    const char *fn = "q_nvfp4_rht_amax";
+    TRY(check_dims(fn, M, K));
+    TRY(check_in(fn, x, in, M * K));
+    if (sign_mask > 0xFFFFu) return fail(Q_ERR_ARG, "%s: sign_mask 0x%x has bits above bit 15", fn, sign_mask);
+    TRY(multiple(fn, "K", K, 16));
+    TRY(multiple(fn, "M", M, 16));
+    TRY(need(fn, "amax", amax, 4));
+    LAUNCH(fn, qk::launch_rht_amax(x, (int)in, M, K, sign_mask, amax, status, S(stream)));
+    return Q_OK;
+}
+
+q_status q_nvfp4_rht_colT(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, q_round rnd,
+                          uint64_t seed, uint64_t offset, uint8_t *q_colT, uint8_t *sb_colT, float *amax,
+                          q_amax_mode amax_mode, float *s_global, int32_t *status, q_stream_t stream)
+{
+    const char *fn = "q_nvfp4_rht_colT";
+    TRY(check_dims(fn, M, K));
+    TRY(check_in(fn, x, in, M * K));
+    if (rnd != Q_RN && rnd != Q_SR) return fail(Q_ERR_ARG, "%s: rnd %d is not Q_RN or Q_SR", fn, (int)rnd);
+    if (amax_mode != Q_AMAX_COMPUTE && amax_mode != Q_AMAX_GIVEN) return fail(Q_ERR_ARG, "%s: bad amax_mode %d", fn, (int)amax_mode);
+    if (sign_mask > 0xFFFFu) return fail(Q_ERR_ARG, "%s: sign_mask 0x%x has bits above bit 15", fn, sign_mask);
+    TRY(multiple(fn, "K", K, 16));
+    TRY(multiple(fn, "M", M, 16));
+    if (M * K > 0) {
+        TRY(need(fn, "q_colT", q_colT, 16));
+        TRY(need(fn, "sb_colT", sb_colT, 16));
+    }
+    TRY(need(fn, "amax", amax, 4));
+    TRY(need(fn, "s_global", s_global, 4));
+    LAUNCH(fn, qk::launch_nvfp4_rht_colT(x, (int)in, M, K, sign_mask, (int)rnd, seed, offset, amax_mode == Q_AMAX_COMPUTE,
+                                         amax, q_colT, sb_colT, s_global, status, S(stream)));
+    return Q_OK;
+}
+
 q_status dq_current_scaling(const uint8_t *q, const float *scale, int64_t R, int64_t C, q_fp8 fmt, q_dtype out,
                             void *y, q_stream_t stream)
 {

@@ -255,6 +255,20 @@ QD void mul2(float &a, float &b, float s0, float s1)
         : "+f"(a), "+f"(b) : "f"(s0), "f"(s1));
 }
 
+// Butterfly on two column pairs: (a, b) -> (a + b, a - b) for (a0, b0) and
+// (a1, b1) together (one packed FP32x2 add and one sub, each rounded once).
+QD void bfly2(float &a0, float &a1, float &b0, float &b1)
+{
+    asm("{\n\t.reg .b64 x, y, s, d;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %3};\n\t"
+        "add.rn.f32x2 s, x, y;\n\t"
+        "sub.rn.f32x2 d, x, y;\n\t"
+        "mov.b64 {%0, %1}, s;\n\t"
+        "mov.b64 {%2, %3}, d;\n\t}"
+        : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
+}
+
 // The VEC elements of a 16-byte row chunk times s, as FP8 codes (VEC/4 words,
 // element 0 in the lowest byte).
 template <int DT, int FMT> QD void chunk_fp8(const uint4 &v, float s, uint32_t *o)
@@ -402,6 +416,26 @@ template <int G> QD uint32_t group_max(uint32_t v)
 QD void flag_nonfinite(int32_t *status, uint32_t amax_bits)
 {
     if (status != nullptr && amax_bits >= 0x7F800000u) atomicOr(status, kStNonFinite);
+}
+
+// CTA-wide max of m (blockDim.x a multiple of 32, at most 1024 threads),
+// then one atomicMax into *dst from a CTA that raises it; a non-finite
+// result is reported in *status.
+QD void cta_max_to(uint32_t m, uint32_t *dst, int32_t *status)
+{
+    __shared__ uint32_t red[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    m = warp_max(m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
+        m = warp_max(m);
+        if (lane == 0) {
+            if (m > *reinterpret_cast<volatile uint32_t *>(dst)) atomicMax(dst, m);
+            flag_nonfinite(status, m);
+        }
+    }
 }
 // Thread-local record of non-finite maxima, posted once (see post_nonfinite).
 QD uint32_t nonfinite(uint32_t amax_bits) { return amax_bits >= 0x7F800000u ? 1u : 0u; }

@@ -25,6 +25,19 @@ cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt,
 cudaError_t launch_mxfp8(const void *x, int dt, int64_t M, int64_t K, int fmt, uint8_t *q_row,
                          uint8_t *e_row, uint8_t *q_col, uint8_t *e_col, int32_t *status, cudaStream_t st);
 
+// *w = 0 (one thread), stream-ordered before a reduction into it
+cudaError_t launch_zero_word(float *w, cudaStream_t st);
+
+// max|x'| of the random Hadamard transform along M (zeroes *amax first)
+cudaError_t launch_rht_amax(const void *x, int dt, int64_t M, int64_t K, uint32_t sign_mask, float *amax,
+                           int32_t *status, cudaStream_t st);
+
+// random Hadamard transform along M + columnwise NVFP4 of the result; the
+// amax of the transformed tensor is reduced into *amax first unless given
+cudaError_t launch_nvfp4_rht_colT(const void *x, int dt, int64_t M, int64_t K, uint32_t sign_mask, int rnd,
+                                  uint64_t seed, uint64_t offset, bool compute_amax, float *amax, uint8_t *q_colT,
+                                  uint8_t *sb_colT, float *s_global, int32_t *status, cudaStream_t st);
+
 // delayed scaling: cast with the pair ds = [alpha, s], recording max|x| into
 // *amax_rec (zeroed first); next pair from the window of N amaxes
 cudaError_t launch_ds_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *ds, float *amax_rec,

@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["q_amax", "q_current_scaling", "q_delayed_scaling", "q_delayed_scale_update", "q_mxfp8",
-              "q_mxfp8_requant_col", "q_blockwise", "q_nvfp4", "dq_current_scaling", "dq_mxfp8", "dq_blockwise",
+              "q_mxfp8_requant_col", "q_blockwise", "q_nvfp4", "q_nvfp4_rht_amax", "q_nvfp4_rht_colT",
+              "dq_current_scaling", "dq_mxfp8", "dq_blockwise",
               "dq_nvfp4", "q_last_error", "q_abi_version"]:
         assert n in names
 
@@ -90,6 +91,27 @@ def test_delayed_scaling_validation(L):
     assert st == Q.Q_ERR_ARG                       # bad algo
     st, _ = status_of(L, "q_delayed_scale_update", A, 16, 3, Q.Q_HIST_MAX, Q.Q_E4M3, None, None)
     assert st == Q.Q_ERR_ARG                       # ds required
+
+
+def test_rht_validation(L):
+    args = lambda M, K, mask, rnd, qc, sbc, amax, mode, sg: (A, Q.Q_BF16, M, K, mask, rnd, 0, 0, qc, sbc, amax, mode, sg,
+                                                           None, None)
+    st, _ = status_of(L, "q_nvfp4_rht_colT", *args(24, 32, 0x1234, Q.Q_RN, A, A, A, 0, A))
+    assert st == Q.Q_ERR_SHAPE                     # M % 16
+    st, _ = status_of(L, "q_nvfp4_rht_colT", *args(32, 24, 0x1234, Q.Q_RN, A, A, A, 0, A))
+    assert st == Q.Q_ERR_SHAPE                     # K % 16
+    st, msg = status_of(L, "q_nvfp4_rht_colT", *args(32, 32, 0x10000, Q.Q_RN, A, A, A, 0, A))
+    assert st == Q.Q_ERR_ARG and "bit 15" in msg
+    st, _ = status_of(L, "q_nvfp4_rht_colT", *args(32, 32, 0x1234, 2, A, A, A, 0, A))
+    assert st == Q.Q_ERR_ARG                       # bad rounding
+    st, _ = status_of(L, "q_nvfp4_rht_colT", *args(32, 32, 0x1234, Q.Q_RN, None, A, A, 0, A))
+    assert st == Q.Q_ERR_ARG                       # q_colT required
+    st, _ = status_of(L, "q_nvfp4_rht_colT", *args(32, 32, 0x1234, Q.Q_RN, A, A, A, 0, None))
+    assert st == Q.Q_ERR_ARG                       # s_global required
+    st, _ = status_of(L, "q_nvfp4_rht_amax", A, Q.Q_BF16, 32, 24, 0x1, A, None, None)
+    assert st == Q.Q_ERR_SHAPE
+    st, _ = status_of(L, "q_nvfp4_rht_amax", A, Q.Q_BF16, 32, 32, 0x1, None, None, None)
+    assert st == Q.Q_ERR_ARG
 
 
 def test_requant_validation(L):

@@ -155,6 +155,51 @@ def test_nonfinite_sets_status():
 
 
 # ---------------------------------------------------------------------------
+# random Hadamard transform + columnwise NVFP4 (weight-gradient inputs)
+# ---------------------------------------------------------------------------
+
+RHT_CASES = [
+    ("outliers", (256, 512), True, O.RN, 0xA5C3),
+    ("grad", (96, 800), True, O.SR, 0x0F0F),       # 96 rows < one tile; 800 = 3 x 256 + 32 columns
+    ("normal", (64, 416), False, O.RN, 0xFFFF),    # FP32: 128-column tiles
+    ("outliers", (384, 144), False, O.SR, 0x1234),  # FP32, 3 tile rows, ragged columns
+    ("lognormal_rows", (16, 16), True, O.RN, 0x0000),
+]
+
+
+@pytest.mark.parametrize("kind,shape,bf16,rnd,mask", RHT_CASES)
+def test_nvfp4_rht_colT_parity(kind, shape, bf16, rnd, mask):
+    x = W.gen(kind, shape, 515, bf16=bf16)
+    q, sb, a, sg = O.nvfp4_rht_colT(x, mask, rnd, seed=21, offset=5)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = Q.q_nvfp4_rht_colT(dev(x), mask, "rn" if rnd == O.RN else "sr", seed=21, offset=5, status=st)
+    torch.cuda.synchronize()
+    f32eq(got.amax.item(), a, "amax of the transform")
+    f32eq(Q.q_nvfp4_rht_amax(dev(x), mask).item(), a, "q_nvfp4_rht_amax")
+    f32eq(got.s_global.item(), sg, "s_global")
+    same(host(got.q_colT), q, "q_colT")
+    same(host(got.sb_colT), sb, "sb_colT")
+    assert st.item() == 0
+    # a given amax (the sharded case) sets the tensor scale
+    A = torch.tensor([np.float32(a) * 4], device="cuda")
+    q2, sb2, _, sg2 = O.nvfp4_rht_colT(x, mask, rnd, seed=21, offset=5, amax_in=np.float32(a) * 4)
+    got2 = Q.q_nvfp4_rht_colT(dev(x), mask, "rn" if rnd == O.RN else "sr", seed=21, offset=5, amax=A)
+    same(host(got2.q_colT), q2, "q_colT, given amax")
+    same(host(got2.sb_colT), sb2, "sb_colT, given amax")
+    f32eq(got2.s_global.item(), sg2, "s_global, given amax")
+
+
+def test_nvfp4_rht_colT_empty_and_nonfinite():
+    e = Q.q_nvfp4_rht_colT(torch.empty((0, 32), dtype=torch.bfloat16, device="cuda"), 0x1)
+    assert e.amax.item() == 0.0 and e.s_global.item() == 1.0
+    x = W.gen("normal", (32, 32), 3, bf16=False)
+    x[5, 6] = np.inf
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Q.q_nvfp4_rht_colT(dev(x), 0x1, status=st)
+    assert st.item() & Q.Q_ST_NONFINITE
+
+
+# ---------------------------------------------------------------------------
 # per-tensor delayed scaling
 # ---------------------------------------------------------------------------
 
