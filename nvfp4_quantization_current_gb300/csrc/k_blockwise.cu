@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
     constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, LPB = 128 / VEC;
     constexpr int NT = TC / 128;   // 128-column blocks per tile
     __shared__ uint4 part[kEngWarps][32];      // 1x128: per-warp column maxima (packed like the input)
-    __shared__ float calpha[TC];               // 1x128: column alphas of the tile
+    __shared__ __align__(16) float calpha[TC];   // 1x128: column alphas of the tile
     __shared__ uint32_t tred[kEngWarps][NT];   // 128x128: per-warp tile maxima
     __shared__ BwScaleTab tab;
     if (DT == BF16 && threadIdx.x < 128) {
@@ -94,7 +94,56 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
             }
             // ---------------- 1x128 rowwise ----------------
             uint32_t nf = 0;
-            if (q_row != nullptr) {
+            if (DT == BF16 && q_row != nullptr) {
+                // A block is one row of 16 lanes.  The 8 row maxima, two BF16
+                // magnitudes per word, are reduced over the 16 lanes by a halving
+                // exchange (5 shuffles); afterwards lane L of the group holds the
+                // maximum of row (L >> 1) & 7, computes that row's alpha and s once,
+                // and the alphas go back to every lane by index shuffles.
+                const int nrows = !kok ? 0 : (m0 + 8 <= M ? 8 : (m0 < M ? (int)(M - m0) : 0));
+                uint32_t P[4];
+#pragma unroll
+                for (int p = 0; p < 4; p++) {
+                    const uint4 &a = v[2 * p], &b = v[2 * p + 1];
+                    const uint32_t ma = hmax_abs2(hmax_abs2(a.x, a.y), hmax_abs2(a.z, a.w));
+                    const uint32_t mb = hmax_abs2(hmax_abs2(b.x, b.y), hmax_abs2(b.z, b.w));
+                    P[p] = hmax_abs2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632));   // row 2p low, 2p+1 high
+                }
+                const int L = lane & 15;
+                const bool b3 = L & 8, b2 = L & 4, b1 = L & 2;
+                uint32_t k0 = b3 ? P[2] : P[0], k1 = b3 ? P[3] : P[1];          // keep rows 4*b3 .. 4*b3+3
+                const uint32_t s0 = b3 ? P[0] : P[2], s1 = b3 ? P[1] : P[3];
+                k0 = hmax_abs2(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, 8));
+                k1 = hmax_abs2(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, 8));
+                uint32_t kw = b2 ? k1 : k0;                                        // rows 4*b3+2*b2, +1
+                kw = hmax_abs2(kw, __shfl_xor_sync(0xFFFFFFFFu, b2 ? k0 : k1, 4));
+                kw = hmax_abs2(kw, __shfl_xor_sync(0xFFFFFFFFu, kw, 2));
+                kw = hmax_abs2(kw, __shfl_xor_sync(0xFFFFFFFFu, kw, 1));
+                const int r = (L >> 1) & 7;
+                const uint32_t bm = (b1 ? kw : (kw << 16)) & 0x7FFF0000u;         // FP32 bits of row r's block max
+                float alpha_r, s_r;
+                bw_scales<DT>(bm, tab, alpha_r, s_r);
+                if ((L & 1) == 0 && r < nrows) {
+                    s_row[(m0 + r) * (K / 128) + k / 128] = s_r;
+                    nf |= nonfinite(bm);
+                }
+                uint8_t *qr = q_row + m0 * K + k;
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float alpha = __shfl_sync(0xFFFFFFFFu, alpha_r, (lane & 16) + 2 * j);
+                    uint32_t o[CW];
+                    chunk_fp8<DT, E4M3>(v[j], alpha, o);
+                    if (j < nrows) {
+                        if (CW == 2) stg8(qr + j * K, o[0], o[CW - 1]);
+                        else stg4(qr + j * K, o[0]);
+                    }
+                }
+            } else if (q_row != nullptr) {
+                // rows of this thread that exist (all 8 except in the last tile row)
+                const int nrows = !kok ? 0 : (m0 + 8 <= M ? 8 : (m0 < M ? (int)(M - m0) : 0));
+                uint8_t *qr = q_row + m0 * K + k;
+                float *sr = s_row + m0 * (K / 128) + k / 128;
+                const bool sl = lane % LPB == 0;
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
                     uint32_t bb[2] = {absmax_bits<DT>(v[j]), absmax_bits<DT>(v[j + 1])};
@@ -105,38 +154,50 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
                         bw_scales<DT>(bb[h], tab, alpha, sc);
                         uint32_t o[CW];
                         chunk_fp8<DT, E4M3>(v[j + h], alpha, o);
-                        const bool ok = m0 + j + h < M && kok;
-                        if (ok) {
-                            uint8_t *dst = q_row + (m0 + j + h) * K + k;
+                        if (j + h < nrows) {
+                            uint8_t *dst = qr + (j + h) * K;
                             if (CW == 2) stg8(dst, o[0], o[CW - 1]);
                             else stg4(dst, o[0]);
+                            if (sl) sr[(j + h) * (K / 128)] = sc;
+                            nf |= nonfinite(bb[h]);
                         }
-                        if (ok && lane % LPB == 0) s_row[(m0 + j + h) * (K / 128) + k / 128] = sc;
-                        nf |= ok ? nonfinite(bb[h]) : 0u;
                     }
                 }
             }
             post_nonfinite(status, nf);
             if (q_colT == nullptr) return;
             __syncthreads();   // partial column maxima posted
-            // ---------------- 128x1 columnwise: one thread per column reduces the 16 partials
-            if (t < TC) {
-                const int q = t / VEC, c = t % VEC;   // lane q of the partials holds this column
-                uint32_t b = 0;
+            // ---------------- 128x1 columnwise: two threads per column reduce 8 partials each
+            {
+                constexpr int TPC = 2 * kEngThreads / TC >= 2 ? 2 : 1;   // threads per column (TC <= 256)
+                const int col = t / TPC, half = t % TPC;
+                if (col < TC) {
+                    const int q = col / VEC, c = col % VEC;   // lane q of the partials holds this column
+                    uint32_t b = 0;
 #pragma unroll
-                for (int w = 0; w < kEngWarps; w++) b = max(b, colmax_bits<DT>(part[w][q], c));
-                float alpha, sc;
-                bw_scales<DT>(b, tab, alpha, sc);
-                calpha[t] = alpha;
-                if (kb + t < K) {
-                    s_colT[(kb + t) * (M / 128) + tm] = sc;
-                    flag_nonfinite(status, b);
+                    for (int w = half; w < kEngWarps; w += TPC) b = max(b, colmax_bits<DT>(part[w][q], c));
+                    if (TPC == 2) b = max(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
+                    if (half == 0) {
+                        float alpha, sc;
+                        bw_scales<DT>(b, tab, alpha, sc);
+                        calpha[col] = alpha;
+                        if (kb + col < K) {
+                            s_colT[(kb + col) * (M / 128) + tm] = sc;
+                            flag_nonfinite(status, b);
+                        }
+                    }
                 }
             }
             __syncthreads();   // column alphas visible; every read of the stage is done
             float ca[VEC];
 #pragma unroll
-            for (int c = 0; c < VEC; c++) ca[c] = calpha[lane * VEC + c];
+            for (int c = 0; c < VEC; c += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(&calpha[lane * VEC + c]);
+                ca[c] = a4.x;
+                ca[c + 1] = a4.y;
+                ca[c + 2] = a4.z;
+                ca[c + 3] = a4.w;
+            }
 #pragma unroll
             for (int j = 0; j < 8; j++) {
                 float f[VEC];
