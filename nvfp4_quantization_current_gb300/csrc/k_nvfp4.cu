@@ -55,8 +55,6 @@ template <int DT> QD uint32_t nv_sb_code(uint32_t b, float alpha_g, const uint32
 // the code: each CTA tabulates it for the 128 positive codes (enc_tab[0x38]
 // = alpha_g also serves b = 0).
 
-// 16 random bits for element e (0..7) of a Philox block.
-QD uint32_t r16_of(const uint4 &R, int e) { return (word(R, e >> 1) >> (16 * (e & 1))) & 0xFFFFu; }
 
 // In-place transpose of an 8x8 nibble matrix: a[i] nibble j -> a[j] nibble i.
 QD void transpose8x8_nibbles(uint32_t *a)
@@ -98,7 +96,12 @@ QD uint32_t nv_row_codes(const uint4 &v, float enc, uint64_t seed, uint64_t offs
         const uint4 R = sr_bits(seed, offset + (uint64_t)(i0 >> 3), 0u);
         const int e0 = (int)(i0 & 7);
 #pragma unroll
-        for (int j = 0; j < VEC; j++) y[j] = sr_e2m1_value(y[j], r16_of(R, e0 + j));
+        for (int j = 0; j < VEC; j += 2) {   // draws e0 + j, e0 + j + 1: one word (e0 is 0, or 4 for FP32 chunks)
+            float r0, r1;
+            r16_pair(VEC == 8 ? word(R, j >> 1) : (e0 ? word(R, 2 + (j >> 1)) : word(R, j >> 1)), r0, r1);
+            y[j] = sr_e2m1_value(y[j], r0);
+            y[j + 1] = sr_e2m1_value(y[j + 1], r1);
+        }
     }
     return cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
@@ -243,33 +246,35 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                 cm.z = colmax_word<DT>(cm.z, o4.z);
                 cm.w = colmax_word<DT>(cm.w, o4.w);
             }
-            float enc[VEC];
+            // each column's block scale, then its 8 rows with the block's factor:
+            // one E2M1 word per column (row 8w in bits 3-0)
             uint32_t nfc = 0;
 #pragma unroll
             for (int c = 0; c < VEC; c++) {
                 const uint32_t b = colmax_bits<DT>(cm, c);
                 const uint32_t sb = nv_sb_code<DT>(b, alpha_g, sb_tab, ae);
-                enc[c] = enc_tab[sb];
+                const float enc = enc_tab[sb];
                 if ((warp & 1) == 0) sSB[warp >> 1][lane * VEC + c] = (uint8_t)sb;
                 nfc |= ((warp & 1) == 0 && kok && m0 < M) ? nonfinite(b) : 0u;
-            }
-            post_nonfinite(status, nfc);
-            // each column's 8 rows with its factor: one E2M1 word per column (row 8w in bits 3-0)
-#pragma unroll
-            for (int c = 0; c < VEC; c++) {
                 float y[8];
 #pragma unroll
                 for (int j = 0; j < 8; j++) y[j] = elem<DT>(v[j], c);
 #pragma unroll
-                for (int j = 0; j < 8; j += 2) mul2(y[j], y[j + 1], enc[c], enc[c]);
+                for (int j = 0; j < 8; j += 2) mul2(y[j], y[j + 1], enc, enc);
                 if (RND == 1) {
                     // elements (k + c) * M + m0 .. + 7 of stream 1: one Philox block
                     const uint4 R = sr_bits(seed, offset + (uint64_t)(((k + c) * M + m0) >> 3), 1u);
 #pragma unroll
-                    for (int j = 0; j < 8; j++) y[j] = sr_e2m1_value(y[j], r16_of(R, j));
+                    for (int j = 0; j < 8; j += 2) {
+                        float r0, r1;
+                        r16_pair(word(R, j >> 1), r0, r1);
+                        y[j] = sr_e2m1_value(y[j], r0);
+                        y[j + 1] = sr_e2m1_value(y[j + 1], r1);
+                    }
                 }
                 colw[c] = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
             }
+            post_nonfinite(status, nfc);
         } else {
             // ---------------- 16x16: one scale per tile ----------------
             uint32_t b = 0;
@@ -451,10 +456,13 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
                 for (int hh = 0; hh < 2; hh++) {
                     const uint4 Ra = sr_bits(seed, offset + (uint64_t)(((kb + c0) * M + m + 8 * hh) >> 3), 1u);
                     const uint4 Rb = sr_bits(seed, offset + (uint64_t)(((kb + c0 + 1) * M + m + 8 * hh) >> 3), 1u);
+                    float ra[8], rb[8];
+                    r16_block(Ra, ra);
+                    r16_block(Rb, rb);
 #pragma unroll
                     for (int j = 0; j < 8; j++) {
-                        a[8 * hh + j] = sr_e2m1_value(a[8 * hh + j], r16_of(Ra, j));
-                        b[8 * hh + j] = sr_e2m1_value(b[8 * hh + j], r16_of(Rb, j));
+                        a[8 * hh + j] = sr_e2m1_value(a[8 * hh + j], ra[j]);
+                        b[8 * hh + j] = sr_e2m1_value(b[8 * hh + j], rb[j]);
                     }
                 }
             }

@@ -378,25 +378,43 @@ QD uint4 sr_bits(uint64_t seed, uint64_t g, uint32_t stream)
                          make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
 }
 
-// Stochastic rounding of y onto the E2M1 grid with 16 random bits r16:
-// with a = |y| < 6, ulp the grid spacing at a (0.5 below 2, 1 in [2, 4), 2
-// in [4, 6)), t = a / ulp, fl = floor(t) and frac = t - fl, the result is
-// (fl + 1) * ulp iff r16 < frac * 2^16, else fl * ulp.  With u = r16 / 2^16
-// that is ceil(t - u) * ulp: frac > u gives fl + 1, frac <= u gives fl.
-// t - u is formed by one FMA; it is exact for t >= 1 (both terms are
-// multiples of 2^-23 and the difference is below 4), and for t < 1 only its
-// sign decides the ceiling (0 or 1), which round-to-nearest keeps.  |y| >= 6
-// and NaN return y unchanged (the RTNE conversion saturates them).  The
-// result carries y's sign.
-QD float sr_e2m1_value(float y, uint32_t r16)
+// Stochastic rounding of y onto the E2M1 grid with 16 random bits, given
+// as the exact float r (0..65535): with a = |y| < 6, ulp the grid spacing at
+// a (0.5 below 2, 1 in [2, 4), 2 in [4, 6)), t = a / ulp, fl = floor(t) and
+// frac = t - fl, the result is (fl + 1) * ulp iff r < frac * 2^16, else
+// fl * ulp.  With u = r / 2^16 that is ceil(t - u) * ulp: frac > u gives
+// fl + 1, frac <= u gives fl.  t - u is formed by one FMA; it is exact for
+// t >= 1 (both terms are multiples of 2^-23 and the difference is below 4),
+// and for t < 1 only its sign decides the ceiling (0 or 1), which
+// round-to-nearest keeps.  The result carries y's sign.  |y| >= 6 needs no
+// case of its own: there ulp = 2 and ceil(a/2 - u) >= 3, so the result is at
+// least 6 in magnitude (or inf) and the saturating conversion gives +-6, as
+// it does for y; a NaN stays NaN with y's sign.
+QD float sr_e2m1_value(float y, float r)
 {
     const float a = fabsf(y);
-    const float s = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);   // 1 / ulp
+    const float s = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);           // 1 / ulp
     const float ulp = __uint_as_float(0x7F000000u - __float_as_uint(s));   // 2^-k from 2^k
-    const float t = __fmul_rn(a, s);                                  // exact
-    const float n = ceilf(__fmaf_rn(-(float)r16, 1.0f / 65536.0f, t));
-    const float v = copysignf(__fmul_rn(n, ulp), y);                  // exact, on the grid
-    return a < 6.0f ? v : y;
+    const float t = __fmul_rn(a, s);                                        // exact
+    const float n = ceilf(__fmaf_rn(-r, 1.0f / 65536.0f, t));
+    return copysignf(__fmul_rn(n, ulp), y);                                 // exact, on the grid
+}
+
+// The two 16-bit draws of a Philox word (low half first) as exact floats.
+QD void r16_pair(uint32_t w, float &lo, float &hi)
+{
+    asm("{\n\t.reg .u16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f32.u16 %0, l;\n\tcvt.rn.f32.u16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(w));
+}
+
+// The 8 draws of a Philox block as exact floats, element e in rf[e].
+QD void r16_block(const uint4 &R, float *rf)
+{
+    r16_pair(R.x, rf[0], rf[1]);
+    r16_pair(R.y, rf[2], rf[3]);
+    r16_pair(R.z, rf[4], rf[5]);
+    r16_pair(R.w, rf[6], rf[7]);
 }
 
 // ---------------------------------------------------------------------------
