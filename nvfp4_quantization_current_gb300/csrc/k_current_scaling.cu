@@ -36,8 +36,10 @@ int sm_count()
 }
 
 // ---------------------------------------------------------------------------
-// a1: amax.  Grid-stride 16-byte loads, eight in flight per thread, |x| max
-// on bit patterns, warp reduce, CTA reduce, one atomicMax per CTA.
+// a1: amax.  Grid-stride 16-byte loads, eight in flight per thread (each
+// batch predicated, so the tail costs one memory round trip, not one per
+// leftover load), |x| max on bit patterns, warp reduce, CTA reduce, one
+// atomicMax per CTA.
 // ---------------------------------------------------------------------------
 constexpr int kAmaxThreads = 256, kAmaxUnroll = 8;
 
@@ -50,14 +52,14 @@ __global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     uint32_t m = 0;
-    for (; i + (kAmaxUnroll - 1) * stride < nv; i += kAmaxUnroll * stride) {
+    for (; i < nv; i += kAmaxUnroll * stride) {
         uint4 a[kAmaxUnroll];
 #pragma unroll
-        for (int u = 0; u < kAmaxUnroll; u++) a[u] = ldg_stream(xv + i + u * stride);
+        for (int u = 0; u < kAmaxUnroll; u++)
+            a[u] = i + u * stride < nv ? ldg_stream(xv + i + u * stride) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; u++) m = max(m, absmax_bits<DT>(a[u]));
     }
-    for (; i < nv; i += stride) m = max(m, absmax_bits<DT>(ldg_stream(xv + i)));
     // the last n % VEC elements, one per thread of CTA 0
     if (blockIdx.x == 0 && threadIdx.x < n - nv * VEC) {
         const int64_t t = nv * VEC + threadIdx.x;
@@ -254,7 +256,7 @@ cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *
     const int vec = dt == BF16 ? 8 : 4;
     const int64_t nv = n / vec;
     int64_t blocks = (nv + (int64_t)kAmaxThreads * kAmaxUnroll - 1) / ((int64_t)kAmaxThreads * kAmaxUnroll);
-    const int64_t cap = (int64_t)sm_count() * 4;
+    const int64_t cap = (int64_t)sm_count() * 8;   // two waves of the 4 resident CTAs: a shorter tail
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (dt == BF16) k_amax<BF16><<<(unsigned)blocks, kAmaxThreads, 0, st>>>(x, n, reinterpret_cast<uint32_t *>(amax));
