@@ -55,13 +55,11 @@ RHT_MASK = 0xB4E1   # the 16 random signs of the Hadamard transform (any fixed d
 # capture time; reported as null when the source has changed since.
 TRAFFIC = {
     # profiles/k_blockwise_1x128T_bw3_act.md
-    "bw3.act:bw_1x128_T": {"bytes_per_launch": 421391616, "src_hash": "fddd6d313857c53e"},
-    # profiles/k_cs_tiles_e5m2T_hy4_grad.md
-    "hy4.grad:cs_cast_T": {"bytes_per_launch": 415883520, "src_hash": "d12e6156f38966b8"},
-    # profiles/k_mxfp8_mx2_act.md
-    "mx2.act:mxfp8": {"bytes_per_launch": 80156160, "src_hash": "0845a8fdfed6070a"},
+    "bw3.act:bw_1x128_T": {"bytes_per_launch": 421356032, "src_hash": "03a8180a7a056a89"},
+    # profiles/k_nvfp4_1x16_sr_T_nv5_grad.md
+    "nv5.grad:nvfp4_1x16_sr": {"bytes_per_launch": 71108864, "src_hash": "0af8c4e225f1711f"},
     # profiles/k_nvfp4_1x16_rn_T_nv5_act.md
-    "nv5.act:nvfp4_1x16_rn": {"bytes_per_launch": 70753280, "src_hash": "6643a1db22a5044b"},
+    "nv5.act:nvfp4_1x16_rn": {"bytes_per_launch": 70936064, "src_hash": "0af8c4e225f1711f"},
 }
 
 
