@@ -46,7 +46,7 @@ METRIC = "quantize GB/s (bytes read+written) and % of GB300 HBM peak per recipe"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-CPU_SAMPLE_FRAC = 1.0 / 8.0
+CPU_SAMPLE_FRAC = 1.0 / 2.0
 REF_BUDGET_S = 120.0
 RHT_MASK = 0xB4E1   # the 16 random signs of the Hadamard transform (any fixed draw)
 
@@ -56,6 +56,8 @@ RHT_MASK = 0xB4E1   # the 16 random signs of the Hadamard transform (any fixed d
 TRAFFIC = {
     # profiles/k_blockwise_1x128T_bw3_act.md
     "bw3.act:bw_1x128_T": {"bytes_per_launch": 421356032, "src_hash": "03a8180a7a056a89"},
+    # profiles/k_blockwise_128x128T_bw3_w.md
+    "bw3.w:bw_128x128_T": {"bytes_per_launch": 473322496, "src_hash": "03a8180a7a056a89"},
     # profiles/k_nvfp4_1x16_sr_T_nv5_grad.md
     "nv5.grad:nvfp4_1x16_sr": {"bytes_per_launch": 71108864, "src_hash": "0af8c4e225f1711f"},
     # profiles/k_nvfp4_1x16_rn_T_nv5_act.md
