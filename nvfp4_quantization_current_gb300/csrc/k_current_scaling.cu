@@ -47,6 +47,7 @@ template <int DT>
 __global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict__ x, int64_t n, uint32_t *__restrict__ amax)
 {
     constexpr int VEC = In<DT>::VEC;
+    griddep_launch_dependents();   // the cast behind this pass may be scheduled; it waits for the amax
     const uint4 *xv = static_cast<const uint4 *>(x);
     const int64_t nv = n / VEC;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict
     if (warp == 0) {
         m = lane < kAmaxThreads / 32 ? red[lane] : 0u;
         m = warp_max(m);
+        griddep_wait();   // the zeroing of *amax (the kernel ahead of this one) is complete
         // same-address atomics serialize in L2: only a CTA that raises the
         // running maximum pays for one
         if (lane == 0 && m > *reinterpret_cast<volatile uint32_t *>(amax)) atomicMax(amax, m);
@@ -86,6 +88,7 @@ __global__ void __launch_bounds__(kAmaxThreads, 4) k_amax(const void *__restrict
 template <int FMT, bool DS>
 QD float cast_alpha(const float *amax, const float *ds, float *scale, int32_t *status)
 {
+    griddep_wait();   // the amax pass (or the zeroing of the delayed-scaling slot) ahead of this kernel is complete
     const float a = DS ? 0.0f : *amax;
     const float alpha = DS ? ds[0] : alpha_from_amax(Fp8<FMT>::FMAX, a);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -239,7 +242,11 @@ __global__ void k_empty_scales(float *amax_out, float *scale)
 
 // Zeroes the amax word before the reduction (a kernel on the same stream: the
 // next kernel starts right behind it, which a driver memset does not).
-__global__ void k_zero_word(uint32_t *w) { *w = 0u; }
+__global__ void k_zero_word(uint32_t *w)
+{
+    griddep_launch_dependents();   // the reduction behind may start; it waits before its atomic
+    *w = 0u;
+}
 
 cudaError_t launch_zero_word(float *w, cudaStream_t st)
 {
@@ -259,15 +266,17 @@ cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *
     const int64_t cap = (int64_t)sm_count() * 8;   // two waves of the 4 resident CTAs: a shorter tail
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (dt == BF16) k_amax<BF16><<<(unsigned)blocks, kAmaxThreads, 0, st>>>(x, n, reinterpret_cast<uint32_t *>(amax));
-    else k_amax<F32><<<(unsigned)blocks, kAmaxThreads, 0, st>>>(x, n, reinterpret_cast<uint32_t *>(amax));
-    return cudaGetLastError();
+    uint32_t *w = reinterpret_cast<uint32_t *>(amax);
+    return dt == BF16 ? launch_k(true, k_amax<BF16>, dim3((unsigned)blocks), dim3(kAmaxThreads), 0, st, x, n, w)
+                      : launch_k(true, k_amax<F32>, dim3((unsigned)blocks), dim3(kAmaxThreads), 0, st, x, n, w);
 }
 
 template <int DT, int FMT, bool DS>
 static cudaError_t cs_cast_t(const void *x, int64_t M, int64_t K, const float *amax, const float *ds, float *amax_rec,
-                             uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st)
+                             uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st,
+                             bool after_amax)
 {
+    const bool pdl = DS || after_amax;   // behind the zeroing kernel (DS) or the amax pass
     uint32_t *rec = reinterpret_cast<uint32_t *>(amax_rec);
     if (DS) {
         k_zero_word<<<1, 1, 0, st>>>(rec);
@@ -280,8 +289,8 @@ static cudaError_t cs_cast_t(const void *x, int64_t M, int64_t K, const float *a
         const int64_t cap = (int64_t)sm_count() * 8;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        k_cs_cast_flat<DT, FMT, DS><<<(unsigned)blocks, 256, 0, st>>>(x, n, amax, ds, rec, q_row, scale, status);
-        return cudaGetLastError();
+        return launch_k(pdl, k_cs_cast_flat<DT, FMT, DS>, dim3((unsigned)blocks), dim3(256), 0, st, x, n, amax, ds, rec,
+                        q_row, scale, status);
     }
     constexpr int TC = 32 * In<DT>::VEC;
     alignas(64) CUtensorMap map;
@@ -295,33 +304,32 @@ static cudaError_t cs_cast_t(const void *x, int64_t M, int64_t K, const float *a
     }
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-    k_cs_tiles<DT, FMT, DS><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, amax, ds, rec, q_row, q_colT, scale, status);
-    return cudaGetLastError();
+    return launch_k(pdl, k_cs_tiles<DT, FMT, DS>, dim3(grid), dim3(kEngThreads), kEngSmem, st, map, M, K, amax, ds, rec,
+                    q_row, q_colT, scale, status);
 }
 
 template <bool DS>
 static cudaError_t cast_dispatch(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *amax, const float *ds,
                                  float *amax_rec, uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status,
-                                 cudaStream_t st)
+                                 cudaStream_t st, bool after_amax)
 {
-    if (dt == BF16) {
-        return fmt == E4M3 ? cs_cast_t<BF16, E4M3, DS>(x, M, K, amax, ds, amax_rec, q_row, q_colT, scale, status, st)
-                           : cs_cast_t<BF16, E5M2, DS>(x, M, K, amax, ds, amax_rec, q_row, q_colT, scale, status, st);
-    }
-    return fmt == E4M3 ? cs_cast_t<F32, E4M3, DS>(x, M, K, amax, ds, amax_rec, q_row, q_colT, scale, status, st)
-                       : cs_cast_t<F32, E5M2, DS>(x, M, K, amax, ds, amax_rec, q_row, q_colT, scale, status, st);
+#define CS_ARGS x, M, K, amax, ds, amax_rec, q_row, q_colT, scale, status, st, after_amax
+    if (dt == BF16) return fmt == E4M3 ? cs_cast_t<BF16, E4M3, DS>(CS_ARGS) : cs_cast_t<BF16, E5M2, DS>(CS_ARGS);
+    return fmt == E4M3 ? cs_cast_t<F32, E4M3, DS>(CS_ARGS) : cs_cast_t<F32, E5M2, DS>(CS_ARGS);
+#undef CS_ARGS
 }
 
 cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *amax,
-                           uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st)
+                           uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st,
+                           bool after_amax)
 {
-    return cast_dispatch<false>(x, dt, M, K, fmt, amax, nullptr, nullptr, q_row, q_colT, scale, status, st);
+    return cast_dispatch<false>(x, dt, M, K, fmt, amax, nullptr, nullptr, q_row, q_colT, scale, status, st, after_amax);
 }
 
 cudaError_t launch_ds_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *ds, float *amax_rec,
                            uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st)
 {
-    return cast_dispatch<true>(x, dt, M, K, fmt, nullptr, ds, amax_rec, q_row, q_colT, scale, status, st);
+    return cast_dispatch<true>(x, dt, M, K, fmt, nullptr, ds, amax_rec, q_row, q_colT, scale, status, st, false);
 }
 
 cudaError_t launch_ds_update(const float *hist, int64_t N, int64_t pos, int algo, int fmt, float *ds, cudaStream_t st)

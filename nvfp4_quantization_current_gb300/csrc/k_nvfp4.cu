@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
     __shared__ uint8_t sSB[8][TC];               // 1x16: columnwise block scales of a tile
     __shared__ uint32_t bred[kEngWarps][TC / 16];   // 16x16: half-block maxima
 
+    griddep_wait();   // the amax pass ahead of this kernel is complete
     const float A = *amax;
     const float alpha_g = alpha_from_amax(2688.0f, A);
     const uint32_t ag = __float_as_uint(alpha_g);
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
 template <int DT, int BLK, int RND>
 static cudaError_t nv_t(const void *x, int64_t M, int64_t K, const float *amax, uint64_t seed, uint64_t offset,
                         uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT, float *s_global,
-                        int32_t *status, cudaStream_t st)
+                        int32_t *status, cudaStream_t st, bool after_amax)
 {
     constexpr int TC = 32 * In<DT>::VEC;
     alignas(64) CUtensorMap map;
@@ -337,16 +338,15 @@ static cudaError_t nv_t(const void *x, int64_t M, int64_t K, const float *amax, 
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     int grid = (int)(tiles < sm_count() ? tiles : sm_count());
     if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
-    k_nvfp4<DT, BLK, RND><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, amax, seed, offset, q_row, sb_row, q_colT,
-                                                               sb_colT, s_global, status);
-    return cudaGetLastError();
+    return launch_k(after_amax, k_nvfp4<DT, BLK, RND>, dim3(grid), dim3(kEngThreads), kEngSmem, st, map, M, K, amax,
+                    seed, offset, q_row, sb_row, q_colT, sb_colT, s_global, status);
 }
 
 cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, int rnd, uint64_t seed,
                          uint64_t offset, const float *amax, uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT,
-                         uint8_t *sb_colT, float *s_global, int32_t *status, cudaStream_t st)
+                         uint8_t *sb_colT, float *s_global, int32_t *status, cudaStream_t st, bool after_amax)
 {
-#define NV_ARGS x, M, K, amax, seed, offset, q_row, sb_row, q_colT, sb_colT, s_global, status, st
+#define NV_ARGS x, M, K, amax, seed, offset, q_row, sb_row, q_colT, sb_colT, s_global, status, st, after_amax
     if (dt == BF16) {
         if (blk == 0) return rnd == 0 ? nv_t<BF16, 0, 0>(NV_ARGS) : nv_t<BF16, 0, 1>(NV_ARGS);
         return rnd == 0 ? nv_t<BF16, 1, 0>(NV_ARGS) : nv_t<BF16, 1, 1>(NV_ARGS);
@@ -382,7 +382,9 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
     __shared__ float enc_tab[128];
     __shared__ uint8_t sSB[8][TC];
     float alpha_g = 1.0f;
+    if (PASS == 0) griddep_launch_dependents();   // the encode pass may be scheduled; it waits for the amax
     if (PASS == 1) {
+        griddep_wait();   // the amax pass ahead of this one is complete
         const float A = *amax;
         alpha_g = alpha_from_amax(2688.0f, A);
         if (threadIdx.x < 128) {
@@ -489,13 +491,16 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
         copy_out_fp4T<VEC>(st, q_colT, M, K, mb, kb);
         copy_out_sbT<TC>(sSB, sb_colT, M, K, mb, kb);
     });
-    if (PASS == 0) cta_max_to(mx, reinterpret_cast<uint32_t *>(amax), status);
+    if (PASS == 0) {
+        griddep_wait();   // the zeroing of *amax ahead of this pass is complete
+        cta_max_to(mx, reinterpret_cast<uint32_t *>(amax), status);
+    }
 }
 
 template <int DT, int RND, int PASS>
-static cudaError_t rht_pass(const CUtensorMap &map, int64_t M, int64_t K, uint32_t mask, float *amax, uint64_t seed,
-                            uint64_t offset, uint8_t *q_colT, uint8_t *sb_colT, float *s_global, int32_t *status,
-                            cudaStream_t st)
+static cudaError_t rht_pass(bool pdl, const CUtensorMap &map, int64_t M, int64_t K, uint32_t mask, float *amax,
+                            uint64_t seed, uint64_t offset, uint8_t *q_colT, uint8_t *sb_colT, float *s_global,
+                            int32_t *status, cudaStream_t st)
 {
     constexpr int TC = 32 * In<DT>::VEC;
     static bool attr = false;
@@ -507,9 +512,8 @@ static cudaError_t rht_pass(const CUtensorMap &map, int64_t M, int64_t K, uint32
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     int grid = (int)(tiles < sm_count() ? tiles : sm_count());
     if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
-    k_nvfp4_rht<DT, RND, PASS><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, mask, amax, seed, offset, q_colT, sb_colT,
-                                                                    s_global, status);
-    return cudaGetLastError();
+    return launch_k(pdl, k_nvfp4_rht<DT, RND, PASS>, dim3(grid), dim3(kEngThreads), kEngSmem, st, map, M, K, mask, amax,
+                    seed, offset, q_colT, sb_colT, s_global, status);
 }
 
 template <int DT, int RND>
@@ -528,10 +532,10 @@ static cudaError_t rht_t(const void *x, int64_t M, int64_t K, uint32_t mask, boo
     if (compute_amax) {
         cudaError_t e = launch_zero_word(amax, st);
         if (e != cudaSuccess) return e;
-        e = rht_pass<DT, 0, 0>(map, M, K, mask, amax, seed, offset, q_colT, sb_colT, s_global, status, st);   // no rounding in the amax pass
+        e = rht_pass<DT, 0, 0>(true, map, M, K, mask, amax, seed, offset, q_colT, sb_colT, s_global, status, st);   // no rounding in the amax pass
         if (e != cudaSuccess) return e;
     }
-    return rht_pass<DT, RND, 1>(map, M, K, mask, amax, seed, offset, q_colT, sb_colT, s_global, status, st);
+    return rht_pass<DT, RND, 1>(compute_amax, map, M, K, mask, amax, seed, offset, q_colT, sb_colT, s_global, status, st);
 }
 
 cudaError_t launch_rht_amax(const void *x, int dt, int64_t M, int64_t K, uint32_t sign_mask, float *amax,
@@ -542,8 +546,8 @@ cudaError_t launch_rht_amax(const void *x, int dt, int64_t M, int64_t K, uint32_
     cudaError_t e = make_tile_map(&map, x, dt, M, K);
     if (e == cudaSuccess) e = launch_zero_word(amax, st);
     if (e != cudaSuccess) return e;
-    return dt == BF16 ? rht_pass<BF16, 0, 0>(map, M, K, sign_mask, amax, 0, 0, nullptr, nullptr, nullptr, status, st)
-                      : rht_pass<F32, 0, 0>(map, M, K, sign_mask, amax, 0, 0, nullptr, nullptr, nullptr, status, st);
+    return dt == BF16 ? rht_pass<BF16, 0, 0>(true, map, M, K, sign_mask, amax, 0, 0, nullptr, nullptr, nullptr, status, st)
+                      : rht_pass<F32, 0, 0>(true, map, M, K, sign_mask, amax, 0, 0, nullptr, nullptr, nullptr, status, st);
 }
 
 cudaError_t launch_nvfp4_rht_colT(const void *x, int dt, int64_t M, int64_t K, uint32_t sign_mask, int rnd,

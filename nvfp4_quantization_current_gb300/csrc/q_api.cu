@@ -119,7 +119,7 @@ q_status q_current_scaling(const void *x, q_dtype in, int64_t M, int64_t K, q_fp
     // an empty tensor takes the flat path, which only writes the scale
     LAUNCH("q_current_scaling/cast",
            qk::launch_cs_cast(x, (int)in, n == 0 ? 0 : M, n == 0 ? 0 : K, (int)fmt, amax, q_row,
-                              n == 0 ? nullptr : q_colT, scale, status, S(stream)));
+                              n == 0 ? nullptr : q_colT, scale, status, S(stream), amax_mode == Q_AMAX_COMPUTE));
     return Q_OK;
 }
 
@@ -252,7 +252,7 @@ q_status q_nvfp4(const void *x, q_dtype in, int64_t M, int64_t K, q_nvblk blk, q
     TRY(need(fn, "s_global", s_global, 4));
     if (amax_mode == Q_AMAX_COMPUTE) LAUNCH("q_nvfp4/amax", qk::launch_amax(x, (int)in, M * K, amax, status, S(stream)));
     LAUNCH("q_nvfp4/cast", qk::launch_nvfp4(x, (int)in, M, K, (int)blk, (int)rnd, seed, offset, amax, q_row, sb_row,
-                                            q_colT, sb_colT, s_global, status, S(stream)));
+                                            q_colT, sb_colT, s_global, status, S(stream), amax_mode == Q_AMAX_COMPUTE));
     return Q_OK;
 }
 

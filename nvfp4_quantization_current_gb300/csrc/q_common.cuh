@@ -431,6 +431,14 @@ template <int G> QD uint32_t group_max(uint32_t v)
     return v;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it in the stream has
+// finished (once every CTA of that kernel has signalled or exited); it must
+// call griddep_wait() before it touches anything that kernel writes.  In a
+// kernel launched normally griddep_wait() returns at once.
+QD void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+QD void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 QD void flag_nonfinite(int32_t *status, uint32_t amax_bits)
 {
     if (status != nullptr && amax_bits >= 0x7F800000u) atomicOr(status, kStNonFinite);

@@ -9,6 +9,26 @@ namespace qk {
 
 int sm_count();
 
+// Launch `kernel`; with pdl = true, as a programmatic dependent of the kernel
+// before it in the stream (the kernel then calls griddep_wait() before it
+// reads that kernel's output).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? at : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // A 2-D TMA tensor map over a row-major [M, K] input (dt: BF16, F32, or U8
 // for code matrices, K even) whose box is 128 rows x 512 bytes (the tile
 // engine's stage).  The x coordinate counts elements of 2 bytes (BF16, U8)
@@ -19,7 +39,8 @@ cudaError_t make_tile_map(void *map /* CUtensorMap, 64-byte aligned */, const vo
 // current scaling
 cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *status, cudaStream_t st);
 cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *amax,
-                           uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st);
+                           uint8_t *q_row, uint8_t *q_colT, float *scale, int32_t *status, cudaStream_t st,
+                           bool after_amax);
 
 // MXFP8
 cudaError_t launch_mxfp8(const void *x, int dt, int64_t M, int64_t K, int fmt, uint8_t *q_row,
@@ -56,7 +77,7 @@ cudaError_t launch_blockwise(const void *x, int dt, int64_t M, int64_t K, int ti
 cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, int rnd, uint64_t seed,
                          uint64_t offset, const float *amax, uint8_t *q_row, uint8_t *sb_row,
                          uint8_t *q_colT, uint8_t *sb_colT, float *s_global, int32_t *status,
-                         cudaStream_t st);
+                         cudaStream_t st, bool after_amax);
 
 // dequantizers
 cudaError_t launch_dq_cs(const uint8_t *q, const float *s, int64_t R, int64_t C, int fmt, int out,
