@@ -87,6 +87,7 @@ class Call:
         self.h2d = h2d              # input tensors (device) whose bytes an end-to-end call copies in
         self.d2h = d2h              # output tensors copied back end to end
         self.e2e_thunk = e2e_thunk  # the single public-API call (amax computed inside)
+        self.prime = None           # copies a producer call's outputs into this call's own inputs
 
     @property
     def alg_bytes(self):
@@ -98,9 +99,21 @@ def nbytes(*ts):
 
 
 def build_step(dev_tensors, torch, Q):
-    """Preallocate every output and return the list of calls of one step."""
+    """Preallocate every output and return the list of calls of one step.
+    A call that consumes another call's outputs (a dequantizer, the MXFP8
+    re-quantize) reads device buffers of its own, filled from the producer's
+    outputs once before timing (``Call.prime``): its end-to-end upload then
+    never waits for the producer's download of the same buffer."""
     calls = []
     d = dev_tensors
+
+    def own(*ts):
+        mine = [torch.empty_like(t) for t in ts]
+
+        def prime():
+            for m, t in zip(mine, ts):
+                m.copy_(t)
+        return mine, prime
 
     def cs(tag, x, fmt, colwise):
         out = Q.alloc_current_scaling(x.shape[0], x.shape[1], x.device, fmt, True, colwise)
@@ -120,10 +133,11 @@ def build_step(dev_tensors, torch, Q):
         calls.append(Call(f"{tag} cs_{fmt} row{'+colT' if colwise else ''}", "current_scaling", pieces, [x],
                           [out.q_row, out.q_colT, out.scale], e2e))
         y = torch.empty(x.shape, dtype=torch.bfloat16 if x.dtype == torch.bfloat16 else torch.float32, device=x.device)
+        (qd, sd), prime = own(out.q_row, out.scale)
+        r = lambda: Q.dq_current_scaling(qd, sd, fmt, y.dtype, out=y)
         calls.append(Call(f"{tag} dq_cs row->{str(y.dtype)[6:]}", "dequant",
-                          [("dq_cs", "k_dequant.cu", nbytes(out.q_row, out.scale, y),
-                            lambda: Q.dq_current_scaling(out.q_row, out.scale, fmt, y.dtype, out=y))],
-                          [out.q_row], [y], lambda: Q.dq_current_scaling(out.q_row, out.scale, fmt, y.dtype, out=y)))
+                          [("dq_cs", "k_dequant.cu", nbytes(qd, sd, y), r)], [qd, sd], [y], r))
+        calls[-1].prime = prime
 
     def ds(tag, x, fmt, N=1024):
         st = Q.DelayedScaling(fmt, history_len=N, algo="max", device=x.device)
@@ -145,15 +159,19 @@ def build_step(dev_tensors, torch, Q):
         calls.append(Call(f"{tag} mxfp8_e4m3 row+col", "mxfp8", [("mxfp8", "k_mxfp8.cu", b, run)], [x],
                           [out.q_row, out.e8m0_row, out.q_col, out.e8m0_col], run))
         rq = Q.alloc_mxfp8(x.shape[0], x.shape[1], x.device, "e4m3", False, True)
-        rrun = lambda: Q.q_mxfp8_requant_col(out.q_row, out.e8m0_row, "e4m3", out=rq)
+        (qr, er), prime = own(out.q_row, out.e8m0_row)
+        rrun = lambda: Q.q_mxfp8_requant_col(qr, er, "e4m3", out=rq)
         calls.append(Call(f"{tag} mxfp8_requant row->col", "mxfp8",
-                          [("mxfp8_requant", "k_mxfp8.cu", nbytes(out.q_row, out.e8m0_row, rq.q_col, rq.e8m0_col),
-                            rrun)], [out.q_row, out.e8m0_row], [rq.q_col, rq.e8m0_col], rrun))
-        for direction, q, e in ((Q.Q_ROW, out.q_row, out.e8m0_row), (Q.Q_COL, out.q_col, out.e8m0_col)):
+                          [("mxfp8_requant", "k_mxfp8.cu", nbytes(qr, er, rq.q_col, rq.e8m0_col), rrun)],
+                          [qr, er], [rq.q_col, rq.e8m0_col], rrun))
+        calls[-1].prime = prime
+        for direction, q0, e0 in ((Q.Q_ROW, out.q_row, out.e8m0_row), (Q.Q_COL, out.q_col, out.e8m0_col)):
             y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+            (q, e), prime = own(q0, e0)
             r = (lambda q=q, e=e, direction=direction, y=y: Q.dq_mxfp8(q, e, "e4m3", direction, torch.bfloat16, out=y))
             calls.append(Call(f"{tag} dq_mxfp8 {'row' if direction == Q.Q_ROW else 'col'}->bf16", "dequant",
                               [("dq_mxfp8", "k_dequant.cu", nbytes(q, e, y), r)], [q, e], [y], r))
+            calls[-1].prime = prime
 
     def bw(tag, x, tile, colwise):
         out = Q.alloc_blockwise(x.shape[0], x.shape[1], x.device, tile, True, colwise)
@@ -163,10 +181,11 @@ def build_step(dev_tensors, torch, Q):
                           [("bw_" + tile + ("_T" if colwise else ""), "k_blockwise.cu", b, run)], [x],
                           [out.q_row, out.s_row, out.q_colT, out.s_colT], run))
         y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
-        r = lambda: Q.dq_blockwise(out.q_row, out.s_row, tile, torch.bfloat16, out=y)
+        (qb, sb), prime = own(out.q_row, out.s_row)
+        r = lambda: Q.dq_blockwise(qb, sb, tile, torch.bfloat16, out=y)
         calls.append(Call(f"{tag} dq_blockwise_{tile} row->bf16", "dequant",
-                          [("dq_blockwise", "k_dequant.cu", nbytes(out.q_row, out.s_row, y), r)],
-                          [out.q_row, out.s_row], [y], r))
+                          [("dq_blockwise", "k_dequant.cu", nbytes(qb, sb, y), r)], [qb, sb], [y], r))
+        calls[-1].prime = prime
 
     def nv(tag, x, blk, rnd, seed):
         out = Q.alloc_nvfp4(x.shape[0], x.shape[1], x.device, blk, True, True)
@@ -186,10 +205,11 @@ def build_step(dev_tensors, torch, Q):
         calls.append(Call(f"{tag} nvfp4_{blk}_{rnd} row+colT", "nvfp4", pieces, [x],
                           [out.q_row, out.sb_row, out.q_colT, out.sb_colT, out.s_global], e2e))
         y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
-        r = lambda: Q.dq_nvfp4(out.q_row, out.sb_row, out.s_global, blk, torch.bfloat16, out=y)
+        (qn, sbn, sgn), prime = own(out.q_row, out.sb_row, out.s_global)
+        r = lambda: Q.dq_nvfp4(qn, sbn, sgn, blk, torch.bfloat16, out=y)
         calls.append(Call(f"{tag} dq_nvfp4_{blk} row->bf16", "dequant",
-                          [("dq_nvfp4", "k_dequant.cu", nbytes(out.q_row, out.sb_row, y), r)],
-                          [out.q_row, out.sb_row, out.s_global], [y], r))
+                          [("dq_nvfp4", "k_dequant.cu", nbytes(qn, sbn, sgn, y), r)], [qn, sbn, sgn], [y], r))
+        calls[-1].prime = prime
 
     def rht(tag, x, rnd, seed, mask=RHT_MASK):
         out = Q.alloc_nvfp4(x.shape[0], x.shape[1], x.device, "1x16", rowwise=False, colwise=True)
@@ -478,8 +498,12 @@ def run_ours(args):
     def new_events():
         return [[torch.cuda.Event(enable_timing=True) for _ in range(len(c.pieces) + 1)] for c in calls]
 
-    for _ in range(args.warmup):
+    for w in range(args.warmup):
         one_step(new_events())
+        if w == 0:   # the producers' outputs exist now: fill the consumers' own inputs
+            for c in calls:
+                if c.prime is not None:
+                    c.prime()
     torch.cuda.synchronize()
 
     all_evs = [new_events() for _ in range(args.steps)]
@@ -580,24 +604,56 @@ def run_ours(args):
                         in_host[id(t)] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
         h2d_b = sum(nbytes(t) for c in calls for t in c.h2d if t is not None)
         d2h_b = sum(nbytes(t) for c in calls for t in c.d2h if t is not None)
+        # Three streams: host->device copies, the public calls, device->host
+        # copies; call i+1's inputs upload while call i computes and call i-1's
+        # results download.  Each device tensor keeps the event of its last use
+        # (compute reading it, or the download of it), and an upload into it
+        # waits for that event; a call waits for its own uploads and its
+        # download for the call.  One event pair spans the whole step.
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        s_cmp = stream
         e_ms = []
         for s in range(e2e_steps + 1):
-            tot = 0.0
+            torch.cuda.synchronize()
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record(s_cmp)
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+            last = {}
             for c in calls:
-                flush.fill_(1.0)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
                 for t in c.h2d:
-                    t.copy_(in_host[id(t)], non_blocking=True)
-                c.e2e_thunk()
+                    if id(t) in last:
+                        s_in.wait_event(last[id(t)])
+                with torch.cuda.stream(s_in):
+                    for t in c.h2d:
+                        t.copy_(in_host[id(t)], non_blocking=True)
+                e_in = torch.cuda.Event()
+                e_in.record(s_in)
+                s_cmp.wait_event(e_in)
+                for t in c.d2h:
+                    if t is not None and id(t) in last:
+                        s_cmp.wait_event(last[id(t)])
+                with torch.cuda.stream(s_cmp):
+                    c.e2e_thunk()
+                e_c = torch.cuda.Event()
+                e_c.record(s_cmp)
+                s_out.wait_event(e_c)
+                with torch.cuda.stream(s_out):
+                    for t in c.d2h:
+                        if t is not None:
+                            out_host[id(t)].copy_(t, non_blocking=True)
+                e_o = torch.cuda.Event()
+                e_o.record(s_out)
+                for t in c.h2d:
+                    last[id(t)] = e_c
                 for t in c.d2h:
                     if t is not None:
-                        out_host[id(t)].copy_(t, non_blocking=True)
-                b.record(stream)
-                b.synchronize()
-                tot += a.elapsed_time(b)
+                        last[id(t)] = e_o
+            s_cmp.wait_event(e_o)
+            end.record(s_cmp)
+            end.synchronize()
             if s > 0:          # the first pass warms the copy engines
-                e_ms.append(tot)
+                e_ms.append(start.elapsed_time(end))
         ems = statistics.mean(e_ms)
         if world > 1:
             t = torch.tensor([ems], device=dev)
@@ -605,7 +661,7 @@ def run_ours(args):
             ems = float(t.item())
         e2e = {"value": round(step_bytes * world / (ems * 1e-3) / 1e9, 1), "unit": UNIT,
                "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b, "ms_per_step": round(ems, 3),
-               "steps": e2e_steps}
+               "steps": e2e_steps, "schedule": "uploads, calls and downloads on three streams, overlapped across calls"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu and not args.only:
