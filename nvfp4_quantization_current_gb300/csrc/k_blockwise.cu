@@ -167,8 +167,31 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
             post_nonfinite(status, nf);
             if (q_colT == nullptr) return;
             __syncthreads();   // partial column maxima posted
-            // ---------------- 128x1 columnwise: two threads per column reduce 8 partials each
-            {
+            // ---------------- 128x1 columnwise ----------------
+            if constexpr (DT == BF16) {
+                // four threads per BF16 column pair (one 32-bit word of the
+                // partials), each reducing 4 of the 16 warp partials; two shuffles
+                // combine them and two of the four take one column each
+                const int wp = t >> 2, sub = t & 3;          // 128 column pairs
+                const int q = wp >> 2, wi = wp & 3;          // lane q of the partials, word wi
+                const uint32_t *pw = reinterpret_cast<const uint32_t *>(&part[0][0]) + q * 4 + wi;
+                uint32_t b2 = 0;
+#pragma unroll
+                for (int w = sub; w < kEngWarps; w += 4) b2 = hmax_abs2(b2, pw[w * 32 * 4]);
+                b2 = hmax_abs2(b2, __shfl_xor_sync(0xFFFFFFFFu, b2, 1));
+                b2 = hmax_abs2(b2, __shfl_xor_sync(0xFFFFFFFFu, b2, 2));
+                if (sub < 2) {
+                    const int col = 2 * wp + sub;             // low half: even column
+                    const uint32_t b = (sub ? b2 : (b2 << 16)) & 0x7FFF0000u;
+                    float alpha, sc;
+                    bw_scales<DT>(b, tab, alpha, sc);
+                    calpha[col] = alpha;
+                    if (kb + col < K) {
+                        s_colT[(kb + col) * (M / 128) + tm] = sc;
+                        flag_nonfinite(status, b);
+                    }
+                }
+            } else {
                 constexpr int TPC = 2 * kEngThreads / TC >= 2 ? 2 : 1;   // threads per column (TC <= 256)
                 const int col = t / TPC, half = t % TPC;
                 if (col < TC) {

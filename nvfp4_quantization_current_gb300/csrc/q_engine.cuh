@@ -103,20 +103,24 @@ template <int VEC> QD void park_fp8T(uint8_t *stage, const uint32_t (*code)[VEC 
     }
 }
 
-// Writes the parked [TC][128] code tile as q_colT rows (16 threads x 8 bytes
-// per 128-byte row).
+// Writes the parked [TC][128] code tile as q_colT rows (8 threads x 16 bytes
+// per 128-byte row; M % 16 == 0).  Chunks 2p and 2p+1 (rows 16p..16p+15)
+// sit in the aligned pair of 8-byte slots 2p ^ (s & ~1), in swapped order
+// when the swizzle s is odd.
 template <int VEC>
 QD void copy_out_fp8T(const uint8_t *stage, uint8_t *q_colT, int64_t M, int64_t K, int64_t mb, int64_t kb)
 {
     constexpr int TC = 32 * VEC;
 #pragma unroll
-    for (int it = 0; it < TC * 16 / kEngThreads; it++) {
+    for (int it = 0; it < TC * 8 / kEngThreads; it++) {
         const int idx = it * kEngThreads + threadIdx.x;
-        const int col = idx >> 4, ch = idx & 15;
-        const int64_t kg = kb + col, mg = mb + 8 * ch;
+        const int col = idx >> 3, pr = idx & 7;
+        const int s = (col / VEC) & 15;
+        const int64_t kg = kb + col, mg = mb + 16 * pr;
         if (kg < K && mg < M) {
-            const uint2 v = *reinterpret_cast<const uint2 *>(stage + col * 128 + ((ch ^ ((col / VEC) & 15)) * 8));
-            stg8(q_colT + kg * M + mg, v.x, v.y);
+            uint4 v = *reinterpret_cast<const uint4 *>(stage + col * 128 + ((2 * pr) ^ (s & ~1)) * 8);
+            if (s & 1) v = make_uint4(v.z, v.w, v.x, v.y);
+            stg16(q_colT + kg * M + mg, v);
         }
     }
 }
