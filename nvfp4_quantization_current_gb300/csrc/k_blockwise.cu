@@ -239,9 +239,18 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
             b = group_max<LPB>(b);
             if (lane % LPB == 0) tred[warp][lane / LPB] = b;
             __syncthreads();   // tile maxima posted; every read of the stage is done
-            uint32_t bt = 0;
+            uint32_t bt;
+            if constexpr (NT * kEngWarps == 32) {
+                // lane l fetches warp (l % 16)'s maximum of block l / 16 (the block
+                // of its own columns); 4 shuffles reduce over the 16 warps
+                bt = tred[lane & 15][lane >> 4];
 #pragma unroll
-            for (int q = 0; q < kEngWarps; q++) bt = max(bt, tred[q][lane / LPB]);
+                for (int o = 1; o < 16; o <<= 1) bt = max(bt, __shfl_xor_sync(0xFFFFFFFFu, bt, o));
+            } else {
+                bt = 0;
+#pragma unroll
+                for (int q = 0; q < kEngWarps; q++) bt = max(bt, tred[q][lane / LPB]);
+            }
             float alpha, sc;
             bw_scales<DT>(bt, tab, alpha, sc);
             if (warp == 0 && lane % LPB == 0 && kok) {
