@@ -117,10 +117,29 @@ template <int VEC> QD void park_fp4T(uint8_t *stage, const uint32_t *col, int wa
         *reinterpret_cast<uint32_t *>(stage + (lane * VEC + c) * 64 + ((warp ^ (lane & 15)) * 4)) = col[c];
 }
 
+// With M % 32 == 0 the rows go out as 16-byte pieces (4 threads per 64-byte
+// row): slots 4g..4g+3 sit in the aligned group 4g ^ (s & ~3), word k holding
+// slot 4g + (k ^ (s & 3)).
 template <int VEC>
 QD void copy_out_fp4T(const uint8_t *stage, uint8_t *q_colT, int64_t M, int64_t K, int64_t mb, int64_t kb)
 {
     constexpr int TC = 32 * VEC;
+    if ((M & 31) == 0) {
+#pragma unroll
+        for (int it = 0; it < TC * 4 / kEngThreads; it++) {
+            const int idx = it * kEngThreads + threadIdx.x;
+            const int col = idx >> 2, g = idx & 3;   // rows 32g..32g+31 of the tile
+            const int s = (col / VEC) & 15;
+            const int64_t kg = kb + col, mg = mb + 32 * g;
+            if (kg < K && mg < M) {
+                uint4 w = *reinterpret_cast<const uint4 *>(stage + col * 64 + ((4 * g) ^ (s & ~3)) * 4);
+                if (s & 1) w = make_uint4(w.y, w.x, w.w, w.z);
+                if (s & 2) w = make_uint4(w.z, w.w, w.x, w.y);
+                stg16(q_colT + kg * (M / 2) + mg / 2, w);
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int it = 0; it < TC * 16 / kEngThreads; it++) {
         const int idx = it * kEngThreads + threadIdx.x;
@@ -214,7 +233,52 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
             }
             // ---------------- 1x16 rowwise ----------------
             uint32_t nf = 0;
-            if (q_row != nullptr) {
+            if (DT == BF16 && q_row != nullptr) {
+                // A block is 2 lanes.  The 8 row maxima, two BF16 magnitudes per
+                // word, are halved across the pair: this lane keeps rows
+                // rb..rb+3 (rb = 4 * (lane & 1)), computes their block scales and
+                // encode factors, and takes the partner's 4 factors by shuffle.
+                const int nrows = !kok ? 0 : (m0 + 8 <= M ? 8 : (m0 < M ? (int)(M - m0) : 0));
+                uint32_t P[4];
+#pragma unroll
+                for (int p = 0; p < 4; p++) {
+                    const uint4 &a = v[2 * p], &b = v[2 * p + 1];
+                    const uint32_t ma = hmax_abs2(hmax_abs2(a.x, a.y), hmax_abs2(a.z, a.w));
+                    const uint32_t mb2 = hmax_abs2(hmax_abs2(b.x, b.y), hmax_abs2(b.z, b.w));
+                    P[p] = hmax_abs2(__byte_perm(ma, mb2, 0x5410), __byte_perm(ma, mb2, 0x7632));   // row 2p low, 2p+1 high
+                }
+                const bool b0 = lane & 1;
+                const int rb = b0 ? 4 : 0;
+                uint32_t k0 = b0 ? P[2] : P[0], k1 = b0 ? P[3] : P[1];
+                const uint32_t s0 = b0 ? P[0] : P[2], s1 = b0 ? P[1] : P[3];
+                k0 = hmax_abs2(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, 1));
+                k1 = hmax_abs2(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, 1));
+                float own[4];
+#pragma unroll
+                for (int h = 0; h < 4; h++) {
+                    const uint32_t kw = h < 2 ? k0 : k1;
+                    const uint32_t bits = ((h & 1) ? kw : (kw << 16)) & 0x7FFF0000u;   // row rb + h
+                    const uint32_t sb = nv_sb_code<DT>(bits, alpha_g, sb_tab, ae);
+                    own[h] = enc_tab[sb];
+                    if (rb + h < nrows) {
+                        sb_row[(m0 + rb + h) * (K / 16) + k / 16] = (uint8_t)sb;
+                        nf |= nonfinite(bits);
+                    }
+                }
+                float encr[8];
+#pragma unroll
+                for (int h = 0; h < 4; h++) {
+                    const float other = __shfl_xor_sync(0xFFFFFFFFu, own[h], 1);
+                    encr[h] = b0 ? other : own[h];
+                    encr[4 + h] = b0 ? own[h] : other;
+                }
+                uint8_t *qr = q_row + m0 * (K / 2) + k / 2;
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const uint32_t code = nv_row_codes<DT, RND>(v[j], encr[j], seed, offset, (m0 + j) * K + k);
+                    if (j < nrows) stg4(qr + j * (K / 2), code);
+                }
+            } else if (q_row != nullptr) {
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
                     uint32_t bb[2] = {absmax_bits<DT>(v[j]), absmax_bits<DT>(v[j + 1])};
