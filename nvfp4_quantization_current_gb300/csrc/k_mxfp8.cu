@@ -52,7 +52,50 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8(const __grid_constant_
             part[warp][lane] = acc;
         }
         uint32_t nf = 0;   // non-finite block maxima seen by this thread
-        if (q_row != nullptr) {
+        if (DT == BF16 && q_row != nullptr) {
+            // A block is 4 lanes.  The 8 row maxima, two BF16 magnitudes per
+            // word, are halved across the group twice (3 shuffles): lane L keeps
+            // rows 4*(L>>1 & 1) + 2*(L & 1) and the next, computes their codes
+            // once, and the inverse scales go back by index shuffles.
+            const int nrows = !kok ? 0 : (m0 + 8 <= M ? 8 : (m0 < M ? (int)(M - m0) : 0));
+            uint32_t P[4];
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+                const uint4 &a = v[2 * p], &b = v[2 * p + 1];
+                const uint32_t ma = hmax_abs2(hmax_abs2(a.x, a.y), hmax_abs2(a.z, a.w));
+                const uint32_t mb = hmax_abs2(hmax_abs2(b.x, b.y), hmax_abs2(b.z, b.w));
+                P[p] = hmax_abs2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632));   // row 2p low, 2p+1 high
+            }
+            const bool b1 = lane & 2, b0 = lane & 1;
+            uint32_t k0 = b1 ? P[2] : P[0], k1 = b1 ? P[3] : P[1];          // rows 4*b1 .. 4*b1+3
+            const uint32_t s0 = b1 ? P[0] : P[2], s1 = b1 ? P[1] : P[3];
+            k0 = hmax_abs2(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, 2));
+            k1 = hmax_abs2(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, 2));
+            uint32_t kw = b0 ? k1 : k0;                                        // rows 4*b1+2*b0, +1
+            kw = hmax_abs2(kw, __shfl_xor_sync(0xFFFFFFFFu, b0 ? k0 : k1, 1));
+            const int r = 4 * (b1 ? 1 : 0) + 2 * (b0 ? 1 : 0);
+            const uint32_t blo = (kw << 16) & 0x7FFF0000u, bhi = kw & 0x7FFF0000u;   // rows r, r + 1
+            const uint32_t clo = mx_code<FMT>(blo), chi = mx_code<FMT>(bhi);
+            const float ilo = mx_inv_scale(clo), ihi = mx_inv_scale(chi);
+            if (r < nrows) {
+                e_row[(m0 + r) * (K / 32) + k / 32] = (uint8_t)clo;
+                nf |= nonfinite(blo);
+            }
+            if (r + 1 < nrows) {
+                e_row[(m0 + r + 1) * (K / 32) + k / 32] = (uint8_t)chi;
+                nf |= nonfinite(bhi);
+            }
+            uint8_t *qr = q_row + m0 * K + k;
+            const int gb = lane & ~3;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                // row j lives in lane gb + 2*(j >> 2) + ((j >> 1) & 1), low half for even j
+                const float inv = __shfl_sync(0xFFFFFFFFu, (j & 1) ? ihi : ilo, gb + 2 * (j >> 2) + ((j >> 1) & 1));
+                uint32_t o[CW];
+                chunk_fp8<DT, FMT>(v[j], inv, o);
+                if (j < nrows) stg8(qr + j * K, o[0], o[CW - 1]);
+            }
+        } else if (q_row != nullptr) {
 #pragma unroll
             for (int j = 0; j < 8; j += 2) {
                 uint32_t bb[2] = {absmax_bits<DT>(v[j]), absmax_bits<DT>(v[j + 1])};
