@@ -4,16 +4,21 @@
 // One CTA of 512 threads per SM.  Thread 0 keeps kStages tiles in flight:
 // each is one cp.async.bulk.tensor.2d load (the tensor map's box is 128 rows
 // x 512 bytes; rows or columns past the tensor's edge arrive as zeros) that
-// completes on the stage's mbarrier.  All threads then run the recipe's tile
-// body on the stage; when they are done (barrier) thread 0 refills the stage
-// with the tile kS tiles ahead.  Bytes in flight per SM are set by the
-// stages, not by registers or occupancy, so the bodies can spend registers on
-// arithmetic.
+// completes on the stage's mbarrier.  Every thread waits on that mbarrier
+// itself (its acquire makes the tile visible to the thread, so no CTA
+// barrier is needed at the start of a tile), runs the recipe's tile body on
+// the stage, and when all are done (barrier) thread 0 refills the stage with
+// the tile kStages tiles ahead.  Bytes in flight per SM are set by the
+// stages, not by registers or occupancy, so the bodies can spend registers
+// on arithmetic.
 //
-// Every wait is bounded: thread 0 polls the stage barrier with try_wait and
-// gives up after kWaitNs of %globaltimer, ORs Q_ST_TIMEOUT into the status
-// word, waits (bounded again) for the copies it still has in flight, and
-// the CTA returns.
+// Every wait is bounded: a thread polls the stage barrier with try_wait and
+// gives up after kWaitNs of %globaltimer.  A thread that gives up ORs
+// Q_ST_TIMEOUT into the status word and carries on with the same control
+// flow as the others (every barrier of the bodies is still reached by all
+// threads; the outputs of such a launch are not meaningful).  After the last
+// tile thread 0 waits (bounded again) for any copy it saw time out, so that
+// no copy is in flight when the CTA's shared memory goes away.
 #pragma once
 
 #include <cuda.h>
@@ -135,7 +140,6 @@ __device__ __forceinline__ void run_tiles(const CUtensorMap *tmap, int64_t tiles
 {
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t full[kStages];
-    __shared__ int s_ok;
 
     const int64_t ntiles = tiles_m * tiles_k;
     const int64_t count = ntiles > (int64_t)blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
@@ -158,27 +162,25 @@ __device__ __forceinline__ void run_tiles(const CUtensorMap *tmap, int64_t tiles
     if (threadIdx.x == 0)
         for (int64_t i = 0; i < count && i < kStages; i++) issue(i, (int)i);
 
+    int64_t late = -1;   // thread 0: the first tile whose wait it gave up on
     for (int64_t i = 0; i < count; i++) {
         const int s = (int)(i % kStages);
-        if (threadIdx.x == 0) s_ok = mbar_wait_bounded(&full[s], (uint32_t)((i / kStages) & 1)) ? 1 : 0;
-        __syncthreads();
-        if (!s_ok) {
-            if (threadIdx.x == 0) {
-                if (status != nullptr) atomicOr(status, kStTimeout);
-                // let the copies still in flight land before the CTA's shared memory goes away
-                for (int64_t j = i; j < count && j < i + kStages; j++)
-                    (void)mbar_wait_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1));
-            }
-            return;
+        if (!mbar_wait_bounded(&full[s], (uint32_t)((i / kStages) & 1))) {
+            if (status != nullptr) atomicOr(status, kStTimeout);
+            if (threadIdx.x == 0 && late < 0) late = i;
         }
         const int64_t t = tile_of(i);
         const int64_t tm = t / tiles_k, tk = t - tm * tiles_k;
         body(dsm + s * kTileBytes, tm, tk);
-        __syncthreads();
+        __syncthreads();   // every thread is done with the stage
         if (threadIdx.x == 0 && i + kStages < count) {
             fence_proxy_async();   // generic-proxy accesses of the stage before the async-proxy refill
             issue(i + kStages, s);
         }
+    }
+    if (threadIdx.x == 0 && late >= 0) {
+        // let copies that were still in flight land before the CTA's shared memory goes away
+        for (int64_t j = late; j < count; j++) (void)mbar_wait_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1));
     }
 }
 
