@@ -256,6 +256,17 @@ q_status q_nvfp4_rht_colT(const void *x, q_dtype in, int64_t M, int64_t K, uint3
                           float *amax, q_amax_mode amax_mode, float *s_global, int32_t *status, q_stream_t stream);
 
 /*
+ * Diagnostic of the device-side failure path (a library check, not an
+ * operation of the pages).  Every wait in the kernels is bounded: a thread
+ * that polls a shared-memory barrier longer than its limit gives up and ORs
+ * Q_ST_TIMEOUT into the status word, and the context stays usable.  This
+ * entry runs one warp that waits, with limit wait_ns, on a barrier whose
+ * phase needs an arrival nobody makes, so the wait runs out and *status gets
+ * Q_ST_TIMEOUT.  status: one device int32 (required); 0 < wait_ns <= 10^9.
+ */
+q_status q_selftest_wait_timeout(int32_t *status, uint64_t wait_ns, q_stream_t stream);
+
+/*
  * a12: dequantizers.  Output y [R, C] in `out` (Q_F32, or Q_BF16 rounded to
  * nearest even from the FP32 value).  A transposed columnwise output is
  * passed as the [K, M] matrix it is (R = K, C = M).

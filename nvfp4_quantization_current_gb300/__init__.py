@@ -51,7 +51,7 @@ Q_B1x16, Q_B16x16 = 0, 1
 Q_RN, Q_SR = 0, 1
 Q_ROW, Q_COL = 0, 1
 Q_AMAX_COMPUTE, Q_AMAX_GIVEN = 0, 1
-Q_ST_NONFINITE = 1
+Q_ST_NONFINITE, Q_ST_TIMEOUT = 1, 2
 
 STATUS_NAMES = {Q_OK: "Q_OK", Q_ERR_ARG: "Q_ERR_ARG", Q_ERR_SHAPE: "Q_ERR_SHAPE", Q_ERR_ALIGN: "Q_ERR_ALIGN",
                 Q_ERR_DTYPE: "Q_ERR_DTYPE", Q_ERR_CUDA: "Q_ERR_CUDA"}
@@ -66,6 +66,7 @@ SIGNATURES = {
     "q_mxfp8": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "q_delayed_scaling": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P, _P]),
     "q_delayed_scale_update": (_I, [_P, _I64, _I64, _I, _I, _P, _P]),
+    "q_selftest_wait_timeout": (_I, [_P, _U64, _P]),
     "q_mxfp8_requant_col": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
     "q_blockwise": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "q_nvfp4": (_I, [_P, _I, _I64, _I64, _I, _I, _U64, _U64, _P, _P, _P, _P, _P, _I, _P, _P, _P]),
@@ -463,6 +464,14 @@ def q_nvfp4_rht_colT(x: torch.Tensor, sign_mask: int, rounding="rn", seed=0, off
     _call("q_nvfp4_rht_colT", _ptr(x), dt, M, K, int(sign_mask), rnd, int(seed), int(offset), _ptr(out.q_colT),
           _ptr(out.sb_colT), _ptr(out.amax), mode, _ptr(out.s_global), _ptr(status), _stream(x.device))
     return out
+
+
+def selftest_wait_timeout(status: torch.Tensor, wait_ns: int = 50_000_000) -> torch.Tensor:
+    """Diagnostic: one warp waits ``wait_ns`` on a barrier nothing completes and
+    reports Q_ST_TIMEOUT in ``status`` (a one-element int32 device tensor),
+    exercising the bounded-wait path every kernel uses."""
+    _call("q_selftest_wait_timeout", _ptr(status), int(wait_ns), _stream(status.device))
+    return status
 
 
 def dq_nvfp4(q, sb, s_global, blk="1x16", dtype=torch.float32, out=None):

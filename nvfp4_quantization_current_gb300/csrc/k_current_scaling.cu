@@ -338,6 +338,27 @@ cudaError_t launch_ds_update(const float *hist, int64_t N, int64_t pos, int algo
     return cudaGetLastError();
 }
 
+// Diagnostic of the bounded waits: one warp waits on a barrier whose first
+// phase needs an arrival that no thread makes, so every wait can only end by
+// its time limit; each thread that gives up ORs Q_ST_TIMEOUT into *status.
+// Nothing is in flight when the CTA exits.
+__global__ void k_selftest_wait(int32_t *status, unsigned long long wait_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (!mbar_wait_bounded(&bar, 0u, wait_ns)) atomicOr(status, kStTimeout);
+}
+
+cudaError_t launch_selftest_wait(int32_t *status, unsigned long long wait_ns, cudaStream_t st)
+{
+    k_selftest_wait<<<1, 32, 0, st>>>(status, wait_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_empty_scales(float *amax_out, float *scale, cudaStream_t st)
 {
     k_empty_scales<<<1, 1, 0, st>>>(amax_out, scale);

@@ -293,6 +293,15 @@ q_status q_nvfp4_rht_colT(const void *x, q_dtype in, int64_t M, int64_t K, uint3
     return Q_OK;
 }
 
+q_status q_selftest_wait_timeout(int32_t *status, uint64_t wait_ns, q_stream_t stream)
+{
+    const char *fn = "q_selftest_wait_timeout";
+    TRY(need(fn, "status", status, 4));
+    if (wait_ns == 0 || wait_ns > 1000000000ull) return fail(Q_ERR_ARG, "%s: wait_ns %llu is outside (0, 1e9]", fn, (unsigned long long)wait_ns);
+    LAUNCH(fn, qk::launch_selftest_wait(status, (unsigned long long)wait_ns, S(stream)));
+    return Q_OK;
+}
+
 q_status dq_current_scaling(const uint8_t *q, const float *scale, int64_t R, int64_t C, q_fp8 fmt, q_dtype out,
                             void *y, q_stream_t stream)
 {

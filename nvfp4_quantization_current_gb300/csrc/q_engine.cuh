@@ -67,14 +67,15 @@ QD unsigned long long globaltimer()
     return t;
 }
 
-// Poll until the barrier's phase with this parity completes; false after kWaitNs.
-QD bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+// Poll until the barrier's phase with this parity completes; false after
+// limit_ns (kWaitNs unless given).
+QD bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, unsigned long long limit_ns = kWaitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 

@@ -46,6 +46,9 @@ cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt,
 cudaError_t launch_mxfp8(const void *x, int dt, int64_t M, int64_t K, int fmt, uint8_t *q_row,
                          uint8_t *e_row, uint8_t *q_col, uint8_t *e_col, int32_t *status, cudaStream_t st);
 
+// one warp waits wait_ns on a barrier nothing completes, then reports Q_ST_TIMEOUT
+cudaError_t launch_selftest_wait(int32_t *status, unsigned long long wait_ns, cudaStream_t st);
+
 // *w = 0 (one thread), stream-ordered before a reduction into it
 cudaError_t launch_zero_word(float *w, cudaStream_t st);
 

@@ -114,6 +114,15 @@ def test_rht_validation(L):
     assert st == Q.Q_ERR_ARG
 
 
+def test_selftest_validation(L):
+    st, _ = status_of(L, "q_selftest_wait_timeout", None, 1000, None)
+    assert st == Q.Q_ERR_ARG
+    st, msg = status_of(L, "q_selftest_wait_timeout", A, 0, None)
+    assert st == Q.Q_ERR_ARG and "wait_ns" in msg
+    st, _ = status_of(L, "q_selftest_wait_timeout", A, 2_000_000_000, None)
+    assert st == Q.Q_ERR_ARG
+
+
 def test_requant_validation(L):
     st, _ = status_of(L, "q_mxfp8_requant_col", A, A, 48, 64, Q.Q_E4M3, A, A, None, None)
     assert st == Q.Q_ERR_SHAPE                     # M % 32

@@ -137,6 +137,24 @@ def test_tiny_values_scale_to_fp32_subnormals():
     f32eq(got.scale.item(), want.scale)
 
 
+def test_bounded_wait_times_out_and_context_stays_usable():
+    """A wait on a barrier that nothing completes gives up after its limit,
+    reports Q_ST_TIMEOUT, and the next calls work normally."""
+    import time
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    Q.selftest_wait_timeout(st, 50_000_000)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 >= 0.045
+    assert st.item() & Q.Q_ST_TIMEOUT
+    x = W.gen("outliers", (64, 48), 5, bf16=True)
+    got = Q.q_current_scaling(dev(x), "e4m3", colwise=True)
+    want = O.current_scaling(x, O.E4M3, colwise=True)
+    same(host(got.q_row), want.q_row)
+    same(host(got.q_colT), want.q_colT)
+
+
 def test_nonfinite_sets_status():
     x = W.gen("normal", (32, 32), 3, bf16=False)
     x[3, 4] = np.inf
