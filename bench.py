@@ -602,14 +602,17 @@ def run_ours(args):
                     in_host[id(t)] = dev_to_pin.get(id(t))
                     if in_host[id(t)] is None:
                         in_host[id(t)] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-        h2d_b = sum(nbytes(t) for c in calls for t in c.h2d if t is not None)
+        h2d_unique = {id(t): t for c in calls for t in c.h2d if t is not None}
+        h2d_b = sum(nbytes(t) for t in h2d_unique.values())   # each input uploads once per step
         d2h_b = sum(nbytes(t) for c in calls for t in c.d2h if t is not None)
         # Three streams: host->device copies, the public calls, device->host
         # copies; call i+1's inputs upload while call i computes and call i-1's
-        # results download.  Each device tensor keeps the event of its last use
-        # (compute reading it, or the download of it), and an upload into it
-        # waits for that event; a call waits for its own uploads and its
-        # download for the call.  One event pair spans the whole step.
+        # results download.  Each input tensor uploads once per step (two calls
+        # on one tensor share the upload); each device tensor keeps the event
+        # of its last use (compute reading it, or the download of it), and an
+        # upload into it waits for that event; a call waits for the uploads of
+        # its inputs and its download for the call.  One event pair spans the
+        # whole step.
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         s_cmp = stream
         e_ms = []
@@ -619,17 +622,19 @@ def run_ours(args):
             start.record(s_cmp)
             s_in.wait_event(start)
             s_out.wait_event(start)
-            last = {}
+            last, up = {}, {}
             for c in calls:
                 for t in c.h2d:
+                    if id(t) in up:
+                        continue
                     if id(t) in last:
                         s_in.wait_event(last[id(t)])
-                with torch.cuda.stream(s_in):
-                    for t in c.h2d:
+                    with torch.cuda.stream(s_in):
                         t.copy_(in_host[id(t)], non_blocking=True)
-                e_in = torch.cuda.Event()
-                e_in.record(s_in)
-                s_cmp.wait_event(e_in)
+                    up[id(t)] = torch.cuda.Event()
+                    up[id(t)].record(s_in)
+                for t in c.h2d:
+                    s_cmp.wait_event(up[id(t)])
                 for t in c.d2h:
                     if t is not None and id(t) in last:
                         s_cmp.wait_event(last[id(t)])
