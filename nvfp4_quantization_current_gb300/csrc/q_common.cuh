@@ -1,10 +1,10 @@
-// Device helpers shared by the quantizer kernels (sm_103a).
-//
-// Every kernel that tiles the input uses the same geometry: a CTA of 8 warps
-// owns a tile of 128 rows x (32 * VEC) columns, each warp 16 rows, each lane
-// a 16-row x VEC-column micro-tile held in registers as 16 x 16-byte vectors
-// (VEC = 8 BF16 or 4 FP32 elements).  A warp's load of one row is 512
-// contiguous bytes; a thread keeps 16 independent 16-byte loads in flight.
+// Device helpers shared by the quantizer kernels (sm_103a): loads and
+// stores, element access, |x| maxima, FP8 / FP4 conversions, the scale
+// rules, Philox4x32-10 and stochastic rounding, reductions, the CTA-wide
+// maximum, programmatic-dependent-launch waits and the 4x4 byte transpose.
+// The tile geometry of the kernels that stream 128-row tiles is in
+// q_engine.cuh (a 16-byte chunk of 8 rows per thread, VEC = 8 BF16 or 4 FP32
+// elements per chunk).
 //
 // FP32 arithmetic that decides a code is written with explicit round-to-
 // nearest intrinsics (__fmul_rn, __fdiv_rn) so that no product is fused into
@@ -23,10 +23,6 @@ namespace qk {
 enum { BF16 = 0, F32 = 1, U8 = 2 };
 enum { E4M3 = 0, E5M2 = 1 };
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRowsPerWarp = 16;
-constexpr int kTileRows = kWarps * kRowsPerWarp;   // 128
 constexpr int32_t kStNonFinite = 1;
 
 template <int DT> struct In;
@@ -281,44 +277,6 @@ template <int DT, int FMT> QD void chunk_fp8(const uint4 &v, float s, uint32_t *
     for (int j = 0; j < VEC; j += 2) mul2(f[j], f[j + 1], s, s);
 #pragma unroll
     for (int w = 0; w < VEC / 4; w++) o[w] = cvt_fp8x4<FMT>(f[4 * w], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
-}
-
-// Element c (0..CPW-1) of a 4-byte word of the input (two BF16 or one FP32).
-template <int DT> QD float word_elem(uint32_t w, int c)
-{
-    return DT == BF16 ? __uint_as_float(c ? (w & 0xFFFF0000u) : (w << 16)) : __uint_as_float(w);
-}
-
-// Column c of N consecutive rows (N words) times s, as FP8 codes (N/4 words,
-// row 0 in the lowest byte).
-template <int DT, int FMT, int N> QD void column_fp8(const uint32_t *w, int c, float s, uint32_t *o)
-{
-    float f[N];
-#pragma unroll
-    for (int r = 0; r < N; r++) f[r] = word_elem<DT>(w[r], c);
-#pragma unroll
-    for (int r = 0; r < N; r += 2) mul2(f[r], f[r + 1], s, s);
-#pragma unroll
-    for (int g = 0; g < N / 4; g++) o[g] = cvt_fp8x4<FMT>(f[4 * g], f[4 * g + 1], f[4 * g + 2], f[4 * g + 3]);
-}
-
-// Per-column |x| maxima over N rows of words, as FP32 bit patterns:
-// m[c] for c < CPW.  BF16 words keep both columns' maxima packed
-// (one 16x2 max per row).
-template <int DT, int N> QD void column_absmax(const uint32_t *w, uint32_t *m)
-{
-    if (DT == BF16) {
-        uint32_t acc = 0;
-#pragma unroll
-        for (int r = 0; r < N; r++) acc = __vmaxu2(acc, w[r] & 0x7FFF7FFFu);
-        m[0] = acc << 16;
-        m[DT == BF16 ? 1 : 0] = acc & 0xFFFF0000u;
-    } else {
-        uint32_t acc = 0;
-#pragma unroll
-        for (int r = 0; r < N; r++) acc = max(acc, w[r] & 0x7FFFFFFFu);
-        m[0] = acc;
-    }
 }
 
 // ---------------------------------------------------------------------------

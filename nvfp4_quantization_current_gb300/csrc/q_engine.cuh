@@ -87,7 +87,6 @@ QD void tma_load_tile(void *dst, const CUtensorMap *map, int x, int y, uint64_t 
 }
 
 QD uint4 lds16(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
-QD uint32_t lds4(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
 // Transposed FP8 codes of a tile, staged for full-line writes: each thread
 // holds 8 rows (8w..8w+7) x VEC columns of codes, as VEC/4 words per row
