@@ -11,7 +11,13 @@ multi-GPU use": compute amax, synchronize amax, scale + cast, all-gather;
 the FP8 tensor must be identical with or without TP).
 
 The block-scaled recipes (MXFP8, blockwise, NVFP4 block scales) need no
-exchange when shards split rows on block boundaries.
+exchange when shards split rows on block boundaries.  Delayed scaling
+all-reduces the step's recorded amax into every rank's window slot
+(``DelayedScaling.quantize(group=...)``), so the windows, and the scales
+they give, stay identical.  The random-Hadamard NVFP4 copy of the
+weight-gradient inputs all-reduces the amax of the transformed shard; shards
+that split rows on 16-row boundaries transform exactly like the slices of
+the whole tensor.
 
 ``allreduce_amax_`` works on any torch.distributed backend (NCCL for CUDA
 tensors, gloo for CPU tensors); the ``quantize_shard_*`` helpers run the
@@ -43,6 +49,17 @@ def quantize_shard_current_scaling(x_local: torch.Tensor, fmt="e4m3", rowwise=Tr
     a = q_amax(x_local, status=status)
     allreduce_amax_(a, group)
     return q_current_scaling(x_local, fmt, rowwise, colwise, amax=a, status=status)
+
+
+def quantize_shard_nvfp4_rht_colT(x_local: torch.Tensor, sign_mask: int, rounding="rn", seed=0, offset=0, group=None,
+                                  status: Optional[torch.Tensor] = None):
+    """The random-Hadamard NVFP4 columnwise copy of this rank's row shard
+    (rows split on 16-row boundaries) with the amax of the whole transformed
+    tensor."""
+    from . import q_nvfp4_rht_amax, q_nvfp4_rht_colT
+    a = q_nvfp4_rht_amax(x_local, sign_mask, status=status)
+    allreduce_amax_(a, group)
+    return q_nvfp4_rht_colT(x_local, sign_mask, rounding, seed, offset, amax=a, status=status)
 
 
 def quantize_shard_nvfp4(x_local: torch.Tensor, blk="1x16", rounding="rn", seed=0, offset=0, rowwise=True,

@@ -207,6 +207,22 @@ def test_nvfp4_rht_colT_parity(kind, shape, bf16, rnd, mask):
     f32eq(got2.s_global.item(), sg2, "s_global, given amax")
 
 
+def test_nvfp4_rht_colT_row_shards_with_the_global_amax():
+    """Row shards on 16-row boundaries, each encoded with the maximum of the
+    shards' transform amaxes, concatenate to the unsharded copy (RTNE)."""
+    x = W.gen("outliers", (256, 512), 77, bf16=True)
+    xd = dev(x)
+    mask = 0x6B1D
+    cuts = [0, 64, 80, 256]
+    amaxes = [Q.q_nvfp4_rht_amax(xd[a:b].contiguous(), mask) for a, b in zip(cuts, cuts[1:])]
+    A = torch.stack(amaxes).max().reshape(1)
+    parts = [Q.q_nvfp4_rht_colT(xd[a:b].contiguous(), mask, "rn", amax=A) for a, b in zip(cuts, cuts[1:])]
+    whole = Q.q_nvfp4_rht_colT(xd, mask, "rn")
+    f32eq(A.item(), whole.amax.item(), "global amax")
+    same(np.concatenate([host(p.q_colT) for p in parts], axis=1), host(whole.q_colT), "q_colT")
+    same(np.concatenate([host(p.sb_colT) for p in parts], axis=1), host(whole.sb_colT), "sb_colT")
+
+
 def test_nvfp4_rht_colT_empty_and_nonfinite():
     e = Q.q_nvfp4_rht_colT(torch.empty((0, 32), dtype=torch.bfloat16, device="cuda"), 0x1)
     assert e.amax.item() == 0.0 and e.s_global.item() == 1.0
