@@ -14,7 +14,8 @@
 // Work unit: 16 bytes of output per lane (8 elements for BF16 output, 4 for
 // FP32), so that one warp store covers 512 contiguous bytes.  A CTA of 256
 // threads covers BX units x BY rows (BX = units per row rounded to a power
-// of two, at most 256); each thread keeps kDqRows rows of loads in flight.
+// of two, at most 256); each thread keeps kDqRows rows of loads in flight
+// (4: more, shorter CTAs fill the waves of mid-size tensors better than 8).
 // No index division happens per element: the 2-D grid (x: row groups, y:
 // unit blocks of a row) gives the row and the unit of every thread.
 #include "q_common.cuh"
@@ -22,7 +23,8 @@
 
 namespace qk {
 
-constexpr int kDqRows = 8;
+constexpr int kDqRows = 4;    // rows per thread in the block-scaled kernels
+constexpr int kDqUnits = 8;   // units per thread in flight in the flat current-scaling kernel
 constexpr int kDqThreads = 256;
 
 // FP32 pairs -> BF16x2 (round to nearest even), lo in the low half.
@@ -57,10 +59,10 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_cs(const uint8_t *__restrict_
     constexpr int EPU = OUT == F32 ? 4 : 8;
     const float s = *scale;
     const int64_t nu = n / EPU, stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < nu; i0 += kDqRows * stride) {
-        uint2 a[kDqRows];
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < nu; i0 += kDqUnits * stride) {
+        uint2 a[kDqUnits];
 #pragma unroll
-        for (int j = 0; j < kDqRows; j++) {
+        for (int j = 0; j < kDqUnits; j++) {
             const int64_t u = i0 + j * stride;
             if (u < nu) {
                 if (EPU == 8) a[j] = *reinterpret_cast<const uint2 *>(q + u * 8);
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_cs(const uint8_t *__restrict_
             }
         }
 #pragma unroll
-        for (int j = 0; j < kDqRows; j++) {
+        for (int j = 0; j < kDqUnits; j++) {
             const int64_t u = i0 + j * stride;
             if (u >= nu) break;
             float f[8];
@@ -174,7 +176,7 @@ cudaError_t launch_dq_cs(const uint8_t *q, const float *s, int64_t R, int64_t C,
     const int64_t n = R * C;
     if (n == 0) return cudaSuccess;
     const int epu = out == F32 ? 4 : 8;
-    int64_t blocks = (n / epu + (int64_t)kDqThreads * kDqRows - 1) / ((int64_t)kDqThreads * kDqRows);
+    int64_t blocks = (n / epu + (int64_t)kDqThreads * kDqUnits - 1) / ((int64_t)kDqThreads * kDqUnits);
     const int64_t cap = (int64_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
