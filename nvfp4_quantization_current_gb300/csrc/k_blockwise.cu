@@ -285,11 +285,9 @@ static cudaError_t bw_t(const void *x, int64_t M, int64_t K, uint8_t *q_row, flo
     alignas(64) CUtensorMap map;
     cudaError_t e = make_tile_map(&map, x, DT, M, K);
     if (e != cudaSuccess) return e;
-    static bool attr = false;
-    if (!attr) {
-        e = cudaFuncSetAttribute(k_blockwise<DT, TILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    {
+        const cudaError_t ea = engine_smem_ready<k_blockwise<DT, TILE>>();
+        if (ea != cudaSuccess) return ea;
     }
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());

@@ -296,11 +296,9 @@ static cudaError_t cs_cast_t(const void *x, int64_t M, int64_t K, const float *a
     alignas(64) CUtensorMap map;
     cudaError_t e = make_tile_map(&map, x, DT, M, K);
     if (e != cudaSuccess) return e;
-    static bool attr = false;
-    if (!attr) {
-        e = cudaFuncSetAttribute(k_cs_tiles<DT, FMT, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    {
+        const cudaError_t ea = engine_smem_ready<k_cs_tiles<DT, FMT, DS>>();
+        if (ea != cudaSuccess) return ea;
     }
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());

@@ -289,11 +289,9 @@ static cudaError_t mx_requant_t(const uint8_t *q_row, const uint8_t *e_row, int6
     alignas(64) CUtensorMap map;
     cudaError_t e = make_tile_map(&map, q_row, U8, M, K);
     if (e != cudaSuccess) return e;
-    static bool attr = false;
-    if (!attr) {
-        e = cudaFuncSetAttribute(k_mxfp8_requant<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    {
+        const cudaError_t ea = engine_smem_ready<k_mxfp8_requant<FMT>>();
+        if (ea != cudaSuccess) return ea;
     }
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + 511) / 512);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
@@ -316,11 +314,9 @@ static cudaError_t mx_t(const void *x, int64_t M, int64_t K, uint8_t *q_row, uin
     alignas(64) CUtensorMap map;
     cudaError_t e = make_tile_map(&map, x, DT, M, K);
     if (e != cudaSuccess) return e;
-    static bool attr = false;
-    if (!attr) {
-        e = cudaFuncSetAttribute(k_mxfp8<DT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    {
+        const cudaError_t ea = engine_smem_ready<k_mxfp8<DT, FMT>>();
+        if (ea != cudaSuccess) return ea;
     }
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());

@@ -393,11 +393,9 @@ static cudaError_t nv_t(const void *x, int64_t M, int64_t K, const float *amax, 
     } else {
         memset(&map, 0, sizeof map);   // never dereferenced: the kernel returns before touching tiles
     }
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_nvfp4<DT, BLK, RND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    {
+        const cudaError_t ea = engine_smem_ready<k_nvfp4<DT, BLK, RND>>();
+        if (ea != cudaSuccess) return ea;
     }
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     int grid = (int)(tiles < sm_count() ? tiles : sm_count());
@@ -567,11 +565,9 @@ static cudaError_t rht_pass(bool pdl, const CUtensorMap &map, int64_t M, int64_t
                             int32_t *status, cudaStream_t st)
 {
     constexpr int TC = 32 * In<DT>::VEC;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_nvfp4_rht<DT, RND, PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
+    {
+        const cudaError_t ea = engine_smem_ready<k_nvfp4_rht<DT, RND, PASS>>();
+        if (ea != cudaSuccess) return ea;
     }
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     int grid = (int)(tiles < sm_count() ? tiles : sm_count());

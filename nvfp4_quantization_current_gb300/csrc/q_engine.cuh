@@ -21,6 +21,7 @@
 // no copy is in flight when the CTA's shared memory goes away.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include "q_common.cuh"
 
@@ -35,6 +36,22 @@ constexpr int kTileBytes = kTileRowsE * kRowBytes;      // 64 KiB
 constexpr int kEngSmem = kStages * kTileBytes;          // dynamic shared memory of an engine CTA
 constexpr int32_t kStTimeout = 2;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
+
+// The engine's dynamic shared memory exceeds the default per-CTA limit; the
+// opt-in is a per-device attribute of each kernel, set once per device.
+template <auto Kernel>
+inline cudaError_t engine_smem_ready()
+{
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_relaxed);
+    return e;
+}
 
 QD uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
