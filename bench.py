@@ -55,21 +55,21 @@ RHT_MASK = 0xB4E1   # the 16 random signs of the Hadamard transform (any fixed d
 # capture time; reported as null when the source has changed since.
 TRAFFIC = {
     # profiles/k_blockwise_1x128T_bw3_act.md
-    "bw3.act:bw_1x128_T": {"bytes_per_launch": 420743424, "src_hash": "7ec79490289f7e79"},
+    "bw3.act:bw_1x128_T": {"bytes_per_launch": 420879616, "src_hash": "b1dcbe936762fce2"},
     # profiles/k_blockwise_128x128T_bw3_w.md
-    "bw3.w:bw_128x128_T": {"bytes_per_launch": 474636544, "src_hash": "7ec79490289f7e79"},
+    "bw3.w:bw_128x128_T": {"bytes_per_launch": 474289920, "src_hash": "b1dcbe936762fce2"},
     # profiles/k_cs_tiles_e5m2T_hy4_grad.md
-    "hy4.grad:cs_cast_T": {"bytes_per_launch": 416223232, "src_hash": "8ff7f6a63f3db5f9"},
+    "hy4.grad:cs_cast_T": {"bytes_per_launch": 415904256, "src_hash": "ad8fcb140417862d"},
     # profiles/k_mxfp8_mx2_act.md
-    "mx2.act:mxfp8": {"bytes_per_launch": 81382912, "src_hash": "98121e44197e5bd9"},
+    "mx2.act:mxfp8": {"bytes_per_launch": 80998656, "src_hash": "63030beb08e84bc3"},
     # profiles/k_mxfp8_requant_mx2_act.md
-    "mx2.act:mxfp8_requant": {"bytes_per_launch": 34900736, "src_hash": "98121e44197e5bd9"},
+    "mx2.act:mxfp8_requant": {"bytes_per_launch": 34893312, "src_hash": "63030beb08e84bc3"},
     # profiles/k_nvfp4_1x16_rn_T_nv5_act.md
-    "nv5.act:nvfp4_1x16_rn": {"bytes_per_launch": 71227392, "src_hash": "e73c5730c535a490"},
+    "nv5.act:nvfp4_1x16_rn": {"bytes_per_launch": 70683136, "src_hash": "09a39a1b57215aa4"},
     # profiles/k_nvfp4_1x16_sr_T_nv5_grad.md
-    "nv5.grad:nvfp4_1x16_sr": {"bytes_per_launch": 70978304, "src_hash": "e73c5730c535a490"},
+    "nv5.grad:nvfp4_1x16_sr": {"bytes_per_launch": 71076096, "src_hash": "09a39a1b57215aa4"},
     # profiles/k_nvfp4_rht_sr_colT_nv5_grad.md
-    "nv5.grad:nvfp4_rht_colT_sr": {"bytes_per_launch": 69387776, "src_hash": "e73c5730c535a490"},
+    "nv5.grad:nvfp4_rht_colT_sr": {"bytes_per_launch": 69515520, "src_hash": "09a39a1b57215aa4"},
 }
 
 
