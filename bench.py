@@ -14,8 +14,10 @@ preallocated outputs.
 Metric: quantize GB/s = algorithmic bytes (input bytes x reads + all output
 bytes; reads = 2 for current scaling and NVFP4, whose amax pass reads the
 tensor once more, 1 otherwise) / device time, summed over the step.  L2 is
-flushed (a 256 MiB write) before every timed call; the time of a call is
-taken with CUDA events on the launching stream around that call only.
+flushed before every timed call: a 256 MiB write, then a 256 MiB read of
+another buffer, which evicts the written lines so that their write-back is
+not charged to the call.  The time of a call is taken with CUDA events on
+the launching stream around that call only.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -487,6 +489,8 @@ def run_ours(args):
 
     calls = [c for c in build_step(dev_t, torch, Q) if args.only in c.name]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     # A bounded GPU-side delay at the start of each step (outside every timed
@@ -498,6 +502,7 @@ def run_ours(args):
         torch.cuda._sleep(head_start)
         for ci, c in enumerate(calls):
             flush.fill_(float(ci))
+            torch.sum(clean, dim=0, out=sink)   # clean lines replace the dirty ones
             evs[ci][0].record(stream)
             for pi, p in enumerate(c.pieces):
                 p[3]()
@@ -689,7 +694,7 @@ def run_ours(args):
                                    "mx2 BF16 8192x4096 MXFP8 row+col, row->col requant; bw3 BF16 16384x7168 1x128+T and 7168x18432 "
                                    "128x128+T; hy4 BF16 8192x14336 CS-E5M2+T, delayed-scaling E5M2+T (window 1024, max) and 14336x4096 CS-E4M3+T; nv5 BF16 "
                                    "8192x4096 NVFP4 1x16 RN+T, 1x16 SR+T, 4096x4096 16x16 RN+T; each with a dequant; nv5 act/grad random-Hadamard NVFP4 colT (RN / SR)",
-                       "l2": "flushed (256 MiB write) before every timed call",
+                       "l2": "flushed before every timed call (256 MiB write, then a 256 MiB read that evicts the dirty lines)",
                        "scale_rows": args.scale_rows, "parallelism": f"replicas x{world} (independent tensors)"},
             "parity": parity,
             "roofline": roofline,

@@ -117,6 +117,11 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_blocks(const uint8_t *__restr
     uint2 a[kDqRows];
     uint2 e8[kDqRows];   // MX columnwise: the unit's EPU scale codes
     float fac[kDqRows];
+    // MX columnwise: with BY <= 8 a thread's kDqRows rows (BY apart, from a
+    // multiple of kDqRows * BY) lie in one 32-row block and share the unit's
+    // scale codes, loaded and decoded once.
+    const bool one_blk = KIND == 1 && BY * kDqRows <= 32;
+    float ef[EPU];
 #pragma unroll
     for (int i = 0; i < kDqRows; i++) {
         const int64_t r = (grp * kDqRows + i) * BY + ty;
@@ -126,7 +131,7 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_blocks(const uint8_t *__restr
         else if (CB == 4) a[i] = make_uint2(*reinterpret_cast<const uint32_t *>(qp), 0u);
         else a[i] = make_uint2(*reinterpret_cast<const uint16_t *>(qp), 0u);
         if (KIND == 0) fac[i] = e8m0_value(static_cast<const uint8_t *>(sc)[r * (C / 32) + c / 32]);
-        if (KIND == 1) {
+        if (KIND == 1 && (i == 0 || !one_blk)) {
             const uint8_t *ep = static_cast<const uint8_t *>(sc) + (r / 32) * C + c;
             e8[i] = EPU == 8 ? *reinterpret_cast<const uint2 *>(ep) : make_uint2(*reinterpret_cast<const uint32_t *>(ep), 0u);
         }
@@ -140,6 +145,10 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_blocks(const uint8_t *__restr
         const int64_t r = (grp * kDqRows + i) * BY + ty;
         if (r >= R) break;
         float f[8];
+        if (KIND == 1 && (i == 0 || !one_blk)) {
+#pragma unroll
+            for (int p = 0; p < EPU; p++) ef[p] = e8m0_value(((p < 4 ? e8[i].x : e8[i].y) >> (8 * (p & 3))) & 0xFFu);
+        }
         if (FP4) {
 #pragma unroll
             for (int p = 0; p < EPU / 2; p++) {
@@ -153,9 +162,8 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_blocks(const uint8_t *__restr
                 const uint32_t wd = p < 2 ? a[i].x : a[i].y;
                 const float2 d = fp8x2_to_f32<FMT>((wd >> (16 * (p & 1))) & 0xFFFFu);
                 if (KIND == 1) {
-                    const uint32_t ew = p < 2 ? e8[i].x : e8[i].y;
-                    f[2 * p] = __fmul_rn(d.x, e8m0_value((ew >> (16 * (p & 1))) & 0xFFu));
-                    f[2 * p + 1] = __fmul_rn(d.y, e8m0_value((ew >> (16 * (p & 1) + 8)) & 0xFFu));
+                    f[2 * p] = __fmul_rn(d.x, ef[2 * p]);
+                    f[2 * p + 1] = __fmul_rn(d.y, ef[2 * p + 1]);
                 } else {
                     f[2 * p] = __fmul_rn(d.x, fac[i]);
                     f[2 * p + 1] = __fmul_rn(d.y, fac[i]);

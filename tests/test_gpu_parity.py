@@ -322,6 +322,8 @@ MX_CASES = [
     ("t3", (160, 288), True, O.E5M2),
     ("normal", (64, 416), False, O.E4M3),             # FP32 input, 128-column CTA tiles
     ("grad", (32, 32), True, O.E5M2),
+    ("normal", (96, 256), True, O.E4M3),              # dequant: a thread's 4 rows fill a 32-row block exactly
+    ("t3", (128, 128), True, O.E4M3),                 # dequant: a thread's rows span 32-row blocks
 ]
 
 
@@ -501,6 +503,39 @@ def test_nvfp4_parity(kind, shape, bf16, blk, rnd, seed, offset):
     for dt in OUTS:
         same(host(got.dequantize(Q.Q_ROW, dt)), O.dq_nvfp4(want.q_row, want.sb_row, want.s_global, blk, o_out(dt)), "dq row")
         same(host(got.dequantize(Q.Q_COL, dt)), O.dq_nvfp4(want.q_colT, want.sb_colT, want.s_global, blk, o_out(dt)), "dq colT")
+
+
+def test_nvfp4_sr_unbiased_on_the_gpu_over_1e7_draws():
+    """Stochastic rounding through the GPU path is unbiased: E[dq(q(x))] = x
+    within 1e-3 relative over ~10^7 draws, in both copies.  x tiles a 16x16
+    BF16 pattern P whose first row and first column hold the tensor's amax
+    A = 1, so every 1x16 and 16x1 block has maximum A, its scale code is 448
+    exactly (amax * alpha_g / 6 = 2688 / 6) and enc = 6: y = 6x is exact, never
+    above 6, and each entry of P is drawn 40960 times per copy."""
+    rng = np.random.default_rng(11)
+    P = rng.uniform(-1, 1, (16, 16)).astype(np.float32)
+    P = (P.view(np.uint32) & 0xFFFF0000).view(np.float32)   # BF16-exact
+    P[0, :] = 1.0
+    P[:, 0] = 1.0
+    M, K = 4096, 2560
+    x = (np.tile(P, (M // 16, K // 16)).view(np.uint32) >> 16).astype(np.uint16)   # BF16 bits
+    got = Q.q_nvfp4(dev(x), "1x16", "sr", seed=2024, offset=7, rowwise=True, colwise=True)
+    assert got.amax.item() == 1.0
+    assert np.all(host(got.sb_row) == 0x7E) and np.all(host(got.sb_colT) == 0x7E)   # E4M3 448
+    means = {
+        "row": host(got.dequantize(Q.Q_ROW)).astype(np.float64),
+        "col": host(got.dequantize(Q.Q_COL)).astype(np.float64).T,
+    }
+    y = 6.0 * np.abs(P.astype(np.float64))
+    ulp = np.where(y < 2, 0.5, np.where(y < 4, 1.0, 2.0))
+    frac = (y - np.floor(y / ulp) * ulp) / ulp
+    n = (M // 16) * (K // 16)
+    sigma = ulp / 6 * np.sqrt(frac * (1 - frac) / n)
+    for name, d in means.items():
+        mean = d.reshape(M // 16, 16, K // 16, 16).mean(axis=(0, 2))
+        agg = abs((mean - P).sum()) / np.abs(P).sum()
+        assert agg < 1e-3, (name, agg)
+        assert np.all(np.abs(mean - P) <= 5 * sigma + 1e-6), name
 
 
 def test_nvfp4_single_direction_and_given_amax():
