@@ -19,12 +19,18 @@ weight-gradient inputs all-reduces the amax of the transformed shard; shards
 that split rows on 16-row boundaries transform exactly like the slices of
 the whole tensor.
 
-``allreduce_amax_`` works on any torch.distributed backend (NCCL for CUDA
-tensors, gloo for CPU tensors); the ``quantize_shard_*`` helpers run the
-library's CUDA kernels around it.
+After the local quantize, the shards' outputs may be all-gathered into the
+whole tensor's layout (the FP8 all-gather of the TP path): rowwise codes and
+scales concatenate by rows, the transposed copies by columns
+(``all_gather_quantized``).
+
+``allreduce_amax_`` and the gathers work on any torch.distributed backend
+(NCCL for CUDA tensors, gloo for CPU tensors); the ``quantize_shard_*``
+helpers run the library's CUDA kernels around them.
 """
 from __future__ import annotations
 
+import dataclasses
 from typing import Optional
 
 import torch
@@ -71,3 +77,52 @@ def quantize_shard_nvfp4(x_local: torch.Tensor, blk="1x16", rounding="rn", seed=
     a = q_amax(x_local, status=status)
     allreduce_amax_(a, group)
     return q_nvfp4(x_local, blk, rounding, seed, offset, rowwise, colwise, amax=a, status=status)
+
+
+def all_gather_shards(t_local: torch.Tensor, dim: int = 0, group=None) -> torch.Tensor:
+    """The concatenation along ``dim``, in rank order, of every rank's
+    ``t_local``.  Shards may differ in size along ``dim`` (they are padded to
+    the largest for the collective and trimmed after); every other dimension
+    must agree.  Returns ``t_local`` itself when torch.distributed is not
+    initialized."""
+    if not (dist.is_available() and dist.is_initialized()):
+        return t_local
+    world = dist.get_world_size(group)
+    n = torch.tensor([t_local.shape[dim]], dtype=torch.int64, device=t_local.device)
+    sizes = [torch.empty_like(n) for _ in range(world)]
+    dist.all_gather(sizes, n, group=group)
+    sizes = [int(v.item()) for v in sizes]
+    x = t_local.movedim(dim, 0).contiguous()
+    if x.shape[0] < max(sizes):
+        x = torch.cat([x, x.new_zeros((max(sizes) - x.shape[0],) + tuple(x.shape[1:]))])
+    parts = [torch.empty_like(x) for _ in range(world)]
+    dist.all_gather(parts, x, group=group)
+    return torch.cat([p[:k] for p, k in zip(parts, sizes)]).movedim(0, dim).contiguous()
+
+
+# Fields of the quantized-tensor classes that follow the rows of the input
+# (rowwise codes and scales, and the MXFP8 columnwise copy, which keeps the
+# input's [M, K] layout) and those of the transposed copies ([K, M] layouts).
+_ROW_FIELDS = ("q_row", "sb_row", "e8m0_row", "s_row", "q_col", "e8m0_col")
+_COLT_FIELDS = ("q_colT", "sb_colT", "s_colT")
+
+
+def all_gather_quantized(t, group=None):
+    """The whole tensor's quantized outputs from every rank's row-shard
+    outputs ``t`` (a CurrentScalingTensor, MXFP8Tensor, BlockwiseTensor or
+    NVFP4Tensor): rowwise fields gathered by rows, transposed copies by
+    columns.  Shards must split rows on the recipe's block boundaries (32 for
+    MXFP8 columnwise, 16 for NVFP4, 128 for the blockwise columnwise and 2-D
+    tiles) and, for current scaling and NVFP4, share the all-reduced amax, so
+    that the result equals the unsharded quantization.  Tensor-wide fields
+    (amax, scale, s_global) are the same on every rank and are kept."""
+    upd = {}
+    for f in dataclasses.fields(t):
+        v = getattr(t, f.name)
+        if v is None:
+            continue
+        if f.name in _ROW_FIELDS:
+            upd[f.name] = all_gather_shards(v, 0, group)
+        elif f.name in _COLT_FIELDS:
+            upd[f.name] = all_gather_shards(v, 1, group)
+    return dataclasses.replace(t, **upd)

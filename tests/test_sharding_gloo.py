@@ -105,3 +105,87 @@ def test_allreduce_amax_single_process_is_identity():
     assert allreduce_amax_(a).item() == 3.5
     with pytest.raises(ValueError):
         allreduce_amax_(torch.tensor([1.0, 2.0]))
+
+
+def _gather_worker(rank, world, port, result_dir):
+    """Each rank quantizes its row shard (uneven: 128 and 256 rows, on 128-row
+    boundaries) with the CPU oracle, wraps the outputs in the library's
+    result classes and all-gathers them with ``all_gather_quantized``."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import oracle as O
+        import workloads as W
+        import nvfp4_quantization_current_gb300 as Q
+        from nvfp4_quantization_current_gb300.distributed import all_gather_quantized, allreduce_amax_
+
+        x = W.gen("outliers", (384, 256), 23, bf16=True)
+        cut = [0, 128, 384]
+        shard = np.ascontiguousarray(x[cut[rank]:cut[rank + 1]])
+        t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a))
+        a = torch.tensor([O.amax(shard)], dtype=torch.float32)
+        allreduce_amax_(a)
+        glob = float(a.item())
+        cs = O.current_scaling(shard, O.E4M3, rowwise=True, colwise=True, amax_in=glob)
+        mx = O.mxfp8(shard, O.E5M2)
+        bw1 = O.blockwise(shard, O.T1x128, rowwise=True, colwise=True)
+        bw2 = O.blockwise(shard, O.T128x128, rowwise=True, colwise=True)
+        nv1 = O.nvfp4(shard, O.B1x16, O.RN, rowwise=True, colwise=True, amax_in=glob)
+        nv2 = O.nvfp4(shard, O.B16x16, O.RN, rowwise=True, colwise=True, amax_in=glob)
+        got = {
+            "cs": all_gather_quantized(Q.CurrentScalingTensor(t(cs.q_row), t(cs.q_colT), a.clone(),
+                                                              torch.tensor([cs.scale]), Q.Q_E4M3)),
+            "mx": all_gather_quantized(Q.MXFP8Tensor(t(mx.q_row), t(mx.e8m0_row), t(mx.q_col), t(mx.e8m0_col),
+                                                     Q.Q_E5M2)),
+            "bw1": all_gather_quantized(Q.BlockwiseTensor(t(bw1.q_row), t(bw1.s_row), t(bw1.q_colT), t(bw1.s_colT),
+                                                          Q.Q_T1x128)),
+            "bw2": all_gather_quantized(Q.BlockwiseTensor(t(bw2.q_row), t(bw2.s_row), t(bw2.q_colT), t(bw2.s_colT),
+                                                          Q.Q_T128x128)),
+            "nv1": all_gather_quantized(Q.NVFP4Tensor(t(nv1.q_row), t(nv1.sb_row), t(nv1.q_colT), t(nv1.sb_colT),
+                                                      a.clone(), torch.tensor([nv1.s_global]), Q.Q_B1x16)),
+            "nv2": all_gather_quantized(Q.NVFP4Tensor(t(nv2.q_row), t(nv2.sb_row), t(nv2.q_colT), t(nv2.sb_colT),
+                                                      a.clone(), torch.tensor([nv2.s_global]), Q.Q_B16x16)),
+        }
+        if rank == 0:
+            flat = {}
+            for k, v in got.items():
+                for f in ("q_row", "q_colT", "q_col", "e8m0_row", "e8m0_col", "s_row", "s_colT", "sb_row", "sb_colT"):
+                    if getattr(v, f, None) is not None:
+                        flat[f"{k}.{f}"] = getattr(v, f).numpy()
+            np.savez(os.path.join(result_dir, "gathered.npz"), **flat)
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_all_gather_of_quantized_shards_matches_unsharded(tmp_path):
+    world = 2
+    mp.start_processes(_gather_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, start_method="spawn")
+    import oracle as O
+    import workloads as W
+
+    x = W.gen("outliers", (384, 256), 23, bf16=True)
+    g = np.load(os.path.join(tmp_path, "gathered.npz"))
+    want = {
+        "cs": O.current_scaling(x, O.E4M3, rowwise=True, colwise=True),
+        "mx": O.mxfp8(x, O.E5M2),
+        "bw1": O.blockwise(x, O.T1x128, rowwise=True, colwise=True),
+        "bw2": O.blockwise(x, O.T128x128, rowwise=True, colwise=True),
+        "nv1": O.nvfp4(x, O.B1x16, O.RN, rowwise=True, colwise=True),
+        "nv2": O.nvfp4(x, O.B16x16, O.RN, rowwise=True, colwise=True),
+    }
+    n = 0
+    for key in g.files:
+        rec, field = key.split(".")
+        w = getattr(want[rec], field)
+        assert g[key].shape == w.shape, key
+        assert np.array_equal(g[key].view(np.uint8), np.ascontiguousarray(w).view(np.uint8)), key
+        n += 1
+    assert n == 2 + 4 + 4 + 4 + 4 + 4
+
+
+def test_all_gather_single_process_is_identity():
+    from nvfp4_quantization_current_gb300.distributed import all_gather_shards
+    a = torch.arange(6).reshape(2, 3)
+    assert all_gather_shards(a, 1) is a
