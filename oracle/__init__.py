@@ -90,6 +90,7 @@ def _L():
             "or_ds_cast": (None, [P, I, I64, I64, I, F, P, P, P]),
             "or_ds_scale_update": (None, [P, I64, I64, I, I, P, P]),
             "or_blockwise": (None, [P, I, I64, I64, I, P, P, P, P]),
+            "or_blockwise_mx": (None, [P, I, I64, I64, I, P, P, P, P]),
             "or_dq_blockwise": (None, [P, P, I64, I64, I, I, P]),
             "or_nvfp4_global": (None, [F, P, P]),
             "or_nvfp4": (None, [P, I, I64, I64, I, I, U64, U64, P, P, P, P, P, P, P]),
@@ -334,6 +335,27 @@ def blockwise(x, tile=T1x128, rowwise=True, colwise=False):
         s_colT = np.empty((K // 128, M // 128), np.float32) if colwise else None
     _L().or_blockwise(_p(x), dt, M, K, tile, _p(q_row), _p(s_row), _p(q_colT), _p(s_colT))
     return BW(q_row, s_row, q_colT, s_colT)
+
+
+@dataclass
+class BWMX:
+    q_row: np.ndarray | None       # [M, K] E4M3 codes
+    e8m0_row: np.ndarray | None    # [M, K/32], the tile's code repeated
+    q_colT: np.ndarray | None      # [K, M]
+    e8m0_colT: np.ndarray | None   # [K, M/32]
+
+
+def blockwise_mx(x, tile=T1x128, rowwise=True, colwise=False):
+    """Blockwise tiles with power-of-two scales stored as MXFP8 (R-BWMX):
+    both copies dequantize with dq_mxfp8(..., direction=ROW)."""
+    x, dt = _x(x)
+    M, K = x.shape
+    q_row = np.empty((M, K), np.uint8) if rowwise else None
+    e_row = np.empty((M, K // 32), np.uint8) if rowwise else None
+    q_colT = np.empty((K, M), np.uint8) if colwise else None
+    e_colT = np.empty((K, M // 32), np.uint8) if colwise else None
+    _L().or_blockwise_mx(_p(x), dt, M, K, tile, _p(q_row), _p(e_row), _p(q_colT), _p(e_colT))
+    return BWMX(q_row, e_row, q_colT, e_colT)
 
 
 def dq_blockwise(q, s, tile=T1x128, out=F32):

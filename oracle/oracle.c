@@ -50,6 +50,9 @@
  *   R-RHT    the random Hadamard transform of the wgrad inputs: 16-point,
  *            along M on the 16x1 blocks, signs from a 16-bit mask, FP32
  *            butterfly with strides 1, 2, 4, 8, then 1/4 (see or_rht16).
+ *   R-BWMX   blockwise tiles held as MXFP8: the shared E8M0 code is the
+ *            blockwise scale b / 448 rounded up to a power of two; elements
+ *            as in MXFP8 (see or_blockwise_mx).
  *
  * Parity status: every function below is pinned by the tests in tests/
  * (worked examples, brute-force nearest-value search, library casts,
@@ -633,6 +636,80 @@ void or_blockwise(const void *x, int dtype, int64_t M, int64_t K, int tile,
                 for (int64_t m = mb * 128; m < mb * 128 + 128; m++)
                     for (int64_t k = kb * 128; k < kb * 128 + 128; k++) {
                         uint8_t c = or_enc_e4m3(alpha * load_x(x, dtype, m * K + k));
+                        if (q_row) q_row[m * K + k] = c;
+                        if (q_colT) q_colT[k * M + m] = c;
+                    }
+            }
+    }
+}
+
+/*
+ * Blockwise scaling held as MXFP8 ([MP] "Blockwise scaling": on Blackwell the
+ * blockwise recipe is emulated with MXFP8, a 1x128 tile being 4 MXFP8 blocks
+ * that share one scale factor and a 128x128 tile 128 x 4 of them, so that
+ * MXFP8 GEMMs consume it).  An MXFP8 scale is a power of two (E8M0); reading
+ * R-BWMX: the tile's scale is its blockwise scale b / 448 rounded up to a
+ * power of two, code = 127 + n with n the smallest integer such that
+ * b <= 448 * 2^n, clamped to [0, 254]; b = 0 gives 127 and a non-finite b
+ * the MXFP8 code of exponent field 255.  The tile maximum therefore never
+ * saturates.  Elements as in MXFP8: q = Q(x * 2^(127 - code)).  Scales are
+ * stored in the MXFP8 layout, one code per 32 elements along the
+ * quantization direction (the tile's code repeated):
+ *   tile 0: q_row [M, K], e_row [M, K/32]; q_colT [K, M], e_colT [K, M/32]
+ *     (128x1 blocks along M of each column, held transposed);
+ *   tile 1: q_row [M, K], e_row [M, K/32] (a tile's 128 rows share its
+ *     code); q_colT [K, M] the same codes transposed, e_colT [K, M/32].
+ */
+static uint8_t bwmx_scale_code(float b)
+{
+    if (b == 0.0f) return 127;
+    if (!isfinite(b)) return mx_scale_code(b, OR_E4M3);
+    int n = floor_log2((double)b) - 8;
+    while ((double)b > ldexp(448.0, n)) n++;   /* exact comparisons in double */
+    int code = n + 127;
+    return (uint8_t)(code < 0 ? 0 : (code > 254 ? 254 : code));
+}
+
+void or_blockwise_mx(const void *x, int dtype, int64_t M, int64_t K, int tile,
+                     uint8_t *q_row, uint8_t *e_row, uint8_t *q_colT, uint8_t *e_colT)
+{
+    if (tile == 0) {
+        if (q_row)
+            for (int64_t m = 0; m < M; m++)
+                for (int64_t kb = 0; kb < K / 128; kb++) {
+                    uint8_t code = bwmx_scale_code(tile_amax(x, dtype, K, m, kb * 128, 1, 128));
+                    float inv = mx_inv_scale(code);
+                    for (int j = 0; j < 4; j++) e_row[m * (K / 32) + kb * 4 + j] = code;
+                    for (int j = 0; j < 128; j++) {
+                        int64_t i = m * K + kb * 128 + j;
+                        q_row[i] = or_enc_e4m3(load_x(x, dtype, i) * inv);
+                    }
+                }
+        if (q_colT)
+            for (int64_t k = 0; k < K; k++)
+                for (int64_t mb = 0; mb < M / 128; mb++) {
+                    uint8_t code = bwmx_scale_code(tile_amax(x, dtype, K, mb * 128, k, 128, 1));
+                    float inv = mx_inv_scale(code);
+                    for (int j = 0; j < 4; j++) e_colT[k * (M / 32) + mb * 4 + j] = code;
+                    for (int j = 0; j < 128; j++) {
+                        int64_t m = mb * 128 + j;
+                        q_colT[k * M + m] = or_enc_e4m3(load_x(x, dtype, m * K + k) * inv);
+                    }
+                }
+    } else {
+        for (int64_t mb = 0; mb < M / 128; mb++)
+            for (int64_t kb = 0; kb < K / 128; kb++) {
+                uint8_t code = bwmx_scale_code(tile_amax(x, dtype, K, mb * 128, kb * 128, 128, 128));
+                float inv = mx_inv_scale(code);
+                for (int64_t m = mb * 128; m < mb * 128 + 128; m++)
+                    for (int j = 0; j < 4; j++)
+                        if (e_row) e_row[m * (K / 32) + kb * 4 + j] = code;
+                for (int64_t k = kb * 128; k < kb * 128 + 128; k++)
+                    for (int j = 0; j < 4; j++)
+                        if (e_colT) e_colT[k * (M / 32) + mb * 4 + j] = code;
+                for (int64_t m = mb * 128; m < mb * 128 + 128; m++)
+                    for (int64_t k = kb * 128; k < kb * 128 + 128; k++) {
+                        uint8_t c = or_enc_e4m3(load_x(x, dtype, m * K + k) * inv);
                         if (q_row) q_row[m * K + k] = c;
                         if (q_colT) q_colT[k * M + m] = c;
                     }
