@@ -6,7 +6,8 @@ One step = one pass of every recipe over its full-size tensors (all five
 workloads of ``workloads.WORKLOADS``): current-scaling amax + cast (+ the
 transposed copy), delayed scaling (one read + the window update), MXFP8
 row + col and the row->col re-quantize, blockwise 1x128 (+ transposed) and
-128x128 (+ transposed), NVFP4 1x16 RTNE, 1x16 stochastic rounding and 16x16,
+128x128 (+ transposed), both again with power-of-two tile scales held as
+MXFP8, NVFP4 1x16 RTNE, 1x16 stochastic rounding and 16x16,
 the dequantizer of each, and the random-Hadamard NVFP4 columnwise copies of
 the NVFP4 activation and gradient (weight-gradient GEMM inputs).  Every call goes through the C ABI with
 preallocated outputs.
@@ -197,6 +198,14 @@ def build_step(dev_tensors, torch, Q):
                           [("dq_blockwise", "k_dequant.cu", nbytes(qb, sb, y), r)], [qb, sb], [y], r))
         calls[-1].prime = prime
 
+    def bwmx(tag, x, tile):
+        out = Q.alloc_blockwise_mx(x.shape[0], x.shape[1], x.device, tile, True, True)
+        b = nbytes(x, out.q_row, out.e8m0_row, out.q_colT, out.e8m0_colT)
+        run = lambda: Q.q_blockwise_mx(x, tile, True, True, out=out)
+        calls.append(Call(f"{tag} blockwise_mx_{tile} row+colT", "blockwise_mx",
+                          [("bwmx_" + tile + "_T", "k_blockwise.cu", b, run)], [x],
+                          [out.q_row, out.e8m0_row, out.q_colT, out.e8m0_colT], run))
+
     def nv(tag, x, blk, rnd, seed):
         out = Q.alloc_nvfp4(x.shape[0], x.shape[1], x.device, blk, True, True)
         amax = out.amax
@@ -245,6 +254,8 @@ def build_step(dev_tensors, torch, Q):
     if "bw3" in d:
         bw("bw3.act", d["bw3"]["act"], "1x128", True)
         bw("bw3.w", d["bw3"]["w"], "128x128", True)
+        bwmx("bw3.act", d["bw3"]["act"], "1x128")
+        bwmx("bw3.w", d["bw3"]["w"], "128x128")
     if "hy4" in d:
         cs("hy4.grad", d["hy4"]["grad"], "e5m2", True)
         ds("hy4.grad", d["hy4"]["grad"], "e5m2")
@@ -287,6 +298,7 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
     for wl, tn, kind in [("cs1", "x", "cs_e4m3"), ("hy4", "grad", "cs_e5m2"), ("hy4", "grad", "ds_e5m2"),
                          ("hy4", "w", "cs_e4m3"),
                          ("mx2", "act", "mx"), ("bw3", "act", "bw1"), ("bw3", "w", "bw128"),
+                         ("bw3", "act", "bwmx1"), ("bw3", "w", "bwmx128"),
                          ("nv5", "act", "nv_rn"), ("nv5", "grad", "nv_sr"), ("nv5", "w", "nv16"),
                          ("nv5", "act", "rht_rn"), ("nv5", "grad", "rht_sr")]:
         xh, xd = host_tensors[wl][tn], dev_tensors[wl][tn]
@@ -355,6 +367,14 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
             eq(host(g.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} q_row band")
             eq(host(g.s_row[r0 // 128:(r0 + rows) // 128]), w.s_row, f"{wl}.{tn} s band")
             eq(host(g.q_colT[:, r0:r0 + rows]), w.q_colT, f"{wl}.{tn} q_colT band")
+        elif kind in ("bwmx1", "bwmx128"):
+            tile = "1x128" if kind == "bwmx1" else "128x128"
+            g = Q.q_blockwise_mx(xd, tile, True, True)
+            w = O.blockwise_mx(xs, O.T1x128 if kind == "bwmx1" else O.T128x128, True, True)
+            eq(host(g.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} {tile} mx q_row band")
+            eq(host(g.e8m0_row[r0:r0 + rows]), w.e8m0_row, f"{wl}.{tn} {tile} mx e8m0_row band")
+            eq(host(g.q_colT[:, r0:r0 + rows]), w.q_colT, f"{wl}.{tn} {tile} mx q_colT band")
+            eq(host(g.e8m0_colT[:, r0 // 32:(r0 + rows) // 32]), w.e8m0_colT, f"{wl}.{tn} {tile} mx e8m0_colT band")
         else:
             blk = O.B16x16 if kind == "nv16" else O.B1x16
             rnd = O.SR if kind == "nv_sr" else O.RN
@@ -770,6 +790,11 @@ def oracle_sample_work(host_t, frac):
         r = O.blockwise(s, tile, True, False)
         work.append((lambda: O.dq_blockwise(r.q_row, r.s_row, tile, O.BF16), M * K * 3 + sc))
 
+    def bwmx(a, tile):
+        s = np.ascontiguousarray(a[:rows(a)])
+        M, K = s.shape
+        work.append((lambda: O.blockwise_mx(s, tile, True, True), s.nbytes + 2 * M * K + 2 * (M * K // 32)))
+
     def nv(a, blk, rnd, seed):
         s = np.ascontiguousarray(a[:rows(a)])
         M, K = s.shape
@@ -782,6 +807,8 @@ def oracle_sample_work(host_t, frac):
     mx(host_t["mx2"]["act"])
     bw(host_t["bw3"]["act"], O.T1x128)
     bw(host_t["bw3"]["w"], O.T128x128)
+    bwmx(host_t["bw3"]["act"], O.T1x128)
+    bwmx(host_t["bw3"]["w"], O.T128x128)
     cs(host_t["hy4"]["grad"], O.E5M2)
     ds(host_t["hy4"]["grad"], O.E5M2)
     cs(host_t["hy4"]["w"], O.E4M3)

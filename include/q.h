@@ -196,6 +196,29 @@ q_status q_blockwise(const void *x, q_dtype in, int64_t M, int64_t K, q_tile til
                      int32_t *status, q_stream_t stream);
 
 /*
+ * R5: blockwise tiles held as MXFP8 ([MP] "Blockwise scaling": on Blackwell
+ * the blockwise recipe is emulated with MXFP8, a 1x128 tile being 4 MXFP8
+ * blocks that share one scale factor, a 128x128 tile 128 x 4 of them).  E4M3.
+ * The tile scale is b/448 rounded up to a power of two (the tile maximum
+ * never saturates), code = 127 + n for the smallest n with b <= 448 * 2^n,
+ * clamped to [0, 254] (b = 0 -> 127; inf / NaN -> 247); it is stored once
+ * per 32 elements along the quantization direction.  Elements
+ * q = Q(x * 2^(127 - code)), as in MXFP8.
+ *   tile Q_T1x128:   q_row [M, K], e8m0_row [M, K/32]; q_colT [K, M],
+ *                    e8m0_colT [K, M/32] (128x1 blocks along M).
+ *   tile Q_T128x128: q_row [M, K], e8m0_row [M, K/32] (a tile's 128 rows
+ *                    share its code); q_colT [K, M] = the same codes
+ *                    transposed, e8m0_colT [K, M/32].
+ * Both copies dequantize with dq_mxfp8(..., Q_ROW, ...), the transposed copy
+ * as the [K, M] matrix it is.  Shapes as q_blockwise; code buffers 16-byte
+ * aligned, scale buffers 4-byte aligned.  Either direction may be NULL, not
+ * both.  Non-finite tile maxima set Q_ST_NONFINITE in *status.
+ */
+q_status q_blockwise_mx(const void *x, q_dtype in, int64_t M, int64_t K, q_tile tile,
+                        uint8_t *q_row, uint8_t *e8m0_row, uint8_t *q_colT, uint8_t *e8m0_colT,
+                        int32_t *status, q_stream_t stream);
+
+/*
  * a8-a11: NVFP4 ([MP] "NVFP4" and recipe 6; [LP] 2.4 items 1, 4, 5):
  * E2M1 codes packed two per byte (element 2j in bits 3-0, 2j+1 in bits 7-4),
  * one E4M3 scale per block, one FP32 tensor scale.

@@ -69,6 +69,7 @@ SIGNATURES = {
     "q_selftest_wait_timeout": (_I, [_P, _U64, _P]),
     "q_mxfp8_requant_col": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
     "q_blockwise": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
+    "q_blockwise_mx": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "q_nvfp4": (_I, [_P, _I, _I64, _I64, _I, _I, _U64, _U64, _P, _P, _P, _P, _P, _I, _P, _P, _P]),
     "q_nvfp4_rht_amax": (_I, [_P, _I, _I64, _I64, _U32, _P, _P, _P]),
     "q_nvfp4_rht_colT": (_I, [_P, _I, _I64, _I64, _U32, _I, _U64, _U64, _P, _P, _P, _I, _P, _P, _P]),
@@ -377,6 +378,41 @@ def dq_blockwise(q, s, tile="1x128", dtype=torch.float32, out=None):
     return y
 
 
+@dataclass
+class BlockwiseMXTensor:
+    """Blockwise tiles held as MXFP8: E4M3 codes with the tile's power-of-two
+    scale as an E8M0 code once per 32 elements (MXFP8 row layout for both
+    copies, so an MXFP8 GEMM consumes them)."""
+    q_row: Optional[torch.Tensor]       # [M, K] E4M3 codes
+    e8m0_row: Optional[torch.Tensor]    # [M, K/32], the tile's code repeated
+    q_colT: Optional[torch.Tensor]      # [K, M] (128x1 blocks along M, or the 2D codes transposed)
+    e8m0_colT: Optional[torch.Tensor]   # [K, M/32]
+    tile: int
+
+    def dequantize(self, direction=Q_ROW, dtype=torch.float32):
+        if direction == Q_ROW:
+            return dq_mxfp8(self.q_row, self.e8m0_row, Q_E4M3, Q_ROW, dtype)
+        return dq_mxfp8(self.q_colT, self.e8m0_colT, Q_E4M3, Q_ROW, dtype)
+
+
+def alloc_blockwise_mx(M, K, device, tile="1x128", rowwise=True, colwise=False) -> BlockwiseMXTensor:
+    return BlockwiseMXTensor(_u8((M, K), device) if rowwise else None, _u8((M, K // 32), device) if rowwise else None,
+                             _u8((K, M), device) if colwise else None, _u8((K, M // 32), device) if colwise else None,
+                             _tile(tile))
+
+
+def q_blockwise_mx(x: torch.Tensor, tile="1x128", rowwise=True, colwise=False,
+                   out: Optional[BlockwiseMXTensor] = None, status: Optional[torch.Tensor] = None):
+    """Blockwise 1x128 / 128x128 quantization with power-of-two tile scales
+    stored as MXFP8 E8M0 codes (the blockwise recipe emulated on MXFP8)."""
+    dt = _in(x)
+    M, K = x.shape
+    out = alloc_blockwise_mx(M, K, x.device, tile, rowwise, colwise) if out is None else out
+    _call("q_blockwise_mx", _ptr(x), dt, M, K, out.tile, _ptr(out.q_row), _ptr(out.e8m0_row), _ptr(out.q_colT),
+          _ptr(out.e8m0_colT), _ptr(status), _stream(x.device))
+    return out
+
+
 # ---------------------------------------------------------------------------
 # a8-a11: NVFP4
 # ---------------------------------------------------------------------------
@@ -482,5 +518,5 @@ def dq_nvfp4(q, sb, s_global, blk="1x16", dtype=torch.float32, out=None):
 
 
 __all__ = [n for n in dir() if n.startswith(("q_", "dq_", "alloc_", "Q_"))] + [
-    "CurrentScalingTensor", "DelayedScaling", "MXFP8Tensor", "BlockwiseTensor", "NVFP4Tensor", "QuantError", "lib",
-    "SIGNATURES"]
+    "CurrentScalingTensor", "DelayedScaling", "MXFP8Tensor", "BlockwiseTensor", "BlockwiseMXTensor", "NVFP4Tensor",
+    "QuantError", "lib", "SIGNATURES"]

@@ -20,6 +20,12 @@
 //  128x128        - the tile maximum comes from warp shuffles and one
 //                   shared-memory reduction across the 16 warps; the
 //                   transposed copy is the same codes byte-transposed.
+//
+// With P2 the tiles are held as MXFP8 ("Mixed-precision training ...",
+// "Blockwise scaling": on Blackwell the recipe is emulated with MXFP8, a 1x128
+// tile being 4 MXFP8 blocks that share one scale): the tile scale is b / 448
+// rounded up to a power of two, stored as its E8M0 code once per 32 elements
+// (e_row [M, K/32], e_colT [K, M/32]), and alpha = 2^(127 - code).
 #include "q_engine.cuh"
 #include "q_internal.h"
 
@@ -50,19 +56,51 @@ template <int DT> QD void bw_scales(uint32_t b, const BwScaleTab &tab, float &al
     }
 }
 
-template <int DT, int TILE>
+// E8M0 code of the power-of-two tile scale: the smallest 2^n with
+// b <= 448 * 2^n, code = 127 + n clamped to [0, 254].  For b = (1 + f)
+// 2^(E - 127) and 448 = 1.75 * 2^8 that is E - 8, plus one when the mantissa
+// field exceeds that of 1.75 (0x600000); b = 0 -> 127 (scale 1); inf / NaN
+// (E = 255) -> 247, the MXFP8 code of that exponent field.
+QD uint32_t bw_p2_code(uint32_t b)
+{
+    if (b == 0u) return 127u;
+    const int E = (int)(b >> 23);
+    if (E == 255) return 247u;
+    const int c = E - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return (uint32_t)(c < 0 ? 0 : (c > 254 ? 254 : c));
+}
+
+// alpha (and the FP32 s, or the E8M0 code with P2) of a tile maximum b.
+template <int DT, bool P2> QD void bw_tile_scale(uint32_t b, const BwScaleTab &tab, float &alpha, float &s, uint32_t &code)
+{
+    if constexpr (P2) {
+        code = bw_p2_code(b);
+        alpha = mx_inv_scale(code);
+        s = 0.0f;
+    } else {
+        bw_scales<DT>(b, tab, alpha, s);
+        code = 0u;
+    }
+}
+
+template <int DT, int TILE, bool P2>
 __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
-                                                              uint8_t *__restrict__ q_row, float *__restrict__ s_row,
-                                                              uint8_t *__restrict__ q_colT, float *__restrict__ s_colT,
+                                                              uint8_t *__restrict__ q_row, void *__restrict__ sc_row,
+                                                              uint8_t *__restrict__ q_colT, void *__restrict__ sc_colT,
                                                               int32_t *status)
 {
+    // scales: FP32 [M, K/128] / [K, M/128] (2D: [M/128, K/128] / [K/128, M/128]),
+    // or with P2 E8M0 codes [M, K/32] / [K, M/32], one 4-byte word per 128 elements
+    float *const s_row = static_cast<float *>(sc_row), *const s_colT = static_cast<float *>(sc_colT);
+    uint8_t *const e_row = static_cast<uint8_t *>(sc_row), *const e_colT = static_cast<uint8_t *>(sc_colT);
+    constexpr uint32_t kRep4 = 0x01010101u;
     constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, LPB = 128 / VEC;
     constexpr int NT = TC / 128;   // 128-column blocks per tile
     __shared__ uint4 part[kEngWarps][32];      // 1x128: per-warp column maxima (packed like the input)
     __shared__ __align__(16) float calpha[TC];   // 1x128: column alphas of the tile
     __shared__ uint32_t tred[kEngWarps][NT];   // 128x128: per-warp tile maxima
     __shared__ BwScaleTab tab;
-    if (DT == BF16 && threadIdx.x < 128) {
+    if (DT == BF16 && !P2 && threadIdx.x < 128) {
         const float a = __fdiv_rn(448.0f, 1.0f + (float)threadIdx.x * (1.0f / 128.0f));
         tab.a[threadIdx.x] = a;
         tab.s[threadIdx.x] = __fdiv_rn(1.0f, a);
@@ -79,6 +117,24 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
 #pragma unroll
         for (int j = 0; j < 8; j++) v[j] = lds16(st + (8 * warp + j) * kRowBytes + lane * 16);
         uint32_t code[8][CW];
+        uint32_t cc2 = 0;   // 128x128 with P2: this lane's block code
+        // 128x128 with P2: the code once per 32 elements, one 4-byte word per
+        // thread: threads 0 .. 128*NT-1 take a row and block of e_row, threads
+        // 256 .. 256+TC-1 a column of e_colT.  Lane h*LPB of every warp holds
+        // block h's code (the branches are warp-uniform).  Issued after the
+        // tile's codes are out.
+        auto put_p2_codes = [&]() {
+            if (t < 128 * NT) {
+                const int r = t / NT, h = t % NT;
+                const uint32_t ch = __shfl_sync(0xFFFFFFFFu, cc2, h * LPB);
+                if (e_row != nullptr && kb + 128 * h < K)
+                    stg4(e_row + (mb + r) * (K / 32) + (kb / 128 + h) * 4, ch * kRep4);
+            } else if (t >= 256 && t < 256 + TC) {
+                const int c = t - 256;
+                const uint32_t ch = __shfl_sync(0xFFFFFFFFu, cc2, (c / 128) * LPB);
+                if (e_colT != nullptr && kb + c < K) stg4(e_colT + (kb + c) * (M / 32) + tm * 4, ch * kRep4);
+            }
+        };
 
         if constexpr (TILE == 0) {
             if (q_colT != nullptr) {   // column maxima of this warp's 8 rows
@@ -122,9 +178,11 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
                 const int r = (L >> 1) & 7;
                 const uint32_t bm = (b1 ? kw : (kw << 16)) & 0x7FFF0000u;         // FP32 bits of row r's block max
                 float alpha_r, s_r;
-                bw_scales<DT>(bm, tab, alpha_r, s_r);
+                uint32_t c_r;
+                bw_tile_scale<DT, P2>(bm, tab, alpha_r, s_r, c_r);
                 if ((L & 1) == 0 && r < nrows) {
-                    s_row[(m0 + r) * (K / 128) + k / 128] = s_r;
+                    if (P2) stg4(e_row + (m0 + r) * (K / 32) + (k / 128) * 4, c_r * kRep4);
+                    else s_row[(m0 + r) * (K / 128) + k / 128] = s_r;
                     nf |= nonfinite(bm);
                 }
                 uint8_t *qr = q_row + m0 * K + k;
@@ -142,7 +200,6 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
                 // rows of this thread that exist (all 8 except in the last tile row)
                 const int nrows = !kok ? 0 : (m0 + 8 <= M ? 8 : (m0 < M ? (int)(M - m0) : 0));
                 uint8_t *qr = q_row + m0 * K + k;
-                float *sr = s_row + m0 * (K / 128) + k / 128;
                 const bool sl = lane % LPB == 0;
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
@@ -151,14 +208,16 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
 #pragma unroll
                     for (int h = 0; h < 2; h++) {
                         float alpha, sc;
-                        bw_scales<DT>(bb[h], tab, alpha, sc);
+                        uint32_t cc;
+                        bw_tile_scale<DT, P2>(bb[h], tab, alpha, sc, cc);
                         uint32_t o[CW];
                         chunk_fp8<DT, E4M3>(v[j + h], alpha, o);
                         if (j + h < nrows) {
                             uint8_t *dst = qr + (j + h) * K;
                             if (CW == 2) stg8(dst, o[0], o[CW - 1]);
                             else stg4(dst, o[0]);
-                            if (sl) sr[(j + h) * (K / 128)] = sc;
+                            if (sl && P2) stg4(e_row + (m0 + j + h) * (K / 32) + (k / 128) * 4, cc * kRep4);
+                            if (sl && !P2) s_row[(m0 + j + h) * (K / 128) + k / 128] = sc;
                             nf |= nonfinite(bb[h]);
                         }
                     }
@@ -184,10 +243,12 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
                     const int col = 2 * wp + sub;             // low half: even column
                     const uint32_t b = (sub ? b2 : (b2 << 16)) & 0x7FFF0000u;
                     float alpha, sc;
-                    bw_scales<DT>(b, tab, alpha, sc);
+                    uint32_t cc;
+                    bw_tile_scale<DT, P2>(b, tab, alpha, sc, cc);
                     calpha[col] = alpha;
                     if (kb + col < K) {
-                        s_colT[(kb + col) * (M / 128) + tm] = sc;
+                        if (P2) stg4(e_colT + (kb + col) * (M / 32) + tm * 4, cc * kRep4);
+                        else s_colT[(kb + col) * (M / 128) + tm] = sc;
                         flag_nonfinite(status, b);
                     }
                 }
@@ -202,10 +263,12 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
                     if (TPC == 2) b = max(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
                     if (half == 0) {
                         float alpha, sc;
-                        bw_scales<DT>(b, tab, alpha, sc);
+                        uint32_t cc;
+                        bw_tile_scale<DT, P2>(b, tab, alpha, sc, cc);
                         calpha[col] = alpha;
                         if (kb + col < K) {
-                            s_colT[(kb + col) * (M / 128) + tm] = sc;
+                            if (P2) stg4(e_colT + (kb + col) * (M / 32) + tm * 4, cc * kRep4);
+                            else s_colT[(kb + col) * (M / 128) + tm] = sc;
                             flag_nonfinite(status, b);
                         }
                     }
@@ -252,12 +315,14 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
                 for (int q = 0; q < kEngWarps; q++) bt = max(bt, tred[q][lane / LPB]);
             }
             float alpha, sc;
-            bw_scales<DT>(bt, tab, alpha, sc);
-            if (warp == 0 && lane % LPB == 0 && kok) {
+            uint32_t cc;
+            bw_tile_scale<DT, P2>(bt, tab, alpha, sc, cc);
+            if (!P2 && warp == 0 && lane % LPB == 0 && kok) {
                 if (s_row != nullptr) s_row[tm * (K / 128) + k / 128] = sc;
                 if (s_colT != nullptr) s_colT[(k / 128) * (M / 128) + tm] = sc;
-                flag_nonfinite(status, bt);
             }
+            cc2 = cc;
+            if (warp == 0 && lane % LPB == 0 && kok) flag_nonfinite(status, bt);
 #pragma unroll
             for (int j = 0; j < 8; j++) chunk_fp8<DT, E4M3>(v[j], alpha, code[j]);
             if (q_row != nullptr && kok) {
@@ -268,30 +333,34 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_blockwise(const __grid_const
                     else stg4(dst, code[j][0]);
                 }
             }
-            if (q_colT == nullptr) return;
+            if (q_colT == nullptr) {
+                if constexpr (P2) put_p2_codes();
+                return;
+            }
         }
         // ---- transposed codes: parked in the consumed stage, then full 128-byte rows
         park_fp8T<VEC>(st, code, warp, lane);
         __syncthreads();
         copy_out_fp8T<VEC>(st, q_colT, M, K, mb, kb);
+        if constexpr (TILE == 1 && P2) put_p2_codes();
     });
 }
 
-template <int DT, int TILE>
-static cudaError_t bw_t(const void *x, int64_t M, int64_t K, uint8_t *q_row, float *s_row, uint8_t *q_colT,
-                        float *s_colT, int32_t *status, cudaStream_t st)
+template <int DT, int TILE, bool P2>
+static cudaError_t bw_t(const void *x, int64_t M, int64_t K, uint8_t *q_row, void *s_row, uint8_t *q_colT,
+                        void *s_colT, int32_t *status, cudaStream_t st)
 {
     constexpr int TC = 32 * In<DT>::VEC;
     alignas(64) CUtensorMap map;
     cudaError_t e = make_tile_map(&map, x, DT, M, K);
     if (e != cudaSuccess) return e;
     {
-        const cudaError_t ea = engine_smem_ready<k_blockwise<DT, TILE>>();
+        const cudaError_t ea = engine_smem_ready<k_blockwise<DT, TILE, P2>>();
         if (ea != cudaSuccess) return ea;
     }
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-    k_blockwise<DT, TILE><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, q_row, s_row, q_colT, s_colT, status);
+    k_blockwise<DT, TILE, P2><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, q_row, s_row, q_colT, s_colT, status);
     return cudaGetLastError();
 }
 
@@ -299,10 +368,20 @@ cudaError_t launch_blockwise(const void *x, int dt, int64_t M, int64_t K, int ti
                              uint8_t *q_colT, float *s_colT, int32_t *status, cudaStream_t st)
 {
     if (dt == BF16)
-        return tile == 0 ? bw_t<BF16, 0>(x, M, K, q_row, s_row, q_colT, s_colT, status, st)
-                         : bw_t<BF16, 1>(x, M, K, q_row, s_row, q_colT, s_colT, status, st);
-    return tile == 0 ? bw_t<F32, 0>(x, M, K, q_row, s_row, q_colT, s_colT, status, st)
-                     : bw_t<F32, 1>(x, M, K, q_row, s_row, q_colT, s_colT, status, st);
+        return tile == 0 ? bw_t<BF16, 0, false>(x, M, K, q_row, s_row, q_colT, s_colT, status, st)
+                         : bw_t<BF16, 1, false>(x, M, K, q_row, s_row, q_colT, s_colT, status, st);
+    return tile == 0 ? bw_t<F32, 0, false>(x, M, K, q_row, s_row, q_colT, s_colT, status, st)
+                     : bw_t<F32, 1, false>(x, M, K, q_row, s_row, q_colT, s_colT, status, st);
+}
+
+cudaError_t launch_blockwise_mx(const void *x, int dt, int64_t M, int64_t K, int tile, uint8_t *q_row,
+                                uint8_t *e_row, uint8_t *q_colT, uint8_t *e_colT, int32_t *status, cudaStream_t st)
+{
+    if (dt == BF16)
+        return tile == 0 ? bw_t<BF16, 0, true>(x, M, K, q_row, e_row, q_colT, e_colT, status, st)
+                         : bw_t<BF16, 1, true>(x, M, K, q_row, e_row, q_colT, e_colT, status, st);
+    return tile == 0 ? bw_t<F32, 0, true>(x, M, K, q_row, e_row, q_colT, e_colT, status, st)
+                     : bw_t<F32, 1, true>(x, M, K, q_row, e_row, q_colT, e_colT, status, st);
 }
 
 }  // namespace qk

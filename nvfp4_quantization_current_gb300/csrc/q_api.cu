@@ -226,6 +226,31 @@ q_status q_blockwise(const void *x, q_dtype in, int64_t M, int64_t K, q_tile til
     return Q_OK;
 }
 
+q_status q_blockwise_mx(const void *x, q_dtype in, int64_t M, int64_t K, q_tile tile, uint8_t *q_row,
+                        uint8_t *e8m0_row, uint8_t *q_colT, uint8_t *e8m0_colT, int32_t *status, q_stream_t stream)
+{
+    const char *fn = "q_blockwise_mx";
+    TRY(check_dims(fn, M, K));
+    TRY(check_in(fn, x, in, M * K));
+    if (tile != Q_T1x128 && tile != Q_T128x128) return fail(Q_ERR_ARG, "%s: tile %d is not Q_T1x128 or Q_T128x128", fn, (int)tile);
+    TRY(multiple(fn, "K", K, 128));
+    if (tile == Q_T128x128) TRY(multiple(fn, "M (128x128 tiles)", M, 128));
+    if (M * K == 0) return Q_OK;
+    if (q_row == nullptr && q_colT == nullptr) return fail(Q_ERR_ARG, "%s: neither direction requested", fn);
+    if (q_row != nullptr) {
+        TRY(need(fn, "q_row", q_row, 16));
+        TRY(need(fn, "e8m0_row", e8m0_row, 4));
+    }
+    if (q_colT != nullptr) {
+        TRY(need(fn, "q_colT", q_colT, 16));
+        TRY(need(fn, "e8m0_colT", e8m0_colT, 4));
+        TRY(multiple(fn, "M (with q_colT)", M, 128));
+    }
+    LAUNCH(fn, qk::launch_blockwise_mx(x, (int)in, M, K, (int)tile, q_row, e8m0_row, q_colT, e8m0_colT, status,
+                                       S(stream)));
+    return Q_OK;
+}
+
 q_status q_nvfp4(const void *x, q_dtype in, int64_t M, int64_t K, q_nvblk blk, q_round rnd, uint64_t seed,
                  uint64_t offset, uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT, float *amax,
                  q_amax_mode amax_mode, float *s_global, int32_t *status, q_stream_t stream)

@@ -75,6 +75,8 @@ cudaError_t launch_mxfp8_requant_col(const uint8_t *q_row, const uint8_t *e_row,
 // blockwise
 cudaError_t launch_blockwise(const void *x, int dt, int64_t M, int64_t K, int tile, uint8_t *q_row,
                              float *s_row, uint8_t *q_colT, float *s_colT, int32_t *status, cudaStream_t st);
+cudaError_t launch_blockwise_mx(const void *x, int dt, int64_t M, int64_t K, int tile, uint8_t *q_row,
+                                uint8_t *e_row, uint8_t *q_colT, uint8_t *e_colT, int32_t *status, cudaStream_t st);
 
 // NVFP4 (the amax is already in *amax)
 cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, int rnd, uint64_t seed,

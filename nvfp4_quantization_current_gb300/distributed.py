@@ -104,13 +104,13 @@ def all_gather_shards(t_local: torch.Tensor, dim: int = 0, group=None) -> torch.
 # (rowwise codes and scales, and the MXFP8 columnwise copy, which keeps the
 # input's [M, K] layout) and those of the transposed copies ([K, M] layouts).
 _ROW_FIELDS = ("q_row", "sb_row", "e8m0_row", "s_row", "q_col", "e8m0_col")
-_COLT_FIELDS = ("q_colT", "sb_colT", "s_colT")
+_COLT_FIELDS = ("q_colT", "sb_colT", "s_colT", "e8m0_colT")
 
 
 def all_gather_quantized(t, group=None):
     """The whole tensor's quantized outputs from every rank's row-shard
-    outputs ``t`` (a CurrentScalingTensor, MXFP8Tensor, BlockwiseTensor or
-    NVFP4Tensor): rowwise fields gathered by rows, transposed copies by
+    outputs ``t`` (a CurrentScalingTensor, MXFP8Tensor, BlockwiseTensor,
+    BlockwiseMXTensor or NVFP4Tensor): rowwise fields gathered by rows, transposed copies by
     columns.  Shards must split rows on the recipe's block boundaries (32 for
     MXFP8 columnwise, 16 for NVFP4, 128 for the blockwise columnwise and 2-D
     tiles) and, for current scaling and NVFP4, share the all-reduced amax, so

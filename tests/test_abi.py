@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["q_amax", "q_current_scaling", "q_delayed_scaling", "q_delayed_scale_update", "q_mxfp8",
-              "q_mxfp8_requant_col", "q_blockwise", "q_nvfp4", "q_nvfp4_rht_amax", "q_nvfp4_rht_colT",
+              "q_mxfp8_requant_col", "q_blockwise", "q_blockwise_mx", "q_nvfp4", "q_nvfp4_rht_amax",
+              "q_nvfp4_rht_colT",
               "dq_current_scaling", "dq_mxfp8", "dq_blockwise",
               "dq_nvfp4", "q_last_error", "q_abi_version"]:
         assert n in names
@@ -153,6 +154,27 @@ def test_block_recipes_validation(L):
     assert st == Q.Q_ERR_ARG
     st, _ = status_of(L, "q_nvfp4", A, Q.Q_BF16, 16, 32, Q.Q_B1x16, Q.Q_RN, 0, 0, A, A, None, None, A, 0, None, None, None)
     assert st == Q.Q_ERR_ARG                       # s_global required
+
+
+def test_blockwise_mx_validation(L):
+    st, _ = status_of(L, "q_blockwise_mx", A, Q.Q_BF16, 128, 192, Q.Q_T1x128, A, A, None, None, None, None)
+    assert st == Q.Q_ERR_SHAPE                     # K % 128
+    st, _ = status_of(L, "q_blockwise_mx", A, Q.Q_BF16, 192, 128, Q.Q_T128x128, A, A, None, None, None, None)
+    assert st == Q.Q_ERR_SHAPE                     # M % 128 for 2D tiles
+    st, _ = status_of(L, "q_blockwise_mx", A, Q.Q_BF16, 64, 128, Q.Q_T1x128, None, None, A, A, None, None)
+    assert st == Q.Q_ERR_SHAPE                     # M % 128 with the transposed copy
+    st, _ = status_of(L, "q_blockwise_mx", A, Q.Q_BF16, 128, 128, 3, A, A, None, None, None, None)
+    assert st == Q.Q_ERR_ARG
+    st, msg = status_of(L, "q_blockwise_mx", A, Q.Q_BF16, 128, 128, Q.Q_T1x128, A, ctypes.c_void_p(0x10002),
+                        None, None, None, None)
+    assert st == Q.Q_ERR_ALIGN and "e8m0_row" in msg
+    st, msg = status_of(L, "q_blockwise_mx", A, Q.Q_BF16, 128, 128, Q.Q_T1x128, None, None, A,
+                        ctypes.c_void_p(0x10002), None, None)
+    assert st == Q.Q_ERR_ALIGN and "e8m0_colT" in msg
+    st, _ = status_of(L, "q_blockwise_mx", A, Q.Q_BF16, 128, 128, Q.Q_T1x128, None, None, None, None, None, None)
+    assert st == Q.Q_ERR_ARG                       # neither direction
+    st, _ = status_of(L, "q_blockwise_mx", A, Q.Q_BF16, 0, 128, Q.Q_T1x128, None, None, None, None, None, None)
+    assert st == Q.Q_OK                            # empty: nothing to do
 
 
 def test_dequant_validation(L):

@@ -105,6 +105,19 @@ def test_blockwise_stays_in_bounds(tile, shape, colwise):
     g.check(f"blockwise {tile} {shape}")
 
 
+@pytest.mark.parametrize("tile,shape,colwise", [("1x128", (256, 384), True), ("1x128", (100, 256), False),
+                                                ("128x128", (256, 384), True), ("128x128", (128, 128), True),
+                                                ("128x128", (128, 512), True)])
+def test_blockwise_mx_stays_in_bounds(tile, shape, colwise):
+    x = W.gen("normal", shape, 3, bf16=True)
+    g = Guards()
+    out = g.wrap(Q.alloc_blockwise_mx(*shape, "cuda", tile, True, colwise))
+    Q.q_blockwise_mx(dev(x), tile, True, colwise, out=out)
+    y = g.like(torch.empty(shape, dtype=torch.bfloat16, device="cuda"))
+    Q.dq_mxfp8(out.q_row, out.e8m0_row, "e4m3", Q.Q_ROW, torch.bfloat16, out=y)
+    g.check(f"blockwise_mx {tile} {shape}")
+
+
 @pytest.mark.parametrize("blk,rnd,shape", [("1x16", "rn", (272, 528)), ("1x16", "sr", (256, 512)),
                                            ("16x16", "rn", (144, 272)), ("1x16", "rn", (48, 160))])
 def test_nvfp4_and_rht_stay_in_bounds(blk, rnd, shape):

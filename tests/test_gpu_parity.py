@@ -467,6 +467,59 @@ def test_blockwise_parity(kind, shape, bf16, tile, colwise):
             same(host(got.dequantize(Q.Q_COL, dt)), O.dq_blockwise(want.q_colT, want.s_colT, tile, o_out(dt)), "dq colT")
 
 
+BWMX_CASES = [
+    ("normal", (256, 640), True, O.T1x128, True),
+    ("outliers", (384, 384), False, O.T1x128, True),     # FP32 input, 128-column CTA tiles
+    ("t3", (300, 384), True, O.T1x128, False),           # ragged rows, rowwise only
+    ("weight", (384, 640), True, O.T128x128, True),      # ragged last tile: one 128-column block
+    ("weight", (256, 512), True, O.T128x128, True),
+    ("lognormal_rows", (128, 128), False, O.T128x128, True),
+]
+
+
+@pytest.mark.parametrize("kind,shape,bf16,tile,colwise", BWMX_CASES)
+def test_blockwise_mx_parity(kind, shape, bf16, tile, colwise):
+    """Blockwise tiles with power-of-two scales held as MXFP8 E8M0 codes."""
+    x = W.gen(kind, shape, 313, bf16=bf16)
+    if shape[0] >= 256:
+        x[128:256, 128:256] = 0      # an all-zero tile
+    if not bf16:
+        x[:128, :128] *= np.float32(1e-39)   # FP32 subnormal tile maxima: code clamps to 0
+    want = O.blockwise_mx(x, tile, rowwise=True, colwise=colwise)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = Q.q_blockwise_mx(dev(x), "1x128" if tile == O.T1x128 else "128x128", rowwise=True, colwise=colwise,
+                           status=st)
+    torch.cuda.synchronize()
+    same(host(got.q_row), want.q_row, "q_row")
+    same(host(got.e8m0_row), want.e8m0_row, "e8m0_row")
+    if colwise:
+        same(host(got.q_colT), want.q_colT, "q_colT")
+        same(host(got.e8m0_colT), want.e8m0_colT, "e8m0_colT")
+    assert st.item() == 0
+    for dt in OUTS:
+        same(host(got.dequantize(Q.Q_ROW, dt)), O.dq_mxfp8(want.q_row, want.e8m0_row, O.E4M3, O.ROW, o_out(dt)), "dq row")
+        if colwise:
+            same(host(got.dequantize(Q.Q_COL, dt)), O.dq_mxfp8(want.q_colT, want.e8m0_colT, O.E4M3, O.ROW, o_out(dt)),
+                 "dq colT")
+
+
+def test_blockwise_mx_nonfinite_and_empty():
+    x = W.gen("normal", (128, 256), 5, bf16=False)
+    x[3, 200] = np.inf
+    x[70, 10] = np.nan
+    want = O.blockwise_mx(x, O.T1x128, rowwise=True, colwise=True)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = Q.q_blockwise_mx(dev(x), "1x128", rowwise=True, colwise=True, status=st)
+    torch.cuda.synchronize()
+    same(host(got.q_row), want.q_row, "q_row")
+    same(host(got.e8m0_row), want.e8m0_row, "e8m0_row")
+    same(host(got.q_colT), want.q_colT, "q_colT")
+    same(host(got.e8m0_colT), want.e8m0_colT, "e8m0_colT")
+    assert st.item() & Q.Q_ST_NONFINITE
+    empty = Q.q_blockwise_mx(torch.empty((0, 128), dtype=torch.bfloat16, device="cuda"))
+    assert empty.q_row.shape == (0, 128)
+
+
 # ---------------------------------------------------------------------------
 # NVFP4
 # ---------------------------------------------------------------------------
