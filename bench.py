@@ -58,11 +58,13 @@ RHT_MASK = 0xB4E1   # the 16 random signs of the Hadamard transform (any fixed d
 # capture time; reported as null when the source has changed since.
 TRAFFIC = {
     # profiles/k_blockwise_1x128T_bw3_act.md
-    "bw3.act:bw_1x128_T": {"bytes_per_launch": 420879616, "src_hash": "b1dcbe936762fce2"},
+    "bw3.act:bw_1x128_T": {"bytes_per_launch": 421635328, "src_hash": "6c3e28c748e48b9d"},
     # profiles/k_blockwise_128x128T_bw3_w.md
-    "bw3.w:bw_128x128_T": {"bytes_per_launch": 474289920, "src_hash": "b1dcbe936762fce2"},
+    "bw3.w:bw_128x128_T": {"bytes_per_launch": 474617856, "src_hash": "6c3e28c748e48b9d"},
+    # profiles/k_blockwise_mx_128x128T_bw3_w.md
+    "bw3.w:bwmx_128x128_T": {"bytes_per_launch": 484780032, "src_hash": "6c3e28c748e48b9d"},
     # profiles/k_cs_tiles_e5m2T_hy4_grad.md
-    "hy4.grad:cs_cast_T": {"bytes_per_launch": 415904256, "src_hash": "ad8fcb140417862d"},
+    "hy4.grad:cs_cast_T": {"bytes_per_launch": 415887104, "src_hash": "6aea2a644b520ea9"},
     # profiles/k_mxfp8_mx2_act.md
     "mx2.act:mxfp8": {"bytes_per_launch": 80998656, "src_hash": "63030beb08e84bc3"},
     # profiles/k_mxfp8_requant_mx2_act.md
