@@ -31,19 +31,27 @@
 
 namespace qk {
 
+// With 1x16 blocks both per-CTA lookup tables of k_nvfp4 hold 16
+// interleaved copies (entry e, copy j at word 16 e + j) and lane l reads copy
+// l % 16, so lanes that look up different entries meet in one bank at most in
+// pairs (with one copy up to four entries share a bank).  16x16 lookups are
+// uniform across the lanes of a block and keep one copy.
+template <int BLK> constexpr int kTabCopies = BLK == 0 ? 16 : 1;
+
 // Block scale code sb = E4M3(RN(RN(b * alpha_g) / 6)) (b = 0 -> 0x38, 1.0).
+// T1 points at this lane's copy of the mantissa table.
 // For BF16 inputs b = (1 + m/128) 2^(E-127); writing alpha_g = a_m 2^ae with
 // a_m in [1, 2), RN(RN(b alpha_g) / 6) = RN(RN((1 + m/128) a_m) / 6)
 // 2^(E-127+ae) while the values stay normal (rounding commutes with
 // power-of-two scaling), so it is a per-CTA 128-entry table plus an exponent
 // shift; anything that would fall below 2^-126 encodes to E4M3 +0 either way.
 // FP32 inputs and subnormal or non-finite b take the two operations.
-template <int DT> QD uint32_t nv_sb_code(uint32_t b, float alpha_g, const uint32_t *T1, int ae)
+template <int DT, int C = 1> QD uint32_t nv_sb_code(uint32_t b, float alpha_g, const uint32_t *T1, int ae)
 {
     if (b == 0) return 0x38u;
     const uint32_t E = b >> 23;
     if (DT == BF16 && E != 0u && E != 255u) {
-        const uint32_t t = T1[(b >> 16) & 0x7Fu];
+        const uint32_t t = T1[((b >> 16) & 0x7Fu) * C];
         const int ne = (int)(t >> 23) + (int)E - 127 + ae;
         if (ne <= 0) return 0u;
         return e4m3_code(__uint_as_float((t & 0x807FFFFFu) | ((uint32_t)ne << 23)));
@@ -52,8 +60,8 @@ template <int DT> QD uint32_t nv_sb_code(uint32_t b, float alpha_g, const uint32
 }
 
 // The encode factor enc = alpha_g / f(sb) (0 when f(sb) = 0) depends only on
-// the code: each CTA tabulates it for the 128 positive codes (enc_tab[0x38]
-// = alpha_g also serves b = 0).
+// the code: each CTA tabulates it for the 128 positive codes (entry 0x38 =
+// alpha_g also serves b = 0).
 
 
 // In-place transpose of an 8x8 nibble matrix: a[i] nibble j -> a[j] nibble i.
@@ -183,9 +191,9 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                                                           uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
                                                           float *__restrict__ s_global, int32_t *status)
 {
-    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, LPB = 16 / VEC;
-    __shared__ float enc_tab[128];
-    __shared__ uint32_t sb_tab[128];             // BF16: RN(RN((1 + m/128) a_m) / 6) per mantissa m
+    constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, LPB = 16 / VEC, TCP = kTabCopies<BLK>;
+    __shared__ float enc_tab[128 * TCP];
+    __shared__ uint32_t sb_tab[128 * TCP];   // BF16: RN(RN((1 + m/128) a_m) / 6) per mantissa m
     __shared__ uint4 part[kEngWarps][32];        // 1x16: per-warp column maxima over 8 rows
     __shared__ uint8_t sSB[8][TC];               // 1x16: columnwise block scales of a tile
     __shared__ uint32_t bred[kEngWarps][TC / 16];   // 16x16: half-block maxima
@@ -197,10 +205,14 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
     const int ae = (int)(ag >> 23) - 127;   // alpha_g is always a normal float
     if (threadIdx.x < 128) {
         const float sv = e4m3_value(threadIdx.x);
-        enc_tab[threadIdx.x] = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_g, sv);
+        const float ev = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_g, sv);
         const float a_m = __uint_as_float((ag & 0x807FFFFFu) | (127u << 23));
-        sb_tab[threadIdx.x] = __float_as_uint(
-            __fdiv_rn(__fmul_rn(1.0f + (float)threadIdx.x * (1.0f / 128.0f), a_m), 6.0f));
+        const uint32_t tv = __float_as_uint(__fdiv_rn(__fmul_rn(1.0f + (float)threadIdx.x * (1.0f / 128.0f), a_m), 6.0f));
+#pragma unroll
+        for (int j = 0; j < TCP; j++) {
+            enc_tab[threadIdx.x * TCP + j] = ev;
+            sb_tab[threadIdx.x * TCP + j] = tv;
+        }
     }   // visible after the engine's first barrier
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         *s_global = __fdiv_rn(1.0f, alpha_g);
@@ -209,6 +221,8 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
     if (M == 0 || K == 0) return;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
+    const float *encT = enc_tab + (lane & (TCP - 1));   // this lane's copy: entry e at encT[e * TCP]
+    const uint32_t *sbT = sb_tab + (lane & (TCP - 1));
 
     run_tiles(&tmap, tiles_m, tiles_k, TC, true, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
@@ -258,8 +272,8 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                 for (int h = 0; h < 4; h++) {
                     const uint32_t kw = h < 2 ? k0 : k1;
                     const uint32_t bits = ((h & 1) ? kw : (kw << 16)) & 0x7FFF0000u;   // row rb + h
-                    const uint32_t sb = nv_sb_code<DT>(bits, alpha_g, sb_tab, ae);
-                    own[h] = enc_tab[sb];
+                    const uint32_t sb = nv_sb_code<DT, TCP>(bits, alpha_g, sbT, ae);
+                    own[h] = encT[sb * TCP];
                     if (rb + h < nrows) {
                         sb_row[(m0 + rb + h) * (K / 16) + k / 16] = (uint8_t)sb;
                         nf |= nonfinite(bits);
@@ -286,8 +300,8 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
 #pragma unroll
                     for (int h = 0; h < 2; h++) {
                         const int64_t m = m0 + j + h;
-                        const uint32_t sb = nv_sb_code<DT>(bb[h], alpha_g, sb_tab, ae);
-                        const uint32_t code = nv_row_codes<DT, RND>(v[j + h], enc_tab[sb], seed, offset, m * K + k);
+                        const uint32_t sb = nv_sb_code<DT, TCP>(bb[h], alpha_g, sbT, ae);
+                        const uint32_t code = nv_row_codes<DT, RND>(v[j + h], encT[sb * TCP], seed, offset, m * K + k);
                         const bool ok = m < M && kok;
                         if (ok) {
                             uint8_t *dst = q_row + m * (K / 2) + k / 2;
@@ -317,8 +331,8 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
 #pragma unroll
             for (int c = 0; c < VEC; c++) {
                 const uint32_t b = colmax_bits<DT>(cm, c);
-                const uint32_t sb = nv_sb_code<DT>(b, alpha_g, sb_tab, ae);
-                const float enc = enc_tab[sb];
+                const uint32_t sb = nv_sb_code<DT, TCP>(b, alpha_g, sbT, ae);
+                const float enc = encT[sb * TCP];
                 if ((warp & 1) == 0) sSB[warp >> 1][lane * VEC + c] = (uint8_t)sb;
                 nfc |= ((warp & 1) == 0 && kok && m0 < M) ? nonfinite(b) : 0u;
                 float y[8];
@@ -349,8 +363,8 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
             if (lane % LPB == 0) bred[warp][lane / LPB] = b;
             __syncthreads();   // half-block maxima posted; every read of the stage is done
             b = max(bred[warp & ~1][lane / LPB], bred[warp | 1][lane / LPB]);
-            const uint32_t sb = nv_sb_code<DT>(b, alpha_g, sb_tab, ae);
-            const float enc = enc_tab[sb];
+            const uint32_t sb = nv_sb_code<DT, TCP>(b, alpha_g, sbT, ae);
+            const float enc = encT[sb * TCP];
             const int64_t m16 = mb + 16 * (warp >> 1);
             if ((warp & 1) == 0 && lane % LPB == 0 && m16 < M && kok) {
                 if (sb_row != nullptr) sb_row[(m16 / 16) * (K / 16) + k / 16] = (uint8_t)sb;
