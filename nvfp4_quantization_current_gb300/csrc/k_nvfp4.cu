@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
     __shared__ float enc_tab[128 * TCP];
     __shared__ uint32_t sb_tab[128 * TCP];   // BF16: RN(RN((1 + m/128) a_m) / 6) per mantissa m
     __shared__ uint4 part[kEngWarps][32];        // 1x16: per-warp column maxima over 8 rows
-    __shared__ uint8_t sSB[8][TC];               // 1x16: columnwise block scales of a tile
+    __shared__ __align__(8) uint8_t sSB[8][TC];   // 1x16: columnwise block scales of a tile
     __shared__ uint32_t bred[kEngWarps][TC / 16];   // 16x16: half-block maxima
 
     griddep_wait();   // the amax pass ahead of this kernel is complete
@@ -328,12 +328,16 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
             // each column's block scale, then its 8 rows with the block's factor:
             // one E2M1 word per column (row 8w in bits 3-0)
             uint32_t nfc = 0;
+            // RTNE: this thread's VEC column scale codes, stored together below
+            // (with SR the register they take costs more than the byte stores)
+            uint32_t sbw[VEC / 4] = {};
 #pragma unroll
             for (int c = 0; c < VEC; c++) {
                 const uint32_t b = colmax_bits<DT>(cm, c);
                 const uint32_t sb = nv_sb_code<DT, TCP>(b, alpha_g, sbT, ae);
                 const float enc = encT[sb * TCP];
-                if ((warp & 1) == 0) sSB[warp >> 1][lane * VEC + c] = (uint8_t)sb;
+                if (RND == 0) sbw[c >> 2] |= sb << (8 * (c & 3));
+                else if ((warp & 1) == 0) sSB[warp >> 1][lane * VEC + c] = (uint8_t)sb;
                 nfc |= ((warp & 1) == 0 && kok && m0 < M) ? nonfinite(b) : 0u;
                 float y[8];
 #pragma unroll
@@ -352,6 +356,10 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                     }
                 }
                 colw[c] = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+            }
+            if (RND == 0 && (warp & 1) == 0) {   // one store of VEC codes (bytes lane*VEC .. +VEC-1)
+                if constexpr (VEC == 8) *reinterpret_cast<uint2 *>(&sSB[warp >> 1][lane * VEC]) = make_uint2(sbw[0], sbw[1]);
+                else *reinterpret_cast<uint32_t *>(&sSB[warp >> 1][lane * VEC]) = sbw[0];
             }
             post_nonfinite(status, nfc);
         } else {
