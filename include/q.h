@@ -26,6 +26,9 @@
  * parameter says otherwise); the library never allocates, never frees and
  * keeps no per-call state.  Each call enqueues its kernels on `stream`
  * (NULL = the legacy default stream) and returns without synchronizing.
+ * Outputs must not overlap the inputs or each other.  Calls share no device
+ * state, so calls on different streams (or devices) may run concurrently;
+ * the caller orders a call after the producer of its inputs.
  *
  * Alignment: x, y and every code buffer must be 16-byte aligned; FP32 scale
  * buffers 4-byte aligned.
