@@ -637,3 +637,33 @@ def test_fp8_cast_exhaustive_bf16(fmt, fmax):
     f32eq(got.scale.item(), 1.0)
     same(host(got.q_row), want.q_row, "q_row")
     same(host(got.q_colT), want.q_colT, "q_colT")
+
+
+def test_calls_on_two_streams_run_concurrently_and_match_the_oracle():
+    """The calls share no device state: NVFP4 SR and current scaling on one
+    stream, blockwise and MXFP8 on another, enqueued back to back without
+    synchronizing, give the oracle's results."""
+    x1 = W.gen("t3", (1024, 2048), 61, bf16=True)
+    x2 = W.gen("normal", (1024, 2048), 62, bf16=True)
+    d1, d2 = dev(x1), dev(x2)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        nv = Q.q_nvfp4(d1, "1x16", "sr", seed=3, offset=1, colwise=True)
+        cs = Q.q_current_scaling(d1, "e5m2", colwise=True)
+    with torch.cuda.stream(s2):
+        bw = Q.q_blockwise(d2, "1x128", colwise=True)
+        mx = Q.q_mxfp8(d2)
+    torch.cuda.synchronize()
+    w = O.nvfp4(x1, O.B1x16, O.SR, seed=3, offset=1, rowwise=True, colwise=True)
+    same(host(nv.q_row), w.q_row, "nv q_row")
+    same(host(nv.q_colT), w.q_colT, "nv q_colT")
+    w = O.current_scaling(x1, O.E5M2, rowwise=True, colwise=True)
+    same(host(cs.q_row), w.q_row, "cs q_row")
+    same(host(cs.q_colT), w.q_colT, "cs q_colT")
+    w = O.blockwise(x2, O.T1x128, rowwise=True, colwise=True)
+    same(host(bw.q_colT), w.q_colT, "bw q_colT")
+    same(host(bw.s_colT), w.s_colT, "bw s_colT")
+    w = O.mxfp8(x2)
+    same(host(mx.q_col), w.q_col, "mx q_col")
+    same(host(mx.e8m0_row), w.e8m0_row, "mx e8m0_row")
