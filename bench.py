@@ -9,7 +9,9 @@ row + col and the row->col re-quantize, blockwise 1x128 (+ transposed) and
 128x128 (+ transposed), both again with power-of-two tile scales held as
 MXFP8, NVFP4 1x16 RTNE, 1x16 stochastic rounding and 16x16,
 the dequantizer of each, and the random-Hadamard NVFP4 columnwise copies of
-the NVFP4 activation and gradient (weight-gradient GEMM inputs).  Every call goes through the C ABI with
+the NVFP4 activation and gradient (weight-gradient GEMM inputs), and the
+NVFP4 recipe's two copies of the gradient (rowwise SR + random-Hadamard
+columnwise SR, one amax pass for both).  Every call goes through the C ABI with
 preallocated outputs.
 
 Metric: quantize GB/s = algorithmic bytes (input bytes x reads + all output
@@ -249,6 +251,22 @@ def build_step(dev_tensors, torch, Q):
         calls.append(Call(f"{tag} nvfp4_rht_{rnd} colT", "nvfp4_rht", pieces, [x],
                           [out.q_colT, out.sb_colT, out.s_global], e2e))
 
+    def recipe(tag, x, rnd, seed, mask=RHT_MASK):
+        M, K = x.shape
+        row = Q.alloc_nvfp4(M, K, x.device, "1x16", rowwise=True, colwise=False)
+        col = Q.alloc_nvfp4(M, K, x.device, "1x16", rowwise=False, colwise=True)
+        ins = nbytes(x)
+        pieces = [
+            ("rht_amax2", "k_nvfp4.cu", ins, lambda: Q.q_nvfp4_rht_amax2(x, mask, out=(col.amax, row.amax))),
+            (f"nvfp4_row_{rnd}", "k_nvfp4.cu", ins + nbytes(row.q_row, row.sb_row, row.s_global) + 4,
+             lambda: Q.q_nvfp4(x, "1x16", rnd, seed, 0, True, False, amax=row.amax, out=row)),
+            (f"nvfp4_rht_colT_{rnd}", "k_nvfp4.cu", ins + nbytes(col.q_colT, col.sb_colT, col.s_global) + 4,
+             lambda: Q.q_nvfp4_rht_colT(x, mask, rnd, seed, 0, amax=col.amax, out=col)),
+        ]
+        calls.append(Call(f"{tag} nvfp4_recipe_{rnd} row + RHT colT", "nvfp4_recipe", pieces, [x],
+                          [row.q_row, row.sb_row, row.s_global, col.q_colT, col.sb_colT, col.s_global],
+                          lambda: Q.q_nvfp4_recipe(x, mask, rnd, seed, 0, out=(row, col))))
+
     if "cs1" in d:
         cs("cs1.x", d["cs1"]["x"], "e4m3", True)
     if "mx2" in d:
@@ -268,6 +286,7 @@ def build_step(dev_tensors, torch, Q):
         nv("nv5.w", d["nv5"]["w"], "16x16", "rn", 0)
         rht("nv5.act", d["nv5"]["act"], "rn", 0)
         rht("nv5.grad", d["nv5"]["grad"], "sr", 4)
+        recipe("nv5.grad", d["nv5"]["grad"], "sr", 4)
     return calls
 
 
@@ -302,7 +321,7 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
                          ("mx2", "act", "mx"), ("bw3", "act", "bw1"), ("bw3", "w", "bw128"),
                          ("bw3", "act", "bwmx1"), ("bw3", "w", "bwmx128"),
                          ("nv5", "act", "nv_rn"), ("nv5", "grad", "nv_sr"), ("nv5", "w", "nv16"),
-                         ("nv5", "act", "rht_rn"), ("nv5", "grad", "rht_sr")]:
+                         ("nv5", "act", "rht_rn"), ("nv5", "grad", "rht_sr"), ("nv5", "grad", "recipe_sr")]:
         xh, xd = host_tensors[wl][tn], dev_tensors[wl][tn]
         M, K = xh.shape
         r0 = band(M)
@@ -333,6 +352,17 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
             eq(host(g.sb_colT[:, r0 // 16:(r0 + rows) // 16]), sb, f"{wl}.{tn} rht sb_colT band")
             if rnd == O.RN:   # SR draws depend on the full-height index k*M + m: scales only
                 eq(host(g.q_colT[:, r0 // 2:(r0 + rows) // 2]), q, f"{wl}.{tn} rht q_colT band")
+        elif kind == "recipe_sr":
+            A_x, A_r = O.amax(xh), O.amax(O.rht_cols(xh, RHT_MASK))
+            row, col = Q.q_nvfp4_recipe(xd, RHT_MASK, "sr", 4, 0)
+            eq(np.float32(row.amax.item()), np.float32(A_x), f"{wl}.{tn} recipe amax_row")
+            eq(np.float32(col.amax.item()), np.float32(A_r), f"{wl}.{tn} recipe amax_colT")
+            # the band's rowwise draws start at counter r0*K/8
+            w = O.nvfp4(xs, O.B1x16, O.SR, seed=4, offset=r0 * K // 8, rowwise=True, colwise=False, amax_in=A_x)
+            eq(host(row.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} recipe q_row band")
+            eq(host(row.sb_row[r0:r0 + rows]), w.sb_row, f"{wl}.{tn} recipe sb_row band")
+            _, sb, _, _ = O.nvfp4_rht_colT(xs, RHT_MASK, O.RN, amax_in=A_r)
+            eq(host(col.sb_colT[:, r0 // 16:(r0 + rows) // 16]), sb, f"{wl}.{tn} recipe sb_colT band")
         elif kind.startswith("cs"):
             fmt = O.E5M2 if kind == "cs_e5m2" else O.E4M3
             A = O.amax(xh)
@@ -615,7 +645,7 @@ def run_ours(args):
                 "share_of_step": round(dom_us / (step_ms * 1e3), 3), "peak_kind": peak_kind + " hbm_gbs"}
     # q_amax, the delayed-scaling cast and the transform's amax launch two
     # kernels (zero the amax word, then the pass); every other call one
-    n_launches = args.steps * sum((2 if p[0] in ("amax", "ds_cast_T", "rht_amax") else 1) for c in calls for p in c.pieces)
+    n_launches = args.steps * sum((2 if p[0] in ("amax", "ds_cast_T", "rht_amax", "rht_amax2") else 1) for c in calls for p in c.pieces)
 
     # ---- end to end: pinned host input -> device, the public call, outputs -> pinned host
     e2e = None
@@ -819,6 +849,12 @@ def oracle_sample_work(host_t, frac):
     nv(host_t["nv5"]["w"], O.B16x16, O.RN, 0)
     rht(host_t["nv5"]["act"], O.RN, 0)
     rht(host_t["nv5"]["grad"], O.SR, 4)
+    nv_rows = np.ascontiguousarray(host_t["nv5"]["grad"][:rows(host_t["nv5"]["grad"])])
+    Mr, Kr = nv_rows.shape
+    work.append((lambda: (O.amax(nv_rows), O.amax(O.rht_cols(nv_rows, RHT_MASK))), nv_rows.nbytes))
+    work.append((lambda: O.nvfp4(nv_rows, O.B1x16, O.SR, seed=4, rowwise=True, colwise=False),
+                 nv_rows.nbytes + Mr * Kr // 2 + Mr * Kr // 16 + 4))
+    work.append((lambda: O.nvfp4_rht_colT(nv_rows, RHT_MASK, O.SR, seed=4), nv_rows.nbytes + Mr * Kr // 2 + Mr * Kr // 16 + 4))
     return work
 
 

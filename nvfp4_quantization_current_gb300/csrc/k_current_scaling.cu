@@ -248,22 +248,23 @@ __global__ void k_empty_scales(float *amax_out, float *scale)
 
 // Zeroes the amax word before the reduction (a kernel on the same stream: the
 // next kernel starts right behind it, which a driver memset does not).
-__global__ void k_zero_word(uint32_t *w)
+__global__ void k_zero_word(uint32_t *w, uint32_t *w2)
 {
     griddep_launch_dependents();   // the reduction behind may start; it waits before its atomic
     *w = 0u;
+    if (w2 != nullptr) *w2 = 0u;
 }
 
-cudaError_t launch_zero_word(float *w, cudaStream_t st)
+cudaError_t launch_zero_word(float *w, cudaStream_t st, float *w2)
 {
-    k_zero_word<<<1, 1, 0, st>>>(reinterpret_cast<uint32_t *>(w));
+    k_zero_word<<<1, 1, 0, st>>>(reinterpret_cast<uint32_t *>(w), reinterpret_cast<uint32_t *>(w2));
     return cudaGetLastError();
 }
 
 cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *status, cudaStream_t st)
 {
     (void)status;
-    k_zero_word<<<1, 1, 0, st>>>(reinterpret_cast<uint32_t *>(amax));
+    k_zero_word<<<1, 1, 0, st>>>(reinterpret_cast<uint32_t *>(amax), nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || n == 0) return e;
     const int vec = dt == BF16 ? 8 : 4;
@@ -285,7 +286,7 @@ static cudaError_t cs_cast_t(const void *x, int64_t M, int64_t K, const float *a
     const bool pdl = DS || after_amax;   // behind the zeroing kernel (DS) or the amax pass
     uint32_t *rec = reinterpret_cast<uint32_t *>(amax_rec);
     if (DS) {
-        k_zero_word<<<1, 1, 0, st>>>(rec);
+        k_zero_word<<<1, 1, 0, st>>>(rec, nullptr);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -463,6 +463,9 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
                                                               int32_t *status)
 {
     constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CPT = VEC / 2;
+    // PASS 0 writes no tensor scale: its s_global slot carries the optional
+    // max|x| output (the untransformed tensor's amax, in the same read)
+    float *const amax_x = PASS == 0 ? s_global : nullptr;
     __shared__ float enc_tab[128];
     __shared__ uint8_t sSB[8][TC];
     float alpha_g = 1.0f;
@@ -484,12 +487,23 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
     const int g = threadIdx.x >> 6, q = threadIdx.x & 63;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
     uint32_t mx = 0;   // PASS 0: max |x'| bits of this thread (zero-filled rows and columns give 0)
+    uint32_t mxx = 0;  // PASS 0 with amax_x: max |x| bits of this thread (the untransformed tensor)
 
     run_tiles(&tmap, tiles_m, tiles_k, TC, PASS == 1, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
         uint2 raw[16];
 #pragma unroll
         for (int r = 0; r < 16; r++) raw[r] = *reinterpret_cast<const uint2 *>(st + (16 * g + r) * kRowBytes + q * 8);
+        if (PASS == 0 && amax_x != nullptr) {
+#pragma unroll
+            for (int r = 0; r < 16; r++) {
+                if (DT == BF16)
+                    mxx = max(mxx, max(max((raw[r].x << 16) & 0x7FFF0000u, raw[r].x & 0x7FFF0000u),
+                                       max((raw[r].y << 16) & 0x7FFF0000u, raw[r].y & 0x7FFF0000u)));
+                else
+                    mxx = max(mxx, max(raw[r].x & 0x7FFFFFFFu, raw[r].y & 0x7FFFFFFFu));
+            }
+        }
         uint32_t code[CPT][2];   // per column: rows 16g..16g+7 and 16g+8..16g+15, first row in bits 3-0
 #pragma unroll
         for (int p = 0; p < CPT / 2; p++) {   // column pair (2p, 2p+1) of the thread's CPT columns
@@ -576,15 +590,19 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
         copy_out_sbT<TC>(sSB, sb_colT, M, K, mb, kb);
     });
     if (PASS == 0) {
-        griddep_wait();   // the zeroing of *amax ahead of this pass is complete
+        griddep_wait();   // the zeroing of the amax words ahead of this pass is complete
         cta_max_to(mx, reinterpret_cast<uint32_t *>(amax), status);
+        if (amax_x != nullptr) {
+            __syncthreads();   // the CTA reduction's shared words are free again
+            cta_max_to(mxx, reinterpret_cast<uint32_t *>(amax_x), status);
+        }
     }
 }
 
 template <int DT, int RND, int PASS>
 static cudaError_t rht_pass(bool pdl, const CUtensorMap &map, int64_t M, int64_t K, uint32_t mask, float *amax,
-                            uint64_t seed, uint64_t offset, uint8_t *q_colT, uint8_t *sb_colT, float *s_global,
-                            int32_t *status, cudaStream_t st)
+                            float *amax_x, uint64_t seed, uint64_t offset, uint8_t *q_colT, uint8_t *sb_colT,
+                            float *s_global, int32_t *status, cudaStream_t st)
 {
     constexpr int TC = 32 * In<DT>::VEC;
     {
@@ -595,7 +613,7 @@ static cudaError_t rht_pass(bool pdl, const CUtensorMap &map, int64_t M, int64_t
     int grid = (int)(tiles < sm_count() ? tiles : sm_count());
     if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
     return launch_k(pdl, k_nvfp4_rht<DT, RND, PASS>, dim3(grid), dim3(kEngThreads), kEngSmem, st, map, M, K, mask, amax,
-                    seed, offset, q_colT, sb_colT, s_global, status);
+                    seed, offset, q_colT, sb_colT, PASS == 0 ? amax_x : s_global, status);
 }
 
 template <int DT, int RND>
@@ -614,22 +632,26 @@ static cudaError_t rht_t(const void *x, int64_t M, int64_t K, uint32_t mask, boo
     if (compute_amax) {
         cudaError_t e = launch_zero_word(amax, st);
         if (e != cudaSuccess) return e;
-        e = rht_pass<DT, 0, 0>(true, map, M, K, mask, amax, seed, offset, q_colT, sb_colT, s_global, status, st);   // no rounding in the amax pass
+        e = rht_pass<DT, 0, 0>(true, map, M, K, mask, amax, nullptr, seed, offset, q_colT, sb_colT, s_global, status,
+                               st);   // no rounding in the amax pass
         if (e != cudaSuccess) return e;
     }
-    return rht_pass<DT, RND, 1>(compute_amax, map, M, K, mask, amax, seed, offset, q_colT, sb_colT, s_global, status, st);
+    return rht_pass<DT, RND, 1>(compute_amax, map, M, K, mask, amax, nullptr, seed, offset, q_colT, sb_colT, s_global,
+                                status, st);
 }
 
 cudaError_t launch_rht_amax(const void *x, int dt, int64_t M, int64_t K, uint32_t sign_mask, float *amax,
-                           int32_t *status, cudaStream_t st)
+                            float *amax_x, int32_t *status, cudaStream_t st)
 {
     alignas(64) CUtensorMap map;
-    if (M == 0 || K == 0) return launch_zero_word(amax, st);
+    if (M == 0 || K == 0) return launch_zero_word(amax, st, amax_x);
     cudaError_t e = make_tile_map(&map, x, dt, M, K);
-    if (e == cudaSuccess) e = launch_zero_word(amax, st);
+    if (e == cudaSuccess) e = launch_zero_word(amax, st, amax_x);
     if (e != cudaSuccess) return e;
-    return dt == BF16 ? rht_pass<BF16, 0, 0>(true, map, M, K, sign_mask, amax, 0, 0, nullptr, nullptr, nullptr, status, st)
-                      : rht_pass<F32, 0, 0>(true, map, M, K, sign_mask, amax, 0, 0, nullptr, nullptr, nullptr, status, st);
+    return dt == BF16 ? rht_pass<BF16, 0, 0>(true, map, M, K, sign_mask, amax, amax_x, 0, 0, nullptr, nullptr, nullptr,
+                                            status, st)
+                      : rht_pass<F32, 0, 0>(true, map, M, K, sign_mask, amax, amax_x, 0, 0, nullptr, nullptr, nullptr,
+                                           status, st);
 }
 
 cudaError_t launch_nvfp4_rht_colT(const void *x, int dt, int64_t M, int64_t K, uint32_t sign_mask, int rnd,

@@ -291,7 +291,53 @@ q_status q_nvfp4_rht_amax(const void *x, q_dtype in, int64_t M, int64_t K, uint3
     TRY(multiple(fn, "K", K, 16));
     TRY(multiple(fn, "M", M, 16));
     TRY(need(fn, "amax", amax, 4));
-    LAUNCH(fn, qk::launch_rht_amax(x, (int)in, M, K, sign_mask, amax, status, S(stream)));
+    LAUNCH(fn, qk::launch_rht_amax(x, (int)in, M, K, sign_mask, amax, nullptr, status, S(stream)));
+    return Q_OK;
+}
+
+q_status q_nvfp4_rht_amax2(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, float *amax_rht,
+                           float *amax_x, int32_t *status, q_stream_t stream)
+{
+    const char *fn = "q_nvfp4_rht_amax2";
+    TRY(check_dims(fn, M, K));
+    TRY(check_in(fn, x, in, M * K));
+    if (sign_mask > 0xFFFFu) return fail(Q_ERR_ARG, "%s: sign_mask 0x%x has bits above bit 15", fn, sign_mask);
+    TRY(multiple(fn, "K", K, 16));
+    TRY(multiple(fn, "M", M, 16));
+    TRY(need(fn, "amax_rht", amax_rht, 4));
+    TRY(need(fn, "amax_x", amax_x, 4));
+    LAUNCH(fn, qk::launch_rht_amax(x, (int)in, M, K, sign_mask, amax_rht, amax_x, status, S(stream)));
+    return Q_OK;
+}
+
+q_status q_nvfp4_recipe(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, q_round rnd,
+                        uint64_t seed, uint64_t offset, uint8_t *q_row, uint8_t *sb_row, float *amax_row,
+                        float *s_global_row, uint8_t *q_colT, uint8_t *sb_colT, float *amax_colT,
+                        float *s_global_colT, int32_t *status, q_stream_t stream)
+{
+    const char *fn = "q_nvfp4_recipe";
+    TRY(check_dims(fn, M, K));
+    TRY(check_in(fn, x, in, M * K));
+    if (rnd != Q_RN && rnd != Q_SR) return fail(Q_ERR_ARG, "%s: rnd %d is not Q_RN or Q_SR", fn, (int)rnd);
+    if (sign_mask > 0xFFFFu) return fail(Q_ERR_ARG, "%s: sign_mask 0x%x has bits above bit 15", fn, sign_mask);
+    TRY(multiple(fn, "K", K, 16));
+    TRY(multiple(fn, "M", M, 16));
+    TRY(need(fn, "amax_row", amax_row, 4));
+    TRY(need(fn, "s_global_row", s_global_row, 4));
+    TRY(need(fn, "amax_colT", amax_colT, 4));
+    TRY(need(fn, "s_global_colT", s_global_colT, 4));
+    if (M * K != 0) {
+        TRY(need(fn, "q_row", q_row, 16));
+        TRY(need(fn, "sb_row", sb_row, 1));
+        TRY(need(fn, "q_colT", q_colT, 16));
+        TRY(need(fn, "sb_colT", sb_colT, 1));
+    }
+    // one read for both maxima, then the rowwise cast and the transformed columnwise cast with them
+    LAUNCH(fn, qk::launch_rht_amax(x, (int)in, M, K, sign_mask, amax_colT, amax_row, status, S(stream)));
+    LAUNCH(fn, qk::launch_nvfp4(x, (int)in, M, K, (int)Q_B1x16, (int)rnd, seed, offset, amax_row, q_row, sb_row, nullptr,
+                                nullptr, s_global_row, status, S(stream), true));
+    LAUNCH(fn, qk::launch_nvfp4_rht_colT(x, (int)in, M, K, sign_mask, (int)rnd, seed, offset, false, amax_colT, q_colT,
+                                         sb_colT, s_global_colT, status, S(stream)));
     return Q_OK;
 }
 

@@ -49,12 +49,13 @@ cudaError_t launch_mxfp8(const void *x, int dt, int64_t M, int64_t K, int fmt, u
 // one warp waits wait_ns on a barrier nothing completes, then reports Q_ST_TIMEOUT
 cudaError_t launch_selftest_wait(int32_t *status, unsigned long long wait_ns, cudaStream_t st);
 
-// *w = 0 (one thread), stream-ordered before a reduction into it
-cudaError_t launch_zero_word(float *w, cudaStream_t st);
+// *w = 0 (and *w2 = 0 when given; one thread), stream-ordered before a reduction into it
+cudaError_t launch_zero_word(float *w, cudaStream_t st, float *w2 = nullptr);
 
-// max|x'| of the random Hadamard transform along M (zeroes *amax first)
+// max|x'| of the random Hadamard transform along M, and max|x| into *amax_x
+// when it is given, in one read (zeroes both words first)
 cudaError_t launch_rht_amax(const void *x, int dt, int64_t M, int64_t K, uint32_t sign_mask, float *amax,
-                           int32_t *status, cudaStream_t st);
+                            float *amax_x, int32_t *status, cudaStream_t st);
 
 // random Hadamard transform along M + columnwise NVFP4 of the result; the
 // amax of the transformed tensor is reduced into *amax first unless given

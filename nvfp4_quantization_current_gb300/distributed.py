@@ -79,6 +79,21 @@ def quantize_shard_nvfp4(x_local: torch.Tensor, blk="1x16", rounding="rn", seed=
     return q_nvfp4(x_local, blk, rounding, seed, offset, rowwise, colwise, amax=a, status=status)
 
 
+def quantize_shard_nvfp4_recipe(x_local: torch.Tensor, sign_mask: int, rounding="rn", seed=0, offset=0, group=None,
+                                status: Optional[torch.Tensor] = None):
+    """Both NVFP4 recipe copies of this rank's row shard (rows split on 16-row
+    boundaries): one read for the two local maxima, a MAX all-reduce of each,
+    then the rowwise copy of x and the columnwise copy of its transform with
+    the global maxima.  Returns (row, colT) like q_nvfp4_recipe."""
+    from . import q_nvfp4, q_nvfp4_rht_amax2, q_nvfp4_rht_colT
+    a_rht, a_x = q_nvfp4_rht_amax2(x_local, sign_mask, status=status)
+    allreduce_amax_(a_rht, group)
+    allreduce_amax_(a_x, group)
+    row = q_nvfp4(x_local, "1x16", rounding, seed, offset, rowwise=True, colwise=False, amax=a_x, status=status)
+    col = q_nvfp4_rht_colT(x_local, sign_mask, rounding, seed, offset, amax=a_rht, status=status)
+    return row, col
+
+
 def all_gather_shards(t_local: torch.Tensor, dim: int = 0, group=None) -> torch.Tensor:
     """The concatenation along ``dim``, in rank order, of every rank's
     ``t_local``.  Shards may differ in size along ``dim`` (they are padded to

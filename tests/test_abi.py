@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["q_amax", "q_current_scaling", "q_delayed_scaling", "q_delayed_scale_update", "q_mxfp8",
               "q_mxfp8_requant_col", "q_blockwise", "q_blockwise_mx", "q_nvfp4", "q_nvfp4_rht_amax",
-              "q_nvfp4_rht_colT",
+              "q_nvfp4_rht_colT", "q_nvfp4_rht_amax2", "q_nvfp4_recipe",
               "dq_current_scaling", "dq_mxfp8", "dq_blockwise",
               "dq_nvfp4", "q_last_error", "q_abi_version"]:
         assert n in names
@@ -175,6 +175,26 @@ def test_blockwise_mx_validation(L):
     assert st == Q.Q_ERR_ARG                       # neither direction
     st, _ = status_of(L, "q_blockwise_mx", A, Q.Q_BF16, 0, 128, Q.Q_T1x128, None, None, None, None, None, None)
     assert st == Q.Q_OK                            # empty: nothing to do
+
+
+def test_nvfp4_recipe_validation(L):
+    U64 = ctypes.c_uint64
+    args = lambda M, K, mask=0x1234, rnd=Q.Q_RN, amax_row=A: (A, Q.Q_BF16, M, K, mask, rnd, U64(0), U64(0), A, A,
+                                                           amax_row, A, A, A, A, A, None, None)
+    st, _ = status_of(L, "q_nvfp4_recipe", *args(32, 24))
+    assert st == Q.Q_ERR_SHAPE                     # K % 16
+    st, _ = status_of(L, "q_nvfp4_recipe", *args(24, 32))
+    assert st == Q.Q_ERR_SHAPE                     # M % 16
+    st, _ = status_of(L, "q_nvfp4_recipe", *args(32, 32, mask=0x10000))
+    assert st == Q.Q_ERR_ARG
+    st, _ = status_of(L, "q_nvfp4_recipe", *args(32, 32, rnd=2))
+    assert st == Q.Q_ERR_ARG
+    st, msg = status_of(L, "q_nvfp4_recipe", *args(32, 32, amax_row=None))
+    assert st == Q.Q_ERR_ARG and "amax_row" in msg
+    st, msg = status_of(L, "q_nvfp4_rht_amax2", A, Q.Q_BF16, 32, 32, 0x1234, A, ctypes.c_void_p(0x10002), None, None)
+    assert st == Q.Q_ERR_ALIGN and "amax_x" in msg
+    st, _ = status_of(L, "q_nvfp4_rht_amax2", A, Q.Q_BF16, 32, 40, 0x1234, A, A, None, None)
+    assert st == Q.Q_ERR_SHAPE
 
 
 def test_dequant_validation(L):

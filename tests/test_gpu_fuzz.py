@@ -202,3 +202,11 @@ def test_fuzz_rht_colT(recipe, i):
     same(host(got.s_global), np.float32(sg).reshape(1), "s_global")
     same(host(got.q_colT), q, "q_colT")
     same(host(got.sb_colT), sb, "sb_colT")
+    # the fused recipe: the same transposed copy, plus the rowwise copy of x
+    row, col = Q.q_nvfp4_recipe(dev(x), mask, "rn" if rnd == O.RN else "sr", seed, offset)
+    same(host(col.q_colT), q, "recipe q_colT")
+    same(host(col.sb_colT), sb, "recipe sb_colT")
+    w = O.nvfp4(x, O.B1x16, rnd, seed=seed, offset=offset, rowwise=True, colwise=False)
+    same(host(row.q_row), w.q_row, "recipe q_row")
+    same(host(row.sb_row), w.sb_row, "recipe sb_row")
+    same(host(row.s_global), np.float32(w.s_global).reshape(1), "recipe s_global_row")

@@ -129,6 +129,9 @@ def test_nvfp4_and_rht_stay_in_bounds(blk, rnd, shape):
         y = g.like(torch.empty((q.shape[0], q.shape[1] * 2), dtype=torch.bfloat16, device="cuda"))
         Q.dq_nvfp4(q, sb, out.s_global, blk, torch.bfloat16, out=y)
     if blk == "1x16":
+        rw = g.wrap(Q.alloc_nvfp4(*shape, "cuda", "1x16", True, False))
+        cl = g.wrap(Q.alloc_nvfp4(*shape, "cuda", "1x16", False, True))
+        Q.q_nvfp4_recipe(dev(x), 0x3C5A, rnd, 3, 0, out=(rw, cl))
         h = g.wrap(Q.alloc_nvfp4(*shape, "cuda", "1x16", False, True))
         Q.q_nvfp4_rht_colT(dev(x), 0x3C5A, rnd, 3, 0, out=h)
         a = g.like(torch.empty(1, device="cuda"))

@@ -207,6 +207,53 @@ def test_nvfp4_rht_colT_parity(kind, shape, bf16, rnd, mask):
     f32eq(got2.s_global.item(), sg2, "s_global, given amax")
 
 
+RECIPE_CASES = [
+    ("t3", (256, 512), True, O.SR, 0xB4E1, 9, 3),
+    ("outliers", (272, 528), True, O.RN, 0x5A5A, 0, 0),      # ragged tiles both ways
+    ("normal", (96, 160), False, O.SR, 0x0F0F, 77, 1000),    # FP32 input
+    ("lognormal_rows", (16, 16), True, O.RN, 0xFFFF, 0, 0),
+]
+
+
+@pytest.mark.parametrize("kind,shape,bf16,rnd,mask,seed,offset", RECIPE_CASES)
+def test_nvfp4_recipe_equals_its_two_calls(kind, shape, bf16, rnd, mask, seed, offset):
+    """The fused recipe (one amax pass for max|x| and max|x'|, the rowwise
+    copy of x, the columnwise copy of x') gives what q_nvfp4 (rowwise) and
+    q_nvfp4_rht_colT give, both checked against the oracle."""
+    x = W.gen(kind, shape, 616, bf16=bf16)
+    x[:16, :16] = 0
+    r = "rn" if rnd == O.RN else "sr"
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    row, col = Q.q_nvfp4_recipe(dev(x), mask, r, seed, offset, status=st)
+    torch.cuda.synchronize()
+    w = O.nvfp4(x, O.B1x16, rnd, seed=seed, offset=offset, rowwise=True, colwise=False)
+    f32eq(row.amax.item(), w.amax, "amax_row")
+    f32eq(row.s_global.item(), w.s_global, "s_global_row")
+    same(host(row.q_row), w.q_row, "q_row")
+    same(host(row.sb_row), w.sb_row, "sb_row")
+    q, sb, a, sg = O.nvfp4_rht_colT(x, mask, rnd, seed=seed, offset=offset)
+    f32eq(col.amax.item(), a, "amax_colT")
+    f32eq(col.s_global.item(), sg, "s_global_colT")
+    same(host(col.q_colT), q, "q_colT")
+    same(host(col.sb_colT), sb, "sb_colT")
+    assert st.item() == 0
+    a_rht, a_x = Q.q_nvfp4_rht_amax2(dev(x), mask)
+    f32eq(a_rht.item(), a, "amax2 rht")
+    f32eq(a_x.item(), O.amax(x), "amax2 x")
+
+
+def test_nvfp4_recipe_empty_and_nonfinite():
+    row, col = Q.q_nvfp4_recipe(torch.empty((0, 32), dtype=torch.bfloat16, device="cuda"), 0x1234)
+    assert row.amax.item() == 0 and col.amax.item() == 0
+    assert row.s_global.item() == 1 and col.s_global.item() == 1
+    x = W.gen("normal", (32, 48), 3, bf16=False)
+    x[5, 7] = np.nan
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a_rht, a_x = Q.q_nvfp4_rht_amax2(dev(x), 0x1234, status=st)
+    assert st.item() & Q.Q_ST_NONFINITE
+    assert np.isnan(a_x.item()) and np.float32(a_x.item()).view(np.uint32) == np.float32(O.amax(x)).view(np.uint32)
+
+
 def test_nvfp4_rht_colT_row_shards_with_the_global_amax():
     """Row shards on 16-row boundaries, each encoded with the maximum of the
     shards' transform amaxes, concatenate to the unsharded copy (RTNE)."""
