@@ -744,8 +744,10 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy; see workloads.WORKLOADS)",
             "config": {"workload": "all five workloads at full size per step: cs1 FP32 1024x1024 CS-E4M3+T; "
                                    "mx2 BF16 8192x4096 MXFP8 row+col, row->col requant; bw3 BF16 16384x7168 1x128+T and 7168x18432 "
-                                   "128x128+T; hy4 BF16 8192x14336 CS-E5M2+T, delayed-scaling E5M2+T (window 1024, max) and 14336x4096 CS-E4M3+T; nv5 BF16 "
-                                   "8192x4096 NVFP4 1x16 RN+T, 1x16 SR+T, 4096x4096 16x16 RN+T; each with a dequant; nv5 act/grad random-Hadamard NVFP4 colT (RN / SR)",
+                                   "128x128+T, each also held as MXFP8 (power-of-two scales); hy4 BF16 8192x14336 CS-E5M2+T, "
+                                   "delayed-scaling E5M2+T (window 1024, max) and 14336x4096 CS-E4M3+T; nv5 BF16 8192x4096 NVFP4 "
+                                   "1x16 RN+T, 1x16 SR+T, 4096x4096 16x16 RN+T; each with a dequant; nv5 act/grad random-Hadamard "
+                                   "NVFP4 colT (RN / SR); nv5 grad NVFP4 recipe (row SR + RHT colT SR, one amax pass)",
                        "l2": "flushed before every timed call (256 MiB write, then a 256 MiB read that evicts the dirty lines)",
                        "scale_rows": args.scale_rows, "parallelism": f"replicas x{world} (independent tensors)"},
             "parity": parity,

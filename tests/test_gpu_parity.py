@@ -714,3 +714,26 @@ def test_calls_on_two_streams_run_concurrently_and_match_the_oracle():
     w = O.mxfp8(x2)
     same(host(mx.q_col), w.q_col, "mx q_col")
     same(host(mx.e8m0_row), w.e8m0_row, "mx e8m0_row")
+
+
+def test_nvfp4_recipe_row_shards_with_the_global_maxima():
+    """Two row shards (16-row boundaries) that take their local maxima from
+    q_nvfp4_rht_amax2, reduce them with MAX and cast with the global values
+    give the unsharded recipe's outputs (RTNE; the shard helper itself runs
+    as one rank)."""
+    from nvfp4_quantization_current_gb300.distributed import quantize_shard_nvfp4_recipe
+    x = W.gen("outliers", (384, 256), 71, bf16=True)
+    whole_row, whole_col = Q.q_nvfp4_recipe(dev(x), 0x2D4B)
+    parts = [x[:144], x[144:]]
+    maxima = [Q.q_nvfp4_rht_amax2(dev(p), 0x2D4B) for p in parts]
+    a_rht = torch.maximum(maxima[0][0], maxima[1][0])
+    a_x = torch.maximum(maxima[0][1], maxima[1][1])
+    rows = [Q.q_nvfp4(dev(p), "1x16", "rn", rowwise=True, colwise=False, amax=a_x.clone()) for p in parts]
+    cols = [Q.q_nvfp4_rht_colT(dev(p), 0x2D4B, "rn", amax=a_rht.clone()) for p in parts]
+    same(np.concatenate([host(r.q_row) for r in rows]), host(whole_row.q_row), "q_row")
+    same(np.concatenate([host(r.sb_row) for r in rows]), host(whole_row.sb_row), "sb_row")
+    same(np.concatenate([host(c.q_colT) for c in cols], axis=1), host(whole_col.q_colT), "q_colT")
+    same(np.concatenate([host(c.sb_colT) for c in cols], axis=1), host(whole_col.sb_colT), "sb_colT")
+    r1, c1 = quantize_shard_nvfp4_recipe(dev(x), 0x2D4B)
+    same(host(r1.q_row), host(whole_row.q_row), "helper q_row")
+    same(host(c1.q_colT), host(whole_col.q_colT), "helper q_colT")
