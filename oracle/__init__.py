@@ -11,8 +11,9 @@ library's C ABI:
 * FP8 codes ``uint8`` [M, K] (rowwise) or [K, M] (columnwise, transposed);
 * NVFP4 codes ``uint8`` [M, K/2] / [K, M/2], two E2M1 codes per byte, even
   element in the low nibble;
-* scales: FP32 (current scaling, blockwise), E8M0 bytes (MXFP8), E4M3 bytes
-  (NVFP4 block scales) + one FP32 tensor scale.
+* scales: FP32 (current scaling, blockwise), E8M0 bytes (MXFP8, and
+  blockwise tiles held as MXFP8), E4M3 bytes (NVFP4 block scales) + one FP32
+  tensor scale.
 
 The arithmetic lives in ``oracle.c`` (plain loops, FP32 steps as single
 IEEE operations, no FMA contraction); its header lists the pages followed and
