@@ -737,3 +737,24 @@ def test_nvfp4_recipe_row_shards_with_the_global_maxima():
     r1, c1 = quantize_shard_nvfp4_recipe(dev(x), 0x2D4B)
     same(host(r1.q_row), host(whole_row.q_row), "helper q_row")
     same(host(c1.q_colT), host(whole_col.q_colT), "helper q_colT")
+
+
+def test_shard_helpers_on_one_rank_equal_the_plain_calls():
+    """Without torch.distributed the all-reduce is the identity, so each shard
+    helper must give exactly the unsharded call's outputs through the
+    library."""
+    from nvfp4_quantization_current_gb300 import distributed as D
+    x = dev(W.gen("outliers", (256, 384), 91, bf16=True))
+    a = D.quantize_shard_current_scaling(x, "e4m3", True, True)
+    b = Q.q_current_scaling(x, "e4m3", True, True)
+    same(host(a.q_row), host(b.q_row), "cs q_row")
+    same(host(a.q_colT), host(b.q_colT), "cs q_colT")
+    a = D.quantize_shard_nvfp4(x, "1x16", "sr", 5, 0, True, True)
+    b = Q.q_nvfp4(x, "1x16", "sr", 5, 0, True, True)
+    same(host(a.q_row), host(b.q_row), "nv q_row")
+    same(host(a.q_colT), host(b.q_colT), "nv q_colT")
+    a = D.quantize_shard_nvfp4_rht_colT(x, 0x1357, "rn")
+    b = Q.q_nvfp4_rht_colT(x, 0x1357, "rn")
+    same(host(a.q_colT), host(b.q_colT), "rht q_colT")
+    g = D.all_gather_quantized(b)
+    assert g.q_colT is b.q_colT
