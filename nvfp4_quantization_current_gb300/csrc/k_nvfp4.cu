@@ -487,7 +487,8 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
     const int g = threadIdx.x >> 6, q = threadIdx.x & 63;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
     uint32_t mx = 0;   // PASS 0: max |x'| bits of this thread (zero-filled rows and columns give 0)
-    uint32_t mxx = 0;  // PASS 0 with amax_x: max |x| bits of this thread (the untransformed tensor)
+    uint32_t mxx = 0;  // PASS 0 with amax_x: max |x| of this thread (the untransformed tensor), as k_amax takes
+                       // it: BF16 packed two per word, FP32 as a float
 
     run_tiles(&tmap, tiles_m, tiles_k, TC, PASS == 1, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
@@ -498,10 +499,10 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
 #pragma unroll
             for (int r = 0; r < 16; r++) {
                 if (DT == BF16)
-                    mxx = max(mxx, max(max((raw[r].x << 16) & 0x7FFF0000u, raw[r].x & 0x7FFF0000u),
-                                       max((raw[r].y << 16) & 0x7FFF0000u, raw[r].y & 0x7FFF0000u)));
+                    mxx = hmax_abs2(mxx, hmax_abs2(raw[r].x, raw[r].y));
                 else
-                    mxx = max(mxx, max(raw[r].x & 0x7FFFFFFFu, raw[r].y & 0x7FFFFFFFu));
+                    mxx = __float_as_uint(fmax_abs(fmax_abs(__uint_as_float(mxx), __uint_as_float(raw[r].x)),
+                                                   __uint_as_float(raw[r].y)));
             }
         }
         uint32_t code[CPT][2];   // per column: rows 16g..16g+7 and 16g+8..16g+15, first row in bits 3-0
@@ -593,6 +594,8 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
         griddep_wait();   // the zeroing of the amax words ahead of this pass is complete
         cta_max_to(mx, reinterpret_cast<uint32_t *>(amax), status);
         if (amax_x != nullptr) {
+            if (DT == BF16) mxx = (hmax_abs2(mxx, __byte_perm(mxx, 0u, 0x1032)) << 16) & 0x7FFF0000u;
+            else mxx &= 0x7FFFFFFFu;
             __syncthreads();   // the CTA reduction's shared words are free again
             cta_max_to(mxx, reinterpret_cast<uint32_t *>(amax_x), status);
         }
