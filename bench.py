@@ -72,11 +72,11 @@ TRAFFIC = {
     # profiles/k_mxfp8_requant_mx2_act.md
     "mx2.act:mxfp8_requant": {"bytes_per_launch": 34893312, "src_hash": "63030beb08e84bc3"},
     # profiles/k_nvfp4_1x16_rn_T_nv5_act.md
-    "nv5.act:nvfp4_1x16_rn": {"bytes_per_launch": 70868224, "src_hash": "58368dda3a5a9d30"},
+    "nv5.act:nvfp4_1x16_rn": {"bytes_per_launch": 71000320, "src_hash": "27db71b3293b653b"},
     # profiles/k_nvfp4_1x16_sr_T_nv5_grad.md
-    "nv5.grad:nvfp4_1x16_sr": {"bytes_per_launch": 71240960, "src_hash": "58368dda3a5a9d30"},
+    "nv5.grad:nvfp4_1x16_sr": {"bytes_per_launch": 71192320, "src_hash": "27db71b3293b653b"},
     # profiles/k_nvfp4_rht_sr_colT_nv5_grad.md
-    "nv5.grad:nvfp4_rht_colT_sr": {"bytes_per_launch": 69522176, "src_hash": "58368dda3a5a9d30"},
+    "nv5.grad:nvfp4_rht_colT_sr": {"bytes_per_launch": 69547264, "src_hash": "27db71b3293b653b"},
 }
 
 
