@@ -66,7 +66,7 @@ TRAFFIC = {
     # profiles/k_blockwise_mx_128x128T_bw3_w.md
     "bw3.w:bwmx_128x128_T": {"bytes_per_launch": 484780032, "src_hash": "6c3e28c748e48b9d"},
     # profiles/k_cs_tiles_e5m2T_hy4_grad.md
-    "hy4.grad:cs_cast_T": {"bytes_per_launch": 415887104, "src_hash": "6aea2a644b520ea9"},
+    "hy4.grad:cs_cast_T": {"bytes_per_launch": 416344064, "src_hash": "3ea9cf2821aea093"},
     # profiles/k_mxfp8_mx2_act.md
     "mx2.act:mxfp8": {"bytes_per_launch": 80998656, "src_hash": "63030beb08e84bc3"},
     # profiles/k_mxfp8_requant_mx2_act.md
