@@ -19,6 +19,14 @@ weight-gradient inputs all-reduces the amax of the transformed shard; shards
 that split rows on 16-row boundaries transform exactly like the slices of
 the whole tensor.
 
+Stochastic rounding draws depend only on an element's position in the
+whole tensor: element (m, k) takes its 16 random bits from Philox block
+offset + (m*K + k)/8 (rowwise) or offset + (m/8)*K + k (columnwise), so a
+rank whose shard starts at global row r0 passes offset + r0*K/8 and draws
+exactly what the unsharded call draws for those rows.  The ``quantize_shard_*``
+helpers do this by default (``row_base=None`` gathers the shard heights and
+takes the rank's first global row).
+
 After the local quantize, the shards' outputs may be all-gathered into the
 whole tensor's layout (the FP8 all-gather of the TP path): rowwise codes and
 scales concatenate by rows, the transposed copies by columns
@@ -47,6 +55,35 @@ def allreduce_amax_(amax: torch.Tensor, group=None) -> torch.Tensor:
     return amax
 
 
+def shard_row_base(rows_local: int, group=None, device=None) -> int:
+    """The global index of this rank's first row when the ranks hold
+    consecutive row shards in rank order (an exclusive prefix sum of the
+    shard heights, from one all-gather of an int64).  0 on a single rank."""
+    if not (dist.is_available() and dist.is_initialized()):
+        return 0
+    world = dist.get_world_size(group)
+    n = torch.tensor([int(rows_local)], dtype=torch.int64, device=device)
+    sizes = [torch.empty_like(n) for _ in range(world)]
+    dist.all_gather(sizes, n, group=group)
+    rank = dist.get_rank(group)
+    return int(sum(int(v.item()) for v in sizes[:rank]))
+
+
+def sr_offset(offset: int, row_base: int, K: int) -> int:
+    """The Philox counter offset for a row shard that starts at global row
+    ``row_base`` (a multiple of 8): the unsharded call's ``offset`` moved by
+    the row_base * K elements ahead of the shard (8 draws per counter)."""
+    if row_base % 8 != 0 or K % 8 != 0:
+        raise ValueError("row_base and K must be multiples of 8")
+    return int(offset) + int(row_base) * int(K) // 8
+
+
+def _shard_offset(x_local, offset, row_base, group):
+    if row_base is None:
+        row_base = shard_row_base(x_local.shape[0], group, x_local.device if x_local.is_cuda else None)
+    return sr_offset(offset, row_base, x_local.shape[1])
+
+
 def quantize_shard_current_scaling(x_local: torch.Tensor, fmt="e4m3", rowwise=True, colwise=False, group=None,
                                    status: Optional[torch.Tensor] = None):
     """Current scaling of this rank's row shard with the amax of the whole
@@ -58,39 +95,48 @@ def quantize_shard_current_scaling(x_local: torch.Tensor, fmt="e4m3", rowwise=Tr
 
 
 def quantize_shard_nvfp4_rht_colT(x_local: torch.Tensor, sign_mask: int, rounding="rn", seed=0, offset=0, group=None,
-                                  status: Optional[torch.Tensor] = None):
+                                  status: Optional[torch.Tensor] = None, row_base: Optional[int] = None):
     """The random-Hadamard NVFP4 columnwise copy of this rank's row shard
     (rows split on 16-row boundaries) with the amax of the whole transformed
-    tensor."""
+    tensor.  ``offset`` is the unsharded call's counter offset; the shard's
+    own is derived from ``row_base`` (this rank's first global row, gathered
+    when None), so stochastic draws match the unsharded copy."""
     from . import q_nvfp4_rht_amax, q_nvfp4_rht_colT
+    off = _shard_offset(x_local, offset, row_base, group)
     a = q_nvfp4_rht_amax(x_local, sign_mask, status=status)
     allreduce_amax_(a, group)
-    return q_nvfp4_rht_colT(x_local, sign_mask, rounding, seed, offset, amax=a, status=status)
+    return q_nvfp4_rht_colT(x_local, sign_mask, rounding, seed, off, amax=a, status=status)
 
 
 def quantize_shard_nvfp4(x_local: torch.Tensor, blk="1x16", rounding="rn", seed=0, offset=0, rowwise=True,
-                         colwise=False, group=None, status: Optional[torch.Tensor] = None):
+                         colwise=False, group=None, status: Optional[torch.Tensor] = None,
+                         row_base: Optional[int] = None):
     """NVFP4 of this rank's row shard with the global amax (so the FP32 tensor
     scale, and therefore every block scale, matches the unsharded tensor).
-    For stochastic rounding pass each rank its own counter ``offset``."""
+    ``offset`` is the unsharded call's counter offset; the shard's own is
+    derived from ``row_base`` (this rank's first global row, gathered when
+    None), so stochastic draws match the unsharded quantization."""
     from . import q_amax, q_nvfp4
+    off = _shard_offset(x_local, offset, row_base, group)
     a = q_amax(x_local, status=status)
     allreduce_amax_(a, group)
-    return q_nvfp4(x_local, blk, rounding, seed, offset, rowwise, colwise, amax=a, status=status)
+    return q_nvfp4(x_local, blk, rounding, seed, off, rowwise, colwise, amax=a, status=status)
 
 
 def quantize_shard_nvfp4_recipe(x_local: torch.Tensor, sign_mask: int, rounding="rn", seed=0, offset=0, group=None,
-                                status: Optional[torch.Tensor] = None):
+                                status: Optional[torch.Tensor] = None, row_base: Optional[int] = None):
     """Both NVFP4 recipe copies of this rank's row shard (rows split on 16-row
     boundaries): one read for the two local maxima, a MAX all-reduce of each,
     then the rowwise copy of x and the columnwise copy of its transform with
-    the global maxima.  Returns (row, colT) like q_nvfp4_recipe."""
+    the global maxima, both with the shard's counter offset (see
+    quantize_shard_nvfp4).  Returns (row, colT) like q_nvfp4_recipe."""
     from . import q_nvfp4, q_nvfp4_rht_amax2, q_nvfp4_rht_colT
+    off = _shard_offset(x_local, offset, row_base, group)
     a_rht, a_x = q_nvfp4_rht_amax2(x_local, sign_mask, status=status)
     allreduce_amax_(a_rht, group)
     allreduce_amax_(a_x, group)
-    row = q_nvfp4(x_local, "1x16", rounding, seed, offset, rowwise=True, colwise=False, amax=a_x, status=status)
-    col = q_nvfp4_rht_colT(x_local, sign_mask, rounding, seed, offset, amax=a_rht, status=status)
+    row = q_nvfp4(x_local, "1x16", rounding, seed, off, rowwise=True, colwise=False, amax=a_x, status=status)
+    col = q_nvfp4_rht_colT(x_local, sign_mask, rounding, seed, off, amax=a_rht, status=status)
     return row, col
 
 
@@ -128,8 +174,10 @@ def all_gather_quantized(t, group=None):
     BlockwiseMXTensor or NVFP4Tensor): rowwise fields gathered by rows, transposed copies by
     columns.  Shards must split rows on the recipe's block boundaries (32 for
     MXFP8 columnwise, 16 for NVFP4, 128 for the blockwise columnwise and 2-D
-    tiles) and, for current scaling and NVFP4, share the all-reduced amax, so
-    that the result equals the unsharded quantization.  Tensor-wide fields
+    tiles), for current scaling and NVFP4 share the all-reduced amax, and for
+    stochastic rounding use the counter offset of their first global row
+    (``sr_offset``; the ``quantize_shard_*`` helpers do both), so that the
+    result equals the unsharded quantization.  Tensor-wide fields
     (amax, scale, s_global) are the same on every rank and are kept."""
     upd = {}
     for f in dataclasses.fields(t):

@@ -35,7 +35,8 @@
  *   R-PACK   E2M1 packing: element 2j in bits 3-0, element 2j+1 in bits 7-4.
  *   R-SR     stochastic rounding on the E2M1 grid with 16 random bits per
  *            element drawn from Philox4x32-10 (see or_sr_e2m1 and
- *            or_philox_bits16).
+ *            or_philox_bits16), indexed by the element's position in x so
+ *            that row shards draw what the whole tensor draws (or_nvfp4).
  *   R-LAYOUT columnwise outputs of current scaling, blockwise and NVFP4 are
  *            stored transposed [K, M]; MXFP8 columnwise stays [M, K].
  *   R-AMAX   amax is the largest |x| bit pattern, which is the largest |x|
@@ -748,9 +749,18 @@ void or_dq_blockwise(const uint8_t *q, const float *s, int64_t R, int64_t C, int
  *   sb_colT [K, M/16] quantizes 16x1 blocks along M of each column.
  * blk 1 (16x16): q_row [M, K/2], sb_row [M/16, K/16]; q_colT [K, M/2] is the
  *   same codes transposed, sb_colT [K/16, M/16].
- * rnd 0: RTNE; rnd 1: stochastic rounding (R-SR) with stream 0 for the
- *   rowwise output (index m*K + k) and stream 1 for the 1x16 columnwise
- *   output (index k*M + m); a 16x16 transposed copy reuses the row codes.
+ * rnd 0: RTNE; rnd 1: stochastic rounding (R-SR).  The draw index of
+ *   element (m, k) of x depends only on its position in x and on K, never
+ *   on M, so a shard holding rows [r0, r0 + M) of a taller tensor draws
+ *   exactly what the whole tensor draws there when it passes
+ *   offset + r0 * K / 8 (r0 a multiple of 8); the quantized tensor is then
+ *   the same with or without the split ([MP] "FP8 communication", TP; [CS]
+ *   "Cost and multi-GPU use"):
+ *     rowwise (stream 0):    i = m * K + k          (row-major in x)
+ *     columnwise (stream 1): i = ((m / 8) * K + k) * 8 + m % 8
+ *                            (8-row groups of x, then columns, then rows)
+ *   so a Philox block (8 draws) covers 8 consecutive k of one row, or 8
+ *   consecutive m of one column; a 16x16 transposed copy reuses the row codes.
  */
 typedef struct { float alpha_g; int rnd; uint64_t seed, offset; } nv_ctx;
 
@@ -813,8 +823,8 @@ void or_nvfp4(const void *x, int dtype, int64_t M, int64_t K, int blk, int rnd,
                     sb_colT[k * (M / 16) + mb] = sb;
                     for (int j = 0; j < 16; j++) {
                         int64_t m = mb * 16 + j;
-                        int64_t it = k * M + m;
-                        put_nibble(q_colT, it, nv_code(&c, load_x(x, dtype, m * K + k), enc, 1, (uint64_t)it));
+                        int64_t draw = ((m / 8) * K + k) * 8 + m % 8;
+                        put_nibble(q_colT, k * M + m, nv_code(&c, load_x(x, dtype, m * K + k), enc, 1, (uint64_t)draw));
                     }
                 }
     } else {

@@ -1,9 +1,11 @@
 """The N > 1 path on CPU: two gloo ranks each hold a row shard, agree on the
 amax through the library's MAX all-reduce helper, quantize their shard with
 the CPU oracle, and the gathered codes must equal the unsharded oracle
-result bit for bit (per-tensor current scaling, NVFP4, two steps of delayed
-scaling with all-reduced window slots, and the random-Hadamard NVFP4
-columnwise copy with the all-reduced amax of the transform)."""
+result bit for bit (per-tensor current scaling, NVFP4 with round-to-nearest
+and with stochastic rounding (each rank's counter offset moved to its first
+global row), two steps of delayed scaling with all-reduced window slots, and
+the random-Hadamard NVFP4 columnwise copy with the all-reduced amax of the
+transform)."""
 import os
 import socket
 
@@ -27,7 +29,7 @@ def _worker(rank, world, port, result_dir):
     try:
         import oracle as O
         import workloads as W
-        from nvfp4_quantization_current_gb300.distributed import allreduce_amax_
+        from nvfp4_quantization_current_gb300.distributed import allreduce_amax_, shard_row_base, sr_offset
 
         x = W.gen("outliers", (256, 96), 17, bf16=True)
         cut = [0, 64, 256]                                  # uneven shards on 16-row boundaries
@@ -54,10 +56,19 @@ def _worker(rank, world, port, result_dir):
         ra = torch.tensor([O.amax(O.rht_cols(shard, mask))], dtype=torch.float32)
         allreduce_amax_(ra)
         rq, rsb, _, rsg = O.nvfp4_rht_colT(shard, mask, O.RN, amax_in=float(ra.item()))
+        # stochastic rounding: each rank moves the unsharded call's counter
+        # offset by its first global row, so its draws are the whole tensor's
+        r0 = shard_row_base(shard.shape[0])
+        assert r0 == cut[rank]
+        off = sr_offset(77, r0, shard.shape[1])
+        sr1 = O.nvfp4(shard, O.B1x16, O.SR, seed=9, offset=off, rowwise=True, colwise=True, amax_in=glob)
+        sr2 = O.nvfp4(shard, O.B16x16, O.SR, seed=9, offset=off, rowwise=True, colwise=True, amax_in=glob)
+        srq, srsb, _, _ = O.nvfp4_rht_colT(shard, mask, O.SR, seed=9, offset=off, amax_in=float(ra.item()))
         np.savez(os.path.join(result_dir, f"r{rank}.npz"), amax=np.float32(glob), cs_row=cs.q_row, cs_colT=cs.q_colT,
                  cs_s=cs.scale, nv_row=nv.q_row, nv_sb=nv.sb_row, nv_colT=nv.q_colT, nv_sbT=nv.sb_colT,
                  nv_sg=nv.s_global, ds0_row=ds[0], ds0_colT=ds[1], ds1_row=ds[2], ds1_colT=ds[3],
-                 rht_q=rq, rht_sb=rsb, rht_sg=np.float32(rsg))
+                 rht_q=rq, rht_sb=rsb, rht_sg=np.float32(rsg), sr1_row=sr1.q_row, sr1_colT=sr1.q_colT,
+                 sr2_row=sr2.q_row, sr2_colT=sr2.q_colT, srrht_q=srq, srrht_sb=srsb)
         dist.barrier()
     finally:
         dist.destroy_process_group()
@@ -97,6 +108,14 @@ def test_two_rank_amax_allreduce_matches_unsharded(tmp_path):
     assert np.array_equal(np.concatenate([q["rht_q"] for q in r], axis=1), rq)
     assert np.array_equal(np.concatenate([q["rht_sb"] for q in r], axis=1), rsb)
     assert r[0]["rht_sg"] == r[1]["rht_sg"] == rsg
+    # stochastic rounding: the gathered shards equal the unsharded call (seed 9, offset 77)
+    for blk, key in ((O.B1x16, "sr1"), (O.B16x16, "sr2")):
+        w = O.nvfp4(x, blk, O.SR, seed=9, offset=77, rowwise=True, colwise=True)
+        assert np.array_equal(np.concatenate([q[f"{key}_row"] for q in r]), w.q_row), key
+        assert np.array_equal(np.concatenate([q[f"{key}_colT"] for q in r], axis=1), w.q_colT), key
+    sq, ssb, _, _ = O.nvfp4_rht_colT(x, 0x6B1D, O.SR, seed=9, offset=77)
+    assert np.array_equal(np.concatenate([q["srrht_q"] for q in r], axis=1), sq)
+    assert np.array_equal(np.concatenate([q["srrht_sb"] for q in r], axis=1), ssb)
 
 
 def test_allreduce_amax_single_process_is_identity():
