@@ -55,29 +55,11 @@ CPU_SAMPLE_FRAC = 1.0 / 2.0
 REF_BUDGET_S = 120.0
 RHT_MASK = 0xB4E1   # the 16 random signs of the Hadamard transform (any fixed draw)
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
-# ncu capture, keyed by kernel, with the hash of the kernel's source file at
-# capture time; reported as null when the source has changed since.
-TRAFFIC = {
-    # profiles/k_blockwise_1x128T_bw3_act.md
-    "bw3.act:bw_1x128_T": {"bytes_per_launch": 421635328, "src_hash": "6c3e28c748e48b9d"},
-    # profiles/k_blockwise_128x128T_bw3_w.md
-    "bw3.w:bw_128x128_T": {"bytes_per_launch": 474617856, "src_hash": "6c3e28c748e48b9d"},
-    # profiles/k_blockwise_mx_128x128T_bw3_w.md
-    "bw3.w:bwmx_128x128_T": {"bytes_per_launch": 484780032, "src_hash": "6c3e28c748e48b9d"},
-    # profiles/k_cs_tiles_e5m2T_hy4_grad.md
-    "hy4.grad:cs_cast_T": {"bytes_per_launch": 416344064, "src_hash": "3ea9cf2821aea093"},
-    # profiles/k_mxfp8_mx2_act.md
-    "mx2.act:mxfp8": {"bytes_per_launch": 80998656, "src_hash": "63030beb08e84bc3"},
-    # profiles/k_mxfp8_requant_mx2_act.md
-    "mx2.act:mxfp8_requant": {"bytes_per_launch": 34893312, "src_hash": "63030beb08e84bc3"},
-    # profiles/k_nvfp4_1x16_rn_T_nv5_act.md
-    "nv5.act:nvfp4_1x16_rn": {"bytes_per_launch": 71000320, "src_hash": "27db71b3293b653b"},
-    # profiles/k_nvfp4_1x16_sr_T_nv5_grad.md
-    "nv5.grad:nvfp4_1x16_sr": {"bytes_per_launch": 71192320, "src_hash": "27db71b3293b653b"},
-    # profiles/k_nvfp4_rht_sr_colT_nv5_grad.md
-    "nv5.grad:nvfp4_rht_colT_sr": {"bytes_per_launch": 69547264, "src_hash": "27db71b3293b653b"},
-}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the kernel on the named call, with the hash of the kernel's
+# source (file + shared device headers) at capture time; reported as null
+# once the source has changed since.
+TRAFFIC = {}
 
 
 def src_hash(fname):
@@ -345,13 +327,14 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
         elif kind.startswith("rht"):
             rnd = O.SR if kind == "rht_sr" else O.RN
             A = O.amax(O.rht_cols(xh, RHT_MASK))
-            g = Q.q_nvfp4_rht_colT(xd, RHT_MASK, "sr" if rnd == O.SR else "rn", 4 if rnd == O.SR else 0, 0)
+            seed = 4 if rnd == O.SR else 0
+            g = Q.q_nvfp4_rht_colT(xd, RHT_MASK, "sr" if rnd == O.SR else "rn", seed, 0)
             eq(np.float32(g.amax.item()), np.float32(A), f"{wl}.{tn} rht amax")
-            q, sb, _, sg = O.nvfp4_rht_colT(xs, RHT_MASK, O.RN, amax_in=A)
+            # the band's draws: the whole tensor's counter offset moved by r0*K/8
+            q, sb, _, sg = O.nvfp4_rht_colT(xs, RHT_MASK, rnd, seed=seed, offset=r0 * K // 8, amax_in=A)
             eq(np.float32(g.s_global.item()), sg, f"{wl}.{tn} rht s_global")
             eq(host(g.sb_colT[:, r0 // 16:(r0 + rows) // 16]), sb, f"{wl}.{tn} rht sb_colT band")
-            if rnd == O.RN:   # SR draws depend on the full-height index k*M + m: scales only
-                eq(host(g.q_colT[:, r0 // 2:(r0 + rows) // 2]), q, f"{wl}.{tn} rht q_colT band")
+            eq(host(g.q_colT[:, r0 // 2:(r0 + rows) // 2]), q, f"{wl}.{tn} rht q_colT band")
         elif kind == "recipe_sr":
             A_x, A_r = O.amax(xh), O.amax(O.rht_cols(xh, RHT_MASK))
             row, col = Q.q_nvfp4_recipe(xd, RHT_MASK, "sr", 4, 0)
@@ -361,8 +344,9 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
             w = O.nvfp4(xs, O.B1x16, O.SR, seed=4, offset=r0 * K // 8, rowwise=True, colwise=False, amax_in=A_x)
             eq(host(row.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} recipe q_row band")
             eq(host(row.sb_row[r0:r0 + rows]), w.sb_row, f"{wl}.{tn} recipe sb_row band")
-            _, sb, _, _ = O.nvfp4_rht_colT(xs, RHT_MASK, O.RN, amax_in=A_r)
+            q, sb, _, _ = O.nvfp4_rht_colT(xs, RHT_MASK, O.SR, seed=4, offset=r0 * K // 8, amax_in=A_r)
             eq(host(col.sb_colT[:, r0 // 16:(r0 + rows) // 16]), sb, f"{wl}.{tn} recipe sb_colT band")
+            eq(host(col.q_colT[:, r0 // 2:(r0 + rows) // 2]), q, f"{wl}.{tn} recipe q_colT band")
         elif kind.startswith("cs"):
             fmt = O.E5M2 if kind == "cs_e5m2" else O.E4M3
             A = O.amax(xh)
@@ -413,21 +397,17 @@ def sampled_parity(host_tensors, dev_tensors, torch, Q, O, rows=128, seed=0):
             seed = 4 if rnd == O.SR else 0
             A = O.amax(xh)
             g = Q.q_nvfp4(xd, "16x16" if blk == O.B16x16 else "1x16", "sr" if rnd == O.SR else "rn", seed, 0, True, True)
-            # the rowwise stream of the band starts at element r0*K: a counter offset of r0*K/8
-            w = O.nvfp4(xs, blk, rnd, seed=seed, offset=r0 * K // 8, rowwise=True, colwise=(rnd == O.RN), amax_in=A)
+            # the band draws what the whole tensor draws there with the counter offset r0*K/8
+            w = O.nvfp4(xs, blk, rnd, seed=seed, offset=r0 * K // 8, rowwise=True, colwise=True, amax_in=A)
             eq(np.float32(g.s_global.item()), w.s_global, f"{wl}.{tn} s_global")
             eq(host(g.q_row[r0:r0 + rows]), w.q_row, f"{wl}.{tn} q_row band")
             if blk == O.B1x16:
                 eq(host(g.sb_row[r0:r0 + rows]), w.sb_row, f"{wl}.{tn} sb_row band")
             else:
                 eq(host(g.sb_row[r0 // 16:(r0 + rows) // 16]), w.sb_row, f"{wl}.{tn} sb band")
-            if rnd == O.RN:
-                eq(host(g.q_colT[:, r0 // 2:(r0 + rows) // 2]), w.q_colT, f"{wl}.{tn} q_colT band")
-            else:
-                # SR columnwise draws depend on the full-height index k*M + m: check the
-                # deterministic block scales of the band instead
-                w2 = O.nvfp4(xs, blk, O.RN, colwise=True, rowwise=False, amax_in=A)
-                eq(host(g.sb_colT[:, r0 // 16:(r0 + rows) // 16]), w2.sb_colT, f"{wl}.{tn} sb_colT band")
+            eq(host(g.q_colT[:, r0 // 2:(r0 + rows) // 2]), w.q_colT, f"{wl}.{tn} q_colT band")
+            if blk == O.B1x16:
+                eq(host(g.sb_colT[:, r0 // 16:(r0 + rows) // 16]), w.sb_colT, f"{wl}.{tn} sb_colT band")
     torch.cuda.synchronize()
     return checked
 

@@ -31,7 +31,12 @@
  * the caller orders a call after the producer of its inputs.
  *
  * Alignment: x, y and every code buffer must be 16-byte aligned; FP32 scale
- * buffers 4-byte aligned.
+ * buffers 4-byte aligned.  The byte-scale buffers of columnwise copies
+ * (e8m0_col of q_mxfp8 and q_mxfp8_requant_col, sb_colT of the NVFP4 calls,
+ * e8m0 of dq_mxfp8 with Q_COL) are written or read in 8- or 16-byte pieces
+ * and must be 16-byte aligned; the E8M0 buffers of q_blockwise_mx 4-byte
+ * aligned; other byte-scale buffers (e8m0_row, sb_row, sb of dq_nvfp4) have
+ * no alignment rule.  A violation returns Q_ERR_ALIGN before any launch.
  *
  * Errors: argument problems are detected on the host, before any launch,
  * and returned as a q_status (nothing is enqueued).  A failed launch returns
@@ -86,7 +91,9 @@ typedef enum { Q_HIST_MAX = 0, Q_HIST_MOST_RECENT = 1 } q_hist_algo;
 /* Thread-local message describing this thread's last failed call ("" if none). */
 const char *q_last_error(void);
 
-/* Version of this ABI (incremented on incompatible change). */
+/* Version of this ABI (incremented on incompatible change).  2: the
+ * stochastic-rounding draws of the columnwise NVFP4 copies are numbered by
+ * the element's position in x (see q_nvfp4), so results differ from 1. */
 int q_abi_version(void);
 
 /*
@@ -229,12 +236,17 @@ q_status q_blockwise_mx(const void *x, q_dtype in, int64_t M, int64_t K, q_tile 
  *   per block: sb = E4M3(RTNE((b * alpha_g) / 6)), b = 0 -> sb = 1.0;
  *              enc = alpha_g / sb (0 if sb == 0); q = E2M1(x * enc)
  *   rnd Q_RN: round to nearest even.  rnd Q_SR: stochastic rounding; the
- *   16 random bits of element i of an output come from Philox4x32-10 with
- *   key (seed lo, seed hi) and counter (g lo, g hi, stream, 0),
- *   g = offset + i / 8, word (i % 8) / 2, low half for even i; stream 0 for
- *   q_row (i = m*K + k), 1 for a 1x16 q_colT (i = k*M + m); it rounds up iff
- *   the 16 bits, as an integer, are below frac * 65536 where frac is the
- *   position of |x * enc| between its two neighbouring E2M1 values.
+ *   16 random bits of element (m, k) of x come from Philox4x32-10 with key
+ *   (seed lo, seed hi) and counter (g lo, g hi, stream, 0), g = offset + i / 8,
+ *   word (i % 8) / 2, low half for even i, where i is the draw index:
+ *   stream 0 (q_row):         i = m*K + k;
+ *   stream 1 (a 1x16 q_colT): i = ((m / 8)*K + k)*8 + m % 8.
+ *   It rounds up iff the 16 bits, as an integer, are below frac * 65536 where
+ *   frac is the position of |x * enc| between its two neighbouring E2M1
+ *   values.  The index depends on K but not on M: a row shard holding rows
+ *   [r0, r0 + M) of a taller tensor (r0 % 16 == 0) that passes
+ *   offset + r0*K/8 draws exactly what the unsharded call draws for those
+ *   rows, in both copies ([MP] "FP8 communication", TP).
  *   blk Q_B1x16 (activations, gradients):
  *     q_row [M, K/2], sb_row [M, K/16];  q_colT [K, M/2], sb_colT [K, M/16]
  *     (16x1 blocks along M of each column).
@@ -263,7 +275,7 @@ q_status q_nvfp4(const void *x, q_dtype in, int64_t M, int64_t K, q_nvblk blk, q
  * are the 16x1 blocks of the columnwise copy; H is orthogonal, so applying
  * the same transform to both wgrad operands leaves their product unchanged.
  * Then exactly the columnwise part of q_nvfp4 (Q_B1x16, rounding rnd,
- * stochastic draws of stream 1 indexed k * M + m) on x':
+ * stochastic draws of stream 1 indexed ((m / 8)*K + k)*8 + m % 8) on x':
  *   q_colT [K, M/2], sb_colT [K, M/16] (written);
  *   amax   one float: max|x'| written (Q_AMAX_COMPUTE, an extra read of x)
  *          or read (Q_AMAX_GIVEN, e.g. all-reduced over shards);
@@ -280,6 +292,17 @@ q_status q_nvfp4_rht_amax(const void *x, q_dtype in, int64_t M, int64_t K, uint3
 q_status q_nvfp4_rht_colT(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, q_round rnd,
                           uint64_t seed, uint64_t offset, uint8_t *q_colT, uint8_t *sb_colT,
                           float *amax, q_amax_mode amax_mode, float *s_global, int32_t *status, q_stream_t stream);
+
+/*
+ * Diagnostic of the host-side failure path (a library check, not an
+ * operation of the pages): the next n launches attempted by the calling
+ * thread fail as if the CUDA launch had returned cudaErrorLaunchFailure.
+ * The entry point that meets one returns Q_ERR_CUDA with q_last_error()
+ * naming the launch and the error, after its argument checks and before
+ * anything is enqueued.  n = 0 clears a pending injection; n < 0 is
+ * Q_ERR_ARG.
+ */
+q_status q_selftest_inject_launch_error(int n);
 
 /*
  * Diagnostic of the device-side failure path (a library check, not an

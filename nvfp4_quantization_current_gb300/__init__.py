@@ -67,6 +67,7 @@ SIGNATURES = {
     "q_delayed_scaling": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P, _P]),
     "q_delayed_scale_update": (_I, [_P, _I64, _I64, _I, _I, _P, _P]),
     "q_selftest_wait_timeout": (_I, [_P, _U64, _P]),
+    "q_selftest_inject_launch_error": (_I, [_I]),
     "q_mxfp8_requant_col": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
     "q_blockwise": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "q_blockwise_mx": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),

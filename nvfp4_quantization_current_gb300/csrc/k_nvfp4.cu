@@ -44,16 +44,20 @@ template <int BLK> constexpr int kTabCopies = BLK == 0 ? 16 : 1;
 // a_m in [1, 2), RN(RN(b alpha_g) / 6) = RN(RN((1 + m/128) a_m) / 6)
 // 2^(E-127+ae) while the values stay normal (rounding commutes with
 // power-of-two scaling), so it is a per-CTA 128-entry table plus an exponent
-// shift; anything that would fall below 2^-126 encodes to E4M3 +0 either way.
-// FP32 inputs and subnormal or non-finite b take the two operations.
+// shift; anything that would fall below 2^-126 encodes to E4M3 +0 either way,
+// and anything at or above 2^128 saturates to 448 (0x7E) either way.
+// FP32 inputs, subnormal or non-finite b, and an alpha_g that is 0 or NaN
+// (a non-finite tensor amax; ae is then kNoTable) take the two operations.
+constexpr int kNoTable = -100000;
 template <int DT, int C = 1> QD uint32_t nv_sb_code(uint32_t b, float alpha_g, const uint32_t *T1, int ae)
 {
     if (b == 0) return 0x38u;
     const uint32_t E = b >> 23;
-    if (DT == BF16 && E != 0u && E != 255u) {
+    if (DT == BF16 && E != 0u && E != 255u && ae != kNoTable) {
         const uint32_t t = T1[((b >> 16) & 0x7Fu) * C];
         const int ne = (int)(t >> 23) + (int)E - 127 + ae;
         if (ne <= 0) return 0u;
+        if (ne >= 255) return 0x7Eu;
         return e4m3_code(__uint_as_float((t & 0x807FFFFFu) | ((uint32_t)ne << 23)));
     }
     return e4m3_code(__fdiv_rn(__fmul_rn(__uint_as_float(b), alpha_g), 6.0f));
@@ -202,7 +206,10 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
     const float A = *amax;
     const float alpha_g = alpha_from_amax(2688.0f, A);
     const uint32_t ag = __float_as_uint(alpha_g);
-    const int ae = (int)(ag >> 23) - 127;   // alpha_g is always a normal float
+    // alpha_g = 2688 / A is a normal float for every finite A > 0 (and 1 for
+    // A = 0); a non-finite A gives 0 or NaN, which the table cannot scale
+    const bool ag_normal = (ag >> 23) != 0u && (ag >> 23) != 255u;
+    const int ae = ag_normal ? (int)(ag >> 23) - 127 : kNoTable;
     if (threadIdx.x < 128) {
         const float sv = e4m3_value(threadIdx.x);
         const float ev = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_g, sv);
@@ -273,7 +280,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                     const uint32_t kw = h < 2 ? k0 : k1;
                     const uint32_t bits = ((h & 1) ? kw : (kw << 16)) & 0x7FFF0000u;   // row rb + h
                     const uint32_t sb = nv_sb_code<DT, TCP>(bits, alpha_g, sbT, ae);
-                    own[h] = encT[sb * TCP];
+                    own[h] = encT[(sb & 0x7Fu) * TCP];
                     if (rb + h < nrows) {
                         sb_row[(m0 + rb + h) * (K / 16) + k / 16] = (uint8_t)sb;
                         nf |= nonfinite(bits);
@@ -301,7 +308,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                     for (int h = 0; h < 2; h++) {
                         const int64_t m = m0 + j + h;
                         const uint32_t sb = nv_sb_code<DT, TCP>(bb[h], alpha_g, sbT, ae);
-                        const uint32_t code = nv_row_codes<DT, RND>(v[j + h], encT[sb * TCP], seed, offset, m * K + k);
+                        const uint32_t code = nv_row_codes<DT, RND>(v[j + h], encT[(sb & 0x7Fu) * TCP], seed, offset, m * K + k);
                         const bool ok = m < M && kok;
                         if (ok) {
                             uint8_t *dst = q_row + m * (K / 2) + k / 2;
@@ -335,7 +342,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
             for (int c = 0; c < VEC; c++) {
                 const uint32_t b = colmax_bits<DT>(cm, c);
                 const uint32_t sb = nv_sb_code<DT, TCP>(b, alpha_g, sbT, ae);
-                const float enc = encT[sb * TCP];
+                const float enc = encT[(sb & 0x7Fu) * TCP];
                 if (RND == 0) sbw[c >> 2] |= sb << (8 * (c & 3));
                 else if ((warp & 1) == 0) sSB[warp >> 1][lane * VEC + c] = (uint8_t)sb;
                 nfc |= ((warp & 1) == 0 && kok && m0 < M) ? nonfinite(b) : 0u;
@@ -345,8 +352,8 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) mul2(y[j], y[j + 1], enc, enc);
                 if (RND == 1) {
-                    // elements (k + c) * M + m0 .. + 7 of stream 1: one Philox block
-                    const uint4 R = sr_bits(seed, offset + (uint64_t)(((k + c) * M + m0) >> 3), 1u);
+                    // rows m0 .. m0 + 7 of column k + c, stream 1: Philox block (m0 / 8) * K + k + c
+                    const uint4 R = sr_bits(seed, offset + (uint64_t)((m0 >> 3) * K + k + c), 1u);
 #pragma unroll
                     for (int j = 0; j < 8; j += 2) {
                         float r0, r1;
@@ -372,7 +379,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
             __syncthreads();   // half-block maxima posted; every read of the stage is done
             b = max(bred[warp & ~1][lane / LPB], bred[warp | 1][lane / LPB]);
             const uint32_t sb = nv_sb_code<DT, TCP>(b, alpha_g, sbT, ae);
-            const float enc = encT[sb * TCP];
+            const float enc = encT[(sb & 0x7Fu) * TCP];
             const int64_t m16 = mb + 16 * (warp >> 1);
             if ((warp & 1) == 0 && lane % LPB == 0 && m16 < M && kok) {
                 if (sb_row != nullptr) sb_row[(m16 / 16) * (K / 16) + k / 16] = (uint8_t)sb;
@@ -542,7 +549,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
             }
             const uint32_t ba = __float_as_uint(ma) & 0x7FFFFFFFu, bb = __float_as_uint(mbx) & 0x7FFFFFFFu;
             const uint32_t sa = nv_sb_code<F32>(ba, alpha_g, nullptr, 0), sbb = nv_sb_code<F32>(bb, alpha_g, nullptr, 0);
-            const float ea = enc_tab[sa], eb = enc_tab[sbb];
+            const float ea = enc_tab[sa & 0x7Fu], eb = enc_tab[sbb & 0x7Fu];
             const int c0 = q * CPT + 2 * p;   // tile column of a
             sSB[g][c0] = (uint8_t)sa;
             sSB[g][c0 + 1] = (uint8_t)sbb;
@@ -551,12 +558,14 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
 #pragma unroll
             for (int i = 0; i < 16; i++) mul2(a[i], b[i], ea, eb);
             if constexpr (RND == 1) {
-                // elements k * M + m of the transposed layout, stream 1: two Philox blocks per column
+                // rows m .. m + 15 of columns kb + c0, kb + c0 + 1, stream 1: Philox blocks
+                // (m / 8 + hh) * K + column, two per column
                 const int64_t m = mb + 16 * g;
 #pragma unroll
                 for (int hh = 0; hh < 2; hh++) {
-                    const uint4 Ra = sr_bits(seed, offset + (uint64_t)(((kb + c0) * M + m + 8 * hh) >> 3), 1u);
-                    const uint4 Rb = sr_bits(seed, offset + (uint64_t)(((kb + c0 + 1) * M + m + 8 * hh) >> 3), 1u);
+                    const uint64_t gb = offset + (uint64_t)(((m >> 3) + hh) * K + kb + c0);
+                    const uint4 Ra = sr_bits(seed, gb, 1u);
+                    const uint4 Rb = sr_bits(seed, gb + 1, 1u);
                     float ra[8], rb[8];
                     r16_block(Ra, ra);
                     r16_block(Rb, rb);

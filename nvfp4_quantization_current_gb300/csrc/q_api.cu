@@ -69,10 +69,19 @@ q_status check_out(const char *fn, q_dtype out)
         if (s_ != Q_OK) return s_;     \
     } while (0)
 
-#define LAUNCH(where, expr)                            \
-    do {                                               \
-        cudaError_t e_ = (expr);                       \
-        if (e_ != cudaSuccess) return cuda_fail(where, e_); \
+// Launch failures injected by q_selftest_inject_launch_error: the next n
+// launches of this thread fail with cudaErrorLaunchFailure before anything is
+// enqueued (the error path of every entry point, exercised without a GPU).
+thread_local int g_inject_launch_failures = 0;
+
+#define LAUNCH(where, expr)                                                \
+    do {                                                                   \
+        if (g_inject_launch_failures > 0) {                                \
+            g_inject_launch_failures--;                                    \
+            return cuda_fail(where, cudaErrorLaunchFailure);               \
+        }                                                                  \
+        cudaError_t e_ = (expr);                                           \
+        if (e_ != cudaSuccess) return cuda_fail(where, e_);                \
     } while (0)
 
 cudaStream_t S(q_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -83,7 +92,7 @@ extern "C" {
 
 const char *q_last_error(void) { return g_err; }
 
-int q_abi_version(void) { return 1; }
+int q_abi_version(void) { return 2; }
 
 q_status q_amax(const void *x, q_dtype in, int64_t n, float *amax, int32_t *status, q_stream_t stream)
 {
@@ -330,7 +339,7 @@ q_status q_nvfp4_recipe(const void *x, q_dtype in, int64_t M, int64_t K, uint32_
         TRY(need(fn, "q_row", q_row, 16));
         TRY(need(fn, "sb_row", sb_row, 1));
         TRY(need(fn, "q_colT", q_colT, 16));
-        TRY(need(fn, "sb_colT", sb_colT, 1));
+        TRY(need(fn, "sb_colT", sb_colT, 16));   // written in 8-byte pieces
     }
     // one read for both maxima, then the rowwise cast and the transformed columnwise cast with them
     LAUNCH(fn, qk::launch_rht_amax(x, (int)in, M, K, sign_mask, amax_colT, amax_row, status, S(stream)));
@@ -361,6 +370,13 @@ q_status q_nvfp4_rht_colT(const void *x, q_dtype in, int64_t M, int64_t K, uint3
     TRY(need(fn, "s_global", s_global, 4));
     LAUNCH(fn, qk::launch_nvfp4_rht_colT(x, (int)in, M, K, sign_mask, (int)rnd, seed, offset, amax_mode == Q_AMAX_COMPUTE,
                                          amax, q_colT, sb_colT, s_global, status, S(stream)));
+    return Q_OK;
+}
+
+q_status q_selftest_inject_launch_error(int n)
+{
+    if (n < 0) return fail(Q_ERR_ARG, "q_selftest_inject_launch_error: n = %d is negative", n);
+    g_inject_launch_failures = n;
     return Q_OK;
 }
 

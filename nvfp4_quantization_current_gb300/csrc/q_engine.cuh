@@ -14,11 +14,15 @@
 //
 // Every wait is bounded: a thread polls the stage barrier with try_wait and
 // gives up after kWaitNs of %globaltimer.  A thread that gives up ORs
-// Q_ST_TIMEOUT into the status word and carries on with the same control
-// flow as the others (every barrier of the bodies is still reached by all
-// threads; the outputs of such a launch are not meaningful).  After the last
-// tile thread 0 waits (bounded again) for any copy it saw time out, so that
-// no copy is in flight when the CTA's shared memory goes away.
+// Q_ST_TIMEOUT into the status word, raises the CTA's abort flag and runs
+// the rest of the tile with the others (every barrier of the body is still
+// reached by all threads; the outputs of such a launch are not meaningful).
+// At the end of that tile the whole CTA sees the flag and leaves the loop:
+// no further copy is issued.  Thread 0 then waits (bounded again) for every
+// copy it issued and did not see complete, so that no copy is in flight when
+// the CTA's shared memory goes away -- unless one of those waits also runs
+// out, in which case the CTA exits anyway and the status word already says
+// Q_ST_TIMEOUT.
 #pragma once
 
 #include <atomic>
@@ -179,25 +183,32 @@ __device__ __forceinline__ void run_tiles(const CUtensorMap *tmap, int64_t tiles
     if (threadIdx.x == 0)
         for (int64_t i = 0; i < count && i < kStages; i++) issue(i, (int)i);
 
-    int64_t late = -1;   // thread 0: the first tile whose wait it gave up on
+    // Tile i is issued before iteration i - kStages + 1 at the latest, so when
+    // the loop leaves after tile i the copies of tiles i + 1 .. i + kStages - 1
+    // are outstanding, and tile i's own if thread 0's wait for it gave up.
+    int64_t drain_from = -1, drain_to = -1;
     for (int64_t i = 0; i < count; i++) {
         const int s = (int)(i % kStages);
-        if (!mbar_wait_bounded(&full[s], (uint32_t)((i / kStages) & 1))) {
-            if (status != nullptr) atomicOr(status, kStTimeout);
-            if (threadIdx.x == 0 && late < 0) late = i;
-        }
+        const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / kStages) & 1));
+        if (!ok && status != nullptr) atomicOr(status, kStTimeout);
         const int64_t t = tile_of(i);
         const int64_t tm = t / tiles_k, tk = t - tm * tiles_k;
         body(dsm + s * kTileBytes, tm, tk);
-        __syncthreads();   // every thread is done with the stage
+        // every thread is done with the stage; any wait of this tile that gave up stops the whole CTA
+        if (__syncthreads_or(!ok)) {
+            drain_from = ok ? i + 1 : i;
+            drain_to = i + kStages - 1 < count - 1 ? i + kStages - 1 : count - 1;
+            break;
+        }
         if (threadIdx.x == 0 && i + kStages < count) {
             fence_proxy_async();   // generic-proxy accesses of the stage before the async-proxy refill
             issue(i + kStages, s);
         }
     }
-    if (threadIdx.x == 0 && late >= 0) {
-        // let copies that were still in flight land before the CTA's shared memory goes away
-        for (int64_t j = late; j < count; j++) (void)mbar_wait_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1));
+    if (threadIdx.x == 0 && drain_from >= 0) {
+        // copies still in flight land before the CTA's shared memory goes away
+        for (int64_t j = drain_from; j <= drain_to; j++)
+            (void)mbar_wait_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1));
     }
 }
 

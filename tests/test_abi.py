@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
               "q_mxfp8_requant_col", "q_blockwise", "q_blockwise_mx", "q_nvfp4", "q_nvfp4_rht_amax",
               "q_nvfp4_rht_colT", "q_nvfp4_rht_amax2", "q_nvfp4_recipe",
               "dq_current_scaling", "dq_mxfp8", "dq_blockwise",
-              "dq_nvfp4", "q_last_error", "q_abi_version"]:
+              "dq_nvfp4", "q_last_error", "q_abi_version", "q_selftest_inject_launch_error"]:
         assert n in names
 
 
@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
     for n in declared_functions():
         assert hasattr(L, n), n
         assert n in Q.SIGNATURES, n
-    assert L.q_abi_version() == 1
+    assert L.q_abi_version() == 2
 
 
 A = ctypes.c_void_p(0x10000)        # an aligned non-NULL address that is never dereferenced
@@ -218,3 +218,75 @@ def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError, match="CUDA"):
         Q.q_current_scaling(torch.zeros(4, 16))
+
+
+def test_nvfp4_columnwise_scale_buffers_need_16_byte_alignment(L):
+    """sb_colT is written in 8-byte pieces by every NVFP4 entry point that
+    produces it, so a 1-byte-aligned pointer is refused on the host."""
+    U64 = ctypes.c_uint64
+    odd = ctypes.c_void_p(0x10001)
+    st, msg = status_of(L, "q_nvfp4_recipe", A, Q.Q_BF16, 32, 32, 0x1234, Q.Q_RN, U64(0), U64(0), A, A, A, A,
+                        A, odd, A, A, None, None)
+    assert st == Q.Q_ERR_ALIGN and "sb_colT" in msg
+    st, msg = status_of(L, "q_nvfp4", A, Q.Q_BF16, 16, 32, Q.Q_B1x16, Q.Q_RN, 0, 0, None, None, A, odd, A, 0, A,
+                        None, None)
+    assert st == Q.Q_ERR_ALIGN and "sb_colT" in msg
+    st, msg = status_of(L, "q_nvfp4_rht_colT", A, Q.Q_BF16, 32, 32, 0x1, Q.Q_RN, 0, 0, A, odd, A, 0, A, None, None)
+    assert st == Q.Q_ERR_ALIGN and "sb_colT" in msg
+
+
+def _valid_calls():
+    """One argument list per launching entry point that passes every host
+    check (A is aligned and never dereferenced: the injected failure stops
+    the call before anything is enqueued)."""
+    U64 = ctypes.c_uint64
+    return {
+        "q_amax": (A, Q.Q_BF16, 64, A, None, None),
+        "q_current_scaling": (A, Q.Q_BF16, 16, 16, Q.Q_E4M3, A, A, A, Q.Q_AMAX_COMPUTE, A, None, None),
+        "q_delayed_scaling": (A, Q.Q_BF16, 16, 16, Q.Q_E4M3, A, A, A, A, A, None, None),
+        "q_delayed_scale_update": (A, 16, 3, Q.Q_HIST_MAX, Q.Q_E4M3, A, None),
+        "q_mxfp8": (A, Q.Q_BF16, 32, 32, Q.Q_E4M3, A, A, A, A, None, None),
+        "q_mxfp8_requant_col": (A, A, 32, 32, Q.Q_E4M3, A, A, None, None),
+        "q_blockwise": (A, Q.Q_BF16, 128, 128, Q.Q_T1x128, A, A, A, A, None, None),
+        "q_blockwise_mx": (A, Q.Q_BF16, 128, 128, Q.Q_T1x128, A, A, A, A, None, None),
+        "q_nvfp4": (A, Q.Q_BF16, 16, 32, Q.Q_B1x16, Q.Q_SR, 1, 0, A, A, A, A, A, Q.Q_AMAX_COMPUTE, A, None, None),
+        "q_nvfp4_rht_amax": (A, Q.Q_BF16, 16, 16, 0x1, A, None, None),
+        "q_nvfp4_rht_amax2": (A, Q.Q_BF16, 16, 16, 0x1, A, A, None, None),
+        "q_nvfp4_rht_colT": (A, Q.Q_BF16, 16, 16, 0x1, Q.Q_RN, 0, 0, A, A, A, Q.Q_AMAX_COMPUTE, A, None, None),
+        "q_nvfp4_recipe": (A, Q.Q_BF16, 16, 16, 0x1, Q.Q_RN, U64(0), U64(0), A, A, A, A, A, A, A, A, None, None),
+        "q_selftest_wait_timeout": (A, 1000, None),
+        "dq_current_scaling": (A, A, 4, 4, Q.Q_E4M3, Q.Q_F32, A, None),
+        "dq_mxfp8": (A, A, 4, 32, Q.Q_E4M3, Q.Q_ROW, Q.Q_F32, A, None),
+        "dq_blockwise": (A, A, 4, 128, Q.Q_T1x128, Q.Q_F32, A, None),
+        "dq_nvfp4": (A, A, A, 4, 32, Q.Q_B1x16, Q.Q_F32, A, None),
+    }
+
+
+def test_injected_launch_failure_returns_q_err_cuda(L):
+    """A CUDA launch failure reaches the caller as Q_ERR_CUDA with a message
+    naming the entry point and the CUDA error, from every entry point that
+    launches (failures injected on the host: no GPU, nothing enqueued)."""
+    calls = _valid_calls()
+    declared = set(declared_functions())
+    launching = declared - {"q_last_error", "q_abi_version", "q_selftest_inject_launch_error"}
+    assert launching == set(calls)
+    try:
+        for name, args in calls.items():
+            assert L.q_selftest_inject_launch_error(1) == Q.Q_OK
+            st, msg = status_of(L, name, *args)
+            assert st == Q.Q_ERR_CUDA, (name, st, msg)
+            assert name in msg and "cudaErrorLaunchFailure" in msg, (name, msg)
+        # n failures are consumed one launch at a time
+        assert L.q_selftest_inject_launch_error(2) == Q.Q_OK
+        for _ in range(2):
+            st, _ = status_of(L, "q_amax", *calls["q_amax"])
+            assert st == Q.Q_ERR_CUDA
+        # the binding raises QuantError carrying the status
+        assert L.q_selftest_inject_launch_error(1) == Q.Q_OK
+        with pytest.raises(Q.QuantError) as ei:
+            Q._call("dq_nvfp4", *calls["dq_nvfp4"])
+        assert ei.value.status == Q.Q_ERR_CUDA
+        st, msg = status_of(L, "q_selftest_inject_launch_error", -1)
+        assert st == Q.Q_ERR_ARG and "negative" in msg
+    finally:
+        L.q_selftest_inject_launch_error(0)

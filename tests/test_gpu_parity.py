@@ -640,6 +640,51 @@ def test_nvfp4_sr_unbiased_on_the_gpu_over_1e7_draws():
         assert np.all(np.abs(mean - P) <= 5 * sigma + 1e-6), name
 
 
+def _f32_same_or_both_nan(a, b, what):
+    a, b = np.float32(a), np.float32(b)
+    if np.isnan(a) or np.isnan(b):
+        assert np.isnan(a) and np.isnan(b), (what, a, b)
+    else:
+        f32eq(a, b, what)
+
+
+@pytest.mark.parametrize("blk", [O.B1x16, O.B16x16])
+@pytest.mark.parametrize("rnd", [O.RN, O.SR])
+@pytest.mark.parametrize("case", ["inf", "nan", "given_amax_below_block_max"])
+def test_nvfp4_bf16_nonfinite_and_overflowing_scales_match_the_oracle(case, rnd, blk):
+    """BF16 inputs whose tensor amax is inf or NaN (the FP32 tensor scale is
+    then 0 or NaN), and a caller-given amax far below a block's maximum (the
+    block scale's product overflows FP32): every code and scale byte still
+    follows the oracle's IEEE rules, and Q_ST_NONFINITE is reported."""
+    x = W.gen("normal", (64, 96), 808, bf16=True)
+    xf = W.bf16_bits_to_f32(x)
+    big = np.float32(3.0e38)
+    xf[5, 7] = big                                   # huge finite values in other blocks
+    xf[40, 70] = -big
+    amax_in = None
+    if case == "inf":
+        xf[20, 33] = np.inf
+    elif case == "nan":
+        xf[20, 33] = np.nan
+    else:
+        amax_in = 1.0e-30                            # b * alpha_g overflows for every block
+    x = O.bf16_round(xf)
+    want = O.nvfp4(x, blk, rnd, seed=3, offset=11, rowwise=True, colwise=True, amax_in=amax_in)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = None if amax_in is None else torch.tensor([amax_in], dtype=torch.float32, device="cuda")
+    got = Q.q_nvfp4(dev(x), "1x16" if blk == O.B1x16 else "16x16", "rn" if rnd == O.RN else "sr", seed=3,
+                    offset=11, rowwise=True, colwise=True, amax=a, status=st)
+    torch.cuda.synchronize()
+    _f32_same_or_both_nan(got.amax.item(), want.amax, "amax")
+    _f32_same_or_both_nan(got.s_global.item(), want.s_global, "s_global")
+    same(host(got.sb_row), want.sb_row, "sb_row")
+    same(host(got.q_row), want.q_row, "q_row")
+    same(host(got.sb_colT), want.sb_colT, "sb_colT")
+    same(host(got.q_colT), want.q_colT, "q_colT")
+    if case != "given_amax_below_block_max":
+        assert st.item() & Q.Q_ST_NONFINITE
+
+
 def test_nvfp4_single_direction_and_given_amax():
     x = W.gen("t3", (128, 256), 5, bf16=True)
     a = Q.q_amax(dev(x)) * 2          # a larger (e.g. all-reduced) amax
