@@ -19,8 +19,10 @@ bytes; reads = 2 for current scaling and NVFP4, whose amax pass reads the
 tensor once more, 1 otherwise) / device time, summed over the step.  L2 is
 flushed before every timed call: a 256 MiB write, then a 256 MiB read of
 another buffer, which evicts the written lines so that their write-back is
-not charged to the call.  The time of a call is taken with CUDA events on
-the launching stream around that call only.
+not charged to the call.  The time of a call is taken with one pair of CUDA
+events on the launching stream around that call only (its kernels overlap as
+they do for a caller).  A second timed region of the same K steps records an
+event after every kernel for the per-kernel breakdown and the roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -199,7 +201,7 @@ def build_step(dev_tensors, torch, Q):
         outs = nbytes(out.q_row, out.sb_row, out.q_colT, out.sb_colT, out.s_global)
         pieces = [
             ("amax", "k_current_scaling.cu", ins, lambda: Q.q_amax(x, out=amax)),
-            (f"nvfp4_{blk}_{rnd}", "k_nvfp4.cu", ins + outs + 4,
+            (f"nvfp4_{blk}_{rnd}", "k_nvfp4_bf16.cu" if x.dtype == torch.bfloat16 else "k_nvfp4.cu", ins + outs + 4,
              lambda: Q.q_nvfp4(x, blk, rnd, seed, 0, True, True, amax=amax, out=out)),
         ]
 
@@ -240,7 +242,8 @@ def build_step(dev_tensors, torch, Q):
         ins = nbytes(x)
         pieces = [
             ("rht_amax2", "k_nvfp4.cu", ins, lambda: Q.q_nvfp4_rht_amax2(x, mask, out=(col.amax, row.amax))),
-            (f"nvfp4_row_{rnd}", "k_nvfp4.cu", ins + nbytes(row.q_row, row.sb_row, row.s_global) + 4,
+            (f"nvfp4_row_{rnd}", "k_nvfp4_bf16.cu" if x.dtype == torch.bfloat16 else "k_nvfp4.cu",
+             ins + nbytes(row.q_row, row.sb_row, row.s_global) + 4,
              lambda: Q.q_nvfp4(x, "1x16", rnd, seed, 0, True, False, amax=row.amax, out=row)),
             (f"nvfp4_rht_colT_{rnd}", "k_nvfp4.cu", ins + nbytes(col.q_colT, col.sb_colT, col.s_global) + 4,
              lambda: Q.q_nvfp4_rht_colT(x, mask, rnd, seed, 0, amax=col.amax, out=col)),
@@ -530,7 +533,11 @@ def run_ours(args):
     # that no call's events include host submission latency.
     head_start = int(2e-3 * 2.0e9)
 
-    def one_step(evs):
+    def one_step(evs, per_kernel):
+        """One pass over every call.  per_kernel False (the step): one event
+        pair around each call, so the kernels of a call overlap as they do for
+        a caller (programmatic dependent launch); True (the breakdown): an
+        event after every kernel of a call, which serializes them."""
         torch.cuda._sleep(head_start)
         for ci, c in enumerate(calls):
             flush.fill_(float(ci))
@@ -538,45 +545,50 @@ def run_ours(args):
             evs[ci][0].record(stream)
             for pi, p in enumerate(c.pieces):
                 p[3]()
-                evs[ci][pi + 1].record(stream)
+                if per_kernel:
+                    evs[ci][pi + 1].record(stream)
+            if not per_kernel:
+                evs[ci][1].record(stream)
 
-    def new_events():
-        return [[torch.cuda.Event(enable_timing=True) for _ in range(len(c.pieces) + 1)] for c in calls]
+    def new_events(per_kernel):
+        return [[torch.cuda.Event(enable_timing=True) for _ in range((len(c.pieces) if per_kernel else 1) + 1)]
+                for c in calls]
 
     for w in range(args.warmup):
-        one_step(new_events())
+        one_step(new_events(w % 2 == 1), w % 2 == 1)
         if w == 0:   # the producers' outputs exist now: fill the consumers' own inputs
             for c in calls:
                 if c.prime is not None:
                     c.prime()
     torch.cuda.synchronize()
 
-    all_evs = [new_events() for _ in range(args.steps)]
     props = torch.cuda.get_device_properties(dev)
     uuid = getattr(props, "uuid", None)
-    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
-    sampler.start()
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for s in range(args.steps):
-        one_step(all_evs[s])
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
 
-    # per-kernel and per-call device times
-    kern_ms = {}      # (call index, piece index) -> list of ms
-    for s in range(args.steps):
-        for ci, c in enumerate(calls):
-            ev = all_evs[s][ci]
-            for pi in range(len(c.pieces)):
-                kern_ms.setdefault((ci, pi), []).append(ev[pi].elapsed_time(ev[pi + 1]))
-    step_ms = sum(statistics.mean(v) for v in kern_ms.values())
+    def timed(per_kernel):
+        """K steps between a barrier + synchronize on both sides, with the SM
+        clocks sampled meanwhile; returns (events, wall seconds, clocks)."""
+        all_evs = [new_events(per_kernel) for _ in range(args.steps)]
+        sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+        sampler.start()
+        time.sleep(0.3)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            one_step(all_evs[s], per_kernel)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        if world > 1:
+            dist.barrier()
+        return all_evs, wall, sampler.stop()
+
+    # the step: K steps timed call by call
+    step_evs, wall, clocks = timed(False)
+    call_ms = {ci: [step_evs[s][ci][0].elapsed_time(step_evs[s][ci][1]) for s in range(args.steps)]
+               for ci in range(len(calls))}
+    step_ms = sum(statistics.mean(v) for v in call_ms.values())
     step_bytes = sum(c.alg_bytes for c in calls)
     if world > 1:
         t = torch.tensor([step_ms], device=dev)
@@ -584,12 +596,21 @@ def run_ours(args):
         step_ms = float(t.item())
     value = step_bytes * world / (step_ms * 1e-3) / 1e9
 
+    # the breakdown: K more steps with an event after every kernel
+    brk_evs, brk_wall, brk_clocks = timed(True)
+    kern_ms = {}      # (call index, piece index) -> list of ms
+    for s in range(args.steps):
+        for ci, c in enumerate(calls):
+            ev = brk_evs[s][ci]
+            for pi in range(len(c.pieces)):
+                kern_ms.setdefault((ci, pi), []).append(ev[pi].elapsed_time(ev[pi + 1]))
+
     peak, peak_kind = measured_peak()
     per_call = []
     per_recipe = {}
     per_kernel = {}
     for ci, c in enumerate(calls):
-        ms = sum(statistics.mean(kern_ms[(ci, pi)]) for pi in range(len(c.pieces)))
+        ms = statistics.mean(call_ms[ci])
         gbs = c.alg_bytes / (ms * 1e-3) / 1e9
         per_call.append({"call": c.name, "us": round(ms * 1e3, 2), "bytes": c.alg_bytes, "GB/s": round(gbs, 1),
                          "frac": round(gbs / peak, 3),
@@ -729,6 +750,8 @@ def run_ours(args):
                                    "1x16 RN+T, 1x16 SR+T, 4096x4096 16x16 RN+T; each with a dequant; nv5 act/grad random-Hadamard "
                                    "NVFP4 colT (RN / SR); nv5 grad NVFP4 recipe (row SR + RHT colT SR, one amax pass)",
                        "l2": "flushed before every timed call (256 MiB write, then a 256 MiB read that evicts the dirty lines)",
+                       "timing": "one CUDA event pair around each call on its stream (the kernels of a call overlap "
+                                 "as they do for a caller); value = step bytes / sum of call times",
                        "scale_rows": args.scale_rows, "parallelism": f"replicas x{world} (independent tensors)"},
             "parity": parity,
             "roofline": roofline,
@@ -743,6 +766,9 @@ def run_ours(args):
             "e2e": e2e,
             "gpu_launches": n_launches,
             "clocks": clocks,
+            "breakdown": {"what": "per_kernel, per_call kernels and roofline: K more steps with a CUDA event after "
+                                  "every kernel (which serializes the kernels of a call)",
+                          "steps": args.steps, "clocks": brk_clocks, "wall_s_timed": round(brk_wall, 3)},
             "wall_s_timed": round(wall, 3),
         }
         print(json.dumps(line), flush=True)

@@ -31,67 +31,24 @@
 
 namespace qk {
 
-// With 1x16 blocks both per-CTA lookup tables of k_nvfp4 hold 16
+// With 1x16 blocks the per-CTA encode table of k_nvfp4 holds 16
 // interleaved copies (entry e, copy j at word 16 e + j) and lane l reads copy
 // l % 16, so lanes that look up different entries meet in one bank at most in
 // pairs (with one copy up to four entries share a bank).  16x16 lookups are
 // uniform across the lanes of a block and keep one copy.
 template <int BLK> constexpr int kTabCopies = BLK == 0 ? 16 : 1;
 
-// Block scale code sb = E4M3(RN(RN(b * alpha_g) / 6)) (b = 0 -> 0x38, 1.0).
-// T1 points at this lane's copy of the mantissa table.
-// For BF16 inputs b = (1 + m/128) 2^(E-127); writing alpha_g = a_m 2^ae with
-// a_m in [1, 2), RN(RN(b alpha_g) / 6) = RN(RN((1 + m/128) a_m) / 6)
-// 2^(E-127+ae) while the values stay normal (rounding commutes with
-// power-of-two scaling), so it is a per-CTA 128-entry table plus an exponent
-// shift; anything that would fall below 2^-126 encodes to E4M3 +0 either way,
-// and anything at or above 2^128 saturates to 448 (0x7E) either way.
-// FP32 inputs, subnormal or non-finite b, and an alpha_g that is 0 or NaN
-// (a non-finite tensor amax; ae is then kNoTable) take the two operations.
-constexpr int kNoTable = -100000;
-template <int DT, int C = 1> QD uint32_t nv_sb_code(uint32_t b, float alpha_g, const uint32_t *T1, int ae)
+// Block scale code sb = E4M3(RN(RN(b * alpha_g) / 6)) (b = 0 -> 0x38, 1.0) of
+// an FP32 block maximum with bits b.
+QD uint32_t nv_sb_code(uint32_t b, float alpha_g)
 {
     if (b == 0) return 0x38u;
-    const uint32_t E = b >> 23;
-    if (DT == BF16 && E != 0u && E != 255u && ae != kNoTable) {
-        const uint32_t t = T1[((b >> 16) & 0x7Fu) * C];
-        const int ne = (int)(t >> 23) + (int)E - 127 + ae;
-        if (ne <= 0) return 0u;
-        if (ne >= 255) return 0x7Eu;
-        return e4m3_code(__uint_as_float((t & 0x807FFFFFu) | ((uint32_t)ne << 23)));
-    }
     return e4m3_code(__fdiv_rn(__fmul_rn(__uint_as_float(b), alpha_g), 6.0f));
 }
 
 // The encode factor enc = alpha_g / f(sb) (0 when f(sb) = 0) depends only on
 // the code: each CTA tabulates it for the 128 positive codes (entry 0x38 =
 // alpha_g also serves b = 0).
-
-
-// In-place transpose of an 8x8 nibble matrix: a[i] nibble j -> a[j] nibble i.
-QD void transpose8x8_nibbles(uint32_t *a)
-{
-#pragma unroll
-    for (int i = 0; i < 4; i++) {   // 4x4 blocks
-        uint32_t t = ((a[i] >> 16) ^ a[i + 4]) & 0x0000FFFFu;
-        a[i + 4] ^= t;
-        a[i] ^= t << 16;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; i += 4)
-#pragma unroll
-        for (int j = 0; j < 2; j++) {   // 2x2 blocks
-            uint32_t t = ((a[i + j] >> 8) ^ a[i + j + 2]) & 0x00FF00FFu;
-            a[i + j + 2] ^= t;
-            a[i + j] ^= t << 8;
-        }
-#pragma unroll
-    for (int i = 0; i < 8; i += 2) {   // single nibbles
-        uint32_t t = ((a[i] >> 4) ^ a[i + 1]) & 0x0F0F0F0Fu;
-        a[i + 1] ^= t;
-        a[i] ^= t << 4;
-    }
-}
 
 // Codes of one row chunk (VEC elements, VEC/2 bytes) with scale factor enc;
 // SR draws the Philox block of element index i0 (row-major, stream 0).
@@ -118,76 +75,7 @@ QD uint32_t nv_row_codes(const uint4 &v, float enc, uint64_t seed, uint64_t offs
     return cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
 
-// Transposed FP4 codes of a tile: col[c] holds, for column c of this
-// thread's chunk, the 8 codes of rows 8w..8w+7 (row 8w in bits 3-0).  They
-// are parked at [column][64 bytes] in the consumed stage (4-byte slot w,
-// XOR-swizzled by lane) and written as q_colT rows by copy_out_fp4T.
-template <int VEC> QD void park_fp4T(uint8_t *stage, const uint32_t *col, int warp, int lane)
-{
-#pragma unroll
-    for (int c = 0; c < VEC; c++)
-        *reinterpret_cast<uint32_t *>(stage + (lane * VEC + c) * 64 + ((warp ^ (lane & 15)) * 4)) = col[c];
-}
-
-// With M % 32 == 0 the rows go out as 16-byte pieces (4 threads per 64-byte
-// row): slots 4g..4g+3 sit in the aligned group 4g ^ (s & ~3), word k holding
-// slot 4g + (k ^ (s & 3)).
-template <int VEC>
-QD void copy_out_fp4T(const uint8_t *stage, uint8_t *q_colT, int64_t M, int64_t K, int64_t mb, int64_t kb)
-{
-    constexpr int TC = 32 * VEC;
-    if ((M & 31) == 0) {
-#pragma unroll
-        for (int it = 0; it < TC * 4 / kEngThreads; it++) {
-            const int idx = it * kEngThreads + threadIdx.x;
-            const int col = idx >> 2, g = idx & 3;   // rows 32g..32g+31 of the tile
-            const int s = (col / VEC) & 15;
-            const int64_t kg = kb + col, mg = mb + 32 * g;
-            if (kg < K && mg < M) {
-                uint4 w = *reinterpret_cast<const uint4 *>(stage + col * 64 + ((4 * g) ^ (s & ~3)) * 4);
-                if (s & 1) w = make_uint4(w.y, w.x, w.w, w.z);
-                if (s & 2) w = make_uint4(w.z, w.w, w.x, w.y);
-                stg16(q_colT + kg * (M / 2) + mg / 2, w);
-            }
-        }
-        return;
-    }
-#pragma unroll
-    for (int it = 0; it < TC * 16 / kEngThreads; it++) {
-        const int idx = it * kEngThreads + threadIdx.x;
-        const int col = idx >> 4, sl = idx & 15;   // slot sl = rows 8sl..8sl+7 of the tile
-        const int64_t kg = kb + col, mg = mb + 8 * sl;
-        if (kg < K && mg < M)
-            stg4(q_colT + kg * (M / 2) + mg / 2,
-                 *reinterpret_cast<const uint32_t *>(stage + col * 64 + ((sl ^ ((col / VEC) & 15)) * 4)));
-    }
-}
-
-// Columnwise block scales of a tile, sSB[g][col] for the 16-row group g of
-// tile column col, written as sb_colT[kb + col][mb/16 + g].
-template <int TC>
-QD void copy_out_sbT(const uint8_t (*sSB)[TC], uint8_t *sb_colT, int64_t M, int64_t K, int64_t mb, int64_t kb)
-{
-    const int64_t left = (M - mb) / 16;
-    const int nb = left < 8 ? (int)left : 8;
-    for (int col = threadIdx.x; col < TC; col += kEngThreads) {
-        const int64_t kg = kb + col;
-        if (kg >= K) continue;
-        uint8_t *dst = sb_colT + kg * (M / 16) + mb / 16;
-        if (nb == 8 && (M % 128) == 0) {
-            uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                w0 |= (uint32_t)sSB[q][col] << (8 * q);
-                w1 |= (uint32_t)sSB[q + 4][col] << (8 * q);
-            }
-            stg8(dst, w0, w1);
-        } else {
-            for (int q = 0; q < nb; q++) dst[q] = sSB[q][col];
-        }
-    }
-}
-
+// FP32 inputs (BF16 inputs take k_nvfp4_bf16).
 template <int DT, int BLK, int RND>
 __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
                                                           const float *__restrict__ amax, uint64_t seed, uint64_t offset,
@@ -195,9 +83,9 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                                                           uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
                                                           float *__restrict__ s_global, int32_t *status)
 {
+    static_assert(DT == F32, "BF16 inputs take k_nvfp4_bf16");
     constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, LPB = 16 / VEC, TCP = kTabCopies<BLK>;
     __shared__ float enc_tab[128 * TCP];
-    __shared__ uint32_t sb_tab[128 * TCP];   // BF16: RN(RN((1 + m/128) a_m) / 6) per mantissa m
     __shared__ uint4 part[kEngWarps][32];        // 1x16: per-warp column maxima over 8 rows
     __shared__ __align__(8) uint8_t sSB[8][TC];   // 1x16: columnwise block scales of a tile
     __shared__ uint32_t bred[kEngWarps][TC / 16];   // 16x16: half-block maxima
@@ -205,21 +93,11 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
     griddep_wait();   // the amax pass ahead of this kernel is complete
     const float A = *amax;
     const float alpha_g = alpha_from_amax(2688.0f, A);
-    const uint32_t ag = __float_as_uint(alpha_g);
-    // alpha_g = 2688 / A is a normal float for every finite A > 0 (and 1 for
-    // A = 0); a non-finite A gives 0 or NaN, which the table cannot scale
-    const bool ag_normal = (ag >> 23) != 0u && (ag >> 23) != 255u;
-    const int ae = ag_normal ? (int)(ag >> 23) - 127 : kNoTable;
     if (threadIdx.x < 128) {
         const float sv = e4m3_value(threadIdx.x);
         const float ev = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_g, sv);
-        const float a_m = __uint_as_float((ag & 0x807FFFFFu) | (127u << 23));
-        const uint32_t tv = __float_as_uint(__fdiv_rn(__fmul_rn(1.0f + (float)threadIdx.x * (1.0f / 128.0f), a_m), 6.0f));
 #pragma unroll
-        for (int j = 0; j < TCP; j++) {
-            enc_tab[threadIdx.x * TCP + j] = ev;
-            sb_tab[threadIdx.x * TCP + j] = tv;
-        }
+        for (int j = 0; j < TCP; j++) enc_tab[threadIdx.x * TCP + j] = ev;
     }   // visible after the engine's first barrier
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         *s_global = __fdiv_rn(1.0f, alpha_g);
@@ -229,7 +107,6 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
     const float *encT = enc_tab + (lane & (TCP - 1));   // this lane's copy: entry e at encT[e * TCP]
-    const uint32_t *sbT = sb_tab + (lane & (TCP - 1));
 
     run_tiles(&tmap, tiles_m, tiles_k, TC, true, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
@@ -254,52 +131,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
             }
             // ---------------- 1x16 rowwise ----------------
             uint32_t nf = 0;
-            if (DT == BF16 && q_row != nullptr) {
-                // A block is 2 lanes.  The 8 row maxima, two BF16 magnitudes per
-                // word, are halved across the pair: this lane keeps rows
-                // rb..rb+3 (rb = 4 * (lane & 1)), computes their block scales and
-                // encode factors, and takes the partner's 4 factors by shuffle.
-                const int nrows = !kok ? 0 : (m0 + 8 <= M ? 8 : (m0 < M ? (int)(M - m0) : 0));
-                uint32_t P[4];
-#pragma unroll
-                for (int p = 0; p < 4; p++) {
-                    const uint4 &a = v[2 * p], &b = v[2 * p + 1];
-                    const uint32_t ma = hmax_abs2(hmax_abs2(a.x, a.y), hmax_abs2(a.z, a.w));
-                    const uint32_t mb2 = hmax_abs2(hmax_abs2(b.x, b.y), hmax_abs2(b.z, b.w));
-                    P[p] = hmax_abs2(__byte_perm(ma, mb2, 0x5410), __byte_perm(ma, mb2, 0x7632));   // row 2p low, 2p+1 high
-                }
-                const bool b0 = lane & 1;
-                const int rb = b0 ? 4 : 0;
-                uint32_t k0 = b0 ? P[2] : P[0], k1 = b0 ? P[3] : P[1];
-                const uint32_t s0 = b0 ? P[0] : P[2], s1 = b0 ? P[1] : P[3];
-                k0 = hmax_abs2(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, 1));
-                k1 = hmax_abs2(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, 1));
-                float own[4];
-#pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    const uint32_t kw = h < 2 ? k0 : k1;
-                    const uint32_t bits = ((h & 1) ? kw : (kw << 16)) & 0x7FFF0000u;   // row rb + h
-                    const uint32_t sb = nv_sb_code<DT, TCP>(bits, alpha_g, sbT, ae);
-                    own[h] = encT[(sb & 0x7Fu) * TCP];
-                    if (rb + h < nrows) {
-                        sb_row[(m0 + rb + h) * (K / 16) + k / 16] = (uint8_t)sb;
-                        nf |= nonfinite(bits);
-                    }
-                }
-                float encr[8];
-#pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    const float other = __shfl_xor_sync(0xFFFFFFFFu, own[h], 1);
-                    encr[h] = b0 ? other : own[h];
-                    encr[4 + h] = b0 ? own[h] : other;
-                }
-                uint8_t *qr = q_row + m0 * (K / 2) + k / 2;
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const uint32_t code = nv_row_codes<DT, RND>(v[j], encr[j], seed, offset, (m0 + j) * K + k);
-                    if (j < nrows) stg4(qr + j * (K / 2), code);
-                }
-            } else if (q_row != nullptr) {
+            if (q_row != nullptr) {
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
                     uint32_t bb[2] = {absmax_bits<DT>(v[j]), absmax_bits<DT>(v[j + 1])};
@@ -307,7 +139,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
 #pragma unroll
                     for (int h = 0; h < 2; h++) {
                         const int64_t m = m0 + j + h;
-                        const uint32_t sb = nv_sb_code<DT, TCP>(bb[h], alpha_g, sbT, ae);
+                        const uint32_t sb = nv_sb_code(bb[h], alpha_g);
                         const uint32_t code = nv_row_codes<DT, RND>(v[j + h], encT[(sb & 0x7Fu) * TCP], seed, offset, m * K + k);
                         const bool ok = m < M && kok;
                         if (ok) {
@@ -341,7 +173,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
 #pragma unroll
             for (int c = 0; c < VEC; c++) {
                 const uint32_t b = colmax_bits<DT>(cm, c);
-                const uint32_t sb = nv_sb_code<DT, TCP>(b, alpha_g, sbT, ae);
+                const uint32_t sb = nv_sb_code(b, alpha_g);
                 const float enc = encT[(sb & 0x7Fu) * TCP];
                 if (RND == 0) sbw[c >> 2] |= sb << (8 * (c & 3));
                 else if ((warp & 1) == 0) sSB[warp >> 1][lane * VEC + c] = (uint8_t)sb;
@@ -378,7 +210,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
             if (lane % LPB == 0) bred[warp][lane / LPB] = b;
             __syncthreads();   // half-block maxima posted; every read of the stage is done
             b = max(bred[warp & ~1][lane / LPB], bred[warp | 1][lane / LPB]);
-            const uint32_t sb = nv_sb_code<DT, TCP>(b, alpha_g, sbT, ae);
+            const uint32_t sb = nv_sb_code(b, alpha_g);
             const float enc = encT[(sb & 0x7Fu) * TCP];
             const int64_t m16 = mb + 16 * (warp >> 1);
             if ((warp & 1) == 0 && lane % LPB == 0 && m16 < M && kok) {
@@ -438,10 +270,9 @@ cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, i
                          uint8_t *sb_colT, float *s_global, int32_t *status, cudaStream_t st, bool after_amax)
 {
 #define NV_ARGS x, M, K, amax, seed, offset, q_row, sb_row, q_colT, sb_colT, s_global, status, st, after_amax
-    if (dt == BF16) {
-        if (blk == 0) return rnd == 0 ? nv_t<BF16, 0, 0>(NV_ARGS) : nv_t<BF16, 0, 1>(NV_ARGS);
-        return rnd == 0 ? nv_t<BF16, 1, 0>(NV_ARGS) : nv_t<BF16, 1, 1>(NV_ARGS);
-    }
+    if (dt == BF16)
+        return launch_nvfp4_bf16(x, M, K, blk, rnd, seed, offset, amax, q_row, sb_row, q_colT, sb_colT, s_global,
+                                 status, st, after_amax);
     if (blk == 0) return rnd == 0 ? nv_t<F32, 0, 0>(NV_ARGS) : nv_t<F32, 0, 1>(NV_ARGS);
     return rnd == 0 ? nv_t<F32, 1, 0>(NV_ARGS) : nv_t<F32, 1, 1>(NV_ARGS);
 #undef NV_ARGS
@@ -548,7 +379,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
                 mbx = fmax_abs(mbx, b[i]);
             }
             const uint32_t ba = __float_as_uint(ma) & 0x7FFFFFFFu, bb = __float_as_uint(mbx) & 0x7FFFFFFFu;
-            const uint32_t sa = nv_sb_code<F32>(ba, alpha_g, nullptr, 0), sbb = nv_sb_code<F32>(bb, alpha_g, nullptr, 0);
+            const uint32_t sa = nv_sb_code(ba, alpha_g), sbb = nv_sb_code(bb, alpha_g);
             const float ea = enc_tab[sa & 0x7Fu], eb = enc_tab[sbb & 0x7Fu];
             const int c0 = q * CPT + 2 * p;   // tile column of a
             sSB[g][c0] = (uint8_t)sa;

@@ -186,7 +186,12 @@ QD uint32_t cvt_fp4x8(float v0, float v1, float v2, float v3, float v4, float v5
 }
 
 // One E4M3 code (saturating RTNE) of an FP32 value, and its exact value.
-QD uint32_t e4m3_code(float f) { return cvt_fp8x4<E4M3>(f, 0.f, 0.f, 0.f) & 0xFFu; }
+QD uint32_t e4m3_code(float f)
+{
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.0f), "f"(f));
+    return (uint32_t)h & 0xFFu;
+}
 QD float e4m3_value(uint32_t code)
 {
     uint32_t h2;
@@ -316,17 +321,59 @@ QD float mx_inv_scale(uint32_t code)
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11)
 // ---------------------------------------------------------------------------
 
+// Round multipliers and key increments (Weyl constants) of the paper.
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u, kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
+
 QD uint4 philox4x32_10(uint4 c, uint2 k)
 {
 #pragma unroll
     for (int r = 0; r < 10; r++) {
-        uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-        uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        uint32_t hi0 = __umulhi(kPhiloxM0, c.x), lo0 = kPhiloxM0 * c.x;
+        uint32_t hi1 = __umulhi(kPhiloxM1, c.z), lo1 = kPhiloxM1 * c.z;
         c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
-        k.x += 0x9E3779B9u;
-        k.y += 0xBB67AE85u;
+        k.x += kPhiloxW0;
+        k.y += kPhiloxW1;
     }
     return c;
+}
+
+// The ten round keys of a seed (round r: key + r * increments), formed once
+// on the host and passed to a kernel by value, so that each round reads its
+// key from the kernel's parameters instead of adding the increments.
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];
+};
+inline __host__ __device__ PhiloxKeys philox_keys(uint64_t seed)
+{
+    PhiloxKeys K;
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; r++) {
+        K.k0[r] = a;
+        K.k1[r] = b;
+        a += kPhiloxW0;
+        b += kPhiloxW1;
+    }
+    return K;
+}
+
+// Philox4x32-10 of counter c with precomputed round keys (same output as
+// philox4x32_10(c, (seed lo, seed hi))).
+QD uint4 philox4x32_10_rk(uint4 c, const PhiloxKeys &K)
+{
+#pragma unroll
+    for (int r = 0; r < 10; r++) {
+        const uint32_t hi0 = __umulhi(kPhiloxM0, c.x), lo0 = kPhiloxM0 * c.x;
+        const uint32_t hi1 = __umulhi(kPhiloxM1, c.z), lo1 = kPhiloxM1 * c.z;
+        c = make_uint4(hi1 ^ c.y ^ K.k0[r], lo1, hi0 ^ c.w ^ K.k1[r], lo0);
+    }
+    return c;
+}
+
+// The 128 random bits of Philox block g of a stream, with round keys.
+template <uint32_t STREAM> QD uint4 sr_bits_rk(uint64_t g, const PhiloxKeys &K)
+{
+    return philox4x32_10_rk(make_uint4((uint32_t)g, (uint32_t)(g >> 32), STREAM, 0u), K);
 }
 
 // The 128 random bits of block g (= offset + element index / 8) of a stream.
@@ -357,6 +404,38 @@ QD float sr_e2m1_value(float y, float r)
     const float n = ceilf(__fmaf_rn(-r, 1.0f / 65536.0f, t));
     return copysignf(__fmul_rn(n, ulp), y);                                 // exact, on the grid
 }
+
+// Stochastic rounding onto the E2M1 grid as an integer dither, the same
+// rule as sr_e2m1_value: with a = |y| < 6, t = a / ulp, fl = floor(t) and
+// frac = t - fl, round up iff R < frac * 2^16 for the element's 16 random
+// bits R.
+// ys = a * 2^-126 rounded up maps the grid onto FP32 values with one
+// mantissa bit: 1 -> 2^-126 (the smallest normal), the spacing 0.5 below 2
+// onto the subnormal / first-binade spacing 2^-127, and so on up to 6.  Its
+// 22 bits below that kept bit are L = ceil(frac * 2^22) (exact, L = frac * 2^22,
+// for a >= 1; the rounding up makes L the ceiling below 1, and a carry into
+// the kept bit means a already rounds to the next grid value).  Adding
+// D = 2^22 - 1 - 64 R and dropping the 22 bits carries into the kept bit iff
+// L > 64 R, i.e. iff R < frac * 2^16 (64 R is an integer, so 64 R < F iff
+// 64 R < ceil(F)).  Magnitudes from 6 up to inf stay >= 6 (or inf) and the
+// saturating conversion gives 6 as for y; D = 0 (dither_mask 0, taken for a
+// block whose encode factor is not finite) passes inf and NaN through
+// unchanged, as round-to-nearest would see them.  The result carries y's
+// sign, through the exact factor +-2^126.
+QD float sr_e2m1_dither(float y, uint32_t D)
+{
+    const float ys = __fmul_ru(fabsf(y), 0x1p-126f);
+    const uint32_t t = (__float_as_uint(ys) + D) & 0xFFC00000u;
+    return __fmul_rn(__uint_as_float(t), __uint_as_float((__float_as_uint(y) & 0x80000000u) | 0x7E800000u));
+}
+
+// D of the low / high 16-bit draw of a Philox word: m & ~(R << 6), which for
+// m = 2^22 - 1 is 2^22 - 1 - 64 R, and for m = 0 is 0.
+QD uint32_t sr_dither_lo(uint32_t w, uint32_t m) { return m & ~((w << 6) & 0x3FFFC0u); }
+QD uint32_t sr_dither_hi(uint32_t w, uint32_t m) { return m & ~((w >> 10) & 0x3FFFC0u); }
+// The dither mask of a block with encode factor enc: 2^22 - 1 if enc is
+// finite, 0 otherwise.
+QD uint32_t sr_dither_mask(float enc) { return (__float_as_uint(enc) & 0x7F800000u) != 0x7F800000u ? 0x3FFFFFu : 0u; }
 
 // The two 16-bit draws of a Philox word (low half first) as exact floats.
 QD void r16_pair(uint32_t w, float &lo, float &hi)

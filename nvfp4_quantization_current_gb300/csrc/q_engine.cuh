@@ -41,10 +41,24 @@ constexpr int kEngSmem = kStages * kTileBytes;          // dynamic shared memory
 constexpr int32_t kStTimeout = 2;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
 
+// Tile geometry of an engine kernel: ROWS x 512-byte tiles, STAGES in
+// flight, THREADS per CTA.  The default is one 512-thread CTA per SM with
+// 128-row tiles; TileCfg<64, 256> runs two 256-thread CTAs per SM (each with
+// its own stages), so that one CTA's barriers and latency-bound phases
+// overlap the other's work.
+template <int ROWS, int THREADS, int STAGES = 3> struct TileCfg {
+    static constexpr int kRows = ROWS, kThreads = THREADS, kStages = STAGES;
+    static constexpr int kTileBytes = ROWS * kRowBytes;
+    static constexpr int kSmem = STAGES * kTileBytes;   // dynamic shared memory of the stages
+};
+using EngCfg = TileCfg<kTileRowsE, kEngThreads, kStages>;
+
 // The engine's dynamic shared memory exceeds the default per-CTA limit; the
 // opt-in is a per-device attribute of each kernel, set once per device.
+// max_shared also asks for the largest shared-memory carveout (kernels that
+// keep two CTAs per SM).
 template <auto Kernel>
-inline cudaError_t engine_smem_ready()
+inline cudaError_t engine_smem_ready(int bytes = kEngSmem, bool max_shared = false)
 {
     static std::atomic<unsigned long long> done{0};
     int dev = 0;
@@ -52,7 +66,9 @@ inline cudaError_t engine_smem_ready()
     if (e != cudaSuccess) return e;
     const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
     if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
-    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && max_shared)
+        e = cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_relaxed);
     return e;
 }
@@ -108,6 +124,15 @@ QD void tma_load_tile(void *dst, const CUtensorMap *map, int x, int y, uint64_t 
 }
 
 QD uint4 lds16(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+// The same load, issued again even when the compiler could reuse an earlier
+// one (a second pass over a stage re-reads it instead of keeping registers).
+QD uint4 lds16_again(const uint8_t *p)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)));
+    return v;
+}
 
 // Transposed FP8 codes of a tile, staged for full-line writes: each thread
 // holds 8 rows (8w..8w+7) x VEC columns of codes, as VEC/4 words per row
@@ -151,28 +176,158 @@ QD void copy_out_fp8T(const uint8_t *stage, uint8_t *q_colT, int64_t M, int64_t 
     }
 }
 
-// Tiles of this CTA: t = blockIdx.x + i * gridDim.x (reversed when `reverse`,
+// In-place transpose of an 8x8 nibble matrix: a[i] nibble j -> a[j] nibble i.
+QD void transpose8x8_nibbles(uint32_t *a)
+{
+#pragma unroll
+    for (int i = 0; i < 4; i++) {   // 4x4 blocks
+        uint32_t t = ((a[i] >> 16) ^ a[i + 4]) & 0x0000FFFFu;
+        a[i + 4] ^= t;
+        a[i] ^= t << 16;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += 4)
+#pragma unroll
+        for (int j = 0; j < 2; j++) {   // 2x2 blocks
+            uint32_t t = ((a[i + j] >> 8) ^ a[i + j + 2]) & 0x00FF00FFu;
+            a[i + j + 2] ^= t;
+            a[i + j] ^= t << 8;
+        }
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {   // single nibbles
+        uint32_t t = ((a[i] >> 4) ^ a[i + 1]) & 0x0F0F0F0Fu;
+        a[i + 1] ^= t;
+        a[i] ^= t << 4;
+    }
+}
+
+// Transposed FP4 codes of a tile: col[c] holds, for column c of this
+// thread's chunk, the 8 codes of rows 8w..8w+7 (row 8w in bits 3-0).  They
+// are parked at [column][64 bytes] in the consumed stage (4-byte slot w,
+// XOR-swizzled by lane) and written as q_colT rows by copy_out_fp4T.
+template <int VEC> QD void park_fp4T(uint8_t *stage, const uint32_t *col, int warp, int lane)
+{
+#pragma unroll
+    for (int c = 0; c < VEC; c++)
+        *reinterpret_cast<uint32_t *>(stage + (lane * VEC + c) * 64 + ((warp ^ (lane & 15)) * 4)) = col[c];
+}
+
+// Writes the parked transposed FP4 codes of a ROWS-row tile as q_colT rows.
+// Parking layout: [tile column][ROWS / 2 bytes], the ROWS / 8 4-byte slots of
+// a column (slot sl = its rows 8 sl .. 8 sl + 7) XOR-swizzled by
+// s = (column / VEC) & (ROWS / 8 - 1).  With M % 32 == 0 the rows go out as
+// 16-byte pieces (ROWS / 32 per column): slots 4g..4g+3 sit in the aligned
+// group 4g ^ (s & ~3), word k holding slot 4g + (k ^ (s & 3)).
+template <int VEC, int ROWS = kTileRowsE, int THREADS = kEngThreads>
+QD void copy_out_fp4T(const uint8_t *stage, uint8_t *q_colT, int64_t M, int64_t K, int64_t mb, int64_t kb)
+{
+    constexpr int TC = 32 * VEC, CB = ROWS / 2, SL = ROWS / 8, PC = ROWS / 32;
+    if ((M & 31) == 0) {
+#pragma unroll
+        for (int it = 0; it < TC * PC / THREADS; it++) {
+            const int idx = it * THREADS + threadIdx.x;
+            const int col = idx / PC, g = idx % PC;   // rows 32g..32g+31 of the tile
+            const int s = (col / VEC) & (SL - 1);
+            const int64_t kg = kb + col, mg = mb + 32 * g;
+            if (kg < K && mg < M) {
+                uint4 w = *reinterpret_cast<const uint4 *>(stage + col * CB + ((4 * g) ^ (s & ~3)) * 4);
+                if (s & 1) w = make_uint4(w.y, w.x, w.w, w.z);
+                if (s & 2) w = make_uint4(w.z, w.w, w.x, w.y);
+                stg16(q_colT + kg * (M / 2) + mg / 2, w);
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int it = 0; it < TC * SL / THREADS; it++) {
+        const int idx = it * THREADS + threadIdx.x;
+        const int col = idx / SL, sl = idx % SL;   // slot sl = rows 8sl..8sl+7 of the tile
+        const int64_t kg = kb + col, mg = mb + 8 * sl;
+        if (kg < K && mg < M)
+            stg4(q_colT + kg * (M / 2) + mg / 2,
+                 *reinterpret_cast<const uint32_t *>(stage + col * CB + ((sl ^ ((col / VEC) & (SL - 1))) * 4)));
+    }
+}
+
+// Columnwise block scales of a ROWS-row tile, sSB[g][col] for the 16-row
+// group g of tile column col, written as sb_colT[kb + col][mb/16 + g]: one
+// store of ROWS / 16 bytes per column when the whole tile height is inside
+// the tensor and aligned, byte stores otherwise.
+template <int TC, int ROWS = kTileRowsE, int THREADS = kEngThreads>
+QD void copy_out_sbT(const uint8_t (*sSB)[TC], uint8_t *sb_colT, int64_t M, int64_t K, int64_t mb, int64_t kb)
+{
+    constexpr int G = ROWS / 16;
+    const int64_t left = (M - mb) / 16;
+    const int nb = left < G ? (int)left : G;
+    for (int col = threadIdx.x; col < TC; col += THREADS) {
+        const int64_t kg = kb + col;
+        if (kg >= K) continue;
+        uint8_t *dst = sb_colT + kg * (M / 16) + mb / 16;
+        if (nb == G && (M % (16 * G)) == 0) {
+            uint32_t w[G / 4] = {};
+#pragma unroll
+            for (int q = 0; q < G; q++) w[q / 4] |= (uint32_t)sSB[q][col] << (8 * (q & 3));
+            if constexpr (G == 8) stg8(dst, w[0], w[1]);
+            else stg4(dst, w[0]);
+        } else {
+            for (int q = 0; q < nb; q++) dst[q] = sSB[q][col];
+        }
+    }
+}
+
+// Tiles of this CTA (Cfg: tile rows, stages): t = blockIdx.x + i * gridDim.x (reversed when `reverse`,
 // so that a second pass over a tensor meets the part the first pass left in
-// L2 first).  body(stage, tm, tk) runs with all threads; it may use
-// __syncthreads() and may overwrite its stage.
-template <class Body>
+// L2 first).  pre() runs with all threads once the first kStages copies are
+// issued and before the first tile is awaited (a kernel whose input tensor is
+// ready but whose scalar inputs come from the kernel ahead of it can wait for
+// those there, while its first tiles load).  body(stage, tm, tk) runs with
+// all threads; it may use __syncthreads() and may overwrite its stage.
+template <class Cfg = EngCfg, class Pre, class Body>
+__device__ __forceinline__ void run_tiles(const CUtensorMap *tmap, int64_t tiles_m, int64_t tiles_k, int tile_cols,
+                                          bool reverse, int32_t *status, Pre &&pre, Body &&body);
+
+template <class Cfg = EngCfg, class Body>
 __device__ __forceinline__ void run_tiles(const CUtensorMap *tmap, int64_t tiles_m, int64_t tiles_k, int tile_cols,
                                           bool reverse, int32_t *status, Body &&body)
 {
+    run_tiles<Cfg>(tmap, tiles_m, tiles_k, tile_cols, reverse, status, [] {}, static_cast<Body &&>(body));
+}
+
+template <class Cfg, class Pre, class Body>
+__device__ __forceinline__ void run_tiles(const CUtensorMap *tmap, int64_t tiles_m, int64_t tiles_k, int tile_cols,
+                                          bool reverse, int32_t *status, Pre &&pre, Body &&body)
+{
+    constexpr int kStages = Cfg::kStages, kTileBytes = Cfg::kTileBytes, kTileRowsE = Cfg::kRows;
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t full[kStages];
 
     const int64_t ntiles = tiles_m * tiles_k;
     const int64_t count = ntiles > (int64_t)blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    auto tile_of = [&](int64_t i) -> int64_t {
-        const int64_t t = (int64_t)blockIdx.x + i * gridDim.x;
-        return reverse ? ntiles - 1 - t : t;
+    // Tile t = blockIdx.x + i * gridDim.x as (row, column) of the tile grid,
+    // advanced without a division per tile: the stride gridDim.x is
+    // q rows + r columns.  Reversed walks use (tiles_m - 1 - tm, tiles_k - 1 - tk).
+    const int64_t tkd = tiles_k > 0 ? tiles_k : 1;   // an empty tensor has no tiles to walk
+    const int64_t q = (int64_t)gridDim.x / tkd, r = (int64_t)gridDim.x - q * tkd;
+    struct Cursor {
+        int64_t tm, tk;
     };
-    auto issue = [&](int64_t i, int s) {
-        const int64_t t = tile_of(i);
-        const int64_t tm = t / tiles_k, tk = t - tm * tiles_k;
+    auto advance = [&](Cursor &c) {
+        c.tk += r;
+        c.tm += q;
+        if (c.tk >= tiles_k) {
+            c.tk -= tiles_k;
+            c.tm += 1;
+        }
+    };
+    Cursor first;
+    first.tm = (int64_t)blockIdx.x / tkd;
+    first.tk = (int64_t)blockIdx.x - first.tm * tkd;
+    Cursor ahead = first;   // thread 0: the next tile to request
+    auto issue = [&](int s) {
+        const int64_t tm = reverse ? tiles_m - 1 - ahead.tm : ahead.tm, tk = reverse ? tiles_k - 1 - ahead.tk : ahead.tk;
         mbar_arrive_expect_tx(&full[s], (uint32_t)kTileBytes);
         tma_load_tile(dsm + s * kTileBytes, tmap, (int)(tk * tile_cols), (int)(tm * kTileRowsE), &full[s]);
+        advance(ahead);
     };
 
     if (threadIdx.x == 0) {
@@ -181,19 +336,21 @@ __device__ __forceinline__ void run_tiles(const CUtensorMap *tmap, int64_t tiles
     }
     __syncthreads();
     if (threadIdx.x == 0)
-        for (int64_t i = 0; i < count && i < kStages; i++) issue(i, (int)i);
+        for (int64_t i = 0; i < count && i < kStages; i++) issue((int)i);
+    pre();
 
     // Tile i is issued before iteration i - kStages + 1 at the latest, so when
     // the loop leaves after tile i the copies of tiles i + 1 .. i + kStages - 1
     // are outstanding, and tile i's own if thread 0's wait for it gave up.
     int64_t drain_from = -1, drain_to = -1;
+    Cursor cur = first;
+    int s = 0;
+    uint32_t parity = 0;
     for (int64_t i = 0; i < count; i++) {
-        const int s = (int)(i % kStages);
-        const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / kStages) & 1));
+        const bool ok = mbar_wait_bounded(&full[s], parity);
         if (!ok && status != nullptr) atomicOr(status, kStTimeout);
-        const int64_t t = tile_of(i);
-        const int64_t tm = t / tiles_k, tk = t - tm * tiles_k;
-        body(dsm + s * kTileBytes, tm, tk);
+        body(dsm + s * kTileBytes, reverse ? tiles_m - 1 - cur.tm : cur.tm, reverse ? tiles_k - 1 - cur.tk : cur.tk);
+        advance(cur);
         // every thread is done with the stage; any wait of this tile that gave up stops the whole CTA
         if (__syncthreads_or(!ok)) {
             drain_from = ok ? i + 1 : i;
@@ -202,7 +359,11 @@ __device__ __forceinline__ void run_tiles(const CUtensorMap *tmap, int64_t tiles
         }
         if (threadIdx.x == 0 && i + kStages < count) {
             fence_proxy_async();   // generic-proxy accesses of the stage before the async-proxy refill
-            issue(i + kStages, s);
+            issue(s);
+        }
+        if (++s == kStages) {
+            s = 0;
+            parity ^= 1u;
         }
     }
     if (threadIdx.x == 0 && drain_from >= 0) {

@@ -30,11 +30,12 @@ cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 }
 
 // A 2-D TMA tensor map over a row-major [M, K] input (dt: BF16, F32, or U8
-// for code matrices, K even) whose box is 128 rows x 512 bytes (the tile
-// engine's stage).  The x coordinate counts elements of 2 bytes (BF16, U8)
-// or 4 bytes (F32).  Fails with
-// cudaErrorNotSupported if the driver entry point is unavailable.
-cudaError_t make_tile_map(void *map /* CUtensorMap, 64-byte aligned */, const void *x, int dt, int64_t M, int64_t K);
+// for code matrices, K even) whose box is box_rows rows x 512 bytes (the tile
+// engine's stage; box_rows <= 256).  The x coordinate counts elements of 2
+// bytes (BF16, U8) or 4 bytes (F32).  Fails with cudaErrorNotSupported if the
+// driver entry point is unavailable.
+cudaError_t make_tile_map(void *map /* CUtensorMap, 64-byte aligned */, const void *x, int dt, int64_t M, int64_t K,
+                          int box_rows = 128);
 
 // current scaling
 cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *status, cudaStream_t st);
@@ -84,6 +85,11 @@ cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, i
                          uint64_t offset, const float *amax, uint8_t *q_row, uint8_t *sb_row,
                          uint8_t *q_colT, uint8_t *sb_colT, float *s_global, int32_t *status,
                          cudaStream_t st, bool after_amax);
+
+// NVFP4 of a BF16 tensor (the BF16 path of launch_nvfp4)
+cudaError_t launch_nvfp4_bf16(const void *x, int64_t M, int64_t K, int blk, int rnd, uint64_t seed, uint64_t offset,
+                              const float *amax, uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT,
+                              float *s_global, int32_t *status, cudaStream_t st, bool after_amax);
 
 // dequantizers
 cudaError_t launch_dq_cs(const uint8_t *q, const float *s, int64_t R, int64_t C, int fmt, int out,

@@ -22,7 +22,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-cudaError_t make_tile_map(void *map, const void *x, int dt, int64_t M, int64_t K)
+cudaError_t make_tile_map(void *map, const void *x, int dt, int64_t M, int64_t K, int box_rows)
 {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return cudaErrorNotSupported;
@@ -33,7 +33,7 @@ cudaError_t make_tile_map(void *map, const void *x, int dt, int64_t M, int64_t K
                                    : (dt == F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16);
     cuuint64_t dims[2] = {(cuuint64_t)(dt == U8 ? K / 2 : K), (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)(dt == U8 ? K : K * es)};
-    cuuint32_t box[2] = {(cuuint32_t)(512 / es), 128u};
+    cuuint32_t box[2] = {(cuuint32_t)(512 / es), (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = fn(static_cast<CUtensorMap *>(map), ty,
                     2, const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
