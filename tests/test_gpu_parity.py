@@ -685,6 +685,25 @@ def test_nvfp4_bf16_nonfinite_and_overflowing_scales_match_the_oracle(case, rnd,
         assert st.item() & Q.Q_ST_NONFINITE
 
 
+@pytest.mark.parametrize("bf16", [True, False])
+def test_nvfp4_encode_factor_case_through_the_kernel(bf16):
+    """The hand-derived case of the oracle pin (A = 39, block maximum 19.625
+    -> block scale 224, x = 0.8125 -> fl(x * fl(alpha_g / 224)) = 0.25, a tie
+    that rounds to 0): the kernels' block scale table (BF16) and two-operation
+    path (FP32) give block code 0x76 and element codes 0x7, 0x0."""
+    x = np.zeros((16, 32), np.float32)
+    x[0, 0], x[0, 1], x[0, 16] = 19.625, 0.8125, 39.0
+    if bf16:
+        x = O.bf16_round(x)
+    got = Q.q_nvfp4(dev(x), rowwise=True, colwise=True)
+    want = O.nvfp4(x, O.B1x16, O.RN, rowwise=True, colwise=True)
+    same(host(got.q_row), want.q_row, "q_row")
+    same(host(got.sb_row), want.sb_row, "sb_row")
+    same(host(got.q_colT), want.q_colT, "q_colT")
+    assert int(host(got.sb_row)[0, 0]) == 0x76
+    assert int(host(got.q_row)[0, 0]) == 0x07   # element 0 -> 6 (low nibble), element 1 -> 0 (high nibble)
+
+
 def test_nvfp4_single_direction_and_given_amax():
     x = W.gen("t3", (128, 256), 5, bf16=True)
     a = Q.q_amax(dev(x)) * 2          # a larger (e.g. all-reduced) amax

@@ -368,6 +368,39 @@ def test_nv_dequant_identity_and_error_bound(blk):
     assert np.all(np.abs(y - xf) <= bound)
 
 
+def test_nv_encode_factor_is_one_division_per_block():
+    """The encode factor is enc = fl(alpha_g / f(sb)), one FP32 division per
+    block (R-NV; "Mixed-precision training: fp16 to fp8", recipe 6: E4M3
+    block scale with an FP32 tensor scale).  A hand-derived case where the
+    element lands exactly on an E2M1 tie under that reading and just past it
+    under either plausible alternative:
+      A = 39 (the row's other block holds 39), alpha_g = fl(2688 / 39)
+        = 68.92308 (bits 0x4289D89E);
+      block maximum b = 19.625: fl(fl(b * alpha_g) / 6) = 225.43591, E4M3
+        RTNE -> 224 (code 0x76: 1.75 * 2^7);
+      enc = fl(alpha_g / 224) = 0.30769232 (bits 0x3E9D89D9);
+      x = 0.8125: fl(x * enc) = 0.25 exactly, the tie between 0 and 0.5 ->
+        0 (even), code 0x0; b itself: fl(19.625 * enc) = 6.038 -> 6, code 0x7.
+    The alternatives fl(alpha_g * fl(1 / 224)) = 0.30769235 and
+    fl(fl(x * alpha_g) / 224) both give 0.25000003 -> 0.5, code 0x1."""
+    row = np.zeros((1, 32), np.float32)
+    row[0, 0], row[0, 1] = 19.625, 0.8125
+    row[0, 16] = 39.0
+    r = O.nvfp4(row, O.B1x16, O.RN, rowwise=True)
+    assert np.float32(r.amax) == np.float32(39.0)
+    assert int(r.sb_row[0, 0]) == 0x76
+    codes = O.unpack_e2m1(r.q_row, 32)[0]
+    assert int(codes[0]) == 0x7 and int(codes[1]) == 0x0
+    # the arithmetic behind the literals, in numpy FP32
+    f32 = np.float32
+    alpha = f32(f32(2688.0) / f32(39.0))
+    assert int(alpha.view(np.uint32)) == 0x4289D89E
+    enc = f32(alpha / f32(224.0))
+    assert int(enc.view(np.uint32)) == 0x3E9D89D9 and f32(f32(0.8125) * enc) == f32(0.25)
+    for wrong in (f32(f32(0.8125) * f32(alpha * f32(f32(1.0) / f32(224.0)))), f32(f32(f32(0.8125) * alpha) / f32(224.0))):
+        assert wrong > f32(0.25) and O.cast_e2m1(np.array([wrong], np.float32))[0] == 0x1
+
+
 def test_nv_zero_block_scale_one():
     x = W.gen("normal", (16, 32), 1, bf16=False)
     x[:, 16:] = 0
