@@ -838,8 +838,9 @@ def run_ours(args):
                "steps": e2e_steps, "schedule": "uploads, calls and downloads on three streams, overlapped across calls",
                "host_link": {"h2d_GBps": up_gbs, "h2d_ms": up_ms, "d2h_GBps": down_gbs, "d2h_ms": down_ms,
                              "both_GBps": both_gbs, "both_ms": both_ms,
-                             "what": "the step's own copies alone (pinned host buffers, no kernels), measured in "
-                                     "the same run; both_ms bounds the end-to-end step from below"}}
+                             "what": "the step's own copies alone (pinned host buffers, no kernels) in the same "
+                                     "run: all uploads, all downloads, and both issued at once on two streams; the "
+                                     "longer one-way time bounds the end-to-end step from below"}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu and not args.only:

@@ -53,7 +53,7 @@ QD uint32_t nv_sb_code(uint32_t b, float alpha_g)
 // Codes of one row chunk (VEC elements, VEC/2 bytes) with scale factor enc;
 // SR draws the Philox block of element index i0 (row-major, stream 0).
 template <int DT, int RND>
-QD uint32_t nv_row_codes(const uint4 &v, float enc, uint64_t seed, uint64_t offset, int64_t i0)
+QD uint32_t nv_row_codes(const uint4 &v, float enc, const PhiloxKeys &keys, uint64_t offset, int64_t i0)
 {
     constexpr int VEC = In<DT>::VEC;
     float y[8];
@@ -62,14 +62,14 @@ QD uint32_t nv_row_codes(const uint4 &v, float enc, uint64_t seed, uint64_t offs
 #pragma unroll
     for (int j = 0; j < VEC; j += 2) mul2(y[j], y[j + 1], enc, enc);
     if (RND == 1) {
-        const uint4 R = sr_bits(seed, offset + (uint64_t)(i0 >> 3), 0u);
+        const uint4 R = sr_bits_rk<0>(offset + (uint64_t)(i0 >> 3), keys);
         const int e0 = (int)(i0 & 7);
+        const uint32_t dm = sr_dither_mask(enc);
 #pragma unroll
         for (int j = 0; j < VEC; j += 2) {   // draws e0 + j, e0 + j + 1: one word (e0 is 0, or 4 for FP32 chunks)
-            float r0, r1;
-            r16_pair(VEC == 8 ? word(R, j >> 1) : (e0 ? word(R, 2 + (j >> 1)) : word(R, j >> 1)), r0, r1);
-            y[j] = sr_e2m1_value(y[j], r0);
-            y[j + 1] = sr_e2m1_value(y[j + 1], r1);
+            const uint32_t w = VEC == 8 ? word(R, j >> 1) : (e0 ? word(R, 2 + (j >> 1)) : word(R, j >> 1));
+            y[j] = sr_e2m1_dither(y[j], sr_dither_lo(w, dm));
+            y[j + 1] = sr_e2m1_dither(y[j + 1], sr_dither_hi(w, dm));
         }
     }
     return cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
@@ -78,7 +78,8 @@ QD uint32_t nv_row_codes(const uint4 &v, float enc, uint64_t seed, uint64_t offs
 // FP32 inputs (BF16 inputs take k_nvfp4_bf16).
 template <int DT, int BLK, int RND>
 __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
-                                                          const float *__restrict__ amax, uint64_t seed, uint64_t offset,
+                                                          const float *__restrict__ amax,
+                                                          const __grid_constant__ PhiloxKeys keys, uint64_t offset,
                                                           uint8_t *__restrict__ q_row, uint8_t *__restrict__ sb_row,
                                                           uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
                                                           float *__restrict__ s_global, int32_t *status)
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                     for (int h = 0; h < 2; h++) {
                         const int64_t m = m0 + j + h;
                         const uint32_t sb = nv_sb_code(bb[h], alpha_g);
-                        const uint32_t code = nv_row_codes<DT, RND>(v[j + h], encT[(sb & 0x7Fu) * TCP], seed, offset, m * K + k);
+                        const uint32_t code = nv_row_codes<DT, RND>(v[j + h], encT[(sb & 0x7Fu) * TCP], keys, offset, m * K + k);
                         const bool ok = m < M && kok;
                         if (ok) {
                             uint8_t *dst = q_row + m * (K / 2) + k / 2;
@@ -185,13 +186,12 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
                 for (int j = 0; j < 8; j += 2) mul2(y[j], y[j + 1], enc, enc);
                 if (RND == 1) {
                     // rows m0 .. m0 + 7 of column k + c, stream 1: Philox block (m0 / 8) * K + k + c
-                    const uint4 R = sr_bits(seed, offset + (uint64_t)((m0 >> 3) * K + k + c), 1u);
+                    const uint4 R = sr_bits_rk<1>(offset + (uint64_t)((m0 >> 3) * K + k + c), keys);
+                    const uint32_t dm = sr_dither_mask(enc);
 #pragma unroll
                     for (int j = 0; j < 8; j += 2) {
-                        float r0, r1;
-                        r16_pair(word(R, j >> 1), r0, r1);
-                        y[j] = sr_e2m1_value(y[j], r0);
-                        y[j + 1] = sr_e2m1_value(y[j + 1], r1);
+                        y[j] = sr_e2m1_dither(y[j], sr_dither_lo(word(R, j >> 1), dm));
+                        y[j + 1] = sr_e2m1_dither(y[j + 1], sr_dither_hi(word(R, j >> 1), dm));
                     }
                 }
                 colw[c] = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
 #pragma unroll
             for (int j = 0; j < 8; j++) {
                 const int64_t m = m0 + j;
-                const uint32_t code = nv_row_codes<DT, RND>(v[j], enc, seed, offset, m * K + k);
+                const uint32_t code = nv_row_codes<DT, RND>(v[j], enc, keys, offset, m * K + k);
                 if (q_row != nullptr && m < M && kok) {
                     uint8_t *dst = q_row + m * (K / 2) + k / 2;
                     if (VEC == 8) stg4(dst, code);
@@ -261,8 +261,9 @@ static cudaError_t nv_t(const void *x, int64_t M, int64_t K, const float *amax, 
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     int grid = (int)(tiles < sm_count() ? tiles : sm_count());
     if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
+    const PhiloxKeys keys = philox_keys(seed);
     return launch_k(after_amax, k_nvfp4<DT, BLK, RND>, dim3(grid), dim3(kEngThreads), kEngSmem, st, map, M, K, amax,
-                    seed, offset, q_row, sb_row, q_colT, sb_colT, s_global, status);
+                    keys, offset, q_row, sb_row, q_colT, sb_colT, s_global, status);
 }
 
 cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, int rnd, uint64_t seed,
@@ -295,7 +296,8 @@ cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, i
 // ---------------------------------------------------------------------------
 template <int DT, int RND, int PASS>
 __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_constant__ CUtensorMap tmap, int64_t M,
-                                                              int64_t K, uint32_t sign_mask, float *amax, uint64_t seed,
+                                                              int64_t K, uint32_t sign_mask, float *amax,
+                                                              const __grid_constant__ PhiloxKeys keys,
                                                               uint64_t offset, uint8_t *__restrict__ q_colT,
                                                               uint8_t *__restrict__ sb_colT, float *__restrict__ s_global,
                                                               int32_t *status)
@@ -392,18 +394,19 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
                 // rows m .. m + 15 of columns kb + c0, kb + c0 + 1, stream 1: Philox blocks
                 // (m / 8 + hh) * K + column, two per column
                 const int64_t m = mb + 16 * g;
+                const uint32_t dma = sr_dither_mask(ea), dmb = sr_dither_mask(eb);
 #pragma unroll
                 for (int hh = 0; hh < 2; hh++) {
                     const uint64_t gb = offset + (uint64_t)(((m >> 3) + hh) * K + kb + c0);
-                    const uint4 Ra = sr_bits(seed, gb, 1u);
-                    const uint4 Rb = sr_bits(seed, gb + 1, 1u);
-                    float ra[8], rb[8];
-                    r16_block(Ra, ra);
-                    r16_block(Rb, rb);
+                    const uint4 Ra = sr_bits_rk<1>(gb, keys);
+                    const uint4 Rb = sr_bits_rk<1>(gb + 1, keys);
 #pragma unroll
-                    for (int j = 0; j < 8; j++) {
-                        a[8 * hh + j] = sr_e2m1_value(a[8 * hh + j], ra[j]);
-                        b[8 * hh + j] = sr_e2m1_value(b[8 * hh + j], rb[j]);
+                    for (int j = 0; j < 8; j += 2) {
+                        const uint32_t wa = word(Ra, j >> 1), wb = word(Rb, j >> 1);
+                        a[8 * hh + j] = sr_e2m1_dither(a[8 * hh + j], sr_dither_lo(wa, dma));
+                        a[8 * hh + j + 1] = sr_e2m1_dither(a[8 * hh + j + 1], sr_dither_hi(wa, dma));
+                        b[8 * hh + j] = sr_e2m1_dither(b[8 * hh + j], sr_dither_lo(wb, dmb));
+                        b[8 * hh + j + 1] = sr_e2m1_dither(b[8 * hh + j + 1], sr_dither_hi(wb, dmb));
                     }
                 }
             }
@@ -455,8 +458,9 @@ static cudaError_t rht_pass(bool pdl, const CUtensorMap &map, int64_t M, int64_t
     const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
     int grid = (int)(tiles < sm_count() ? tiles : sm_count());
     if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
+    const PhiloxKeys keys = philox_keys(seed);
     return launch_k(pdl, k_nvfp4_rht<DT, RND, PASS>, dim3(grid), dim3(kEngThreads), kEngSmem, st, map, M, K, mask, amax,
-                    seed, offset, q_colT, sb_colT, PASS == 0 ? amax_x : s_global, status);
+                    keys, offset, q_colT, sb_colT, PASS == 0 ? amax_x : s_global, status);
 }
 
 template <int DT, int RND>

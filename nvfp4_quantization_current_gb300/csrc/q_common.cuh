@@ -325,19 +325,6 @@ QD float mx_inv_scale(uint32_t code)
 constexpr uint32_t kPhiloxM0 = 0xD2511F53u, kPhiloxM1 = 0xCD9E8D57u;
 constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
 
-QD uint4 philox4x32_10(uint4 c, uint2 k)
-{
-#pragma unroll
-    for (int r = 0; r < 10; r++) {
-        uint32_t hi0 = __umulhi(kPhiloxM0, c.x), lo0 = kPhiloxM0 * c.x;
-        uint32_t hi1 = __umulhi(kPhiloxM1, c.z), lo1 = kPhiloxM1 * c.z;
-        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
-        k.x += kPhiloxW0;
-        k.y += kPhiloxW1;
-    }
-    return c;
-}
-
 // The ten round keys of a seed (round r: key + r * increments), formed once
 // on the host and passed to a kernel by value, so that each round reads its
 // key from the kernel's parameters instead of adding the increments.
@@ -357,8 +344,9 @@ inline __host__ __device__ PhiloxKeys philox_keys(uint64_t seed)
     return K;
 }
 
-// Philox4x32-10 of counter c with precomputed round keys (same output as
-// philox4x32_10(c, (seed lo, seed hi))).
+// Philox4x32-10 of counter c under the key whose round keys K holds: ten
+// rounds of (hi0, lo0) = M0 * c0, (hi1, lo1) = M1 * c2 (32 x 32 -> 64-bit
+// products), c = (hi1 ^ c1 ^ k0[r], lo1, hi0 ^ c3 ^ k1[r], lo0).
 QD uint4 philox4x32_10_rk(uint4 c, const PhiloxKeys &K)
 {
 #pragma unroll
@@ -376,39 +364,11 @@ template <uint32_t STREAM> QD uint4 sr_bits_rk(uint64_t g, const PhiloxKeys &K)
     return philox4x32_10_rk(make_uint4((uint32_t)g, (uint32_t)(g >> 32), STREAM, 0u), K);
 }
 
-// The 128 random bits of block g (= offset + element index / 8) of a stream.
-QD uint4 sr_bits(uint64_t seed, uint64_t g, uint32_t stream)
-{
-    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, 0u),
-                         make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
-}
-
-// Stochastic rounding of y onto the E2M1 grid with 16 random bits, given
-// as the exact float r (0..65535): with a = |y| < 6, ulp the grid spacing at
-// a (0.5 below 2, 1 in [2, 4), 2 in [4, 6)), t = a / ulp, fl = floor(t) and
-// frac = t - fl, the result is (fl + 1) * ulp iff r < frac * 2^16, else
-// fl * ulp.  With u = r / 2^16 that is ceil(t - u) * ulp: frac > u gives
-// fl + 1, frac <= u gives fl.  t - u is formed by one FMA; it is exact for
-// t >= 1 (both terms are multiples of 2^-23 and the difference is below 4),
-// and for t < 1 only its sign decides the ceiling (0 or 1), which
-// round-to-nearest keeps.  The result carries y's sign.  |y| >= 6 needs no
-// case of its own: there ulp = 2 and ceil(a/2 - u) >= 3, so the result is at
-// least 6 in magnitude (or inf) and the saturating conversion gives +-6, as
-// it does for y; a NaN stays NaN with y's sign.
-QD float sr_e2m1_value(float y, float r)
-{
-    const float a = fabsf(y);
-    const float s = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);           // 1 / ulp
-    const float ulp = __uint_as_float(0x7F000000u - __float_as_uint(s));   // 2^-k from 2^k
-    const float t = __fmul_rn(a, s);                                        // exact
-    const float n = ceilf(__fmaf_rn(-r, 1.0f / 65536.0f, t));
-    return copysignf(__fmul_rn(n, ulp), y);                                 // exact, on the grid
-}
-
-// Stochastic rounding onto the E2M1 grid as an integer dither, the same
-// rule as sr_e2m1_value: with a = |y| < 6, t = a / ulp, fl = floor(t) and
-// frac = t - fl, round up iff R < frac * 2^16 for the element's 16 random
-// bits R.
+// Stochastic rounding onto the E2M1 grid as an integer dither.  With
+// a = |y| < 6 between the grid neighbours lo and lo + ulp (ulp 0.5 below 2,
+// 1 in [2, 4), 2 in [4, 6)) and frac = (a - lo) / ulp, the result rounds up
+// iff R < frac * 2^16 for the element's 16 random bits R (read as an
+// integer); it carries y's sign, and |y| >= 6 gives 6.
 // ys = a * 2^-126 rounded up maps the grid onto FP32 values with one
 // mantissa bit: 1 -> 2^-126 (the smallest normal), the spacing 0.5 below 2
 // onto the subnormal / first-binade spacing 2^-127, and so on up to 6.  Its
@@ -437,22 +397,6 @@ QD uint32_t sr_dither_hi(uint32_t w, uint32_t m) { return m & ~((w >> 10) & 0x3F
 // finite, 0 otherwise.
 QD uint32_t sr_dither_mask(float enc) { return (__float_as_uint(enc) & 0x7F800000u) != 0x7F800000u ? 0x3FFFFFu : 0u; }
 
-// The two 16-bit draws of a Philox word (low half first) as exact floats.
-QD void r16_pair(uint32_t w, float &lo, float &hi)
-{
-    asm("{\n\t.reg .u16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-        "cvt.rn.f32.u16 %0, l;\n\tcvt.rn.f32.u16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi) : "r"(w));
-}
-
-// The 8 draws of a Philox block as exact floats, element e in rf[e].
-QD void r16_block(const uint4 &R, float *rf)
-{
-    r16_pair(R.x, rf[0], rf[1]);
-    r16_pair(R.y, rf[2], rf[3]);
-    r16_pair(R.z, rf[4], rf[5]);
-    r16_pair(R.w, rf[6], rf[7]);
-}
 
 // ---------------------------------------------------------------------------
 // reductions
