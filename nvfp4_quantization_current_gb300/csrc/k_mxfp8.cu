@@ -7,8 +7,10 @@
 // Scale code = clamp(floor(log2 b) - emax + 127, 0, 254), emax = 8 (E4M3) or
 // 15 (E5M2), b = 0 -> 127; q = RTNE-saturate(x * 2^(127 - code)).
 //
-// On the tile engine (128 x TC tiles in shared memory): thread (warp w,
-// lane l) holds rows 8w..8w+7 x one 16-byte column chunk in registers.
+// On the tile engine with two 256-thread CTAs per SM (64 x TC tiles in
+// shared memory, TileCfg<64, 256>; one CTA's barrier and latency-bound phases
+// overlap the other's work): thread (warp w, lane l) holds rows 8w..8w+7 x
+// one 16-byte column chunk in registers.
 //  row pass - a 1x32 block spans 32/VEC lanes (xor-shuffle max);
 //  col pass - each warp reduces its 8 rows per column in registers; the four
 //             warps of a 32-row block meet in shared memory (one barrier);
@@ -21,19 +23,21 @@
 
 namespace qk {
 
+using MxCfg = TileCfg<64, 256, 3>;
+
 template <int DT, int FMT>
-__global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
-                                                          uint8_t *__restrict__ q_row, uint8_t *__restrict__ e_row,
-                                                          uint8_t *__restrict__ q_col, uint8_t *__restrict__ e_col,
-                                                          int32_t *status)
+__global__ void __launch_bounds__(MxCfg::kThreads, 2) k_mxfp8(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K,
+                                                              uint8_t *__restrict__ q_row, uint8_t *__restrict__ e_row,
+                                                              uint8_t *__restrict__ q_col, uint8_t *__restrict__ e_col,
+                                                              int32_t *status)
 {
     constexpr int VEC = In<DT>::VEC, TC = 32 * VEC, CW = VEC / 4, LPB = 32 / VEC;
-    __shared__ uint4 part[kEngWarps][32];   // per-warp column maxima over 8 rows (packed like the input)
+    __shared__ uint4 part[MxCfg::kThreads / 32][32];   // per-warp column maxima over 8 rows (packed like the input)
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
+    const int64_t tiles_m = (M + MxCfg::kRows - 1) / MxCfg::kRows, tiles_k = (K + TC - 1) / TC;
 
-    run_tiles(&tmap, tiles_m, tiles_k, TC, false, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
-        const int64_t mb = tm * kTileRowsE, kb = tk * TC;
+    run_tiles<MxCfg>(&tmap, tiles_m, tiles_k, TC, false, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
+        const int64_t mb = tm * MxCfg::kRows, kb = tk * TC;
         const int64_t k = kb + lane * VEC, m0 = mb + 8 * warp;
         const bool kok = k < K;
         uint4 v[8];
@@ -176,8 +180,9 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8(const __grid_constant_
 // travels; a dequantize and re-quantize in the other direction makes the
 // columnwise copy).  x_hat = code * 2^(e_row - 127) (one exact FP32
 // product), then 32x1 blocks of x_hat as in k_mxfp8.  On the tile engine over
-// the code matrix: a stage is 128 rows x 512 codes, thread (warp w, lane l)
-// covers rows 8w..8w+7 x codes 16l..16l+15; x_hat is formed twice from the
+// the code matrix (two 256-thread CTAs per SM, TileCfg<64, 256>): a stage is
+// 64 rows x 512 codes, thread (warp w, lane l) covers rows 8w..8w+7 x codes
+// 16l..16l+15; x_hat is formed twice from the
 // stage (once for the column maxima, which meet across the 4 warps of a
 // 32-row block in shared memory, once for the codes) instead of being held
 // in registers.
@@ -198,13 +203,14 @@ template <int FMT> QD void dq16(const uint4 &c, float f, float *x)
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8_requant(const __grid_constant__ CUtensorMap tmap, int64_t M,
-                                                                  int64_t K, const uint8_t *__restrict__ e_row,
-                                                                  uint8_t *__restrict__ q_col, uint8_t *__restrict__ e_col,
-                                                                  int32_t *status)
+__global__ void __launch_bounds__(MxCfg::kThreads, 2) k_mxfp8_requant(const __grid_constant__ CUtensorMap tmap, int64_t M,
+                                                                      int64_t K, const uint8_t *__restrict__ e_row,
+                                                                      uint8_t *__restrict__ q_col, uint8_t *__restrict__ e_col,
+                                                                      int32_t *status)
 {
     constexpr int TC = 512;   // codes per tile row
-    __shared__ uint32_t part[kEngWarps][16][32];   // per warp, column, lane: |x_hat| maxima over 8 rows
+    constexpr int kTileRowsE = MxCfg::kRows;
+    __shared__ uint32_t part[MxCfg::kThreads / 32][16][32];   // per warp, column, lane: |x_hat| maxima over 8 rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles_m = (M + kTileRowsE - 1) / kTileRowsE, tiles_k = (K + TC - 1) / TC;
 
@@ -222,7 +228,7 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_mxfp8_requant(const __grid_c
     load_e(blockIdx.x);
 
     // the tensor map counts 2-byte elements: a tile is 256 of them per row
-    run_tiles(&tmap, tiles_m, tiles_k, TC / 2, false, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
+    run_tiles<MxCfg>(&tmap, tiles_m, tiles_k, TC / 2, false, status, [&](uint8_t *st, int64_t tm, int64_t tk) {
         const int64_t mb = tm * kTileRowsE, kb = tk * TC;
         const int64_t k = kb + lane * 16, m0 = mb + 8 * warp;
         const bool kok = k < K;
@@ -287,15 +293,16 @@ static cudaError_t mx_requant_t(const uint8_t *q_row, const uint8_t *e_row, int6
                                 uint8_t *e_col, int32_t *status, cudaStream_t st)
 {
     alignas(64) CUtensorMap map;
-    cudaError_t e = make_tile_map(&map, q_row, U8, M, K);
+    cudaError_t e = make_tile_map(&map, q_row, U8, M, K, MxCfg::kRows);
     if (e != cudaSuccess) return e;
     {
-        const cudaError_t ea = engine_smem_ready<k_mxfp8_requant<FMT>>();
+        const cudaError_t ea = engine_smem_ready<k_mxfp8_requant<FMT>>(MxCfg::kSmem, true);
         if (ea != cudaSuccess) return ea;
     }
-    const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + 511) / 512);
-    const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-    k_mxfp8_requant<FMT><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, e_row, q_col, e_col, status);
+    const int64_t tiles = ((M + MxCfg::kRows - 1) / MxCfg::kRows) * ((K + 511) / 512);
+    const int64_t slots = 2 * (int64_t)sm_count();   // two CTAs per SM
+    const int grid = (int)(tiles < slots ? tiles : slots);
+    k_mxfp8_requant<FMT><<<grid, MxCfg::kThreads, MxCfg::kSmem, st>>>(map, M, K, e_row, q_col, e_col, status);
     return cudaGetLastError();
 }
 
@@ -312,15 +319,16 @@ static cudaError_t mx_t(const void *x, int64_t M, int64_t K, uint8_t *q_row, uin
 {
     constexpr int TC = 32 * In<DT>::VEC;
     alignas(64) CUtensorMap map;
-    cudaError_t e = make_tile_map(&map, x, DT, M, K);
+    cudaError_t e = make_tile_map(&map, x, DT, M, K, MxCfg::kRows);
     if (e != cudaSuccess) return e;
     {
-        const cudaError_t ea = engine_smem_ready<k_mxfp8<DT, FMT>>();
+        const cudaError_t ea = engine_smem_ready<k_mxfp8<DT, FMT>>(MxCfg::kSmem, true);
         if (ea != cudaSuccess) return ea;
     }
-    const int64_t tiles = ((M + kTileRowsE - 1) / kTileRowsE) * ((K + TC - 1) / TC);
-    const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-    k_mxfp8<DT, FMT><<<grid, kEngThreads, kEngSmem, st>>>(map, M, K, q_row, e_row, q_col, e_col, status);
+    const int64_t tiles = ((M + MxCfg::kRows - 1) / MxCfg::kRows) * ((K + TC - 1) / TC);
+    const int64_t slots = 2 * (int64_t)sm_count();   // two CTAs per SM
+    const int grid = (int)(tiles < slots ? tiles : slots);
+    k_mxfp8<DT, FMT><<<grid, MxCfg::kThreads, MxCfg::kSmem, st>>>(map, M, K, q_row, e_row, q_col, e_col, status);
     return cudaGetLastError();
 }
 
