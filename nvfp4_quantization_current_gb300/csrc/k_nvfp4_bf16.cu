@@ -9,31 +9,36 @@
 //   enc = alpha_g / sb (0 if sb is 0), q = E2M1(x * enc).
 //
 // Two CTAs of 256 threads per SM, each with its own three 64 x 256 stages
-// (32 KiB of BF16 each; TileCfg<64, 256>): one CTA's barriers and
-// latency-bound phases overlap the other's work, which one 512-thread CTA
-// with 128-row tiles could not (its 16 warps move through the same phases
-// together).
-// Thread layout.  The 8 warps of a CTA cover a 64 x 256 tile: warp w takes
-// rows 16 (w / 2) .. + 15 and columns 128 (w % 2) .. + 127 of the tile; lane
-// l takes 8 of those rows (8 (l / 16) .. + 7) of one 16-byte column chunk
-// (columns 8 (l % 16) .. + 7).  Hence
-//   a 1x16 row block    is the lane pair l, l ^ 1,
-//   a 16x1 column block is the lane pair l, l ^ 16,
-//   a 16x16 block       is the lanes l, l ^ 1, l ^ 16, l ^ 17:
-// block maxima and block factors move by warp shuffles, and each block's
-// scale is computed once (the two lanes of a pair split the pair's rows or
-// columns between them and swap the factors).
-// Row codes leave from registers (4 bytes per row and thread).  The
-// columnwise codes of a thread (one word of 8 row nibbles per column) are
-// parked in a buffer of their own behind the stages and leave as 16-byte
-// pieces of q_colT rows, the column block scales through shared memory as
-// 4-byte pieces of sb_colT rows.
+// (32 KiB of BF16 each; TileCfg<64, 256>).
 //
-// Stochastic rounding: Philox4x32-10 with round keys formed on the host;
-// the rowwise copy draws one Philox block per row and thread (8 consecutive
-// columns, stream 0), the columnwise copy one per column and thread (8
-// consecutive rows, stream 1); each element is rounded with
-// sr_e2m1_dither.
+// Block scales come from two per-CTA tables built once from alpha_g: a byte
+// table of sb over the BF16 bit patterns of b in a 24-binade window (below
+// it sb is 0, above it 0x7E; see nv_lut_base) and the 128 encode factors
+// alpha_g / f(sb).  A block whose maximum is not finite, and every block of
+// a CTA whose alpha_g is not a normal float (an amax of inf or NaN), takes
+// the two operations instead.
+//
+// 1x16 (k_nvfp4_bf16_1x16): the warps of a CTA split the two copies.
+//   Row warps: a thread quantizes whole 1x16 row blocks (two 16-byte loads
+//   from the stage, one 8-byte store of codes, one scale byte), so no block
+//   needs a shuffle.
+//   Column warps: a thread takes a pair of adjacent columns over 16-row
+//   groups of the tile (4-byte loads, 32 lanes on 32 consecutive words), and
+//   writes each column's codes as 16-byte pieces of a q_colT row and its
+//   scales as one word (or bytes) of an sb_colT row.
+//   With both copies requested warps 0-3 take the rows and 4-7 the columns;
+//   with one copy all eight warps take it.
+// 16x16 (k_nvfp4_bf16_2d): a thread holds 8 rows x 8 columns (lanes l, l ^ 1,
+//   l ^ 16, l ^ 17 share a block), the codes are computed once rowwise and
+//   the columnwise copy is their nibble transpose, parked behind the stages
+//   and written as q_colT rows.
+//
+// Stochastic rounding: Philox4x32-10 with round keys formed on the host.
+// The rowwise copy takes stream 0 block offset + (m K + k) / 8 for the 8
+// consecutive columns k.. of row m, the columnwise copy stream 1 block
+// offset + (m / 8) K + k for the 8 consecutive rows m.. of column k (m a
+// multiple of 8); element j of a block uses the 16 bits at word j / 2, low
+// half for even j, and is rounded with sr_e2m1_dither.
 #include <cstring>
 
 #include "q_engine.cuh"
@@ -42,58 +47,107 @@
 namespace qk {
 
 using NvCfg = TileCfg<64, 256, 3>;
-constexpr int kNvRows = NvCfg::kRows, kNvThreads = NvCfg::kThreads;
-constexpr int kNvTabCopies = 4;                          // interleaved copies of each per-CTA table
-constexpr int kNvParkBytes = 256 * (kNvRows / 2);        // parked columnwise codes of a tile: [256 columns][rows / 2]
-constexpr int kNvSmem = NvCfg::kSmem + kNvParkBytes;     // dynamic shared memory of a CTA
+constexpr int kNvRows = NvCfg::kRows, kNvThreads = NvCfg::kThreads, kNvTC = 256;
+constexpr int kNvTabCopies = 4;                          // interleaved copies of the encode-factor table
+constexpr int kNvParkBytes = 256 * (kNvRows / 2);        // 16x16: parked columnwise codes of a tile
+constexpr int kLutBinades = 24, kLut = kLutBinades * 128;
 
-// Block scale code of a block with maximum b (FP32 bits of a BF16 value):
-// sb = E4M3(RN(RN(b * alpha_g) / 6)), b = 0 -> 0x38.
-// nvb_sb_exact takes the two operations.  nvb_sb_fast, for a normal b and a
-// normal alpha_g = a_m 2^ae (a_m in [1, 2)), writes b = (1 + m/128) 2^(E-127):
-// the rounded quotient is RN(RN((1 + m/128) a_m) / 6) 2^(E-127+ae) while it
-// stays a normal float (rounding commutes with power-of-two scaling), i.e. a
-// per-CTA table over the 128 mantissas (T: this lane's copy) plus an exponent
-// shift.  A quotient below 2^-126 encodes to E4M3 +0 either way and one at or
-// above 2^128 saturates to 448 (0x7E) either way, so the exponent is clamped
-// to [0, 254] instead of branching.  aem = ae - 127.
-// nvb_sb_rare: b needs the two operations (a subnormal, inf or NaN maximum).
+// ---------------------------------------------------------------------------
+// block scales
+// ---------------------------------------------------------------------------
+
+// sb of a block with maximum b (FP32 bits of |x|, a BF16 value): the two
+// operations as written.
 QD uint32_t nvb_sb_exact(uint32_t b, float alpha_g)
 {
     return b == 0 ? 0x38u : e4m3_code(__fdiv_rn(__fmul_rn(__uint_as_float(b), alpha_g), 6.0f));
 }
-QD uint32_t nvb_sb_fast(uint32_t b, const uint32_t *T, int aem)
-{
-    const uint32_t t = T[((b >> 16) & 0x7Fu) * kNvTabCopies];
-    int ne = (int)(t >> 23) + (int)(b >> 23) + aem;
-    ne = min(max(ne, 0), 254);
-    const uint32_t code = e4m3_code(__uint_as_float((t & 0x807FFFFFu) | ((uint32_t)ne << 23)));
-    return b == 0 ? 0x38u : code;
-}
-QD bool nvb_sb_rare(uint32_t b) { return b != 0 && ((b >> 23) - 1u) >= 254u; }
 
-// Block scale codes of N blocks with maxima b[]: the table path, and, when
-// any lane of the warp holds a rare maximum or the CTA has no table (a
-// non-finite amax), the two operations for those (one warp-uniform branch).
+// First BF16 pattern of the table window for alpha_g with biased exponent
+// ea (1..254).  The window covers maxima b with biased exponent E in
+// [244 - ea, 268 - ea).  Below it b < 2^(117 - ea) and alpha_g < 2^(ea - 126),
+// so b alpha_g < 2^-9 and RN(RN(b alpha_g) / 6) <= RN(2^-9 / 6) < 2^-10, half
+// the smallest E4M3 subnormal: code 0.  At or above its top b >= 2^(141 - ea)
+// and alpha_g >= 2^(ea - 127), so b alpha_g >= 2^14 and the quotient exceeds
+// 448: code 0x7E (the same for b = inf).
+QD int nv_lut_base(uint32_t alpha_bits) { return (244 - (int)(alpha_bits >> 23)) * 128; }
+
+// Builds this CTA's tables (all threads; a CTA barrier follows before use).
+QD void nv_build_tables(float alpha_g, bool tab, int lut_base, uint8_t *lut, float *enc_tab)
+{
+    const int t = threadIdx.x;
+    if (t < 128) {
+        const float sv = e4m3_value(t);
+        const float ev = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_g, sv);
+#pragma unroll
+        for (int j = 0; j < kNvTabCopies; j++) enc_tab[t * kNvTabCopies + j] = ev;
+    }
+    if (tab) {
+        for (int i = t; i < kLut; i += blockDim.x) {
+            const int bb = i + lut_base;
+            lut[i] = (uint8_t)((bb >= 0 && bb <= 0x7FFF) ? nvb_sb_exact((uint32_t)bb << 16, alpha_g) : 0u);
+        }
+    }
+}
+
+// sb of N blocks with maxima b[] from the table; when any lane of the warp
+// holds a non-finite maximum or the CTA has no table, the two operations for
+// those (one warp-uniform branch).
 template <int N>
-QD void nvb_sb_codes(const uint32_t (&b)[N], uint32_t (&sb)[N], float alpha_g, const uint32_t *T, int aem, bool tab)
+QD void nv_sb_codes(const uint32_t (&b)[N], uint32_t (&sb)[N], float alpha_g, const uint8_t *lut, int lut_base,
+                    bool tab)
 {
     bool rare = !tab;
 #pragma unroll
     for (int h = 0; h < N; h++) {
-        sb[h] = nvb_sb_fast(b[h], T, aem);
-        rare |= nvb_sb_rare(b[h]);
+        const int idx = min(max((int)(b[h] >> 16) - lut_base, 0), kLut - 1);
+        const uint32_t c = lut[idx];
+        sb[h] = b[h] == 0 ? 0x38u : c;
+        rare |= b[h] >= 0x7F800000u;
     }
     if (__any_sync(0xFFFFFFFFu, rare)) {
 #pragma unroll
         for (int h = 0; h < N; h++)
-            if (!tab || nvb_sb_rare(b[h])) sb[h] = nvb_sb_exact(b[h], alpha_g);
+            if (!tab || b[h] >= 0x7F800000u) sb[h] = nvb_sb_exact(b[h], alpha_g);
+    }
+}
+
+QD float nv_enc(const float *enc_tab, uint32_t sb, int lane)
+{
+    return enc_tab[(sb & 0x7Fu) * kNvTabCopies + (lane & (kNvTabCopies - 1))];
+}
+
+// ---------------------------------------------------------------------------
+// element arithmetic
+// ---------------------------------------------------------------------------
+
+// BF16 halves of a word as FP32, by the mixed-precision add x + (-0) (exact;
+// it runs on the FMA pipe, which the rest of the kernel leaves less busy
+// than the integer / logic pipe).
+QD float bf16_lo_f32(uint32_t w)
+{
+    float r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, l, 0f80000000;\n\t}" : "=f"(r) : "r"(w));
+    return r;
+}
+QD float bf16_hi_f32(uint32_t w)
+{
+    float r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, h, 0f80000000;\n\t}" : "=f"(r) : "r"(w));
+    return r;
+}
+QD void bf16x8_to_f32(const uint4 &v, float (&y)[8])
+{
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        y[2 * j] = bf16_lo_f32(word(v, j));
+        y[2 * j + 1] = bf16_hi_f32(word(v, j));
     }
 }
 
 // E2M1 codes of 8 values (y[0] in bits 3-0) after the products y *= enc;
-// with stochastic rounding each element takes the dither of its 16 bits of
-// the Philox block R (element j: word j / 2, low half for even j).
+// with stochastic rounding element j takes the dither of its 16 bits of the
+// Philox block R (word j / 2, low half for even j) under the block's mask dm.
 template <int RND> QD uint32_t nvb_codes8(float (&y)[8], float enc, const uint4 &R, uint32_t dm)
 {
 #pragma unroll
@@ -109,37 +163,37 @@ template <int RND> QD uint32_t nvb_codes8(float (&y)[8], float enc, const uint4 
     return cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
 
-// The 8 BF16 values of a 16-byte chunk as FP32.
-QD void bf16x8_to_f32(const uint4 &v, float (&y)[8])
+// FP32 bits of the larger magnitude of the two BF16 halves of a packed
+// |max| word.
+QD uint32_t halves_max_bits(uint32_t m)
 {
-#pragma unroll
-    for (int j = 0; j < 8; j++) y[j] = elem<BF16>(v, j);
+    const uint32_t mm = hmax_abs2(m, __byte_perm(m, 0u, 0x1032));
+    return (mm << 16) & 0x7FFF0000u;
 }
 
-template <int BLK, int RND>
+// ---------------------------------------------------------------------------
+// 1x16
+// ---------------------------------------------------------------------------
+
+// MODE 0: both copies (warps 0-3 rows, 4-7 columns); 1: rowwise only;
+// 2: columnwise only (all warps).
+template <int MODE, int RND>
 __global__ void __launch_bounds__(kNvThreads, 2)
-    k_nvfp4_bf16(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K, const float *__restrict__ amax,
-                 const __grid_constant__ PhiloxKeys keys, uint64_t offset, uint8_t *__restrict__ q_row,
-                 uint8_t *__restrict__ sb_row, uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
-                 float *__restrict__ s_global, int32_t *status)
+    k_nvfp4_bf16_1x16(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K, const float *__restrict__ amax,
+                      const __grid_constant__ PhiloxKeys keys, uint64_t offset, uint8_t *__restrict__ q_row,
+                      uint8_t *__restrict__ sb_row, uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
+                      float *__restrict__ s_global, int32_t *status)
 {
-    constexpr int TC = 256;   // tile columns
-    __shared__ float enc_tab[128 * kNvTabCopies];      // alpha_g / f(code), entry e copy j at e * copies + j
-    __shared__ uint32_t sb_tab[128 * kNvTabCopies];    // RN(RN((1 + m/128) a_m) / 6) per mantissa m
-    __shared__ __align__(8) uint8_t sSB[kNvRows / 16][TC];   // 1x16: column block scales [16-row group][tile column]
-    extern __shared__ __align__(1024) uint8_t dsm[];
-    uint8_t *const park = dsm + NvCfg::kSmem;
+    constexpr int NR = MODE == 0 ? 128 : MODE == 1 ? 256 : 0;   // row threads (threads 0 .. NR - 1)
+    constexpr int NC = kNvThreads - NR;                          // column threads (the rest)
+    __shared__ float enc_tab[128 * kNvTabCopies];
+    __shared__ uint8_t lut[kLut];
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int wr = warp >> 1, wc = warp & 1, rp = lane >> 4, cc = lane & 15;
-    const int tr = 16 * wr + 8 * rp;      // the thread's first row in a tile
-    const int tcol = 128 * wc + 8 * cc;   // its first column in a tile
-    const float *encT = enc_tab + (lane & (kNvTabCopies - 1));
-    const uint32_t *sbT = sb_tab + (lane & (kNvTabCopies - 1));
-    const int64_t tiles_m = (M + kNvRows - 1) / kNvRows, tiles_k = (K + TC - 1) / TC;
+    const int64_t tiles_m = (M + kNvRows - 1) / kNvRows, tiles_k = (K + kNvTC - 1) / kNvTC;
     float alpha_g = 1.0f;
-    int aem = 0;        // exponent of alpha_g minus 127, for the mantissa table
-    bool tab = true;    // alpha_g is a normal float, so the mantissa table applies
+    int lut_base = 0;
+    bool tab = true;   // alpha_g is a normal float, so the byte table applies
 
     // after the first tiles are requested: the tensor scale from the amax of
     // the pass ahead of this kernel, and the per-CTA tables
@@ -149,20 +203,10 @@ __global__ void __launch_bounds__(kNvThreads, 2)
         alpha_g = alpha_from_amax(2688.0f, A);
         const uint32_t ag = __float_as_uint(alpha_g);
         // alpha_g is a normal float for every finite amax (1 for amax 0); a
-        // non-finite amax gives 0 or NaN, which the mantissa table cannot scale
+        // non-finite amax gives 0 or NaN
         tab = (ag >> 23) != 0u && (ag >> 23) != 255u;
-        aem = (int)(ag >> 23) - 254;
-        if (t < 128) {
-            const float sv = e4m3_value(t);
-            const float ev = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_g, sv);
-            const float a_m = __uint_as_float((ag & 0x807FFFFFu) | (127u << 23));
-            const uint32_t tv = __float_as_uint(__fdiv_rn(__fmul_rn(1.0f + (float)t * (1.0f / 128.0f), a_m), 6.0f));
-#pragma unroll
-            for (int j = 0; j < kNvTabCopies; j++) {
-                enc_tab[t * kNvTabCopies + j] = ev;
-                sb_tab[t * kNvTabCopies + j] = tv;
-            }
-        }
+        lut_base = nv_lut_base(ag);
+        nv_build_tables(alpha_g, tab, lut_base, lut, enc_tab);
         if (blockIdx.x == 0 && t == 0) {
             *s_global = __fdiv_rn(1.0f, alpha_g);
             flag_nonfinite(status, __float_as_uint(A) & 0x7FFFFFFFu);
@@ -170,8 +214,181 @@ __global__ void __launch_bounds__(kNvThreads, 2)
         __syncthreads();   // tables visible to every thread
     };
 
+    auto row_part = [&](const uint8_t *st, int64_t mb, int64_t kb, uint32_t &nf) {
+        if constexpr (NR > 0) {
+            constexpr int RPW = kNvRows / (NR / 32);          // rows per row warp
+            constexpr int BPT = kNvRows * (kNvTC / 16) / NR;   // blocks per row thread
+            // block b of row r: the lane's 16-byte loads go to chunks 2b + s and
+            // 2b + 1 - s with s = bit 2 of b, so that the 8 lanes of each load
+            // phase hit 8 different 16-byte bank groups
+            const int b = lane & 15, s = (b >> 2) & 1;
+            const int64_t k0 = kb + 16 * b;
+            const int64_t ka = k0 + 8 * s, kz = k0 + 8 - 8 * s;   // columns of the first / second chunk
+#pragma unroll 2
+            for (int i = 0; i < BPT; i++) {
+                const int r = warp * RPW + 2 * i + (lane >> 4);
+                const int64_t m = mb + r;
+                const uint8_t *src = st + r * kRowBytes + 32 * b;
+                const uint4 va = lds16(src + 16 * s), vz = lds16(src + 16 - 16 * s);
+                const uint32_t mx = hmax_abs2(hmax_abs2(hmax_abs2(va.x, va.y), hmax_abs2(va.z, va.w)),
+                                              hmax_abs2(hmax_abs2(vz.x, vz.y), hmax_abs2(vz.z, vz.w)));
+                uint32_t bits[1] = {halves_max_bits(mx)}, sb[1];
+                nv_sb_codes<1>(bits, sb, alpha_g, lut, lut_base, tab);
+                const float enc = nv_enc(enc_tab, sb[0], lane);
+                const uint32_t dm = RND == 1 ? sr_dither_mask(enc) : 0u;
+                uint4 Ra = make_uint4(0u, 0u, 0u, 0u), Rz = Ra;
+                if (RND == 1) {
+                    Ra = sr_bits_rk<0>(offset + (uint64_t)((m * K + ka) >> 3), keys);
+                    Rz = sr_bits_rk<0>(offset + (uint64_t)((m * K + kz) >> 3), keys);
+                }
+                float y[8];
+                bf16x8_to_f32(va, y);
+                const uint32_t ca = nvb_codes8<RND>(y, enc, Ra, dm);
+                bf16x8_to_f32(vz, y);
+                const uint32_t cz = nvb_codes8<RND>(y, enc, Rz, dm);
+                if (m < M && k0 < K) {
+                    stg8(q_row + m * (K / 2) + (k0 >> 1), s ? cz : ca, s ? ca : cz);
+                    sb_row[m * (K / 16) + (k0 >> 4)] = (uint8_t)sb[0];
+                    nf |= nonfinite(bits[0]);
+                }
+            }
+        }
+    };
+
+    auto col_part = [&](const uint8_t *st, int64_t mb, int64_t kb, uint32_t &nf) {
+        if constexpr (NC > 0) {
+            constexpr int GPT = (kNvRows / 16) * (kNvTC / 2) / NC;   // 16-row groups per column thread
+            const int c = t - NR;
+            const int p = c & (kNvTC / 2 - 1);
+            const int g0 = (c / (kNvTC / 2)) * GPT;
+            const int64_t k = kb + 2 * p;
+            uint32_t code[2][2 * GPT];   // [column][2 group + half]: 8 rows' nibbles, first row in bits 3-0
+            uint32_t sbw[2] = {0u, 0u};  // [column]: scale of group g0 + gi at byte gi
+#pragma unroll
+            for (int gi = 0; gi < GPT; gi++) {
+                const int g = g0 + gi;
+                const uint8_t *src = st + (16 * g) * kRowBytes + 4 * p;
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) w[j] = *reinterpret_cast<const uint32_t *>(src + j * kRowBytes);
+                uint32_t m8[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) m8[j] = hmax_abs2(w[j], w[j + 8]);
+#pragma unroll
+                for (int j = 0; j < 4; j++) m8[j] = hmax_abs2(m8[j], m8[j + 4]);
+                const uint32_t mx = hmax_abs2(hmax_abs2(m8[0], m8[2]), hmax_abs2(m8[1], m8[3]));
+                uint32_t bits[2] = {(mx << 16) & 0x7FFF0000u, mx & 0x7FFF0000u}, sb[2];
+                nv_sb_codes<2>(bits, sb, alpha_g, lut, lut_base, tab);
+                const int64_t m16 = mb + 16 * g;
+                const bool live = m16 < M && k < K;
+#pragma unroll
+                for (int h = 0; h < 2; h++) {   // h = 0: column 2p (low halves), 1: column 2p + 1
+                    const float enc = nv_enc(enc_tab, sb[h], lane);
+                    const uint32_t dm = RND == 1 ? sr_dither_mask(enc) : 0u;
+#pragma unroll
+                    for (int half = 0; half < 2; half++) {   // rows 8 half .. 8 half + 7 of the group
+                        float y[8];
+#pragma unroll
+                        for (int j = 0; j < 8; j++) y[j] = h ? bf16_hi_f32(w[8 * half + j]) : bf16_lo_f32(w[8 * half + j]);
+                        uint4 R = make_uint4(0u, 0u, 0u, 0u);
+                        if (RND == 1)
+                            R = sr_bits_rk<1>(offset + (uint64_t)(((m16 >> 3) + half) * K + k + h), keys);
+                        code[h][2 * gi + half] = nvb_codes8<RND>(y, enc, R, dm);
+                    }
+                    sbw[h] |= sb[h] << (8 * gi);
+                    nf |= live ? nonfinite(bits[h]) : 0u;
+                }
+            }
+            if (k < K) {
+                const int64_t mg = mb + 16 * g0;   // first row of this thread's groups
+                const int64_t left = (M - mg) / 16;
+                const int ng = left < GPT ? (int)(left > 0 ? left : 0) : GPT;   // groups inside the tensor
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    uint8_t *qc = q_colT + (k + h) * (M / 2) + mg / 2;
+                    uint8_t *sc = sb_colT + (k + h) * (M / 16) + mg / 16;
+                    if (ng == GPT && (M & 31) == 0) {
+#pragma unroll
+                        for (int q = 0; q < GPT / 2; q++)
+                            stg16(qc + 16 * q, make_uint4(code[h][4 * q], code[h][4 * q + 1], code[h][4 * q + 2],
+                                                          code[h][4 * q + 3]));
+                    } else {
+#pragma unroll
+                        for (int gi = 0; gi < GPT; gi++)
+                            if (gi < ng) stg8(qc + 8 * gi, code[h][2 * gi], code[h][2 * gi + 1]);
+                    }
+                    if (GPT == 4 && ng == 4 && (M & 63) == 0) {
+                        stg4(sc, sbw[h]);
+                    } else {
+#pragma unroll
+                        for (int gi = 0; gi < GPT; gi++)
+                            if (gi < ng) sc[gi] = (uint8_t)(sbw[h] >> (8 * gi));
+                    }
+                }
+            }
+        }
+    };
+
     auto body = [&](uint8_t *st, int64_t tm, int64_t tk) {
-        const int64_t mb = tm * kNvRows, kb = tk * TC;
+        const int64_t mb = tm * kNvRows, kb = tk * kNvTC;
+        uint32_t nf = 0;   // a non-finite block maximum seen by this thread
+        if (t < NR) row_part(st, mb, kb, nf);
+        else col_part(st, mb, kb, nf);
+        post_nonfinite(status, nf);
+    };
+
+    run_tiles<NvCfg>(&tmap, tiles_m, tiles_k, kNvTC, true, status, pre, body);
+}
+
+// ---------------------------------------------------------------------------
+// 16x16
+// ---------------------------------------------------------------------------
+
+// Thread layout: the 8 warps of a CTA cover a 64 x 256 tile: warp w takes
+// rows 16 (w / 2) .. + 15 and columns 128 (w % 2) .. + 127 of the tile; lane
+// l takes 8 of those rows (8 (l / 16) .. + 7) of one 16-byte column chunk
+// (columns 8 (l % 16) .. + 7), so a 16x16 block is the lanes l, l ^ 1, l ^ 16,
+// l ^ 17.  The columnwise codes of a thread (one word of 8 row nibbles per
+// column) are parked in a buffer of their own behind the stages and leave as
+// 16-byte pieces of q_colT rows.
+template <int RND>
+__global__ void __launch_bounds__(kNvThreads, 2)
+    k_nvfp4_bf16_2d(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K, const float *__restrict__ amax,
+                    const __grid_constant__ PhiloxKeys keys, uint64_t offset, uint8_t *__restrict__ q_row,
+                    uint8_t *__restrict__ sb_row, uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
+                    float *__restrict__ s_global, int32_t *status)
+{
+    __shared__ float enc_tab[128 * kNvTabCopies];
+    __shared__ uint8_t lut[kLut];
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    uint8_t *const park = dsm + NvCfg::kSmem;
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int wr = warp >> 1, wc = warp & 1, rp = lane >> 4, cc = lane & 15;
+    const int tr = 16 * wr + 8 * rp;      // the thread's first row in a tile
+    const int tcol = 128 * wc + 8 * cc;   // its first column in a tile
+    const int64_t tiles_m = (M + kNvRows - 1) / kNvRows, tiles_k = (K + kNvTC - 1) / kNvTC;
+    float alpha_g = 1.0f;
+    int lut_base = 0;
+    bool tab = true;
+
+    auto pre = [&] {
+        griddep_wait();
+        const float A = *amax;
+        alpha_g = alpha_from_amax(2688.0f, A);
+        const uint32_t ag = __float_as_uint(alpha_g);
+        tab = (ag >> 23) != 0u && (ag >> 23) != 255u;
+        lut_base = nv_lut_base(ag);
+        nv_build_tables(alpha_g, tab, lut_base, lut, enc_tab);
+        if (blockIdx.x == 0 && t == 0) {
+            *s_global = __fdiv_rn(1.0f, alpha_g);
+            flag_nonfinite(status, __float_as_uint(A) & 0x7FFFFFFFu);
+        }
+        __syncthreads();
+    };
+
+    auto body = [&](uint8_t *st, int64_t tm, int64_t tk) {
+        const int64_t mb = tm * kNvRows, kb = tk * kNvTC;
         const int64_t m0 = mb + tr, k = kb + tcol;
         // M and K are multiples of 16: a thread's 8 rows and 8 columns are all
         // inside the tensor or all outside
@@ -179,176 +396,59 @@ __global__ void __launch_bounds__(kNvThreads, 2)
         uint4 v[8];
 #pragma unroll
         for (int j = 0; j < 8; j++) v[j] = lds16(st + (tr + j) * kRowBytes + 2 * tcol);
-        uint32_t colw[8];   // columnwise codes: column c -> its 8 rows' nibbles, row tr in bits 3-0
-        uint32_t nf = 0;    // a non-finite block maximum seen by this thread
-
-        if constexpr (BLK == 0) {
-            // ---------------- 1x16 rowwise ----------------
-            if (q_row != nullptr) {
-                // row maxima, two rows per word: P[p] = (row 2p, row 2p + 1)
-                uint32_t P[4];
+        uint32_t colw[8];   // the 8 rows' codes, then (transposed) the 8 columns'
+        uint32_t nf = 0;
+        uint32_t m = 0;
 #pragma unroll
-                for (int p = 0; p < 4; p++) {
-                    const uint4 &a = v[2 * p], &b = v[2 * p + 1];
-                    const uint32_t ma = hmax_abs2(hmax_abs2(a.x, a.y), hmax_abs2(a.z, a.w));
-                    const uint32_t mb2 = hmax_abs2(hmax_abs2(b.x, b.y), hmax_abs2(b.z, b.w));
-                    P[p] = hmax_abs2(__byte_perm(ma, mb2, 0x5410), __byte_perm(ma, mb2, 0x7632));
-                }
-                // the pair's lane with cc even takes the block maxima of rows 0-3,
-                // its partner those of rows 4-7
-                const bool odd = cc & 1;
-                const int rb = odd ? 4 : 0;
-                uint32_t k0 = odd ? P[2] : P[0], k1 = odd ? P[3] : P[1];
-                const uint32_t s0 = odd ? P[0] : P[2], s1 = odd ? P[1] : P[3];
-                k0 = hmax_abs2(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, 1));
-                k1 = hmax_abs2(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, 1));
-                uint32_t bits[4], sb[4];
+        for (int j = 0; j < 8; j++) m = hmax_abs2(m, hmax_abs2(hmax_abs2(v[j].x, v[j].y), hmax_abs2(v[j].z, v[j].w)));
+        uint32_t bb[1] = {halves_max_bits(m)}, sbb[1];
+        bb[0] = max(bb[0], __shfl_xor_sync(0xFFFFFFFFu, bb[0], 1));
+        bb[0] = max(bb[0], __shfl_xor_sync(0xFFFFFFFFu, bb[0], 16));
+        nv_sb_codes<1>(bb, sbb, alpha_g, lut, lut_base, tab);
+        const uint32_t bits = bb[0], sb = sbb[0];
+        const float enc = nv_enc(enc_tab, sb, lane);
+        const int64_t m16 = mb + 16 * wr;   // the block's first row
+        if (live && (lane & 17) == 0) {
+            if (sb_row != nullptr) sb_row[(m16 >> 4) * (K / 16) + (k >> 4)] = (uint8_t)sb;
+            if (sb_colT != nullptr) sb_colT[(k >> 4) * (M / 16) + (m16 >> 4)] = (uint8_t)sb;
+            nf |= nonfinite(bits);
+        }
+        uint8_t *qr = q_row + m0 * (K / 2) + (k >> 1);
+        const uint64_t g0 = offset + (uint64_t)((m0 * K + k) >> 3);
+        const uint32_t dm = RND == 1 ? sr_dither_mask(enc) : 0u;
 #pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    const uint32_t kw = h < 2 ? k0 : k1;
-                    bits[h] = ((h & 1) ? kw : (kw << 16)) & 0x7FFF0000u;
-                }
-                nvb_sb_codes<4>(bits, sb, alpha_g, sbT, aem, tab);
-                float own[4];
-                uint8_t *sbr = sb_row + (m0 + rb) * (K / 16) + (k >> 4);
-#pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    own[h] = encT[(sb[h] & 0x7Fu) * kNvTabCopies];
-                    if (live) {
-                        sbr[h * (K / 16)] = (uint8_t)sb[h];
-                        nf |= nonfinite(bits[h]);
-                    }
-                }
-                float encr[8];
-#pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    const float other = __shfl_xor_sync(0xFFFFFFFFu, own[h], 1);
-                    encr[h] = odd ? other : own[h];
-                    encr[4 + h] = odd ? own[h] : other;
-                }
-                uint8_t *qr = q_row + m0 * (K / 2) + (k >> 1);
-                const uint64_t g0 = offset + (uint64_t)((m0 * K + k) >> 3);   // row m0's Philox block
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    float y[8];
-                    bf16x8_to_f32(v[j], y);
-                    uint4 R = make_uint4(0u, 0u, 0u, 0u);
-                    if (RND == 1) R = sr_bits_rk<0>(g0 + (uint64_t)j * (uint64_t)(K >> 3), keys);
-                    const uint32_t code = nvb_codes8<RND>(y, encr[j], R, RND == 1 ? sr_dither_mask(encr[j]) : 0u);
-                    if (live) stg4(qr + j * (K / 2), code);
-                }
-            }
-            if (q_colT != nullptr) {
-                // ---------------- 16x1 columnwise ----------------
-                // the chunk again from the stage (it stays valid for the whole tile:
-                // the codes are parked elsewhere), so the row pass did not have to
-                // keep it in registers
-                if (q_row != nullptr) {
-#pragma unroll
-                    for (int j = 0; j < 8; j++) v[j] = lds16_again(st + (tr + j) * kRowBytes + 2 * tcol);
-                }
-                // column maxima of the 8 rows (two columns per word), then of the pair's 16
-                uint4 acc = v[0];
-#pragma unroll
-                for (int j = 1; j < 8; j++) {
-                    acc.x = hmax_abs2(acc.x, v[j].x);
-                    acc.y = hmax_abs2(acc.y, v[j].y);
-                    acc.z = hmax_abs2(acc.z, v[j].z);
-                    acc.w = hmax_abs2(acc.w, v[j].w);
-                }
-                acc.x = hmax_abs2(acc.x, __shfl_xor_sync(0xFFFFFFFFu, acc.x, 16));
-                acc.y = hmax_abs2(acc.y, __shfl_xor_sync(0xFFFFFFFFu, acc.y, 16));
-                acc.z = hmax_abs2(acc.z, __shfl_xor_sync(0xFFFFFFFFu, acc.z, 16));
-                acc.w = hmax_abs2(acc.w, __shfl_xor_sync(0xFFFFFFFFu, acc.w, 16));
-                // the lane of the upper 8 rows takes columns 4-7, its partner columns 0-3
-                const uint32_t wA = rp ? acc.z : acc.x, wB = rp ? acc.w : acc.y;
-                uint32_t bits[4], sb[4];
-#pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    const uint32_t w = h < 2 ? wA : wB;
-                    bits[h] = ((h & 1) ? w : (w << 16)) & 0x7FFF0000u;
-                }
-                nvb_sb_codes<4>(bits, sb, alpha_g, sbT, aem, tab);
-                float ownc[4];
-                uint32_t sbw = 0;
-#pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    ownc[h] = encT[(sb[h] & 0x7Fu) * kNvTabCopies];
-                    sbw |= sb[h] << (8 * h);
-                    nf |= live ? nonfinite(bits[h]) : 0u;
-                }
-                *reinterpret_cast<uint32_t *>(&sSB[wr][tcol + 4 * rp]) = sbw;
-                float encc[8];
-#pragma unroll
-                for (int h = 0; h < 4; h++) {
-                    const float other = __shfl_xor_sync(0xFFFFFFFFu, ownc[h], 16);
-                    encc[h] = rp ? other : ownc[h];
-                    encc[4 + h] = rp ? ownc[h] : other;
-                }
-                // column (k + c) rows m0 .. m0 + 7 draw Philox block (m0 / 8) * K + k + c of stream 1
-                const uint64_t gc = offset + (uint64_t)((m0 >> 3) * K + k);
-#pragma unroll
-                for (int c = 0; c < 8; c++) {
-                    float y[8];
-#pragma unroll
-                    for (int j = 0; j < 8; j++) y[j] = elem<BF16>(v[j], c);
-                    uint4 R = make_uint4(0u, 0u, 0u, 0u);
-                    if (RND == 1) R = sr_bits_rk<1>(gc + (uint64_t)c, keys);
-                    colw[c] = nvb_codes8<RND>(y, encc[c], R, RND == 1 ? sr_dither_mask(encc[c]) : 0u);
-                }
-            }
-        } else {
-            // ---------------- 16x16: one scale per block of four lanes ----------------
-            uint32_t m = 0;
-#pragma unroll
-            for (int j = 0; j < 8; j++) m = hmax_abs2(m, hmax_abs2(hmax_abs2(v[j].x, v[j].y), hmax_abs2(v[j].z, v[j].w)));
-            m = hmax_abs2(m, __byte_perm(m, 0u, 0x1032));
-            uint32_t bb[1] = {(m << 16) & 0x7FFF0000u}, sbb[1];
-            bb[0] = max(bb[0], __shfl_xor_sync(0xFFFFFFFFu, bb[0], 1));
-            bb[0] = max(bb[0], __shfl_xor_sync(0xFFFFFFFFu, bb[0], 16));
-            nvb_sb_codes<1>(bb, sbb, alpha_g, sbT, aem, tab);
-            const uint32_t bits = bb[0], sb = sbb[0];
-            const float enc = encT[(sb & 0x7Fu) * kNvTabCopies];
-            const int64_t m16 = mb + 16 * wr;   // the block's first row
-            if (live && (lane & 17) == 0) {
-                if (sb_row != nullptr) sb_row[(m16 >> 4) * (K / 16) + (k >> 4)] = (uint8_t)sb;
-                if (sb_colT != nullptr) sb_colT[(k >> 4) * (M / 16) + (m16 >> 4)] = (uint8_t)sb;
-                nf |= nonfinite(bits);
-            }
-            uint8_t *qr = q_row + m0 * (K / 2) + (k >> 1);
-            const uint64_t g0 = offset + (uint64_t)((m0 * K + k) >> 3);
-            const uint32_t dm = RND == 1 ? sr_dither_mask(enc) : 0u;
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                float y[8];
-                bf16x8_to_f32(v[j], y);
-                uint4 R = make_uint4(0u, 0u, 0u, 0u);
-                if (RND == 1) R = sr_bits_rk<0>(g0 + (uint64_t)j * (uint64_t)(K >> 3), keys);
-                colw[j] = nvb_codes8<RND>(y, enc, R, dm);
-                if (q_row != nullptr && live) stg4(qr + j * (K / 2), colw[j]);
-            }
-            if (q_colT != nullptr) transpose8x8_nibbles(colw);   // now column c -> its 8 rows
+        for (int j = 0; j < 8; j++) {
+            float y[8];
+            bf16x8_to_f32(v[j], y);
+            uint4 R = make_uint4(0u, 0u, 0u, 0u);
+            if (RND == 1) R = sr_bits_rk<0>(g0 + (uint64_t)j * (uint64_t)(K >> 3), keys);
+            colw[j] = nvb_codes8<RND>(y, enc, R, dm);
+            if (q_row != nullptr && live) stg4(qr + j * (K / 2), colw[j]);
         }
         post_nonfinite(status, nf);
         if (q_colT == nullptr) return;
-        // ---- columnwise codes: parked as [column][rows / 2 bytes], 4-byte slot tr / 8
-        // XOR-swizzled by the column chunk, then written as q_colT rows
+        transpose8x8_nibbles(colw);   // now column c -> its 8 rows
+        // parked as [column][rows / 2 bytes], 4-byte slot tr / 8 XOR-swizzled
+        // by the column chunk, then written as q_colT rows
 #pragma unroll
         for (int c = 0; c < 8; c++)
             *reinterpret_cast<uint32_t *>(park + (tcol + c) * (kNvRows / 2) +
                                           ((((tr >> 3) ^ cc) & (kNvRows / 8 - 1)) * 4)) = colw[c];
         __syncthreads();
         copy_out_fp4T<8, kNvRows, kNvThreads>(park, q_colT, M, K, mb, kb);
-        if constexpr (BLK == 0) copy_out_sbT<TC, kNvRows, kNvThreads>(sSB, sb_colT, M, K, mb, kb);
     };
 
-    run_tiles<NvCfg>(&tmap, tiles_m, tiles_k, TC, true, status, pre, body);
+    run_tiles<NvCfg>(&tmap, tiles_m, tiles_k, kNvTC, true, status, pre, body);
 }
 
-template <int BLK, int RND>
-static cudaError_t nvb_t(const void *x, int64_t M, int64_t K, const float *amax, uint64_t seed, uint64_t offset,
-                         uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT, float *s_global,
-                         int32_t *status, cudaStream_t st, bool after_amax)
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+
+template <auto Kernel>
+static cudaError_t nvb_launch(int smem, const void *x, int64_t M, int64_t K, const float *amax, uint64_t seed,
+                              uint64_t offset, uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT,
+                              float *s_global, int32_t *status, cudaStream_t st, bool after_amax)
 {
     alignas(64) CUtensorMap map;
     if (M != 0 && K != 0) {
@@ -358,16 +458,16 @@ static cudaError_t nvb_t(const void *x, int64_t M, int64_t K, const float *amax,
         memset(&map, 0, sizeof map);   // never dereferenced: an empty tensor has no tiles
     }
     {
-        const cudaError_t ea = engine_smem_ready<k_nvfp4_bf16<BLK, RND>>(kNvSmem, true);
+        const cudaError_t ea = engine_smem_ready<Kernel>(smem, true);
         if (ea != cudaSuccess) return ea;
     }
-    const int64_t tiles = ((M + kNvRows - 1) / kNvRows) * ((K + 255) / 256);
+    const int64_t tiles = ((M + kNvRows - 1) / kNvRows) * ((K + kNvTC - 1) / kNvTC);
     const int64_t slots = 2 * (int64_t)sm_count();   // two CTAs per SM
     int grid = (int)(tiles < slots ? tiles : slots);
     if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
     const PhiloxKeys keys = philox_keys(seed);
-    return launch_k(after_amax, k_nvfp4_bf16<BLK, RND>, dim3(grid), dim3(kNvThreads), kNvSmem, st, map, M, K, amax,
-                    keys, offset, q_row, sb_row, q_colT, sb_colT, s_global, status);
+    return launch_k(after_amax, Kernel, dim3(grid), dim3(kNvThreads), smem, st, map, M, K, amax, keys, offset, q_row,
+                    sb_row, q_colT, sb_colT, s_global, status);
 }
 
 cudaError_t launch_nvfp4_bf16(const void *x, int64_t M, int64_t K, int blk, int rnd, uint64_t seed, uint64_t offset,
@@ -375,8 +475,19 @@ cudaError_t launch_nvfp4_bf16(const void *x, int64_t M, int64_t K, int blk, int 
                               float *s_global, int32_t *status, cudaStream_t st, bool after_amax)
 {
 #define NVB_ARGS x, M, K, amax, seed, offset, q_row, sb_row, q_colT, sb_colT, s_global, status, st, after_amax
-    if (blk == 0) return rnd == 0 ? nvb_t<0, 0>(NVB_ARGS) : nvb_t<0, 1>(NVB_ARGS);
-    return rnd == 0 ? nvb_t<1, 0>(NVB_ARGS) : nvb_t<1, 1>(NVB_ARGS);
+    if (blk == 1) {
+        constexpr int smem = NvCfg::kSmem + kNvParkBytes;
+        return rnd == 0 ? nvb_launch<k_nvfp4_bf16_2d<0>>(smem, NVB_ARGS) : nvb_launch<k_nvfp4_bf16_2d<1>>(smem, NVB_ARGS);
+    }
+    constexpr int smem = NvCfg::kSmem;
+    if (q_row != nullptr && q_colT != nullptr)
+        return rnd == 0 ? nvb_launch<k_nvfp4_bf16_1x16<0, 0>>(smem, NVB_ARGS)
+                        : nvb_launch<k_nvfp4_bf16_1x16<0, 1>>(smem, NVB_ARGS);
+    if (q_colT == nullptr)   // rowwise only (also an empty tensor with no outputs)
+        return rnd == 0 ? nvb_launch<k_nvfp4_bf16_1x16<1, 0>>(smem, NVB_ARGS)
+                        : nvb_launch<k_nvfp4_bf16_1x16<1, 1>>(smem, NVB_ARGS);
+    return rnd == 0 ? nvb_launch<k_nvfp4_bf16_1x16<2, 0>>(smem, NVB_ARGS)
+                    : nvb_launch<k_nvfp4_bf16_1x16<2, 1>>(smem, NVB_ARGS);
 #undef NVB_ARGS
 }
 
