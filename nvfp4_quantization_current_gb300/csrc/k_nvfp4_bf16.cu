@@ -23,9 +23,12 @@
 //   from the stage, one 8-byte store of codes, one scale byte), so no block
 //   needs a shuffle.
 //   Column warps: a thread takes a pair of adjacent columns over 16-row
-//   groups of the tile (4-byte loads, 32 lanes on 32 consecutive words), and
-//   writes each column's codes as 16-byte pieces of a q_colT row and its
-//   scales as one word (or bytes) of an sb_colT row.
+//   groups of the tile (4-byte loads, 32 lanes on 32 consecutive words).
+//   The tile's columnwise codes are collected in shared memory as the dense
+//   256 x 32-byte box of q_colT that they fill, and one bulk tensor store
+//   (TMA) writes it in whole sectors; scattered 16-byte stores from the
+//   lanes cost the load/store pipe a sector operation each.  The scales go
+//   out as one word (or bytes) of an sb_colT row per column.
 //   With both copies requested warps 0-3 take the rows and 4-7 the columns;
 //   with one copy all eight warps take it.
 // 16x16 (k_nvfp4_bf16_2d): a thread holds 8 rows x 8 columns (lanes l, l ^ 1,
@@ -182,12 +185,15 @@ __global__ void __launch_bounds__(kNvThreads, 2)
     k_nvfp4_bf16_1x16(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K, const float *__restrict__ amax,
                       const __grid_constant__ PhiloxKeys keys, uint64_t offset, uint8_t *__restrict__ q_row,
                       uint8_t *__restrict__ sb_row, uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
-                      float *__restrict__ s_global, int32_t *status)
+                      float *__restrict__ s_global, int32_t *status, const __grid_constant__ CUtensorMap cmap,
+                      int col_tma)
 {
     constexpr int NR = MODE == 0 ? 128 : MODE == 1 ? 256 : 0;   // row threads (threads 0 .. NR - 1)
     constexpr int NC = kNvThreads - NR;                          // column threads (the rest)
     __shared__ float enc_tab[128 * kNvTabCopies];
     __shared__ uint8_t lut[kLut];
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    uint8_t *const park = dsm + NvCfg::kSmem;   // columnwise codes of a tile: [256 columns][32 bytes]
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t tiles_m = (M + kNvRows - 1) / kNvRows, tiles_k = (K + kNvTC - 1) / kNvTC;
@@ -299,6 +305,25 @@ __global__ void __launch_bounds__(kNvThreads, 2)
                     nf |= live ? nonfinite(bits[h]) : 0u;
                 }
             }
+            if (col_tma) {
+                // the tile's columnwise codes as a dense [256 columns][32 bytes]
+                // box, which one bulk tensor store writes (the parts past the
+                // tensor's edges are not written)
+                if (c == 0) bulk_wait_read_all();   // the previous tile's store has read the box
+                named_barrier(1, NC);
+#pragma unroll
+                for (int h = 0; h < 2; h++)
+#pragma unroll
+                    for (int q = 0; q < GPT / 2; q++)
+                        *reinterpret_cast<uint4 *>(park + (2 * p + h) * 32 + 8 * g0 + 16 * q) =
+                            make_uint4(code[h][4 * q], code[h][4 * q + 1], code[h][4 * q + 2], code[h][4 * q + 3]);
+                fence_proxy_async();   // generic-proxy writes of the box before the async-proxy read
+                named_barrier(1, NC);
+                if (c == 0) {
+                    tma_store_tile(&cmap, park, (int)(mb / 2), (int)kb);
+                    bulk_commit();
+                }
+            }
             if (k < K) {
                 const int64_t mg = mb + 16 * g0;   // first row of this thread's groups
                 const int64_t left = (M - mg) / 16;
@@ -307,7 +332,9 @@ __global__ void __launch_bounds__(kNvThreads, 2)
                 for (int h = 0; h < 2; h++) {
                     uint8_t *qc = q_colT + (k + h) * (M / 2) + mg / 2;
                     uint8_t *sc = sb_colT + (k + h) * (M / 16) + mg / 16;
-                    if (ng == GPT && (M & 31) == 0) {
+                    if (col_tma) {
+                        // codes leave with the bulk store
+                    } else if (ng == GPT && (M & 31) == 0) {
 #pragma unroll
                         for (int q = 0; q < GPT / 2; q++)
                             stg16(qc + 16 * q, make_uint4(code[h][4 * q], code[h][4 * q + 1], code[h][4 * q + 2],
@@ -338,6 +365,7 @@ __global__ void __launch_bounds__(kNvThreads, 2)
     };
 
     run_tiles<NvCfg>(&tmap, tiles_m, tiles_k, kNvTC, true, status, pre, body);
+    if (NC > 0 && col_tma && t == NR) bulk_wait_all();   // the last box is written before the CTA ends
 }
 
 // ---------------------------------------------------------------------------
@@ -445,6 +473,41 @@ __global__ void __launch_bounds__(kNvThreads, 2)
 // launchers
 // ---------------------------------------------------------------------------
 
+// 1x16: the input's tensor map, and, when the columnwise copy is requested
+// and its rows (M / 2 bytes) are a multiple of 16 bytes, a store map over
+// q_colT for the bulk tensor stores of the column warps.
+template <auto Kernel>
+static cudaError_t nvb_launch_1x16(const void *x, int64_t M, int64_t K, const float *amax, uint64_t seed,
+                                   uint64_t offset, uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT,
+                                   float *s_global, int32_t *status, cudaStream_t st, bool after_amax)
+{
+    constexpr int smem = NvCfg::kSmem + kNvParkBytes;
+    alignas(64) CUtensorMap map, cmap;
+    memset(&map, 0, sizeof map);
+    memset(&cmap, 0, sizeof cmap);
+    int col_tma = 0;
+    if (M != 0 && K != 0) {
+        cudaError_t e = make_tile_map(&map, x, BF16, M, K, kNvRows);
+        if (e != cudaSuccess) return e;
+        if (q_colT != nullptr && (M % 32) == 0) {
+            e = make_store_map_u8(&cmap, q_colT, M / 2, K, kNvRows / 2, kNvTC);
+            if (e != cudaSuccess) return e;
+            col_tma = 1;
+        }
+    }
+    {
+        const cudaError_t ea = engine_smem_ready<Kernel>(smem, true);
+        if (ea != cudaSuccess) return ea;
+    }
+    const int64_t tiles = ((M + kNvRows - 1) / kNvRows) * ((K + kNvTC - 1) / kNvTC);
+    const int64_t slots = 2 * (int64_t)sm_count();   // two CTAs per SM
+    int grid = (int)(tiles < slots ? tiles : slots);
+    if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
+    const PhiloxKeys keys = philox_keys(seed);
+    return launch_k(after_amax, Kernel, dim3(grid), dim3(kNvThreads), smem, st, map, M, K, amax, keys, offset, q_row,
+                    sb_row, q_colT, sb_colT, s_global, status, cmap, col_tma);
+}
+
 template <auto Kernel>
 static cudaError_t nvb_launch(int smem, const void *x, int64_t M, int64_t K, const float *amax, uint64_t seed,
                               uint64_t offset, uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT,
@@ -479,15 +542,14 @@ cudaError_t launch_nvfp4_bf16(const void *x, int64_t M, int64_t K, int blk, int 
         constexpr int smem = NvCfg::kSmem + kNvParkBytes;
         return rnd == 0 ? nvb_launch<k_nvfp4_bf16_2d<0>>(smem, NVB_ARGS) : nvb_launch<k_nvfp4_bf16_2d<1>>(smem, NVB_ARGS);
     }
-    constexpr int smem = NvCfg::kSmem;
     if (q_row != nullptr && q_colT != nullptr)
-        return rnd == 0 ? nvb_launch<k_nvfp4_bf16_1x16<0, 0>>(smem, NVB_ARGS)
-                        : nvb_launch<k_nvfp4_bf16_1x16<0, 1>>(smem, NVB_ARGS);
+        return rnd == 0 ? nvb_launch_1x16<k_nvfp4_bf16_1x16<0, 0>>(NVB_ARGS)
+                        : nvb_launch_1x16<k_nvfp4_bf16_1x16<0, 1>>(NVB_ARGS);
     if (q_colT == nullptr)   // rowwise only (also an empty tensor with no outputs)
-        return rnd == 0 ? nvb_launch<k_nvfp4_bf16_1x16<1, 0>>(smem, NVB_ARGS)
-                        : nvb_launch<k_nvfp4_bf16_1x16<1, 1>>(smem, NVB_ARGS);
-    return rnd == 0 ? nvb_launch<k_nvfp4_bf16_1x16<2, 0>>(smem, NVB_ARGS)
-                    : nvb_launch<k_nvfp4_bf16_1x16<2, 1>>(smem, NVB_ARGS);
+        return rnd == 0 ? nvb_launch_1x16<k_nvfp4_bf16_1x16<1, 0>>(NVB_ARGS)
+                        : nvb_launch_1x16<k_nvfp4_bf16_1x16<1, 1>>(NVB_ARGS);
+    return rnd == 0 ? nvb_launch_1x16<k_nvfp4_bf16_1x16<2, 0>>(NVB_ARGS)
+                    : nvb_launch_1x16<k_nvfp4_bf16_1x16<2, 1>>(NVB_ARGS);
 #undef NVB_ARGS
 }
 

@@ -123,6 +123,22 @@ QD void tma_load_tile(void *dst, const CUtensorMap *map, int x, int y, uint64_t 
                  ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
 }
 
+// A 2-D tile from shared memory to global memory (x = first column in
+// elements, y = first row; the parts of the box outside the tensor are not
+// written), in this thread's bulk-async group.
+QD void tma_store_tile(const CUtensorMap *map, const void *src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(map), "r"(x), "r"(y), "r"(smem_u32(src)) : "memory");
+}
+QD void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's committed bulk stores have finished reading shared memory.
+QD void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// This thread's committed bulk stores are complete.
+QD void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Barrier `id` (1..15) among `count` threads (whole warps).
+QD void named_barrier(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
+
 QD uint4 lds16(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 // The same load, issued again even when the compiler could reuse an earlier
 // one (a second pass over a stage re-reads it instead of keeping registers).

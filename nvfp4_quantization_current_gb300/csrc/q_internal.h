@@ -37,6 +37,12 @@ cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 cudaError_t make_tile_map(void *map /* CUtensorMap, 64-byte aligned */, const void *x, int dt, int64_t M, int64_t K,
                           int box_rows = 128);
 
+// A 2-D TMA tensor map for bulk stores into a row-major byte matrix of
+// `rows` rows of row_bytes bytes (row_bytes a multiple of 16, base 16-byte
+// aligned), box box_bytes x box_rows (box_bytes a multiple of 16, both <= 256).
+cudaError_t make_store_map_u8(void *map /* CUtensorMap, 64-byte aligned */, void *base, int64_t row_bytes,
+                              int64_t rows, int box_bytes, int box_rows);
+
 // current scaling
 cudaError_t launch_amax(const void *x, int dt, int64_t n, float *amax, int32_t *status, cudaStream_t st);
 cudaError_t launch_cs_cast(const void *x, int dt, int64_t M, int64_t K, int fmt, const float *amax,
