@@ -11,8 +11,9 @@
 // element is rounded to nearest; BF16 output rounds that FP32 value to
 // nearest even.
 //
-// Work unit: 16 bytes of output per lane (8 elements for BF16 output, 4 for
-// FP32), so that one warp store covers 512 contiguous bytes.  A CTA of 256
+// Work unit of the FP8 kernels: 16 bytes of output per lane (8 elements for
+// BF16 output, 4 for FP32), so that one warp store covers 512 contiguous
+// bytes; NVFP4 units are 16-element block rows (k_dq_fp4).  A CTA of 256
 // threads covers BX units x BY rows (BX = units per row rounded to a power
 // of two, at most 256); each thread keeps kDqRows rows of loads in flight
 // (4: more, shorter CTAs fill the waves of mid-size tensors better than 8).
@@ -93,25 +94,21 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_cs(const uint8_t *__restrict_
 }
 
 // ---------------------------------------------------------------------------
-// block-scaled codes.  KIND 0: MX row, e [R, C/32]; 1: MX col, e [R/32, C];
-// 2: blockwise 1x128, s [R, C/128]; 3: blockwise 128x128, s [R/128, C/128];
-// 4: NVFP4 1x16, sb [R, C/16] + s_g; 5: NVFP4 16x16, sb [R/16, C/16] + s_g.
+// FP8 block-scaled codes.  KIND 0: MX row, e [R, C/32]; 1: MX col, e [R/32, C];
+// 2: blockwise 1x128, s [R, C/128]; 3: blockwise 128x128, s [R/128, C/128].
 // ---------------------------------------------------------------------------
 template <int KIND, int FMT, int OUT>
 __global__ void __launch_bounds__(kDqThreads) k_dq_blocks(const uint8_t *__restrict__ q, const void *__restrict__ sc,
-                                                          const float *__restrict__ s_global, int64_t R, int64_t C,
-                                                          int bx_log2, void *__restrict__ y)
+                                                          int64_t R, int64_t C, int bx_log2, void *__restrict__ y)
 {
     constexpr int EPU = OUT == F32 ? 4 : 8;
-    constexpr bool FP4 = KIND >= 4;
-    constexpr int CB = FP4 ? EPU / 2 : EPU;   // code bytes per unit
+    constexpr int CB = EPU;   // code bytes per unit
     const int BX = 1 << bx_log2, BY = kDqThreads >> bx_log2;
     const int tx = threadIdx.x & (BX - 1), ty = threadIdx.x >> bx_log2;
     const int64_t upr = C / EPU;
     const int64_t u = (int64_t)blockIdx.y * BX + tx;
     if (u >= upr) return;
     const int64_t c = u * EPU;
-    const float sg = FP4 ? *s_global : 1.0f;
     const int64_t grp = blockIdx.x;
 
     uint2 a[kDqRows];
@@ -126,10 +123,9 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_blocks(const uint8_t *__restr
     for (int i = 0; i < kDqRows; i++) {
         const int64_t r = (grp * kDqRows + i) * BY + ty;
         if (r >= R) break;
-        const uint8_t *qp = q + (r * C + c) / (FP4 ? 2 : 1);
+        const uint8_t *qp = q + r * C + c;
         if (CB == 8) a[i] = *reinterpret_cast<const uint2 *>(qp);
-        else if (CB == 4) a[i] = make_uint2(*reinterpret_cast<const uint32_t *>(qp), 0u);
-        else a[i] = make_uint2(*reinterpret_cast<const uint16_t *>(qp), 0u);
+        else a[i] = make_uint2(*reinterpret_cast<const uint32_t *>(qp), 0u);
         if (KIND == 0) fac[i] = e8m0_value(static_cast<const uint8_t *>(sc)[r * (C / 32) + c / 32]);
         if (KIND == 1 && (i == 0 || !one_blk)) {
             const uint8_t *ep = static_cast<const uint8_t *>(sc) + (r / 32) * C + c;
@@ -137,8 +133,6 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_blocks(const uint8_t *__restr
         }
         if (KIND == 2) fac[i] = static_cast<const float *>(sc)[r * (C / 128) + c / 128];
         if (KIND == 3) fac[i] = static_cast<const float *>(sc)[(r / 128) * (C / 128) + c / 128];
-        if (KIND == 4) fac[i] = __fmul_rn(e4m3_value(static_cast<const uint8_t *>(sc)[r * (C / 16) + c / 16]), sg);
-        if (KIND == 5) fac[i] = __fmul_rn(e4m3_value(static_cast<const uint8_t *>(sc)[(r / 16) * (C / 16) + c / 16]), sg);
     }
 #pragma unroll
     for (int i = 0; i < kDqRows; i++) {
@@ -149,28 +143,123 @@ __global__ void __launch_bounds__(kDqThreads) k_dq_blocks(const uint8_t *__restr
 #pragma unroll
             for (int p = 0; p < EPU; p++) ef[p] = e8m0_value(((p < 4 ? e8[i].x : e8[i].y) >> (8 * (p & 3))) & 0xFFu);
         }
-        if (FP4) {
 #pragma unroll
-            for (int p = 0; p < EPU / 2; p++) {
-                const float2 d = fp4x2_to_f32((a[i].x >> (8 * p)) & 0xFFu);
+        for (int p = 0; p < EPU / 2; p++) {
+            const uint32_t wd = p < 2 ? a[i].x : a[i].y;
+            const float2 d = fp8x2_to_f32<FMT>((wd >> (16 * (p & 1))) & 0xFFFFu);
+            if (KIND == 1) {
+                f[2 * p] = __fmul_rn(d.x, ef[2 * p]);
+                f[2 * p + 1] = __fmul_rn(d.y, ef[2 * p + 1]);
+            } else {
                 f[2 * p] = __fmul_rn(d.x, fac[i]);
                 f[2 * p + 1] = __fmul_rn(d.y, fac[i]);
             }
-        } else {
-#pragma unroll
-            for (int p = 0; p < EPU / 2; p++) {
-                const uint32_t wd = p < 2 ? a[i].x : a[i].y;
-                const float2 d = fp8x2_to_f32<FMT>((wd >> (16 * (p & 1))) & 0xFFFFu);
-                if (KIND == 1) {
-                    f[2 * p] = __fmul_rn(d.x, ef[2 * p]);
-                    f[2 * p + 1] = __fmul_rn(d.y, ef[2 * p + 1]);
-                } else {
-                    f[2 * p] = __fmul_rn(d.x, fac[i]);
-                    f[2 * p + 1] = __fmul_rn(d.y, fac[i]);
-                }
-            }
         }
         store_unit<OUT>(y, r * C + c, f);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4: a unit is one 16-element row segment of a block (8 code bytes, one
+// block scale, so the factor sb * s_g is formed once per 16 outputs).  The
+// E2M1 pairs decode to f16x2 and widen to FP32 by a mixed-precision add of
+// -0 (exact; FMA pipe); the products are packed FP32 multiplies.
+// BLK 0: 1x16, sb [R, C/16]; 1: 16x16, sb [R/16, C/16].
+// ---------------------------------------------------------------------------
+QD float f16_lo_f32(uint32_t h2)
+{
+    float r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.f16 %0, l, 0f80000000;\n\t}" : "=f"(r) : "r"(h2));
+    return r;
+}
+QD float f16_hi_f32(uint32_t h2)
+{
+    float r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.f16 %0, h, 0f80000000;\n\t}" : "=f"(r) : "r"(h2));
+    return r;
+}
+// The 8 E2M1 codes of a word (code j in bits 4j+3..4j) as FP32, scaled by fac.
+QD void fp4x8_scaled(uint32_t w, float fac, float *f)
+{
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        f[2 * p] = f16_lo_f32(h[p]);
+        f[2 * p + 1] = f16_hi_f32(h[p]);
+        mul2(f[2 * p], f[2 * p + 1], fac, fac);
+    }
+}
+
+// 16 FP32 values as 32 bytes (BF16) or 64 bytes (FP32) of output at element
+// e; W32: y is 32-byte aligned and each 32 bytes leave in one store (a
+// lane's 16-byte halves would each fill only half of 32 sectors per warp
+// store).
+template <int OUT, bool W32> QD void store16(void *y, int64_t e, const float *f)
+{
+    if (OUT == F32) {
+        float *d = static_cast<float *>(y) + e;
+        const uint4 v0 = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+        const uint4 v1 = make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]), __float_as_uint(f[7]));
+        const uint4 v2 = make_uint4(__float_as_uint(f[8]), __float_as_uint(f[9]), __float_as_uint(f[10]), __float_as_uint(f[11]));
+        const uint4 v3 = make_uint4(__float_as_uint(f[12]), __float_as_uint(f[13]), __float_as_uint(f[14]), __float_as_uint(f[15]));
+        if (W32) {
+            stg32(d, v0, v1);
+            stg32(d + 8, v2, v3);
+        } else {
+            stg16(d, v0);
+            stg16(d + 4, v1);
+            stg16(d + 8, v2);
+            stg16(d + 12, v3);
+        }
+    } else {
+        uint16_t *d = static_cast<uint16_t *>(y) + e;
+        const uint4 v0 = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+        const uint4 v1 = make_uint4(pack_bf16x2(f[8], f[9]), pack_bf16x2(f[10], f[11]), pack_bf16x2(f[12], f[13]),
+                                    pack_bf16x2(f[14], f[15]));
+        if (W32) {
+            stg32(d, v0, v1);
+        } else {
+            stg16(d, v0);
+            stg16(d + 8, v1);
+        }
+    }
+}
+
+template <int BLK, int OUT, bool W32>
+__global__ void __launch_bounds__(kDqThreads) k_dq_fp4(const uint8_t *__restrict__ q, const uint8_t *__restrict__ sb,
+                                                       const float *__restrict__ s_global, int64_t R, int64_t C,
+                                                       int bx_log2, void *__restrict__ y)
+{
+    const int BX = 1 << bx_log2, BY = kDqThreads >> bx_log2;
+    const int tx = threadIdx.x & (BX - 1), ty = threadIdx.x >> bx_log2;
+    const int64_t upr = C / 16;
+    const int64_t u = (int64_t)blockIdx.y * BX + tx;
+    if (u >= upr) return;
+    const float sg = *s_global;
+    const int64_t r0 = (int64_t)blockIdx.x * (kDqRows * BY) + ty;
+    uint2 a[kDqRows];
+    uint32_t code[kDqRows];
+#pragma unroll
+    for (int i = 0; i < kDqRows; i++) {
+        const int64_t r = r0 + (int64_t)i * BY;
+        if (r < R) {
+            a[i] = *reinterpret_cast<const uint2 *>(q + r * (C / 2) + u * 8);
+            code[i] = sb[(BLK == 0 ? r : r / 16) * upr + u];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kDqRows; i++) {
+        const int64_t r = r0 + (int64_t)i * BY;
+        if (r >= R) break;
+        const float fac = __fmul_rn(e4m3_value(code[i]), sg);
+        float f[16];
+        fp4x8_scaled(a[i].x, fac, f);
+        fp4x8_scaled(a[i].y, fac, f + 8);
+        store16<OUT, W32>(y, r * C + u * 16, f);
     }
 }
 
@@ -199,8 +288,8 @@ cudaError_t launch_dq_cs(const uint8_t *q, const float *s, int64_t R, int64_t C,
 }
 
 template <int KIND>
-static cudaError_t dq_blocks_t(const uint8_t *q, const void *sc, const float *s_g, int64_t R, int64_t C, int fmt,
-                               int out, void *y, cudaStream_t st)
+static cudaError_t dq_blocks_t(const uint8_t *q, const void *sc, int64_t R, int64_t C, int fmt, int out, void *y,
+                               cudaStream_t st)
 {
     if (R == 0 || C == 0) return cudaSuccess;
     const int epu = out == F32 ? 4 : 8;
@@ -212,7 +301,7 @@ static cudaError_t dq_blocks_t(const uint8_t *q, const void *sc, const float *s_
     const int64_t gr = (R + (int64_t)BY * kDqRows - 1) / ((int64_t)BY * kDqRows);   // row groups
     if (gu > 65535 || gr > 2147483647LL) return cudaErrorInvalidConfiguration;
     const dim3 gridxy((unsigned)gr, (unsigned)gu);
-#define DQ_LAUNCH(F, O) k_dq_blocks<KIND, F, O><<<gridxy, kDqThreads, 0, st>>>(q, sc, s_g, R, C, lg, y)
+#define DQ_LAUNCH(F, O) k_dq_blocks<KIND, F, O><<<gridxy, kDqThreads, 0, st>>>(q, sc, R, C, lg, y)
     if (fmt == E4M3) {
         if (out == F32) DQ_LAUNCH(E4M3, F32);
         else DQ_LAUNCH(E4M3, BF16);
@@ -227,22 +316,40 @@ static cudaError_t dq_blocks_t(const uint8_t *q, const void *sc, const float *s_
 cudaError_t launch_dq_mxfp8(const uint8_t *q, const uint8_t *e, int64_t R, int64_t C, int fmt, int dir, int out,
                             void *y, cudaStream_t st)
 {
-    return dir == 0 ? dq_blocks_t<0>(q, e, nullptr, R, C, fmt, out, y, st)
-                    : dq_blocks_t<1>(q, e, nullptr, R, C, fmt, out, y, st);
+    return dir == 0 ? dq_blocks_t<0>(q, e, R, C, fmt, out, y, st) : dq_blocks_t<1>(q, e, R, C, fmt, out, y, st);
 }
 
 cudaError_t launch_dq_blockwise(const uint8_t *q, const float *s, int64_t R, int64_t C, int tile, int out, void *y,
                                 cudaStream_t st)
 {
-    return tile == 0 ? dq_blocks_t<2>(q, s, nullptr, R, C, E4M3, out, y, st)
-                     : dq_blocks_t<3>(q, s, nullptr, R, C, E4M3, out, y, st);
+    return tile == 0 ? dq_blocks_t<2>(q, s, R, C, E4M3, out, y, st) : dq_blocks_t<3>(q, s, R, C, E4M3, out, y, st);
 }
 
 cudaError_t launch_dq_nvfp4(const uint8_t *q, const uint8_t *sb, const float *s_g, int64_t R, int64_t C, int blk,
                             int out, void *y, cudaStream_t st)
 {
-    return blk == 0 ? dq_blocks_t<4>(q, sb, s_g, R, C, E4M3, out, y, st)
-                    : dq_blocks_t<5>(q, sb, s_g, R, C, E4M3, out, y, st);
+    if (R == 0 || C == 0) return cudaSuccess;
+    const int64_t upr = C / 16;   // units (16 elements) per row
+    int lg = 0;
+    while ((1 << lg) < upr && lg < 8) lg++;
+    const int BY = kDqThreads >> lg;
+    const int64_t gu = (upr + (1 << lg) - 1) >> lg;                                   // unit blocks of a row
+    const int64_t gr = (R + (int64_t)BY * kDqRows - 1) / ((int64_t)BY * kDqRows);   // row groups
+    if (gu > 65535 || gr > 2147483647LL) return cudaErrorInvalidConfiguration;
+    const dim3 gridxy((unsigned)gr, (unsigned)gu);
+    const bool w32 = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
+#define DQ4(B, O)                                                                                \
+    (w32 ? k_dq_fp4<B, O, true><<<gridxy, kDqThreads, 0, st>>>(q, sb, s_g, R, C, lg, y)          \
+         : k_dq_fp4<B, O, false><<<gridxy, kDqThreads, 0, st>>>(q, sb, s_g, R, C, lg, y))
+    if (blk == 0) {
+        if (out == F32) DQ4(0, F32);
+        else DQ4(0, BF16);
+    } else {
+        if (out == F32) DQ4(1, F32);
+        else DQ4(1, BF16);
+    }
+#undef DQ4
+    return cudaGetLastError();
 }
 
 }  // namespace qk

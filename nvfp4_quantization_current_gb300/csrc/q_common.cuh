@@ -50,6 +50,12 @@ QD void stg16(void *p, uint4 v)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
+// 32 bytes in one store (p 32-byte aligned): a warp's store covers 1 KiB.
+QD void stg32(void *p, const uint4 &a, const uint4 &b)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+                 "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w) : "memory");
+}
 QD void stg8(void *p, uint32_t a, uint32_t b)
 {
     asm volatile("st.global.v2.u32 [%0], {%1, %2};" :: "l"(p), "r"(a), "r"(b) : "memory");
@@ -219,17 +225,6 @@ template <> QD float2 fp8x2_to_f32<E5M2>(uint32_t two)
     uint32_t h2;
     uint16_t c = (uint16_t)two;
     asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(c));
-    float lo, hi;
-    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi) : "r"(h2));
-    return make_float2(lo, hi);
-}
-
-// Two E2M1 codes (one byte: low nibble first) -> two exact FP32 values.
-QD float2 fp4x2_to_f32(uint32_t byte)
-{
-    uint32_t h2;
-    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h2) : "r"(byte));
     float lo, hi;
     asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
         : "=f"(lo), "=f"(hi) : "r"(h2));

@@ -607,6 +607,26 @@ def test_nvfp4_parity(kind, shape, bf16, blk, rnd, seed, offset):
         same(host(got.dequantize(Q.Q_COL, dt)), O.dq_nvfp4(want.q_colT, want.sb_colT, want.s_global, blk, o_out(dt)), "dq colT")
 
 
+@pytest.mark.parametrize("blk", [O.B1x16, O.B16x16])
+def test_dq_nvfp4_into_outputs_off_a_32_byte_boundary(blk):
+    """The dequantizer writes 32 bytes per store only into 32-byte aligned
+    outputs; an output 16 bytes past such a boundary (what the C ABI still
+    accepts) takes 16-byte stores and must hold the same values."""
+    x = W.gen("normal", (96, 160), 405, bf16=True)
+    want = O.nvfp4(x, blk, O.RN, rowwise=True, colwise=False)
+    b = "1x16" if blk == O.B1x16 else "16x16"
+    got = Q.q_nvfp4(dev(x), b, "rn", rowwise=True, colwise=False)
+    for dt in OUTS:
+        esz = torch.empty((), dtype=dt).element_size()
+        buf = torch.empty(96 * 160 + 64 // esz, dtype=dt, device="cuda")
+        base = buf.data_ptr() % 32
+        shift = ((16 - base) % 32) // esz   # elements to a 16 (mod 32) address
+        y = buf[shift:shift + 96 * 160].view(96, 160)
+        assert y.data_ptr() % 32 == 16
+        Q.dq_nvfp4(got.q_row, got.sb_row, got.s_global, b, dt, out=y)
+        same(host(y), O.dq_nvfp4(want.q_row, want.sb_row, want.s_global, blk, o_out(dt)), f"dq {dt}")
+
+
 def test_nvfp4_sr_unbiased_on_the_gpu_over_1e7_draws():
     """Stochastic rounding through the GPU path is unbiased: E[dq(q(x))] = x
     within 1e-3 relative over ~10^7 draws, in both copies.  x tiles a 16x16
