@@ -58,10 +58,14 @@ REF_BUDGET_S = 120.0
 RHT_MASK = 0xB4E1   # the 16 random signs of the Hadamard transform (any fixed draw)
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of the kernel on the named call, with the hash of the kernel's
-# source (file + shared device headers) at capture time; reported as null
-# once the source has changed since.
-TRAFFIC = {}
+# ncu --set full capture of the kernel on the named call (key "workload.tensor:
+# piece"), with the kernel, the commit the capture measured, and the hash of
+# the kernel's source (file + shared device headers) at capture time;
+# reported as null once the source has changed since.
+TRAFFIC = {
+    "bw3.w:bwmx_128x128_T": {"kernel": "qk::k_blockwise<0, 1, 1>", "capture_commit": "65e0d34",
+                             "bytes_per_launch": 484726784, "src_hash": "936b54c608eb07ca"},
+}
 
 
 def src_hash(fname):
