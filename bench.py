@@ -803,8 +803,9 @@ def run_ours(args):
 
         # The host link in the same run, with the same pinned buffers: every
         # input of the step up alone, every output down alone, and both at once
-        # (on two streams), no kernels; the step's end-to-end time is bounded
-        # below by the both-at-once figure.
+        # (on two streams), no kernels.  The end-to-end step is bounded below by
+        # the longer one-way time; it can beat the both-at-once figure, which
+        # saturates the link in both directions for the whole time.
         def link(up, down, reps=3):
             ms = []
             for r in range(reps + 1):
