@@ -734,6 +734,27 @@ def test_nvfp4_single_direction_and_given_amax():
     f32eq(got.s_global.item(), want.s_global)
 
 
+@pytest.mark.parametrize("rows", [48, 272, 288])
+@pytest.mark.parametrize("direction", ["row", "col"])
+@pytest.mark.parametrize("rnd", [O.RN, O.SR])
+def test_nvfp4_1x16_one_direction_ragged(rows, direction, rnd):
+    """One copy only (all warps of the 1x16 kernel on it): row counts that
+    are not multiples of 32 (48, 272) take the columnwise path's 8-byte
+    stores, 288 its bulk tensor store with a half-filled last row tile;
+    528 columns leave a partial column tile."""
+    x = W.gen("t3", (rows, 528), 406, bf16=True)
+    rw, cw = direction == "row", direction == "col"
+    want = O.nvfp4(x, O.B1x16, rnd, seed=3, offset=11, rowwise=rw, colwise=cw)
+    got = Q.q_nvfp4(dev(x), "1x16", "rn" if rnd == O.RN else "sr", seed=3, offset=11, rowwise=rw, colwise=cw)
+    f32eq(got.s_global.item(), want.s_global, "s_global")
+    if rw:
+        same(host(got.q_row), want.q_row, "q_row")
+        same(host(got.sb_row), want.sb_row, "sb_row")
+    else:
+        same(host(got.q_colT), want.q_colT, "q_colT")
+        same(host(got.sb_colT), want.sb_colT, "sb_colT")
+
+
 def test_nvfp4_empty():
     got = Q.q_nvfp4(torch.empty((0, 32), dtype=torch.bfloat16, device="cuda"))
     assert got.amax.item() == 0 and got.s_global.item() == 1
