@@ -54,6 +54,10 @@ constexpr int kNvRows = NvCfg::kRows, kNvThreads = NvCfg::kThreads, kNvTC = 256;
 constexpr int kNvTabCopies = 4;                          // interleaved copies of the encode-factor table
 constexpr int kNvParkBytes = 256 * (kNvRows / 2);        // 16x16: parked columnwise codes of a tile
 constexpr int kLutBinades = 24, kLut = kLutBinades * 128;
+// 1x16: tiles of kN1Rows rows, kN1Ctas CTAs of 256 threads per SM
+constexpr int kN1Rows = 64, kN1Ctas = 2;
+using N1Cfg = TileCfg<kN1Rows, 256, 3>;
+constexpr int kN1BoxBytes = 256 * (kN1Rows / 2);        // columnwise codes of a tile: [256 columns][kN1Rows / 2]
 
 // ---------------------------------------------------------------------------
 // block scales
@@ -181,7 +185,7 @@ QD uint32_t halves_max_bits(uint32_t m)
 // MODE 0: both copies (warps 0-3 rows, 4-7 columns); 1: rowwise only;
 // 2: columnwise only (all warps).
 template <int MODE, int RND>
-__global__ void __launch_bounds__(kNvThreads, 2)
+__global__ void __launch_bounds__(kNvThreads, kN1Ctas)
     k_nvfp4_bf16_1x16(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K, const float *__restrict__ amax,
                       const __grid_constant__ PhiloxKeys keys, uint64_t offset, uint8_t *__restrict__ q_row,
                       uint8_t *__restrict__ sb_row, uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
@@ -193,10 +197,10 @@ __global__ void __launch_bounds__(kNvThreads, 2)
     __shared__ float enc_tab[128 * kNvTabCopies];
     __shared__ uint8_t lut[kLut];
     extern __shared__ __align__(1024) uint8_t dsm[];
-    uint8_t *const park = dsm + NvCfg::kSmem;   // columnwise codes of a tile: [256 columns][32 bytes]
+    uint8_t *const park = dsm + N1Cfg::kSmem;   // columnwise codes of a tile: [256 columns][kN1Rows / 2 bytes]
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int64_t tiles_m = (M + kNvRows - 1) / kNvRows, tiles_k = (K + kNvTC - 1) / kNvTC;
+    const int64_t tiles_m = (M + kN1Rows - 1) / kN1Rows, tiles_k = (K + kNvTC - 1) / kNvTC;
     float alpha_g = 1.0f;
     int lut_base = 0;
     bool tab = true;   // alpha_g is a normal float, so the byte table applies
@@ -222,8 +226,8 @@ __global__ void __launch_bounds__(kNvThreads, 2)
 
     auto row_part = [&](const uint8_t *st, int64_t mb, int64_t kb, uint32_t &nf) {
         if constexpr (NR > 0) {
-            constexpr int RPW = kNvRows / (NR / 32);          // rows per row warp
-            constexpr int BPT = kNvRows * (kNvTC / 16) / NR;   // blocks per row thread
+            constexpr int RPW = kN1Rows / (NR / 32);          // rows per row warp
+            constexpr int BPT = kN1Rows * (kNvTC / 16) / NR;   // blocks per row thread
             // block b of row r: the lane's 16-byte loads go to chunks 2b + s and
             // 2b + 1 - s with s = bit 2 of b, so that the 8 lanes of each load
             // phase hit 8 different 16-byte bank groups
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(kNvThreads, 2)
 
     auto col_part = [&](const uint8_t *st, int64_t mb, int64_t kb, uint32_t &nf) {
         if constexpr (NC > 0) {
-            constexpr int GPT = (kNvRows / 16) * (kNvTC / 2) / NC;   // 16-row groups per column thread
+            constexpr int GPT = (kN1Rows / 16) * (kNvTC / 2) / NC;   // 16-row groups per column thread
             const int c = t - NR;
             const int p = c & (kNvTC / 2 - 1);
             const int g0 = (c / (kNvTC / 2)) * GPT;
@@ -323,17 +327,23 @@ __global__ void __launch_bounds__(kNvThreads, 2)
                 }
             }
             if (col_tma) {
-                // the tile's columnwise codes as a dense [256 columns][32 bytes]
-                // box, which one bulk tensor store writes (the parts past the
-                // tensor's edges are not written)
+                // the tile's columnwise codes as a dense [256 columns][kN1Rows / 2
+                // bytes] box, which one bulk tensor store writes (the parts past
+                // the tensor's edges are not written)
                 if (c == 0) bulk_wait_read_all();   // the previous tile's store has read the box
                 named_barrier(1, NC);
 #pragma unroll
-                for (int h = 0; h < 2; h++)
+                for (int h = 0; h < 2; h++) {
+                    uint8_t *dst = park + (2 * p + h) * (kN1Rows / 2) + 8 * g0;
+                    if constexpr (GPT == 1) {
+                        *reinterpret_cast<uint2 *>(dst) = make_uint2(code[h][0], code[h][1]);
+                    } else {
 #pragma unroll
-                    for (int q = 0; q < GPT / 2; q++)
-                        *reinterpret_cast<uint4 *>(park + (2 * p + h) * 32 + 8 * g0 + 16 * q) =
-                            make_uint4(code[h][4 * q], code[h][4 * q + 1], code[h][4 * q + 2], code[h][4 * q + 3]);
+                        for (int q = 0; q < GPT / 2; q++)
+                            *reinterpret_cast<uint4 *>(dst + 16 * q) =
+                                make_uint4(code[h][4 * q], code[h][4 * q + 1], code[h][4 * q + 2], code[h][4 * q + 3]);
+                    }
+                }
                 fence_proxy_async();   // generic-proxy writes of the box before the async-proxy read
                 named_barrier(1, NC);
                 if (c == 0) {
@@ -351,7 +361,7 @@ __global__ void __launch_bounds__(kNvThreads, 2)
                     uint8_t *sc = sb_colT + (k + h) * (M / 16) + mg / 16;
                     if (col_tma) {
                         // codes leave with the bulk store
-                    } else if (ng == GPT && (M & 31) == 0) {
+                    } else if (GPT >= 2 && ng == GPT && (M & 31) == 0) {
 #pragma unroll
                         for (int q = 0; q < GPT / 2; q++)
                             stg16(qc + 16 * q, make_uint4(code[h][4 * q], code[h][4 * q + 1], code[h][4 * q + 2],
@@ -363,6 +373,8 @@ __global__ void __launch_bounds__(kNvThreads, 2)
                     }
                     if (GPT == 4 && ng == 4 && (M & 63) == 0) {
                         stg4(sc, sbw[h]);
+                    } else if (GPT == 2 && ng == 2 && (M & 31) == 0) {
+                        *reinterpret_cast<uint16_t *>(sc) = (uint16_t)sbw[h];
                     } else {
 #pragma unroll
                         for (int gi = 0; gi < GPT; gi++)
@@ -374,14 +386,14 @@ __global__ void __launch_bounds__(kNvThreads, 2)
     };
 
     auto body = [&](uint8_t *st, int64_t tm, int64_t tk) {
-        const int64_t mb = tm * kNvRows, kb = tk * kNvTC;
+        const int64_t mb = tm * kN1Rows, kb = tk * kNvTC;
         uint32_t nf = 0;   // a non-finite block maximum seen by this thread
         if (t < NR) row_part(st, mb, kb, nf);
         else col_part(st, mb, kb, nf);
         post_nonfinite(status, nf);
     };
 
-    run_tiles<NvCfg>(&tmap, tiles_m, tiles_k, kNvTC, true, status, pre, body);
+    run_tiles<N1Cfg>(&tmap, tiles_m, tiles_k, kNvTC, true, status, pre, body);
     if (NC > 0 && col_tma && t == NR) bulk_wait_all();   // the last box is written before the CTA ends
 }
 
@@ -498,16 +510,16 @@ static cudaError_t nvb_launch_1x16(const void *x, int64_t M, int64_t K, const fl
                                    uint64_t offset, uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT,
                                    float *s_global, int32_t *status, cudaStream_t st, bool after_amax)
 {
-    constexpr int smem = NvCfg::kSmem + kNvParkBytes;
+    constexpr int smem = N1Cfg::kSmem + kN1BoxBytes;
     alignas(64) CUtensorMap map, cmap;
     memset(&map, 0, sizeof map);
     memset(&cmap, 0, sizeof cmap);
     int col_tma = 0;
     if (M != 0 && K != 0) {
-        cudaError_t e = make_tile_map(&map, x, BF16, M, K, kNvRows);
+        cudaError_t e = make_tile_map(&map, x, BF16, M, K, kN1Rows);
         if (e != cudaSuccess) return e;
         if (q_colT != nullptr && (M % 32) == 0) {
-            e = make_store_map_u8(&cmap, q_colT, M / 2, K, kNvRows / 2, kNvTC);
+            e = make_store_map_u8(&cmap, q_colT, M / 2, K, kN1Rows / 2, kNvTC);
             if (e != cudaSuccess) return e;
             col_tma = 1;
         }
@@ -516,8 +528,8 @@ static cudaError_t nvb_launch_1x16(const void *x, int64_t M, int64_t K, const fl
         const cudaError_t ea = engine_smem_ready<Kernel>(smem, true);
         if (ea != cudaSuccess) return ea;
     }
-    const int64_t tiles = ((M + kNvRows - 1) / kNvRows) * ((K + kNvTC - 1) / kNvTC);
-    const int64_t slots = 2 * (int64_t)sm_count();   // two CTAs per SM
+    const int64_t tiles = ((M + kN1Rows - 1) / kN1Rows) * ((K + kNvTC - 1) / kNvTC);
+    const int64_t slots = kN1Ctas * (int64_t)sm_count();   // kN1Ctas CTAs per SM
     int grid = (int)(tiles < slots ? tiles : slots);
     if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
     const PhiloxKeys keys = philox_keys(seed);
