@@ -244,14 +244,20 @@ def build_step(dev_tensors, torch, Q):
         row = Q.alloc_nvfp4(M, K, x.device, "1x16", rowwise=True, colwise=False)
         col = Q.alloc_nvfp4(M, K, x.device, "1x16", rowwise=False, colwise=True)
         ins = nbytes(x)
-        pieces = [
-            ("rht_amax2", "k_nvfp4.cu", ins, lambda: Q.q_nvfp4_rht_amax2(x, mask, out=(col.amax, row.amax))),
-            (f"nvfp4_row_{rnd}", "k_nvfp4_bf16.cu" if x.dtype == torch.bfloat16 else "k_nvfp4.cu",
-             ins + nbytes(row.q_row, row.sb_row, row.s_global) + 4,
-             lambda: Q.q_nvfp4(x, "1x16", rnd, seed, 0, True, False, amax=row.amax, out=row)),
-            (f"nvfp4_rht_colT_{rnd}", "k_nvfp4.cu", ins + nbytes(col.q_colT, col.sb_colT, col.s_global) + 4,
-             lambda: Q.q_nvfp4_rht_colT(x, mask, rnd, seed, 0, amax=col.amax, out=col)),
-        ]
+        pieces = [("rht_amax2", "k_nvfp4.cu", ins, lambda: Q.q_nvfp4_rht_amax2(x, mask, out=(col.amax, row.amax)))]
+        if x.dtype == torch.bfloat16:
+            # one kernel writes both copies from one read of x, the maxima given
+            pieces.append((f"nvfp4_recipe_{rnd}", "k_nvfp4_bf16.cu",
+                           ins + nbytes(row.q_row, row.sb_row, row.s_global, col.q_colT, col.sb_colT, col.s_global) + 8,
+                           lambda: Q.q_nvfp4_recipe(x, mask, rnd, seed, 0, amax_row=row.amax, amax_col=col.amax,
+                                                    out=(row, col))))
+        else:
+            pieces += [
+                (f"nvfp4_row_{rnd}", "k_nvfp4.cu", ins + nbytes(row.q_row, row.sb_row, row.s_global) + 4,
+                 lambda: Q.q_nvfp4(x, "1x16", rnd, seed, 0, True, False, amax=row.amax, out=row)),
+                (f"nvfp4_rht_colT_{rnd}", "k_nvfp4.cu", ins + nbytes(col.q_colT, col.sb_colT, col.s_global) + 4,
+                 lambda: Q.q_nvfp4_rht_colT(x, mask, rnd, seed, 0, amax=col.amax, out=col)),
+            ]
         calls.append(Call(f"{tag} nvfp4_recipe_{rnd} row + RHT colT", "nvfp4_recipe", pieces, [x],
                           [row.q_row, row.sb_row, row.s_global, col.q_colT, col.sb_colT, col.s_global],
                           lambda: Q.q_nvfp4_recipe(x, mask, rnd, seed, 0, out=(row, col))))

@@ -93,7 +93,8 @@ const char *q_last_error(void);
 
 /* Version of this ABI (incremented on incompatible change).  2: the
  * stochastic-rounding draws of the columnwise NVFP4 copies are numbered by
- * the element's position in x (see q_nvfp4), so results differ from 1. */
+ * the element's position in x (see q_nvfp4), so results differ from 1.
+ * 3: q_nvfp4_recipe takes a q_amax_mode. */
 int q_abi_version(void);
 
 /*
@@ -318,22 +319,25 @@ q_status q_selftest_wait_timeout(int32_t *status, uint64_t wait_ns, q_stream_t s
 /*
  * Both maxima the NVFP4 recipe needs, in one read: *amax_rht = max|x'| (as
  * q_nvfp4_rht_amax) and *amax_x = max|x| (as q_amax).  For sharded tensors:
- * all-reduce both, then q_nvfp4 (rowwise, Q_AMAX_GIVEN with amax_x) and
- * q_nvfp4_rht_colT (Q_AMAX_GIVEN with amax_rht).  M % 16 == 0, K % 16 == 0.
+ * all-reduce both, then q_nvfp4_recipe with Q_AMAX_GIVEN (or q_nvfp4 rowwise
+ * with amax_x and q_nvfp4_rht_colT with amax_rht, both Q_AMAX_GIVEN).
+ * M % 16 == 0, K % 16 == 0.
  */
 q_status q_nvfp4_rht_amax2(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, float *amax_rht,
                            float *amax_x, int32_t *status, q_stream_t stream);
 
 /*
- * The NVFP4 training recipe's two copies of one tensor in three reads
- * ([LP] §2.4: 1x16 blocks for activations and gradients, stochastic
- * rounding on gradients, the random Hadamard transform on the inputs of the
- * weight-gradient GEMM, which reads the columnwise copy): one pass takes both
- * max|x| and max|x'| (x' the transform of q_nvfp4_rht_amax), then the
- * rowwise 1x16 copy of x as q_nvfp4 gives it (q_row [M, K/2], sb_row
- * [M, K/16], *s_global_row) and the columnwise copy of x' as
+ * The NVFP4 training recipe's two copies of one tensor ([LP] §2.4: 1x16
+ * blocks for activations and gradients, stochastic rounding on gradients,
+ * the random Hadamard transform on the inputs of the weight-gradient GEMM,
+ * which reads the columnwise copy): the rowwise 1x16 copy of x as q_nvfp4
+ * gives it (q_row [M, K/2], sb_row [M, K/16], *s_global_row) and the
+ * columnwise copy of x' (the transform of q_nvfp4_rht_amax) as
  * q_nvfp4_rht_colT gives it (q_colT [K, M/2], sb_colT [K, M/16],
- * *s_global_colT).  amax_row / amax_colT receive the two maxima.  With the
+ * *s_global_colT).  amax_mode Q_AMAX_COMPUTE: one pass takes both max|x| and
+ * max|x'| into *amax_row / *amax_colT (as q_nvfp4_rht_amax2); Q_AMAX_GIVEN:
+ * they are read from there (e.g. all-reduced over shards).  A BF16 x is then
+ * read once more for both copies together, an FP32 x once for each.  With the
  * same seed and offset every output is bit-identical to q_nvfp4(rowwise
  * only) plus q_nvfp4_rht_colT (row draws from stream 0, transposed draws
  * from stream 1).  M % 16 == 0 and K % 16 == 0; all buffers required.
@@ -341,7 +345,7 @@ q_status q_nvfp4_rht_amax2(const void *x, q_dtype in, int64_t M, int64_t K, uint
 q_status q_nvfp4_recipe(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, q_round rnd,
                         uint64_t seed, uint64_t offset, uint8_t *q_row, uint8_t *sb_row, float *amax_row,
                         float *s_global_row, uint8_t *q_colT, uint8_t *sb_colT, float *amax_colT,
-                        float *s_global_colT, int32_t *status, q_stream_t stream);
+                        float *s_global_colT, q_amax_mode amax_mode, int32_t *status, q_stream_t stream);
 
 /*
  * a12: dequantizers.  Output y [R, C] in `out` (Q_F32, or Q_BF16 rounded to

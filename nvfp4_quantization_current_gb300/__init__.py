@@ -71,7 +71,7 @@ SIGNATURES = {
     "q_mxfp8_requant_col": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
     "q_blockwise": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
     "q_blockwise_mx": (_I, [_P, _I, _I64, _I64, _I, _P, _P, _P, _P, _P, _P]),
-    "q_nvfp4_recipe": (_I, [_P, _I, _I64, _I64, _U32, _I, _U64, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "q_nvfp4_recipe": (_I, [_P, _I, _I64, _I64, _U32, _I, _U64, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "q_nvfp4_rht_amax2": (_I, [_P, _I, _I64, _I64, _U32, _P, _P, _P, _P]),
     "q_nvfp4": (_I, [_P, _I, _I64, _I64, _I, _I, _U64, _U64, _P, _P, _P, _P, _P, _I, _P, _P, _P]),
     "q_nvfp4_rht_amax": (_I, [_P, _I, _I64, _I64, _U32, _P, _P, _P]),
@@ -495,22 +495,31 @@ def q_nvfp4_rht_amax2(x: torch.Tensor, sign_mask: int, out: Optional[tuple] = No
 
 
 def q_nvfp4_recipe(x: torch.Tensor, sign_mask: int, rounding="rn", seed=0, offset=0,
+                   amax_row: Optional[torch.Tensor] = None, amax_col: Optional[torch.Tensor] = None,
                    out: Optional[tuple] = None, status: Optional[torch.Tensor] = None):
-    """Both NVFP4 copies of x as the training recipe uses them, in three reads:
-    the rowwise 1x16 copy of x and the columnwise copy of its random Hadamard
-    transform, with one amax pass for both.  Returns (row, colT), two
-    NVFP4Tensor whose outputs equal q_nvfp4(x, rowwise only) and
-    q_nvfp4_rht_colT(x, sign_mask) with the same seed and offset."""
+    """Both NVFP4 copies of x as the training recipe uses them: the rowwise
+    1x16 copy of x and the columnwise copy of its random Hadamard transform,
+    with one amax pass for both maxima (or both given as one-element device
+    tensors: max|x| as ``amax_row``, max|x'| as ``amax_col``), then one pass
+    for both copies of a BF16 x.  Returns (row, colT), two NVFP4Tensor whose
+    outputs equal q_nvfp4(x, rowwise only) and q_nvfp4_rht_colT(x, sign_mask)
+    with the same seed and offset."""
     dt = _in(x)
     M, K = x.shape
+    if (amax_row is None) != (amax_col is None):
+        raise ValueError("give both maxima or neither")
     if out is None:
         out = (alloc_nvfp4(M, K, x.device, "1x16", rowwise=True, colwise=False),
                alloc_nvfp4(M, K, x.device, "1x16", rowwise=False, colwise=True))
     row, col = out
+    mode = Q_AMAX_COMPUTE
+    if amax_row is not None:
+        row.amax, col.amax = amax_row, amax_col
+        mode = Q_AMAX_GIVEN
     rnd = {"rn": Q_RN, "sr": Q_SR, Q_RN: Q_RN, Q_SR: Q_SR}[rounding]
     _call("q_nvfp4_recipe", _ptr(x), dt, M, K, sign_mask, rnd, seed, offset, _ptr(row.q_row),
           _ptr(row.sb_row), _ptr(row.amax), _ptr(row.s_global), _ptr(col.q_colT), _ptr(col.sb_colT), _ptr(col.amax),
-          _ptr(col.s_global), _ptr(status), _stream(x.device))
+          _ptr(col.s_global), mode, _ptr(status), _stream(x.device))
     return row, col
 
 

@@ -184,17 +184,26 @@ QD uint32_t halves_max_bits(uint32_t m)
 
 // MODE 0: both copies (warps 0-3 rows, 4-7 columns); 1: rowwise only;
 // 2: columnwise only (all warps).
-template <int MODE, int RND>
+// RHT (with MODE 0): the NVFP4 recipe's two copies in one pass.  The row
+// warps quantize x with the tensor scale from *amax; the column warps
+// quantize the random Hadamard transform x' = (1/4) H D x of every 16-row
+// group of every column (D the signs of sign_mask) with the tensor scale from
+// *amax_c, in the order of k_nvfp4_rht: signs on the FP32 bits, the butterfly
+// with strides 1, 2, 4, 8, the exact factor 1/4, and the block scale by the
+// two operations (x' is not a BF16 value, so the byte table does not apply).
+template <int MODE, int RND, bool RHT = false>
 __global__ void __launch_bounds__(kNvThreads, kN1Ctas)
     k_nvfp4_bf16_1x16(const __grid_constant__ CUtensorMap tmap, int64_t M, int64_t K, const float *__restrict__ amax,
                       const __grid_constant__ PhiloxKeys keys, uint64_t offset, uint8_t *__restrict__ q_row,
                       uint8_t *__restrict__ sb_row, uint8_t *__restrict__ q_colT, uint8_t *__restrict__ sb_colT,
                       float *__restrict__ s_global, int32_t *status, const __grid_constant__ CUtensorMap cmap,
-                      int col_tma)
+                      int col_tma, uint32_t sign_mask, const float *__restrict__ amax_c, float *__restrict__ s_global_c)
 {
+    static_assert(!RHT || MODE == 0, "the transformed column copy runs beside the row copy");
     constexpr int NR = MODE == 0 ? 128 : MODE == 1 ? 256 : 0;   // row threads (threads 0 .. NR - 1)
     constexpr int NC = kNvThreads - NR;                          // column threads (the rest)
     __shared__ float enc_tab[128 * kNvTabCopies];
+    __shared__ float enc_tab_c[RHT ? 128 * kNvTabCopies : 1];   // RHT: alpha_c / f(code) for the column copy
     __shared__ uint8_t lut[kLut];
     extern __shared__ __align__(1024) uint8_t dsm[];
     uint8_t *const park = dsm + N1Cfg::kSmem;   // columnwise codes of a tile: [256 columns][kN1Rows / 2 bytes]
@@ -202,6 +211,7 @@ __global__ void __launch_bounds__(kNvThreads, kN1Ctas)
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t tiles_m = (M + kN1Rows - 1) / kN1Rows, tiles_k = (K + kNvTC - 1) / kNvTC;
     float alpha_g = 1.0f;
+    float alpha_c = 1.0f;   // RHT: the column copy's tensor scale
     int lut_base = 0;
     bool tab = true;   // alpha_g is a normal float, so the byte table applies
 
@@ -220,6 +230,20 @@ __global__ void __launch_bounds__(kNvThreads, kN1Ctas)
         if (blockIdx.x == 0 && t == 0) {
             *s_global = __fdiv_rn(1.0f, alpha_g);
             flag_nonfinite(status, __float_as_uint(A) & 0x7FFFFFFFu);
+        }
+        if constexpr (RHT) {
+            const float Ac = *amax_c;
+            alpha_c = alpha_from_amax(2688.0f, Ac);
+            if (t < 128) {
+                const float sv = e4m3_value(t);
+                const float ev = sv == 0.0f ? 0.0f : __fdiv_rn(alpha_c, sv);
+#pragma unroll
+                for (int j = 0; j < kNvTabCopies; j++) enc_tab_c[t * kNvTabCopies + j] = ev;
+            }
+            if (blockIdx.x == 0 && t == 0) {
+                *s_global_c = __fdiv_rn(1.0f, alpha_c);
+                flag_nonfinite(status, __float_as_uint(Ac) & 0x7FFFFFFFu);
+            }
         }
         __syncthreads();   // tables visible to every thread
     };
@@ -298,6 +322,65 @@ __global__ void __launch_bounds__(kNvThreads, kN1Ctas)
                 uint32_t w[16];
 #pragma unroll
                 for (int j = 0; j < 16; j++) w[j] = *reinterpret_cast<const uint32_t *>(src + j * kRowBytes);
+                if constexpr (RHT) {
+                const int64_t m16 = mb + 16 * g;
+                const bool live = m16 < M && k < K;
+                // columns 2p (a) and 2p + 1 (b) of the group's 16 rows: signs,
+                // butterfly, 1/4
+                float a[16], bv[16];
+#pragma unroll
+                for (int r = 0; r < 16; r++) {
+                    const uint32_t neg = ((sign_mask >> r) & 1u) << 31;
+                    a[r] = __uint_as_float((w[r] << 16) ^ neg);
+                    bv[r] = __uint_as_float((w[r] & 0xFFFF0000u) ^ neg);
+                }
+#pragma unroll
+                for (int hs = 1; hs < 16; hs *= 2)
+#pragma unroll
+                    for (int r = 0; r < 16; r++)
+                        if ((r & hs) == 0) bfly2(a[r], bv[r], a[r + hs], bv[r + hs]);
+#pragma unroll
+                for (int r = 0; r < 16; r++) mul2(a[r], bv[r], 0.25f, 0.25f);
+                float ma = 0.0f, mbx = 0.0f;
+#pragma unroll
+                for (int r = 0; r < 16; r++) {
+                    ma = fmax_abs(ma, a[r]);
+                    mbx = fmax_abs(mbx, bv[r]);
+                }
+                const uint32_t ba = __float_as_uint(ma) & 0x7FFFFFFFu, bb = __float_as_uint(mbx) & 0x7FFFFFFFu;
+                const uint32_t sa = nvb_sb_exact(ba, alpha_c), sbb = nvb_sb_exact(bb, alpha_c);
+                const float ea = nv_enc(enc_tab_c, sa, lane), eb = nv_enc(enc_tab_c, sbb, lane);
+#pragma unroll
+                for (int r = 0; r < 16; r++) mul2(a[r], bv[r], ea, eb);
+                if constexpr (RND == 1) {
+                    // rows m16 .. m16 + 15 of columns k, k + 1, stream 1: Philox blocks
+                    // (m16 / 8 + hh) K + column, two per column
+                    const uint32_t dma = sr_dither_mask(ea), dmb = sr_dither_mask(eb);
+#pragma unroll
+                    for (int hh = 0; hh < 2; hh++) {
+                        const uint64_t gb = offset + (uint64_t)(((m16 >> 3) + hh) * K + k);
+                        const uint4 Ra = sr_bits_rk<1>(gb, keys), Rb = sr_bits_rk<1>(gb + 1, keys);
+#pragma unroll
+                        for (int jj = 0; jj < 8; jj += 2) {
+                            const uint32_t wa = word(Ra, jj >> 1), wb = word(Rb, jj >> 1);
+                            a[8 * hh + jj] = sr_e2m1_dither(a[8 * hh + jj], sr_dither_lo(wa, dma));
+                            a[8 * hh + jj + 1] = sr_e2m1_dither(a[8 * hh + jj + 1], sr_dither_hi(wa, dma));
+                            bv[8 * hh + jj] = sr_e2m1_dither(bv[8 * hh + jj], sr_dither_lo(wb, dmb));
+                            bv[8 * hh + jj + 1] = sr_e2m1_dither(bv[8 * hh + jj + 1], sr_dither_hi(wb, dmb));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int hh = 0; hh < 2; hh++) {
+                    code[0][2 * gi + hh] = cvt_fp4x8(a[8 * hh], a[8 * hh + 1], a[8 * hh + 2], a[8 * hh + 3],
+                                                     a[8 * hh + 4], a[8 * hh + 5], a[8 * hh + 6], a[8 * hh + 7]);
+                    code[1][2 * gi + hh] = cvt_fp4x8(bv[8 * hh], bv[8 * hh + 1], bv[8 * hh + 2], bv[8 * hh + 3],
+                                                     bv[8 * hh + 4], bv[8 * hh + 5], bv[8 * hh + 6], bv[8 * hh + 7]);
+                }
+                sbw[0] |= sa << (8 * gi);
+                sbw[1] |= sbb << (8 * gi);
+                nf |= live ? nonfinite(ba) | nonfinite(bb) : 0u;
+                } else {
                 uint32_t m8[8];
 #pragma unroll
                 for (int j = 0; j < 8; j++) m8[j] = hmax_abs2(w[j], w[j + 8]);
@@ -324,6 +407,7 @@ __global__ void __launch_bounds__(kNvThreads, kN1Ctas)
                     }
                     sbw[h] |= sb[h] << (8 * gi);
                     nf |= live ? nonfinite(bits[h]) : 0u;
+                }
                 }
             }
             if (col_tma) {
@@ -508,7 +592,8 @@ __global__ void __launch_bounds__(kNvThreads, 2)
 template <auto Kernel>
 static cudaError_t nvb_launch_1x16(const void *x, int64_t M, int64_t K, const float *amax, uint64_t seed,
                                    uint64_t offset, uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT,
-                                   float *s_global, int32_t *status, cudaStream_t st, bool after_amax)
+                                   float *s_global, int32_t *status, cudaStream_t st, bool after_amax,
+                                   uint32_t sign_mask = 0, const float *amax_c = nullptr, float *s_global_c = nullptr)
 {
     constexpr int smem = N1Cfg::kSmem + kN1BoxBytes;
     alignas(64) CUtensorMap map, cmap;
@@ -534,7 +619,7 @@ static cudaError_t nvb_launch_1x16(const void *x, int64_t M, int64_t K, const fl
     if (grid < 1) grid = 1;   // an empty tensor still gets its global scale
     const PhiloxKeys keys = philox_keys(seed);
     return launch_k(after_amax, Kernel, dim3(grid), dim3(kNvThreads), smem, st, map, M, K, amax, keys, offset, q_row,
-                    sb_row, q_colT, sb_colT, s_global, status, cmap, col_tma);
+                    sb_row, q_colT, sb_colT, s_global, status, cmap, col_tma, sign_mask, amax_c, s_global_c);
 }
 
 template <auto Kernel>
@@ -580,6 +665,22 @@ cudaError_t launch_nvfp4_bf16(const void *x, int64_t M, int64_t K, int blk, int 
     return rnd == 0 ? nvb_launch_1x16<k_nvfp4_bf16_1x16<2, 0>>(NVB_ARGS)
                     : nvb_launch_1x16<k_nvfp4_bf16_1x16<2, 1>>(NVB_ARGS);
 #undef NVB_ARGS
+}
+
+// The NVFP4 recipe's two copies of a BF16 tensor in one pass (the rowwise
+// 1x16 copy of x with the tensor scale from amax_row, the columnwise copy of
+// its random Hadamard transform with the one from amax_col), behind the pass
+// that reduced both maxima (after_amax) or with maxima given.
+cudaError_t launch_nvfp4_bf16_recipe(const void *x, int64_t M, int64_t K, uint32_t sign_mask, int rnd, uint64_t seed,
+                                     uint64_t offset, const float *amax_row, uint8_t *q_row, uint8_t *sb_row,
+                                     float *s_global_row, const float *amax_col, uint8_t *q_colT, uint8_t *sb_colT,
+                                     float *s_global_col, int32_t *status, cudaStream_t st, bool after_amax)
+{
+#define NVR_ARGS x, M, K, amax_row, seed, offset, q_row, sb_row, q_colT, sb_colT, s_global_row, status, st, after_amax, \
+                 sign_mask, amax_col, s_global_col
+    return rnd == 0 ? nvb_launch_1x16<k_nvfp4_bf16_1x16<0, 0, true>>(NVR_ARGS)
+                    : nvb_launch_1x16<k_nvfp4_bf16_1x16<0, 1, true>>(NVR_ARGS);
+#undef NVR_ARGS
 }
 
 }  // namespace qk

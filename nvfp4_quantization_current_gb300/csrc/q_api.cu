@@ -92,7 +92,7 @@ extern "C" {
 
 const char *q_last_error(void) { return g_err; }
 
-int q_abi_version(void) { return 2; }
+int q_abi_version(void) { return 3; }
 
 q_status q_amax(const void *x, q_dtype in, int64_t n, float *amax, int32_t *status, q_stream_t stream)
 {
@@ -322,12 +322,13 @@ q_status q_nvfp4_rht_amax2(const void *x, q_dtype in, int64_t M, int64_t K, uint
 q_status q_nvfp4_recipe(const void *x, q_dtype in, int64_t M, int64_t K, uint32_t sign_mask, q_round rnd,
                         uint64_t seed, uint64_t offset, uint8_t *q_row, uint8_t *sb_row, float *amax_row,
                         float *s_global_row, uint8_t *q_colT, uint8_t *sb_colT, float *amax_colT,
-                        float *s_global_colT, int32_t *status, q_stream_t stream)
+                        float *s_global_colT, q_amax_mode amax_mode, int32_t *status, q_stream_t stream)
 {
     const char *fn = "q_nvfp4_recipe";
     TRY(check_dims(fn, M, K));
     TRY(check_in(fn, x, in, M * K));
     if (rnd != Q_RN && rnd != Q_SR) return fail(Q_ERR_ARG, "%s: rnd %d is not Q_RN or Q_SR", fn, (int)rnd);
+    if (amax_mode != Q_AMAX_COMPUTE && amax_mode != Q_AMAX_GIVEN) return fail(Q_ERR_ARG, "%s: bad amax_mode %d", fn, (int)amax_mode);
     if (sign_mask > 0xFFFFu) return fail(Q_ERR_ARG, "%s: sign_mask 0x%x has bits above bit 15", fn, sign_mask);
     TRY(multiple(fn, "K", K, 16));
     TRY(multiple(fn, "M", M, 16));
@@ -341,10 +342,19 @@ q_status q_nvfp4_recipe(const void *x, q_dtype in, int64_t M, int64_t K, uint32_
         TRY(need(fn, "q_colT", q_colT, 16));
         TRY(need(fn, "sb_colT", sb_colT, 16));   // written in 8-byte pieces
     }
-    // one read for both maxima, then the rowwise cast and the transformed columnwise cast with them
-    LAUNCH(fn, qk::launch_rht_amax(x, (int)in, M, K, sign_mask, amax_colT, amax_row, status, S(stream)));
+    // one read for both maxima (unless given), then the rowwise cast and the
+    // transformed columnwise cast with them: for BF16 in one pass over x,
+    // for FP32 in two
+    const bool compute = amax_mode == Q_AMAX_COMPUTE;
+    if (compute) LAUNCH(fn, qk::launch_rht_amax(x, (int)in, M, K, sign_mask, amax_colT, amax_row, status, S(stream)));
+    if (in == Q_BF16) {
+        LAUNCH(fn, qk::launch_nvfp4_bf16_recipe(x, M, K, sign_mask, (int)rnd, seed, offset, amax_row, q_row, sb_row,
+                                                s_global_row, amax_colT, q_colT, sb_colT, s_global_colT, status,
+                                                S(stream), compute));
+        return Q_OK;
+    }
     LAUNCH(fn, qk::launch_nvfp4(x, (int)in, M, K, (int)Q_B1x16, (int)rnd, seed, offset, amax_row, q_row, sb_row, nullptr,
-                                nullptr, s_global_row, status, S(stream), true));
+                                nullptr, s_global_row, status, S(stream), compute));
     LAUNCH(fn, qk::launch_nvfp4_rht_colT(x, (int)in, M, K, sign_mask, (int)rnd, seed, offset, false, amax_colT, q_colT,
                                          sb_colT, s_global_colT, status, S(stream)));
     return Q_OK;

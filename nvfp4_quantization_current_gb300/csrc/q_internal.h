@@ -96,6 +96,13 @@ cudaError_t launch_nvfp4(const void *x, int dt, int64_t M, int64_t K, int blk, i
 cudaError_t launch_nvfp4_bf16(const void *x, int64_t M, int64_t K, int blk, int rnd, uint64_t seed, uint64_t offset,
                               const float *amax, uint8_t *q_row, uint8_t *sb_row, uint8_t *q_colT, uint8_t *sb_colT,
                               float *s_global, int32_t *status, cudaStream_t st, bool after_amax);
+// NVFP4 recipe, BF16 input: rowwise 1x16 copy of x and columnwise copy of its
+// random Hadamard transform in one pass, with the two tensor maxima given
+// (after_amax: launched behind the kernel that reduced them)
+cudaError_t launch_nvfp4_bf16_recipe(const void *x, int64_t M, int64_t K, uint32_t sign_mask, int rnd, uint64_t seed,
+                                     uint64_t offset, const float *amax_row, uint8_t *q_row, uint8_t *sb_row,
+                                     float *s_global_row, const float *amax_col, uint8_t *q_colT, uint8_t *sb_colT,
+                                     float *s_global_col, int32_t *status, cudaStream_t st, bool after_amax);
 
 // dequantizers
 cudaError_t launch_dq_cs(const uint8_t *q, const float *s, int64_t R, int64_t C, int fmt, int out,

@@ -130,14 +130,12 @@ def quantize_shard_nvfp4_recipe(x_local: torch.Tensor, sign_mask: int, rounding=
     then the rowwise copy of x and the columnwise copy of its transform with
     the global maxima, both with the shard's counter offset (see
     quantize_shard_nvfp4).  Returns (row, colT) like q_nvfp4_recipe."""
-    from . import q_nvfp4, q_nvfp4_rht_amax2, q_nvfp4_rht_colT
+    from . import q_nvfp4_recipe, q_nvfp4_rht_amax2
     off = _shard_offset(x_local, offset, row_base, group)
     a_rht, a_x = q_nvfp4_rht_amax2(x_local, sign_mask, status=status)
     allreduce_amax_(a_rht, group)
     allreduce_amax_(a_x, group)
-    row = q_nvfp4(x_local, "1x16", rounding, seed, off, rowwise=True, colwise=False, amax=a_x, status=status)
-    col = q_nvfp4_rht_colT(x_local, sign_mask, rounding, seed, off, amax=a_rht, status=status)
-    return row, col
+    return q_nvfp4_recipe(x_local, sign_mask, rounding, seed, off, amax_row=a_x, amax_col=a_rht, status=status)
 
 
 def all_gather_shards(t_local: torch.Tensor, dim: int = 0, group=None) -> torch.Tensor:

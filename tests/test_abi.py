@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
     for n in declared_functions():
         assert hasattr(L, n), n
         assert n in Q.SIGNATURES, n
-    assert L.q_abi_version() == 2
+    assert L.q_abi_version() == 3
 
 
 A = ctypes.c_void_p(0x10000)        # an aligned non-NULL address that is never dereferenced
@@ -179,8 +179,8 @@ def test_blockwise_mx_validation(L):
 
 def test_nvfp4_recipe_validation(L):
     U64 = ctypes.c_uint64
-    args = lambda M, K, mask=0x1234, rnd=Q.Q_RN, amax_row=A: (A, Q.Q_BF16, M, K, mask, rnd, U64(0), U64(0), A, A,
-                                                           amax_row, A, A, A, A, A, None, None)
+    args = lambda M, K, mask=0x1234, rnd=Q.Q_RN, amax_row=A, mode=Q.Q_AMAX_COMPUTE: (
+        A, Q.Q_BF16, M, K, mask, rnd, U64(0), U64(0), A, A, amax_row, A, A, A, A, A, mode, None, None)
     st, _ = status_of(L, "q_nvfp4_recipe", *args(32, 24))
     assert st == Q.Q_ERR_SHAPE                     # K % 16
     st, _ = status_of(L, "q_nvfp4_recipe", *args(24, 32))
@@ -191,6 +191,8 @@ def test_nvfp4_recipe_validation(L):
     assert st == Q.Q_ERR_ARG
     st, msg = status_of(L, "q_nvfp4_recipe", *args(32, 32, amax_row=None))
     assert st == Q.Q_ERR_ARG and "amax_row" in msg
+    st, msg = status_of(L, "q_nvfp4_recipe", *args(32, 32, mode=7))
+    assert st == Q.Q_ERR_ARG and "amax_mode" in msg
     st, msg = status_of(L, "q_nvfp4_rht_amax2", A, Q.Q_BF16, 32, 32, 0x1234, A, ctypes.c_void_p(0x10002), None, None)
     assert st == Q.Q_ERR_ALIGN and "amax_x" in msg
     st, _ = status_of(L, "q_nvfp4_rht_amax2", A, Q.Q_BF16, 32, 40, 0x1234, A, A, None, None)
@@ -226,7 +228,7 @@ def test_nvfp4_columnwise_scale_buffers_need_16_byte_alignment(L):
     U64 = ctypes.c_uint64
     odd = ctypes.c_void_p(0x10001)
     st, msg = status_of(L, "q_nvfp4_recipe", A, Q.Q_BF16, 32, 32, 0x1234, Q.Q_RN, U64(0), U64(0), A, A, A, A,
-                        A, odd, A, A, None, None)
+                        A, odd, A, A, Q.Q_AMAX_COMPUTE, None, None)
     assert st == Q.Q_ERR_ALIGN and "sb_colT" in msg
     st, msg = status_of(L, "q_nvfp4", A, Q.Q_BF16, 16, 32, Q.Q_B1x16, Q.Q_RN, 0, 0, None, None, A, odd, A, 0, A,
                         None, None)
@@ -253,7 +255,8 @@ def _valid_calls():
         "q_nvfp4_rht_amax": (A, Q.Q_BF16, 16, 16, 0x1, A, None, None),
         "q_nvfp4_rht_amax2": (A, Q.Q_BF16, 16, 16, 0x1, A, A, None, None),
         "q_nvfp4_rht_colT": (A, Q.Q_BF16, 16, 16, 0x1, Q.Q_RN, 0, 0, A, A, A, Q.Q_AMAX_COMPUTE, A, None, None),
-        "q_nvfp4_recipe": (A, Q.Q_BF16, 16, 16, 0x1, Q.Q_RN, U64(0), U64(0), A, A, A, A, A, A, A, A, None, None),
+        "q_nvfp4_recipe": (A, Q.Q_BF16, 16, 16, 0x1, Q.Q_RN, U64(0), U64(0), A, A, A, A, A, A, A, A,
+                           Q.Q_AMAX_COMPUTE, None, None),
         "q_selftest_wait_timeout": (A, 1000, None),
         "dq_current_scaling": (A, A, 4, 4, Q.Q_E4M3, Q.Q_F32, A, None),
         "dq_mxfp8": (A, A, 4, 32, Q.Q_E4M3, Q.Q_ROW, Q.Q_F32, A, None),

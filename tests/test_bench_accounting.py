@@ -54,7 +54,8 @@ def expected(name, M, K, b):
         "dq_nvfp4_16x16 row->bf16": E // 2 + E // 256 + 4 + 2 * E,
         "nvfp4_rht_rn colT": 2 * E * b + E // 2 + E // 16 + 4 + 4,
         "nvfp4_rht_sr colT": 2 * E * b + E // 2 + E // 16 + 4 + 4,
-        "nvfp4_recipe_sr row + RHT colT": 3 * E * b + E + 2 * (E // 16) + 2 * (4 + 4),
+        # BF16: one read for both maxima, one for both copies; FP32 reads x once per copy
+        "nvfp4_recipe_sr row + RHT colT": (2 if b == 2 else 3) * E * b + E + 2 * (E // 16) + 2 * (4 + 4),
     }
     if name.startswith("dq_cs row->"):
         ob = 4 if name.endswith("float32") else 2

@@ -240,6 +240,20 @@ def test_nvfp4_recipe_equals_its_two_calls(kind, shape, bf16, rnd, mask, seed, o
     a_rht, a_x = Q.q_nvfp4_rht_amax2(dev(x), mask)
     f32eq(a_rht.item(), a, "amax2 rht")
     f32eq(a_x.item(), O.amax(x), "amax2 x")
+    # the same casts with both maxima given (the path a sharded caller takes)
+    ar = torch.tensor([w.amax], dtype=torch.float32, device="cuda")
+    ac = torch.tensor([a], dtype=torch.float32, device="cuda")
+    row2, col2 = Q.q_nvfp4_recipe(dev(x), mask, r, seed, offset, amax_row=ar, amax_col=ac, status=st)
+    torch.cuda.synchronize()
+    f32eq(ar.item(), w.amax, "given amax_row untouched")
+    f32eq(ac.item(), a, "given amax_colT untouched")
+    f32eq(row2.s_global.item(), w.s_global, "s_global_row, given")
+    f32eq(col2.s_global.item(), sg, "s_global_colT, given")
+    same(host(row2.q_row), w.q_row, "q_row, given")
+    same(host(row2.sb_row), w.sb_row, "sb_row, given")
+    same(host(col2.q_colT), q, "q_colT, given")
+    same(host(col2.sb_colT), sb, "sb_colT, given")
+    assert st.item() == 0
 
 
 def test_nvfp4_recipe_empty_and_nonfinite():
@@ -835,8 +849,8 @@ def test_nvfp4_recipe_row_shards_with_the_global_maxima():
     maxima = [Q.q_nvfp4_rht_amax2(dev(p), 0x2D4B) for p in parts]
     a_rht = torch.maximum(maxima[0][0], maxima[1][0])
     a_x = torch.maximum(maxima[0][1], maxima[1][1])
-    rows = [Q.q_nvfp4(dev(p), "1x16", "rn", rowwise=True, colwise=False, amax=a_x.clone()) for p in parts]
-    cols = [Q.q_nvfp4_rht_colT(dev(p), 0x2D4B, "rn", amax=a_rht.clone()) for p in parts]
+    got = [Q.q_nvfp4_recipe(dev(p), 0x2D4B, amax_row=a_x.clone(), amax_col=a_rht.clone()) for p in parts]
+    rows, cols = [g[0] for g in got], [g[1] for g in got]
     same(np.concatenate([host(r.q_row) for r in rows]), host(whole_row.q_row), "q_row")
     same(np.concatenate([host(r.sb_row) for r in rows]), host(whole_row.sb_row), "sb_row")
     same(np.concatenate([host(c.q_colT) for c in cols], axis=1), host(whole_col.q_colT), "q_colT")
@@ -844,6 +858,14 @@ def test_nvfp4_recipe_row_shards_with_the_global_maxima():
     r1, c1 = quantize_shard_nvfp4_recipe(dev(x), 0x2D4B)
     same(host(r1.q_row), host(whole_row.q_row), "helper q_row")
     same(host(c1.q_colT), host(whole_col.q_colT), "helper q_colT")
+    # stochastic rounding: each shard moves the Philox offset by its first row
+    from nvfp4_quantization_current_gb300.distributed import sr_offset
+    sw_row, sw_col = Q.q_nvfp4_recipe(dev(x), 0x2D4B, "sr", 12, 40)
+    got = [Q.q_nvfp4_recipe(dev(p), 0x2D4B, "sr", 12, sr_offset(40, r0, x.shape[1]), amax_row=a_x.clone(),
+                            amax_col=a_rht.clone()) for p, r0 in zip(parts, (0, 144))]
+    same(np.concatenate([host(g[0].q_row) for g in got]), host(sw_row.q_row), "SR q_row")
+    same(np.concatenate([host(g[1].q_colT) for g in got], axis=1), host(sw_col.q_colT), "SR q_colT")
+    same(np.concatenate([host(g[1].sb_colT) for g in got], axis=1), host(sw_col.sb_colT), "SR sb_colT")
 
 
 def test_shard_helpers_on_one_rank_equal_the_plain_calls():
