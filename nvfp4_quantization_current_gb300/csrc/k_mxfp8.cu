@@ -254,26 +254,35 @@ __global__ void __launch_bounds__(MxCfg::kThreads, 2) k_mxfp8_requant(const __gr
         for (int i = 0; i < 16; i++) part[warp][i][lane] = __float_as_uint(acc[i]) & 0x7FFFFFFFu;
         // the four warps of this 32-row block have posted their maxima (named
         // barrier 1..4 per block; the engine's CTA barrier after each tile
-        // orders the reads here before the next tile's writes)
+        // orders the reads here before the next tile's writes).  Warp wq of
+        // the block reduces columns 4wq..4wq+3 of each lane's 16, writes their
+        // scale codes and leaves their factors 2^(127 - code) in its own
+        // slots of those columns (read by no other warp before the second
+        // barrier); then every warp reads the 16 factors.
         asm volatile("bar.sync %0, 128;" ::"r"(1 + (warp >> 2)) : "memory");
-        const int w0 = warp & ~3;
-        float inv[16];
-        uint32_t code[16], nf = 0;
+        const int w0 = warp & ~3, wq = warp & 3;
+        const int64_t mblk = mb + 32 * (warp >> 2);
+        uint32_t cw = 0, nf = 0;
+        float invq[4];
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
+        for (int j = 0; j < 4; j++) {
+            const int i = 4 * wq + j;
             const uint32_t b = max(max(part[w0][i][lane], part[w0 + 1][i][lane]), max(part[w0 + 2][i][lane], part[w0 + 3][i][lane]));
-            code[i] = mx_code<FMT>(b);
-            inv[i] = mx_inv_scale(code[i]);
+            const uint32_t c = mx_code<FMT>(b);
+            cw |= c << (8 * j);
+            invq[j] = mx_inv_scale(c);
             nf |= nonfinite(b);
         }
-        if ((warp & 3) == 0 && kok && m0 < M) {
-            uint32_t sw[4];
 #pragma unroll
-            for (int q = 0; q < 4; q++)
-                sw[q] = code[4 * q] | (code[4 * q + 1] << 8) | (code[4 * q + 2] << 16) | (code[4 * q + 3] << 24);
-            stg16(e_col + (m0 / 32) * K + k, make_uint4(sw[0], sw[1], sw[2], sw[3]));
+        for (int j = 0; j < 4; j++) part[warp][4 * wq + j][lane] = __float_as_uint(invq[j]);
+        if (kok && mblk < M) {
+            stg4(e_col + (mblk / 32) * K + k + 4 * wq, cw);
             post_nonfinite(status, nf);
         }
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + (warp >> 2)) : "memory");
+        float inv[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) inv[i] = __uint_as_float(part[w0 + (i >> 2)][i][lane]);
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             float x[16];
