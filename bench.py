@@ -33,6 +33,7 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -648,6 +649,11 @@ def run_ours(args):
         sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
         sampler.start()
         time.sleep(0.3)
+        # no collector pass while the host queues the steps: a pause that
+        # outlasts the queued work would leave the device idle inside a call
+        gc.collect()
+        gc_on = gc.isenabled()
+        gc.disable()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
@@ -656,6 +662,8 @@ def run_ours(args):
             one_step(all_evs[s], per_kernel)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        if gc_on:
+            gc.enable()
         if world > 1:
             dist.barrier()
         return all_evs, wall, sampler.stop()
@@ -680,6 +688,11 @@ def run_ours(args):
             ev = brk_evs[s][ci]
             for pi in range(len(c.pieces)):
                 kern_ms.setdefault((ci, pi), []).append(ev[pi].elapsed_time(ev[pi + 1]))
+    # per-kernel time: the median over the K steps.  With an event after
+    # every kernel, a host stall long enough to drain the queued work leaves
+    # the device idle inside one event interval; the median keeps such a
+    # step from moving a kernel's time (and the choice of the dominant one).
+    kern_med = {key: statistics.median(v) for key, v in kern_ms.items()}
 
     peak, peak_kind = measured_peak()
     per_call = []
@@ -690,7 +703,7 @@ def run_ours(args):
         gbs = c.alg_bytes / (ms * 1e-3) / 1e9
         per_call.append({"call": c.name, "us": round(ms * 1e3, 2), "bytes": c.alg_bytes, "GB/s": round(gbs, 1),
                          "frac": round(gbs / peak, 3),
-                         "kernels": [[p[0], round(statistics.mean(kern_ms[(ci, pi)]) * 1e3, 2)]
+                         "kernels": [[p[0], round(kern_med[(ci, pi)] * 1e3, 2)]
                                      for pi, p in enumerate(c.pieces)]})
         r = per_recipe.setdefault(c.recipe, {"bytes": 0, "us": 0.0})
         r["bytes"] += c.alg_bytes
@@ -698,16 +711,16 @@ def run_ours(args):
         for pi, p in enumerate(c.pieces):
             k = per_kernel.setdefault(p[0], {"src": p[1], "bytes": 0, "us": 0.0, "launches": 0})
             k["bytes"] += p[2]
-            k["us"] += statistics.mean(kern_ms[(ci, pi)]) * 1e3
+            k["us"] += kern_med[(ci, pi)] * 1e3
             k["launches"] += 1
     for r in per_recipe.values():
         r["GB/s"] = round(r["bytes"] / (r["us"] * 1e-6) / 1e9, 1)
         r["frac"] = round(r["GB/s"] / peak, 3)
         r["us"] = round(r["us"], 2)
-    # dominant kernel: the single launch with the longest mean time in the step
-    (dci, dpi) = max(kern_ms, key=lambda key: statistics.mean(kern_ms[key]))
+    # dominant kernel: the single launch with the longest (median) time in the step
+    (dci, dpi) = max(kern_med, key=lambda key: kern_med[key])
     dcall, dpiece = calls[dci], calls[dci].pieces[dpi]
-    dom_us = statistics.mean(kern_ms[(dci, dpi)]) * 1e3
+    dom_us = kern_med[(dci, dpi)] * 1e3
     dom_bytes = dpiece[2]
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
     key = f"{dcall.name.split()[0]}:{dpiece[0]}"
@@ -887,7 +900,8 @@ def run_ours(args):
             "gpu_launches": n_launches,
             "clocks": clocks,
             "breakdown": {"what": "per_kernel, per_call kernels and roofline: K more steps with a CUDA event after "
-                                  "every kernel (which serializes the kernels of a call)",
+                                  "every kernel (which serializes the kernels of a call); each kernel's time is "
+                                  "the median over the K steps",
                           "steps": args.steps, "clocks": brk_clocks, "wall_s_timed": round(brk_wall, 3)},
             "wall_s_timed": round(wall, 3),
         }
