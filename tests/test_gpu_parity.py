@@ -719,6 +719,48 @@ def test_nvfp4_bf16_nonfinite_and_overflowing_scales_match_the_oracle(case, rnd,
         assert st.item() & Q.Q_ST_NONFINITE
 
 
+@pytest.mark.parametrize("rnd", [O.RN, O.SR])
+@pytest.mark.parametrize("case", ["inf", "nan", "given_maxima_below_block_max"])
+def test_nvfp4_recipe_bf16_nonfinite_and_overflowing_scales_match_the_oracle(case, rnd):
+    """The one-pass recipe kernel on BF16 inputs with an inf or NaN element
+    (the transform spreads it over its 16-row group; the tensor scales become
+    0 or NaN) and with caller-given maxima far below the blocks' maxima: both
+    copies follow the oracle's IEEE rules byte for byte."""
+    x = W.gen("normal", (64, 96), 809, bf16=True)
+    xf = W.bf16_bits_to_f32(x)
+    big = np.float32(3.0e38)
+    xf[5, 7] = big
+    xf[40, 70] = -big
+    given = None
+    if case == "inf":
+        xf[20, 33] = np.inf
+    elif case == "nan":
+        xf[20, 33] = np.nan
+    else:
+        given = 1.0e-30
+    x = O.bf16_round(xf)
+    mask, r = 0x5A3C, "rn" if rnd == O.RN else "sr"
+    w = O.nvfp4(x, O.B1x16, rnd, seed=3, offset=11, rowwise=True, colwise=False, amax_in=given)
+    q, sb, a, sg = O.nvfp4_rht_colT(x, mask, rnd, seed=3, offset=11, amax_in=given)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kw = {}
+    if given is not None:
+        kw = dict(amax_row=torch.tensor([given], dtype=torch.float32, device="cuda"),
+                  amax_col=torch.tensor([given], dtype=torch.float32, device="cuda"))
+    row, col = Q.q_nvfp4_recipe(dev(x), mask, r, 3, 11, status=st, **kw)
+    torch.cuda.synchronize()
+    _f32_same_or_both_nan(row.amax.item(), w.amax, "amax_row")
+    _f32_same_or_both_nan(row.s_global.item(), w.s_global, "s_global_row")
+    _f32_same_or_both_nan(col.amax.item(), a, "amax_colT")
+    _f32_same_or_both_nan(col.s_global.item(), sg, "s_global_colT")
+    same(host(row.sb_row), w.sb_row, "sb_row")
+    same(host(row.q_row), w.q_row, "q_row")
+    same(host(col.sb_colT), sb, "sb_colT")
+    same(host(col.q_colT), q, "q_colT")
+    if given is None:
+        assert st.item() & Q.Q_ST_NONFINITE
+
+
 @pytest.mark.parametrize("bf16", [True, False])
 def test_nvfp4_encode_factor_case_through_the_kernel(bf16):
     """The hand-derived case of the oracle pin (A = 39, block maximum 19.625
