@@ -301,7 +301,7 @@ def parity_check(host_t, dev_t, torch, Q, O, full=True, threads=None, seed=0):
     ctypes calls release the GIL), with the tensor-wide maxima given: a band
     of a current-scaling or NVFP4 tensor is quantized with the whole tensor's
     amax, and a stochastic band with the counter offset of its first row
-    (r0 * K / 8), so that it is exactly that band of the whole-tensor result.
+    (r0 * K / 16), so that it is exactly that band of the whole-tensor result.
     Returns (fields compared, bytes compared)."""
     from concurrent.futures import ThreadPoolExecutor
 
@@ -446,7 +446,7 @@ def parity_check(host_t, dev_t, torch, Q, O, full=True, threads=None, seed=0):
             f32eq(g.s_global.item(), O.nvfp4_global(A)[1], f"{tag} s_global")
 
             def work(r0, r1, band):
-                w = O.nvfp4(band, blk, rnd, seed=sd, offset=r0 * K // 8, rowwise=True, colwise=True, amax_in=A)
+                w = O.nvfp4(band, blk, rnd, seed=sd, offset=r0 * K // 16, rowwise=True, colwise=True, amax_in=A)
                 sbr = h["sb_row"][r0:r1] if blk == O.B1x16 else h["sb_row"][r0 // 16:r1 // 16]
                 return [(h["q_row"][r0:r1], w.q_row, f"{tag} q_row"), (sbr, w.sb_row, f"{tag} sb_row"),
                         (h["q_colT"][:, r0 // 2:r1 // 2], w.q_colT, f"{tag} q_colT"),
@@ -463,7 +463,7 @@ def parity_check(host_t, dev_t, torch, Q, O, full=True, threads=None, seed=0):
             f32eq(g.s_global.item(), O.nvfp4_global(A)[1], f"{tag} s_global")
 
             def work(r0, r1, band):
-                q, sb, _, _ = O.nvfp4_rht_colT(band, RHT_MASK, rnd, seed=sd, offset=r0 * K // 8, amax_in=A)
+                q, sb, _, _ = O.nvfp4_rht_colT(band, RHT_MASK, rnd, seed=sd, offset=r0 * K // 16, amax_in=A)
                 return [(qc[:, r0 // 2:r1 // 2], q, f"{tag} q_colT"), (sc[:, r0 // 16:r1 // 16], sb, f"{tag} sb_colT")]
             over_bands(xh, work)
         elif kind == "recipe_sr":
@@ -477,8 +477,8 @@ def parity_check(host_t, dev_t, torch, Q, O, full=True, threads=None, seed=0):
             qr, sr, qc, sc = host(row.q_row), host(row.sb_row), host(col.q_colT), host(col.sb_colT)
 
             def work(r0, r1, band):
-                w = O.nvfp4(band, O.B1x16, O.SR, seed=4, offset=r0 * K // 8, rowwise=True, colwise=False, amax_in=A_x)
-                q, sb, _, _ = O.nvfp4_rht_colT(band, RHT_MASK, O.SR, seed=4, offset=r0 * K // 8, amax_in=A_r)
+                w = O.nvfp4(band, O.B1x16, O.SR, seed=4, offset=r0 * K // 16, rowwise=True, colwise=False, amax_in=A_x)
+                q, sb, _, _ = O.nvfp4_rht_colT(band, RHT_MASK, O.SR, seed=4, offset=r0 * K // 16, amax_in=A_r)
                 return [(qr[r0:r1], w.q_row, f"{tag} q_row"), (sr[r0:r1], w.sb_row, f"{tag} sb_row"),
                         (qc[:, r0 // 2:r1 // 2], q, f"{tag} q_colT"), (sc[:, r0 // 16:r1 // 16], sb, f"{tag} sb_colT")]
             over_bands(xh, work)
@@ -1087,7 +1087,7 @@ def oracle_band_work(host_t, frac, nbands):
         A = Max(len(bs))
         sb = M * K // 16 if blk == O.B1x16 else M * K // 256
         work.append(([[lambda i=i, b=b: A.put(i, O.amax(b[2])) for i, b in enumerate(bs)],
-                      [lambda b=b: O.nvfp4(b[2], blk, rnd, seed=seed, offset=b[0] * K // 8, rowwise=True, colwise=True,
+                      [lambda b=b: O.nvfp4(b[2], blk, rnd, seed=seed, offset=b[0] * K // 16, rowwise=True, colwise=True,
                                            amax_in=A.get()) for b in bs]],
                      2 * s_.nbytes + M * K + 2 * sb + 4))
         r = O.nvfp4(s_, blk, rnd, seed=seed)
@@ -1106,9 +1106,9 @@ def oracle_band_work(host_t, frac, nbands):
                 Ax.put(i, O.amax(b[2]))
         phases = [[lambda i=i, b=b: maxima(i, b) for i, b in enumerate(bs)]]
         if row_copy:
-            phases.append([lambda b=b: O.nvfp4(b[2], O.B1x16, rnd, seed=seed, offset=b[0] * K // 8, rowwise=True,
+            phases.append([lambda b=b: O.nvfp4(b[2], O.B1x16, rnd, seed=seed, offset=b[0] * K // 16, rowwise=True,
                                                colwise=False, amax_in=Ax.get()) for b in bs])
-        phases.append([lambda b=b: O.nvfp4_rht_colT(b[2], RHT_MASK, rnd, seed=seed, offset=b[0] * K // 8,
+        phases.append([lambda b=b: O.nvfp4_rht_colT(b[2], RHT_MASK, rnd, seed=seed, offset=b[0] * K // 16,
                                                      amax_in=Ar.get()) for b in bs])
         copies = (2 if row_copy else 1) * (M * K // 2 + M * K // 16 + 4)
         work.append((phases, (3 if row_copy else 2) * s_.nbytes + copies))

@@ -51,7 +51,8 @@ QD uint32_t nv_sb_code(uint32_t b, float alpha_g)
 // alpha_g also serves b = 0).
 
 // Codes of one row chunk (VEC elements, VEC/2 bytes) with scale factor enc;
-// SR draws the Philox block of element index i0 (row-major, stream 0).
+// SR: the chunk's elements i0 .. (row-major, stream 0) are word (i0 % 16) / 4
+// onward of Philox block offset + i0 / 16.
 template <int DT, int RND>
 QD uint32_t nv_row_codes(const uint4 &v, float enc, const PhiloxKeys &keys, uint64_t offset, int64_t i0)
 {
@@ -62,15 +63,10 @@ QD uint32_t nv_row_codes(const uint4 &v, float enc, const PhiloxKeys &keys, uint
 #pragma unroll
     for (int j = 0; j < VEC; j += 2) mul2(y[j], y[j + 1], enc, enc);
     if (RND == 1) {
-        const uint4 R = sr_bits_rk<0>(offset + (uint64_t)(i0 >> 3), keys);
-        const int e0 = (int)(i0 & 7);
-        const uint32_t dm = sr_dither_mask(enc);
-#pragma unroll
-        for (int j = 0; j < VEC; j += 2) {   // draws e0 + j, e0 + j + 1: one word (e0 is 0, or 4 for FP32 chunks)
-            const uint32_t w = VEC == 8 ? word(R, j >> 1) : (e0 ? word(R, 2 + (j >> 1)) : word(R, j >> 1));
-            y[j] = sr_e2m1_dither(y[j], sr_dither_lo(w, dm));
-            y[j + 1] = sr_e2m1_dither(y[j + 1], sr_dither_hi(w, dm));
-        }
+        const uint4 R = sr_bits_rk<0>(offset + (uint64_t)(i0 >> 4), keys);
+        const int t = (int)((i0 >> 2) & 3);
+        if (VEC == 4) return cvt_rs_fp4x4(y[0], y[1], y[2], y[3], word(R, t));
+        return cvt_rs_fp4x8(y, word(R, t), word(R, t + 1));
     }
     return cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
@@ -185,16 +181,14 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4(const __grid_constant_
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) mul2(y[j], y[j + 1], enc, enc);
                 if (RND == 1) {
-                    // rows m0 .. m0 + 7 of column k + c, stream 1: Philox block (m0 / 8) * K + k + c
-                    const uint4 R = sr_bits_rk<1>(offset + (uint64_t)((m0 >> 3) * K + k + c), keys);
-                    const uint32_t dm = sr_dither_mask(enc);
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
-                        y[j] = sr_e2m1_dither(y[j], sr_dither_lo(word(R, j >> 1), dm));
-                        y[j + 1] = sr_e2m1_dither(y[j + 1], sr_dither_hi(word(R, j >> 1), dm));
-                    }
+                    // rows m0 .. m0 + 7 of column k + c, stream 1: half (m0 % 16) / 8 of
+                    // Philox block (m0 / 16) * K + k + c (words 0-1 or 2-3)
+                    const uint4 R = sr_bits_rk<1>(offset + (uint64_t)((m0 >> 4) * K + k + c), keys);
+                    const bool hi8 = (m0 & 8) != 0;
+                    colw[c] = cvt_rs_fp4x8(y, hi8 ? R.z : R.x, hi8 ? R.w : R.y);
+                } else {
+                    colw[c] = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
                 }
-                colw[c] = cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
             }
             if (RND == 0 && (warp & 1) == 0) {   // one store of VEC codes (bytes lane*VEC .. +VEC-1)
                 if constexpr (VEC == 8) *reinterpret_cast<uint2 *>(&sSB[warp >> 1][lane * VEC]) = make_uint2(sbw[0], sbw[1]);
@@ -390,32 +384,26 @@ __global__ void __launch_bounds__(kEngThreads, 1) k_nvfp4_rht(const __grid_const
             post_nonfinite(status, live && (kb + c0 < K) ? nonfinite(ba) | nonfinite(bb) : 0u);
 #pragma unroll
             for (int i = 0; i < 16; i++) mul2(a[i], b[i], ea, eb);
+            // rows m .. m + 15 of columns kb + c0, kb + c0 + 1, stream 1: Philox blocks
+            // (m / 16) * K + column, words 0-1 for rows 0-7 and 2-3 for rows 8-15
+            uint4 Ra = make_uint4(0u, 0u, 0u, 0u), Rb = Ra;
             if constexpr (RND == 1) {
-                // rows m .. m + 15 of columns kb + c0, kb + c0 + 1, stream 1: Philox blocks
-                // (m / 8 + hh) * K + column, two per column
-                const int64_t m = mb + 16 * g;
-                const uint32_t dma = sr_dither_mask(ea), dmb = sr_dither_mask(eb);
-#pragma unroll
-                for (int hh = 0; hh < 2; hh++) {
-                    const uint64_t gb = offset + (uint64_t)(((m >> 3) + hh) * K + kb + c0);
-                    const uint4 Ra = sr_bits_rk<1>(gb, keys);
-                    const uint4 Rb = sr_bits_rk<1>(gb + 1, keys);
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
-                        const uint32_t wa = word(Ra, j >> 1), wb = word(Rb, j >> 1);
-                        a[8 * hh + j] = sr_e2m1_dither(a[8 * hh + j], sr_dither_lo(wa, dma));
-                        a[8 * hh + j + 1] = sr_e2m1_dither(a[8 * hh + j + 1], sr_dither_hi(wa, dma));
-                        b[8 * hh + j] = sr_e2m1_dither(b[8 * hh + j], sr_dither_lo(wb, dmb));
-                        b[8 * hh + j + 1] = sr_e2m1_dither(b[8 * hh + j + 1], sr_dither_hi(wb, dmb));
-                    }
-                }
+                const uint64_t gb = offset + (uint64_t)(((mb + 16 * g) >> 4) * K + kb + c0);
+                Ra = sr_bits_rk<1>(gb, keys);
+                Rb = sr_bits_rk<1>(gb + 1, keys);
             }
 #pragma unroll
             for (int hh = 0; hh < 2; hh++) {
-                code[2 * p][hh] = cvt_fp4x8(a[8 * hh], a[8 * hh + 1], a[8 * hh + 2], a[8 * hh + 3], a[8 * hh + 4],
-                                            a[8 * hh + 5], a[8 * hh + 6], a[8 * hh + 7]);
-                code[2 * p + 1][hh] = cvt_fp4x8(b[8 * hh], b[8 * hh + 1], b[8 * hh + 2], b[8 * hh + 3], b[8 * hh + 4],
-                                                b[8 * hh + 5], b[8 * hh + 6], b[8 * hh + 7]);
+                const float *pa = a + 8 * hh, *pb = b + 8 * hh;
+                if constexpr (RND == 1) {
+                    code[2 * p][hh] = cvt_rs_fp4x8(pa[0], pa[1], pa[2], pa[3], pa[4], pa[5], pa[6], pa[7],
+                                                   hh ? Ra.z : Ra.x, hh ? Ra.w : Ra.y);
+                    code[2 * p + 1][hh] = cvt_rs_fp4x8(pb[0], pb[1], pb[2], pb[3], pb[4], pb[5], pb[6], pb[7],
+                                                       hh ? Rb.z : Rb.x, hh ? Rb.w : Rb.y);
+                } else {
+                    code[2 * p][hh] = cvt_fp4x8(pa[0], pa[1], pa[2], pa[3], pa[4], pa[5], pa[6], pa[7]);
+                    code[2 * p + 1][hh] = cvt_fp4x8(pb[0], pb[1], pb[2], pb[3], pb[4], pb[5], pb[6], pb[7]);
+                }
             }
         }
         if (PASS == 0) return;

@@ -37,11 +37,11 @@
 //   and written as q_colT rows.
 //
 // Stochastic rounding: Philox4x32-10 with round keys formed on the host.
-// The rowwise copy takes stream 0 block offset + (m K + k) / 8 for the 8
+// The rowwise copy takes stream 0 block offset + (m K + k) / 16 for the 16
 // consecutive columns k.. of row m, the columnwise copy stream 1 block
-// offset + (m / 8) K + k for the 8 consecutive rows m.. of column k (m a
-// multiple of 8); element j of a block uses the 16 bits at word j / 2, low
-// half for even j, and is rounded with sr_e2m1_dither.
+// offset + (m / 16) K + k for the 16 consecutive rows m.. of column k (k,
+// m multiples of 16); word t of a block serves elements 4t .. 4t + 3, which
+// the conversion with random bits rounds (cvt_rs_fp4x4).
 #include <cstring>
 
 #include "q_engine.cuh"
@@ -153,20 +153,12 @@ QD void bf16x8_to_f32(const uint4 &v, float (&y)[8])
 }
 
 // E2M1 codes of 8 values (y[0] in bits 3-0) after the products y *= enc;
-// with stochastic rounding element j takes the dither of its 16 bits of the
-// Philox block R (word j / 2, low half for even j) under the block's mask dm.
-template <int RND> QD uint32_t nvb_codes8(float (&y)[8], float enc, const uint4 &R, uint32_t dm)
+// with stochastic rounding y[0..3] take the random word r0 and y[4..7] r1.
+template <int RND> QD uint32_t nvb_codes8(float (&y)[8], float enc, uint32_t r0, uint32_t r1)
 {
 #pragma unroll
     for (int j = 0; j < 8; j += 2) mul2(y[j], y[j + 1], enc, enc);
-    if (RND == 1) {
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-            const uint32_t w = word(R, j >> 1);
-            y[j] = sr_e2m1_dither(y[j], sr_dither_lo(w, dm));
-            y[j + 1] = sr_e2m1_dither(y[j + 1], sr_dither_hi(w, dm));
-        }
-    }
+    if (RND == 1) return cvt_rs_fp4x8(y, r0, r1);
     return cvt_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
 
@@ -263,13 +255,13 @@ __global__ void __launch_bounds__(kNvThreads, kN1Ctas)
             const int64_t left = M - (mb + r0);
             const int live_rows = k0 < K ? (int)(left < 2 * BPT ? (left > 0 ? left : 0) : 2 * BPT) : 0;
             // row m0 = mb + r0 and its successors every 2 rows: output pointers and the Philox
-            // block of the first chunk, each advanced by a fixed stride per row pair
+            // block of the 1x16 block (words 0-1: its first 8 elements, 2-3: the last 8), each
+            // advanced by a fixed stride per row pair
             uint8_t *qr = q_row + (mb + r0) * (K / 2) + (k0 >> 1);
             uint8_t *sr = sb_row + (mb + r0) * (K / 16) + (k0 >> 4);
-            uint64_t ga = offset + (uint64_t)(((mb + r0) * K + k0 + 8 * s) >> 3);
+            uint64_t ga = offset + (uint64_t)(((mb + r0) * K + k0) >> 4);
             const int64_t qstep = K, sstep = K / 8;   // two rows of codes / scales
-            const uint64_t gstep = (uint64_t)(K >> 2);   // two rows of Philox blocks
-            const uint64_t gz = (uint64_t)(1 - 2 * s);   // the second chunk's block, relative to the first
+            const uint64_t gstep = (uint64_t)(K >> 3);   // two rows of Philox blocks
             // fully unrolled, except with stochastic rounding beside the column role, where eight
             // copies of the Philox-heavy body next to the column code stall on instruction fetch
             // (ncu: 61 -> 79 us at 8192 x 4096)
@@ -283,17 +275,15 @@ __global__ void __launch_bounds__(kNvThreads, kN1Ctas)
                 uint32_t bits[1] = {halves_max_bits(mx)}, sb[1];
                 nv_sb_codes<1>(bits, sb, alpha_g, lut, lut_base, tab);
                 const float enc = nv_enc(enc_tab, sb[0], lane);
-                const uint32_t dm = RND == 1 ? sr_dither_mask(enc) : 0u;
-                uint4 Ra = make_uint4(0u, 0u, 0u, 0u), Rz = Ra;
-                if (RND == 1) {
-                    Ra = sr_bits_rk<0>(ga, keys);
-                    Rz = sr_bits_rk<0>(ga + gz, keys);
-                }
+                uint4 R = make_uint4(0u, 0u, 0u, 0u);
+                if (RND == 1) R = sr_bits_rk<0>(ga, keys);
+                // va holds elements 8s .. 8s + 7 of the block, vz the other half
+                const uint32_t ra0 = s ? R.z : R.x, ra1 = s ? R.w : R.y, rz0 = s ? R.x : R.z, rz1 = s ? R.y : R.w;
                 float y[8];
                 bf16x8_to_f32(va, y);
-                const uint32_t ca = nvb_codes8<RND>(y, enc, Ra, dm);
+                const uint32_t ca = nvb_codes8<RND>(y, enc, ra0, ra1);
                 bf16x8_to_f32(vz, y);
-                const uint32_t cz = nvb_codes8<RND>(y, enc, Rz, dm);
+                const uint32_t cz = nvb_codes8<RND>(y, enc, rz0, rz1);
                 if (2 * i < live_rows) {
                     stg8(qr, s ? cz : ca, s ? ca : cz);
                     *sr = (uint8_t)sb[0];
@@ -352,30 +342,26 @@ __global__ void __launch_bounds__(kNvThreads, kN1Ctas)
                 const float ea = nv_enc(enc_tab_c, sa, lane), eb = nv_enc(enc_tab_c, sbb, lane);
 #pragma unroll
                 for (int r = 0; r < 16; r++) mul2(a[r], bv[r], ea, eb);
+                // rows m16 .. m16 + 15 of columns k, k + 1, stream 1: Philox blocks
+                // (m16 / 16) K + column, words 0-1 for rows 0-7 and 2-3 for rows 8-15
+                uint4 Ra = make_uint4(0u, 0u, 0u, 0u), Rb = Ra;
                 if constexpr (RND == 1) {
-                    // rows m16 .. m16 + 15 of columns k, k + 1, stream 1: Philox blocks
-                    // (m16 / 8 + hh) K + column, two per column
-                    const uint32_t dma = sr_dither_mask(ea), dmb = sr_dither_mask(eb);
-#pragma unroll
-                    for (int hh = 0; hh < 2; hh++) {
-                        const uint64_t gb = offset + (uint64_t)(((m16 >> 3) + hh) * K + k);
-                        const uint4 Ra = sr_bits_rk<1>(gb, keys), Rb = sr_bits_rk<1>(gb + 1, keys);
-#pragma unroll
-                        for (int jj = 0; jj < 8; jj += 2) {
-                            const uint32_t wa = word(Ra, jj >> 1), wb = word(Rb, jj >> 1);
-                            a[8 * hh + jj] = sr_e2m1_dither(a[8 * hh + jj], sr_dither_lo(wa, dma));
-                            a[8 * hh + jj + 1] = sr_e2m1_dither(a[8 * hh + jj + 1], sr_dither_hi(wa, dma));
-                            bv[8 * hh + jj] = sr_e2m1_dither(bv[8 * hh + jj], sr_dither_lo(wb, dmb));
-                            bv[8 * hh + jj + 1] = sr_e2m1_dither(bv[8 * hh + jj + 1], sr_dither_hi(wb, dmb));
-                        }
-                    }
+                    const uint64_t gb = offset + (uint64_t)((m16 >> 4) * K + k);
+                    Ra = sr_bits_rk<1>(gb, keys);
+                    Rb = sr_bits_rk<1>(gb + 1, keys);
                 }
 #pragma unroll
                 for (int hh = 0; hh < 2; hh++) {
-                    code[0][2 * gi + hh] = cvt_fp4x8(a[8 * hh], a[8 * hh + 1], a[8 * hh + 2], a[8 * hh + 3],
-                                                     a[8 * hh + 4], a[8 * hh + 5], a[8 * hh + 6], a[8 * hh + 7]);
-                    code[1][2 * gi + hh] = cvt_fp4x8(bv[8 * hh], bv[8 * hh + 1], bv[8 * hh + 2], bv[8 * hh + 3],
-                                                     bv[8 * hh + 4], bv[8 * hh + 5], bv[8 * hh + 6], bv[8 * hh + 7]);
+                    const float *pa = a + 8 * hh, *pb = bv + 8 * hh;
+                    if constexpr (RND == 1) {
+                        code[0][2 * gi + hh] = cvt_rs_fp4x8(pa[0], pa[1], pa[2], pa[3], pa[4], pa[5], pa[6], pa[7],
+                                                            hh ? Ra.z : Ra.x, hh ? Ra.w : Ra.y);
+                        code[1][2 * gi + hh] = cvt_rs_fp4x8(pb[0], pb[1], pb[2], pb[3], pb[4], pb[5], pb[6], pb[7],
+                                                            hh ? Rb.z : Rb.x, hh ? Rb.w : Rb.y);
+                    } else {
+                        code[0][2 * gi + hh] = cvt_fp4x8(pa[0], pa[1], pa[2], pa[3], pa[4], pa[5], pa[6], pa[7]);
+                        code[1][2 * gi + hh] = cvt_fp4x8(pb[0], pb[1], pb[2], pb[3], pb[4], pb[5], pb[6], pb[7]);
+                    }
                 }
                 sbw[0] |= sa << (8 * gi);
                 sbw[1] |= sbb << (8 * gi);
@@ -394,16 +380,15 @@ __global__ void __launch_bounds__(kNvThreads, kN1Ctas)
 #pragma unroll
                 for (int h = 0; h < 2; h++) {   // h = 0: column 2p (low halves), 1: column 2p + 1
                     const float enc = nv_enc(enc_tab, sb[h], lane);
-                    const uint32_t dm = RND == 1 ? sr_dither_mask(enc) : 0u;
+                    // the column's 16 rows, stream 1: Philox block (m16 / 16) K + column
+                    uint4 R = make_uint4(0u, 0u, 0u, 0u);
+                    if (RND == 1) R = sr_bits_rk<1>(offset + (uint64_t)((m16 >> 4) * K + k + h), keys);
 #pragma unroll
                     for (int half = 0; half < 2; half++) {   // rows 8 half .. 8 half + 7 of the group
                         float y[8];
 #pragma unroll
                         for (int j = 0; j < 8; j++) y[j] = h ? bf16_hi_f32(w[8 * half + j]) : bf16_lo_f32(w[8 * half + j]);
-                        uint4 R = make_uint4(0u, 0u, 0u, 0u);
-                        if (RND == 1)
-                            R = sr_bits_rk<1>(offset + (uint64_t)(((m16 >> 3) + half) * K + k + h), keys);
-                        code[h][2 * gi + half] = nvb_codes8<RND>(y, enc, R, dm);
+                        code[h][2 * gi + half] = nvb_codes8<RND>(y, enc, half ? R.z : R.x, half ? R.w : R.y);
                     }
                     sbw[h] |= sb[h] << (8 * gi);
                     nf |= live ? nonfinite(bits[h]) : 0u;
@@ -555,15 +540,17 @@ __global__ void __launch_bounds__(kNvThreads, 2)
             nf |= nonfinite(bits);
         }
         uint8_t *qr = q_row + m0 * (K / 2) + (k >> 1);
-        const uint64_t g0 = offset + (uint64_t)((m0 * K + k) >> 3);
-        const uint32_t dm = RND == 1 ? sr_dither_mask(enc) : 0u;
+        // row m0 + j: Philox block of its 16 columns k & ~15 ..; this thread's 8
+        // columns are that block's first half (words 0-1) or second (2-3)
+        const uint64_t g0 = offset + (uint64_t)((m0 * K + k) >> 4);
+        const bool hi8 = (k & 8) != 0;
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             float y[8];
             bf16x8_to_f32(v[j], y);
             uint4 R = make_uint4(0u, 0u, 0u, 0u);
-            if (RND == 1) R = sr_bits_rk<0>(g0 + (uint64_t)j * (uint64_t)(K >> 3), keys);
-            colw[j] = nvb_codes8<RND>(y, enc, R, dm);
+            if (RND == 1) R = sr_bits_rk<0>(g0 + (uint64_t)j * (uint64_t)(K >> 4), keys);
+            colw[j] = nvb_codes8<RND>(y, enc, hi8 ? R.z : R.x, hi8 ? R.w : R.y);
             if (q_row != nullptr && live) stg4(qr + j * (K / 2), colw[j]);
         }
         post_nonfinite(status, nf);

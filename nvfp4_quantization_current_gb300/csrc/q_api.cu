@@ -92,7 +92,7 @@ extern "C" {
 
 const char *q_last_error(void) { return g_err; }
 
-int q_abi_version(void) { return 3; }
+int q_abi_version(void) { return 4; }
 
 q_status q_amax(const void *x, q_dtype in, int64_t n, float *amax, int32_t *status, q_stream_t stream)
 {

@@ -359,38 +359,39 @@ template <uint32_t STREAM> QD uint4 sr_bits_rk(uint64_t g, const PhiloxKeys &K)
     return philox4x32_10_rk(make_uint4((uint32_t)g, (uint32_t)(g >> 32), STREAM, 0u), K);
 }
 
-// Stochastic rounding onto the E2M1 grid as an integer dither.  With
-// a = |y| < 6 between the grid neighbours lo and lo + ulp (ulp 0.5 below 2,
-// 1 in [2, 4), 2 in [4, 6)) and frac = (a - lo) / ulp, the result rounds up
-// iff R < frac * 2^16 for the element's 16 random bits R (read as an
-// integer); it carries y's sign, and |y| >= 6 gives 6.
-// ys = a * 2^-126 rounded up maps the grid onto FP32 values with one
-// mantissa bit: 1 -> 2^-126 (the smallest normal), the spacing 0.5 below 2
-// onto the subnormal / first-binade spacing 2^-127, and so on up to 6.  Its
-// 22 bits below that kept bit are L = ceil(frac * 2^22) (exact, L = frac * 2^22,
-// for a >= 1; the rounding up makes L the ceiling below 1, and a carry into
-// the kept bit means a already rounds to the next grid value).  Adding
-// D = 2^22 - 1 - 64 R and dropping the 22 bits carries into the kept bit iff
-// L > 64 R, i.e. iff R < frac * 2^16 (64 R is an integer, so 64 R < F iff
-// 64 R < ceil(F)).  Magnitudes from 6 up to inf stay >= 6 (or inf) and the
-// saturating conversion gives 6 as for y; D = 0 (dither_mask 0, taken for a
-// block whose encode factor is not finite) passes inf and NaN through
-// unchanged, as round-to-nearest would see them.  The result carries y's
-// sign, through the exact factor +-2^126.
-QD float sr_e2m1_dither(float y, uint32_t D)
+// Stochastic rounding onto the E2M1 grid by the conversion with random bits
+// (cvt.rs.satfinite.e2m1x4.f32).  For a = |y| < 6 between the grid
+// neighbours lo and lo + ulp (ulp 0.5 below 2, 1 in [2, 4), 2 in [4, 6)),
+// T = floor(((a - lo) / ulp) * 2^16), the code rounds up iff T + R >= 2^16
+// for the element's 16-bit draw R; |y| >= 6 gives 6, NaN gives +6 as the
+// round-to-nearest conversion does, and the code carries y's sign.  The 32
+// random bits r of a group of four give two draws, U0 = bytes 0 and 2 of r
+// (byte 2 high) and U1 = bytes 1 and 3 (byte 3 high): y0 takes U0, y1 U0
+// bit-reversed, y2 U1 and y3 U1 bit-reversed (the instruction's assignment
+// when the operands are passed as {y3, y2, y1, y0}, which also puts y0's
+// code in bits 3-0).
+QD uint32_t cvt_rs_fp4x4(float y0, float y1, float y2, float y3, uint32_t r)
 {
-    const float ys = __fmul_ru(fabsf(y), 0x1p-126f);
-    const uint32_t t = (__float_as_uint(ys) + D) & 0xFFC00000u;
-    return __fmul_rn(__uint_as_float(t), __uint_as_float((__float_as_uint(y) & 0x80000000u) | 0x7E800000u));
+    uint16_t d;
+    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;" : "=h"(d) : "f"(y3), "f"(y2), "f"(y1), "f"(y0), "r"(r));
+    return d;
 }
-
-// D of the low / high 16-bit draw of a Philox word: m & ~(R << 6), which for
-// m = 2^22 - 1 is 2^22 - 1 - 64 R, and for m = 0 is 0.
-QD uint32_t sr_dither_lo(uint32_t w, uint32_t m) { return m & ~((w << 6) & 0x3FFFC0u); }
-QD uint32_t sr_dither_hi(uint32_t w, uint32_t m) { return m & ~((w >> 10) & 0x3FFFC0u); }
-// The dither mask of a block with encode factor enc: 2^22 - 1 if enc is
-// finite, 0 otherwise.
-QD uint32_t sr_dither_mask(float enc) { return (__float_as_uint(enc) & 0x7F800000u) != 0x7F800000u ? 0x3FFFFFu : 0u; }
+// Eight values (y0 in bits 3-0) with the random words r0 (y0..y3) and r1 (y4..y7).
+QD uint32_t cvt_rs_fp4x8(float y0, float y1, float y2, float y3, float y4, float y5, float y6, float y7,
+                         uint32_t r0, uint32_t r1)
+{
+    uint32_t c;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 lo, {%4, %3, %2, %1}, %9;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 hi, {%8, %7, %6, %5}, %10;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(c) : "f"(y0), "f"(y1), "f"(y2), "f"(y3), "f"(y4), "f"(y5), "f"(y6), "f"(y7), "r"(r0), "r"(r1));
+    return c;
+}
+QD uint32_t cvt_rs_fp4x8(const float (&y)[8], uint32_t r0, uint32_t r1)
+{
+    return cvt_rs_fp4x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7], r0, r1);
+}
 
 
 // ---------------------------------------------------------------------------

@@ -20,10 +20,11 @@ that split rows on 16-row boundaries transform exactly like the slices of
 the whole tensor.
 
 Stochastic rounding draws depend only on an element's position in the
-whole tensor: element (m, k) takes its 16 random bits from Philox block
-offset + (m*K + k)/8 (rowwise) or offset + (m/8)*K + k (columnwise), so a
-rank whose shard starts at global row r0 passes offset + r0*K/8 and draws
-exactly what the unsharded call draws for those rows.  The ``quantize_shard_*``
+whole tensor: element (m, k) takes its random bits from Philox block
+offset + (m*K + k)/16 (rowwise) or offset + (m/16)*K + k (columnwise), so a
+rank whose shard starts at global row r0 (a multiple of 16) passes
+offset + r0*K/16 and draws exactly what the unsharded call draws for those
+rows.  The ``quantize_shard_*``
 helpers do this by default (``row_base=None`` gathers the shard heights and
 takes the rank's first global row).
 
@@ -71,11 +72,11 @@ def shard_row_base(rows_local: int, group=None, device=None) -> int:
 
 def sr_offset(offset: int, row_base: int, K: int) -> int:
     """The Philox counter offset for a row shard that starts at global row
-    ``row_base`` (a multiple of 8): the unsharded call's ``offset`` moved by
-    the row_base * K elements ahead of the shard (8 draws per counter)."""
-    if row_base % 8 != 0 or K % 8 != 0:
-        raise ValueError("row_base and K must be multiples of 8")
-    return int(offset) + int(row_base) * int(K) // 8
+    ``row_base`` (a multiple of 16): the unsharded call's ``offset`` moved by
+    the row_base * K elements ahead of the shard (16 draws per counter)."""
+    if row_base % 16 != 0 or K % 16 != 0:
+        raise ValueError("row_base and K must be multiples of 16")
+    return int(offset) + int(row_base) * int(K) // 16
 
 
 def _shard_offset(x_local, offset, row_base, group):

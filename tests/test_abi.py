@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
     for n in declared_functions():
         assert hasattr(L, n), n
         assert n in Q.SIGNATURES, n
-    assert L.q_abi_version() == 3
+    assert L.q_abi_version() == 4
 
 
 A = ctypes.c_void_p(0x10000)        # an aligned non-NULL address that is never dereferenced

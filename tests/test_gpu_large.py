@@ -86,9 +86,9 @@ def test_nvfp4_past_2_31_elements(big):
     same(host(got.sb_colT[:, (M - BAND) // 16:]), want.sb_colT, "sb_colT band")
     del got
     # stochastic rounding: the band draws what the whole tensor draws there with counter offset
-    # offset + (M - BAND) * K / 8, in both copies
+    # offset + (M - BAND) * K / 16, in both copies
     got = Q.q_nvfp4(x, "1x16", "sr", seed=77, offset=5, rowwise=True, colwise=True)
-    want = O.nvfp4(band, O.B1x16, O.SR, seed=77, offset=5 + (M - BAND) * K // 8, rowwise=True, colwise=True,
+    want = O.nvfp4(band, O.B1x16, O.SR, seed=77, offset=5 + (M - BAND) * K // 16, rowwise=True, colwise=True,
                    amax_in=float(A))
     same(host(got.q_row[M - BAND:]), want.q_row, "SR q_row band")
     same(host(got.q_colT[:, (M - BAND) // 2:]), want.q_colT, "SR q_colT band")
@@ -96,7 +96,7 @@ def test_nvfp4_past_2_31_elements(big):
     del got
     for rnd, orn in (("rn", O.RN), ("sr", O.SR)):
         got = Q.q_nvfp4(x, "16x16", rnd, seed=9, offset=3, rowwise=True, colwise=True)
-        want = O.nvfp4(band, O.B16x16, orn, seed=9, offset=3 + (M - BAND) * K // 8, rowwise=True, colwise=True,
+        want = O.nvfp4(band, O.B16x16, orn, seed=9, offset=3 + (M - BAND) * K // 16, rowwise=True, colwise=True,
                        amax_in=float(A))
         same(host(got.q_row[M - BAND:]), want.q_row, f"16x16 {rnd} q_row band")
         same(host(got.sb_row[(M - BAND) // 16:]), want.sb_row, f"16x16 {rnd} sb_row band")
@@ -110,7 +110,7 @@ def test_nvfp4_rht_and_recipe_past_2_31_elements(big):
     for rnd, orn in (("rn", O.RN), ("sr", O.SR)):
         got = Q.q_nvfp4_rht_colT(x, MASK, rnd, seed=21, offset=8)
         assert got.amax.item() == A_RHT
-        q, sb, _, sg = O.nvfp4_rht_colT(band, MASK, orn, seed=21, offset=8 + (M - BAND) * K // 8,
+        q, sb, _, sg = O.nvfp4_rht_colT(band, MASK, orn, seed=21, offset=8 + (M - BAND) * K // 16,
                                         amax_in=float(A_RHT))
         same(np.float32(got.s_global.item()), np.float32(sg), f"rht {rnd} s_global")
         same(host(got.q_colT[:, (M - BAND) // 2:]), q, f"rht {rnd} q_colT band")
@@ -118,9 +118,9 @@ def test_nvfp4_rht_and_recipe_past_2_31_elements(big):
         del got
     row, col = Q.q_nvfp4_recipe(x, MASK, "sr", seed=21, offset=8)
     assert row.amax.item() == A and col.amax.item() == A_RHT
-    w = O.nvfp4(band, O.B1x16, O.SR, seed=21, offset=8 + (M - BAND) * K // 8, rowwise=True, colwise=False,
+    w = O.nvfp4(band, O.B1x16, O.SR, seed=21, offset=8 + (M - BAND) * K // 16, rowwise=True, colwise=False,
                 amax_in=float(A))
-    q, sb, _, _ = O.nvfp4_rht_colT(band, MASK, O.SR, seed=21, offset=8 + (M - BAND) * K // 8, amax_in=float(A_RHT))
+    q, sb, _, _ = O.nvfp4_rht_colT(band, MASK, O.SR, seed=21, offset=8 + (M - BAND) * K // 16, amax_in=float(A_RHT))
     same(host(row.q_row[M - BAND:]), w.q_row, "recipe q_row band")
     same(host(row.sb_row[M - BAND:]), w.sb_row, "recipe sb_row band")
     same(host(col.q_colT[:, (M - BAND) // 2:]), q, "recipe q_colT band")

@@ -18,7 +18,7 @@ PROGRAM = r"""
 
 int main(void)
 {
-    if (q_abi_version() != 3) return 1;
+    if (q_abi_version() != 4) return 1;
     /* K = 24 is not a multiple of 16: rejected on the host, nothing launched */
     q_status s = q_nvfp4((const void *)0x10000, Q_BF16, 16, 24, Q_B1x16, Q_RN, 0, 0,
                          (uint8_t *)0x10000, (uint8_t *)0x10000, NULL, NULL, (float *)0x10000,

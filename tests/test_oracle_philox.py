@@ -64,15 +64,45 @@ def test_weyl_constants_closed_form():
     assert [int(v) for v in full] == [int(v) for v in gen]
 
 
+def _rev16(v):
+    return int(format(v, "016b")[::-1], 2)
+
+
 def test_bits16_layout():
-    """Element i takes half (i % 2) of word (i % 8) / 2 of block offset + i // 8."""
+    """Element i takes a 16-bit draw from word (i % 16) // 4 of Philox block
+    offset + i // 16: the word's bytes 0 and 2 form U0 (byte 2 high), bytes 1
+    and 3 form U1 (byte 3 high), and elements 4t .. 4t + 3 take U0, U0
+    bit-reversed, U1, U1 bit-reversed."""
     seed, off = 0x1234_5678_9ABC_DEF0, 77
     for stream in (0, 1):
         for g in range(3):
             w = O.philox4x32_10([(off + g) & 0xFFFFFFFF, (off + g) >> 32, stream, 0],
                                 [seed & 0xFFFFFFFF, seed >> 32])
-            halves = [int(w[j // 2]) >> (16 * (j % 2)) & 0xFFFF for j in range(8)]
-            assert [O.philox_bits16(seed, off, stream, 8 * g + j) for j in range(8)] == halves
+            want = []
+            for t in range(4):
+                b = int(w[t]).to_bytes(4, "little")
+                u0, u1 = b[0] + 256 * b[2], b[1] + 256 * b[3]
+                want += [u0, _rev16(u0), u1, _rev16(u1)]
+            assert [O.philox_bits16(seed, off, stream, 16 * g + j) for j in range(16)] == want
+
+
+def test_sr_round_up_count_is_the_truncated_fraction():
+    """Over all 2^16 draws R the E2M1 stochastic rounding of y rounds up for
+    exactly floor(frac * 2^16) of them, frac the position of |y| between its
+    grid neighbours (from the E2M1 values), so P(up) = floor(frac * 2^16) / 2^16;
+    the draws that round up are the largest ones."""
+    from fractions import Fraction
+    grid = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3), Fraction(4), Fraction(6)]
+    for y in (0.1, 0.3, 0.25, 0.75, 1.2, 1.9999, 2.5, 3.75, 4.1, 5.99, -0.3, -2.5, 1e-30, 0.5 + 2.0 ** -20):
+        y = float(np.float32(y))
+        a = abs(Fraction(y))
+        lo = max(gv for gv in grid if gv <= a)
+        hi = min(gv for gv in grid if gv > a)
+        T = int((a - lo) / (hi - lo) * 65536)          # floor of a non-negative Fraction
+        up_code = O.cast_e2m1(np.array([float(hi) * (1 if y > 0 else -1)], np.float32))[0]
+        ups = [r for r in range(65536) if O.sr_e2m1(y, r) == up_code]
+        assert len(ups) == T, (y, len(ups), T)
+        assert ups == list(range(65536 - T, 65536)), y
 
 
 def test_bits16_uniform():

@@ -429,33 +429,36 @@ def test_nv_sr_rounds_to_neighbours_and_matches_rn_on_grid():
 
 def test_nv_sr_uses_row_and_column_indices():
     """Rowwise element (m, k) draws index m*K + k on stream 0; the columnwise
-    copy of element (m, k) draws index ((m // 8)*K + k)*8 + m % 8 on stream 1
-    (8-row groups of x, then columns, then rows), which does not depend on M."""
-    x = W.gen("t3", (16, 32), 13, bf16=False)
+    copy of element (m, k) draws index ((m // 16)*K + k)*16 + m % 16 on stream 1
+    (16-row groups of x, then columns, then rows), which does not depend on M."""
+    x = W.gen("t3", (32, 32), 13, bf16=False)
     r = O.nvfp4(x, O.B1x16, O.SR, seed=99, offset=5, rowwise=True, colwise=True)
     alpha_g, _ = O.nvfp4_global(r.amax)
     sbv = dec8(r.sb_row)
     enc = (alpha_g / sbv).astype(np.float32)
     y = (x * np.repeat(enc, 16, axis=1)).astype(np.float32)
-    want = O.sr_e2m1_batch(y.ravel(), seed=99, offset=5, stream=0).reshape(16, 32)
+    want = O.sr_e2m1_batch(y.ravel(), seed=99, offset=5, stream=0).reshape(32, 32)
     assert np.array_equal(O.unpack_e2m1(r.q_row, 32), want)
     sbc = dec8(r.sb_colT)
     encc = (alpha_g / sbc).astype(np.float32)
     yt = (np.ascontiguousarray(x.T) * np.repeat(encc, 16, axis=1)).astype(np.float32)
     M, K = x.shape
-    wantc = np.array([[O.sr_e2m1(yt[k, m], O.philox_bits16(99, 5, 1, ((m // 8) * K + k) * 8 + m % 8))
+    wantc = np.array([[O.sr_e2m1(yt[k, m], O.philox_bits16(99, 5, 1, ((m // 16) * K + k) * 16 + m % 16))
                        for m in range(M)] for k in range(K)], np.uint8)
-    assert np.array_equal(O.unpack_e2m1(r.q_colT, 16), wantc)
-    # the old transposed-layout numbering k*M + m gives different codes here
-    # (so the test tells the two numberings apart)
-    old = O.sr_e2m1_batch(yt.ravel(), seed=99, offset=5, stream=1).reshape(32, 16)
+    assert np.array_equal(O.unpack_e2m1(r.q_colT, M), wantc)
+    # the transposed-layout numbering k*M + m, and 8-row groups, give other
+    # codes here (so the test tells the numberings apart)
+    old = O.sr_e2m1_batch(yt.ravel(), seed=99, offset=5, stream=1).reshape(32, 32)
     assert not np.array_equal(old, wantc)
+    old8 = np.array([[O.sr_e2m1(yt[k, m], O.philox_bits16(99, 5, 1, ((m // 8) * K + k) * 8 + m % 8))
+                      for m in range(M)] for k in range(K)], np.uint8)
+    assert not np.array_equal(old8, wantc)
 
 
 @pytest.mark.parametrize("blk", [O.B1x16, O.B16x16])
 def test_nv_sr_row_shards_draw_what_the_whole_tensor_draws(blk):
     """A band of rows [r0, r0 + h) quantized alone with counter offset
-    offset + r0*K/8 and the whole tensor's amax gives exactly that band of the
+    offset + r0*K/16 and the whole tensor's amax gives exactly that band of the
     unsharded stochastic quantization, rowwise and columnwise ("Mixed-precision
     training: fp16 to fp8", FP8 communication, TP: the FP8 tensor must not
     depend on the split)."""
@@ -464,7 +467,7 @@ def test_nv_sr_row_shards_draw_what_the_whole_tensor_draws(blk):
     A = O.amax(x)
     whole = O.nvfp4(x, blk, O.SR, seed=31, offset=1000, rowwise=True, colwise=True)
     for r0, h in ((0, 32), (32, 16), (48, 48)):
-        band = O.nvfp4(np.ascontiguousarray(x[r0:r0 + h]), blk, O.SR, seed=31, offset=1000 + r0 * K // 8,
+        band = O.nvfp4(np.ascontiguousarray(x[r0:r0 + h]), blk, O.SR, seed=31, offset=1000 + r0 * K // 16,
                        rowwise=True, colwise=True, amax_in=A)
         assert np.array_equal(band.q_row, whole.q_row[r0:r0 + h])
         assert np.array_equal(band.q_colT, whole.q_colT[:, r0 // 2:(r0 + h) // 2])

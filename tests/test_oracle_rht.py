@@ -124,7 +124,7 @@ def test_rht_lowers_block_amax_on_outlier_blocks():
 
 def test_rht_colT_sr_row_shards_draw_what_the_whole_tensor_draws():
     """Row bands on 16-row boundaries, each with the transformed tensor's
-    global amax and counter offset offset + r0*K/8, give exactly the columns
+    global amax and counter offset offset + r0*K/16, give exactly the columns
     [r0/2, (r0 + h)/2) of the unsharded stochastic copy: the transform acts
     within 16-row groups and the draws depend on the position in x only."""
     x = W.gen("t3", (80, 48), 15, bf16=True)
@@ -133,6 +133,6 @@ def test_rht_colT_sr_row_shards_draw_what_the_whole_tensor_draws():
     q, sb, A, _ = O.nvfp4_rht_colT(x, mask, O.SR, seed=17, offset=3)
     for r0, h in ((0, 16), (16, 48), (64, 16)):
         qb, sbb, _, _ = O.nvfp4_rht_colT(np.ascontiguousarray(x[r0:r0 + h]), mask, O.SR, seed=17,
-                                         offset=3 + r0 * K // 8, amax_in=A)
+                                         offset=3 + r0 * K // 16, amax_in=A)
         assert np.array_equal(qb, q[:, r0 // 2:(r0 + h) // 2])
         assert np.array_equal(sbb, sb[:, r0 // 16:(r0 + h) // 16])
