@@ -599,6 +599,7 @@ NV_CASES = [
     ("weight", (144, 272), True, O.B16x16, O.RN, 0, 0),
     ("weight", (144, 272), True, O.B16x16, O.SR, 77, 5),
     ("weight", (64, 96), False, O.B16x16, O.RN, 0, 0),
+    ("t3", (96, 160), False, O.B16x16, O.SR, 21, 7),        # FP32 16x16 SR: four-element words
 ]
 
 
