@@ -126,6 +126,19 @@ def test_allreduce_amax_single_process_is_identity():
         allreduce_amax_(torch.tensor([1.0, 2.0]))
 
 
+def test_sr_offset_counts_sixteen_draws_per_philox_block():
+    """A shard at global row r0 moves the counter offset by the r0*K draws
+    ahead of it, 16 per Philox block; rows that split a 16-row block (or a K
+    that splits a 1x16 block) have no such offset."""
+    from nvfp4_quantization_current_gb300.distributed import sr_offset
+    assert sr_offset(5, 0, 64) == 5
+    assert sr_offset(5, 32, 64) == 5 + 32 * 64 // 16
+    assert sr_offset(0, 8192, 4096) == 8192 * 4096 // 16
+    for r0, K in ((8, 64), (24, 64), (16, 40)):
+        with pytest.raises(ValueError):
+            sr_offset(0, r0, K)
+
+
 def _gather_worker(rank, world, port, result_dir):
     """Each rank quantizes its row shard (uneven: 128 and 256 rows, on 128-row
     boundaries) with the CPU oracle, wraps the outputs in the library's
