@@ -15,13 +15,14 @@
 // On the tile engine (the amax comes from the preceding amax pass or the
 // caller; tiles are walked backwards for L2 reuse), thread (warp w, lane l)
 // holds rows 8w..8w+7 x one 16-byte column chunk in registers.
-//  1x16 rowwise - a block spans 16/VEC lanes; stochastic rounding draws one
-//                 Philox block (8 elements) per thread and row;
+//  1x16 rowwise - a block spans 16/VEC lanes; stochastic rounding takes the
+//                 words of the block's Philox block (16 elements) that cover
+//                 the thread's chunk;
 //  16x1 colwise - a block is the 8 rows of warps 2p and 2p+1: their column
 //                 maxima meet in shared memory; each column's 8 values are
-//                 encoded into one word of row nibbles (SR: one Philox block
-//                 per column), parked in the consumed stage and written as
-//                 q_colT rows;
+//                 encoded into one word of row nibbles (SR: half of the
+//                 column block's Philox block), parked in the consumed stage
+//                 and written as q_colT rows;
 //  16x16        - the block maximum spans 2 warps x 16/VEC lanes; the
 //                 transposed copy is the row codes nibble-transposed.
 #include <cstring>
